@@ -1,0 +1,161 @@
+"""Pins of the oracle's MXFP8 quantizer (E4M3 elements, E8M0 block scales).
+
+The rule pinned here: scale exponent e = the smallest integer with
+amax <= 448 * 2^e (= ceil(log2(amax/448))), clamped to [-127, 127], stored as
+the byte e + 127; elements encoded as round-to-nearest-even E4M3 (OCP "FN":
+max 448, no infinity) of v * 2^-e with saturation. It is the MXFP8 output of
+the fused up-projection (TransformerEngine PR "Add support for fused Q
+Up-Proj GEMM/RoPE/Quant", description paragraph) and the standalone
+quantization helper of the same PR (Greptile summary: "two-phase MXFP8
+quantization" helpers).
+
+Pins are independent of the oracle's own code: torch's float8_e4m3fn
+conversion (a library routine), an exhaustive nearest-value search over the
+256 codes, hand-derived closed forms and the rounding error bound.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _all_code_values_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_decode_all_codes_match_torch():
+    ref = _all_code_values_torch()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    nan_ref, nan_got = np.isnan(ref), np.isnan(got)
+    assert (nan_ref == nan_got).all()
+    assert nan_got.sum() == 2  # 0x7F and 0xFF only (no infinity in E4M3 "FN")
+    assert np.array_equal(ref[~nan_ref], got[~nan_got])
+    # sign of zero
+    assert math.copysign(1.0, got[0x80]) == -1.0
+
+
+@pytest.mark.parametrize("code,value", [
+    (0x00, 0.0), (0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9), (0x08, 2.0 ** -6),
+    (0x38, 1.0), (0x3C, 1.5), (0x70, 2.0 ** 7), (0x78, 2.0 ** 8), (0x7E, 448.0),
+    (0xB8, -1.0), (0xFE, -448.0),
+])
+def test_decode_closed_form(code, value):
+    # sign bit, exponent field (bias 7), 3 mantissa bits; field 0 = subnormal m * 2^-9
+    assert oracle.e4m3_decode(code) == value
+
+
+def test_encode_every_bf16_matches_torch_rne():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.decode_bf16(bits)
+    finite = np.isfinite(vals) & (np.abs(vals) < 464.0)  # torch maps >= 464 to NaN
+    v = vals[finite]
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(x) for x in v], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_encode_bruteforce_nearest_ties_even():
+    """Nearest of the finite codes by exhaustive search, ties to the even code."""
+    rng = np.random.default_rng(1234)
+    table = _all_code_values_torch()
+    pos_codes = np.array([c for c in range(0x7F)])  # 0x00..0x7E: non-negative finite
+    pos_vals = table[pos_codes]
+    # random magnitudes over the whole range, plus every exact midpoint between codes
+    mids = (pos_vals[:-1] + pos_vals[1:]) / 2.0
+    rnd = np.concatenate([rng.uniform(0, 448, 20000), np.exp2(rng.uniform(-12, 8.8, 20000)), mids])
+    rnd = rnd[rnd <= 448.0]
+    for a in rnd:
+        d = np.abs(pos_vals - a)
+        best = np.flatnonzero(d == d.min())
+        if best.size == 2:  # a tie: pick the even code
+            best = best[(pos_codes[best] & 1) == 0]
+        exp_code = int(pos_codes[best[0]])
+        assert oracle.e4m3_encode(a) == exp_code, a
+        assert oracle.e4m3_encode(-a) == (exp_code | 0x80), -a
+
+
+def test_encode_saturates_and_nan():
+    for v in [448.0, 449.0, 463.9, 464.0, 500.0, 1e30, float("inf")]:
+        assert oracle.e4m3_encode(v) == 0x7E
+        assert oracle.e4m3_encode(-v) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) & 0x7F == 0x7F
+    assert oracle.e4m3_encode(-0.0) == 0x80
+    assert oracle.e4m3_encode(2.0 ** -11) == 0x00  # below half the smallest subnormal
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00  # exact tie with 0 -> even (0)
+    assert oracle.e4m3_encode(3 * 2.0 ** -10) == 0x02  # tie 1.5 steps -> 2 (even)
+
+
+@pytest.mark.parametrize("e", [-127, -126, -20, -8, -1, 0, 1, 7, 60, 119])
+def test_scale_exponent_edges(e):
+    edge = math.ldexp(448.0, e)
+    assert oracle.e8m0_exponent(edge) == e  # exactly 448*2^e -> e, not e+1
+    if e < 127:
+        assert oracle.e8m0_exponent(np.nextafter(edge, np.inf)) == e + 1
+    if e > -127:
+        assert oracle.e8m0_exponent(np.nextafter(edge, 0.0)) == e
+        assert oracle.e8m0_exponent(math.ldexp(448.0, e - 1)) == e - 1
+
+
+def test_scale_exponent_matches_ceil_log2():
+    rng = np.random.default_rng(7)
+    for a in np.exp2(rng.uniform(-100, 100, 5000)):
+        # away from exact powers of two the float log is safe to compare against
+        e_ref = math.ceil(math.log2(a / 448.0))
+        if abs(math.log2(a / 448.0) - round(math.log2(a / 448.0))) > 1e-9:
+            assert oracle.e8m0_exponent(a) == max(-127, min(127, e_ref))
+
+
+def test_scale_exponent_zero_and_tiny():
+    assert oracle.e8m0_exponent(0.0) == -127
+    assert oracle.e8m0_exponent(1e-45) == -127
+    assert oracle.e8m0_exponent(math.ldexp(448.0, -130)) == -127
+
+
+def test_block_hand_example():
+    # amax 2 -> e = -7 (448/128 = 3.5 >= 2 > 448/256); byte 120
+    # 1.0 * 2^7 = 128 = 2^7 -> 0x70; -2 * 2^7 = -256 -> 0xF8; 0.5 * 2^7 = 64 -> 0x68;
+    # 0.1 * 128 = 12.8 -> step 1 in [8,16) -> 13 = 1.625 * 8 -> exp field 10, m 5 -> 0x55
+    blk = np.zeros((1, 32))
+    blk[0, :4] = [1.0, -2.0, 0.5, 0.1]
+    codes, scales = oracle.mxfp8_quantize(blk)
+    assert scales[0, 0] == 120
+    assert list(codes[0, :4]) == [0x70, 0xF8, 0x68, 0x55]
+    assert (codes[0, 4:] == 0).all()
+
+
+def test_block_rules_partial_zero_nonfinite_signed_zero():
+    v = np.zeros((3, 48))
+    v[0, :] = np.linspace(-3, 3, 48)           # two blocks: 32 + partial 16
+    v[1, :] = -0.0                             # all-zero block, signed zeros kept
+    v[2, :] = 1.0
+    v[2, 5] = np.nan
+    v[2, 40] = -np.inf
+    codes, scales = oracle.mxfp8_quantize(v)
+    assert scales.shape == (3, 2)
+    # partial block: amax over its 16 valid values only
+    assert scales[0, 1] == oracle.e8m0_exponent(np.abs(v[0, 32:]).max()) + 127
+    assert (scales[1] == 0).all() and (codes[1] == 0x80).all()
+    assert scales[2, 0] == 0xFF and scales[2, 1] == 0xFF
+    assert (codes[2, :32] == 0x7F).all()
+    assert codes[2, 40] == 0xFF and (np.delete(codes[2, 32:], 8) == 0x7F).all()
+
+
+def test_roundtrip_error_bound_and_saturation_free():
+    """|deq - v| <= half an E4M3 step at v * 2^-e on that grid; never saturates."""
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((64, 96)) * np.exp2(rng.integers(-30, 30, (64, 1)))
+    codes, scales = oracle.mxfp8_quantize(v)
+    deq = oracle.mxfp8_dequantize(codes, scales)
+    e = scales.astype(np.int64).repeat(32, axis=1)[:, :96] - 127
+    u = np.abs(v) * np.exp2(-e.astype(np.float64))
+    assert (u <= 448.0).all()
+    step = np.where(u < 2.0 ** -6, 2.0 ** -9, np.exp2(np.floor(np.log2(np.maximum(u, 1e-300))) - 3))
+    err = np.abs(deq - v) * np.exp2(-e.astype(np.float64))
+    assert (err <= step / 2 + 1e-300).all()
+    # each block's largest magnitude rounds into [224, 448]
+    amax_codes = (codes & 0x7F).reshape(64, 3, 32).max(axis=2)
+    assert (amax_codes >= 0x76).all()  # amax * 2^-e lies in (224, 448]
