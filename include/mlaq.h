@@ -1,0 +1,200 @@
+/*
+ * mlaq.h: C ABI of libmlaq.so, the GB300 (sm_103a) fused MLA query
+ * up-projection.
+ *
+ * The operation (TransformerEngine PR "Add support for fused Q Up-Proj
+ * GEMM/RoPE/Quant", description paragraph): the Q up-projection GEMM of
+ * DeepSeek-V3-style Multi-Latent Attention, fused with the RoPE that follows
+ * it and with MXFP8 quantization of the result, with either a 16-bit or an
+ * MXFP8 projection weight. Its backward (TransformerEngine PR "Add a
+ * backwards linear function to be used with the fused mla q up-proj",
+ * sequence diagram): the query gradient goes through the RoPE backward, then
+ * the linear backward yields the input, weight and bias gradients.
+ *
+ * Notation: T tokens, K = q_lora_rank, H heads, each of D = Dn + Dr channels
+ * (Dn pass-through, Dr rotated), N = H * D.
+ *   forward   y[t, n] = sum_k x[t, k] W[n, k] + b[n]
+ *             q[t, h, c] = y[t, hD + c]                           for c < Dn
+ *             q[t, h, Dn+i]      = a cos[p, i]      - c sin[p, i]
+ *             q[t, h, Dn+i+Dr/2] = c cos[p, i+Dr/2] + a sin[p, i+Dr/2]
+ *             with a = y[t, hD+Dn+i], c = y[t, hD+Dn+i+Dr/2], i < Dr/2,
+ *             p = pos[t] (or t), optionally MXFP8-quantized per 32 channels
+ *             of each head (E4M3 codes + one E8M0 scale per block).
+ *   backward  dq_pre = J^T dq (J the Jacobian of the rotation above)
+ *             dx = dq_pre W,  dW = dq_pre^T x,  db = sum_t dq_pre.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     allocates nothing and keeps no state between calls.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronizing.
+ *   - The return value is a synchronous mla_status. Nothing is launched when
+ *     it is not MLA_OK. Conditions only the GPU can see (a position outside
+ *     the cos/sin table, a pipeline wait that timed out) are written to
+ *     *dev_status (a device int the caller zeroes before the call; NULL = not
+ *     reported); the first one recorded wins.
+ *   - Inputs are never written. Outputs must not overlap any input
+ *     (MLA_ERR_ALIAS); the Megatron-LM PR "Fix fused MLA YaRN RoPE query
+ *     kernel corrupting upstream tensor in-place" is about exactly this
+ *     in-place hazard.
+ *   - bf16 means IEEE-754 binary16 with 8 exponent bits (bfloat16), stored as
+ *     uint16 bit patterns; all row-major, innermost dimension contiguous.
+ */
+#ifndef MLAQ_H
+#define MLAQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MLAQ_API __attribute__((visibility("default")))
+#else
+#define MLAQ_API
+#endif
+
+/* Status codes. */
+enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1, /* null required pointer, bad mode, non-positive dims, odd Dr, ... */
+    MLA_ERR_ROPE_WIDTH = 2,  /* cos/sin table narrower than Dr: rejected, never read past a row */
+    MLA_ERR_ALIGNMENT = 3,   /* pointer or row pitch not aligned as the kernel's loads need */
+    MLA_ERR_ALIAS = 4,       /* an output byte range overlaps an input byte range */
+    MLA_ERR_UNSUPPORTED = 5, /* a valid problem the kernels do not tile (see each call) */
+    MLA_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed (no device, launch error) */
+    MLA_ERR_TIMEOUT = 7,     /* device only: a pipeline wait gave up; outputs are unspecified */
+    MLA_ERR_POS_RANGE = 8,   /* a position outside [0, cs_rows); device-side for pos arrays */
+    MLA_ERR_WORKSPACE = 9    /* workspace pointer/size smaller than the size query returned */
+};
+
+/* weight_mode */
+enum { MLA_WEIGHT_BF16 = 0, MLA_WEIGHT_MXFP8 = 1 };
+/* out_mode */
+enum { MLA_OUT_BF16 = 0, MLA_OUT_MXFP8 = 1 };
+/* in_dtype of mxfp8_quantize_rows */
+enum { MLA_IN_F32 = 0, MLA_IN_BF16 = 1 };
+
+/* Problem shape.
+ *   T        tokens (rows of x and q), >= 0
+ *   K        q_lora_rank (columns of x and W), > 0
+ *   H        heads, > 0
+ *   Dn       pass-through channels per head, >= 0
+ *   Dr       rotated channels per head, even, > 0
+ *   cs_rows  rows of the cos and sin tables (positions)
+ *   cs_width columns of the tables = their row pitch in floats; must be >= Dr
+ *            (the width guard of the Megatron-LM PR above: a narrow table
+ *            gives MLA_ERR_ROPE_WIDTH, never an out-of-bounds read). Rope
+ *            channel j of a head reads column j. */
+typedef struct {
+    int64_t T;
+    int64_t K;
+    int32_t H;
+    int32_t Dn;
+    int32_t Dr;
+    int32_t reserved; /* set to 0 */
+    int64_t cs_rows;
+    int64_t cs_width;
+} mla_q_shape;
+
+/*
+ * Forward: q = RoPE(x W^T + b), optionally MXFP8-quantized.
+ * TransformerEngine PR "Add support for fused Q Up-Proj GEMM/RoPE/Quant",
+ * description paragraph and flowchart (input activation, BF16 or MXFP8
+ * weight and RoPE cos/sin into the fused up-projection, MXFP8 query out).
+ *
+ *   weight_mode MLA_WEIGHT_BF16:  x [T, K] bf16, W [N, K] bf16; x_scales and
+ *               w_scales must be NULL.
+ *   weight_mode MLA_WEIGHT_MXFP8: x [T, K] E4M3 codes (uint8) with x_scales
+ *               [T, K/32] E8M0 bytes, W [N, K] E4M3 codes with w_scales
+ *               [N, K/32]: value = e4m3(code) * 2^(scale - 127), blocks of 32
+ *               along K (the layout mxfp8_quantize_rows writes).
+ *               Requires K % 128 == 0.
+ *   bias        [N] bf16 or NULL (added before the rotation).
+ *   cos_tab, sin_tab [cs_rows, cs_width] fp32.
+ *   pos         [T] int32 positions, or NULL for pos[t] = t (then
+ *               T <= cs_rows is checked here, else MLA_ERR_POS_RANGE).
+ *   out_mode MLA_OUT_BF16:  q_out [T, H, D] bf16 (round to nearest even);
+ *               q_scales_out must be NULL.
+ *   out_mode MLA_OUT_MXFP8: q_out [T, H, D] E4M3 codes (uint8) and
+ *               q_scales_out [T, H, ceil(D/32)] E8M0 bytes; blocks of 32
+ *               consecutive channels of one head (the last may be partial);
+ *               scale exponent = the smallest e with amax <= 448 * 2^e,
+ *               clamped to [-127, 127]; codes = RNE E4M3 of v * 2^-e with
+ *               saturation; a block holding NaN/Inf gets scale 0xFF and NaN
+ *               codes.
+ * Tiling limits (else MLA_ERR_UNSUPPORTED): Dr in {16, 32, 64}, Dn % 32 == 0;
+ * bf16 weights need K % 8 == 0 (16-byte rows). Pointers must be 16-byte
+ * aligned (scales and bias: 4-byte), else MLA_ERR_ALIGNMENT.
+ */
+MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_mode,
+                             const void *x, const uint8_t *x_scales, const void *W,
+                             const uint8_t *w_scales, const void *bias, const float *cos_tab,
+                             const float *sin_tab, const int32_t *pos, void *q_out,
+                             uint8_t *q_scales_out, int *dev_status, void *stream);
+
+/*
+ * Backward, input gradient: dx = (J^T dq) W.
+ * TransformerEngine PR "Add a backwards linear function to be used with the
+ * fused mla q up-proj", summary and sequence diagram (RoPE backward, then the
+ * linear backward with the weight). The inverse rotation is applied to dq
+ * tiles on their way into the tensor cores; dq_pre is never stored.
+ *   dq [T, H, D] bf16, W [N, K] bf16 (the bf16 master weight), dx [T, K] bf16
+ *   (fp32 accumulation). cos_tab/sin_tab/pos as in the forward.
+ *   workspace/ws_bytes: see mla_q_uproj_workspace_size (may be NULL/0 when the
+ *   size query returns 0).
+ * Requires K % 8 == 0, Dr in {16, 32, 64}, Dn % Dr == 0, and 16-byte aligned
+ * pointers.
+ */
+MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape *shape, const void *dq, const void *W,
+                                   const float *cos_tab, const float *sin_tab, const int32_t *pos,
+                                   void *dx, void *workspace, size_t ws_bytes, int *dev_status,
+                                   void *stream);
+
+/*
+ * Backward, weight and bias gradients: dW = (J^T dq)^T x, db = sum_t J^T dq.
+ * Same pull request (input and weight gradients from the saved input), its
+ * review comment "BF16 bias gradient remains missing" (db belongs here), and
+ * the Megatron-LM PR above (wgrad dw = dy^T x uses the linear's saved INPUT;
+ * it may run later, as a separate call, for delayed weight-gradient
+ * schedules).
+ *   dq [T, H, D] bf16, x [T, K] bf16, dW [N, K] bf16, db [N] bf16 or NULL
+ *   (skipped). fp32 accumulation over all T.
+ * Requirements as for mla_q_uproj_bwd_dgrad.
+ */
+MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape *shape, const void *dq, const void *x,
+                                   const float *cos_tab, const float *sin_tab, const int32_t *pos,
+                                   void *dW, void *db, void *workspace, size_t ws_bytes,
+                                   int *dev_status, void *stream);
+
+/*
+ * Standalone rowwise MXFP8 quantization of in[R, C] (row pitch ld_in
+ * elements, ld_in >= C): codes [R, C] uint8 (dense, pitch C) and scales
+ * [R, ceil(C/32)] uint8 (dense). Same rule as the forward's MXFP8 output,
+ * blocks of 32 consecutive elements of a row (the last may be partial).
+ * TransformerEngine PR "Add support for fused Q Up-Proj GEMM/RoPE/Quant",
+ * Greptile summary ("two-phase MXFP8 quantization" helpers) and review
+ * thread (mxfp8_quantize_only). Bit-exact: codes and scales depend only on
+ * the input values. in_dtype is MLA_IN_F32 or MLA_IN_BF16. R = 0 or C = 0 is
+ * a no-op. Pointers must be 4-byte aligned (16-byte for the fast path).
+ */
+MLAQ_API int mxfp8_quantize_rows(int64_t R, int64_t C, int in_dtype, const void *in,
+                                 int64_t ld_in, uint8_t *codes, uint8_t *scales, void *stream);
+
+/* which: 0 = forward, 1 = dgrad, 2 = wgrad. Bytes of device workspace the
+ * call needs for this shape (0 = pass NULL). Returns 0 for an invalid shape. */
+MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape *shape, int which);
+
+/* Static, human-readable name of a status code. */
+MLAQ_API const char *mla_status_string(int status);
+
+/* ABI version of this header (major * 10000 + minor * 100 + patch). */
+MLAQ_API int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLAQ_H */

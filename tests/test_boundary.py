@@ -1,0 +1,166 @@
+"""The C ABI of libmlaq.so, without a GPU: it loads, exports every symbol that
+include/mlaq.h declares, and rejects bad arguments on the host with the
+documented status before touching CUDA.
+
+Cases follow the contract of the pages: the cos/sin width guard (Megatron-LM
+PR "Fix fused MLA YaRN RoPE query kernel corrupting upstream tensor
+in-place", Problem section: an out-of-bounds table read when the table is
+narrower than the rotary dim) and no in-place output (same PR).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import up_proj_gemm_gb300 as mlaq
+from up_proj_gemm_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+S = mlaq.STATUS
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return mlaq.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "mlaq.h")).read()
+    return re.findall(r"MLAQ_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_symbols()
+    assert set(names) >= {"mla_q_uproj_fwd", "mla_q_uproj_bwd_dgrad", "mla_q_uproj_bwd_wgrad",
+                          "mxfp8_quantize_rows", "mla_q_uproj_workspace_size", "mla_status_string",
+                          "mla_version"}
+    for n in names:
+        assert hasattr(L, n), n
+    # nothing else is exported
+    out = os.popen(f"nm -D --defined-only {mlaq.library_path}").read().split("\n")
+    exported = {ln.split()[-1] for ln in out if ln.strip() and " T " in ln}
+    assert exported == set(names)
+
+
+def test_status_strings(L):
+    for name, code in S.items():
+        assert mlaq.status_string(code) == name
+    assert L.mla_version() >= 10000
+
+
+FAKE = 0x10000  # 64 KiB-aligned fake device addresses: never dereferenced
+
+
+def p(i):
+    return ctypes.c_void_p(FAKE * (i + 1))
+
+
+def shape(T=256, K=64, H=4, Dn=32, Dr=16, cs_rows=256, cs_width=16):
+    return mlaq.Shape(T=T, K=K, H=H, Dn=Dn, Dr=Dr, reserved=0, cs_rows=cs_rows, cs_width=cs_width)
+
+
+def fwd(L, s, wm=0, om=1, x=p(0), xs=None, W=p(1), ws=None, b=None, cos=p(2), sin=p(3), pos=None,
+        q=p(4), qs=p(5), st=None):
+    return L.mla_q_uproj_fwd(ctypes.byref(s) if s is not None else None, wm, om, x, xs, W, ws, b, cos,
+                             sin, pos, q, qs, st, None)
+
+
+def test_fwd_valid_args_reach_cuda(L):
+    # all host checks pass; without a GPU the first CUDA call fails cleanly
+    r = fwd(L, shape())
+    assert r in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(s=None), "MLA_ERR_INVALID_ARG"),
+    (dict(s=shape(Dr=15)), "MLA_ERR_INVALID_ARG"),          # odd rope dim
+    (dict(s=shape(K=0)), "MLA_ERR_INVALID_ARG"),
+    (dict(s=shape(H=0)), "MLA_ERR_INVALID_ARG"),
+    (dict(s=shape(T=-1)), "MLA_ERR_INVALID_ARG"),
+    (dict(x=None), "MLA_ERR_INVALID_ARG"),
+    (dict(W=None), "MLA_ERR_INVALID_ARG"),
+    (dict(q=None), "MLA_ERR_INVALID_ARG"),
+    (dict(qs=None), "MLA_ERR_INVALID_ARG"),                 # MXFP8 out needs scales
+    (dict(om=0), "MLA_ERR_INVALID_ARG"),                    # bf16 out must not get scales
+    (dict(wm=2), "MLA_ERR_INVALID_ARG"),
+    (dict(wm=1), "MLA_ERR_INVALID_ARG"),                    # MXFP8 weights need both scale arrays
+    (dict(cos=None), "MLA_ERR_INVALID_ARG"),
+    (dict(s=shape(cs_width=15)), "MLA_ERR_ROPE_WIDTH"),     # table narrower than Dr
+    (dict(s=shape(cs_width=0)), "MLA_ERR_ROPE_WIDTH"),
+    (dict(s=shape(T=300, cs_rows=256)), "MLA_ERR_POS_RANGE"),  # implicit pos = t beyond the table
+    (dict(s=shape(Dr=18, cs_width=18)), "MLA_ERR_UNSUPPORTED"),
+    (dict(s=shape(Dn=16)), "MLA_ERR_UNSUPPORTED"),
+    (dict(s=shape(K=60)), "MLA_ERR_ALIGNMENT"),             # bf16 rows not 16-byte multiples
+    (dict(x=ctypes.c_void_p(FAKE + 8)), "MLA_ERR_ALIGNMENT"),
+    (dict(q=p(0)), "MLA_ERR_ALIAS"),                        # in-place output
+    (dict(q=ctypes.c_void_p(FAKE + 256 * 64 * 2 - 16)), "MLA_ERR_ALIAS"),  # partial overlap with x
+    (dict(qs=p(4)), "MLA_ERR_ALIAS"),                       # outputs overlap each other
+    (dict(qs=p(3)), "MLA_ERR_ALIAS"),                       # scales written over the sin table
+])
+def test_fwd_rejects(L, kw, code):
+    assert fwd(L, kw.pop("s", shape()), **kw) == S[code]
+
+
+def test_fwd_mxfp8_weight_checks(L):
+    s = shape(K=64)
+    assert fwd(L, s, wm=1, xs=p(6), ws=p(7)) == S["MLA_ERR_UNSUPPORTED"]  # K % 128
+    s = shape(K=48)
+    assert fwd(L, s, wm=1, xs=p(6), ws=p(7)) == S["MLA_ERR_INVALID_ARG"]  # K % 32
+    s = shape(K=128)
+    r = fwd(L, s, wm=1, xs=ctypes.c_void_p(FAKE * 7 + 2), ws=p(7))
+    assert r == S["MLA_ERR_ALIGNMENT"]
+
+
+def test_fwd_empty_tokens_is_noop(L):
+    assert fwd(L, shape(T=0)) == S["MLA_OK"]
+
+
+def _bwd(L, which, s, dq=p(0), op=p(1), cos=p(2), sin=p(3), pos=None, out=p(4), db=None, ws=None,
+         wsb=0):
+    if which == "dgrad":
+        return L.mla_q_uproj_bwd_dgrad(ctypes.byref(s), dq, op, cos, sin, pos, out, ws, wsb, None, None)
+    return L.mla_q_uproj_bwd_wgrad(ctypes.byref(s), dq, op, cos, sin, pos, out, db, ws, wsb, None, None)
+
+
+@pytest.mark.parametrize("which", ["dgrad", "wgrad"])
+def test_bwd_rejects(L, which):
+    assert _bwd(L, which, shape(cs_width=8)) == S["MLA_ERR_ROPE_WIDTH"]
+    assert _bwd(L, which, shape(), dq=None) == S["MLA_ERR_INVALID_ARG"]
+    assert _bwd(L, which, shape(), out=p(0)) == S["MLA_ERR_ALIAS"]
+    assert _bwd(L, which, shape(), out=p(1)) == S["MLA_ERR_ALIAS"]
+    assert _bwd(L, which, shape(Dn=24)) == S["MLA_ERR_UNSUPPORTED"]   # Dn % Dr
+    assert _bwd(L, which, shape(K=36)) == S["MLA_ERR_ALIGNMENT"]
+    assert _bwd(L, which, shape(T=257)) == S["MLA_ERR_POS_RANGE"]
+    assert _bwd(L, which, shape()) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+
+
+def test_wgrad_bias_alias(L):
+    assert _bwd(L, "wgrad", shape(), db=p(0)) == S["MLA_ERR_ALIAS"]
+    assert _bwd(L, "wgrad", shape(), db=p(4)) == S["MLA_ERR_ALIAS"]
+
+
+def test_workspace_size(L):
+    s = shape()
+    for which in (0, 1, 2):
+        assert L.mla_q_uproj_workspace_size(ctypes.byref(s), which) == 0
+    assert L.mla_q_uproj_workspace_size(ctypes.byref(shape(Dr=3)), 0) == 0
+
+
+def test_quantize_rejects(L):
+    q = L.mxfp8_quantize_rows
+    assert q(4, 64, 0, p(0), 32, p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]   # ld < C
+    assert q(4, 64, 5, p(0), 64, p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]
+    assert q(4, 64, 0, None, 64, p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]
+    assert q(0, 64, 0, None, 64, None, None, None) == S["MLA_OK"]
+    assert q(4, 64, 0, ctypes.c_void_p(FAKE + 2), 64, p(1), p(2), None) == S["MLA_ERR_ALIGNMENT"]
+    assert q(4, 64, 0, p(0), 64, ctypes.c_void_p(FAKE + 100), p(2), None) == S["MLA_ERR_ALIAS"]
+    assert q(4, 64, 0, p(0), 64, p(1), p(1), None) == S["MLA_ERR_ALIAS"]
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(mlaq, "_lib", None)
+    monkeypatch.setattr(mlaq, "library_path", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no non-CUDA fallback"):
+        mlaq.lib()

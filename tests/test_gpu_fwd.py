@@ -1,0 +1,144 @@
+"""GPU parity of the fused forward (bf16 weights): GEMM + bias + RoPE, bf16 or
+MXFP8 output, against the fp64 oracle.
+
+TransformerEngine PR "Add support for fused Q Up-Proj GEMM/RoPE/Quant",
+description paragraph and flowchart; Megatron-LM PR "Fix fused MLA YaRN RoPE
+query kernel corrupting upstream tensor in-place", Problem section (the
+input must be unchanged afterwards).
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers
+import synth
+import up_proj_gemm_gb300 as mlaq
+
+pytestmark = pytest.mark.gpu
+
+# (name, overrides): several tiles, ragged token / K tails, both rope widths
+SHAPES = [
+    ("tiny", {}),
+    ("tiny", dict(T=300, K=200, H=6)),                    # 3 token tiles (44 ragged), K tail 8
+    ("tiny", dict(T=1, K=8, H=1)),                        # single token, single partial k tile
+    ("tiny", dict(T=129, K=64, H=16, Dn=64, Dr=32, w_std=0.1)),
+    ("dsv3_fwd_bf16w", dict(T=300, H=8)),                 # 256-wide tiles cut heads at 64/128
+    ("dsv3_fwd_bf16w", dict(T=260, K=1000, H=3, bias=True)),
+]
+
+
+def _run(w, inp, dev, out_mode, status=None):
+    d = helpers.to_dev(inp, dev)
+    return mlaq.fwd(d["x"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, bias=d.get("b"),
+                    pos=d["pos"], out_mode=out_mode, status=status)
+
+
+@pytest.mark.parametrize("name,ov", SHAPES)
+def test_fwd_bf16_out(cuda_device, name, ov):
+    w = synth.workload(name, **ov)
+    inp = synth.make_inputs(w, seed=0)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    q = _run(w, inp, cuda_device, "bf16", st)
+    mlaq.check_status(st)
+    ref = helpers.oracle_forward(inp, w)
+    helpers.check_bf16_close(q, ref)
+
+
+@pytest.mark.parametrize("name,ov", SHAPES)
+def test_fwd_mxfp8_out(cuda_device, name, ov):
+    w = synth.workload(name, **ov)
+    inp = synth.make_inputs(w, seed=1)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    codes, scales = _run(w, inp, cuda_device, "mxfp8", st)
+    mlaq.check_status(st)
+    q_ref, rc, rs = helpers.oracle_forward(inp, w, quantize=True)
+    helpers.check_mxfp8_close(codes.cpu().numpy(), scales.cpu().numpy(), q_ref, rc, rs)
+
+
+def test_fwd_passthrough_equals_plain_gemm(cuda_device):
+    """The first Dn channels of each head are the GEMM (+bias) itself: run once
+    at position 0 (cos = 1, sin = 0, so RoPE is the identity) and once at real
+    positions; the pass-through channels must agree bit for bit."""
+    w = synth.workload("tiny", T=200)
+    inp = synth.make_inputs(w, seed=2)
+    q1 = _run(w, inp, cuda_device, "bf16")
+    inp0 = dict(inp, pos=torch.zeros(w.T, dtype=torch.int32))
+    q0 = _run(w, inp0, cuda_device, "bf16")
+    assert torch.equal(q1[..., :w.Dn], q0[..., :w.Dn])
+    ref = helpers.oracle_forward(inp0, w)  # = x W^T + b
+    helpers.check_bf16_close(q0, ref)
+
+
+def test_fwd_inputs_unchanged(cuda_device):
+    w = synth.workload("tiny", T=333, H=8)
+    inp = helpers.to_dev(synth.make_inputs(w, seed=3), cuda_device)
+    before = {k: v.clone() for k, v in inp.items() if isinstance(v, torch.Tensor)}
+    mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"],
+             pos=inp["pos"], out_mode="mxfp8")
+    mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"],
+             pos=inp["pos"], out_mode="bf16")
+    torch.cuda.synchronize()
+    for k, v in before.items():
+        assert torch.equal(inp[k], v), k
+
+
+def test_fwd_writes_nothing_outside_outputs(cuda_device):
+    """Canary bytes around q and its scales stay untouched."""
+    w = synth.workload("tiny", T=130)
+    inp = helpers.to_dev(synth.make_inputs(w, seed=4), cuda_device)
+    pad = 4096
+    nq, ns = w.T * w.H * w.D, w.T * w.H * 2
+    qbuf = torch.full((nq + 2 * pad,), 0xA5, dtype=torch.uint8, device=cuda_device)
+    sbuf = torch.full((ns + 2 * pad,), 0x5A, dtype=torch.uint8, device=cuda_device)
+    q = qbuf[pad:pad + nq].view(w.T, w.H, w.D)
+    s = sbuf[pad:pad + ns].view(w.T, w.H, 2)
+    mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"],
+             pos=inp["pos"], out_mode="mxfp8", q_out=q, q_scales=s)
+    torch.cuda.synchronize()
+    assert (qbuf[:pad] == 0xA5).all() and (qbuf[pad + nq:] == 0xA5).all()
+    assert (sbuf[:pad] == 0x5A).all() and (sbuf[pad + ns:] == 0x5A).all()
+
+
+def test_fwd_position_out_of_range_reports_status(cuda_device):
+    w = synth.workload("tiny", T=64)
+    inp = synth.make_inputs(w, seed=5)
+    inp["pos"] = inp["pos"].clone()
+    inp["pos"][7] = w.cs_rows + 3  # outside the table: reported, never read
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    _run(w, inp, cuda_device, "bf16", st)
+    assert int(st.item()) == mlaq.STATUS["MLA_ERR_POS_RANGE"]
+
+
+def test_fwd_wide_table_and_packed_positions(cuda_device):
+    """cs_width > Dr (row pitch = cs_width) and positions restarting per sequence."""
+    w = synth.workload("tiny", T=256, seq_len=100)
+    inp = synth.make_inputs(w, seed=6)
+    cos, sin = synth.rope_table_standard(100, 24)  # 24 columns, Dr = 16 reads the first 16
+    inp["cos"], inp["sin"] = cos, sin
+    q = _run(w, inp, cuda_device, "bf16")
+    ref = helpers.oracle_forward(inp, w)
+    helpers.check_bf16_close(q, ref)
+
+
+@pytest.mark.parametrize("out_mode", ["mxfp8", "bf16"])
+def test_fwd_full_size_sampled(cuda_device, out_mode):
+    """DeepSeek-V3 shape (T=4096, K=1536, H=128, Dn=128, Dr=64) in the launch
+    configuration the benchmark times; 48 sampled tokens checked in full."""
+    w = synth.workload("dsv3_fwd_bf16w")
+    inp = synth.make_inputs(w, seed=0)
+    d = helpers.to_dev(inp, cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    out = mlaq.fwd(d["x"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
+                   out_mode=out_mode, status=st)
+    mlaq.check_status(st)
+    tokens = np.sort(np.random.default_rng(0).choice(w.T, 48, replace=False))
+    tokens[0], tokens[-1] = 0, w.T - 1
+    if out_mode == "mxfp8":
+        q_ref, rc, rs = helpers.oracle_forward(inp, w, tokens=tokens, quantize=True)
+        codes, scales = out
+        idx = torch.from_numpy(tokens).to(cuda_device)
+        helpers.check_mxfp8_close(codes[idx].cpu().numpy(), scales[idx].cpu().numpy(), q_ref, rc, rs)
+    else:
+        q_ref = helpers.oracle_forward(inp, w, tokens=tokens)
+        idx = torch.from_numpy(tokens).to(cuda_device)
+        helpers.check_bf16_close(out[idx], q_ref)

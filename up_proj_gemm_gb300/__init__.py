@@ -1,0 +1,249 @@
+"""GB300 (sm_103a) fused MLA query up-projection: Python binding of libmlaq.so.
+
+The functions here only marshal torch tensors (device memory, the current
+stream) into the C ABI declared in ``include/mlaq.h``; every step of the
+computation runs in the library's CUDA kernels. There is no fallback: when
+``libmlaq.so`` is missing or the call is rejected, an exception is raised.
+
+Forward (TransformerEngine PR "Add support for fused Q Up-Proj
+GEMM/RoPE/Quant"): ``q = RoPE(x W^T + b)``, optionally MXFP8.
+Backward (TransformerEngine PR "Add a backwards linear function to be used
+with the fused mla q up-proj"): inverse RoPE on dq fused into dgrad and
+wgrad, plus the bias gradient.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "MlaError", "lib", "library_path", "fwd", "bwd_dgrad", "bwd_wgrad", "mxfp8_quantize_rows",
+    "workspace_size", "status_string", "check_status", "Shape", "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libmlaq.so")
+
+STATUS = {
+    "MLA_OK": 0, "MLA_ERR_INVALID_ARG": 1, "MLA_ERR_ROPE_WIDTH": 2, "MLA_ERR_ALIGNMENT": 3,
+    "MLA_ERR_ALIAS": 4, "MLA_ERR_UNSUPPORTED": 5, "MLA_ERR_CUDA": 6, "MLA_ERR_TIMEOUT": 7,
+    "MLA_ERR_POS_RANGE": 8, "MLA_ERR_WORKSPACE": 9,
+}
+WEIGHT_MODES = {"bf16": 0, "mxfp8": 1}
+OUT_MODES = {"bf16": 0, "mxfp8": 1}
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("K", ctypes.c_int64), ("H", ctypes.c_int32),
+                ("Dn", ctypes.c_int32), ("Dr", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("cs_rows", ctypes.c_int64), ("cs_width", ctypes.c_int64)]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_SIGS = {
+    "mla_q_uproj_fwd": (_int, [ctypes.POINTER(Shape), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                               _vp, _vp, _vp, _vp, _vp]),
+    "mla_q_uproj_bwd_dgrad": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     ctypes.c_size_t, _vp, _vp]),
+    "mla_q_uproj_bwd_wgrad": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     ctypes.c_size_t, _vp, _vp]),
+    "mxfp8_quantize_rows": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
+    "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
+    "mla_status_string": (ctypes.c_char_p, [_int]),
+    "mla_version": (_int, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmlaq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise RuntimeError(
+                    f"{library_path} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                    f"g.build()\"` (nvcc, sm_103a). There is no non-CUDA fallback.")
+            l = ctypes.CDLL(library_path)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(l, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = l
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().mla_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, device=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def _shape(T, K, H, Dn, Dr, cos):
+    return Shape(T=int(T), K=int(K), H=int(H), Dn=int(Dn), Dr=int(Dr), reserved=0,
+                 cs_rows=int(cos.shape[0]), cs_width=int(cos.shape[1]))
+
+
+def _call(fn, what, *args):
+    st = fn(*args)
+    if st != 0:
+        raise MlaError(st, what)
+
+
+def check_status(status: torch.Tensor, what: str = "device status") -> None:
+    """Synchronize on the status word written by the kernels; raise if set."""
+    v = int(status.item())
+    if v != 0:
+        raise MlaError(v, what)
+
+
+def workspace_size(T, K, H, Dn, Dr, cs_rows, cs_width, which: int) -> int:
+    s = Shape(T=T, K=K, H=H, Dn=Dn, Dr=Dr, reserved=0, cs_rows=cs_rows, cs_width=cs_width)
+    return int(lib().mla_q_uproj_workspace_size(ctypes.byref(s), int(which)))
+
+
+def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_mode="mxfp8",
+        x_scales=None, w_scales=None, q_out=None, q_scales=None, status=None, stream=None):
+    """Fused forward. Returns q [T, H, D] (bf16 or uint8 E4M3 codes), plus the
+    scales [T, H, ceil(D/32)] uint8 when out_mode is "mxfp8".
+
+    weight_mode "bf16": x [T, K] bf16, W [N, K] bf16.
+    weight_mode "mxfp8": x, W uint8 E4M3 codes with x_scales [T, K/32],
+    w_scales [N, K/32] uint8 E8M0."""
+    wm, om = WEIGHT_MODES[weight_mode], OUT_MODES[out_mode]
+    in_dtype = torch.uint8 if wm else torch.bfloat16
+    dev = x.device
+    _need(x, "x", in_dtype, ndim=2)
+    _need(W, "W", in_dtype, dev, ndim=2)
+    _need(cos, "cos", torch.float32, dev, ndim=2)
+    _need(sin, "sin", torch.float32, dev, ndim=2)
+    if cos.shape != sin.shape:
+        raise ValueError("cos and sin must have the same shape")
+    T, K = x.shape
+    D = Dn + Dr
+    N = H * D
+    if tuple(W.shape) != (N, K):
+        raise ValueError(f"W must be [{N}, {K}]")
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, dev, ndim=1)
+    if pos is not None:
+        _need(pos, "pos", torch.int32, dev, ndim=1)
+    if wm:
+        _need(x_scales, "x_scales", torch.uint8, dev, ndim=2)
+        _need(w_scales, "w_scales", torch.uint8, dev, ndim=2)
+    if q_out is None:
+        q_out = torch.empty((T, H, D), dtype=torch.uint8 if om else torch.bfloat16, device=dev)
+    if om and q_scales is None:
+        q_scales = torch.empty((T, H, (D + 31) // 32), dtype=torch.uint8, device=dev)
+    s = _shape(T, K, H, Dn, Dr, cos)
+    _call(lib().mla_q_uproj_fwd, "mla_q_uproj_fwd", ctypes.byref(s), wm, om, _ptr(x),
+          _ptr(x_scales), _ptr(W), _ptr(w_scales), _ptr(bias), _ptr(cos), _ptr(sin), _ptr(pos),
+          _ptr(q_out), _ptr(q_scales if om else None), _ptr(status), _stream(dev, stream))
+    return (q_out, q_scales) if om else q_out
+
+
+def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream=None):
+    """dx [T, K] bf16 = (inverse-RoPE dq) W."""
+    dev = dq.device
+    _need(dq, "dq", torch.bfloat16)
+    _need(W, "W", torch.bfloat16, dev, ndim=2)
+    _need(cos, "cos", torch.float32, dev, ndim=2)
+    _need(sin, "sin", torch.float32, dev, ndim=2)
+    T = dq.shape[0]
+    N, K = W.shape
+    if dq.numel() != T * N:
+        raise ValueError("dq must hold T * H * (Dn + Dr) elements")
+    if pos is not None:
+        _need(pos, "pos", torch.int32, dev, ndim=1)
+    if dx is None:
+        dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    s = _shape(T, K, H, Dn, Dr, cos)
+    _call(lib().mla_q_uproj_bwd_dgrad, "mla_q_uproj_bwd_dgrad", ctypes.byref(s), _ptr(dq), _ptr(W),
+          _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dx), None, 0, _ptr(status), _stream(dev, stream))
+    return dx
+
+
+def bwd_wgrad(dq, x, cos, sin, H, Dn, Dr, pos=None, dW=None, db=True, status=None, stream=None):
+    """dW [N, K] bf16 = (inverse-RoPE dq)^T x and db [N] bf16 = its token sum.
+
+    db=True allocates the bias gradient, db=None/False skips it, or pass a
+    tensor. Returns (dW, db-or-None)."""
+    dev = dq.device
+    _need(dq, "dq", torch.bfloat16)
+    _need(x, "x", torch.bfloat16, dev, ndim=2)
+    _need(cos, "cos", torch.float32, dev, ndim=2)
+    _need(sin, "sin", torch.float32, dev, ndim=2)
+    T, K = x.shape
+    N = H * (Dn + Dr)
+    if dq.numel() != T * N:
+        raise ValueError("dq must hold T * H * (Dn + Dr) elements")
+    if pos is not None:
+        _need(pos, "pos", torch.int32, dev, ndim=1)
+    if dW is None:
+        dW = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    if db is True:
+        db = torch.empty((N,), dtype=torch.bfloat16, device=dev)
+    elif db is False:
+        db = None
+    s = _shape(T, K, H, Dn, Dr, cos)
+    _call(lib().mla_q_uproj_bwd_wgrad, "mla_q_uproj_bwd_wgrad", ctypes.byref(s), _ptr(dq), _ptr(x),
+          _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dW), _ptr(db), None, 0, _ptr(status),
+          _stream(dev, stream))
+    return dW, db
+
+
+def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None):
+    """Rowwise MXFP8 of a 2-D fp32/bf16 CUDA tensor -> (codes uint8 [R, C], scales uint8 [R, ceil(C/32)]).
+
+    A row pitch larger than C is taken from ``inp.stride(0)`` (the tensor must
+    have unit inner stride)."""
+    if inp.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("input must be float32 or bfloat16")
+    if not inp.is_cuda or inp.dim() != 2 or inp.stride(1) != 1:
+        raise ValueError("input must be a 2-D CUDA tensor with unit inner stride")
+    R, C = inp.shape
+    ld_in = int(inp.stride(0)) if R > 1 else int(C)
+    dev = inp.device
+    if codes is None:
+        codes = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((R, (C + 31) // 32), dtype=torch.uint8, device=dev)
+    dt = 0 if inp.dtype == torch.float32 else 1
+    _call(lib().mxfp8_quantize_rows, "mxfp8_quantize_rows", R, C, dt, _ptr(inp), ld_in, _ptr(codes),
+          _ptr(scales), _stream(dev, stream))
+    return codes, scales

@@ -1,0 +1,335 @@
+// C ABI of libmlaq.so: argument validation, then the kernel launchers.
+//
+// Every check below runs on the host before any CUDA call, so a rejected
+// call touches neither the device nor the stream. The order of checks fixes
+// which status a call with several faults returns: missing/invalid
+// arguments, table width, positions, tiling support, alignment, aliasing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace mlaq {
+
+// ------------------------------------------------------------- device info
+int current_device_info(DeviceInfo* out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo& d = cache[dev];
+    if (d.device != dev) {
+        DeviceInfo n;
+        n.device = dev;
+        if (cudaDeviceGetAttribute(&n.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&n.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return MLA_ERR_CUDA;
+        d = n;
+    }
+    *out = d;
+    // The kernels are built for sm_103a only.
+    if (d.cc_major != 10 || d.cc_minor != 3) return MLA_ERR_CUDA;
+    return MLA_OK;
+}
+
+// ------------------------------------------------------------- tensor maps
+int make_tmap_2d(void* tmap_out, const void* base, int dtype, uint64_t inner, uint64_t outer,
+                 uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!encode) return MLA_ERR_CUDA;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(reinterpret_cast<CUtensorMap*>(tmap_out),
+                        dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                        const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+namespace {
+
+struct Range {
+    uintptr_t lo = 0, hi = 0;  // [lo, hi); empty when lo == hi
+};
+
+Range rng(const void* p, int64_t bytes) {
+    Range r;
+    if (p && bytes > 0) {
+        r.lo = reinterpret_cast<uintptr_t>(p);
+        r.hi = r.lo + (uintptr_t)bytes;
+    }
+    return r;
+}
+
+bool overlap(const Range& a, const Range& b) {
+    return a.lo != a.hi && b.lo != b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+template <size_t NO, size_t NI>
+bool any_alias(const Range (&outs)[NO], const Range (&ins)[NI]) {
+    for (size_t i = 0; i < NO; ++i) {
+        for (size_t j = 0; j < NI; ++j)
+            if (overlap(outs[i], ins[j])) return true;
+        for (size_t j = i + 1; j < NO; ++j)
+            if (overlap(outs[i], outs[j])) return true;
+    }
+    return false;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int64_t kI32Max = 0x7fffffffLL;
+
+// Checks shared by every mla_q_uproj_* call. On success fills D and N.
+int check_shape(const mla_q_shape* s, int* D, int64_t* N) {
+    if (!s) return MLA_ERR_INVALID_ARG;
+    if (s->T < 0 || s->K <= 0 || s->H <= 0 || s->Dn < 0 || s->Dr <= 0 || (s->Dr & 1) ||
+        s->cs_rows < 0 || s->cs_width < 0 || s->reserved != 0)
+        return MLA_ERR_INVALID_ARG;
+    const int64_t d = (int64_t)s->Dn + s->Dr;
+    const int64_t n = d * s->H;
+    if (d > kI32Max || n > kI32Max || s->T > kI32Max || s->K > kI32Max) return MLA_ERR_INVALID_ARG;
+    *D = (int)d;
+    *N = n;
+    return MLA_OK;
+}
+
+int check_table_and_positions(const mla_q_shape* s, const float* cos_tab, const float* sin_tab,
+                              const int32_t* pos) {
+    if (s->cs_width < s->Dr) return MLA_ERR_ROPE_WIDTH;
+    if (s->T > 0 && (!cos_tab || !sin_tab)) return MLA_ERR_INVALID_ARG;
+    if (!pos && s->T > s->cs_rows) return MLA_ERR_POS_RANGE;
+    if (s->cs_rows == 0 && s->T > 0) return MLA_ERR_POS_RANGE;
+    (void)pos;
+    return MLA_OK;
+}
+
+bool rope_dim_supported(int Dr) { return Dr == 16 || Dr == 32 || Dr == 64; }
+
+}  // namespace
+}  // namespace mlaq
+
+using namespace mlaq;
+
+extern "C" {
+
+MLAQ_API int mla_version(void) { return 10000; }
+
+MLAQ_API const char* mla_status_string(int status) {
+    switch (status) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+        case MLA_ERR_ROPE_WIDTH: return "MLA_ERR_ROPE_WIDTH";
+        case MLA_ERR_ALIGNMENT: return "MLA_ERR_ALIGNMENT";
+        case MLA_ERR_ALIAS: return "MLA_ERR_ALIAS";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+        case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+        case MLA_ERR_POS_RANGE: return "MLA_ERR_POS_RANGE";
+        case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+        default: return "MLA_ERR_UNKNOWN";
+    }
+}
+
+MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape* shape, int which) {
+    int D;
+    int64_t N;
+    if (check_shape(shape, &D, &N) != MLA_OK || which < 0 || which > 2) return 0;
+    return 0;  // no kernel of this library needs scratch memory
+}
+
+MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_mode, const void* x,
+                             const uint8_t* x_scales, const void* W, const uint8_t* w_scales,
+                             const void* bias, const float* cos_tab, const float* sin_tab,
+                             const int32_t* pos, void* q_out, uint8_t* q_scales_out, int* dev_status,
+                             void* stream) {
+    int D;
+    int64_t N;
+    int st = check_shape(shape, &D, &N);
+    if (st != MLA_OK) return st;
+    const mla_q_shape& s = *shape;
+    if (weight_mode != MLA_WEIGHT_BF16 && weight_mode != MLA_WEIGHT_MXFP8) return MLA_ERR_INVALID_ARG;
+    if (out_mode != MLA_OUT_BF16 && out_mode != MLA_OUT_MXFP8) return MLA_ERR_INVALID_ARG;
+    const bool mxw = weight_mode == MLA_WEIGHT_MXFP8, mxo = out_mode == MLA_OUT_MXFP8;
+    if (mxw != (x_scales != nullptr) || mxw != (w_scales != nullptr)) return MLA_ERR_INVALID_ARG;
+    if (mxo != (q_scales_out != nullptr)) return MLA_ERR_INVALID_ARG;
+    if (s.T > 0 && (!x || !W || !q_out)) return MLA_ERR_INVALID_ARG;
+    if (mxw && (s.K % 32)) return MLA_ERR_INVALID_ARG;  // scales are per 32 along K
+    st = check_table_and_positions(&s, cos_tab, sin_tab, pos);
+    if (st != MLA_OK) return st;
+    if (s.T == 0) return MLA_OK;
+
+    if (!rope_dim_supported(s.Dr) || s.Dn % 32) return MLA_ERR_UNSUPPORTED;
+    if (mxw && s.K % 128) return MLA_ERR_UNSUPPORTED;
+    if (fwd_tile_n(N, D, s.Dn, s.Dr, mxw ? 192 : 256) == 0) return MLA_ERR_UNSUPPORTED;
+
+    const int64_t esz = mxw ? 1 : 2;
+    if ((s.K * esz) % 16) return MLA_ERR_ALIGNMENT;
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(q_out, 16) || !aligned(x_scales, 4) ||
+        !aligned(w_scales, 4) || !aligned(bias, 2) || !aligned(cos_tab, 4) || !aligned(sin_tab, 4) ||
+        !aligned(pos, 4) || !aligned(dev_status, 4))
+        return MLA_ERR_ALIGNMENT;
+
+    const int64_t NB = (D + 31) / 32;
+    const int64_t table = s.cs_rows * s.cs_width * 4;
+    const Range outs[] = {rng(q_out, s.T * N * (mxo ? 1 : 2)), rng(q_scales_out, s.T * s.H * NB),
+                          rng(dev_status, 4)};
+    const Range ins[] = {rng(x, s.T * s.K * esz), rng(x_scales, s.T * (s.K / 32)),
+                         rng(W, N * s.K * esz),   rng(w_scales, N * (s.K / 32)),
+                         rng(bias, N * 2),        rng(cos_tab, table),
+                         rng(sin_tab, table),     rng(pos, s.T * 4)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+
+    FwdArgs a{};
+    a.T = s.T;
+    a.K = s.K;
+    a.H = s.H;
+    a.Dn = s.Dn;
+    a.Dr = s.Dr;
+    a.cs_rows = s.cs_rows;
+    a.cs_width = s.cs_width;
+    a.weight_mode = weight_mode;
+    a.out_mode = out_mode;
+    a.x = x;
+    a.x_scales = x_scales;
+    a.W = W;
+    a.w_scales = w_scales;
+    a.bias = bias;
+    a.cos_tab = cos_tab;
+    a.sin_tab = sin_tab;
+    a.pos = pos;
+    a.q_out = q_out;
+    a.q_scales = q_scales_out;
+    a.status = dev_status;
+    return launch_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+static int check_bwd(const mla_q_shape* shape, const void* dq, const void* op, const float* cos_tab,
+                     const float* sin_tab, const int32_t* pos, const void* out, void* workspace,
+                     size_t ws_bytes, int which, int* D, int64_t* N) {
+    int st = check_shape(shape, D, N);
+    if (st != MLA_OK) return st;
+    const mla_q_shape& s = *shape;
+    if (s.T > 0 && (!dq || !op || !out)) return MLA_ERR_INVALID_ARG;
+    st = check_table_and_positions(&s, cos_tab, sin_tab, pos);
+    if (st != MLA_OK) return st;
+    if (ws_bytes < mla_q_uproj_workspace_size(shape, which) ||
+        (mla_q_uproj_workspace_size(shape, which) > 0 && !workspace))
+        return MLA_ERR_WORKSPACE;
+    if (!rope_dim_supported(s.Dr) || s.Dn % s.Dr) return MLA_ERR_UNSUPPORTED;
+    if ((s.K * 2) % 16 || ((*N) * 2) % 16) return MLA_ERR_ALIGNMENT;
+    return MLA_OK;
+}
+
+MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape* shape, const void* dq, const void* W,
+                                   const float* cos_tab, const float* sin_tab, const int32_t* pos,
+                                   void* dx, void* workspace, size_t ws_bytes, int* dev_status,
+                                   void* stream) {
+    int D;
+    int64_t N;
+    int st = check_bwd(shape, dq, W, cos_tab, sin_tab, pos, dx, workspace, ws_bytes, 1, &D, &N);
+    if (st != MLA_OK) return st;
+    const mla_q_shape& s = *shape;
+    if (!aligned(dq, 16) || !aligned(W, 16) || !aligned(dx, 16) || !aligned(cos_tab, 4) ||
+        !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4))
+        return MLA_ERR_ALIGNMENT;
+    const int64_t table = s.cs_rows * s.cs_width * 4;
+    const Range outs[] = {rng(dx, s.T * s.K * 2), rng(dev_status, 4)};
+    const Range ins[] = {rng(dq, s.T * N * 2), rng(W, N * s.K * 2), rng(cos_tab, table),
+                         rng(sin_tab, table), rng(pos, s.T * 4)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    if (s.T == 0) return MLA_OK;
+    BwdArgs a{};
+    a.T = s.T;
+    a.K = s.K;
+    a.H = s.H;
+    a.Dn = s.Dn;
+    a.Dr = s.Dr;
+    a.cs_rows = s.cs_rows;
+    a.cs_width = s.cs_width;
+    a.dq = dq;
+    a.W = W;
+    a.cos_tab = cos_tab;
+    a.sin_tab = sin_tab;
+    a.pos = pos;
+    a.dx = dx;
+    a.status = dev_status;
+    return launch_dgrad(a, static_cast<cudaStream_t>(stream));
+}
+
+MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape* shape, const void* dq, const void* x,
+                                   const float* cos_tab, const float* sin_tab, const int32_t* pos,
+                                   void* dW, void* db, void* workspace, size_t ws_bytes,
+                                   int* dev_status, void* stream) {
+    int D;
+    int64_t N;
+    int st = check_bwd(shape, dq, x, cos_tab, sin_tab, pos, dW, workspace, ws_bytes, 2, &D, &N);
+    if (st != MLA_OK) return st;
+    const mla_q_shape& s = *shape;
+    if (!aligned(dq, 16) || !aligned(x, 16) || !aligned(dW, 16) || !aligned(db, 4) ||
+        !aligned(cos_tab, 4) || !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4))
+        return MLA_ERR_ALIGNMENT;
+    const int64_t table = s.cs_rows * s.cs_width * 4;
+    const Range outs[] = {rng(dW, N * s.K * 2), rng(db, N * 2), rng(dev_status, 4)};
+    const Range ins[] = {rng(dq, s.T * N * 2), rng(x, s.T * s.K * 2), rng(cos_tab, table),
+                         rng(sin_tab, table), rng(pos, s.T * 4)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    BwdArgs a{};
+    a.T = s.T;
+    a.K = s.K;
+    a.H = s.H;
+    a.Dn = s.Dn;
+    a.Dr = s.Dr;
+    a.cs_rows = s.cs_rows;
+    a.cs_width = s.cs_width;
+    a.dq = dq;
+    a.x = x;
+    a.cos_tab = cos_tab;
+    a.sin_tab = sin_tab;
+    a.pos = pos;
+    a.dW = dW;
+    a.db = db;
+    a.status = dev_status;
+    // T == 0 still defines dW = 0 and db = 0: the kernel writes zeros.
+    return launch_wgrad(a, static_cast<cudaStream_t>(stream));
+}
+
+MLAQ_API int mxfp8_quantize_rows(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                                 uint8_t* codes, uint8_t* scales, void* stream) {
+    if (R < 0 || C < 0 || ld_in < C) return MLA_ERR_INVALID_ARG;
+    if (in_dtype != MLA_IN_F32 && in_dtype != MLA_IN_BF16) return MLA_ERR_INVALID_ARG;
+    if (R == 0 || C == 0) return MLA_OK;
+    if (!in || !codes || !scales) return MLA_ERR_INVALID_ARG;
+    const int64_t esz = in_dtype == MLA_IN_F32 ? 4 : 2;
+    if (!aligned(in, (uintptr_t)esz)) return MLA_ERR_ALIGNMENT;
+    const int64_t nb = (C + 31) / 32;
+    const Range outs[] = {rng(codes, R * C), rng(scales, R * nb)};
+    const Range ins[] = {rng(in, ((R - 1) * ld_in + C) * esz)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    return launch_mxfp8_quantize(R, C, in_dtype, in, ld_in, codes, scales,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

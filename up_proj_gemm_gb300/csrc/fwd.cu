@@ -1,0 +1,478 @@
+// Fused MLA query up-projection forward on sm_103a tensor cores.
+//
+// TransformerEngine PR "Add support for fused Q Up-Proj GEMM/RoPE/Quant",
+// description paragraph and flowchart: q = RoPE(x W^T + b), then MXFP8
+// quantization, with a 16-bit or an MXFP8 projection weight. The pages name
+// a cuDNN-frontend kernel for SM100; this is an independent design for
+// sm_103a:
+//
+//   * persistent CTAs (one per SM), each walking a static list of
+//     128-token x BN-channel output tiles (token index fastest, so the CTAs
+//     running together share weight tiles in L2);
+//   * warp 0: TMA producer, filling an S-stage shared-memory ring with x and
+//     W tiles (128-byte rows, 128-byte swizzle). For MXFP8 weights it also
+//     gathers the E8M0 scale bytes of both operands with 4-byte cp.async
+//     into the 32x16-byte layout that tcgen05.cp replicates into TMEM;
+//   * warp 1: one thread issues tcgen05.mma (M=128, N=BN, K=16 bf16 or K=32
+//     block-scaled E4M3) into a double-buffered fp32 TMEM accumulator and
+//     commits each stage back to the producer;
+//   * warps 2-5: epilogue. Each thread owns one token row of the tile
+//     (tcgen05.ld 32x32b), adds the bias, applies the rotate-half RoPE pair
+//     (i, i+Dr/2) thread-locally, and writes bf16 or MXFP8 (per-32-channel
+//     amax -> E8M0 scale -> E4M3 codes) with 16-byte stores into a fresh
+//     output. The next tile's mainloop runs in the other accumulator buffer
+//     meanwhile.
+//
+// Tiles never split a rope region or an MXFP8 block (the host picks BN so).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace mlaq {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccStride = 256;  // TMEM column offset of accumulator buffer 1
+constexpr uint32_t kSfCol0 = 448;     // first TMEM column of the per-stage scale factors
+constexpr uint32_t kSfColsPerStage = 12;  // 4 (A: 128 rows) + 8 (B: up to 256 rows)
+constexpr uint32_t kSfBytesPerStage = 512 + 1024;
+
+struct FwdParams {
+    int T, H, N, D, Dn;
+    int BN;
+    int num_m_tiles, num_tiles, k_tiles;
+    int stages;
+    uint32_t a_bytes, stage_bytes, tx_bytes;
+    uint32_t idesc;
+    int ksb;  // scale bytes per operand row (K / 32)
+    const uint16_t* bias;
+    const float* cos_tab;
+    const float* sin_tab;
+    const int32_t* pos;
+    long long cs_rows, cs_width;
+    uint8_t* q_out;
+    uint8_t* q_scales;
+    const uint8_t* x_scales;
+    const uint8_t* w_scales;
+    int* status;
+};
+
+struct Smem {
+    uint32_t base;      // shared address of stage 0 (1024-aligned)
+    uint32_t sf;        // scale staging (MXFP8 weights)
+    uint32_t bars;      // mbarriers
+    int S;
+    __device__ uint32_t a(int s, const FwdParams& p) const { return base + (uint32_t)s * p.stage_bytes; }
+    __device__ uint32_t b(int s, const FwdParams& p) const { return a(s, p) + p.a_bytes; }
+    __device__ uint32_t sfa(int s) const { return sf + (uint32_t)s * kSfBytesPerStage; }
+    __device__ uint32_t sfb(int s) const { return sfa(s) + 512; }
+    __device__ uint32_t full(int s) const { return bars + 8u * s; }
+    __device__ uint32_t empty(int s) const { return bars + 8u * (S + s); }
+    __device__ uint32_t tfull(int b) const { return bars + 8u * (2 * S + b); }
+    __device__ uint32_t tempty(int b) const { return bars + 8u * (2 * S + 2 + b); }
+    __device__ uint32_t drain() const { return bars + 8u * (2 * S + 4); }
+};
+
+__device__ __forceinline__ float bf16_at(const uint16_t* p, int i) {
+    return __uint_as_float((uint32_t)__ldg(p + i) << 16);
+}
+
+// ------------------------------------------------------------ epilogue parts
+template <bool MXOUT, int NV>
+__device__ __forceinline__ void store_unit(const FwdParams& p, const float (&v)[NV], int64_t t,
+                                           int64_t n, int h, int c) {
+    // v holds output channels [n, n + NV) of token t; they are channels
+    // [c, c + NV) of head h. n is a multiple of 16.
+    if (MXOUT) {
+        const int NB = (p.D + 31) / 32;
+#pragma unroll
+        for (int blk = 0; blk < (NV + 31) / 32; ++blk) {
+            constexpr int W = 32;
+            float b[W];
+#pragma unroll
+            for (int i = 0; i < W; ++i) b[i] = (blk * 32 + i < NV) ? v[blk * 32 + i] : 0.f;
+            const int nvalid = (NV - blk * 32) < 32 ? (NV - blk * 32) : 32;
+            uint32_t codes[8];
+            const uint32_t sb = quantize_block_regs<W>(b, nvalid, codes);
+            uint8_t* dst = p.q_out + t * p.N + n + blk * 32;
+            st_global_v4(dst, codes[0], codes[1], codes[2], codes[3]);
+            if (nvalid > 16) st_global_v4(dst + 16, codes[4], codes[5], codes[6], codes[7]);
+            p.q_scales[(t * p.H + h) * NB + (c + blk * 32) / 32] = (uint8_t)sb;
+        }
+    } else {
+        uint8_t* dst = p.q_out + (t * p.N + n) * 2;
+#pragma unroll
+        for (int i = 0; i < NV; i += 8)
+            st_global_v4(dst + 2 * i, pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
+                         pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]));
+    }
+}
+
+template <bool MXOUT>
+__device__ __forceinline__ void nope_unit(const FwdParams& p, uint32_t taddr, bool valid, int64_t t,
+                                          int64_t n, int h, int c) {
+    uint32_t r[32];
+    __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+    tmem_ld32(taddr, r);
+    tmem_ld_wait();
+    if (!valid) return;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    if (p.bias) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] += bf16_at(p.bias, (int)n + i);
+    }
+    store_unit<MXOUT, 32>(p, v, t, n, h, c);
+}
+
+template <bool MXOUT, int DR>
+__device__ __forceinline__ void rope_unit(const FwdParams& p, uint32_t taddr, bool valid, int64_t t,
+                                          int64_t n, int h, int prow) {
+    constexpr int HH = DR / 2;
+    uint32_t r[DR / 16][16];
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < DR / 16; ++j) tmem_ld16(taddr + 16 * j, r[j]);
+    tmem_ld_wait();
+    if (!valid) return;
+    float y[DR];
+#pragma unroll
+    for (int i = 0; i < DR; ++i) y[i] = __uint_as_float(r[i / 16][i % 16]);
+    if (p.bias) {
+#pragma unroll
+        for (int i = 0; i < DR; ++i) y[i] += bf16_at(p.bias, (int)n + i);
+    }
+    const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
+    const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
+    float o[DR];
+#pragma unroll
+    for (int i = 0; i < HH; ++i) {
+        const float a = y[i], c = y[i + HH];
+        const float ci = __ldg(cs + i), si = __ldg(sn + i);
+        const float cj = __ldg(cs + i + HH), sj = __ldg(sn + i + HH);
+        o[i] = a * ci - c * si;
+        o[i + HH] = c * cj + a * sj;
+    }
+    store_unit<MXOUT, DR>(p, o, t, n, h, p.Dn);
+}
+
+// ------------------------------------------------------------------- kernel
+template <bool MXW, bool MXOUT, int DR>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    Smem sm;
+    sm.S = p.stages;
+    sm.base = (raw + 1023u) & ~1023u;
+    sm.sf = sm.base + (uint32_t)p.stages * p.stage_bytes;
+    sm.bars = sm.sf + (MXW ? (uint32_t)p.stages * kSfBytesPerStage : 0u);
+    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (2 * p.stages + 5);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(sm.full(s), MXW ? 1 + 32 : 1);
+            mbar_init(sm.empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sm.tfull(b), 1);
+            mbar_init(sm.tempty(b), 4);
+        }
+        mbar_init(sm.drain(), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32((const void*)tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t issued_mask = 0, issued_par = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            const int mt = tile % p.num_m_tiles;
+            const int nt = tile / p.num_m_tiles;
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(sm.full(s), p.tx_bytes);
+                    // x / W tiles: inner coordinate is the K element index
+                    const int kc = kt * (MXW ? 128 : 64);
+                    tma_load_2d(sm.a(s, p), &tmA, kc, mt * kBM, sm.full(s));
+                    tma_load_2d(sm.b(s, p), &tmB, kc, nt * p.BN, sm.full(s));
+                }
+                if (MXW) {
+                    // scale bytes [4 kt, 4 kt + 4) of each row; row r of a 128-row
+                    // chunk goes to byte (r % 32) * 16 + (r / 32) * 4.
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = lane + 32 * j;
+                        const int64_t row = (int64_t)mt * kBM + r;
+                        if (row < p.T)
+                            cp_async_4(sm.sfa(s) + lane * 16 + j * 4,
+                                       p.x_scales + row * p.ksb + kt * 4);
+                    }
+                    for (int j = 0; j < p.BN / 32; ++j) {
+                        const int r = lane + 32 * j;
+                        const int64_t row = (int64_t)nt * p.BN + r;
+                        cp_async_4(sm.sfb(s) + (r / 128) * 512 + lane * 16 + ((r % 128) / 32) * 4,
+                                   p.w_scales + row * p.ksb + kt * 4);
+                    }
+                    cp_async_mbar_arrive_noinc(sm.full(s));
+                }
+                issued_mask |= 1u << s;
+                issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                if (++s == p.stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            // unwinding: let every copy this warp started land before the CTA exits
+            for (int q = 0; q < p.stages; ++q)
+                if (issued_mask & (1u << q))
+                    mbar_wait(sm.full(q), (issued_par >> q) & 1u, nullptr, 200000000ull);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+                const int b = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!mbar_wait(sm.tempty(b), (use & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)b * kAccStride;
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!mbar_wait(sm.full(s), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
+                    if (MXW) {
+                        fence_proxy_async_smem();  // scale bytes arrived through the generic proxy
+                        const uint32_t sfa_col = tmem_base + kSfCol0 + kSfColsPerStage * s;
+                        const uint32_t sfb_col = sfa_col + 4;
+                        tmem_cp_32x128b_warpx4(sfa_col, smem_desc(sm.sfa(s), 0, 128, kLayoutNone));
+                        for (int c = 0; c < (p.BN + 127) / 128; ++c)
+                            tmem_cp_32x128b_warpx4(sfb_col + 4 * c,
+                                                   smem_desc(sm.sfb(s) + 512 * c, 0, 128, kLayoutNone));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t id = p.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
+                            mma_mxf8(d_tmem, desc_kmajor_sw128(a0 + 32 * j), desc_kmajor_sw128(b0 + 32 * j),
+                                     id, sfa_col, sfb_col, (kt | j) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma_bf16(d_tmem, desc_kmajor_sw128(a0 + 32 * j), desc_kmajor_sw128(b0 + 32 * j),
+                                     p.idesc, (kt | j) != 0);
+                    }
+                    mma_commit(sm.empty(s));
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(sm.tfull(b));
+            }
+            if (!ok) {
+                // unwinding: wait (bounded) for the MMAs already issued
+                mma_commit(sm.drain());
+                mbar_wait(sm.drain(), 0, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+        const int row = quad * 32 + lane;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+            const int b = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int mt = tile % p.num_m_tiles;
+            const int nt = tile / p.num_m_tiles;
+            const int64_t t = (int64_t)mt * kBM + row;
+            const bool valid = t < p.T;
+            int prow = 0;
+            if (valid) {
+                const int64_t pp = p.pos ? (int64_t)__ldg(p.pos + t) : t;
+                if (pp < 0 || pp >= p.cs_rows) record_status(p.status, MLA_ERR_POS_RANGE);
+                else prow = (int)pp;
+            }
+            const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
+            const int64_t n0 = (int64_t)nt * p.BN;
+            int col = 0;
+            while (col < p.BN) {
+                const int64_t n = n0 + col;
+                const int h = (int)(n / p.D);
+                const int c = (int)(n - (int64_t)h * p.D);
+                if (c < p.Dn) {
+                    nope_unit<MXOUT>(p, trow + col, valid, t, n, h, c);
+                    col += 32;
+                } else {
+                    rope_unit<MXOUT, DR>(p, trow + col, valid, t, n, h, prow);
+                    col += DR;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.tempty(b));
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) record_status(p.status, MLA_ERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <bool MXW, bool MXOUT, int DR>
+int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const FwdParams& p, int grid,
+                   size_t smem, cudaStream_t stream) {
+    auto kern = fwd_kernel<MXW, MXOUT, DR>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return MLA_ERR_CUDA;
+    kern<<<grid, kThreads, smem, stream>>>(ta, tb, p);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+template <bool MXW, bool MXOUT>
+int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const FwdParams& p, int grid,
+              size_t smem, cudaStream_t stream) {
+    switch (Dr) {
+        case 16: return launch_variant<MXW, MXOUT, 16>(ta, tb, p, grid, smem, stream);
+        case 32: return launch_variant<MXW, MXOUT, 32>(ta, tb, p, grid, smem, stream);
+        case 64: return launch_variant<MXW, MXOUT, 64>(ta, tb, p, grid, smem, stream);
+        default: return MLA_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn) {
+    for (int bn = max_bn; bn >= 16; bn -= 16) {
+        if (N % bn) continue;
+        bool ok = true;
+        const int64_t heads = N / D;
+        for (int64_t h = 0; ok && h < heads; ++h) {
+            const int64_t rs = h * D + Dn, re = h * D + D - 1;  // rope region
+            if (rs / bn != re / bn) ok = false;
+            for (int c = 0; ok && c < Dn; c += 32)  // pass-through blocks
+                if ((h * D + c) / bn != (h * D + c + 31) / bn) ok = false;
+        }
+        if (ok) return bn;
+    }
+    return 0;
+}
+
+int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+    DeviceInfo di;
+    int st = current_device_info(&di);
+    if (st != MLA_OK) return st;
+    const bool mxw = a.weight_mode == MLA_WEIGHT_MXFP8;
+    const int D = a.Dn + a.Dr;
+    const int64_t N = (int64_t)a.H * D;
+    // TMEM: two accumulators at columns 0 and 256; MXFP8 scale factors from column 448.
+    const int BN = fwd_tile_n(N, D, a.Dn, a.Dr, mxw ? 192 : 256);
+    if (BN == 0 || (mxw && BN % 32)) return MLA_ERR_UNSUPPORTED;
+
+    FwdParams p{};
+    p.T = (int)a.T;
+    p.H = a.H;
+    p.N = (int)N;
+    p.D = D;
+    p.Dn = a.Dn;
+    p.BN = BN;
+    p.num_m_tiles = (int)((a.T + kBM - 1) / kBM);
+    p.num_tiles = p.num_m_tiles * (int)(N / BN);
+    const int bk = mxw ? 128 : 64;  // K elements per 128-byte row
+    p.k_tiles = (int)((a.K + bk - 1) / bk);
+    p.a_bytes = kBM * 128;
+    p.stage_bytes = p.a_bytes + (uint32_t)BN * 128;
+    p.tx_bytes = p.stage_bytes;
+    p.idesc = mxw ? idesc_mxf8(kBM, BN, 0) : idesc_bf16(kBM, BN, 0, 0);
+    p.ksb = (int)(a.K / 32);
+    p.bias = static_cast<const uint16_t*>(a.bias);
+    p.cos_tab = a.cos_tab;
+    p.sin_tab = a.sin_tab;
+    p.pos = a.pos;
+    p.cs_rows = a.cs_rows;
+    p.cs_width = a.cs_width;
+    p.q_out = static_cast<uint8_t*>(a.q_out);
+    p.q_scales = a.q_scales;
+    p.x_scales = a.x_scales;
+    p.w_scales = a.w_scales;
+    p.status = a.status;
+
+    const size_t fixed = 1024 /* alignment slack */ + 256 /* barriers + slots */;
+    const size_t per_stage = p.stage_bytes + (mxw ? kSfBytesPerStage : 0);
+    int stages = (int)((size_t)(di.max_smem_optin - fixed) / per_stage);
+    if (stages > 8) stages = 8;
+    if (stages < 2) return MLA_ERR_UNSUPPORTED;
+    if (mxw && kSfCol0 + kSfColsPerStage * (uint32_t)stages > kTmemCols) stages = (kTmemCols - kSfCol0) / kSfColsPerStage;
+    p.stages = stages;
+    const size_t smem = fixed + (size_t)stages * per_stage;
+
+    alignas(64) CUtensorMap ta, tb;
+    st = make_tmap_2d(&ta, a.x, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)a.T,
+                      (uint64_t)a.K * (mxw ? 1 : 2), 128 / (mxw ? 1 : 2), kBM, true);
+    if (st != MLA_OK) return st;
+    st = make_tmap_2d(&tb, a.W, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * (mxw ? 1 : 2),
+                      128 / (mxw ? 1 : 2), (uint32_t)BN, true);
+    if (st != MLA_OK) return st;
+
+    int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
+    const bool mxo = a.out_mode == MLA_OUT_MXFP8;
+    if (mxw)
+        return mxo ? launch_dr<true, true>(a.Dr, ta, tb, p, grid, smem, stream)
+                   : launch_dr<true, false>(a.Dr, ta, tb, p, grid, smem, stream);
+    return mxo ? launch_dr<false, true>(a.Dr, ta, tb, p, grid, smem, stream)
+               : launch_dr<false, false>(a.Dr, ta, tb, p, grid, smem, stream);
+}
+
+}  // namespace mlaq

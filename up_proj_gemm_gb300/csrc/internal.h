@@ -1,0 +1,74 @@
+// Declarations shared by the translation units of libmlaq.so (host side).
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mlaq.h"
+
+namespace mlaq {
+
+// Device properties of the current device, cached per device.
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+int current_device_info(DeviceInfo* out);  // returns an mla status
+
+// cuTensorMapEncodeTiled, resolved through the runtime's driver entry point.
+// 2-D, row-major tensor: dims {inner, outer}, row pitch in bytes, box
+// {box_inner, box_outer}, 128-byte swizzle when swizzle128 else none.
+// dtype: 0 = uint8, 1 = bf16.
+int make_tmap_2d(void* tmap_out /* CUtensorMap, 64 B aligned */, const void* base, int dtype,
+                 uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner,
+                 uint32_t box_outer, bool swizzle128);
+
+// ------------------------------------------------------------- launchers
+// All launchers assume arguments were validated by the API layer.
+int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                          uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+
+struct FwdArgs {
+    int64_t T, K;
+    int H, Dn, Dr;
+    int64_t cs_rows, cs_width;
+    int weight_mode, out_mode;
+    const void* x;
+    const uint8_t* x_scales;
+    const void* W;
+    const uint8_t* w_scales;
+    const void* bias;
+    const float* cos_tab;
+    const float* sin_tab;
+    const int32_t* pos;
+    void* q_out;
+    uint8_t* q_scales;
+    int* status;
+};
+int launch_fwd(const FwdArgs& a, cudaStream_t stream);
+
+struct BwdArgs {
+    int64_t T, K;
+    int H, Dn, Dr;
+    int64_t cs_rows, cs_width;
+    const void* dq;
+    const void* W;   // dgrad
+    const void* x;   // wgrad
+    const float* cos_tab;
+    const float* sin_tab;
+    const int32_t* pos;
+    void* dx;        // dgrad
+    void* dW;        // wgrad
+    void* db;        // wgrad, nullable
+    int* status;
+};
+int launch_dgrad(const BwdArgs& a, cudaStream_t stream);
+int launch_wgrad(const BwdArgs& a, cudaStream_t stream);
+
+// Tile width (channels) of the forward kernel for this shape, or 0 when no
+// width in [16, 256] keeps every rope region and MXFP8 block inside one tile.
+int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn);
+
+}  // namespace mlaq

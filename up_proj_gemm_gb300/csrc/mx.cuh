@@ -1,0 +1,103 @@
+// MXFP8 (E4M3 elements, E8M0 block scales) encoding on fp32 registers.
+//
+// Scale rule: the exponent of a 32-element block is the smallest integer e
+// with amax <= 448 * 2^e, clamped to [-127, 127], stored as the byte e + 127;
+// elements are v * 2^-e rounded to nearest-even E4M3 with saturation (the
+// hardware cvt.rn.satfinite). A block holding NaN or Inf gets scale 0xFF and
+// NaN codes (0x7F with each element's sign).
+#pragma once
+#include <cstdint>
+
+namespace mlaq {
+
+// Exponent from the bits of a non-negative finite fp32 amax:
+// amax = 1.m * 2^E with 448 = 1.75 * 2^8, so amax <= 448 * 2^(E-8) exactly
+// when the 23-bit mantissa field is <= 0x600000 (1.75), else one more.
+// Zero and fp32 subnormals (< 2^-126 < 448 * 2^-127) clamp to -127.
+__device__ __forceinline__ int e8m0_exponent_f32(float amax) {
+    const uint32_t bits = __float_as_uint(amax);
+    const int be = (int)((bits >> 23) & 0xFFu);
+    if (be == 0) return -127;
+    int e = (be - 127) - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    e = e < -127 ? -127 : e;
+    e = e > 127 ? 127 : e;
+    return e;
+}
+
+// 2^-e as an fp32 (e in [-127, 120] for finite fp32 amax: always a normal).
+__device__ __forceinline__ float exp2_neg(int e) {
+    return __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
+// Two fp32 -> two E4M3 bytes (lo in bits 0..7, hi in bits 8..15), RNE, saturating.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    return cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);
+}
+
+__device__ __forceinline__ bool not_finite(float v) {
+    return (__float_as_uint(v) & 0x7F800000u) == 0x7F800000u;
+}
+
+// NaN code keeping the element's sign.
+__device__ __forceinline__ uint32_t nan_code(float v) {
+    return 0x7Fu | ((__float_as_uint(v) >> 24) & 0x80u);
+}
+
+// Round two fp32 to bf16 (RNE) and pack (lo in bits 0..15).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) {
+    return __uint_as_float(packed & 0xFFFF0000u);
+}
+
+// Quantize n <= 32 fp32 values held by ONE thread (a whole block) into codes
+// (packed little-endian, 4 per word) and return the scale byte. Entries past
+// n are ignored for the amax and encoded anyway (callers do not store them).
+template <int NV>
+__device__ __forceinline__ uint32_t quantize_block_regs(const float (&v)[NV], int n,
+                                                        uint32_t (&codes)[(NV + 3) / 4]) {
+    float amax = 0.f;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        if (i < n) {
+            bad |= not_finite(v[i]);
+            amax = fmaxf(amax, fabsf(v[i]));
+        }
+    }
+    if (bad) {
+#pragma unroll
+        for (int w = 0; w < (NV + 3) / 4; ++w) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (4 * w + j < NV) c |= nan_code(v[4 * w + j]) << (8 * j);
+            codes[w] = c;
+        }
+        return 0xFFu;
+    }
+    const int e = e8m0_exponent_f32(amax);
+    const float s = exp2_neg(e);
+#pragma unroll
+    for (int w = 0; w < (NV + 3) / 4; ++w) {
+        float a = v[4 * w] * s;
+        float b = (4 * w + 1 < NV) ? v[4 * w + 1] * s : 0.f;
+        float c = (4 * w + 2 < NV) ? v[4 * w + 2] * s : 0.f;
+        float d = (4 * w + 3 < NV) ? v[4 * w + 3] * s : 0.f;
+        codes[w] = pack_e4m3x4(a, b, c, d);
+    }
+    return (uint32_t)(e + 127);
+}
+
+}  // namespace mlaq
