@@ -1,0 +1,548 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused MLA query up-projection on GB300.
+
+One step = one training pass of the layer at the DeepSeek-V3 query
+up-projection shape (T=4096 tokens, q_lora_rank K=1536, H=128 heads of
+Dn=128 + Dr=64, N=24576): the fused forward (bf16 weights, GEMM + bias +
+RoPE + MXFP8 output), then dgrad (inverse RoPE fused, dx) and wgrad (dW and
+db). Work per step = 6 T K N FLOP (2 TKN forward, 4 TKN backward).
+
+    python bench.py --gpus N --steps K --warmup W [--impl reference]
+
+Prints ONE JSON line (rank 0). ``value`` is TFLOP/s of the whole job with
+inputs resident in HBM (CUDA events on the launch stream, L2 flushed by a
+256 MiB write between steps, outside the events). ``e2e`` is the same
+metric through the C ABI with pinned host buffers: per step the inputs (x,
+dq) go host->device and every output (q codes + scales, dx, dW, db) comes
+back. ``parts`` times each kernel and the other rows of the path (MXFP8
+weights, the standalone quantizer, the backward at T=8192, the long-context
+workload). ``cpu_baseline`` is the fp64 oracle on this host's cores over a
+bounded token sample. Under torchrun, every rank runs its own replica (the
+op does not exchange data); rank 0 prints.
+
+``--impl reference`` times the fp64 CPU oracle on the same workload (a
+bounded token sample per step, rank 0 only) and prints its line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused Q-uproj fwd/bwd TFLOP/s and % of GB300 BF16/FP8 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+# --------------------------------------------------------------------- utils
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(values, world):
+    """Element-wise max over ranks (gloo on CPU; identity for one process)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(step_ms_per_rank_max, flop_per_step, world):
+    """Whole-job throughput: all ranks' work over the slowest rank's time."""
+    return world * flop_per_step / (step_ms_per_rank_max * 1e-3) / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 20):
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", str(period_ms), "-i", gpu_id]
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self, busy_from_mhz: float = 0.0):
+        rows = []
+        for ln in self.out.strip().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[4:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r[0] > busy_from_mhz] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i in range(4) if r[2][i + 1].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+def gpu_id_for(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in vis.split(",") if v.strip()]
+    if ids and local_rank < len(ids):
+        return ids[local_rank]
+    return str(local_rank)
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for name in ("fwd.cu", "bwd.cu", "quantize.cu", "ptx.cuh", "mx.cuh"):
+        with open(os.path.join(ROOT, "up_proj_gemm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernels as they are now (same source hash); else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        if d.get("kernel_hash") != kernel_hash():
+            return None
+        return d["per_launch_bytes"].get(kernel)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- workload
+def shapes():
+    import synth
+    return synth.workload("dsv3_fwd_bf16w", bias=True, passes=("fwd", "bwd"))
+
+
+def make_device_inputs(w, dev, seed=0):
+    """Seeded synthetic inputs drawn on the device (same distributions as the
+    CPU generators the parity tests use): x ~ N(0,1), W ~ N(0,0.02),
+    b ~ N(0,1), dq ~ N(0,0.01), all rounded to bf16; standard RoPE table."""
+    import torch
+    import synth
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def nrm(shape, std):
+        return (torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * std).to(torch.bfloat16)
+
+    x = nrm((w.T, w.K), w.x_std)
+    if w.outlier_frac > 0:
+        pick = torch.rand((w.T, w.K), generator=g, device=dev) < w.outlier_frac
+        x = torch.where(pick, (x.float() * w.outlier_mult).to(torch.bfloat16), x)
+    cos, sin = synth.make_tables(w)
+    return {
+        "x": x, "W": nrm((w.N, w.K), w.w_std), "b": nrm((w.N,), w.b_std) if w.bias else None,
+        "dq": nrm((w.T, w.H, w.D), w.dq_std), "cos": cos.to(dev), "sin": sin.to(dev),
+        "pos": synth.positions(w.T, w.seq_len).to(dev),
+    }
+
+
+def time_loop(fn, iters, flush, stream, warmup=3):
+    """Mean ms per call: CUDA events on `stream` around each call, the L2
+    flush between calls outside the events."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+    torch.cuda.synchronize()
+    for i in range(iters):
+        flush()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import up_proj_gemm_gb300 as mlaq
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    mlaq.lib()  # fails loudly without the CUDA library
+    stream = torch.cuda.current_stream(dev)
+    w = shapes()
+    inp = make_device_inputs(w, dev, seed=rank)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    q_codes = torch.empty((w.T, w.H, w.D), dtype=torch.uint8, device=dev)
+    q_scales = torch.empty((w.T, w.H, (w.D + 31) // 32), dtype=torch.uint8, device=dev)
+    dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
+    db = torch.empty((w.N,), dtype=torch.bfloat16, device=dev)
+
+    def k_fwd():
+        mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"],
+                 pos=inp["pos"], out_mode="mxfp8", q_out=q_codes, q_scales=q_scales, status=status)
+
+    def k_dgrad():
+        mlaq.bwd_dgrad(inp["dq"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                       dx=dx, status=status)
+
+    def k_wgrad():
+        mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                       dW=dW, db=db, status=status)
+
+    def step():
+        k_fwd()
+        k_dgrad()
+        k_wgrad()
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    mlaq.check_status(status, "warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    with ClockSampler(gpu_id_for(local)) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            k_fwd()
+            ev[i][1].record(stream)
+            k_dgrad()
+            ev[i][2].record(stream)
+            k_wgrad()
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    mlaq.check_status(status, "timed steps")
+    per = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(3)]
+    mean_k = [statistics.mean(p) for p in per]
+    step_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in ev)
+    step_ms_max = reduce_max([step_ms], world)[0]
+    flop_step = w.fwd_flop() + w.bwd_flop()
+    value = aggregate(step_ms_max, flop_step, world)
+    clocks = clk.summary(busy_from_mhz=500.0)
+
+    pk, pk_src = peaks()
+    names = ["fwd_bf16w_mxfp8out", "dgrad", "wgrad_db"]
+    flops = [w.fwd_flop(), w.bwd_flop() / 2, w.bwd_flop() / 2]
+    dom = max(range(3), key=lambda j: mean_k[j])
+    peak = pk["bf16_tflops_sustained"]
+    achieved = flops[dom] / (mean_k[dom] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": names[dom], "achieved": round(achieved, 1),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic_for(names[dom]),
+                "peak_source": f"{pk_src} bf16_tflops_sustained (cuBLAS bf16, seconds-long loop)",
+                "algorithmic_flop_per_launch": flops[dom]}
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded device-side draws, DeepSeek-V3 shapes; no datasets or weights)",
+        "config": {"workload": "dsv3_q_uproj_train_step: fwd(bf16 W, +bias, RoPE, MXFP8 q) + dgrad + "
+                               "wgrad + db", "T": w.T, "K": w.K, "H": w.H, "Dn": w.Dn, "Dr": w.Dr,
+                   "N": w.N, "pos": "t", "rope_table": "standard base 1e4",
+                   "l2": "flushed (256 MiB write) between steps, outside the timed events",
+                   "parallelism": f"replicas x{world} (no data exchange)"},
+        "roofline": roofline,
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "kernels_ms": {n: round(m, 4) for n, m in zip(names, mean_k)},
+        "kernels_tflops": {n: round(f / (m * 1e-3) / 1e12, 1) for n, f, m in zip(names, flops, mean_k)},
+    }
+
+    # ---------------------------------------------------------------- e2e
+    e2e_steps = max(3, min(args.e2e_steps, K))
+    hx = inp["x"].cpu().pin_memory()
+    hdq = inp["dq"].cpu().pin_memory()
+    hq = torch.empty(q_codes.shape, dtype=torch.uint8).pin_memory()
+    hs = torch.empty(q_scales.shape, dtype=torch.uint8).pin_memory()
+    hdx = torch.empty(dx.shape, dtype=torch.bfloat16).pin_memory()
+    hdW = torch.empty(dW.shape, dtype=torch.bfloat16).pin_memory()
+    hdb = torch.empty(db.shape, dtype=torch.bfloat16).pin_memory()
+    dxin = torch.empty_like(inp["x"])
+    ddq = torch.empty_like(inp["dq"])
+
+    def e2e_step():
+        dxin.copy_(hx, non_blocking=True)
+        ddq.copy_(hdq, non_blocking=True)
+        mlaq.fwd(dxin, inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"], pos=inp["pos"],
+                 out_mode="mxfp8", q_out=q_codes, q_scales=q_scales, status=status)
+        mlaq.bwd_dgrad(ddq, inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], dx=dx,
+                       status=status)
+        mlaq.bwd_wgrad(ddq, dxin, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], dW=dW, db=db,
+                       status=status)
+        hq.copy_(q_codes, non_blocking=True)
+        hs.copy_(q_scales, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hdW.copy_(dW, non_blocking=True)
+        hdb.copy_(db, non_blocking=True)
+
+    e2e_ms = time_loop(e2e_step, e2e_steps, flush, stream)
+    e2e_ms = reduce_max([e2e_ms], world)[0]
+    mlaq.check_status(status, "e2e steps")
+    h2d = hx.numel() * 2 + hdq.numel() * 2
+    d2h = hq.numel() + hs.numel() + hdx.numel() * 2 + hdW.numel() * 2 + hdb.numel() * 2
+    out["e2e"] = {"value": round(aggregate(e2e_ms, flop_step, world), 2), "unit": "TFLOP/s",
+                  "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "steps": e2e_steps}
+    del hx, hdq, hq, hs, hdx, hdW, hdb, dxin, ddq
+
+    if rank == 0 and not args.no_parts:
+        out["parts"] = run_parts(dev, stream, flush, pk, pk_src)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_parts(dev, stream, flush, pk, pk_src):
+    """The other rows of the path, each timed on its own (CUDA events, L2
+    flushed between calls): MXFP8 weights, the quantizer, the backward at
+    T=8192 and the long-context workload."""
+    import torch
+    import synth
+    import up_proj_gemm_gb300 as mlaq
+    parts = {}
+    bf16_peak = pk["bf16_tflops"]  # kernels timed alone: burst figure
+    fp8_peak = bf16_peak * FP8_OVER_BF16
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # standalone quantizer, [4096, 24576] bf16 and [24576, 1536] bf16 (W)
+    for R, C in ((4096, 24576), (24576, 1536), (16384, 24576)):
+        a = torch.randn((R, C), device=dev, dtype=torch.float32).to(torch.bfloat16)
+        codes = torch.empty((R, C), dtype=torch.uint8, device=dev)
+        sc = torch.empty((R, (C + 31) // 32), dtype=torch.uint8, device=dev)
+        ms = time_loop(lambda: mlaq.mxfp8_quantize_rows(a, codes, sc), 20, flush, stream)
+        byts = R * C * 2 + R * C + R * ((C + 31) // 32)
+        gbs = byts / (ms * 1e-3) / 1e9
+        parts[f"quantize_rows_bf16_{R}x{C}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                                "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                                                "algorithmic_bytes": byts}
+        del a, codes, sc
+
+    # forward with MXFP8 weights (x with 1% x50 outliers), MXFP8 out
+    w = synth.workload("dsv3_fwd_mxfp8w")
+    inp = make_device_inputs(w, dev, seed=11)
+    xq, xs = mlaq.mxfp8_quantize_rows(inp["x"])
+    Wq, Ws = mlaq.mxfp8_quantize_rows(inp["W"])
+    qc = torch.empty((w.T, w.H, w.D), dtype=torch.uint8, device=dev)
+    qs = torch.empty((w.T, w.H, (w.D + 31) // 32), dtype=torch.uint8, device=dev)
+    ms = time_loop(lambda: mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                                    weight_mode="mxfp8", out_mode="mxfp8", x_scales=xs, w_scales=Ws,
+                                    q_out=qc, q_scales=qs, status=st), 30, flush, stream)
+    tf = w.fwd_flop() / (ms * 1e-3) / 1e12
+    parts["fwd_mxfp8w_mxfp8out_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                                          "frac_fp8_peak": round(tf / fp8_peak, 4),
+                                          "peak": f"{pk_src} bf16 burst x{FP8_OVER_BF16:g} (nominal fp8/bf16)"}
+    ms = time_loop(lambda: mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
+                                    pos=inp["pos"], out_mode="mxfp8", q_out=qc, q_scales=qs, status=st),
+                   30, flush, stream)
+    tf = w.fwd_flop() / (ms * 1e-3) / 1e12
+    parts["fwd_bf16w_mxfp8out_T4096_alone"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                                               "frac_bf16_peak": round(tf / bf16_peak, 4)}
+    del inp, xq, xs, Wq, Ws, qc, qs
+
+    # backward at T = 2 x 4096, bias on
+    w = synth.workload("dsv3_bwd")
+    inp = make_device_inputs(w, dev, seed=12)
+    dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
+    db = torch.empty((w.N,), dtype=torch.bfloat16, device=dev)
+    ms_d = time_loop(lambda: mlaq.bwd_dgrad(inp["dq"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
+                                            pos=inp["pos"], dx=dx, status=st), 20, flush, stream)
+    ms_w = time_loop(lambda: mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
+                                            pos=inp["pos"], dW=dW, db=db, status=st), 20, flush, stream)
+    half = w.bwd_flop() / 2
+    parts["bwd_T8192"] = {"dgrad_ms": round(ms_d, 4), "wgrad_db_ms": round(ms_w, 4),
+                          "TFLOP/s": round(w.bwd_flop() / ((ms_d + ms_w) * 1e-3) / 1e12, 1),
+                          "dgrad_TFLOP/s": round(half / (ms_d * 1e-3) / 1e12, 1),
+                          "wgrad_TFLOP/s": round(half / (ms_w * 1e-3) / 1e12, 1),
+                          "frac_bf16_peak": round(w.bwd_flop() / ((ms_d + ms_w) * 1e-3) / 1e12 / bf16_peak, 4)}
+    del inp, dx, dW, db
+
+    # long context: T = 4 x 4096, YaRN table, MXFP8 out, fwd + bwd
+    w = synth.workload("dsv3_long_yarn")
+    inp = make_device_inputs(w, dev, seed=13)
+    qc = torch.empty((w.T, w.H, w.D), dtype=torch.uint8, device=dev)
+    qs = torch.empty((w.T, w.H, (w.D + 31) // 32), dtype=torch.uint8, device=dev)
+    dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
+
+    def long_step():
+        mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                 out_mode="mxfp8", q_out=qc, q_scales=qs, status=st)
+        mlaq.bwd_dgrad(inp["dq"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                       dx=dx, status=st)
+        mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                       dW=dW, db=None, status=st)
+
+    ms = time_loop(long_step, 10, flush, stream)
+    tf = (w.fwd_flop() + w.bwd_flop()) / (ms * 1e-3) / 1e12
+    parts["long_yarn_T16384_fwd_bwd"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                                         "frac_bf16_peak": round(tf / bf16_peak, 4)}
+    del inp, qc, qs, dx, dW
+    torch.cuda.synchronize()
+    mlaq.check_status(st, "parts")
+    parts["peak_note"] = f"{pk_src} peaks; kernels timed alone use the burst bf16 figure"
+    return parts
+
+
+# -------------------------------------------------- CPU oracle (baseline)
+def oracle_step_sample(w, tokens, inputs):
+    """The oracle on a token sample of the step: forward (linear, bias, RoPE,
+    MXFP8), RoPE backward, dgrad, and the sample's share of wgrad and bgrad.
+    Returns seconds; the work is 6 * tokens * K * N FLOP."""
+    import numpy as np
+    import oracle
+    x, W, b, dq, cos, sin, pos = inputs
+    t0 = time.perf_counter()
+    oracle.forward(x[:tokens], W, w.H, w.Dn, w.Dr, cos, sin, pos[:tokens], b, quantize=True)
+    oracle.backward(dq[:tokens], x[:tokens], W, w.H, w.Dn, w.Dr, cos, sin, pos[:tokens])
+    return time.perf_counter() - t0
+
+
+def oracle_inputs(w, tokens):
+    import numpy as np
+    import oracle
+    import synth
+    sub = synth.workload(w.name, T=tokens, bias=w.bias, seq_len=w.seq_len)
+    inp = synth.make_inputs(sub, seed=0)
+    cos, sin = synth.make_tables(w)
+    f = lambda t: oracle.decode_bf16(synth.bf16_bits(t))
+    return (f(inp["x"]), f(inp["W"]), f(inp["b"]) if inp["b"] is not None else None, f(inp["dq"]),
+            cos.numpy(), sin.numpy(), synth.positions(tokens, w.seq_len).numpy())
+
+
+def cpu_baseline(w, budget_s=15.0):
+    import oracle
+    probe = 8
+    t = oracle_step_sample(w, probe, oracle_inputs(w, probe))
+    tokens = int(max(probe, min(2048, probe * budget_s / max(t, 1e-6))))
+    if tokens > probe:
+        t = oracle_step_sample(w, tokens, oracle_inputs(w, tokens))
+    flop = 6.0 * tokens * w.K * w.N
+    return {"value": round(flop / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(t, 3),
+            "sample": f"{tokens} of {w.T} tokens of the step (fwd + MXFP8, RoPE bwd, dgrad, the sample's "
+                      f"wgrad/bgrad share), fp64, OpenMP over rows"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = shapes()
+    inputs = oracle_inputs(w, 64)
+    per_step_budget = max(0.05, args.ref_budget / max(1, args.steps + args.warmup))
+    t = oracle_step_sample(w, 1, inputs)
+    tokens = int(max(1, min(64, per_step_budget / max(t, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_step_sample(w, tokens, inputs)
+    times = [oracle_step_sample(w, tokens, inputs) for _ in range(args.steps)]
+    ms = statistics.mean(times) * 1e3
+    value = 6.0 * tokens * w.K * w.N / (ms * 1e-3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "dsv3_q_uproj_train_step (token sample per step)",
+                                        "T": w.T, "K": w.K, "H": w.H, "Dn": w.Dn, "Dr": w.Dr,
+                                        "tokens_per_step": tokens},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": f"{tokens} of {w.T} tokens per step"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-parts", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds for --impl reference")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

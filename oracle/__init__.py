@@ -69,6 +69,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB_PATH)
             sig = {
+                "oracle_num_threads": (ctypes.c_int, []),
                 "oracle_bf16_to_f64": (ctypes.c_double, [ctypes.c_uint16]),
                 "oracle_decode_bf16": (None, [_i64, _u16, _d]),
                 "oracle_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
@@ -102,6 +103,11 @@ def _ptr(a, ctype):
 
 def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle's row-parallel loops use."""
+    return int(_load().oracle_num_threads())
 
 
 # ----------------------------------------------------------------- scalars

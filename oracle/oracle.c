@@ -38,11 +38,24 @@
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG 1
 #define ORACLE_ERR_ROPE_WIDTH 2
 #define ORACLE_ERR_POS_RANGE 8
+
+/* Threads the parallel loops below use (1 without OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------ decode */
 

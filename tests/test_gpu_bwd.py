@@ -1,0 +1,166 @@
+"""GPU parity of the backward: inverse RoPE fused into dgrad and wgrad, plus db.
+
+TransformerEngine PR "Add a backwards linear function to be used with the
+fused mla q up-proj": sequence diagram (RoPE backward, then the linear
+backward with the saved input and the weight) and the review comment "BF16
+bias gradient remains missing" (db must be produced). Megatron-LM PR "Fix
+fused MLA YaRN RoPE query kernel corrupting upstream tensor in-place",
+discussion: the wgrad must use the linear's saved input and may be delayed
+(a separate call). Tolerance: ||gpu - ref||_F / ||ref||_F <= 5e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers
+import oracle
+import synth
+import up_proj_gemm_gb300 as mlaq
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+
+SHAPES = [
+    ("tiny", {}),
+    ("tiny", dict(T=300, K=200, H=6)),                        # ragged tokens, K, channels
+    ("tiny", dict(T=1, K=8, H=1)),
+    ("tiny", dict(T=130, K=64, H=16, Dn=64, Dr=32)),
+    ("dsv3_bwd", dict(T=300, H=8, seq_len=None)),
+    ("dsv3_bwd", dict(T=260, K=1000, H=3, seq_len=128)),      # positions restart every 128
+    ("dsv3_long_yarn", dict(T=200, H=4, seq_len=None)),       # YaRN table
+]
+
+
+def _dev_inputs(w, seed, dev):
+    inp = synth.make_inputs(w, seed=seed)
+    return inp, helpers.to_dev(inp, dev)
+
+
+def _oracle_bwd(inp, w, **kw):
+    return oracle.backward(helpers.f64(inp["dq"]), helpers.f64(inp["x"]), helpers.f64(inp["W"]), w.H,
+                           w.Dn, w.Dr, inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy(), **kw)
+
+
+@pytest.mark.parametrize("name,ov", SHAPES)
+def test_bwd_matches_oracle(cuda_device, name, ov):
+    w = synth.workload(name, **ov)
+    inp, d = _dev_inputs(w, 0, cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    dx = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
+    dW, db = mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
+                            status=st)
+    mlaq.check_status(st)
+    g = _oracle_bwd(inp, w)
+    for name_, got in (("dx", dx), ("dW", dW), ("db", db)):
+        err = helpers.frob_rel(got, g[name_])
+        assert err <= TOL, f"{name_}: relative Frobenius error {err:.3e}"
+
+
+def test_bwd_at_identity_rotation_is_plain_gemm(cuda_device):
+    """pos = 0 (cos = 1, sin = 0): dq_pre = dq, so dx = dq W, dW = dq^T x, db = sum dq."""
+    w = synth.workload("tiny", T=200, H=8)
+    inp = synth.make_inputs(w, seed=3)
+    inp["pos"] = torch.zeros(w.T, dtype=torch.int32)
+    d = helpers.to_dev(inp, cuda_device)
+    dx = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"])
+    dW, db = mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"])
+    dq = helpers.f64(inp["dq"]).reshape(w.T, -1)
+    x, W = helpers.f64(inp["x"]), helpers.f64(inp["W"])
+    assert helpers.frob_rel(dx, dq @ W) <= TOL
+    assert helpers.frob_rel(dW, dq.T @ x) <= TOL
+    assert helpers.frob_rel(db, dq.sum(0)) <= TOL
+
+
+def test_wgrad_without_bias_and_inputs_unchanged(cuda_device):
+    w = synth.workload("tiny", T=190, H=5)
+    inp, d = _dev_inputs(w, 4, cuda_device)
+    before = {k: v.clone() for k, v in d.items() if isinstance(v, torch.Tensor)}
+    db_canary = torch.full((w.N,), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    dW, none = mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
+                              db=None)
+    mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"])
+    torch.cuda.synchronize()
+    assert none is None and (db_canary == 7.0).all()
+    for k, v in before.items():
+        assert torch.equal(d[k], v), k
+    g = _oracle_bwd(inp, w, want=("dW",))
+    assert helpers.frob_rel(dW, g["dW"]) <= TOL
+
+
+def test_wgrad_zero_tokens_gives_zero(cuda_device):
+    w = synth.workload("tiny", T=0)
+    d = helpers.to_dev(synth.make_inputs(synth.workload("tiny"), seed=5), cuda_device)
+    dq = torch.empty((0, w.H, w.D), dtype=torch.bfloat16, device=cuda_device)
+    x = torch.empty((0, w.K), dtype=torch.bfloat16, device=cuda_device)
+    dW = torch.full((w.N, w.K), 3.0, dtype=torch.bfloat16, device=cuda_device)
+    db = torch.full((w.N,), 3.0, dtype=torch.bfloat16, device=cuda_device)
+    mlaq.bwd_wgrad(dq, x, d["cos"], d["sin"], w.H, w.Dn, w.Dr, dW=dW, db=db)
+    torch.cuda.synchronize()
+    assert (dW == 0).all() and (db == 0).all()
+
+
+def test_bwd_canaries_untouched(cuda_device):
+    w = synth.workload("tiny", T=150, H=6)
+    inp, d = _dev_inputs(w, 6, cuda_device)
+    pad = 2048
+    dxb = torch.full((w.T * w.K + 2 * pad,), 9.0, dtype=torch.bfloat16, device=cuda_device)
+    dWb = torch.full((w.N * w.K + 2 * pad,), 9.0, dtype=torch.bfloat16, device=cuda_device)
+    dbb = torch.full((w.N + 2 * pad,), 9.0, dtype=torch.bfloat16, device=cuda_device)
+    mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
+                   dx=dxb[pad:pad + w.T * w.K].view(w.T, w.K))
+    mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
+                   dW=dWb[pad:pad + w.N * w.K].view(w.N, w.K), db=dbb[pad:pad + w.N])
+    torch.cuda.synchronize()
+    for buf, n in ((dxb, w.T * w.K), (dWb, w.N * w.K), (dbb, w.N)):
+        assert (buf[:pad] == 9.0).all() and (buf[pad + n:] == 9.0).all()
+
+
+def test_bwd_position_out_of_range_reports_status(cuda_device):
+    w = synth.workload("tiny", T=64)
+    inp = synth.make_inputs(w, seed=7)
+    inp["pos"] = inp["pos"].clone()
+    inp["pos"][5] = -1
+    d = helpers.to_dev(inp, cuda_device)
+    for which in ("dgrad", "wgrad"):
+        st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+        if which == "dgrad":
+            mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
+        else:
+            mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
+        assert int(st.item()) == mlaq.STATUS["MLA_ERR_POS_RANGE"], which
+
+
+def test_bwd_full_size_sampled(cuda_device):
+    """DeepSeek-V3 backward shape (T = 2 x 4096, pos = t mod 4096, K=1536,
+    H=128): dx on 32 sampled tokens, dW on 4 sampled heads, db on every channel."""
+    w = synth.workload("dsv3_bwd")
+    inp, d = _dev_inputs(w, 0, cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    dx = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
+    dW, db = mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
+                            status=st)
+    mlaq.check_status(st)
+    cos, sin, pos = inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy()
+    rng = np.random.default_rng(1)
+    W = helpers.f64(inp["W"])
+    # dx: sampled tokens (rows are independent)
+    toks = np.sort(rng.choice(w.T, 32, replace=False))
+    dq_t = helpers.f64(inp["dq"][torch.from_numpy(toks)])
+    dqp_t = oracle.rope_bwd(dq_t, w.H, w.Dn, w.Dr, cos, sin, pos[toks]).reshape(len(toks), -1)
+    ref_dx = oracle.dgrad(dqp_t, W)
+    assert helpers.frob_rel(dx[torch.from_numpy(toks).to(cuda_device)], ref_dx) <= TOL
+    # dW: sampled heads over all tokens (a head's channels only need that head's dq)
+    x = helpers.f64(inp["x"])
+    heads = np.array([0, 37, 64, 127])
+    dq_h = helpers.f64(inp["dq"][:, torch.from_numpy(heads)].contiguous())
+    dqp_h = oracle.rope_bwd(dq_h, len(heads), w.Dn, w.Dr, cos, sin, pos).reshape(w.T, -1)
+    ref_dW = oracle.wgrad(dqp_h, x)
+    ch = (heads[:, None] * w.D + np.arange(w.D)[None, :]).reshape(-1)
+    assert helpers.frob_rel(dW[torch.from_numpy(ch).to(cuda_device)], ref_dW) <= TOL
+    # db: every channel, 16 heads at a time
+    ref_db = np.empty(w.N)
+    for h0 in range(0, w.H, 16):
+        dq_c = helpers.f64(inp["dq"][:, h0:h0 + 16].contiguous())
+        dqp = oracle.rope_bwd(dq_c, 16, w.Dn, w.Dr, cos, sin, pos).reshape(w.T, -1)
+        ref_db[h0 * w.D:(h0 + 16) * w.D] = oracle.bgrad(dqp)
+    assert helpers.frob_rel(db, ref_db) <= TOL

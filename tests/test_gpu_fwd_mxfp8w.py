@@ -1,0 +1,92 @@
+"""GPU parity of the forward with MXFP8 weights (block-scaled tcgen05 MMA).
+
+TransformerEngine PR "Add support for fused Q Up-Proj GEMM/RoPE/Quant",
+description paragraph ("supports both 16-bit projection and mxfp8
+projection") and flowchart ("BF16 or MXFP8 weight"). x and W are quantized
+rowwise (1 x 32 blocks along K) by the library's quantizer; the oracle
+quantizes the same bf16 values itself and the two must agree byte for byte
+before the products are compared, so the oracle's operands never come from
+the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers
+import oracle
+import synth
+import up_proj_gemm_gb300 as mlaq
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    ("tiny", dict(T=300, K=512, H=8)),                        # BN 192 = 4 heads of 48
+    ("tiny", dict(T=77, K=256, H=6)),                         # BN 96 (2 heads), ragged tokens
+    ("dsv3_fwd_mxfp8w", dict(T=260, H=4)),                    # one head per 192-wide tile
+    ("dsv3_fwd_mxfp8w", dict(T=140, H=2, K=1024, bias=True)),
+]
+
+
+def _quantized_operands(inp, dev):
+    xs = inp["x"].to(dev)
+    Ws = inp["W"].to(dev)
+    xq, xsc = mlaq.mxfp8_quantize_rows(xs)
+    Wq, Wsc = mlaq.mxfp8_quantize_rows(Ws)
+    torch.cuda.synchronize()
+    # the oracle's own quantization of the same values
+    oxq, oxs = oracle.mxfp8_quantize(helpers.f64(inp["x"]))
+    oWq, oWs = oracle.mxfp8_quantize(helpers.f64(inp["W"]))
+    assert np.array_equal(xq.cpu().numpy(), oxq) and np.array_equal(xsc.cpu().numpy(), oxs)
+    assert np.array_equal(Wq.cpu().numpy(), oWq) and np.array_equal(Wsc.cpu().numpy(), oWs)
+    x_deq = oracle.mxfp8_dequantize(oxq, oxs)
+    W_deq = oracle.mxfp8_dequantize(oWq, oWs)
+    return (xq, xsc, Wq, Wsc), (x_deq, W_deq)
+
+
+def _oracle(inp, w, x_deq, W_deq, tokens=None, quantize=False):
+    b = helpers.f64(inp["b"]) if inp.get("b") is not None else None
+    pos = inp["pos"].numpy()
+    if tokens is not None:
+        x_deq, pos = x_deq[tokens], pos[tokens]
+    return oracle.forward(x_deq, W_deq, w.H, w.Dn, w.Dr, inp["cos"].numpy(), inp["sin"].numpy(), pos, b,
+                          quantize=quantize)
+
+
+@pytest.mark.parametrize("out_mode", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("name,ov", SHAPES)
+def test_fwd_mxfp8_weights(cuda_device, name, ov, out_mode):
+    w = synth.workload(name, **ov)
+    inp = synth.make_inputs(w, seed=2)
+    (xq, xsc, Wq, Wsc), (x_deq, W_deq) = _quantized_operands(inp, cuda_device)
+    d = helpers.to_dev(inp, cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    out = mlaq.fwd(xq, Wq, d["cos"], d["sin"], w.H, w.Dn, w.Dr, bias=d.get("b"), pos=d["pos"],
+                   weight_mode="mxfp8", out_mode=out_mode, x_scales=xsc, w_scales=Wsc, status=st)
+    mlaq.check_status(st)
+    if out_mode == "bf16":
+        helpers.check_bf16_close(out, _oracle(inp, w, x_deq, W_deq))
+    else:
+        q_ref, rc, rs = _oracle(inp, w, x_deq, W_deq, quantize=True)
+        helpers.check_mxfp8_close(out[0].cpu().numpy(), out[1].cpu().numpy(), q_ref, rc, rs)
+
+
+def test_fwd_mxfp8_weights_full_size_sampled(cuda_device):
+    """DeepSeek-V3 shape with 1% x50 activation outliers, MXFP8 x and W, MXFP8
+    out, in the benchmark's launch configuration; 32 sampled tokens."""
+    w = synth.workload("dsv3_fwd_mxfp8w")
+    inp = synth.make_inputs(w, seed=0)
+    (xq, xsc, Wq, Wsc), (x_deq, W_deq) = _quantized_operands(inp, cuda_device)
+    d = helpers.to_dev(inp, cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    codes, scales = mlaq.fwd(xq, Wq, d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
+                             weight_mode="mxfp8", out_mode="mxfp8", x_scales=xsc, w_scales=Wsc,
+                             status=st)
+    mlaq.check_status(st)
+    toks = np.sort(np.random.default_rng(3).choice(w.T, 32, replace=False))
+    q_ref, rc, rs = _oracle(inp, w, x_deq, W_deq, tokens=toks, quantize=True)
+    idx = torch.from_numpy(toks).to(cuda_device)
+    helpers.check_mxfp8_close(codes[idx].cpu().numpy(), scales[idx].cpu().numpy(), q_ref, rc, rs)
+    # context only: error of the quantized path against the unquantized bf16 operands
+    q_bf = helpers.oracle_forward(inp, w, tokens=toks)
+    rel = np.linalg.norm(q_ref - q_bf) / np.linalg.norm(q_bf)
+    assert rel < 0.1

@@ -183,7 +183,7 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
 
     if (!rope_dim_supported(s.Dr) || s.Dn % 32) return MLA_ERR_UNSUPPORTED;
     if (mxw && s.K % 128) return MLA_ERR_UNSUPPORTED;
-    if (fwd_tile_n(N, D, s.Dn, s.Dr, mxw ? 192 : 256) == 0) return MLA_ERR_UNSUPPORTED;
+    if (fwd_tile_n(N, D, s.Dn, s.Dr, mxw ? 192 : 256, mxw ? 32 : 16) == 0) return MLA_ERR_UNSUPPORTED;
 
     const int64_t esz = mxw ? 1 : 2;
     if ((s.K * esz) % 16) return MLA_ERR_ALIGNMENT;

@@ -1,7 +1,511 @@
-// Backward kernels (dgrad, wgrad + bias gradient): placeholder until written.
+// Backward of the fused MLA query up-projection on sm_103a tensor cores.
+//
+// TransformerEngine PR "Add a backwards linear function to be used with the
+// fused mla q up-proj": the query gradient first goes through the RoPE
+// backward (dq_pre = J^T dq), then the linear backward gives
+//   dgrad  dx[T, K] = dq_pre[T, N] W[N, K]
+//   wgrad  dW[N, K] = dq_pre[T, N]^T x[T, K]       (the saved input x)
+//   bgrad  db[N]    = sum_t dq_pre[t, N]          (review: "BF16 bias gradient
+//                                                   remains missing")
+// The pages run the RoPE backward as its own Triton kernel and hand dq_pre
+// to a library GEMM. Here dq_pre never exists in memory: dq tiles land in
+// shared memory by TMA, four "transform" warps rotate the rope channels of
+// each tile in place (fp32 math, rounded to bf16, the MMA operand type),
+// fence them into the async proxy and release the stage to the MMA thread.
+//
+// Warp roles (320 threads, persistent, one CTA per SM):
+//   warp 0     TMA producer (S-stage ring, 128-byte swizzle)
+//   warp 1     single-thread tcgen05.mma issuer, double-buffered TMEM acc
+//   warps 2-5  epilogue: TMEM -> bf16 -> global (16-byte stores)
+//   warps 6-9  transform: inverse RoPE in shared memory; for wgrad also the
+//              per-channel token sums that make db (tiles of the first K
+//              block only), deterministic, no atomics
+//
+// Operand layouts (D = A B^T in tcgen05 terms, M = 128 rows):
+//   dgrad: A = dq   [T x N] K-major (tokens x channels), B = W [N x K]
+//          MN-major (K contiguous); reduction over channels, 64 per stage.
+//   wgrad: A = dq^T MN-major (channels contiguous), B = x [T x K] MN-major;
+//          reduction over tokens, 64 per stage.
+// In both, a shared-memory "row" is 128 bytes = 64 consecutive channels of
+// one token, which is what the transform rewrites.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
 #include "internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
 
 namespace mlaq {
-int launch_dgrad(const BwdArgs&, cudaStream_t) { return MLA_ERR_UNSUPPORTED; }
-int launch_wgrad(const BwdArgs&, cudaStream_t) { return MLA_ERR_UNSUPPORTED; }
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 320;
+constexpr int kXformThreads = 128;
+constexpr int kXformWarp0 = 6;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccStride = 256;
+constexpr uint32_t kChunkBytes = 64 * 128;  // one 64-wide MN chunk x 64 K rows
+
+struct BwdParams {
+    int T, K, N, D, Dn;
+    int BN;
+    int num_m_tiles, num_n_tiles, num_tiles, k_tiles;
+    int stages;
+    uint32_t a_bytes, stage_bytes, tx_bytes;
+    uint32_t idesc;
+    const int32_t* pos;
+    const float* cos_tab;
+    const float* sin_tab;
+    long long cs_rows, cs_width;
+    int cs_vec;  // cos/sin rows 16-byte aligned: float4 loads
+    uint16_t* out;
+    int out_rows, out_cols;
+    uint16_t* db;
+    int* status;
+};
+
+struct Smem {
+    uint32_t base, bars;
+    int S;
+    __device__ uint32_t a(int s, const BwdParams& p) const { return base + (uint32_t)s * p.stage_bytes; }
+    __device__ uint32_t b(int s, const BwdParams& p) const { return a(s, p) + p.a_bytes; }
+    __device__ uint32_t full(int s) const { return bars + 8u * s; }
+    __device__ uint32_t ready(int s) const { return bars + 8u * (S + s); }
+    __device__ uint32_t empty(int s) const { return bars + 8u * (2 * S + s); }
+    __device__ uint32_t tfull(int b) const { return bars + 8u * (3 * S + b); }
+    __device__ uint32_t tempty(int b) const { return bars + 8u * (3 * S + 2 + b); }
+    __device__ uint32_t drain() const { return bars + 8u * (3 * S + 4); }
+};
+
+__device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&v)[4]) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, const uint32_t (&v)[4]) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                 "r"(v[3])
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void load8(const float* p, bool vec, float (&v)[8]) {
+    if (vec) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __ldg(p + e);
+    }
+}
+
+// Inverse RoPE, in place, on one 128-byte swizzled shared-memory row holding
+// channels [n0, n0 + 64) of token t (row index r inside its 1024-byte
+// swizzle atom group gives the XOR). With g = dq[Dn + .] of a head:
+//   out[i]      =  g[i] cos[p, i] + g[i+h] sin[p, i+h]
+//   out[i + h]  = -g[i] sin[p, i] + g[i+h] cos[p, i+h]      (h = Dr / 2)
+// Rope regions are Dr-aligned and Dr <= 64 divides 64, so both halves of a
+// pair lie in the same row; pairs are handled 8 at a time (16 bytes).
+template <int DR>
+__device__ __forceinline__ bool inverse_rope_row(const BwdParams& p, uint32_t row_addr, int r,
+                                                 int64_t n0, int64_t t) {
+    constexpr int HH = DR / 2;
+    int prow = -1;
+    bool wrote = false;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int64_t n = n0 + 8 * q;
+        if (n >= p.N) break;
+        const int c0 = (int)(n % p.D);
+        if (c0 < p.Dn || c0 - p.Dn >= HH) continue;
+        if (prow < 0) {
+            const int64_t pp = p.pos ? (int64_t)__ldg(p.pos + t) : t;
+            if (pp < 0 || pp >= p.cs_rows) {
+                record_status(p.status, MLA_ERR_POS_RANGE);
+                return wrote;
+            }
+            prow = (int)pp;
+        }
+        const int i0 = c0 - p.Dn;
+        const int q2 = q + HH / 8;
+        const uint32_t a1 = row_addr + (uint32_t)((q ^ (r & 7)) * 16);
+        const uint32_t a2 = row_addr + (uint32_t)((q2 ^ (r & 7)) * 16);
+        uint32_t g1[4], g2[4];
+        lds_v4(a1, g1);
+        lds_v4(a2, g2);
+        const float* crow = p.cos_tab + (int64_t)prow * p.cs_width;
+        const float* srow = p.sin_tab + (int64_t)prow * p.cs_width;
+        float ci[8], si[8], cj[8], sj[8];
+        load8(crow + i0, p.cs_vec, ci);
+        load8(srow + i0, p.cs_vec, si);
+        load8(crow + i0 + HH, p.cs_vec, cj);
+        load8(srow + i0 + HH, p.cs_vec, sj);
+        uint32_t o1[4], o2[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float gi0 = bf16lo_to_f32(g1[w]), gi1 = bf16hi_to_f32(g1[w]);
+            const float gj0 = bf16lo_to_f32(g2[w]), gj1 = bf16hi_to_f32(g2[w]);
+            const int e0 = 2 * w, e1 = 2 * w + 1;
+            o1[w] = pack_bf16x2(gi0 * ci[e0] + gj0 * sj[e0], gi1 * ci[e1] + gj1 * sj[e1]);
+            o2[w] = pack_bf16x2(-gi0 * si[e0] + gj0 * cj[e0], -gi1 * si[e1] + gj1 * cj[e1]);
+        }
+        sts_v4(a1, o1);
+        sts_v4(a2, o2);
+        wrote = true;
+    }
+    return wrote;
+}
+
+template <bool WG, int DR>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    Smem sm;
+    sm.S = p.stages;
+    sm.base = (raw + 1023u) & ~1023u;
+    sm.bars = sm.base + (uint32_t)p.stages * p.stage_bytes;
+    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (3 * p.stages + 5);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
+    float* db_part = reinterpret_cast<float*>(tail + 16);  // 128 floats (wgrad bias sums)
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(sm.full(s), 1);
+            mbar_init(sm.ready(s), kXformThreads / 32);
+            mbar_init(sm.empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sm.tfull(b), 1);
+            mbar_init(sm.tempty(b), 4);
+        }
+        mbar_init(sm.drain(), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32((const void*)tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nb_chunks = p.BN / 64;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t issued_mask = 0, issued_par = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            const int mt = tile / p.num_n_tiles;
+            const int nt = tile % p.num_n_tiles;
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t fb = sm.full(s);
+                    mbar_arrive_expect_tx(fb, p.tx_bytes);
+                    if (!WG) {
+                        // A: dq rows [mt*128, +128) x channels [kt*64, +64)
+                        tma_load_2d(sm.a(s, p), &tmA, kt * kBK, mt * kBM, fb);
+                    } else {
+                        // A: dq channels [mt*128 + 64c, +64) x tokens [kt*64, +64)
+                        tma_load_2d(sm.a(s, p), &tmA, mt * kBM, kt * kBK, fb);
+                        tma_load_2d(sm.a(s, p) + kChunkBytes, &tmA, mt * kBM + 64, kt * kBK, fb);
+                    }
+                    // B: 64-column chunks of W (dgrad, rows = channels) or x (wgrad, rows = tokens)
+                    for (int c = 0; c < nb_chunks; ++c)
+                        tma_load_2d(sm.b(s, p) + (uint32_t)c * kChunkBytes, &tmB, nt * p.BN + 64 * c,
+                                    kt * kBK, fb);
+                }
+                issued_mask |= 1u << s;
+                issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                if (++s == p.stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            for (int q = 0; q < p.stages; ++q)
+                if (issued_mask & (1u << q))
+                    mbar_wait(sm.full(q), (issued_par >> q) & 1u, nullptr, 200000000ull);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+                const int b = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!mbar_wait(sm.tempty(b), (use & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)b * kAccStride;
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!mbar_wait(sm.ready(s), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        // 16 reduction rows per MMA: 32 bytes along a K-major row,
+                        // 16 rows of 128 bytes in an MN-major chunk
+                        const uint64_t ad = WG ? desc_mnmajor_sw128(a0 + 2048u * j, kChunkBytes)
+                                               : desc_kmajor_sw128(a0 + 32u * j);
+                        const uint64_t bd = desc_mnmajor_sw128(b0 + 2048u * j, kChunkBytes);
+                        mma_bf16(d_tmem, ad, bd, p.idesc, (kt | j) != 0);
+                    }
+                    mma_commit(sm.empty(s));
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(sm.tfull(b));
+            }
+            if (!ok) {
+                mma_commit(sm.drain());
+                mbar_wait(sm.drain(), 0, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp < kXformWarp0) {
+        // ---------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+            const int b = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int mt = tile / p.num_n_tiles;
+            const int nt = tile % p.num_n_tiles;
+            const int64_t orow = (int64_t)mt * kBM + row;
+            const bool valid = orow < p.out_rows;
+            const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
+            for (int col = 0; col < p.BN; col += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld32(trow + col, r);
+                tmem_ld_wait();
+                const int64_t c0 = (int64_t)nt * p.BN + col;
+                if (valid) {
+                    uint16_t* dst = p.out + orow * p.out_cols + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        if (c0 + i + 8 <= p.out_cols)
+                            st_global_v4(dst + i,
+                                         pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                         pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                         pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
+                                         pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.tempty(b));
+        }
+    } else {
+        // --------------------------------------------------------- transform
+        const int tid = threadIdx.x - kXformWarp0 * 32;  // 0..127
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            const int mt = tile / p.num_n_tiles;
+            const int nt = tile % p.num_n_tiles;
+            const bool do_db = WG && p.db != nullptr && nt == 0;
+            float acc0 = 0.f, acc1 = 0.f;
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!mbar_wait(sm.full(s), ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a0 = sm.a(s, p);
+                bool wrote = false;
+                if (!WG) {
+                    const int r = tid;  // token row of the 128-row tile
+                    const int64_t t = (int64_t)mt * kBM + r;
+                    if (t < p.T) wrote = inverse_rope_row<DR>(p, a0 + (uint32_t)r * 128, r, (int64_t)kt * kBK, t);
+                } else {
+                    const int r = tid & 63, cc = tid >> 6;  // token row, 64-channel chunk
+                    const int64_t t = (int64_t)kt * kBK + r;
+                    if (t < p.T)
+                        wrote = inverse_rope_row<DR>(p, a0 + (uint32_t)cc * kChunkBytes + (uint32_t)r * 128, r,
+                                                     (int64_t)mt * kBM + 64 * cc, t);
+                }
+                if (wrote) fence_proxy_async_smem();
+                if (do_db) {
+                    // per-channel sums of the (rotated) tile: thread = channel pair
+                    // pp of the 128, rows [32 rh, 32 rh + 32) of the 64 tokens
+                    named_bar_sync(1, kXformThreads);
+                    const int pp = tid & 63, rh = tid >> 6;
+                    const uint32_t cbase = a0 + (uint32_t)(pp >> 5) * kChunkBytes + (uint32_t)(pp & 3) * 4;
+                    const int q16 = (pp & 31) >> 2;
+#pragma unroll 8
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int r = rh * 32 + rr;
+                        const uint32_t v = lds_b32(cbase + (uint32_t)r * 128 + (uint32_t)((q16 ^ (r & 7)) * 16));
+                        acc0 += bf16lo_to_f32(v);
+                        acc1 += bf16hi_to_f32(v);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.ready(s));
+                if (++s == p.stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (ok && do_db) {
+                const int pp = tid & 63, rh = tid >> 6;
+                if (rh == 1) {
+                    db_part[2 * pp] = acc0;
+                    db_part[2 * pp + 1] = acc1;
+                }
+                named_bar_sync(1, kXformThreads);
+                if (rh == 0) {
+                    const int64_t n = (int64_t)mt * kBM + 2 * pp;
+                    const float s0 = acc0 + db_part[2 * pp], s1 = acc1 + db_part[2 * pp + 1];
+                    const uint32_t packed = pack_bf16x2(s0, s1);
+                    if (n + 1 < p.N)
+                        *reinterpret_cast<uint32_t*>(p.db + n) = packed;
+                    else if (n < p.N)
+                        p.db[n] = (uint16_t)(packed & 0xFFFFu);
+                }
+                named_bar_sync(1, kXformThreads);
+            }
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) record_status(p.status, MLA_ERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <bool WG>
+int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const BwdParams& p, int grid,
+              size_t smem, cudaStream_t stream) {
+    const void* k = nullptr;
+    switch (Dr) {
+        case 16: k = (const void*)bwd_kernel<WG, 16>; break;
+        case 32: k = (const void*)bwd_kernel<WG, 32>; break;
+        case 64: k = (const void*)bwd_kernel<WG, 64>; break;
+        default: return MLA_ERR_UNSUPPORTED;
+    }
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    switch (Dr) {
+        case 16: bwd_kernel<WG, 16><<<grid, kThreads, smem, stream>>>(ta, tb, p); break;
+        case 32: bwd_kernel<WG, 32><<<grid, kThreads, smem, stream>>>(ta, tb, p); break;
+        default: bwd_kernel<WG, 64><<<grid, kThreads, smem, stream>>>(ta, tb, p); break;
+    }
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
+    DeviceInfo di;
+    int st = current_device_info(&di);
+    if (st != MLA_OK) return st;
+    const int D = a.Dn + a.Dr;
+    const int64_t N = (int64_t)a.H * D;
+    BwdParams p{};
+    p.T = (int)a.T;
+    p.K = (int)a.K;
+    p.N = (int)N;
+    p.D = D;
+    p.Dn = a.Dn;
+    int bn = (int)((a.K + 63) / 64) * 64;
+    p.BN = bn > 256 ? 256 : bn;
+    p.num_m_tiles = (int)(((wg ? N : a.T) + kBM - 1) / kBM);
+    p.num_n_tiles = (int)((a.K + p.BN - 1) / p.BN);
+    p.num_tiles = p.num_m_tiles * p.num_n_tiles;
+    p.k_tiles = (int)(((wg ? a.T : N) + kBK - 1) / kBK);
+    p.a_bytes = kBM * 128;
+    p.stage_bytes = p.a_bytes + (uint32_t)p.BN * 128;
+    p.tx_bytes = p.stage_bytes;
+    p.idesc = idesc_bf16(kBM, (uint32_t)p.BN, wg ? 1u : 0u, 1u);
+    p.pos = a.pos;
+    p.cos_tab = a.cos_tab;
+    p.sin_tab = a.sin_tab;
+    p.cs_rows = a.cs_rows;
+    p.cs_width = a.cs_width;
+    p.cs_vec = (a.cs_width % 4 == 0) && (reinterpret_cast<uintptr_t>(a.cos_tab) % 16 == 0) &&
+               (reinterpret_cast<uintptr_t>(a.sin_tab) % 16 == 0);
+    p.out = static_cast<uint16_t*>(wg ? a.dW : a.dx);
+    p.out_rows = (int)(wg ? N : a.T);
+    p.out_cols = (int)a.K;
+    p.db = wg ? static_cast<uint16_t*>(a.db) : nullptr;
+    p.status = a.status;
+
+    if (wg && a.T == 0) {  // empty reduction: the gradients are zero
+        if (cudaMemsetAsync(a.dW, 0, (size_t)N * a.K * 2, stream) != cudaSuccess) return MLA_ERR_CUDA;
+        if (a.db && cudaMemsetAsync(a.db, 0, (size_t)N * 2, stream) != cudaSuccess) return MLA_ERR_CUDA;
+        return MLA_OK;
+    }
+
+    const size_t fixed = 1024 + 1024;  // alignment slack + barriers, slots, bias partials
+    int stages = (int)((size_t)(di.max_smem_optin - fixed) / p.stage_bytes);
+    if (stages > 8) stages = 8;
+    if (stages < 2) return MLA_ERR_UNSUPPORTED;
+    p.stages = stages;
+    const size_t smem = fixed + (size_t)stages * p.stage_bytes;
+
+    alignas(64) CUtensorMap ta, tb;
+    if (!wg) {
+        st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, kBM, true);
+        if (st == MLA_OK)
+            st = make_tmap_2d(&tb, a.W, 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * 2, 64, kBK, true);
+    } else {
+        st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, kBK, true);
+        if (st == MLA_OK)
+            st = make_tmap_2d(&tb, a.x, 1, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, kBK, true);
+    }
+    if (st != MLA_OK) return st;
+    const int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
+    return wg ? launch_dr<true>(a.Dr, ta, tb, p, grid, smem, stream)
+              : launch_dr<false>(a.Dr, ta, tb, p, grid, smem, stream);
+}
+
+}  // namespace
+
+int launch_dgrad(const BwdArgs& a, cudaStream_t stream) { return launch_common(a, false, stream); }
+int launch_wgrad(const BwdArgs& a, cudaStream_t stream) { return launch_common(a, true, stream); }
+
 }  // namespace mlaq

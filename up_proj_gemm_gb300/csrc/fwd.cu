@@ -394,8 +394,8 @@ int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const FwdPar
 
 }  // namespace
 
-int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn) {
-    for (int bn = max_bn; bn >= 16; bn -= 16) {
+int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn, int step) {
+    for (int bn = max_bn / step * step; bn >= step; bn -= step) {
         if (N % bn) continue;
         bool ok = true;
         const int64_t heads = N / D;
@@ -418,8 +418,8 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     const int D = a.Dn + a.Dr;
     const int64_t N = (int64_t)a.H * D;
     // TMEM: two accumulators at columns 0 and 256; MXFP8 scale factors from column 448.
-    const int BN = fwd_tile_n(N, D, a.Dn, a.Dr, mxw ? 192 : 256);
-    if (BN == 0 || (mxw && BN % 32)) return MLA_ERR_UNSUPPORTED;
+    const int BN = fwd_tile_n(N, D, a.Dn, a.Dr, mxw ? 192 : 256, mxw ? 32 : 16);
+    if (BN == 0) return MLA_ERR_UNSUPPORTED;
 
     FwdParams p{};
     p.T = (int)a.T;

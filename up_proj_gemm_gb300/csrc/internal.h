@@ -67,8 +67,9 @@ struct BwdArgs {
 int launch_dgrad(const BwdArgs& a, cudaStream_t stream);
 int launch_wgrad(const BwdArgs& a, cudaStream_t stream);
 
-// Tile width (channels) of the forward kernel for this shape, or 0 when no
-// width in [16, 256] keeps every rope region and MXFP8 block inside one tile.
-int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn);
+// Tile width (channels) of the forward kernel for this shape: the largest
+// multiple of `step` that is <= max_bn, divides N and keeps every rope region
+// and every 32-channel pass-through block inside one tile; 0 if none.
+int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn, int step);
 
 }  // namespace mlaq
