@@ -254,6 +254,10 @@ def run_ours(args):
         k_dgrad()
         k_wgrad()
 
+    if args.only:
+        return run_only(args, w, inp, {"fwd": k_fwd, "dgrad": k_dgrad, "wgrad": k_wgrad}, flush, stream,
+                        status, dev)
+
     for _ in range(args.warmup):
         flush()
         step()
@@ -360,6 +364,40 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def run_only(args, w, inp, kernels, flush, stream, status, dev):
+    """One kernel alone, K timed calls (for profiling: a short, fixed launch
+    sequence). Prints a JSON line with its mean time."""
+    import torch
+    import up_proj_gemm_gb300 as mlaq
+    if args.only in kernels:
+        fn = kernels[args.only]
+        flop = w.fwd_flop() if args.only == "fwd" else w.bwd_flop() / 2
+    elif args.only == "fwd_mxfp8w":
+        xq, xs = mlaq.mxfp8_quantize_rows(inp["x"])
+        Wq, Ws = mlaq.mxfp8_quantize_rows(inp["W"])
+        qc = torch.empty((w.T, w.H, w.D), dtype=torch.uint8, device=dev)
+        qs = torch.empty((w.T, w.H, (w.D + 31) // 32), dtype=torch.uint8, device=dev)
+
+        def fn():
+            mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], weight_mode="mxfp8",
+                     out_mode="mxfp8", x_scales=xs, w_scales=Ws, q_out=qc, q_scales=qs, status=status)
+        flop = w.fwd_flop()
+    elif args.only == "quant":
+        a = torch.randn((w.T, w.N), device=dev).to(torch.bfloat16)
+        codes = torch.empty((w.T, w.N), dtype=torch.uint8, device=dev)
+        sc = torch.empty((w.T, w.N // 32), dtype=torch.uint8, device=dev)
+
+        def fn():
+            mlaq.mxfp8_quantize_rows(a, codes, sc)
+        flop = 0
+    else:
+        raise SystemExit(f"unknown --only {args.only}")
+    ms = time_loop(fn, args.steps, flush, stream, warmup=args.warmup)
+    mlaq.check_status(status, args.only)
+    print(json.dumps({"only": args.only, "ms": round(ms, 4), "steps": args.steps, "warmup": args.warmup,
+                      "TFLOP/s": round(flop / (ms * 1e-3) / 1e12, 1) if flop else None}), flush=True)
 
 
 def run_parts(dev, stream, flush, pk, pk_src):
@@ -531,6 +569,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "fwd_mxfp8w", "quant"),
+                    help="time one kernel alone (profiling)")
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")

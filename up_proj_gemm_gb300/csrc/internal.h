@@ -4,7 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
-#include "../../include/mlaq.h"
+#include "mlaq.h"
 
 namespace mlaq {
 
