@@ -13,13 +13,21 @@
 // each tile in place (fp32 math, rounded to bf16, the MMA operand type),
 // fence them into the async proxy and release the stage to the MMA thread.
 //
-// Warp roles (320 threads, persistent, one CTA per SM):
+// Warp roles (persistent, one CTA per SM):
 //   warp 0     TMA producer (S-stage ring, 128-byte swizzle)
 //   warp 1     single-thread tcgen05.mma issuer, double-buffered TMEM acc
 //   warps 2-5  epilogue: TMEM -> bf16 -> global (16-byte stores)
-//   warps 6-9  transform: inverse RoPE in shared memory; for wgrad also the
+//   warps 6-   transform: inverse RoPE in shared memory; for wgrad also the
 //              per-channel token sums that make db (tiles of the first K
-//              block only), deterministic, no atomics
+//              block only), deterministic, no atomics.
+//              dgrad: one group of 4 warps. Each thread owns one token row
+//              of its tile for the whole reduction, so it reads its cos/sin
+//              row once per tile and keeps it in registers.
+//              wgrad: three groups of 4 warps taking turns on stages (every
+//              stage brings 64 new tokens, so each needs fresh table rows;
+//              three stages in flight hide the table loads). Two threads
+//              share a token row; the table loads are issued before the
+//              stage's TMA data is awaited.
 //
 // Operand layouts (D = A B^T in tcgen05 terms, M = 128 rows):
 //   dgrad: A = dq   [T x N] K-major (tokens x channels), B = W [N x K]
@@ -40,9 +48,12 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kThreads = 320;
-constexpr int kXformThreads = 128;
+constexpr int kGroupThreads = 128;  // one transform group = 4 warps
 constexpr int kXformWarp0 = 6;
+
+// transform groups taking turns on stages: 1 for dgrad, 3 for wgrad
+__host__ __device__ constexpr int xform_groups(bool wg) { return wg ? 3 : 1; }
+__host__ __device__ constexpr int bwd_threads(bool wg) { return 32 * kXformWarp0 + kGroupThreads * xform_groups(wg); }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;
 constexpr uint32_t kChunkBytes = 64 * 128;  // one 64-wide MN chunk x 64 K rows
@@ -94,7 +105,7 @@ __device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ void load8(const float* p, bool vec, float (&v)[8]) {
+__device__ __forceinline__ void load8(const float* p, bool vec, float* v) {
     if (vec) {
         const float4 a = __ldg(reinterpret_cast<const float4*>(p));
         const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
@@ -106,65 +117,57 @@ __device__ __forceinline__ void load8(const float* p, bool vec, float (&v)[8]) {
     }
 }
 
-// Inverse RoPE, in place, on one 128-byte swizzled shared-memory row holding
-// channels [n0, n0 + 64) of token t (row index r inside its 1024-byte
-// swizzle atom group gives the XOR). With g = dq[Dn + .] of a head:
-//   out[i]      =  g[i] cos[p, i] + g[i+h] sin[p, i+h]
-//   out[i + h]  = -g[i] sin[p, i] + g[i+h] cos[p, i+h]      (h = Dr / 2)
-// Rope regions are Dr-aligned and Dr <= 64 divides 64, so both halves of a
-// pair lie in the same row; pairs are handled 8 at a time (16 bytes).
-template <int DR>
-__device__ __forceinline__ bool inverse_rope_row(const BwdParams& p, uint32_t row_addr, int r,
-                                                 int64_t n0, int64_t t) {
-    constexpr int HH = DR / 2;
-    int prow = -1;
-    bool wrote = false;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const int64_t n = n0 + 8 * q;
-        if (n >= p.N) break;
-        const int c0 = (int)(n % p.D);
-        if (c0 < p.Dn || c0 - p.Dn >= HH) continue;
-        if (prow < 0) {
-            const int64_t pp = p.pos ? (int64_t)__ldg(p.pos + t) : t;
-            if (pp < 0 || pp >= p.cs_rows) {
-                record_status(p.status, MLA_ERR_POS_RANGE);
-                return wrote;
-            }
-            prow = (int)pp;
-        }
-        const int i0 = c0 - p.Dn;
-        const int q2 = q + HH / 8;
-        const uint32_t a1 = row_addr + (uint32_t)((q ^ (r & 7)) * 16);
-        const uint32_t a2 = row_addr + (uint32_t)((q2 ^ (r & 7)) * 16);
-        uint32_t g1[4], g2[4];
-        lds_v4(a1, g1);
-        lds_v4(a2, g2);
-        const float* crow = p.cos_tab + (int64_t)prow * p.cs_width;
-        const float* srow = p.sin_tab + (int64_t)prow * p.cs_width;
-        float ci[8], si[8], cj[8], sj[8];
-        load8(crow + i0, p.cs_vec, ci);
-        load8(srow + i0, p.cs_vec, si);
-        load8(crow + i0 + HH, p.cs_vec, cj);
-        load8(srow + i0 + HH, p.cs_vec, sj);
-        uint32_t o1[4], o2[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float gi0 = bf16lo_to_f32(g1[w]), gi1 = bf16hi_to_f32(g1[w]);
-            const float gj0 = bf16lo_to_f32(g2[w]), gj1 = bf16hi_to_f32(g2[w]);
-            const int e0 = 2 * w, e1 = 2 * w + 1;
-            o1[w] = pack_bf16x2(gi0 * ci[e0] + gj0 * sj[e0], gi1 * ci[e1] + gj1 * sj[e1]);
-            o2[w] = pack_bf16x2(-gi0 * si[e0] + gj0 * cj[e0], -gi1 * si[e1] + gj1 * cj[e1]);
-        }
-        sts_v4(a1, o1);
-        sts_v4(a2, o2);
-        wrote = true;
+// Start channels of the rope regions inside [n0, n0 + width). Rope regions
+// are Dr-aligned and Dr <= 64 divides 64, so none straddles a 64-channel row
+// or a 128-channel tile.
+__device__ __forceinline__ int rope_regions(const BwdParams& p, int64_t n0, int width, int64_t (&st)[8]) {
+    int cnt = 0;
+    for (int64_t h = n0 / p.D; cnt < 8; ++h) {
+        const int64_t rs = h * p.D + p.Dn;
+        if (rs >= n0 + width || rs >= p.N) break;
+        if (rs >= n0) st[cnt++] = rs;
     }
-    return wrote;
+    return cnt;
+}
+
+// Inverse RoPE on 8 pairs of one token, in place in a 128-byte swizzled
+// shared-memory row (row index r inside its 1024-byte swizzle group gives
+// the XOR). Chunk q1 holds g[i], chunk q2 = q1 + Dr/16 holds g[i + Dr/2]:
+//   out[i]        =  g[i] cos[p, i] + g[i+h] sin[p, i+h]
+//   out[i + h]    = -g[i] sin[p, i] + g[i+h] cos[p, i+h]     (h = Dr / 2)
+// ci/si: cos, sin at i; cj/sj: cos, sin at i + h (8 consecutive pairs).
+__device__ __forceinline__ void rot8(uint32_t row_addr, int r, int q1, int q2, const float* ci,
+                                     const float* si, const float* cj, const float* sj) {
+    const uint32_t a1 = row_addr + (uint32_t)((q1 ^ (r & 7)) * 16);
+    const uint32_t a2 = row_addr + (uint32_t)((q2 ^ (r & 7)) * 16);
+    uint32_t g1[4], g2[4];
+    lds_v4(a1, g1);
+    lds_v4(a2, g2);
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float gi0 = bf16lo_to_f32(g1[w]), gi1 = bf16hi_to_f32(g1[w]);
+        const float gj0 = bf16lo_to_f32(g2[w]), gj1 = bf16hi_to_f32(g2[w]);
+        const int e0 = 2 * w, e1 = 2 * w + 1;
+        o1[w] = pack_bf16x2(gi0 * ci[e0] + gj0 * sj[e0], gi1 * ci[e1] + gj1 * sj[e1]);
+        o2[w] = pack_bf16x2(-gi0 * si[e0] + gj0 * cj[e0], -gi1 * si[e1] + gj1 * cj[e1]);
+    }
+    sts_v4(a1, o1);
+    sts_v4(a2, o2);
+}
+
+// Position row of token t, or -1 (recorded) when outside the table.
+__device__ __forceinline__ int pos_row(const BwdParams& p, int64_t t) {
+    const int64_t pp = p.pos ? (int64_t)__ldg(p.pos + t) : t;
+    if (pp < 0 || pp >= p.cs_rows) {
+        record_status(p.status, MLA_ERR_POS_RANGE);
+        return -1;
+    }
+    return (int)pp;
 }
 
 template <bool WG, int DR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(bwd_threads(WG), 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (3 * p.stages + 5);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
-    float* db_part = reinterpret_cast<float*>(tail + 16);  // 128 floats (wgrad bias sums)
+    float* db_part = reinterpret_cast<float*>(tail + 16);  // 2 x groups x 128 floats (wgrad bias sums)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(sm.full(s), 1);
-            mbar_init(sm.ready(s), kXformThreads / 32);
+            mbar_init(sm.ready(s), kGroupThreads / 32);
             mbar_init(sm.empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -338,39 +341,115 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // --------------------------------------------------------- transform
-        const int tid = threadIdx.x - kXformWarp0 * 32;  // 0..127
+        constexpr int G = xform_groups(WG);
+        constexpr int HH = DR / 2;
+        const int xt = threadIdx.x - kXformWarp0 * 32;
+        const int grp = xt / kGroupThreads;  // this thread's group
+        const int gt = xt % kGroupThreads;   // thread within the group
+        const bool vec = p.cs_vec != 0;
         int s = 0;
         uint32_t ph = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int kglob = 0;  // stage counter over all tiles: group kglob % G owns the stage
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
             const int mt = tile / p.num_n_tiles;
             const int nt = tile % p.num_n_tiles;
             const bool do_db = WG && p.db != nullptr && nt == 0;
             float acc0 = 0.f, acc1 = 0.f;
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
-                if (!mbar_wait(sm.full(s), ph, abort_flag)) {
-                    ok = false;
-                    break;
+            // dgrad: this thread's token and its cos/sin row, cached for the whole tile
+            float c1[WG ? 1 : HH], s1[WG ? 1 : HH], c2[WG ? 1 : HH], s2[WG ? 1 : HH];
+            int drow = -1;
+            // wgrad: the tile's rope regions and this thread's share of them
+            int64_t reg[8];
+            int nreg = 0;
+            if (!WG) {
+                const int64_t t = (int64_t)mt * kBM + gt;
+                if (t < p.T) drow = pos_row(p, t);
+                if (drow >= 0) {
+                    const float* cr = p.cos_tab + (int64_t)drow * p.cs_width;
+                    const float* sr = p.sin_tab + (int64_t)drow * p.cs_width;
+#pragma unroll
+                    for (int q = 0; q < HH; q += 8) {
+                        load8(cr + q, vec, c1 + (WG ? 0 : q));
+                        load8(sr + q, vec, s1 + (WG ? 0 : q));
+                        load8(cr + HH + q, vec, c2 + (WG ? 0 : q));
+                        load8(sr + HH + q, vec, s2 + (WG ? 0 : q));
+                    }
                 }
-                const uint32_t a0 = sm.a(s, p);
+            } else {
+                nreg = rope_regions(p, (int64_t)mt * kBM, kBM, reg);
+            }
+            for (int kt = 0; kt < p.k_tiles; ++kt, ++kglob) {
+                if (kglob % G != grp) {
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    continue;
+                }
                 bool wrote = false;
                 if (!WG) {
-                    const int r = tid;  // token row of the 128-row tile
-                    const int64_t t = (int64_t)mt * kBM + r;
-                    if (t < p.T) wrote = inverse_rope_row<DR>(p, a0 + (uint32_t)r * 128, r, (int64_t)kt * kBK, t);
+                    const bool ok = mbar_wait(sm.full(s), ph, abort_flag);
+                    const uint32_t a0 = sm.a(s, p);
+                    int64_t st[8];
+                    const int n = (ok && drow >= 0) ? rope_regions(p, (int64_t)kt * kBK, kBK, st) : 0;
+                    for (int j = 0; j < n; ++j) {
+                        const int q0 = (int)(st[j] - (int64_t)kt * kBK) / 8;
+#pragma unroll
+                        for (int g = 0; g < HH / 8; ++g)
+                            rot8(a0 + (uint32_t)gt * 128, gt, q0 + g, q0 + g + HH / 8, c1 + (WG ? 0 : 8 * g),
+                                 s1 + (WG ? 0 : 8 * g), c2 + (WG ? 0 : 8 * g), s2 + (WG ? 0 : 8 * g));
+                        wrote = true;
+                    }
+                    (void)ok;
                 } else {
-                    const int r = tid & 63, cc = tid >> 6;  // token row, 64-channel chunk
+                    // two threads per token row; Dr = 64 splits each region's 32
+                    // pairs between them, narrower rope dims split the regions
+                    constexpr int PPI = HH < 16 ? HH : 16;  // pairs per item
+                    constexpr int IPR = HH / PPI;           // items per region
+                    const int r = gt >> 1, half = gt & 1;
                     const int64_t t = (int64_t)kt * kBK + r;
-                    if (t < p.T)
-                        wrote = inverse_rope_row<DR>(p, a0 + (uint32_t)cc * kChunkBytes + (uint32_t)r * 128, r,
-                                                     (int64_t)mt * kBM + 64 * cc, t);
+                    const int pb = (IPR == 2) ? PPI * half : 0;
+                    bool mine = false;
+                    for (int j = 0; j < nreg; ++j) mine |= (IPR == 2) || ((j & 1) == half);
+                    int prow = -1;
+                    float ci[PPI], si[PPI], cj[PPI], sj[PPI];
+                    if (mine && t < p.T) {
+                        prow = pos_row(p, t);
+                        if (prow >= 0) {
+                            const float* cr = p.cos_tab + (int64_t)prow * p.cs_width + pb;
+                            const float* sr = p.sin_tab + (int64_t)prow * p.cs_width + pb;
+#pragma unroll
+                            for (int q = 0; q < PPI; q += 8) {
+                                load8(cr + q, vec, ci + q);
+                                load8(sr + q, vec, si + q);
+                                load8(cr + HH + q, vec, cj + q);
+                                load8(sr + HH + q, vec, sj + q);
+                            }
+                        }
+                    }
+                    const bool ok = mbar_wait(sm.full(s), ph, abort_flag);
+                    if (ok && prow >= 0) {
+                        const uint32_t a0 = sm.a(s, p);
+                        for (int j = 0; j < nreg; ++j) {
+                            if (IPR == 1 && (j & 1) != half) continue;
+                            const int o = (int)(reg[j] - (int64_t)mt * kBM);  // channel offset in the tile
+                            const uint32_t row = a0 + (uint32_t)(o / 64) * kChunkBytes + (uint32_t)r * 128;
+                            const int q0 = (o % 64 + pb) / 8;
+#pragma unroll
+                            for (int g = 0; g < PPI / 8; ++g)
+                                rot8(row, r, q0 + g, q0 + g + HH / 8, ci + 8 * g, si + 8 * g, cj + 8 * g,
+                                     sj + 8 * g);
+                            wrote = true;
+                        }
+                    }
                 }
                 if (wrote) fence_proxy_async_smem();
                 if (do_db) {
                     // per-channel sums of the (rotated) tile: thread = channel pair
                     // pp of the 128, rows [32 rh, 32 rh + 32) of the 64 tokens
-                    named_bar_sync(1, kXformThreads);
-                    const int pp = tid & 63, rh = tid >> 6;
+                    named_bar_sync(1 + grp, kGroupThreads);
+                    const uint32_t a0 = sm.a(s, p);
+                    const int pp = gt & 63, rh = gt >> 6;
                     const uint32_t cbase = a0 + (uint32_t)(pp >> 5) * kChunkBytes + (uint32_t)(pp & 3) * 4;
                     const int q16 = (pp & 31) >> 2;
 #pragma unroll 8
@@ -388,23 +467,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ph ^= 1u;
                 }
             }
-            if (ok && do_db) {
-                const int pp = tid & 63, rh = tid >> 6;
-                if (rh == 1) {
-                    db_part[2 * pp] = acc0;
-                    db_part[2 * pp + 1] = acc1;
-                }
-                named_bar_sync(1, kXformThreads);
-                if (rh == 0) {
+            if (do_db) {
+                // combine the 2G partial sums of each channel, write bf16 db
+                const int pp = gt & 63, rh = gt >> 6;
+                const int part = grp * 2 + rh;
+                db_part[part * 128 + 2 * pp] = acc0;
+                db_part[part * 128 + 2 * pp + 1] = acc1;
+                named_bar_sync(1 + G, G * kGroupThreads);
+                if (part == 0) {
+                    float s0 = 0.f, s1v = 0.f;
+                    for (int q = 0; q < 2 * G; ++q) {
+                        s0 += db_part[q * 128 + 2 * pp];
+                        s1v += db_part[q * 128 + 2 * pp + 1];
+                    }
                     const int64_t n = (int64_t)mt * kBM + 2 * pp;
-                    const float s0 = acc0 + db_part[2 * pp], s1 = acc1 + db_part[2 * pp + 1];
-                    const uint32_t packed = pack_bf16x2(s0, s1);
+                    const uint32_t packed = pack_bf16x2(s0, s1v);
                     if (n + 1 < p.N)
                         *reinterpret_cast<uint32_t*>(p.db + n) = packed;
                     else if (n < p.N)
                         p.db[n] = (uint16_t)(packed & 0xFFFFu);
                 }
-                named_bar_sync(1, kXformThreads);
+                named_bar_sync(1 + G, G * kGroupThreads);
             }
         }
     }
@@ -432,9 +515,9 @@ int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const BwdPar
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MLA_ERR_CUDA;
     switch (Dr) {
-        case 16: bwd_kernel<WG, 16><<<grid, kThreads, smem, stream>>>(ta, tb, p); break;
-        case 32: bwd_kernel<WG, 32><<<grid, kThreads, smem, stream>>>(ta, tb, p); break;
-        default: bwd_kernel<WG, 64><<<grid, kThreads, smem, stream>>>(ta, tb, p); break;
+        case 16: bwd_kernel<WG, 16><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, p); break;
+        case 32: bwd_kernel<WG, 32><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, p); break;
+        default: bwd_kernel<WG, 64><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, p); break;
     }
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -480,7 +563,7 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
         return MLA_OK;
     }
 
-    const size_t fixed = 1024 + 1024;  // alignment slack + barriers, slots, bias partials
+    const size_t fixed = 1024 + 4096;  // alignment slack + barriers, slots, bias partials
     int stages = (int)((size_t)(di.max_smem_optin - fixed) / p.stage_bytes);
     if (stages > 8) stages = 8;
     if (stages < 2) return MLA_ERR_UNSUPPORTED;

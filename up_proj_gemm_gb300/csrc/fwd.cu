@@ -41,6 +41,9 @@ constexpr uint32_t kAccStride = 256;  // TMEM column offset of accumulator buffe
 constexpr uint32_t kSfCol0 = 448;     // first TMEM column of the per-stage scale factors
 constexpr uint32_t kSfColsPerStage = 12;  // 4 (A: 128 rows) + 8 (B: up to 256 rows)
 constexpr uint32_t kSfBytesPerStage = 512 + 1024;
+constexpr int kEpiWarps = 4;
+constexpr int kSlotCh = 16;       // channels per slot (one TMA store box: 16 channels x 32 rows)
+constexpr uint32_t kBiasBytes = 512;  // 256 bf16 channels per tile, double-buffered
 
 struct FwdParams {
     int T, H, N, D, Dn;
@@ -50,6 +53,9 @@ struct FwdParams {
     uint32_t a_bytes, stage_bytes, tx_bytes;
     uint32_t idesc;
     int ksb;  // scale bytes per operand row (K / 32)
+    uint32_t slot_bytes;  // 32 rows x 16 channels x output element size
+    int cs_vec;           // cos/sin rows 16-byte aligned: float4 loads
+    int nslots;           // staging slots per epilogue warp
     const uint16_t* bias;
     const float* cos_tab;
     const float* sin_tab;
@@ -65,6 +71,8 @@ struct FwdParams {
 struct Smem {
     uint32_t base;      // shared address of stage 0 (1024-aligned)
     uint32_t sf;        // scale staging (MXFP8 weights)
+    uint32_t out;       // output staging: kEpiWarps x kSlots slots
+    uint32_t bias;      // 2 x kBiasBytes
     uint32_t bars;      // mbarriers
     int S;
     __device__ uint32_t a(int s, const FwdParams& p) const { return base + (uint32_t)s * p.stage_bytes; }
@@ -78,102 +86,168 @@ struct Smem {
     __device__ uint32_t drain() const { return bars + 8u * (2 * S + 4); }
 };
 
-__device__ __forceinline__ float bf16_at(const uint16_t* p, int i) {
-    return __uint_as_float((uint32_t)__ldg(p + i) << 16);
+// ------------------------------------------------------------ epilogue parts
+// Each epilogue warp owns 32 token rows of the tile. Its results go through a
+// ring of p.nslots shared-memory slots (32 rows x 16 channels each) and leave
+// as TMA tile stores (one per slot), so global writes are whole, coalesced
+// boxes and the LSU queue carries no per-row stores.
+struct EpiCtx {
+    uint32_t slots;   // this warp's staging ring
+    uint32_t bias_s;  // this warp's copy of the tile's bias (bf16), 0 if none
+    int cursor;       // next free slot (counts pieces; taken modulo nslots)
+    int prev_pieces;  // pieces of the previous unit (its store may still read)
+    int32_t t0;       // first token row of this warp's 32-row slab
+};
+
+__device__ __forceinline__ uint32_t slot_addr(const FwdParams& p, const EpiCtx& c, int k) {
+    return c.slots + (uint32_t)(k % p.nslots) * p.slot_bytes;
 }
 
-// ------------------------------------------------------------ epilogue parts
+__device__ __forceinline__ void add_bias(float* v, int nv, uint32_t bias_s) {
+    for (int k = 0; k < nv / 8; ++k) {
+        const uint4 b = lds_v4(bias_s + 16u * k);
+        v[8 * k + 0] += bf16lo_to_f32(b.x);
+        v[8 * k + 1] += bf16hi_to_f32(b.x);
+        v[8 * k + 2] += bf16lo_to_f32(b.y);
+        v[8 * k + 3] += bf16hi_to_f32(b.y);
+        v[8 * k + 4] += bf16lo_to_f32(b.z);
+        v[8 * k + 5] += bf16hi_to_f32(b.z);
+        v[8 * k + 6] += bf16lo_to_f32(b.w);
+        v[8 * k + 7] += bf16hi_to_f32(b.w);
+    }
+}
+
+// Quantize/convert this thread's NV values (output channels [n, n + NV) of
+// token t, i.e. channels [cin, cin + NV) of head h) into the staging ring and
+// store them with TMA. NV is a multiple of 16.
 template <bool MXOUT, int NV>
-__device__ __forceinline__ void store_unit(const FwdParams& p, const float (&v)[NV], int64_t t,
-                                           int64_t n, int h, int c) {
-    // v holds output channels [n, n + NV) of token t; they are channels
-    // [c, c + NV) of head h. n is a multiple of 16.
+__device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
+                                          const float (&v)[NV], bool valid, int64_t t, int64_t n, int h,
+                                          int cin) {
+    constexpr int PIECES = NV / 16;
+    const int lane = threadIdx.x & 31;
+    // the slots about to be written were last read by stores older than the previous unit's
+    if (lane == 0) {
+        if (c.prev_pieces + PIECES <= p.nslots) bulk_wait_group_read<1>();
+        else bulk_wait_group_read<0>();
+    }
+    __syncwarp();
+    const int first = c.cursor;
     if (MXOUT) {
         const int NB = (p.D + 31) / 32;
 #pragma unroll
         for (int blk = 0; blk < (NV + 31) / 32; ++blk) {
-            constexpr int W = 32;
-            float b[W];
+            float b[32];
 #pragma unroll
-            for (int i = 0; i < W; ++i) b[i] = (blk * 32 + i < NV) ? v[blk * 32 + i] : 0.f;
+            for (int i = 0; i < 32; ++i) b[i] = (blk * 32 + i < NV) ? v[blk * 32 + i] : 0.f;
             const int nvalid = (NV - blk * 32) < 32 ? (NV - blk * 32) : 32;
             uint32_t codes[8];
-            const uint32_t sb = quantize_block_regs<W>(b, nvalid, codes);
-            uint8_t* dst = p.q_out + t * p.N + n + blk * 32;
-            st_global_v4(dst, codes[0], codes[1], codes[2], codes[3]);
-            if (nvalid > 16) st_global_v4(dst + 16, codes[4], codes[5], codes[6], codes[7]);
-            p.q_scales[(t * p.H + h) * NB + (c + blk * 32) / 32] = (uint8_t)sb;
+            const uint32_t sb = quantize_block_regs<32>(b, nvalid, codes);
+            sts_v4(slot_addr(p, c, first + 2 * blk) + 16u * lane, codes[0], codes[1], codes[2], codes[3]);
+            if (nvalid > 16)
+                sts_v4(slot_addr(p, c, first + 2 * blk + 1) + 16u * lane, codes[4], codes[5], codes[6],
+                       codes[7]);
+            if (valid) p.q_scales[(t * p.H + h) * NB + (cin + blk * 32) / 32] = (uint8_t)sb;
         }
     } else {
-        uint8_t* dst = p.q_out + (t * p.N + n) * 2;
 #pragma unroll
-        for (int i = 0; i < NV; i += 8)
-            st_global_v4(dst + 2 * i, pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
-                         pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]));
+        for (int pc = 0; pc < PIECES; ++pc) {
+            const uint32_t a = slot_addr(p, c, first + pc) + 32u * lane;
+            const float* w = v + 16 * pc;
+            sts_v4(a, pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                   pack_bf16x2(w[6], w[7]));
+            sts_v4(a + 16, pack_bf16x2(w[8], w[9]), pack_bf16x2(w[10], w[11]), pack_bf16x2(w[12], w[13]),
+                   pack_bf16x2(w[14], w[15]));
+        }
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+        for (int pc = 0; pc < PIECES; ++pc)
+            tma_store_2d(tmC, (int32_t)(n + 16 * pc), c.t0, slot_addr(p, c, first + pc));
+        bulk_commit_group();
+    }
+    c.cursor = first + PIECES;
+    c.prev_pieces = PIECES;
 }
 
 template <bool MXOUT>
-__device__ __forceinline__ void nope_unit(const FwdParams& p, uint32_t taddr, bool valid, int64_t t,
-                                          int64_t n, int h, int c) {
+__device__ __forceinline__ void nope_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
+                                          uint32_t taddr, int col, bool valid, int64_t t, int64_t n, int h,
+                                          int cin) {
     uint32_t r[32];
     __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
     tmem_ld32(taddr, r);
     tmem_ld_wait();
-    if (!valid) return;
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-    if (p.bias) {
+    if (c.bias_s) add_bias(v, 32, c.bias_s + 2u * col);
+    emit_unit<MXOUT, 32>(p, tmC, c, v, valid, t, n, h, cin);
+}
+
+__device__ __forceinline__ void load_table8(const float* src, bool vec, float (&o)[8]) {
+    if (vec) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] += bf16_at(p.bias, (int)n + i);
+        for (int e = 0; e < 8; ++e) o[e] = __ldg(src + e);
     }
-    store_unit<MXOUT, 32>(p, v, t, n, h, c);
 }
 
 template <bool MXOUT, int DR>
-__device__ __forceinline__ void rope_unit(const FwdParams& p, uint32_t taddr, bool valid, int64_t t,
-                                          int64_t n, int h, int prow) {
+__device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
+                                          uint32_t taddr, int col, bool valid, int64_t t, int64_t n, int h,
+                                          int prow) {
     constexpr int HH = DR / 2;
     uint32_t r[DR / 16][16];
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < DR / 16; ++j) tmem_ld16(taddr + 16 * j, r[j]);
     tmem_ld_wait();
-    if (!valid) return;
     float y[DR];
 #pragma unroll
     for (int i = 0; i < DR; ++i) y[i] = __uint_as_float(r[i / 16][i % 16]);
-    if (p.bias) {
-#pragma unroll
-        for (int i = 0; i < DR; ++i) y[i] += bf16_at(p.bias, (int)n + i);
-    }
+    if (c.bias_s) add_bias(y, DR, c.bias_s + 2u * col);
     const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
     const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
-    float o[DR];
+    const bool vec = p.cs_vec != 0;
+    // rotate in place, 8 pairs at a time: (a, c) = (y[i], y[i + HH])
 #pragma unroll
-    for (int i = 0; i < HH; ++i) {
-        const float a = y[i], c = y[i + HH];
-        const float ci = __ldg(cs + i), si = __ldg(sn + i);
-        const float cj = __ldg(cs + i + HH), sj = __ldg(sn + i + HH);
-        o[i] = a * ci - c * si;
-        o[i + HH] = c * cj + a * sj;
+    for (int q = 0; q < HH; q += 8) {
+        float ci[8], si[8], cj[8], sj[8];
+        load_table8(cs + q, vec, ci);
+        load_table8(sn + q, vec, si);
+        load_table8(cs + q + HH, vec, cj);
+        load_table8(sn + q + HH, vec, sj);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float a = y[q + e], b = y[q + e + HH];
+            y[q + e] = a * ci[e] - b * si[e];
+            y[q + e + HH] = b * cj[e] + a * sj[e];
+        }
     }
-    store_unit<MXOUT, DR>(p, o, t, n, h, p.Dn);
+    emit_unit<MXOUT, DR>(p, tmC, c, y, valid, t, n, h, p.Dn);
 }
 
 // ------------------------------------------------------------------- kernel
 template <bool MXW, bool MXOUT, int DR>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const FwdParams p) {
+               const __grid_constant__ CUtensorMap tmC, const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     Smem sm;
     sm.S = p.stages;
     sm.base = (raw + 1023u) & ~1023u;
     sm.sf = sm.base + (uint32_t)p.stages * p.stage_bytes;
-    sm.bars = sm.sf + (MXW ? (uint32_t)p.stages * kSfBytesPerStage : 0u);
+    sm.out = sm.sf + (MXW ? (uint32_t)p.stages * kSfBytesPerStage : 0u);
+    sm.bias = sm.out + (uint32_t)(kEpiWarps * p.nslots) * p.slot_bytes;
+    sm.bars = sm.bias + kEpiWarps * kBiasBytes;
     uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (2 * p.stages + 5);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
@@ -197,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32((const void*)tmem_slot), kTmemCols);
@@ -323,6 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- epilogue
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;
+        const int ew = warp - 2;    // epilogue warp 0..3
+        EpiCtx ec;
+        ec.slots = sm.out + (uint32_t)(ew * p.nslots) * p.slot_bytes;
+        ec.cursor = 0;
+        ec.prev_pieces = 0;
+        const uint32_t bias_buf = sm.bias + (uint32_t)ew * kBiasBytes;
         int local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const int b = local & 1;
@@ -341,16 +422,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
             const int64_t n0 = (int64_t)nt * p.BN;
+            ec.t0 = mt * kBM + quad * 32;
+            ec.bias_s = 0;
+            if (p.bias) {
+                // this warp's copy of the tile's bias: lane l holds channels 2l, 2l+1 of each 64
+                __syncwarp();  // previous tile's reads of the buffer are done
+                for (int k = 2 * lane; k < p.BN; k += 64)
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(bias_buf + 2u * k),
+                                 "r"(__ldg(reinterpret_cast<const uint32_t*>(p.bias + n0 + k)))
+                                 : "memory");
+                __syncwarp();
+                ec.bias_s = bias_buf;
+            }
             int col = 0;
             while (col < p.BN) {
                 const int64_t n = n0 + col;
                 const int h = (int)(n / p.D);
                 const int c = (int)(n - (int64_t)h * p.D);
                 if (c < p.Dn) {
-                    nope_unit<MXOUT>(p, trow + col, valid, t, n, h, c);
+                    nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
                     col += 32;
                 } else {
-                    rope_unit<MXOUT, DR>(p, trow + col, valid, t, n, h, prow);
+                    rope_unit<MXOUT, DR>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
                     col += DR;
                 }
             }
@@ -358,6 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.tempty(b));
         }
+        if (lane == 0) bulk_wait_group_all();  // every output store has landed
+        __syncwarp();
     }
 
     // ------------------------------------------------------------- teardown
@@ -371,23 +466,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool MXW, bool MXOUT, int DR>
-int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const FwdParams& p, int grid,
-                   size_t smem, cudaStream_t stream) {
+int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                   const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
     auto kern = fwd_kernel<MXW, MXOUT, DR>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return MLA_ERR_CUDA;
-    kern<<<grid, kThreads, smem, stream>>>(ta, tb, p);
+    kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, p);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 template <bool MXW, bool MXOUT>
-int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const FwdParams& p, int grid,
-              size_t smem, cudaStream_t stream) {
+int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+              const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
     switch (Dr) {
-        case 16: return launch_variant<MXW, MXOUT, 16>(ta, tb, p, grid, smem, stream);
-        case 32: return launch_variant<MXW, MXOUT, 32>(ta, tb, p, grid, smem, stream);
-        case 64: return launch_variant<MXW, MXOUT, 64>(ta, tb, p, grid, smem, stream);
+        case 16: return launch_variant<MXW, MXOUT, 16>(ta, tb, tc, p, grid, smem, stream);
+        case 32: return launch_variant<MXW, MXOUT, 32>(ta, tb, tc, p, grid, smem, stream);
+        case 64: return launch_variant<MXW, MXOUT, 64>(ta, tb, tc, p, grid, smem, stream);
         default: return MLA_ERR_UNSUPPORTED;
     }
 }
@@ -448,8 +543,14 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.x_scales = a.x_scales;
     p.w_scales = a.w_scales;
     p.status = a.status;
+    p.cs_vec = (a.cs_width % 4 == 0) && (reinterpret_cast<uintptr_t>(a.cos_tab) % 16 == 0) &&
+               (reinterpret_cast<uintptr_t>(a.sin_tab) % 16 == 0);
+    const bool mxo = a.out_mode == MLA_OUT_MXFP8;
+    p.slot_bytes = 32u * kSlotCh * (mxo ? 1u : 2u);
+    p.nslots = mxo ? 8 : 6;  // a unit takes at most 4 slots (64 rope channels)
 
-    const size_t fixed = 1024 /* alignment slack */ + 256 /* barriers + slots */;
+    const size_t fixed = 1024 /* alignment slack */ + 256 /* barriers + slots */ +
+                         (size_t)kEpiWarps * p.nslots * p.slot_bytes + kEpiWarps * kBiasBytes;
     const size_t per_stage = p.stage_bytes + (mxw ? kSfBytesPerStage : 0);
     int stages = (int)((size_t)(di.max_smem_optin - fixed) / per_stage);
     if (stages > 8) stages = 8;
@@ -465,14 +566,18 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     st = make_tmap_2d(&tb, a.W, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * (mxw ? 1 : 2),
                       128 / (mxw ? 1 : 2), (uint32_t)BN, true);
     if (st != MLA_OK) return st;
+    // output q [T, N] (bf16 or E4M3 bytes): TMA store boxes of 16 channels x 32 tokens
+    alignas(64) CUtensorMap tc;
+    st = make_tmap_2d(&tc, a.q_out, mxo ? 0 : 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * (mxo ? 1 : 2),
+                      kSlotCh, 32, false);
+    if (st != MLA_OK) return st;
 
     int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
-    const bool mxo = a.out_mode == MLA_OUT_MXFP8;
     if (mxw)
-        return mxo ? launch_dr<true, true>(a.Dr, ta, tb, p, grid, smem, stream)
-                   : launch_dr<true, false>(a.Dr, ta, tb, p, grid, smem, stream);
-    return mxo ? launch_dr<false, true>(a.Dr, ta, tb, p, grid, smem, stream)
-               : launch_dr<false, false>(a.Dr, ta, tb, p, grid, smem, stream);
+        return mxo ? launch_dr<true, true>(a.Dr, ta, tb, tc, p, grid, smem, stream)
+                   : launch_dr<true, false>(a.Dr, ta, tb, tc, p, grid, smem, stream);
+    return mxo ? launch_dr<false, true>(a.Dr, ta, tb, tc, p, grid, smem, stream)
+               : launch_dr<false, false>(a.Dr, ta, tb, tc, p, grid, smem, stream);
 }
 
 }  // namespace mlaq
