@@ -127,7 +127,7 @@ typedef struct {
  *               codes.
  * Tiling limits (else MLA_ERR_UNSUPPORTED): Dr in {16, 32, 64}, Dn % 32 == 0;
  * bf16 weights need K % 8 == 0 (16-byte rows). Pointers must be 16-byte
- * aligned (scales and bias: 4-byte), else MLA_ERR_ALIGNMENT.
+ * aligned (scales: 4-byte; bias: 16-byte), else MLA_ERR_ALIGNMENT.
  */
 MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_mode,
                              const void *x, const uint8_t *x_scales, const void *W,

@@ -188,7 +188,7 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
     const int64_t esz = mxw ? 1 : 2;
     if ((s.K * esz) % 16) return MLA_ERR_ALIGNMENT;
     if (!aligned(x, 16) || !aligned(W, 16) || !aligned(q_out, 16) || !aligned(x_scales, 4) ||
-        !aligned(w_scales, 4) || !aligned(bias, 4) || !aligned(cos_tab, 4) || !aligned(sin_tab, 4) ||
+        !aligned(w_scales, 4) || !aligned(bias, 16) || !aligned(cos_tab, 4) || !aligned(sin_tab, 4) ||
         !aligned(pos, 4) || !aligned(dev_status, 4))
         return MLA_ERR_ALIGNMENT;
 

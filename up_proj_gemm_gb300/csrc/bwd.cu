@@ -47,16 +47,21 @@ namespace mlaq {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBK = 64;
-constexpr int kGroupThreads = 128;  // one transform group = 4 warps
 constexpr int kXformWarp0 = 6;
 
-// transform groups taking turns on stages: 1 for dgrad, 3 for wgrad
+// Reduction rows per stage: 64 channels (dgrad) or 32 tokens (wgrad, whose
+// stages each need fresh cos/sin rows: a deeper ring of smaller stages).
+__host__ __device__ constexpr int bk_of(bool wg) { return wg ? 32 : 64; }
+// bytes of one 64-wide MN-major chunk (bk rows of 128 bytes)
+__host__ __device__ constexpr uint32_t chunk_of(bool wg) { return (uint32_t)bk_of(wg) * 128u; }
+// transform groups taking turns on stages, and threads per group
 __host__ __device__ constexpr int xform_groups(bool wg) { return wg ? 3 : 1; }
-__host__ __device__ constexpr int bwd_threads(bool wg) { return 32 * kXformWarp0 + kGroupThreads * xform_groups(wg); }
+__host__ __device__ constexpr int group_threads(bool wg) { return wg ? 128 : 256; }
+__host__ __device__ constexpr int bwd_threads(bool wg) {
+    return 32 * kXformWarp0 + group_threads(wg) * xform_groups(wg);
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;
-constexpr uint32_t kChunkBytes = 64 * 128;  // one 64-wide MN chunk x 64 K rows
 
 struct BwdParams {
     int T, K, N, D, Dn;
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(sm.full(s), 1);
-            mbar_init(sm.ready(s), kGroupThreads / 32);
+            mbar_init(sm.ready(s), group_threads(WG) / 32);
             mbar_init(sm.empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -211,6 +216,8 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int nb_chunks = p.BN / 64;
+    constexpr int BK = bk_of(WG);
+    constexpr uint32_t CH = chunk_of(WG);
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -231,16 +238,15 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     mbar_arrive_expect_tx(fb, p.tx_bytes);
                     if (!WG) {
                         // A: dq rows [mt*128, +128) x channels [kt*64, +64)
-                        tma_load_2d(sm.a(s, p), &tmA, kt * kBK, mt * kBM, fb);
+                        tma_load_2d(sm.a(s, p), &tmA, kt * BK, mt * kBM, fb);
                     } else {
                         // A: dq channels [mt*128 + 64c, +64) x tokens [kt*64, +64)
-                        tma_load_2d(sm.a(s, p), &tmA, mt * kBM, kt * kBK, fb);
-                        tma_load_2d(sm.a(s, p) + kChunkBytes, &tmA, mt * kBM + 64, kt * kBK, fb);
+                        tma_load_2d(sm.a(s, p), &tmA, mt * kBM, kt * BK, fb);
+                        tma_load_2d(sm.a(s, p) + CH, &tmA, mt * kBM + 64, kt * BK, fb);
                     }
                     // B: 64-column chunks of W (dgrad, rows = channels) or x (wgrad, rows = tokens)
                     for (int c = 0; c < nb_chunks; ++c)
-                        tma_load_2d(sm.b(s, p) + (uint32_t)c * kChunkBytes, &tmB, nt * p.BN + 64 * c,
-                                    kt * kBK, fb);
+                        tma_load_2d(sm.b(s, p) + (uint32_t)c * CH, &tmB, nt * p.BN + 64 * c, kt * BK, fb);
                 }
                 issued_mask |= 1u << s;
                 issued_par = (issued_par & ~(1u << s)) | (ph << s);
@@ -279,12 +285,12 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     tc_fence_after();
                     const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < BK / 16; ++j) {
                         // 16 reduction rows per MMA: 32 bytes along a K-major row,
                         // 16 rows of 128 bytes in an MN-major chunk
-                        const uint64_t ad = WG ? desc_mnmajor_sw128(a0 + 2048u * j, kChunkBytes)
+                        const uint64_t ad = WG ? desc_mnmajor_sw128(a0 + 2048u * j, CH)
                                                : desc_kmajor_sw128(a0 + 32u * j);
-                        const uint64_t bd = desc_mnmajor_sw128(b0 + 2048u * j, kChunkBytes);
+                        const uint64_t bd = desc_mnmajor_sw128(b0 + 2048u * j, CH);
                         mma_bf16(d_tmem, ad, bd, p.idesc, (kt | j) != 0);
                     }
                     mma_commit(sm.empty(s));
@@ -342,10 +348,20 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     } else {
         // --------------------------------------------------------- transform
         constexpr int G = xform_groups(WG);
+        constexpr int GT = group_threads(WG);
         constexpr int HH = DR / 2;
+        // Work split of one stage: TPR threads per token row; each thread owns
+        // the pairs [k PPI, (k + 1) PPI) of the rope regions it takes (region j
+        // goes to the threads with (j * IPR + k) % TPR == sub).
+        constexpr int TPR = WG ? 4 : 2;
+        constexpr int PPI = (HH / TPR >= 8) ? HH / TPR : 8;  // pairs per item: 8 or 16
+        constexpr int IPR = HH / PPI;                        // items per region: 1, 2 or 4
         const int xt = threadIdx.x - kXformWarp0 * 32;
-        const int grp = xt / kGroupThreads;  // this thread's group
-        const int gt = xt % kGroupThreads;   // thread within the group
+        const int grp = xt / GT;  // this thread's group
+        const int gt = xt % GT;   // thread within the group
+        const int r = gt / TPR, sub = gt % TPR;
+        const int kpart = sub % IPR;
+        const int pb = kpart * PPI;  // first pair of this thread's items
         const bool vec = p.cs_vec != 0;
         int s = 0;
         uint32_t ph = 0;
@@ -355,24 +371,23 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             const int nt = tile % p.num_n_tiles;
             const bool do_db = WG && p.db != nullptr && nt == 0;
             float acc0 = 0.f, acc1 = 0.f;
-            // dgrad: this thread's token and its cos/sin row, cached for the whole tile
-            float c1[WG ? 1 : HH], s1[WG ? 1 : HH], c2[WG ? 1 : HH], s2[WG ? 1 : HH];
+            // cos/sin of this thread's pairs for its token (dgrad: fixed per tile)
+            float ci[PPI], si[PPI], cj[PPI], sj[PPI];
             int drow = -1;
-            // wgrad: the tile's rope regions and this thread's share of them
             int64_t reg[8];
             int nreg = 0;
             if (!WG) {
-                const int64_t t = (int64_t)mt * kBM + gt;
+                const int64_t t = (int64_t)mt * kBM + r;
                 if (t < p.T) drow = pos_row(p, t);
                 if (drow >= 0) {
-                    const float* cr = p.cos_tab + (int64_t)drow * p.cs_width;
-                    const float* sr = p.sin_tab + (int64_t)drow * p.cs_width;
+                    const float* cr = p.cos_tab + (int64_t)drow * p.cs_width + pb;
+                    const float* sr = p.sin_tab + (int64_t)drow * p.cs_width + pb;
 #pragma unroll
-                    for (int q = 0; q < HH; q += 8) {
-                        load8(cr + q, vec, c1 + (WG ? 0 : q));
-                        load8(sr + q, vec, s1 + (WG ? 0 : q));
-                        load8(cr + HH + q, vec, c2 + (WG ? 0 : q));
-                        load8(sr + HH + q, vec, s2 + (WG ? 0 : q));
+                    for (int q = 0; q < PPI; q += 8) {
+                        load8(cr + q, vec, ci + q);
+                        load8(sr + q, vec, si + q);
+                        load8(cr + HH + q, vec, cj + q);
+                        load8(sr + HH + q, vec, sj + q);
                     }
                 }
             } else {
@@ -391,31 +406,24 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     const bool ok = mbar_wait(sm.full(s), ph, abort_flag);
                     const uint32_t a0 = sm.a(s, p);
                     int64_t st[8];
-                    const int n = (ok && drow >= 0) ? rope_regions(p, (int64_t)kt * kBK, kBK, st) : 0;
+                    const int n = (ok && drow >= 0) ? rope_regions(p, (int64_t)kt * BK, BK, st) : 0;
                     for (int j = 0; j < n; ++j) {
-                        const int q0 = (int)(st[j] - (int64_t)kt * kBK) / 8;
+                        if ((j * IPR + kpart) % TPR != sub) continue;
+                        const int q0 = ((int)(st[j] - (int64_t)kt * BK) + pb) / 8;
 #pragma unroll
-                        for (int g = 0; g < HH / 8; ++g)
-                            rot8(a0 + (uint32_t)gt * 128, gt, q0 + g, q0 + g + HH / 8, c1 + (WG ? 0 : 8 * g),
-                                 s1 + (WG ? 0 : 8 * g), c2 + (WG ? 0 : 8 * g), s2 + (WG ? 0 : 8 * g));
+                        for (int g = 0; g < PPI / 8; ++g)
+                            rot8(a0 + (uint32_t)r * 128, r, q0 + g, q0 + g + HH / 8, ci + 8 * g, si + 8 * g,
+                                 cj + 8 * g, sj + 8 * g);
                         wrote = true;
                     }
-                    (void)ok;
                 } else {
-                    // two threads per token row; Dr = 64 splits each region's 32
-                    // pairs between them, narrower rope dims split the regions
-                    constexpr int PPI = HH < 16 ? HH : 16;  // pairs per item
-                    constexpr int IPR = HH / PPI;           // items per region
-                    const int r = gt >> 1, half = gt & 1;
-                    const int64_t t = (int64_t)kt * kBK + r;
-                    const int pb = (IPR == 2) ? PPI * half : 0;
+                    const int64_t t = (int64_t)kt * BK + r;
                     bool mine = false;
-                    for (int j = 0; j < nreg; ++j) mine |= (IPR == 2) || ((j & 1) == half);
+                    for (int j = 0; j < nreg; ++j) mine |= ((j * IPR + kpart) % TPR == sub);
                     int prow = -1;
-                    float ci[PPI], si[PPI], cj[PPI], sj[PPI];
                     if (mine && t < p.T) {
                         prow = pos_row(p, t);
-                        if (prow >= 0) {
+                        if (prow >= 0) {  // issued before the stage's data is awaited
                             const float* cr = p.cos_tab + (int64_t)prow * p.cs_width + pb;
                             const float* sr = p.sin_tab + (int64_t)prow * p.cs_width + pb;
 #pragma unroll
@@ -431,9 +439,9 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     if (ok && prow >= 0) {
                         const uint32_t a0 = sm.a(s, p);
                         for (int j = 0; j < nreg; ++j) {
-                            if (IPR == 1 && (j & 1) != half) continue;
+                            if ((j * IPR + kpart) % TPR != sub) continue;
                             const int o = (int)(reg[j] - (int64_t)mt * kBM);  // channel offset in the tile
-                            const uint32_t row = a0 + (uint32_t)(o / 64) * kChunkBytes + (uint32_t)r * 128;
+                            const uint32_t row = a0 + (uint32_t)(o / 64) * CH + (uint32_t)r * 128;
                             const int q0 = (o % 64 + pb) / 8;
 #pragma unroll
                             for (int g = 0; g < PPI / 8; ++g)
@@ -446,16 +454,17 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 if (wrote) fence_proxy_async_smem();
                 if (do_db) {
                     // per-channel sums of the (rotated) tile: thread = channel pair
-                    // pp of the 128, rows [32 rh, 32 rh + 32) of the 64 tokens
-                    named_bar_sync(1 + grp, kGroupThreads);
+                    // pp of the 128, rows [BK/2 rh, BK/2 (rh + 1)) of the stage
+                    named_bar_sync(1 + grp, GT);
                     const uint32_t a0 = sm.a(s, p);
-                    const int pp = gt & 63, rh = gt >> 6;
-                    const uint32_t cbase = a0 + (uint32_t)(pp >> 5) * kChunkBytes + (uint32_t)(pp & 3) * 4;
+                    const int pp = gt & 63, rh = (gt >> 6) & 1;
+                    const uint32_t cbase = a0 + (uint32_t)(pp >> 5) * CH + (uint32_t)(pp & 3) * 4;
                     const int q16 = (pp & 31) >> 2;
 #pragma unroll 8
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const int r = rh * 32 + rr;
-                        const uint32_t v = lds_b32(cbase + (uint32_t)r * 128 + (uint32_t)((q16 ^ (r & 7)) * 16));
+                    for (int rr = 0; rr < BK / 2; ++rr) {
+                        const int row = rh * (BK / 2) + rr;
+                        const uint32_t v =
+                            lds_b32(cbase + (uint32_t)row * 128 + (uint32_t)((q16 ^ (row & 7)) * 16));
                         acc0 += bf16lo_to_f32(v);
                         acc1 += bf16hi_to_f32(v);
                     }
@@ -469,11 +478,11 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             }
             if (do_db) {
                 // combine the 2G partial sums of each channel, write bf16 db
-                const int pp = gt & 63, rh = gt >> 6;
+                const int pp = gt & 63, rh = (gt >> 6) & 1;
                 const int part = grp * 2 + rh;
                 db_part[part * 128 + 2 * pp] = acc0;
                 db_part[part * 128 + 2 * pp + 1] = acc1;
-                named_bar_sync(1 + G, G * kGroupThreads);
+                named_bar_sync(1 + G, G * GT);
                 if (part == 0) {
                     float s0 = 0.f, s1v = 0.f;
                     for (int q = 0; q < 2 * G; ++q) {
@@ -487,7 +496,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     else if (n < p.N)
                         p.db[n] = (uint16_t)(packed & 0xFFFFu);
                 }
-                named_bar_sync(1 + G, G * kGroupThreads);
+                named_bar_sync(1 + G, G * GT);
             }
         }
     }
@@ -539,9 +548,12 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     p.num_m_tiles = (int)(((wg ? N : a.T) + kBM - 1) / kBM);
     p.num_n_tiles = (int)((a.K + p.BN - 1) / p.BN);
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
-    p.k_tiles = (int)(((wg ? a.T : N) + kBK - 1) / kBK);
-    p.a_bytes = kBM * 128;
-    p.stage_bytes = p.a_bytes + (uint32_t)p.BN * 128;
+    const int BK = bk_of(wg);
+    p.k_tiles = (int)(((wg ? a.T : N) + BK - 1) / BK);
+    // A: 128 token rows of 64 channels (dgrad) or two 64-channel chunks of BK
+    // token rows (wgrad); B: BN/64 chunks of BK rows
+    p.a_bytes = wg ? 2u * chunk_of(true) : (uint32_t)kBM * 128u;
+    p.stage_bytes = p.a_bytes + (uint32_t)(p.BN / 64) * chunk_of(wg);
     p.tx_bytes = p.stage_bytes;
     p.idesc = idesc_bf16(kBM, (uint32_t)p.BN, wg ? 1u : 0u, 1u);
     p.pos = a.pos;
@@ -565,7 +577,7 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
 
     const size_t fixed = 1024 + 4096;  // alignment slack + barriers, slots, bias partials
     int stages = (int)((size_t)(di.max_smem_optin - fixed) / p.stage_bytes);
-    if (stages > 8) stages = 8;
+    if (stages > 12) stages = 12;
     if (stages < 2) return MLA_ERR_UNSUPPORTED;
     p.stages = stages;
     const size_t smem = fixed + (size_t)stages * p.stage_bytes;
@@ -574,11 +586,11 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     if (!wg) {
         st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, kBM, true);
         if (st == MLA_OK)
-            st = make_tmap_2d(&tb, a.W, 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * 2, 64, kBK, true);
+            st = make_tmap_2d(&tb, a.W, 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * 2, 64, BK, true);
     } else {
-        st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, kBK, true);
+        st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, BK, true);
         if (st == MLA_OK)
-            st = make_tmap_2d(&tb, a.x, 1, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, kBK, true);
+            st = make_tmap_2d(&tb, a.x, 1, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, BK, true);
     }
     if (st != MLA_OK) return st;
     const int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;

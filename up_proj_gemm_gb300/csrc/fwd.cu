@@ -35,15 +35,14 @@ namespace mlaq {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;  // TMEM column offset of accumulator buffer 1
 constexpr uint32_t kSfCol0 = 448;     // first TMEM column of the per-stage scale factors
 constexpr uint32_t kSfColsPerStage = 12;  // 4 (A: 128 rows) + 8 (B: up to 256 rows)
 constexpr uint32_t kSfBytesPerStage = 512 + 1024;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, splitting the tile's units
 constexpr int kSlotCh = 16;       // channels per slot (one TMA store box: 16 channels x 32 rows)
-constexpr uint32_t kBiasBytes = 512;  // 256 bf16 channels per tile, double-buffered
 
 struct FwdParams {
     int T, H, N, D, Dn;
@@ -71,8 +70,7 @@ struct FwdParams {
 struct Smem {
     uint32_t base;      // shared address of stage 0 (1024-aligned)
     uint32_t sf;        // scale staging (MXFP8 weights)
-    uint32_t out;       // output staging: kEpiWarps x kSlots slots
-    uint32_t bias;      // 2 x kBiasBytes
+    uint32_t out;       // output staging: kEpiWarps x nslots slots
     uint32_t bars;      // mbarriers
     int S;
     __device__ uint32_t a(int s, const FwdParams& p) const { return base + (uint32_t)s * p.stage_bytes; }
@@ -93,7 +91,7 @@ struct Smem {
 // boxes and the LSU queue carries no per-row stores.
 struct EpiCtx {
     uint32_t slots;   // this warp's staging ring
-    uint32_t bias_s;  // this warp's copy of the tile's bias (bf16), 0 if none
+    const uint16_t* bias;  // the tile's bias (bf16, 16-byte aligned rows of 8), or null
     int cursor;       // next free slot (counts pieces; taken modulo nslots)
     int prev_pieces;  // pieces of the previous unit (its store may still read)
     int32_t t0;       // first token row of this warp's 32-row slab
@@ -103,9 +101,9 @@ __device__ __forceinline__ uint32_t slot_addr(const FwdParams& p, const EpiCtx& 
     return c.slots + (uint32_t)(k % p.nslots) * p.slot_bytes;
 }
 
-__device__ __forceinline__ void add_bias(float* v, int nv, uint32_t bias_s) {
+__device__ __forceinline__ void add_bias(float* v, int nv, const uint16_t* bias) {
     for (int k = 0; k < nv / 8; ++k) {
-        const uint4 b = lds_v4(bias_s + 16u * k);
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias) + k);  // same address in every lane
         v[8 * k + 0] += bf16lo_to_f32(b.x);
         v[8 * k + 1] += bf16hi_to_f32(b.x);
         v[8 * k + 2] += bf16lo_to_f32(b.y);
@@ -183,7 +181,7 @@ __device__ __forceinline__ void nope_unit(const FwdParams& p, const CUtensorMap*
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-    if (c.bias_s) add_bias(v, 32, c.bias_s + 2u * col);
+    if (c.bias) add_bias(v, 32, c.bias + col);
     emit_unit<MXOUT, 32>(p, tmC, c, v, valid, t, n, h, cin);
 }
 
@@ -212,7 +210,7 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
     float y[DR];
 #pragma unroll
     for (int i = 0; i < DR; ++i) y[i] = __uint_as_float(r[i / 16][i % 16]);
-    if (c.bias_s) add_bias(y, DR, c.bias_s + 2u * col);
+    if (c.bias) add_bias(y, DR, c.bias + col);
     const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
     const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
     const bool vec = p.cs_vec != 0;
@@ -246,8 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.base = (raw + 1023u) & ~1023u;
     sm.sf = sm.base + (uint32_t)p.stages * p.stage_bytes;
     sm.out = sm.sf + (MXW ? (uint32_t)p.stages * kSfBytesPerStage : 0u);
-    sm.bias = sm.out + (uint32_t)(kEpiWarps * p.nslots) * p.slot_bytes;
-    sm.bars = sm.bias + kEpiWarps * kBiasBytes;
+    sm.bars = sm.out + (uint32_t)(kEpiWarps * p.nslots) * p.slot_bytes;
     uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (2 * p.stages + 5);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
@@ -262,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.tfull(b), 1);
-            mbar_init(sm.tempty(b), 4);
+            mbar_init(sm.tempty(b), kEpiWarps);
         }
         mbar_init(sm.drain(), 1);
         *abort_flag = 0;
@@ -403,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ec.slots = sm.out + (uint32_t)(ew * p.nslots) * p.slot_bytes;
         ec.cursor = 0;
         ec.prev_pieces = 0;
-        const uint32_t bias_buf = sm.bias + (uint32_t)ew * kBiasBytes;
+        const int half = ew >> 2;   // which of the tile's units this warp takes (alternating)
         int local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
             const int b = local & 1;
@@ -423,29 +420,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
             const int64_t n0 = (int64_t)nt * p.BN;
             ec.t0 = mt * kBM + quad * 32;
-            ec.bias_s = 0;
-            if (p.bias) {
-                // this warp's copy of the tile's bias: lane l holds channels 2l, 2l+1 of each 64
-                __syncwarp();  // previous tile's reads of the buffer are done
-                for (int k = 2 * lane; k < p.BN; k += 64)
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(bias_buf + 2u * k),
-                                 "r"(__ldg(reinterpret_cast<const uint32_t*>(p.bias + n0 + k)))
-                                 : "memory");
-                __syncwarp();
-                ec.bias_s = bias_buf;
-            }
-            int col = 0;
+            ec.bias = p.bias ? p.bias + n0 : nullptr;
+            int col = 0, unit = 0;
             while (col < p.BN) {
                 const int64_t n = n0 + col;
                 const int h = (int)(n / p.D);
                 const int c = (int)(n - (int64_t)h * p.D);
-                if (c < p.Dn) {
-                    nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
-                    col += 32;
-                } else {
-                    rope_unit<MXOUT, DR>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
-                    col += DR;
+                const bool nope = c < p.Dn;
+                if ((unit++ & 1) == half) {
+                    if (nope) nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
+                    else rope_unit<MXOUT, DR>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
                 }
+                col += nope ? 32 : DR;
             }
             tc_fence_before();
             __syncwarp();
@@ -547,10 +533,10 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
                (reinterpret_cast<uintptr_t>(a.sin_tab) % 16 == 0);
     const bool mxo = a.out_mode == MLA_OUT_MXFP8;
     p.slot_bytes = 32u * kSlotCh * (mxo ? 1u : 2u);
-    p.nslots = mxo ? 8 : 6;  // a unit takes at most 4 slots (64 rope channels)
+    p.nslots = mxo ? 8 : 4;  // a unit takes at most 4 slots (64 rope channels)
 
     const size_t fixed = 1024 /* alignment slack */ + 256 /* barriers + slots */ +
-                         (size_t)kEpiWarps * p.nslots * p.slot_bytes + kEpiWarps * kBiasBytes;
+                         (size_t)kEpiWarps * p.nslots * p.slot_bytes;
     const size_t per_stage = p.stage_bytes + (mxw ? kSfBytesPerStage : 0);
     int stages = (int)((size_t)(di.max_smem_optin - fixed) / per_stage);
     if (stages > 8) stages = 8;
