@@ -75,6 +75,7 @@ struct BwdParams {
     const float* sin_tab;
     long long cs_rows, cs_width;
     int cs_vec;  // cos/sin rows 16-byte aligned: float4 loads
+    int a3d, b3d;  // operand maps are 3-D chunk views (one TMA op per operand and stage)
     uint16_t* out;
     int out_rows, out_cols;
     uint16_t* db;
@@ -86,12 +87,17 @@ struct Smem {
     int S;
     __device__ uint32_t a(int s, const BwdParams& p) const { return base + (uint32_t)s * p.stage_bytes; }
     __device__ uint32_t b(int s, const BwdParams& p) const { return a(s, p) + p.a_bytes; }
+    // full: TMA landed (stages the transform does not touch; awaited by the MMA)
+    // xfull: TMA landed (transform stages; one set per transform group, awaited
+    //        only by that group, so every barrier sees its uses in order)
+    // ready: transform done (awaited by the MMA); empty: MMA done (producer)
     __device__ uint32_t full(int s) const { return bars + 8u * s; }
     __device__ uint32_t ready(int s) const { return bars + 8u * (S + s); }
     __device__ uint32_t empty(int s) const { return bars + 8u * (2 * S + s); }
     __device__ uint32_t tfull(int b) const { return bars + 8u * (3 * S + b); }
     __device__ uint32_t tempty(int b) const { return bars + 8u * (3 * S + 2 + b); }
     __device__ uint32_t drain() const { return bars + 8u * (3 * S + 4); }
+    __device__ uint32_t xfull(int g, int s) const { return bars + 8u * (3 * S + 5 + g * S + s); }
 };
 
 __device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&v)[4]) {
@@ -124,15 +130,27 @@ __device__ __forceinline__ void load8(const float* p, bool vec, float* v) {
 
 // Start channels of the rope regions inside [n0, n0 + width). Rope regions
 // are Dr-aligned and Dr <= 64 divides 64, so none straddles a 64-channel row
-// or a 128-channel tile.
-__device__ __forceinline__ int rope_regions(const BwdParams& p, int64_t n0, int width, int64_t (&st)[8]) {
+// or a 128-channel tile. (N < 2^31: 32-bit arithmetic.)
+__device__ __forceinline__ int rope_regions(const BwdParams& p, int n0, int width, int (&st)[8]) {
     int cnt = 0;
-    for (int64_t h = n0 / p.D; cnt < 8; ++h) {
-        const int64_t rs = h * p.D + p.Dn;
-        if (rs >= n0 + width || rs >= p.N) break;
+    for (int rs = (n0 / p.D) * p.D + p.Dn; cnt < 8 && rs < n0 + width && rs < p.N; rs += p.D)
         if (rs >= n0) st[cnt++] = rs;
-    }
     return cnt;
+}
+
+__device__ __forceinline__ bool has_rope(const BwdParams& p, int n0, int width) {
+    int rs = (n0 / p.D) * p.D + p.Dn;
+    if (rs < n0) rs += p.D;
+    return rs < n0 + width && rs < p.N;
+}
+
+// Whether a stage goes through the transform warps (else TMA -> MMA directly):
+// dgrad stages whose 64 channels hold rope channels; every stage of a wgrad
+// tile that holds rope channels or sums the bias gradient.
+template <bool WG>
+__device__ __forceinline__ bool stage_needs_xform(const BwdParams& p, int mt, int nt, int kt) {
+    if (WG) return has_rope(p, mt * 128, 128) || (p.db != nullptr && nt == 0);
+    return has_rope(p, kt * bk_of(false), bk_of(false));
 }
 
 // Inverse RoPE on 8 pairs of one token, in place in a 128-byte swizzled
@@ -181,7 +199,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     sm.S = p.stages;
     sm.base = (raw + 1023u) & ~1023u;
     sm.bars = sm.base + (uint32_t)p.stages * p.stage_bytes;
-    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (3 * p.stages + 5);
+    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * ((3 + xform_groups(WG)) * p.stages + 5);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
     float* db_part = reinterpret_cast<float*>(tail + 16);  // 2 x groups x 128 floats (wgrad bias sums)
@@ -194,6 +212,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             mbar_init(sm.full(s), 1);
             mbar_init(sm.ready(s), group_threads(WG) / 32);
             mbar_init(sm.empty(s), 1);
+            for (int g = 0; g < xform_groups(WG); ++g) mbar_init(sm.xfull(g, s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.tfull(b), 1);
@@ -223,7 +242,9 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         // ------------------------------------------------------ TMA producer
         int s = 0;
         uint32_t ph = 0;
-        uint32_t issued_mask = 0, issued_par = 0;
+        int tcount = 0;  // transform stages so far (group tcount % G owns the next)
+        uint32_t fpar = 0, xpar[xform_groups(WG)] = {};  // per-slot parity of each barrier's next use
+        uint32_t last_bar[16], last_par = 0, issued_mask = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
             const int mt = tile / p.num_n_tiles;
@@ -233,23 +254,40 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     ok = false;
                     break;
                 }
+                uint32_t fb, par;
+                if (stage_needs_xform<WG>(p, mt, nt, kt)) {
+                    const int g = tcount++ % xform_groups(WG);
+                    fb = sm.xfull(g, s);
+                    par = (xpar[g] >> s) & 1u;
+                    xpar[g] ^= 1u << s;
+                } else {
+                    fb = sm.full(s);
+                    par = (fpar >> s) & 1u;
+                    fpar ^= 1u << s;
+                }
+                last_bar[s] = fb;  // the phase this use completes (for unwinding)
+                last_par = (last_par & ~(1u << s)) | (par << s);
                 if (lane == 0) {
-                    const uint32_t fb = sm.full(s);
                     mbar_arrive_expect_tx(fb, p.tx_bytes);
                     if (!WG) {
                         // A: dq rows [mt*128, +128) x channels [kt*64, +64)
                         tma_load_2d(sm.a(s, p), &tmA, kt * BK, mt * kBM, fb);
+                    } else if (p.a3d) {
+                        // A: dq^T, both 64-channel chunks of the tile, tokens [kt*BK, +BK)
+                        tma_load_3d(sm.a(s, p), &tmA, 0, kt * BK, mt * 2, fb);
                     } else {
-                        // A: dq channels [mt*128 + 64c, +64) x tokens [kt*64, +64)
                         tma_load_2d(sm.a(s, p), &tmA, mt * kBM, kt * BK, fb);
                         tma_load_2d(sm.a(s, p) + CH, &tmA, mt * kBM + 64, kt * BK, fb);
                     }
                     // B: 64-column chunks of W (dgrad, rows = channels) or x (wgrad, rows = tokens)
-                    for (int c = 0; c < nb_chunks; ++c)
-                        tma_load_2d(sm.b(s, p) + (uint32_t)c * CH, &tmB, nt * p.BN + 64 * c, kt * BK, fb);
+                    if (p.b3d) {
+                        tma_load_3d(sm.b(s, p), &tmB, 0, kt * BK, nt * nb_chunks, fb);
+                    } else {
+                        for (int c = 0; c < nb_chunks; ++c)
+                            tma_load_2d(sm.b(s, p) + (uint32_t)c * CH, &tmB, nt * p.BN + 64 * c, kt * BK, fb);
+                    }
                 }
                 issued_mask |= 1u << s;
-                issued_par = (issued_par & ~(1u << s)) | (ph << s);
                 if (++s == p.stages) {
                     s = 0;
                     ph ^= 1u;
@@ -257,9 +295,11 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             }
         }
         if (!ok) {
+            // unwinding: let every copy this warp started land before the CTA
+            // exits (bounded; the last use of each slot's barrier)
             for (int q = 0; q < p.stages; ++q)
                 if (issued_mask & (1u << q))
-                    mbar_wait(sm.full(q), (issued_par >> q) & 1u, nullptr, 200000000ull);
+                    mbar_wait(last_bar[q], (last_par >> q) & 1u, nullptr, 200000000ull);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -267,6 +307,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             int s = 0;
             uint32_t ph = 0;
             int local = 0;
+            uint32_t rpar = 0, fpar = 0;  // per-slot parities of the ready / full barriers
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
                 const int b = local & 1;
@@ -277,11 +318,19 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)b * kAccStride;
+                const int mt = tile / p.num_n_tiles;
+                const int nt = tile % p.num_n_tiles;
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
-                    if (!mbar_wait(sm.ready(s), ph, abort_flag)) {
+                    const bool xf = stage_needs_xform<WG>(p, mt, nt, kt);
+                    // transform stages: wait for the transform's release; others: the TMA
+                    const uint32_t bar = xf ? sm.ready(s) : sm.full(s);
+                    const uint32_t par = ((xf ? rpar : fpar) >> s) & 1u;
+                    if (!mbar_wait(bar, par, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    if (xf) rpar ^= 1u << s;
+                    else fpar ^= 1u << s;
                     tc_fence_after();
                     const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
 #pragma unroll
@@ -364,8 +413,8 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         const int pb = kpart * PPI;  // first pair of this thread's items
         const bool vec = p.cs_vec != 0;
         int s = 0;
-        uint32_t ph = 0;
-        int kglob = 0;  // stage counter over all tiles: group kglob % G owns the stage
+        uint32_t xpar = 0;  // per-slot parity of this group's next barrier use
+        int tcount = 0;     // transform stages so far: group tcount % G owns the next one
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
             const int mt = tile / p.num_n_tiles;
             const int nt = tile % p.num_n_tiles;
@@ -374,7 +423,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             // cos/sin of this thread's pairs for its token (dgrad: fixed per tile)
             float ci[PPI], si[PPI], cj[PPI], sj[PPI];
             int drow = -1;
-            int64_t reg[8];
+            int reg[8];
             int nreg = 0;
             if (!WG) {
                 const int64_t t = (int64_t)mt * kBM + r;
@@ -391,25 +440,26 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     }
                 }
             } else {
-                nreg = rope_regions(p, (int64_t)mt * kBM, kBM, reg);
+                nreg = rope_regions(p, mt * kBM, kBM, reg);
             }
-            for (int kt = 0; kt < p.k_tiles; ++kt, ++kglob) {
-                if (kglob % G != grp) {
-                    if (++s == p.stages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                const bool skip = !stage_needs_xform<WG>(p, mt, nt, kt) || (tcount++ % G) != grp;
+                if (skip) {
+                    if (++s == p.stages) s = 0;
                     continue;
                 }
+                const uint32_t xbar = sm.xfull(grp, s);
+                const uint32_t xp = (xpar >> s) & 1u;
+                xpar ^= 1u << s;
                 bool wrote = false;
                 if (!WG) {
-                    const bool ok = mbar_wait(sm.full(s), ph, abort_flag);
+                    const bool ok = mbar_wait(xbar, xp, abort_flag);
                     const uint32_t a0 = sm.a(s, p);
-                    int64_t st[8];
-                    const int n = (ok && drow >= 0) ? rope_regions(p, (int64_t)kt * BK, BK, st) : 0;
+                    int st[8];
+                    const int n = (ok && drow >= 0) ? rope_regions(p, kt * BK, BK, st) : 0;
                     for (int j = 0; j < n; ++j) {
                         if ((j * IPR + kpart) % TPR != sub) continue;
-                        const int q0 = ((int)(st[j] - (int64_t)kt * BK) + pb) / 8;
+                        const int q0 = (st[j] - kt * BK + pb) / 8;
 #pragma unroll
                         for (int g = 0; g < PPI / 8; ++g)
                             rot8(a0 + (uint32_t)r * 128, r, q0 + g, q0 + g + HH / 8, ci + 8 * g, si + 8 * g,
@@ -435,12 +485,12 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                             }
                         }
                     }
-                    const bool ok = mbar_wait(sm.full(s), ph, abort_flag);
+                    const bool ok = mbar_wait(xbar, xp, abort_flag);
                     if (ok && prow >= 0) {
                         const uint32_t a0 = sm.a(s, p);
                         for (int j = 0; j < nreg; ++j) {
                             if ((j * IPR + kpart) % TPR != sub) continue;
-                            const int o = (int)(reg[j] - (int64_t)mt * kBM);  // channel offset in the tile
+                            const int o = reg[j] - mt * kBM;  // channel offset in the tile
                             const uint32_t row = a0 + (uint32_t)(o / 64) * CH + (uint32_t)r * 128;
                             const int q0 = (o % 64 + pb) / 8;
 #pragma unroll
@@ -471,10 +521,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.ready(s));
-                if (++s == p.stages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                if (++s == p.stages) s = 0;
             }
             if (do_db) {
                 // combine the 2G partial sums of each channel, write bf16 db
@@ -583,13 +630,20 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     const size_t smem = fixed + (size_t)stages * p.stage_bytes;
 
     alignas(64) CUtensorMap ta, tb;
+    // one TMA operation per MN-major operand and stage when its columns come
+    // in whole 64-element chunks; else one per chunk
     if (!wg) {
         st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, kBM, true);
-        if (st == MLA_OK)
+        p.b3d = (a.K % 64 == 0) &&
+                make_tmap_chunks(&tb, a.W, (uint64_t)N, (uint64_t)a.K, BK, (uint32_t)(p.BN / 64)) == MLA_OK;
+        if (st == MLA_OK && !p.b3d)
             st = make_tmap_2d(&tb, a.W, 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * 2, 64, BK, true);
     } else {
-        st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, BK, true);
-        if (st == MLA_OK)
+        p.a3d = (N % 128 == 0) && make_tmap_chunks(&ta, a.dq, (uint64_t)a.T, (uint64_t)N, BK, 2) == MLA_OK;
+        if (!p.a3d) st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, BK, true);
+        p.b3d = (a.K % 64 == 0) &&
+                make_tmap_chunks(&tb, a.x, (uint64_t)a.T, (uint64_t)a.K, BK, (uint32_t)(p.BN / 64)) == MLA_OK;
+        if (st == MLA_OK && !p.b3d)
             st = make_tmap_2d(&tb, a.x, 1, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, BK, true);
     }
     if (st != MLA_OK) return st;

@@ -55,6 +55,9 @@ struct FwdParams {
     uint32_t slot_bytes;  // 32 rows x 16 channels x output element size
     int cs_vec;           // cos/sin rows 16-byte aligned: float4 loads
     int nslots;           // staging slots per epilogue warp
+    int split_half;       // the two warps of a lane quadrant take the tile's two halves and
+                          // write each row's scale bytes as one 4-byte word (else: units
+                          // alternate between them and scales go byte by byte)
     const uint16_t* bias;
     const float* cos_tab;
     const float* sin_tab;
@@ -95,6 +98,8 @@ struct EpiCtx {
     int cursor;       // next free slot (counts pieces; taken modulo nslots)
     int prev_pieces;  // pieces of the previous unit (its store may still read)
     int32_t t0;       // first token row of this warp's 32-row slab
+    uint32_t sword;   // packed scale bytes of this row's half tile (split_half)
+    int64_t sbase;    // first 32-channel block index of that half
 };
 
 __device__ __forceinline__ uint32_t slot_addr(const FwdParams& p, const EpiCtx& c, int k) {
@@ -145,7 +150,10 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
             if (nvalid > 16)
                 sts_v4(slot_addr(p, c, first + 2 * blk + 1) + 16u * lane, codes[4], codes[5], codes[6],
                        codes[7]);
-            if (valid) p.q_scales[(t * p.H + h) * NB + (cin + blk * 32) / 32] = (uint8_t)sb;
+            if (p.split_half)
+                c.sword |= sb << (8 * (int)((n + 32 * blk) / 32 - c.sbase));
+            else if (valid)
+                p.q_scales[(t * p.H + h) * NB + (cin + blk * 32) / 32] = (uint8_t)sb;
         }
     } else {
 #pragma unroll
@@ -421,18 +429,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t n0 = (int64_t)nt * p.BN;
             ec.t0 = mt * kBM + quad * 32;
             ec.bias = p.bias ? p.bias + n0 : nullptr;
-            int col = 0, unit = 0;
-            while (col < p.BN) {
+            ec.sword = 0;
+            ec.sbase = (n0 + (p.split_half ? half * (p.BN / 2) : 0)) / 32;
+            int col = p.split_half ? half * (p.BN / 2) : 0, unit = 0;
+            const int col_end = p.split_half ? col + p.BN / 2 : p.BN;
+            while (col < col_end) {
                 const int64_t n = n0 + col;
                 const int h = (int)(n / p.D);
                 const int c = (int)(n - (int64_t)h * p.D);
                 const bool nope = c < p.Dn;
-                if ((unit++ & 1) == half) {
+                if (p.split_half || (unit++ & 1) == half) {
                     if (nope) nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
                     else rope_unit<MXOUT, DR>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
                 }
                 col += nope ? 32 : DR;
             }
+            if (MXOUT && p.split_half && valid)
+                *reinterpret_cast<uint32_t*>(p.q_scales + t * (p.N / 32) + ec.sbase) = ec.sword;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.tempty(b));
@@ -534,6 +547,9 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     const bool mxo = a.out_mode == MLA_OUT_MXFP8;
     p.slot_bytes = 32u * kSlotCh * (mxo ? 1u : 2u);
     p.nslots = mxo ? 8 : 4;  // a unit takes at most 4 slots (64 rope channels)
+    p.split_half = mxo && D % 32 == 0 && BN % 128 == 0 && N % 128 == 0 &&
+                   reinterpret_cast<uintptr_t>(a.q_scales) % 4 == 0 &&
+                   fwd_tile_n(N, D, a.Dn, a.Dr, BN / 2, BN / 2) == BN / 2;
 
     const size_t fixed = 1024 /* alignment slack */ + 256 /* barriers + slots */ +
                          (size_t)kEpiWarps * p.nslots * p.slot_bytes;

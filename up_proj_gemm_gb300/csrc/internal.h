@@ -25,6 +25,14 @@ int make_tmap_2d(void* tmap_out /* CUtensorMap, 64 B aligned */, const void* bas
                  uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner,
                  uint32_t box_outer, bool swizzle128);
 
+// 3-D view of a row-major bf16 matrix [rows, cols] as 64-column chunks:
+// dims {64, rows, cols / 64} with strides {row pitch, 128 bytes}; a box
+// {64, box_rows, box_chunks} lands in shared memory as box_chunks
+// consecutive [box_rows][64] blocks (128-byte swizzle), the MN-major
+// operand layout of the tensor cores. cols must be a multiple of 64.
+int make_tmap_chunks(void* tmap_out, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_chunks);
+
 // ------------------------------------------------------------- launchers
 // All launchers assume arguments were validated by the API layer.
 int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,

@@ -64,19 +64,17 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) {
 // Quantize n <= 32 fp32 values held by ONE thread (a whole block) into codes
 // (packed little-endian, 4 per word) and return the scale byte. Entries past
 // n are ignored for the amax and encoded anyway (callers do not store them).
+// The amax is taken on the magnitude bits as integers: for non-negative
+// floats the integer order is the float order, and any Inf/NaN magnitude is
+// >= 0x7F800000, so one max finds both the amax and a non-finite element.
 template <int NV>
 __device__ __forceinline__ uint32_t quantize_block_regs(const float (&v)[NV], int n,
                                                         uint32_t (&codes)[(NV + 3) / 4]) {
-    float amax = 0.f;
-    bool bad = false;
+    uint32_t mbits = 0;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        if (i < n) {
-            bad |= not_finite(v[i]);
-            amax = fmaxf(amax, fabsf(v[i]));
-        }
-    }
-    if (bad) {
+    for (int i = 0; i < NV; ++i)
+        if (i < n) mbits = max(mbits, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    if (mbits >= 0x7F800000u) {
 #pragma unroll
         for (int w = 0; w < (NV + 3) / 4; ++w) {
             uint32_t c = 0;
@@ -87,7 +85,7 @@ __device__ __forceinline__ uint32_t quantize_block_regs(const float (&v)[NV], in
         }
         return 0xFFu;
     }
-    const int e = e8m0_exponent_f32(amax);
+    const int e = e8m0_exponent_f32(__uint_as_float(mbits));
     const float s = exp2_neg(e);
 #pragma unroll
     for (int w = 0; w < (NV + 3) / 4; ++w) {
