@@ -144,14 +144,34 @@ __device__ __forceinline__ bool has_rope(const BwdParams& p, int n0, int width) 
     return rs < n0 + width && rs < p.N;
 }
 
-// Whether a stage goes through the transform warps (else TMA -> MMA directly):
-// dgrad stages whose 64 channels hold rope channels; every stage of a wgrad
-// tile that holds rope channels or sums the bias gradient.
+// Walks a CTA's stages (its tiles, each k-tile of each) and says which go
+// through the transform warps (else TMA -> MMA directly): dgrad stages whose
+// 64 channels hold rope channels; every stage of a wgrad tile that holds
+// rope channels or sums the bias gradient. Incremental: no division per
+// stage, since the producer's loop paces the whole pipeline.
 template <bool WG>
-__device__ __forceinline__ bool stage_needs_xform(const BwdParams& p, int mt, int nt, int kt) {
-    if (WG) return has_rope(p, mt * 128, 128) || (p.db != nullptr && nt == 0);
-    return has_rope(p, kt * bk_of(false), bk_of(false));
-}
+struct StageWalk {
+    int mt = 0, nt = 0;
+    bool tile_x = false;  // wgrad: the tile's stages are transform stages
+    int c0 = 0;           // dgrad: channel phase (kt * 64) mod D of the current stage
+    __device__ void begin_tile(const BwdParams& p, int tile) {
+        mt = tile / p.num_n_tiles;
+        nt = tile % p.num_n_tiles;
+        c0 = 0;
+        if (WG) tile_x = has_rope(p, mt * kBM, kBM) || (p.db != nullptr && nt == 0);
+    }
+    __device__ bool needs(const BwdParams& p, int kt) const {
+        if (WG) return tile_x;
+        const int off = (c0 <= p.Dn) ? (p.Dn - c0) : (p.D + p.Dn - c0);  // next rope region start
+        return off < bk_of(false) && kt * bk_of(false) + off < p.N;
+    }
+    __device__ void next(const BwdParams& p) {
+        if (!WG) {
+            c0 += bk_of(false);
+            while (c0 >= p.D) c0 -= p.D;
+        }
+    }
+};
 
 // Inverse RoPE on 8 pairs of one token, in place in a 128-byte swizzled
 // shared-memory row (row index r inside its 1024-byte swizzle group gives
@@ -242,31 +262,35 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         // ------------------------------------------------------ TMA producer
         int s = 0;
         uint32_t ph = 0;
-        int tcount = 0;  // transform stages so far (group tcount % G owns the next)
-        uint32_t fpar = 0, xpar[xform_groups(WG)] = {};  // per-slot parity of each barrier's next use
-        uint32_t last_bar[16], last_par = 0, issued_mask = 0;
+        int gnext = 0;  // group owning the next transform stage
+        // per-slot parity of each barrier's next use (full, and xfull of groups 0..2),
+        // and which barrier each slot's last use went to (2 bits: 0 full, g+1 xfull g)
+        uint32_t fpar = 0, xp0 = 0, xp1 = 0, xp2 = 0, last_kind = 0, issued_mask = 0;
+        StageWalk<WG> walk;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            const int mt = tile / p.num_n_tiles;
-            const int nt = tile % p.num_n_tiles;
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
+            walk.begin_tile(p, tile);
+            const int mt = walk.mt, nt = walk.nt;
+            for (int kt = 0; kt < p.k_tiles; ++kt, walk.next(p)) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
-                uint32_t fb, par;
-                if (stage_needs_xform<WG>(p, mt, nt, kt)) {
-                    const int g = tcount++ % xform_groups(WG);
+                uint32_t fb;
+                uint32_t kind = 0;
+                if (walk.needs(p, kt)) {
+                    const int g = gnext;
+                    gnext = (gnext + 1 == xform_groups(WG)) ? 0 : gnext + 1;
                     fb = sm.xfull(g, s);
-                    par = (xpar[g] >> s) & 1u;
-                    xpar[g] ^= 1u << s;
+                    if (g == 0) xp0 ^= 1u << s;
+                    else if (g == 1) xp1 ^= 1u << s;
+                    else xp2 ^= 1u << s;
+                    kind = (uint32_t)g + 1;
                 } else {
                     fb = sm.full(s);
-                    par = (fpar >> s) & 1u;
                     fpar ^= 1u << s;
                 }
-                last_bar[s] = fb;  // the phase this use completes (for unwinding)
-                last_par = (last_par & ~(1u << s)) | (par << s);
+                last_kind = (last_kind & ~(3u << (2 * s))) | (kind << (2 * s));
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, p.tx_bytes);
                     if (!WG) {
@@ -297,9 +321,14 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         if (!ok) {
             // unwinding: let every copy this warp started land before the CTA
             // exits (bounded; the last use of each slot's barrier)
-            for (int q = 0; q < p.stages; ++q)
-                if (issued_mask & (1u << q))
-                    mbar_wait(last_bar[q], (last_par >> q) & 1u, nullptr, 200000000ull);
+            for (int q = 0; q < p.stages; ++q) {
+                if (!(issued_mask & (1u << q))) continue;
+                const uint32_t k = (last_kind >> (2 * q)) & 3u;
+                const uint32_t bits = k == 0 ? fpar : (k == 1 ? xp0 : (k == 2 ? xp1 : xp2));
+                // the last use toggled its bit: its phase has the other parity
+                mbar_wait(k == 0 ? sm.full(q) : sm.xfull((int)k - 1, q), ((bits >> q) & 1u) ^ 1u, nullptr,
+                          200000000ull);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -308,6 +337,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             uint32_t ph = 0;
             int local = 0;
             uint32_t rpar = 0, fpar = 0;  // per-slot parities of the ready / full barriers
+            StageWalk<WG> walk;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
                 const int b = local & 1;
@@ -318,10 +348,9 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)b * kAccStride;
-                const int mt = tile / p.num_n_tiles;
-                const int nt = tile % p.num_n_tiles;
-                for (int kt = 0; kt < p.k_tiles; ++kt) {
-                    const bool xf = stage_needs_xform<WG>(p, mt, nt, kt);
+                walk.begin_tile(p, tile);
+                for (int kt = 0; kt < p.k_tiles; ++kt, walk.next(p)) {
+                    const bool xf = walk.needs(p, kt);
                     // transform stages: wait for the transform's release; others: the TMA
                     const uint32_t bar = xf ? sm.ready(s) : sm.full(s);
                     const uint32_t par = ((xf ? rpar : fpar) >> s) & 1u;
@@ -414,11 +443,13 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         const bool vec = p.cs_vec != 0;
         int s = 0;
         uint32_t xpar = 0;  // per-slot parity of this group's next barrier use
-        int tcount = 0;     // transform stages so far: group tcount % G owns the next one
+        int gnext = 0;      // group owning the next transform stage
+        StageWalk<WG> walk;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
             const int mt = tile / p.num_n_tiles;
             const int nt = tile % p.num_n_tiles;
             const bool do_db = WG && p.db != nullptr && nt == 0;
+            walk.begin_tile(p, tile);
             float acc0 = 0.f, acc1 = 0.f;
             // cos/sin of this thread's pairs for its token (dgrad: fixed per tile)
             float ci[PPI], si[PPI], cj[PPI], sj[PPI];
@@ -443,7 +474,13 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 nreg = rope_regions(p, mt * kBM, kBM, reg);
             }
             for (int kt = 0; kt < p.k_tiles; ++kt) {
-                const bool skip = !stage_needs_xform<WG>(p, mt, nt, kt) || (tcount++ % G) != grp;
+                const bool nx = walk.needs(p, kt);
+                walk.next(p);
+                bool skip = !nx;
+                if (nx) {
+                    skip = gnext != grp;
+                    gnext = (gnext + 1 == G) ? 0 : gnext + 1;
+                }
                 if (skip) {
                     if (++s == p.stages) s = 0;
                     continue;
