@@ -143,8 +143,15 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_
  * tiles on their way into the tensor cores; dq_pre is never stored.
  *   dq [T, H, D] bf16, W [N, K] bf16 (the bf16 master weight), dx [T, K] bf16
  *   (fp32 accumulation). cos_tab/sin_tab/pos as in the forward.
- *   workspace/ws_bytes: see mla_q_uproj_workspace_size (may be NULL/0 when the
- *   size query returns 0).
+ *   workspace/ws_bytes: device scratch of at least
+ *   mla_q_uproj_workspace_size(shape, 1) bytes, 16-byte aligned, not
+ *   overlapping any input or output (NULL/0 when the query returns 0). When
+ *   the tiles of dx are too few to fill the GPU's SMs evenly, each tile's
+ *   reduction over channels is split into parts that write fp32 partial
+ *   sums there; a second kernel on the same stream adds them in a fixed
+ *   order (results do not depend on scheduling) and rounds to bf16. The
+ *   contents need no initialization and are garbage afterwards; calls that
+ *   share a workspace must not overlap on the GPU.
  * Requires K % 8 == 0, Dr in {16, 32, 64}, Dn % Dr == 0, and 16-byte aligned
  * pointers.
  */
@@ -184,7 +191,9 @@ MLAQ_API int mxfp8_quantize_rows(int64_t R, int64_t C, int in_dtype, const void 
                                  int64_t ld_in, uint8_t *codes, uint8_t *scales, void *stream);
 
 /* which: 0 = forward, 1 = dgrad, 2 = wgrad. Bytes of device workspace the
- * call needs for this shape (0 = pass NULL). Returns 0 for an invalid shape. */
+ * call needs for this shape on the current device (0 = pass NULL). Only
+ * dgrad ever needs any (see mla_q_uproj_bwd_dgrad). Returns 0 for an
+ * invalid shape or when no CUDA device is usable. */
 MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape *shape, int which);
 
 /* Static, human-readable name of a status code. */

@@ -164,3 +164,31 @@ def test_bwd_full_size_sampled(cuda_device):
         dqp = oracle.rope_bwd(dq_c, 16, w.Dn, w.Dr, cos, sin, pos).reshape(w.T, -1)
         ref_db[h0 * w.D:(h0 + 16) * w.D] = oracle.bgrad(dqp)
     assert helpers.frob_rel(db, ref_db) <= TOL
+
+
+def test_dgrad_split_reduction(cuda_device):
+    """Few tiles for many SMs: dgrad splits each tile's channel reduction,
+    writes fp32 partials to the workspace and adds them in a fixed order.
+    Sampled tokens against the oracle; two runs are bit-identical; a
+    workspace smaller than the query is rejected."""
+    import ctypes
+    w = synth.workload("dsv3_bwd", T=1024, seq_len=None)
+    inp, d = _dev_inputs(w, 9, cuda_device)
+    need = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, w.cs_rows, w.Dr, 1)
+    assert need > 0  # this shape splits
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    dx1 = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
+    ws = torch.empty((need,), dtype=torch.uint8, device=cuda_device)
+    dx2 = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st,
+                         workspace=ws)
+    mlaq.check_status(st)
+    assert torch.equal(dx1, dx2)
+    toks = np.sort(np.random.default_rng(2).choice(w.T, 16, replace=False))
+    dqp = oracle.rope_bwd(helpers.f64(inp["dq"][torch.from_numpy(toks)]), w.H, w.Dn, w.Dr,
+                          inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy()[toks])
+    ref = oracle.dgrad(dqp.reshape(len(toks), -1), helpers.f64(inp["W"]))
+    assert helpers.frob_rel(dx1[torch.from_numpy(toks).to(cuda_device)], ref) <= TOL
+    small = torch.empty((need - 16,), dtype=torch.uint8, device=cuda_device)
+    with pytest.raises(mlaq.MlaError) as ei:
+        mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], workspace=small)
+    assert ei.value.status == mlaq.STATUS["MLA_ERR_WORKSPACE"]

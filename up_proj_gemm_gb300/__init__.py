@@ -177,8 +177,12 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
     return (q_out, q_scales) if om else q_out
 
 
-def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream=None):
-    """dx [T, K] bf16 = (inverse-RoPE dq) W."""
+def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream=None, workspace=None):
+    """dx [T, K] bf16 = (inverse-RoPE dq) W.
+
+    When the library splits the channel reduction for this shape, it needs a
+    device workspace (``workspace_size(..., which=1)`` bytes); it is allocated
+    here unless passed in."""
     dev = dq.device
     _need(dq, "dq", torch.bfloat16)
     _need(W, "W", torch.bfloat16, dev, ndim=2)
@@ -193,8 +197,14 @@ def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream
     if dx is None:
         dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
     s = _shape(T, K, H, Dn, Dr, cos)
+    with torch.cuda.device(dev):
+        need = int(lib().mla_q_uproj_workspace_size(ctypes.byref(s), 1))
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _call(lib().mla_q_uproj_bwd_dgrad, "mla_q_uproj_bwd_dgrad", ctypes.byref(s), _ptr(dq), _ptr(W),
-          _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dx), None, 0, _ptr(status), _stream(dev, stream))
+          _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dx), _ptr(workspace), ws_bytes, _ptr(status),
+          _stream(dev, stream))
     return dx
 
 

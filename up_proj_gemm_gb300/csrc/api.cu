@@ -181,7 +181,10 @@ MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape* shape, int which) 
     int D;
     int64_t N;
     if (check_shape(shape, &D, &N) != MLA_OK || which < 0 || which > 2) return 0;
-    return 0;  // no kernel of this library needs scratch memory
+    if (which != 1 || shape->T == 0) return 0;  // only dgrad may split its reduction
+    DeviceInfo di;
+    if (current_device_info(&di) != MLA_OK) return 0;
+    return dgrad_workspace_bytes(shape->T, shape->K, N, di.num_sms);
 }
 
 MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_mode, const void* x,
@@ -277,10 +280,11 @@ MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape* shape, const void* dq, con
     if (st != MLA_OK) return st;
     const mla_q_shape& s = *shape;
     if (!aligned(dq, 16) || !aligned(W, 16) || !aligned(dx, 16) || !aligned(cos_tab, 4) ||
-        !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4))
+        !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4) || !aligned(workspace, 16))
         return MLA_ERR_ALIGNMENT;
     const int64_t table = s.cs_rows * s.cs_width * 4;
-    const Range outs[] = {rng(dx, s.T * s.K * 2), rng(dev_status, 4)};
+    const size_t need = mla_q_uproj_workspace_size(shape, 1);
+    const Range outs[] = {rng(dx, s.T * s.K * 2), rng(dev_status, 4), rng(workspace, (int64_t)need)};
     const Range ins[] = {rng(dq, s.T * N * 2), rng(W, N * s.K * 2), rng(cos_tab, table),
                          rng(sin_tab, table), rng(pos, s.T * 4)};
     if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
@@ -299,6 +303,8 @@ MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape* shape, const void* dq, con
     a.sin_tab = sin_tab;
     a.pos = pos;
     a.dx = dx;
+    a.workspace = workspace;
+    a.ws_bytes = ws_bytes;
     a.status = dev_status;
     return launch_dgrad(a, static_cast<cudaStream_t>(stream));
 }

@@ -78,6 +78,10 @@ struct BwdParams {
     int a3d, b3d;  // operand maps are 3-D chunk views (one TMA op per operand and stage)
     uint16_t* out;
     int out_rows, out_cols;
+    // work units: each tile's reduction split in ksplit parts of kts stages
+    // (dgrad only; the parts write fp32 partials to ws, summed afterwards)
+    int ksplit, kts, num_units;
+    float* ws;
     uint16_t* db;
     int* status;
 };
@@ -144,6 +148,13 @@ __device__ __forceinline__ bool has_rope(const BwdParams& p, int n0, int width) 
     return rs < n0 + width && rs < p.N;
 }
 
+// Work unit u -> its tile and stage range [k0, k1).
+__device__ __forceinline__ void unit_range(const BwdParams& p, int u, int& tile, int& k0, int& k1) {
+    tile = u / p.ksplit;
+    k0 = (u - tile * p.ksplit) * p.kts;
+    k1 = min(p.k_tiles, k0 + p.kts);
+}
+
 // Walks a CTA's stages (its tiles, each k-tile of each) and says which go
 // through the transform warps (else TMA -> MMA directly): dgrad stages whose
 // 64 channels hold rope channels; every stage of a wgrad tile that holds
@@ -154,10 +165,10 @@ struct StageWalk {
     int mt = 0, nt = 0;
     bool tile_x = false;  // wgrad: the tile's stages are transform stages
     int c0 = 0;           // dgrad: channel phase (kt * 64) mod D of the current stage
-    __device__ void begin_tile(const BwdParams& p, int tile) {
+    __device__ void begin_tile(const BwdParams& p, int tile, int k0) {
         mt = tile / p.num_n_tiles;
         nt = tile % p.num_n_tiles;
-        c0 = 0;
+        c0 = WG ? 0 : (k0 * bk_of(false)) % p.D;
         if (WG) tile_x = has_rope(p, mt * kBM, kBM) || (p.db != nullptr && nt == 0);
     }
     __device__ bool needs(const BwdParams& p, int kt) const {
@@ -268,10 +279,12 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         uint32_t fpar = 0, xp0 = 0, xp1 = 0, xp2 = 0, last_kind = 0, issued_mask = 0;
         StageWalk<WG> walk;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            walk.begin_tile(p, tile);
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            int tile, k0, k1;
+            unit_range(p, u, tile, k0, k1);
+            walk.begin_tile(p, tile, k0);
             const int mt = walk.mt, nt = walk.nt;
-            for (int kt = 0; kt < p.k_tiles; ++kt, walk.next(p)) {
+            for (int kt = k0; kt < k1; ++kt, walk.next(p)) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -339,7 +352,9 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             uint32_t rpar = 0, fpar = 0;  // per-slot parities of the ready / full barriers
             StageWalk<WG> walk;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++local) {
+                int tile, k0, k1;
+                unit_range(p, u, tile, k0, k1);
                 const int b = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
                 if (!mbar_wait(sm.tempty(b), (use & 1u) ^ 1u, abort_flag)) {
@@ -348,8 +363,8 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)b * kAccStride;
-                walk.begin_tile(p, tile);
-                for (int kt = 0; kt < p.k_tiles; ++kt, walk.next(p)) {
+                walk.begin_tile(p, tile, k0);
+                for (int kt = k0; kt < k1; ++kt, walk.next(p)) {
                     const bool xf = walk.needs(p, kt);
                     // transform stages: wait for the transform's release; others: the TMA
                     const uint32_t bar = xf ? sm.ready(s) : sm.full(s);
@@ -369,7 +384,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                         const uint64_t ad = WG ? desc_mnmajor_sw128(a0 + 2048u * j, CH)
                                                : desc_kmajor_sw128(a0 + 32u * j);
                         const uint64_t bd = desc_mnmajor_sw128(b0 + 2048u * j, CH);
-                        mma_bf16(d_tmem, ad, bd, p.idesc, (kt | j) != 0);
+                        mma_bf16(d_tmem, ad, bd, p.idesc, (kt != k0 || j != 0));
                     }
                     mma_commit(sm.empty(s));
                     if (++s == p.stages) {
@@ -390,7 +405,8 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         int local = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
+            const int tile = u / p.ksplit, sp = u - tile * p.ksplit;
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
@@ -406,7 +422,13 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 tmem_ld32(trow + col, r);
                 tmem_ld_wait();
                 const int64_t c0 = (int64_t)nt * p.BN + col;
-                if (valid) {
+                if (valid && p.ws) {
+                    // partial sum of split sp, fp32
+                    float* dst = p.ws + ((int64_t)sp * p.out_rows + orow) * p.out_cols + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        if (c0 + i + 4 <= p.out_cols) st_global_v4(dst + i, r[i], r[i + 1], r[i + 2], r[i + 3]);
+                } else if (valid) {
                     uint16_t* dst = p.out + orow * p.out_cols + c0;
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) {
@@ -445,11 +467,13 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         uint32_t xpar = 0;  // per-slot parity of this group's next barrier use
         int gnext = 0;      // group owning the next transform stage
         StageWalk<WG> walk;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            int tile, k0, k1;
+            unit_range(p, u, tile, k0, k1);
             const int mt = tile / p.num_n_tiles;
             const int nt = tile % p.num_n_tiles;
             const bool do_db = WG && p.db != nullptr && nt == 0;
-            walk.begin_tile(p, tile);
+            walk.begin_tile(p, tile, k0);
             float acc0 = 0.f, acc1 = 0.f;
             // cos/sin of this thread's pairs for its token (dgrad: fixed per tile)
             float ci[PPI], si[PPI], cj[PPI], sj[PPI];
@@ -473,7 +497,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             } else {
                 nreg = rope_regions(p, mt * kBM, kBM, reg);
             }
-            for (int kt = 0; kt < p.k_tiles; ++kt) {
+            for (int kt = k0; kt < k1; ++kt) {
                 const bool nx = walk.needs(p, kt);
                 walk.next(p);
                 bool skip = !nx;
@@ -615,6 +639,25 @@ int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const BwdPar
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// dx = bf16(sum over splits of the fp32 partials), in split order (the
+// result does not depend on which split finished first). 8 elements per
+// thread: ksplit x two 16-byte loads, one 16-byte store.
+__global__ void __launch_bounds__(256) dgrad_reduce_kernel(const float* __restrict__ ws, int ksplit,
+                                                           int64_t n, uint16_t* __restrict__ dx) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x * 8;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < n; i += stride) {
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int sp = 0; sp < ksplit; ++sp) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(ws + sp * n + i));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(ws + sp * n + i) + 1);
+            v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+            v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+        }
+        st_global_v4(dx + i, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                     pack_bf16x2(v[6], v[7]));
+    }
+}
+
 int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     DeviceInfo di;
     int st = current_device_info(&di);
@@ -652,6 +695,12 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     p.out_cols = (int)a.K;
     p.db = wg ? static_cast<uint16_t*>(a.db) : nullptr;
     p.status = a.status;
+    p.ksplit = wg ? 1 : dgrad_ksplit(a.T, a.K, N, di.num_sms);
+    p.kts = (p.k_tiles + p.ksplit - 1) / p.ksplit;
+    p.num_units = p.num_tiles * p.ksplit;
+    p.ws = p.ksplit > 1 ? static_cast<float*>(a.workspace) : nullptr;
+    if (p.ksplit > 1 && (!a.workspace || a.ws_bytes < dgrad_workspace_bytes(a.T, a.K, N, di.num_sms)))
+        return MLA_ERR_WORKSPACE;
 
     if (wg && a.T == 0) {  // empty reduction: the gradients are zero
         if (cudaMemsetAsync(a.dW, 0, (size_t)N * a.K * 2, stream) != cudaSuccess) return MLA_ERR_CUDA;
@@ -684,12 +733,45 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
             st = make_tmap_2d(&tb, a.x, 1, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, BK, true);
     }
     if (st != MLA_OK) return st;
-    const int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
-    return wg ? launch_dr<true>(a.Dr, ta, tb, p, grid, smem, stream)
-              : launch_dr<false>(a.Dr, ta, tb, p, grid, smem, stream);
+    const int grid = p.num_units < di.num_sms ? p.num_units : di.num_sms;
+    st = wg ? launch_dr<true>(a.Dr, ta, tb, p, grid, smem, stream)
+            : launch_dr<false>(a.Dr, ta, tb, p, grid, smem, stream);
+    if (st != MLA_OK || p.ksplit == 1) return st;
+    const int64_t n = a.T * a.K;
+    int64_t blocks = (n / 8 + 255) / 256;
+    if (blocks > (int64_t)di.num_sms * 8) blocks = (int64_t)di.num_sms * 8;
+    dgrad_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p.ws, p.ksplit, n, static_cast<uint16_t*>(a.dx));
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
+
+// Splits of each dgrad tile's channel reduction: the count in 1..4 (keeping
+// >= 32 stages per split) whose units fill the SMs' waves best; ties go to
+// fewer splits. 1 means no split (and no workspace).
+int dgrad_ksplit(int64_t T, int64_t K, int64_t N, int num_sms) {
+    if (num_sms <= 0) return 1;
+    const int64_t tiles = ((T + kBM - 1) / kBM) * ((K + 255) / 256);
+    const int64_t k_tiles = (N + bk_of(false) - 1) / bk_of(false);
+    int best = 1;
+    double best_eff = 0.0;
+    for (int sp = 1; sp <= 4; ++sp) {
+        if (sp > 1 && k_tiles / sp < 32) break;
+        const int64_t units = tiles * sp;
+        const int64_t waves = (units + num_sms - 1) / num_sms;
+        const double eff = (double)units / (double)(waves * num_sms);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = sp;
+        }
+    }
+    return best;
+}
+
+size_t dgrad_workspace_bytes(int64_t T, int64_t K, int64_t N, int num_sms) {
+    const int sp = dgrad_ksplit(T, K, N, num_sms);
+    return sp > 1 ? (size_t)sp * (size_t)T * (size_t)K * sizeof(float) : 0;
+}
 
 int launch_dgrad(const BwdArgs& a, cudaStream_t stream) { return launch_common(a, false, stream); }
 int launch_wgrad(const BwdArgs& a, cudaStream_t stream) { return launch_common(a, true, stream); }

@@ -70,9 +70,15 @@ struct BwdArgs {
     void* dx;        // dgrad
     void* dW;        // wgrad
     void* db;        // wgrad, nullable
+    void* workspace; // dgrad split partials (see dgrad_workspace_bytes)
+    size_t ws_bytes;
     int* status;
 };
 int launch_dgrad(const BwdArgs& a, cudaStream_t stream);
+// dgrad's split of the channel reduction for this shape on a device with
+// num_sms SMs, and the fp32 workspace it needs (0 when not split).
+int dgrad_ksplit(int64_t T, int64_t K, int64_t N, int num_sms);
+size_t dgrad_workspace_bytes(int64_t T, int64_t K, int64_t N, int num_sms);
 int launch_wgrad(const BwdArgs& a, cudaStream_t stream);
 
 // Tile width (channels) of the forward kernel for this shape: the largest
