@@ -176,6 +176,36 @@ MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape *shape, const void *dq, con
                                    void *dW, void *db, void *workspace, size_t ws_bytes,
                                    int *dev_status, void *stream);
 
+/* Size of the device scratch array mla_q_uproj_bwd_dgrad_noalloc uses. */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * dgrad without any workspace argument, for callers that cannot allocate
+ * device memory. (The pages have no counterpart: this is an addition of this
+ * library.) Some callers of a library like this one cannot allocate: a host
+ * framework that lends a plugin only the tensors of one call and owns all
+ * other device memory, or a latency-critical path that cannot pay for
+ * cudaMalloc's implicit synchronization. This entry point computes exactly
+ * what mla_q_uproj_bwd_dgrad computes, with the same arguments minus the
+ * workspace, and takes its split-reduction partials from a scratch array of
+ * MLA_NOALLOC_SCRATCH_BYTES that the library keeps in device global memory
+ * (every GPU that loads the library holds it until the process exits).
+ *   - The first call on a device looks up that device's scratch address (a
+ *     CUDA runtime query, no allocation); make that first call before any
+ *     stream capture. It allocates nothing, ever.
+ *   - A shape whose partials need more than MLA_NOALLOC_SCRATCH_BYTES (see
+ *     mla_q_uproj_workspace_size(shape, 1)) is rejected with
+ *     MLA_ERR_WORKSPACE; shapes that need no workspace always run.
+ *   - All calls share the one array. Nothing in it has to start at zero
+ *     (every partial the reduction reads is written earlier in the same
+ *     call), but calls that overlap on the GPU (other streams, other threads)
+ *     race on it: serialize them.
+ */
+MLAQ_API int mla_q_uproj_bwd_dgrad_noalloc(const mla_q_shape *shape, const void *dq, const void *W,
+                                           const float *cos_tab, const float *sin_tab,
+                                           const int32_t *pos, void *dx, int *dev_status,
+                                           void *stream);
+
 /*
  * Standalone rowwise MXFP8 quantization of in[R, C] (row pitch ld_in
  * elements, ld_in >= C): codes [R, C] uint8 (dense, pitch C) and scales

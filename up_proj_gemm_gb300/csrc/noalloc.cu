@@ -1,0 +1,70 @@
+// dgrad for callers that cannot allocate device memory.
+//
+// mla_q_uproj_bwd_dgrad may need a workspace for the fp32 partial sums of
+// its split reduction, and expects the caller to allocate it. Some callers
+// cannot: a host framework that lends a plugin only the tensors of a call
+// and owns every other byte of device memory, or a latency-critical path
+// that cannot take cudaMalloc's implicit device-wide synchronization. This
+// file gives them one entry point that takes inputs and outputs only and
+// uses a scratch array of fixed size that the library holds in device
+// global memory instead.
+//
+// The array below is file-scope device memory: every GPU that loads the
+// library holds it until the process exits. In host code its name is only a
+// host-side stand-in, not a device address, so the host looks the address
+// up per device (cudaGetSymbolAddress, with that device current) the first
+// time this entry point runs on it, caches it, and passes it to the kernels
+// as their workspace.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace mlaq {
+namespace {
+
+static __device__ __align__(256) float g_dgrad_scratch[MLA_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+// Device address of g_dgrad_scratch on the current device (looked up once
+// per device), or nullptr with the CUDA error code in *err.
+void* scratch_address(int* err) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = MLA_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dgrad_scratch) != cudaSuccess || !p) {
+            *err = MLA_ERR_CUDA;
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+}  // namespace mlaq
+
+extern "C" MLAQ_API int mla_q_uproj_bwd_dgrad_noalloc(const mla_q_shape* shape, const void* dq,
+                                                      const void* W, const float* cos_tab,
+                                                      const float* sin_tab, const int32_t* pos, void* dx,
+                                                      int* dev_status, void* stream) {
+    // Same argument checks as the allocating entry point (a NULL workspace
+    // with size 0 passes them); then the scratch stands in for the workspace.
+    const size_t need = mla_q_uproj_workspace_size(shape, 1);
+    if (need == 0)
+        return mla_q_uproj_bwd_dgrad(shape, dq, W, cos_tab, sin_tab, pos, dx, nullptr, 0, dev_status,
+                                     stream);
+    if (need > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;  // shape too large for the scratch
+    int err = MLA_OK;
+    void* scratch = mlaq::scratch_address(&err);
+    if (!scratch) return err;
+    return mla_q_uproj_bwd_dgrad(shape, dq, W, cos_tab, sin_tab, pos, dx, scratch, need, dev_status,
+                                 stream);
+}
