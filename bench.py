@@ -263,6 +263,10 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     mlaq.check_status(status, "warm-up")
+    # our kernels per step: forward, dgrad (+ its partial-sum reduction when the
+    # channel reduction is split, i.e. when it needs a workspace), wgrad
+    split = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, inp["cos"].shape[0], inp["cos"].shape[1], 1) > 0
+    kernels_per_step = 4 if split else 3
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
@@ -312,7 +316,7 @@ def run_ours(args):
                    "l2": "flushed (256 MiB write) between steps, outside the timed events",
                    "parallelism": f"replicas x{world} (no data exchange)"},
         "roofline": roofline,
-        "gpu_launches": 3 * K,
+        "gpu_launches": kernels_per_step * K,
         "clocks": clocks,
         "kernels_ms": {n: round(m, 4) for n, m in zip(names, mean_k)},
         "kernels_tflops": {n: round(f / (m * 1e-3) / 1e12, 1) for n, f, m in zip(names, flops, mean_k)},
