@@ -236,6 +236,8 @@ def run_ours(args):
     dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=dev)
     dW = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
     db = torch.empty((w.N,), dtype=torch.bfloat16, device=dev)
+    # rotated rope channels, written by dgrad and read by wgrad (T*H*Dr bf16)
+    rope = torch.empty((w.T, w.H, w.Dr), dtype=torch.bfloat16, device=dev)
 
     def k_fwd():
         mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"],
@@ -243,9 +245,13 @@ def run_ours(args):
 
     def k_dgrad():
         mlaq.bwd_dgrad(inp["dq"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
-                       dx=dx, status=status)
+                       dx=dx, status=status, dq_pre_rope=rope)
 
     def k_wgrad():
+        mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                       dW=dW, db=db, status=status, dq_pre_rope=rope)
+
+    def k_wgrad_self():  # a delayed wgrad without dgrad's buffer: rotates dq itself
         mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
                        dW=dW, db=db, status=status)
 
@@ -255,8 +261,9 @@ def run_ours(args):
         k_wgrad()
 
     if args.only:
-        return run_only(args, w, inp, {"fwd": k_fwd, "dgrad": k_dgrad, "wgrad": k_wgrad}, flush, stream,
-                        status, dev)
+        k_dgrad()  # fills the rope buffer wgrad reads
+        return run_only(args, w, inp, {"fwd": k_fwd, "dgrad": k_dgrad, "wgrad": k_wgrad,
+                                       "wgrad_self": k_wgrad_self}, flush, stream, status, dev)
 
     for _ in range(args.warmup):
         flush()
@@ -313,6 +320,7 @@ def run_ours(args):
         "config": {"workload": "dsv3_q_uproj_train_step: fwd(bf16 W, +bias, RoPE, MXFP8 q) + dgrad + "
                                "wgrad + db", "T": w.T, "K": w.K, "H": w.H, "Dn": w.Dn, "Dr": w.Dr,
                    "N": w.N, "pos": "t", "rope_table": "standard base 1e4",
+                   "rope_handoff": "dgrad stores the rotated rope channels [T, H, Dr] bf16; wgrad reads them",
                    "l2": "flushed (256 MiB write) between steps, outside the timed events",
                    "parallelism": f"replicas x{world} (no data exchange)"},
         "roofline": roofline,
@@ -333,6 +341,7 @@ def run_ours(args):
     hdb = torch.empty(db.shape, dtype=torch.bfloat16).pin_memory()
     dxin = torch.empty_like(inp["x"])
     ddq = torch.empty_like(inp["dq"])
+    rope_e = torch.empty_like(rope)
 
     def e2e_step():
         dxin.copy_(hx, non_blocking=True)
@@ -340,9 +349,9 @@ def run_ours(args):
         mlaq.fwd(dxin, inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"], pos=inp["pos"],
                  out_mode="mxfp8", q_out=q_codes, q_scales=q_scales, status=status)
         mlaq.bwd_dgrad(ddq, inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], dx=dx,
-                       status=status)
+                       status=status, dq_pre_rope=rope_e)
         mlaq.bwd_wgrad(ddq, dxin, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], dW=dW, db=db,
-                       status=status)
+                       status=status, dq_pre_rope=rope_e)
         hq.copy_(q_codes, non_blocking=True)
         hs.copy_(q_scales, non_blocking=True)
         hdx.copy_(dx, non_blocking=True)
@@ -357,7 +366,7 @@ def run_ours(args):
     out["e2e"] = {"value": round(aggregate(e2e_ms, flop_step, world), 2), "unit": "TFLOP/s",
                   "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                   "steps": e2e_steps}
-    del hx, hdq, hq, hs, hdx, hdW, hdb, dxin, ddq
+    del hx, hdq, hq, hs, hdx, hdW, hdb, dxin, ddq, rope_e
 
     if rank == 0 and not args.no_parts:
         out["parts"] = run_parts(dev, stream, flush, pk, pk_src)
@@ -457,17 +466,23 @@ def run_parts(dev, stream, flush, pk, pk_src):
     dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=dev)
     dW = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
     db = torch.empty((w.N,), dtype=torch.bfloat16, device=dev)
+    rope = torch.empty((w.T, w.H, w.Dr), dtype=torch.bfloat16, device=dev)
     ms_d = time_loop(lambda: mlaq.bwd_dgrad(inp["dq"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
-                                            pos=inp["pos"], dx=dx, status=st), 20, flush, stream)
+                                            pos=inp["pos"], dx=dx, status=st, dq_pre_rope=rope),
+                     20, flush, stream)
     ms_w = time_loop(lambda: mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
-                                            pos=inp["pos"], dW=dW, db=db, status=st), 20, flush, stream)
+                                            pos=inp["pos"], dW=dW, db=db, status=st, dq_pre_rope=rope),
+                     20, flush, stream)
+    ms_ws = time_loop(lambda: mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
+                                             pos=inp["pos"], dW=dW, db=db, status=st), 20, flush, stream)
     half = w.bwd_flop() / 2
     parts["bwd_T8192"] = {"dgrad_ms": round(ms_d, 4), "wgrad_db_ms": round(ms_w, 4),
+                          "wgrad_db_self_rotating_ms": round(ms_ws, 4),
                           "TFLOP/s": round(w.bwd_flop() / ((ms_d + ms_w) * 1e-3) / 1e12, 1),
                           "dgrad_TFLOP/s": round(half / (ms_d * 1e-3) / 1e12, 1),
                           "wgrad_TFLOP/s": round(half / (ms_w * 1e-3) / 1e12, 1),
                           "frac_bf16_peak": round(w.bwd_flop() / ((ms_d + ms_w) * 1e-3) / 1e12 / bf16_peak, 4)}
-    del inp, dx, dW, db
+    del inp, dx, dW, db, rope
 
     # long context: T = 4 x 4096, YaRN table, MXFP8 out, fwd + bwd
     w = synth.workload("dsv3_long_yarn")
@@ -476,20 +491,21 @@ def run_parts(dev, stream, flush, pk, pk_src):
     qs = torch.empty((w.T, w.H, (w.D + 31) // 32), dtype=torch.uint8, device=dev)
     dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=dev)
     dW = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
+    rope = torch.empty((w.T, w.H, w.Dr), dtype=torch.bfloat16, device=dev)
 
     def long_step():
         mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
                  out_mode="mxfp8", q_out=qc, q_scales=qs, status=st)
         mlaq.bwd_dgrad(inp["dq"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
-                       dx=dx, status=st)
+                       dx=dx, status=st, dq_pre_rope=rope)
         mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
-                       dW=dW, db=None, status=st)
+                       dW=dW, db=None, status=st, dq_pre_rope=rope)
 
     ms = time_loop(long_step, 10, flush, stream)
     tf = (w.fwd_flop() + w.bwd_flop()) / (ms * 1e-3) / 1e12
     parts["long_yarn_T16384_fwd_bwd"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                          "frac_bf16_peak": round(tf / bf16_peak, 4)}
-    del inp, qc, qs, dx, dW
+    del inp, qc, qs, dx, dW, rope
     torch.cuda.synchronize()
     mlaq.check_status(st, "parts")
     parts["peak_note"] = f"{pk_src} peaks; kernels timed alone use the burst bf16 figure"
@@ -573,7 +589,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "fwd_mxfp8w", "quant"),
+    ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "wgrad_self", "fwd_mxfp8w", "quant"),
                     help="time one kernel alone (profiling)")
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -140,9 +140,15 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_
  * TransformerEngine PR "Add a backwards linear function to be used with the
  * fused mla q up-proj", summary and sequence diagram (RoPE backward, then the
  * linear backward with the weight). The inverse rotation is applied to dq
- * tiles on their way into the tensor cores; dq_pre is never stored.
+ * tiles on their way into the tensor cores; the full dq_pre is never stored.
  *   dq [T, H, D] bf16, W [N, K] bf16 (the bf16 master weight), dx [T, K] bf16
  *   (fp32 accumulation). cos_tab/sin_tab/pos as in the forward.
+ *   dq_pre_rope: NULL, or [T, H, Dr] bf16 (16-byte aligned, not overlapping
+ *   anything else) that receives the rope channels of dq_pre = J^T dq, the
+ *   last Dr channels of every head after the inverse rotation, rounded to
+ *   bf16: exactly the values the tensor cores consume. Pass it on to
+ *   mla_q_uproj_bwd_wgrad, which then skips its own rotation. Rows whose
+ *   position is out of range are left unwritten (dev_status reports it).
  *   workspace/ws_bytes: device scratch of at least
  *   mla_q_uproj_workspace_size(shape, 1) bytes, 16-byte aligned, not
  *   overlapping any input or output (NULL/0 when the query returns 0). When
@@ -157,8 +163,8 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_
  */
 MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape *shape, const void *dq, const void *W,
                                    const float *cos_tab, const float *sin_tab, const int32_t *pos,
-                                   void *dx, void *workspace, size_t ws_bytes, int *dev_status,
-                                   void *stream);
+                                   void *dx, void *dq_pre_rope, void *workspace, size_t ws_bytes,
+                                   int *dev_status, void *stream);
 
 /*
  * Backward, weight and bias gradients: dW = (J^T dq)^T x, db = sum_t J^T dq.
@@ -169,12 +175,20 @@ MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape *shape, const void *dq, con
  * schedules).
  *   dq [T, H, D] bf16, x [T, K] bf16, dW [N, K] bf16, db [N] bf16 or NULL
  *   (skipped). fp32 accumulation over all T.
+ *   dq_pre_rope: NULL (the rope channels of dq are rotated here, on their way
+ *   into the tensor cores), or the buffer mla_q_uproj_bwd_dgrad filled from
+ *   the same dq, positions and tables (an input here). When Dr == 64,
+ *   Dn % 128 == 0 and H is even, the rope tiles are then read from it
+ *   instead of rotated again; other shapes rotate dq as with NULL. Either
+ *   way the operands, and so dW and db, are the same bits.
+ *   workspace/ws_bytes: unused (NULL/0; mla_q_uproj_workspace_size(shape, 2)
+ *   is 0).
  * Requirements as for mla_q_uproj_bwd_dgrad.
  */
-MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape *shape, const void *dq, const void *x,
-                                   const float *cos_tab, const float *sin_tab, const int32_t *pos,
-                                   void *dW, void *db, void *workspace, size_t ws_bytes,
-                                   int *dev_status, void *stream);
+MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape *shape, const void *dq, const void *dq_pre_rope,
+                                   const void *x, const float *cos_tab, const float *sin_tab,
+                                   const int32_t *pos, void *dW, void *db, void *workspace,
+                                   size_t ws_bytes, int *dev_status, void *stream);
 
 /* Size of the device scratch array mla_q_uproj_bwd_dgrad_noalloc uses. */
 #define MLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -203,8 +217,8 @@ MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape *shape, const void *dq, con
  */
 MLAQ_API int mla_q_uproj_bwd_dgrad_noalloc(const mla_q_shape *shape, const void *dq, const void *W,
                                            const float *cos_tab, const float *sin_tab,
-                                           const int32_t *pos, void *dx, int *dev_status,
-                                           void *stream);
+                                           const int32_t *pos, void *dx, void *dq_pre_rope,
+                                           int *dev_status, void *stream);
 
 /*
  * Standalone rowwise MXFP8 quantization of in[R, C] (row pitch ld_in

@@ -118,10 +118,12 @@ def test_fwd_empty_tokens_is_noop(L):
 
 
 def _bwd(L, which, s, dq=p(0), op=p(1), cos=p(2), sin=p(3), pos=None, out=p(4), db=None, ws=None,
-         wsb=0):
+         wsb=0, rope=None):
     if which == "dgrad":
-        return L.mla_q_uproj_bwd_dgrad(ctypes.byref(s), dq, op, cos, sin, pos, out, ws, wsb, None, None)
-    return L.mla_q_uproj_bwd_wgrad(ctypes.byref(s), dq, op, cos, sin, pos, out, db, ws, wsb, None, None)
+        return L.mla_q_uproj_bwd_dgrad(ctypes.byref(s), dq, op, cos, sin, pos, out, rope, ws, wsb, None,
+                                       None)
+    return L.mla_q_uproj_bwd_wgrad(ctypes.byref(s), dq, rope, op, cos, sin, pos, out, db, ws, wsb, None,
+                                   None)
 
 
 @pytest.mark.parametrize("which", ["dgrad", "wgrad"])
@@ -134,6 +136,19 @@ def test_bwd_rejects(L, which):
     assert _bwd(L, which, shape(K=36)) == S["MLA_ERR_ALIGNMENT"]
     assert _bwd(L, which, shape(T=257)) == S["MLA_ERR_POS_RANGE"]
     assert _bwd(L, which, shape()) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+
+
+def test_rope_buffer_checks(L):
+    # dgrad writes dq_pre_rope (an output): it may overlap nothing
+    ok = (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert _bwd(L, "dgrad", shape(), rope=p(8)) in ok
+    assert _bwd(L, "dgrad", shape(), rope=p(0)) == S["MLA_ERR_ALIAS"]   # over dq
+    assert _bwd(L, "dgrad", shape(), rope=p(4)) == S["MLA_ERR_ALIAS"]   # over dx
+    assert _bwd(L, "dgrad", shape(), rope=ctypes.c_void_p(FAKE * 9 + 8)) == S["MLA_ERR_ALIGNMENT"]
+    # wgrad reads it (an input): it may share bytes with other inputs, not with dW
+    assert _bwd(L, "wgrad", shape(), rope=p(8)) in ok
+    assert _bwd(L, "wgrad", shape(), rope=p(4)) == S["MLA_ERR_ALIAS"]   # under dW
+    assert _bwd(L, "wgrad", shape(), rope=ctypes.c_void_p(FAKE * 9 + 8)) == S["MLA_ERR_ALIGNMENT"]
 
 
 def test_wgrad_bias_alias(L):

@@ -29,7 +29,7 @@ SCRATCH_BYTES = 32 * 1024 * 1024  # MLA_NOALLOC_SCRATCH_BYTES in include/mlaq.h
 def _noalloc_fn():
     f = mlaq.lib().mla_q_uproj_bwd_dgrad_noalloc
     f.restype = ctypes.c_int
-    f.argtypes = [ctypes.POINTER(mlaq.Shape)] + [ctypes.c_void_p] * 8
+    f.argtypes = [ctypes.POINTER(mlaq.Shape)] + [ctypes.c_void_p] * 9
     return f
 
 
@@ -38,7 +38,7 @@ def _call_noalloc(w, d, dx, st):
                    cs_width=d["cos"].shape[1])
     p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
     return _noalloc_fn()(ctypes.byref(s), p(d["dq"]), p(d["W"]), p(d["cos"]), p(d["sin"]), p(d["pos"]),
-                         p(dx), p(st), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                         p(dx), None, p(st), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
 def test_noalloc_dgrad_matches_workspace_dgrad(cuda_device):

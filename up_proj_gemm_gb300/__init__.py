@@ -56,10 +56,12 @@ _int = ctypes.c_int
 _SIGS = {
     "mla_q_uproj_fwd": (_int, [ctypes.POINTER(Shape), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                _vp, _vp, _vp, _vp, _vp]),
-    "mla_q_uproj_bwd_dgrad": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+    "mla_q_uproj_bwd_dgrad": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _vp, _vp]),
-    "mla_q_uproj_bwd_wgrad": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+    "mla_q_uproj_bwd_wgrad": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _vp, _vp]),
+    "mla_q_uproj_bwd_dgrad_noalloc": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                             _vp, _vp]),
     "mxfp8_quantize_rows": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
     "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
     "mla_status_string": (ctypes.c_char_p, [_int]),
@@ -177,12 +179,22 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
     return (q_out, q_scales) if om else q_out
 
 
-def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream=None, workspace=None):
+def _rope_buf(t, T, H, Dr, dev):
+    if t is not None:
+        _need(t, "dq_pre_rope", torch.bfloat16, dev)
+        if t.numel() != T * H * Dr or not t.is_contiguous():
+            raise ValueError("dq_pre_rope must be a contiguous [T, H, Dr] bf16 tensor")
+    return t
+
+
+def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream=None, workspace=None,
+              dq_pre_rope=None):
     """dx [T, K] bf16 = (inverse-RoPE dq) W.
 
     When the library splits the channel reduction for this shape, it needs a
     device workspace (``workspace_size(..., which=1)`` bytes); it is allocated
-    here unless passed in."""
+    here unless passed in. ``dq_pre_rope`` (a [T, H, Dr] bf16 tensor, or
+    None) receives the rotated rope channels, for bwd_wgrad."""
     dev = dq.device
     _need(dq, "dq", torch.bfloat16)
     _need(W, "W", torch.bfloat16, dev, ndim=2)
@@ -196,6 +208,7 @@ def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream
         _need(pos, "pos", torch.int32, dev, ndim=1)
     if dx is None:
         dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    _rope_buf(dq_pre_rope, T, H, Dr, dev)
     s = _shape(T, K, H, Dn, Dr, cos)
     with torch.cuda.device(dev):
         need = int(lib().mla_q_uproj_workspace_size(ctypes.byref(s), 1))
@@ -203,16 +216,19 @@ def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _call(lib().mla_q_uproj_bwd_dgrad, "mla_q_uproj_bwd_dgrad", ctypes.byref(s), _ptr(dq), _ptr(W),
-          _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dx), _ptr(workspace), ws_bytes, _ptr(status),
-          _stream(dev, stream))
+          _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dx), _ptr(dq_pre_rope), _ptr(workspace), ws_bytes,
+          _ptr(status), _stream(dev, stream))
     return dx
 
 
-def bwd_wgrad(dq, x, cos, sin, H, Dn, Dr, pos=None, dW=None, db=True, status=None, stream=None):
+def bwd_wgrad(dq, x, cos, sin, H, Dn, Dr, pos=None, dW=None, db=True, status=None, stream=None,
+              dq_pre_rope=None):
     """dW [N, K] bf16 = (inverse-RoPE dq)^T x and db [N] bf16 = its token sum.
 
     db=True allocates the bias gradient, db=None/False skips it, or pass a
-    tensor. Returns (dW, db-or-None)."""
+    tensor. ``dq_pre_rope``: None, or the buffer bwd_dgrad filled from the
+    same dq (its rope tiles are then read instead of rotated again).
+    Returns (dW, db-or-None)."""
     dev = dq.device
     _need(dq, "dq", torch.bfloat16)
     _need(x, "x", torch.bfloat16, dev, ndim=2)
@@ -230,10 +246,11 @@ def bwd_wgrad(dq, x, cos, sin, H, Dn, Dr, pos=None, dW=None, db=True, status=Non
         db = torch.empty((N,), dtype=torch.bfloat16, device=dev)
     elif db is False:
         db = None
+    _rope_buf(dq_pre_rope, T, H, Dr, dev)
     s = _shape(T, K, H, Dn, Dr, cos)
-    _call(lib().mla_q_uproj_bwd_wgrad, "mla_q_uproj_bwd_wgrad", ctypes.byref(s), _ptr(dq), _ptr(x),
-          _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dW), _ptr(db), None, 0, _ptr(status),
-          _stream(dev, stream))
+    _call(lib().mla_q_uproj_bwd_wgrad, "mla_q_uproj_bwd_wgrad", ctypes.byref(s), _ptr(dq),
+          _ptr(dq_pre_rope), _ptr(x), _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dW), _ptr(db), None, 0,
+          _ptr(status), _stream(dev, stream))
     return dW, db
 
 

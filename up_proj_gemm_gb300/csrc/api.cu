@@ -68,6 +68,30 @@ int make_tmap_2d(void* tmap_out, const void* base, int dtype, uint64_t inner, ui
     return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
 
+int make_tmap_3d(void* tmap_out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                 uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!encode) return MLA_ERR_CUDA;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1, stride2};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(reinterpret_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
 int make_tmap_chunks(void* tmap_out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
                      uint32_t box_chunks) {
     static std::once_flag once;
@@ -272,19 +296,21 @@ static int check_bwd(const mla_q_shape* shape, const void* dq, const void* op, c
 
 MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape* shape, const void* dq, const void* W,
                                    const float* cos_tab, const float* sin_tab, const int32_t* pos,
-                                   void* dx, void* workspace, size_t ws_bytes, int* dev_status,
-                                   void* stream) {
+                                   void* dx, void* dq_pre_rope, void* workspace, size_t ws_bytes,
+                                   int* dev_status, void* stream) {
     int D;
     int64_t N;
     int st = check_bwd(shape, dq, W, cos_tab, sin_tab, pos, dx, workspace, ws_bytes, 1, &D, &N);
     if (st != MLA_OK) return st;
     const mla_q_shape& s = *shape;
     if (!aligned(dq, 16) || !aligned(W, 16) || !aligned(dx, 16) || !aligned(cos_tab, 4) ||
-        !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4) || !aligned(workspace, 16))
+        !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4) || !aligned(workspace, 16) ||
+        !aligned(dq_pre_rope, 16))
         return MLA_ERR_ALIGNMENT;
     const int64_t table = s.cs_rows * s.cs_width * 4;
     const size_t need = mla_q_uproj_workspace_size(shape, 1);
-    const Range outs[] = {rng(dx, s.T * s.K * 2), rng(dev_status, 4), rng(workspace, (int64_t)need)};
+    const Range outs[] = {rng(dx, s.T * s.K * 2), rng(dev_status, 4), rng(workspace, (int64_t)need),
+                          rng(dq_pre_rope, s.T * s.H * s.Dr * 2)};
     const Range ins[] = {rng(dq, s.T * N * 2), rng(W, N * s.K * 2), rng(cos_tab, table),
                          rng(sin_tab, table), rng(pos, s.T * 4)};
     if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
@@ -303,28 +329,30 @@ MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape* shape, const void* dq, con
     a.sin_tab = sin_tab;
     a.pos = pos;
     a.dx = dx;
+    a.rope_out = dq_pre_rope;
     a.workspace = workspace;
     a.ws_bytes = ws_bytes;
     a.status = dev_status;
     return launch_dgrad(a, static_cast<cudaStream_t>(stream));
 }
 
-MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape* shape, const void* dq, const void* x,
-                                   const float* cos_tab, const float* sin_tab, const int32_t* pos,
-                                   void* dW, void* db, void* workspace, size_t ws_bytes,
-                                   int* dev_status, void* stream) {
+MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape* shape, const void* dq, const void* dq_pre_rope,
+                                   const void* x, const float* cos_tab, const float* sin_tab,
+                                   const int32_t* pos, void* dW, void* db, void* workspace,
+                                   size_t ws_bytes, int* dev_status, void* stream) {
     int D;
     int64_t N;
     int st = check_bwd(shape, dq, x, cos_tab, sin_tab, pos, dW, workspace, ws_bytes, 2, &D, &N);
     if (st != MLA_OK) return st;
     const mla_q_shape& s = *shape;
     if (!aligned(dq, 16) || !aligned(x, 16) || !aligned(dW, 16) || !aligned(db, 4) ||
-        !aligned(cos_tab, 4) || !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4))
+        !aligned(cos_tab, 4) || !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4) ||
+        !aligned(dq_pre_rope, 16))
         return MLA_ERR_ALIGNMENT;
     const int64_t table = s.cs_rows * s.cs_width * 4;
     const Range outs[] = {rng(dW, N * s.K * 2), rng(db, N * 2), rng(dev_status, 4)};
     const Range ins[] = {rng(dq, s.T * N * 2), rng(x, s.T * s.K * 2), rng(cos_tab, table),
-                         rng(sin_tab, table), rng(pos, s.T * 4)};
+                         rng(sin_tab, table), rng(pos, s.T * 4), rng(dq_pre_rope, s.T * s.H * s.Dr * 2)};
     if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
     BwdArgs a{};
     a.T = s.T;
@@ -335,6 +363,7 @@ MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape* shape, const void* dq, con
     a.cs_rows = s.cs_rows;
     a.cs_width = s.cs_width;
     a.dq = dq;
+    a.rope_in = dq_pre_rope;
     a.x = x;
     a.cos_tab = cos_tab;
     a.sin_tab = sin_tab;

@@ -13,6 +13,12 @@
 // each tile in place (fp32 math, rounded to bf16, the MMA operand type),
 // fence them into the async proxy and release the stage to the MMA thread.
 //
+// dgrad can also store the rotated rope channels it computes (dq_pre_rope
+// [T, H, Dr] bf16, exactly the MMA operand values); wgrad, given that
+// buffer, loads its rope tiles from it already rotated: the rotation then
+// runs once, in dgrad's operand path, where each thread reads its cos/sin row
+// once per tile, instead of once per 32-token stage in every wgrad tile.
+//
 // Warp roles (persistent, one CTA per SM):
 //   warp 0     TMA producer (S-stage ring, 128-byte swizzle)
 //   warp 1     single-thread tcgen05.mma issuer, double-buffered TMEM acc
@@ -39,6 +45,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "internal.h"
 #include "mx.cuh"
 #include "ptx.cuh"
@@ -49,11 +57,10 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kXformWarp0 = 6;
 
-// Reduction rows per stage: 64 channels (dgrad) or 32 tokens (wgrad, whose
-// stages each need fresh cos/sin rows: a deeper ring of smaller stages).
-__host__ __device__ constexpr int bk_of(bool wg) { return wg ? 32 : 64; }
-// bytes of one 64-wide MN-major chunk (bk rows of 128 bytes)
-__host__ __device__ constexpr uint32_t chunk_of(bool wg) { return (uint32_t)bk_of(wg) * 128u; }
+// Reduction rows per stage: 64 channels (dgrad); 32 tokens for a wgrad that
+// rotates (its stages each need fresh cos/sin rows: a deeper ring of smaller
+// stages), 64 for a wgrad whose rope tiles come rotated.
+constexpr int kBKD = 64, kBKW = 32, kBKWPre = 64;
 // transform groups taking turns on stages, and threads per group
 __host__ __device__ constexpr int xform_groups(bool wg) { return wg ? 3 : 1; }
 __host__ __device__ constexpr int group_threads(bool wg) { return wg ? 128 : 256; }
@@ -76,6 +83,14 @@ struct BwdParams {
     long long cs_rows, cs_width;
     int cs_vec;  // cos/sin rows 16-byte aligned: float4 loads
     int a3d, b3d;  // operand maps are 3-D chunk views (one TMA op per operand and stage)
+    // wgrad channel tiles by head pair (see tile_chunks); tiles per pair
+    int paired, tiles_per_pair;
+    // wgrad: rope-pair tiles load already rotated values (no transform)
+    int pre;
+    // dgrad: rotated rope channels out, [T, H, Dr] bf16 (nullable; each head's
+    // channels written by the units of column tile head mod num_n_tiles)
+    uint16_t* rope_out;
+    int H, Dr;
     uint16_t* out;
     int out_rows, out_cols;
     // work units: each tile's reduction split in ksplit parts of kts stages
@@ -148,11 +163,46 @@ __device__ __forceinline__ bool has_rope(const BwdParams& p, int n0, int width) 
     return rs < n0 + width && rs < p.N;
 }
 
+// Work unit u -> its tile and split. Units run split-major: the CTAs of a
+// wave share one slice of the reduction, so each slice of the reused operand
+// (W for dgrad) is read from DRAM about once instead of once per wave.
+__device__ __forceinline__ void unit_split(const BwdParams& p, int u, int& tile, int& sp) {
+    sp = u / p.num_tiles;
+    tile = u - sp * p.num_tiles;
+}
+
 // Work unit u -> its tile and stage range [k0, k1).
 __device__ __forceinline__ void unit_range(const BwdParams& p, int u, int& tile, int& k0, int& k1) {
-    tile = u / p.ksplit;
-    k0 = (u - tile * p.ksplit) * p.kts;
+    int sp;
+    unit_split(p, u, tile, sp);
+    k0 = sp * p.kts;
     k1 = min(p.k_tiles, k0 + p.kts);
+}
+
+// wgrad: channel starts of the two 64-channel chunks of channel tile mt
+// (a start >= N means that half is empty) and whether it is a rope pair.
+// Contiguous tiles [128 mt, 128 mt + 128) in general. With heads paired
+// (rope dim 64, pass-through dim a multiple of 128, even H), each head pair
+// has its pass-through chunks in tiles of 128 contiguous channels, then one
+// tile holding both heads' 64 rope channels: only a third of the tiles need
+// the inverse rotation, and each cos/sin row serves two heads.
+__device__ __forceinline__ void tile_chunks(const BwdParams& p, int mt, int& c0, int& c1, bool& rope_pair) {
+    rope_pair = false;
+    if (!p.paired) {
+        c0 = mt * kBM;
+        c1 = c0 + 64;
+        return;
+    }
+    const int g = mt / p.tiles_per_pair, k = mt - g * p.tiles_per_pair;
+    const int nh = p.Dn / 128;  // pass-through tiles per head
+    if (k < 2 * nh) {
+        c0 = (2 * g + k / nh) * p.D + (k % nh) * 128;
+        c1 = c0 + 64;
+    } else {
+        c0 = 2 * g * p.D + p.Dn;
+        c1 = c0 + p.D;
+        rope_pair = true;
+    }
 }
 
 // Walks a CTA's stages (its tiles, each k-tile of each) and says which go
@@ -165,20 +215,29 @@ struct StageWalk {
     int mt = 0, nt = 0;
     bool tile_x = false;  // wgrad: the tile's stages are transform stages
     int c0 = 0;           // dgrad: channel phase (kt * 64) mod D of the current stage
+    // wgrad: the tile's two chunk starts, and the A operand's TMA source:
+    // rope view (head pair) or chunk view / 2-D map; az = its 3rd coordinate
+    int w0 = 0, w1 = 0, az = 0;
+    bool rope_pair = false;
     __device__ void begin_tile(const BwdParams& p, int tile, int k0) {
         mt = tile / p.num_n_tiles;
         nt = tile % p.num_n_tiles;
-        c0 = WG ? 0 : (k0 * bk_of(false)) % p.D;
-        if (WG) tile_x = has_rope(p, mt * kBM, kBM) || (p.db != nullptr && nt == 0);
+        c0 = WG ? 0 : (k0 * kBKD) % p.D;
+        if (WG) {
+            tile_chunks(p, mt, w0, w1, rope_pair);
+            const bool rot = rope_pair ? !p.pre : (has_rope(p, w0, 64) || has_rope(p, w1, 64));
+            tile_x = rot || (p.db != nullptr && nt == 0);
+            az = rope_pair ? (w0 - p.Dn) / p.D : w0 / 64;
+        }
     }
     __device__ bool needs(const BwdParams& p, int kt) const {
         if (WG) return tile_x;
         const int off = (c0 <= p.Dn) ? (p.Dn - c0) : (p.D + p.Dn - c0);  // next rope region start
-        return off < bk_of(false) && kt * bk_of(false) + off < p.N;
+        return off < kBKD && kt * kBKD + off < p.N;
     }
     __device__ void next(const BwdParams& p) {
         if (!WG) {
-            c0 += bk_of(false);
+            c0 += kBKD;
             while (c0 >= p.D) c0 -= p.D;
         }
     }
@@ -190,8 +249,10 @@ struct StageWalk {
 //   out[i]        =  g[i] cos[p, i] + g[i+h] sin[p, i+h]
 //   out[i + h]    = -g[i] sin[p, i] + g[i+h] cos[p, i+h]     (h = Dr / 2)
 // ci/si: cos, sin at i; cj/sj: cos, sin at i + h (8 consecutive pairs).
+// gout (nullable): global copy of the 8 rotated values at i; gout + h gets those at i + h.
 __device__ __forceinline__ void rot8(uint32_t row_addr, int r, int q1, int q2, const float* ci,
-                                     const float* si, const float* cj, const float* sj) {
+                                     const float* si, const float* cj, const float* sj,
+                                     uint16_t* gout = nullptr, int h = 0) {
     const uint32_t a1 = row_addr + (uint32_t)((q1 ^ (r & 7)) * 16);
     const uint32_t a2 = row_addr + (uint32_t)((q2 ^ (r & 7)) * 16);
     uint32_t g1[4], g2[4];
@@ -208,6 +269,10 @@ __device__ __forceinline__ void rot8(uint32_t row_addr, int r, int q1, int q2, c
     }
     sts_v4(a1, o1);
     sts_v4(a2, o2);
+    if (gout != nullptr) {
+        st_global_v4(gout, o1[0], o1[1], o1[2], o1[3]);
+        st_global_v4(gout + h, o2[0], o2[1], o2[2], o2[3]);
+    }
 }
 
 // Position row of token t, or -1 (recorded) when outside the table.
@@ -220,9 +285,10 @@ __device__ __forceinline__ int pos_row(const BwdParams& p, int64_t t) {
     return (int)pp;
 }
 
-template <bool WG, int DR>
+template <bool WG, int DR, int BK>
 __global__ void __launch_bounds__(bwd_threads(WG), 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmR,
                const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -266,8 +332,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int nb_chunks = p.BN / 64;
-    constexpr int BK = bk_of(WG);
-    constexpr uint32_t CH = chunk_of(WG);
+    constexpr uint32_t CH = (uint32_t)BK * 128u;  // bytes of one 64-wide MN-major chunk
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -309,12 +374,15 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     if (!WG) {
                         // A: dq rows [mt*128, +128) x channels [kt*64, +64)
                         tma_load_2d(sm.a(s, p), &tmA, kt * BK, mt * kBM, fb);
-                    } else if (p.a3d) {
-                        // A: dq^T, both 64-channel chunks of the tile, tokens [kt*BK, +BK)
-                        tma_load_3d(sm.a(s, p), &tmA, 0, kt * BK, mt * 2, fb);
                     } else {
-                        tma_load_2d(sm.a(s, p), &tmA, mt * kBM, kt * BK, fb);
-                        tma_load_2d(sm.a(s, p) + CH, &tmA, mt * kBM + 64, kt * BK, fb);
+                        // A: dq^T, the tile's two 64-channel chunks, tokens [kt*BK, +BK)
+                        // (rope pair: the rope view, heads 2g and 2g+1, head stride D)
+                        if (walk.rope_pair || p.a3d)
+                            tma_load_3d(sm.a(s, p), walk.rope_pair ? &tmR : &tmA, 0, kt * BK, walk.az, fb);
+                        else {
+                            tma_load_2d(sm.a(s, p), &tmA, walk.w0, kt * BK, fb);
+                            tma_load_2d(sm.a(s, p) + CH, &tmA, walk.w1, kt * BK, fb);
+                        }
                     }
                     // B: 64-column chunks of W (dgrad, rows = channels) or x (wgrad, rows = tokens)
                     if (p.b3d) {
@@ -406,14 +474,21 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         const int row = quad * 32 + lane;
         int local = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
-            const int tile = u / p.ksplit, sp = u - tile * p.ksplit;
+            int tile, sp;
+            unit_split(p, u, tile, sp);
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
             tc_fence_after();
             const int mt = tile / p.num_n_tiles;
             const int nt = tile % p.num_n_tiles;
-            const int64_t orow = (int64_t)mt * kBM + row;
+            int64_t orow = (int64_t)mt * kBM + row;  // dgrad: token; wgrad: channel
+            if (WG) {
+                int c0, c1;
+                bool rp;
+                tile_chunks(p, mt, c0, c1, rp);
+                orow = (row < 64 ? c0 : c1) + (row & 63);
+            }
             const bool valid = orow < p.out_rows;
             const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
             for (int col = 0; col < p.BN; col += 32) {
@@ -495,7 +570,17 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     }
                 }
             } else {
-                nreg = rope_regions(p, mt * kBM, kBM, reg);
+                // rope regions of the tile, as offsets in its 128 rows
+                int c0, c1;
+                bool rp;
+                tile_chunks(p, mt, c0, c1, rp);
+                // (rotating wgrad only: 32-token stages, 4 threads per token row)
+                if (BK == kBKW && !(rp && p.pre)) {
+                    int r0[8], r1[8];
+                    const int n0r = rope_regions(p, c0, 64, r0), n1r = rope_regions(p, c1, 64, r1);
+                    for (int j = 0; j < n0r && nreg < 8; ++j) reg[nreg++] = r0[j] - c0;
+                    for (int j = 0; j < n1r && nreg < 8; ++j) reg[nreg++] = 64 + r1[j] - c1;
+                }
             }
             for (int kt = k0; kt < k1; ++kt) {
                 const bool nx = walk.needs(p, kt);
@@ -521,10 +606,17 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     for (int j = 0; j < n; ++j) {
                         if ((j * IPR + kpart) % TPR != sub) continue;
                         const int q0 = (st[j] - kt * BK + pb) / 8;
+                        // rope_out[t, head, pb ...]: the rotated values, stored once per
+                        // token by the column tile nt = head mod (column tiles), so
+                        // every unit carries an equal share of the stores
+                        const int head = st[j] / p.D;
+                        uint16_t* g = (p.rope_out != nullptr && head % p.num_n_tiles == nt)
+                                          ? p.rope_out + ((int64_t)(mt * kBM + r) * p.H + head) * DR + pb
+                                          : nullptr;
 #pragma unroll
-                        for (int g = 0; g < PPI / 8; ++g)
-                            rot8(a0 + (uint32_t)r * 128, r, q0 + g, q0 + g + HH / 8, ci + 8 * g, si + 8 * g,
-                                 cj + 8 * g, sj + 8 * g);
+                        for (int e = 0; e < PPI / 8; ++e)
+                            rot8(a0 + (uint32_t)r * 128, r, q0 + e, q0 + e + HH / 8, ci + 8 * e, si + 8 * e,
+                                 cj + 8 * e, sj + 8 * e, g ? g + 8 * e : nullptr, HH);
                         wrote = true;
                     }
                 } else {
@@ -551,7 +643,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                         const uint32_t a0 = sm.a(s, p);
                         for (int j = 0; j < nreg; ++j) {
                             if ((j * IPR + kpart) % TPR != sub) continue;
-                            const int o = reg[j] - mt * kBM;  // channel offset in the tile
+                            const int o = reg[j];  // channel offset in the tile
                             const uint32_t row = a0 + (uint32_t)(o / 64) * CH + (uint32_t)r * 128;
                             const int q0 = (o % 64 + pb) / 8;
 #pragma unroll
@@ -597,7 +689,10 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                         s0 += db_part[q * 128 + 2 * pp];
                         s1v += db_part[q * 128 + 2 * pp + 1];
                     }
-                    const int64_t n = (int64_t)mt * kBM + 2 * pp;
+                    int c0, c1;
+                    bool rp;
+                    tile_chunks(p, mt, c0, c1, rp);
+                    const int64_t n = (int64_t)(pp < 32 ? c0 : c1) + 2 * (pp & 31);
                     const uint32_t packed = pack_bf16x2(s0, s1v);
                     if (n + 1 < p.N)
                         *reinterpret_cast<uint32_t*>(p.db + n) = packed;
@@ -619,23 +714,33 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     }
 }
 
-template <bool WG>
-int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const BwdParams& p, int grid,
-              size_t smem, cudaStream_t stream) {
+template <bool WG, int BK>
+int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr, const BwdParams& p,
+              int grid, size_t smem, cudaStream_t stream) {
     const void* k = nullptr;
     switch (Dr) {
-        case 16: k = (const void*)bwd_kernel<WG, 16>; break;
-        case 32: k = (const void*)bwd_kernel<WG, 32>; break;
-        case 64: k = (const void*)bwd_kernel<WG, 64>; break;
+        case 16: k = (const void*)bwd_kernel<WG, 16, BK>; break;
+        case 32: k = (const void*)bwd_kernel<WG, 32, BK>; break;
+        case 64: k = (const void*)bwd_kernel<WG, 64, BK>; break;
         default: return MLA_ERR_UNSUPPORTED;
     }
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MLA_ERR_CUDA;
     switch (Dr) {
-        case 16: bwd_kernel<WG, 16><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, p); break;
-        case 32: bwd_kernel<WG, 32><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, p); break;
-        default: bwd_kernel<WG, 64><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, p); break;
+        case 16: bwd_kernel<WG, 16, BK><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, tr, p); break;
+        case 32: bwd_kernel<WG, 32, BK><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, tr, p); break;
+        default: bwd_kernel<WG, 64, BK><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, tr, p); break;
     }
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// wgrad with pre-rotated rope tiles: head pairs only, so Dr = 64
+int launch_wgrad_pre(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr, const BwdParams& p,
+                     int grid, size_t smem, cudaStream_t stream) {
+    const void* k = (const void*)bwd_kernel<true, 64, kBKWPre>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    bwd_kernel<true, 64, kBKWPre><<<grid, bwd_threads(true), smem, stream>>>(ta, tb, tr, p);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -673,14 +778,25 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     int bn = (int)((a.K + 63) / 64) * 64;
     p.BN = bn > 256 ? 256 : bn;
     p.num_m_tiles = (int)(((wg ? N : a.T) + kBM - 1) / kBM);
+    // wgrad: tiles by head pair when the rope part is one 64-channel chunk
+    p.paired = wg && a.Dr == 64 && a.Dn % 128 == 0 && a.H % 2 == 0 && N % 64 == 0;
+    if (p.paired) {
+        p.tiles_per_pair = a.Dn / 64 + 1;
+        p.num_m_tiles = (a.H / 2) * p.tiles_per_pair;
+    }
+    p.pre = p.paired && a.rope_in != nullptr;
+    p.rope_out = wg ? nullptr : static_cast<uint16_t*>(a.rope_out);
+    p.H = a.H;
+    p.Dr = a.Dr;
     p.num_n_tiles = (int)((a.K + p.BN - 1) / p.BN);
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
-    const int BK = bk_of(wg);
+    const int BK = wg ? (p.pre ? kBKWPre : kBKW) : kBKD;
+    const uint32_t CH = (uint32_t)BK * 128u;
     p.k_tiles = (int)(((wg ? a.T : N) + BK - 1) / BK);
     // A: 128 token rows of 64 channels (dgrad) or two 64-channel chunks of BK
     // token rows (wgrad); B: BN/64 chunks of BK rows
-    p.a_bytes = wg ? 2u * chunk_of(true) : (uint32_t)kBM * 128u;
-    p.stage_bytes = p.a_bytes + (uint32_t)(p.BN / 64) * chunk_of(wg);
+    p.a_bytes = wg ? 2u * CH : (uint32_t)kBM * 128u;
+    p.stage_bytes = p.a_bytes + (uint32_t)(p.BN / 64) * CH;
     p.tx_bytes = p.stage_bytes;
     p.idesc = idesc_bf16(kBM, (uint32_t)p.BN, wg ? 1u : 0u, 1u);
     p.pos = a.pos;
@@ -715,7 +831,8 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     p.stages = stages;
     const size_t smem = fixed + (size_t)stages * p.stage_bytes;
 
-    alignas(64) CUtensorMap ta, tb;
+    alignas(64) CUtensorMap ta, tb, tr;
+    memset(&tr, 0, sizeof(tr));
     // one TMA operation per MN-major operand and stage when its columns come
     // in whole 64-element chunks; else one per chunk
     if (!wg) {
@@ -726,6 +843,16 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
             st = make_tmap_2d(&tb, a.W, 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * 2, 64, BK, true);
     } else {
         p.a3d = (N % 128 == 0) && make_tmap_chunks(&ta, a.dq, (uint64_t)a.T, (uint64_t)N, BK, 2) == MLA_OK;
+        if (p.paired) {
+            // rope tiles: {64 rope channels, T tokens, H heads} views of the
+            // rotated buffer [T, H, 64] or of dq (head stride D channels)
+            const int r = p.pre ? make_tmap_3d(&tr, a.rope_in, 64, (uint64_t)a.T, (uint64_t)a.H,
+                                               (uint64_t)a.H * 128, 128, 64, BK, 2)
+                                : make_tmap_3d(&tr, static_cast<const uint16_t*>(a.dq) + a.Dn, 64, (uint64_t)a.T,
+                                               (uint64_t)a.H, (uint64_t)N * 2, (uint64_t)D * 2, 64, BK, 2);
+            if (r != MLA_OK) return MLA_ERR_CUDA;
+            if (!p.a3d) return MLA_ERR_CUDA;  // paired tiles load pass-through chunks with the chunk view
+        }
         if (!p.a3d) st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, BK, true);
         p.b3d = (a.K % 64 == 0) &&
                 make_tmap_chunks(&tb, a.x, (uint64_t)a.T, (uint64_t)a.K, BK, (uint32_t)(p.BN / 64)) == MLA_OK;
@@ -734,8 +861,9 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     }
     if (st != MLA_OK) return st;
     const int grid = p.num_units < di.num_sms ? p.num_units : di.num_sms;
-    st = wg ? launch_dr<true>(a.Dr, ta, tb, p, grid, smem, stream)
-            : launch_dr<false>(a.Dr, ta, tb, p, grid, smem, stream);
+    st = !wg     ? launch_dr<false, kBKD>(a.Dr, ta, tb, tr, p, grid, smem, stream)
+         : p.pre ? launch_wgrad_pre(ta, tb, tr, p, grid, smem, stream)
+                 : launch_dr<true, kBKW>(a.Dr, ta, tb, tr, p, grid, smem, stream);
     if (st != MLA_OK || p.ksplit == 1) return st;
     const int64_t n = a.T * a.K;
     int64_t blocks = (n / 8 + 255) / 256;
@@ -752,7 +880,7 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
 int dgrad_ksplit(int64_t T, int64_t K, int64_t N, int num_sms) {
     if (num_sms <= 0) return 1;
     const int64_t tiles = ((T + kBM - 1) / kBM) * ((K + 255) / 256);
-    const int64_t k_tiles = (N + bk_of(false) - 1) / bk_of(false);
+    const int64_t k_tiles = (N + kBKD - 1) / kBKD;
     int best = 1;
     double best_eff = 0.0;
     for (int sp = 1; sp <= 4; ++sp) {

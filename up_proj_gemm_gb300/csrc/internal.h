@@ -33,6 +33,11 @@ int make_tmap_2d(void* tmap_out /* CUtensorMap, 64 B aligned */, const void* bas
 int make_tmap_chunks(void* tmap_out, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_chunks);
 
+// General 3-D bf16 map, 128-byte swizzle: dims {d0 (contiguous), d1, d2},
+// byte strides of d1 and d2, box {b0, b1, b2} (b0 * 2 bytes == 128).
+int make_tmap_3d(void* tmap_out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                 uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2);
+
 // ------------------------------------------------------------- launchers
 // All launchers assume arguments were validated by the API layer.
 int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
@@ -70,6 +75,8 @@ struct BwdArgs {
     void* dx;        // dgrad
     void* dW;        // wgrad
     void* db;        // wgrad, nullable
+    void* rope_out;       // dgrad, nullable: rotated rope channels [T, H, Dr] bf16
+    const void* rope_in;  // wgrad, nullable: the same buffer, read instead of rotating dq
     void* workspace; // dgrad split partials (see dgrad_workspace_bytes)
     size_t ws_bytes;
     int* status;
