@@ -249,10 +249,10 @@ struct StageWalk {
 //   out[i]        =  g[i] cos[p, i] + g[i+h] sin[p, i+h]
 //   out[i + h]    = -g[i] sin[p, i] + g[i+h] cos[p, i+h]     (h = Dr / 2)
 // ci/si: cos, sin at i; cj/sj: cos, sin at i + h (8 consecutive pairs).
-// gout (nullable): global copy of the 8 rotated values at i; gout + h gets those at i + h.
+// o (nullable): the rotated values as written (bf16 pairs: 4 words at i, 4 at i + h).
 __device__ __forceinline__ void rot8(uint32_t row_addr, int r, int q1, int q2, const float* ci,
                                      const float* si, const float* cj, const float* sj,
-                                     uint16_t* gout = nullptr, int h = 0) {
+                                     uint32_t* o = nullptr) {
     const uint32_t a1 = row_addr + (uint32_t)((q1 ^ (r & 7)) * 16);
     const uint32_t a2 = row_addr + (uint32_t)((q2 ^ (r & 7)) * 16);
     uint32_t g1[4], g2[4];
@@ -269,9 +269,12 @@ __device__ __forceinline__ void rot8(uint32_t row_addr, int r, int q1, int q2, c
     }
     sts_v4(a1, o1);
     sts_v4(a2, o2);
-    if (gout != nullptr) {
-        st_global_v4(gout, o1[0], o1[1], o1[2], o1[3]);
-        st_global_v4(gout + h, o2[0], o2[1], o2[2], o2[3]);
+    if (o != nullptr) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            o[w] = o1[w];
+            o[4 + w] = o2[w];
+        }
     }
 }
 
@@ -598,25 +601,41 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 const uint32_t xp = (xpar >> s) & 1u;
                 xpar ^= 1u << s;
                 bool wrote = false;
+                // dgrad: rotated values still to be stored to rope_out once the
+                // stage is released. A thread rotates at most two groups of 8
+                // pairs per 64-channel stage: E = 2 groups of one region when
+                // Dr = 64, else one group of each of at most two regions.
+                constexpr int E = PPI / 8;
+                uint32_t v[2][8];
+                uint16_t* ga = nullptr;
+                uint16_t* gb = nullptr;
                 if (!WG) {
                     const bool ok = mbar_wait(xbar, xp, abort_flag);
                     const uint32_t a0 = sm.a(s, p);
                     int st[8];
                     const int n = (ok && drow >= 0) ? rope_regions(p, kt * BK, BK, st) : 0;
+                    int taken = 0;
                     for (int j = 0; j < n; ++j) {
                         if ((j * IPR + kpart) % TPR != sub) continue;
                         const int q0 = (st[j] - kt * BK + pb) / 8;
-                        // rope_out[t, head, pb ...]: the rotated values, stored once per
-                        // token by the column tile nt = head mod (column tiles), so
-                        // every unit carries an equal share of the stores
+                        // rope_out[t, head, pb ...]: stored once per token, by the column
+                        // tile nt = head mod (column tiles), so every unit carries an
+                        // equal share of the stores
                         const int head = st[j] / p.D;
                         uint16_t* g = (p.rope_out != nullptr && head % p.num_n_tiles == nt)
                                           ? p.rope_out + ((int64_t)(mt * kBM + r) * p.H + head) * DR + pb
                                           : nullptr;
+                        if (E == 2 || taken == 0) {
 #pragma unroll
-                        for (int e = 0; e < PPI / 8; ++e)
-                            rot8(a0 + (uint32_t)r * 128, r, q0 + e, q0 + e + HH / 8, ci + 8 * e, si + 8 * e,
-                                 cj + 8 * e, sj + 8 * e, g ? g + 8 * e : nullptr, HH);
+                            for (int e = 0; e < E; ++e)
+                                rot8(a0 + (uint32_t)r * 128, r, q0 + e, q0 + e + HH / 8, ci + 8 * e, si + 8 * e,
+                                     cj + 8 * e, sj + 8 * e, v[e]);
+                            ga = g;
+                        } else {
+                            rot8(a0 + (uint32_t)r * 128, r, q0, q0 + HH / 8, ci, si, cj, sj, v[1]);
+                            gb = g;
+                        }
+                        ++taken;
                         wrote = true;
                     }
                 } else {
@@ -674,6 +693,19 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.ready(s));
+                if (!WG) {  // after the release: off the MMA's path
+                    if (ga != nullptr) {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            st_global_v4(ga + 8 * e, v[e][0], v[e][1], v[e][2], v[e][3]);
+                            st_global_v4(ga + 8 * e + HH, v[e][4], v[e][5], v[e][6], v[e][7]);
+                        }
+                    }
+                    if (E == 1 && gb != nullptr) {
+                        st_global_v4(gb, v[1][0], v[1][1], v[1][2], v[1][3]);
+                        st_global_v4(gb + HH, v[1][4], v[1][5], v[1][6], v[1][7]);
+                    }
+                }
                 if (++s == p.stages) s = 0;
             }
             if (do_db) {
