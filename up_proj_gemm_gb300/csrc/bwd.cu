@@ -91,6 +91,9 @@ struct BwdParams {
     // channels written by the units of column tile head mod num_n_tiles)
     uint16_t* rope_out;
     int H, Dr;
+    // dgrad: slots of the A ring and of the B ring, bytes of one B slot
+    int sa_slots, sb_slots;
+    uint32_t b_bytes;
     uint16_t* out;
     int out_rows, out_cols;
     // work units: each tile's reduction split in ksplit parts of kts stages
@@ -746,6 +749,355 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     }
 }
 
+// ----------------------------------------------------------------- dgrad
+// dgrad with separate rings for its two operands. A (dq tiles, 16 KB, the
+// ones the transform rotates) has SA slots and its own producer; B (W
+// chunks, BN/64 x 8 KB) has SB slots and another producer. With SA > SB a
+// rope tile lands and is rotated up to SA stages before the MMA needs it,
+// which hides the load + rotation latency that a shared ring of 48 KB stages
+// (4 deep) exposed at every rope stage.
+//
+// Warps: 0 A producer, 1 MMA issuer, 2-5 epilogue, 6-13 transform (one
+// group, two threads per token row), 14 B producer.
+constexpr int kDgThreads = 480;
+constexpr int kDgBWarp = 14;
+constexpr uint32_t kDgABytes = (uint32_t)kBM * 128u;  // 128 token rows x 64 channels (bf16)
+
+struct DgSmem {
+    uint32_t abase, bbase, bars;
+    int SA, SB;
+    uint32_t bbytes;
+    __device__ uint32_t a(int s) const { return abase + (uint32_t)s * kDgABytes; }
+    __device__ uint32_t b(int s) const { return bbase + (uint32_t)s * bbytes; }
+    // afull: A landed; aready: A rotated (transform stages); aempty: A consumed
+    __device__ uint32_t afull(int s) const { return bars + 8u * s; }
+    __device__ uint32_t aready(int s) const { return bars + 8u * (SA + s); }
+    __device__ uint32_t aempty(int s) const { return bars + 8u * (2 * SA + s); }
+    __device__ uint32_t bfull(int s) const { return bars + 8u * (3 * SA + s); }
+    __device__ uint32_t bempty(int s) const { return bars + 8u * (3 * SA + SB + s); }
+    __device__ uint32_t tfull(int b) const { return bars + 8u * (3 * SA + 2 * SB + b); }
+    __device__ uint32_t tempty(int b) const { return bars + 8u * (3 * SA + 2 * SB + 2 + b); }
+    __device__ uint32_t drain() const { return bars + 8u * (3 * SA + 2 * SB + 4); }
+};
+__host__ __device__ constexpr int dg_bar_count(int SA, int SB) { return 3 * SA + 2 * SB + 5; }
+
+template <int DR>
+__global__ void __launch_bounds__(kDgThreads, 1)
+    dgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    DgSmem sm;
+    sm.SA = p.sa_slots;
+    sm.SB = p.sb_slots;
+    sm.bbytes = p.b_bytes;
+    sm.abase = (raw + 1023u) & ~1023u;
+    sm.bbase = sm.abase + (uint32_t)sm.SA * kDgABytes;
+    sm.bars = sm.bbase + (uint32_t)sm.SB * sm.bbytes;
+    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * dg_bar_count(sm.SA, sm.SB);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr int BK = kBKD;
+    constexpr uint32_t CHB = (uint32_t)BK * 128u;  // one 64-column chunk of B (BK rows)
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < sm.SA; ++s) {
+            mbar_init(sm.afull(s), 1);
+            mbar_init(sm.aready(s), 8);  // the transform's 8 warps
+            mbar_init(sm.aempty(s), 1);
+        }
+        for (int s = 0; s < sm.SB; ++s) {
+            mbar_init(sm.bfull(s), 1);
+            mbar_init(sm.bempty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sm.tfull(b), 1);
+            mbar_init(sm.tempty(b), 4);
+        }
+        mbar_init(sm.drain(), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32((const void*)tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nb_chunks = p.BN / 64;
+
+    if (warp == 0 || warp == kDgBWarp) {
+        // ------------------------------------------- TMA producers (A / B)
+        if (lane == 0) {
+            const bool is_a = warp == 0;
+            const int S = is_a ? sm.SA : sm.SB;
+            int s = 0;
+            uint32_t ph = 0, issued_mask = 0, issued_par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                int tile, k0, k1;
+                unit_range(p, u, tile, k0, k1);
+                const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
+                for (int kt = k0; kt < k1; ++kt) {
+                    if (!mbar_wait(is_a ? sm.aempty(s) : sm.bempty(s), ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (is_a) {
+                        // dq rows [mt*128, +128) x channels [kt*64, +64)
+                        mbar_arrive_expect_tx(sm.afull(s), kDgABytes);
+                        tma_load_2d(sm.a(s), &tmA, kt * BK, mt * kBM, sm.afull(s));
+                    } else {
+                        // W rows (channels) [kt*64, +64), columns in BN/64 chunks
+                        mbar_arrive_expect_tx(sm.bfull(s), sm.bbytes);
+                        if (p.b3d) {
+                            tma_load_3d(sm.b(s), &tmB, 0, kt * BK, nt * nb_chunks, sm.bfull(s));
+                        } else {
+                            for (int c = 0; c < nb_chunks; ++c)
+                                tma_load_2d(sm.b(s) + (uint32_t)c * CHB, &tmB, nt * p.BN + 64 * c, kt * BK,
+                                            sm.bfull(s));
+                        }
+                    }
+                    issued_mask |= 1u << s;
+                    issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // unwinding: let every copy this thread started land before the CTA exits
+                for (int q = 0; q < S; ++q)
+                    if (issued_mask & (1u << q))
+                        mbar_wait(is_a ? sm.afull(q) : sm.bfull(q), (issued_par >> q) & 1u, nullptr,
+                                  200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int sa = 0, sb = 0;
+            uint32_t pha = 0, phb = 0, rpar = 0;  // rpar: per-slot parity of aready
+            int local = 0;
+            StageWalk<false> walk;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++local) {
+                int tile, k0, k1;
+                unit_range(p, u, tile, k0, k1);
+                const int b = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!mbar_wait(sm.tempty(b), (use & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)b * kAccStride;
+                walk.begin_tile(p, tile, k0);
+                for (int kt = k0; kt < k1; ++kt, walk.next(p)) {
+                    const bool xf = walk.needs(p, kt);
+                    bool w = xf ? mbar_wait(sm.aready(sa), (rpar >> sa) & 1u, abort_flag)
+                                : mbar_wait(sm.afull(sa), pha, abort_flag);
+                    w = w && mbar_wait(sm.bfull(sb), phb, abort_flag);
+                    if (!w) {
+                        ok = false;
+                        break;
+                    }
+                    if (xf) rpar ^= 1u << sa;
+                    tc_fence_after();
+                    const uint32_t a0 = sm.a(sa), b0 = sm.b(sb);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)
+                        mma_bf16(d_tmem, desc_kmajor_sw128(a0 + 32u * j), desc_mnmajor_sw128(b0 + 2048u * j, CHB),
+                                 p.idesc, (kt != k0 || j != 0));
+                    mma_commit(sm.aempty(sa));
+                    mma_commit(sm.bempty(sb));
+                    if (++sa == sm.SA) {
+                        sa = 0;
+                        pha ^= 1u;
+                    }
+                    if (++sb == sm.SB) {
+                        sb = 0;
+                        phb ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(sm.tfull(b));
+            }
+            if (!ok) {
+                mma_commit(sm.drain());
+                mbar_wait(sm.drain(), 0, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp < kXformWarp0) {
+        // ---------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        int local = 0;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
+            int tile, sp;
+            unit_split(p, u, tile, sp);
+            const int b = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int mt = tile / p.num_n_tiles;
+            const int nt = tile % p.num_n_tiles;
+            const int64_t orow = (int64_t)mt * kBM + row;  // token
+            const bool valid = orow < p.out_rows;
+            const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
+            for (int col = 0; col < p.BN; col += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld32(trow + col, r);
+                tmem_ld_wait();
+                const int64_t c0 = (int64_t)nt * p.BN + col;
+                if (valid && p.ws) {
+                    // partial sum of split sp, fp32
+                    float* dst = p.ws + ((int64_t)sp * p.out_rows + orow) * p.out_cols + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        if (c0 + i + 4 <= p.out_cols) st_global_v4(dst + i, r[i], r[i + 1], r[i + 2], r[i + 3]);
+                } else if (valid) {
+                    uint16_t* dst = p.out + orow * p.out_cols + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        if (c0 + i + 8 <= p.out_cols)
+                            st_global_v4(dst + i,
+                                         pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                         pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                         pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
+                                         pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.tempty(b));
+        }
+    } else {
+        // --------------------------------------------------------- transform
+        // inverse RoPE on the rope channels of each transform stage's A tile,
+        // in place; thread = (token row r, sub) with TPR = 2 threads per row,
+        // each taking PPI pairs of the regions assigned to it
+        constexpr int HH = DR / 2;
+        constexpr int TPR = 2;
+        constexpr int PPI = (HH / TPR >= 8) ? HH / TPR : 8;
+        constexpr int IPR = HH / PPI;
+        constexpr int E = PPI / 8;  // groups of 8 pairs per item
+        // A warp takes 16 token rows; lanes l and l + 16 share row l. The 8 lanes
+        // of each 16-byte shared-memory access phase then sit on 8 different
+        // rows, whose swizzled chunks fall in 8 different bank groups.
+        const int xw = warp - kXformWarp0;  // 0..7
+        const int r = xw * 16 + (lane & 15), sub = lane >> 4;
+        const int kpart = sub % IPR;
+        const int pb = kpart * PPI;
+        const bool vec = p.cs_vec != 0;
+        int sa = 0;
+        uint32_t pha = 0;
+        StageWalk<false> walk;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            int tile, k0, k1;
+            unit_range(p, u, tile, k0, k1);
+            const int mt = tile / p.num_n_tiles;
+            const int nt = tile % p.num_n_tiles;
+            walk.begin_tile(p, tile, k0);
+            // cos/sin of this thread's pairs for its token, kept for the whole unit
+            float ci[PPI], si[PPI], cj[PPI], sj[PPI];
+            int drow = -1;
+            const int64_t tok = (int64_t)mt * kBM + r;
+            if (tok < p.T) drow = pos_row(p, tok);
+            if (drow >= 0) {
+                const float* cr = p.cos_tab + (int64_t)drow * p.cs_width + pb;
+                const float* sr = p.sin_tab + (int64_t)drow * p.cs_width + pb;
+#pragma unroll
+                for (int q = 0; q < PPI; q += 8) {
+                    load8(cr + q, vec, ci + q);
+                    load8(sr + q, vec, si + q);
+                    load8(cr + HH + q, vec, cj + q);
+                    load8(sr + HH + q, vec, sj + q);
+                }
+            }
+            for (int kt = k0; kt < k1; ++kt) {
+                const bool nx = walk.needs(p, kt);
+                walk.next(p);
+                if (nx) {
+                    const bool ok = mbar_wait(sm.afull(sa), pha, abort_flag);
+                    const uint32_t a0 = sm.a(sa);
+                    int st[8];
+                    const int n = (ok && drow >= 0) ? rope_regions(p, kt * BK, BK, st) : 0;
+                    // rotated values still to be stored to rope_out once the stage is
+                    // released: at most two groups of 8 pairs per thread and stage
+                    uint32_t v[2][8];
+                    uint16_t* ga = nullptr;
+                    uint16_t* gb = nullptr;
+                    bool wrote = false;
+                    int taken = 0;
+                    for (int j = 0; j < n; ++j) {
+                        if ((j * IPR + kpart) % TPR != sub) continue;
+                        const int q0 = (st[j] - kt * BK + pb) / 8;
+                        // rope_out[t, head, pb ...]: stored once per token, by the column
+                        // tile nt = head mod (column tiles)
+                        const int head = st[j] / p.D;
+                        uint16_t* g = (p.rope_out != nullptr && head % p.num_n_tiles == nt)
+                                          ? p.rope_out + (tok * p.H + head) * DR + pb
+                                          : nullptr;
+                        if (E == 2 || taken == 0) {
+#pragma unroll
+                            for (int e = 0; e < E; ++e)
+                                rot8(a0 + (uint32_t)r * 128, r, q0 + e, q0 + e + HH / 8, ci + 8 * e, si + 8 * e,
+                                     cj + 8 * e, sj + 8 * e, v[e]);
+                            ga = g;
+                        } else {
+                            rot8(a0 + (uint32_t)r * 128, r, q0, q0 + HH / 8, ci, si, cj, sj, v[1]);
+                            gb = g;
+                        }
+                        ++taken;
+                        wrote = true;
+                    }
+                    if (wrote) fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sm.aready(sa));
+                    if (ga != nullptr) {  // after the release: off the MMA's path
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            st_global_v4(ga + 8 * e, v[e][0], v[e][1], v[e][2], v[e][3]);
+                            st_global_v4(ga + 8 * e + HH, v[e][4], v[e][5], v[e][6], v[e][7]);
+                        }
+                    }
+                    if (E == 1 && gb != nullptr) {
+                        st_global_v4(gb, v[1][0], v[1][1], v[1][2], v[1][3]);
+                        st_global_v4(gb + HH, v[1][4], v[1][5], v[1][6], v[1][7]);
+                    }
+                }
+                if (++sa == sm.SA) {
+                    sa = 0;
+                    pha ^= 1u;
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) record_status(p.status, MLA_ERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
 template <bool WG, int BK>
 int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr, const BwdParams& p,
               int grid, size_t smem, cudaStream_t stream) {
@@ -854,6 +1206,48 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
         if (cudaMemsetAsync(a.dW, 0, (size_t)N * a.K * 2, stream) != cudaSuccess) return MLA_ERR_CUDA;
         if (a.db && cudaMemsetAsync(a.db, 0, (size_t)N * 2, stream) != cudaSuccess) return MLA_ERR_CUDA;
         return MLA_OK;
+    }
+
+    if (!wg) {
+        // separate rings: 4 B slots, as many 16 KB A slots as fit (at most 12)
+        const size_t fixed = 1024 + 512;  // alignment slack + barriers, TMEM slot, abort flag
+        p.b_bytes = (uint32_t)(p.BN / 64) * CH;
+        p.sb_slots = 4;
+        const size_t room = (size_t)di.max_smem_optin - fixed - (size_t)p.sb_slots * p.b_bytes;
+        int sa = (int)(room / (size_t)kBM / 128u);
+        if (sa > 12) sa = 12;
+        if (sa < p.sb_slots) return MLA_ERR_UNSUPPORTED;
+        p.sa_slots = sa;
+        const size_t smem = fixed + (size_t)sa * kBM * 128u + (size_t)p.sb_slots * p.b_bytes;
+        alignas(64) CUtensorMap ta, tb;
+        st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, kBM, true);
+        p.b3d = (a.K % 64 == 0) &&
+                make_tmap_chunks(&tb, a.W, (uint64_t)N, (uint64_t)a.K, BK, (uint32_t)(p.BN / 64)) == MLA_OK;
+        if (st == MLA_OK && !p.b3d)
+            st = make_tmap_2d(&tb, a.W, 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * 2, 64, BK, true);
+        if (st != MLA_OK) return st;
+        const int grid = p.num_units < di.num_sms ? p.num_units : di.num_sms;
+        const void* k = nullptr;
+        switch (a.Dr) {
+            case 16: k = (const void*)dgrad_kernel<16>; break;
+            case 32: k = (const void*)dgrad_kernel<32>; break;
+            case 64: k = (const void*)dgrad_kernel<64>; break;
+            default: return MLA_ERR_UNSUPPORTED;
+        }
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return MLA_ERR_CUDA;
+        switch (a.Dr) {
+            case 16: dgrad_kernel<16><<<grid, kDgThreads, smem, stream>>>(ta, tb, p); break;
+            case 32: dgrad_kernel<32><<<grid, kDgThreads, smem, stream>>>(ta, tb, p); break;
+            default: dgrad_kernel<64><<<grid, kDgThreads, smem, stream>>>(ta, tb, p); break;
+        }
+        if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+        if (p.ksplit == 1) return MLA_OK;
+        const int64_t n = a.T * a.K;
+        int64_t blocks = (n / 8 + 255) / 256;
+        if (blocks > (int64_t)di.num_sms * 8) blocks = (int64_t)di.num_sms * 8;
+        dgrad_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p.ws, p.ksplit, n, static_cast<uint16_t*>(a.dx));
+        return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
     }
 
     const size_t fixed = 1024 + 4096;  // alignment slack + barriers, slots, bias partials
