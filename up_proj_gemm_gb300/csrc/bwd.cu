@@ -8,8 +8,8 @@
 //   bgrad  db[N]    = sum_t dq_pre[t, N]          (review: "BF16 bias gradient
 //                                                   remains missing")
 // The pages run the RoPE backward as its own Triton kernel and hand dq_pre
-// to a library GEMM. Here dq_pre never exists in memory: dq tiles land in
-// shared memory by TMA, four "transform" warps rotate the rope channels of
+// to a library GEMM. Here the full dq_pre never exists in memory: dq tiles
+// land in shared memory by TMA, "transform" warps rotate the rope channels of
 // each tile in place (fp32 math, rounded to bf16, the MMA operand type),
 // fence them into the async proxy and release the stage to the MMA thread.
 //
@@ -19,27 +19,25 @@
 // runs once, in dgrad's operand path, where each thread reads its cos/sin row
 // once per tile, instead of once per 32-token stage in every wgrad tile.
 //
-// Warp roles (persistent, one CTA per SM):
-//   warp 0     TMA producer (S-stage ring, 128-byte swizzle)
-//   warp 1     single-thread tcgen05.mma issuer, double-buffered TMEM acc
-//   warps 2-5  epilogue: TMEM -> bf16 -> global (16-byte stores)
-//   warps 6-   transform: inverse RoPE in shared memory; for wgrad also the
-//              per-channel token sums that make db (tiles of the first K
-//              block only), deterministic, no atomics.
-//              dgrad: one group of 4 warps. Each thread owns one token row
-//              of its tile for the whole reduction, so it reads its cos/sin
-//              row once per tile and keeps it in registers.
-//              wgrad: three groups of 4 warps taking turns on stages (every
-//              stage brings 64 new tokens, so each needs fresh table rows;
-//              three stages in flight hide the table loads). Two threads
-//              share a token row; the table loads are issued before the
-//              stage's TMA data is awaited.
+// Two persistent kernels (one CTA per SM), both with a single-thread
+// tcgen05.mma issuer, double-buffered TMEM accumulators and 128-byte-swizzled
+// TMA stages:
 //
-// Operand layouts (D = A B^T in tcgen05 terms, M = 128 rows):
-//   dgrad: A = dq   [T x N] K-major (tokens x channels), B = W [N x K]
-//          MN-major (K contiguous); reduction over channels, 64 per stage.
-//   wgrad: A = dq^T MN-major (channels contiguous), B = x [T x K] MN-major;
-//          reduction over tokens, 64 per stage.
+//   dgrad_kernel: A = dq [T x N] K-major (tokens x channels), B = W [N x K]
+//     MN-major (K contiguous); reduction over channels, 64 per stage. A and B
+//     have separate rings and producers (warps 0 and 14) so that dq tiles,
+//     the ones the transform rewrites, are fetched further ahead. Warps 2-5
+//     epilogue (bf16 dx, or fp32 partials when the reduction is split),
+//     warps 6-13 transform: each thread owns half of one token row for a
+//     whole work unit and keeps that row's cos/sin in registers.
+//   wgrad_kernel: A = dq^T MN-major (channels contiguous), B = x [T x K]
+//     MN-major; reduction over tokens. Warps 0 producer, 1 MMA, 2-5 epilogue,
+//     then three transform groups of 4 warps taking turns on stages (each
+//     stage brings new tokens, so new table rows); they also sum db over the
+//     tokens on the first column tile (fixed order, no atomics). Given the
+//     buffer dgrad stored, the rope tiles arrive rotated and the stages are
+//     64 tokens; otherwise 32.
+//
 // In both, a shared-memory "row" is 128 bytes = 64 consecutive channels of
 // one token, which is what the transform rewrites.
 #include <cuda.h>
@@ -61,12 +59,10 @@ constexpr int kXformWarp0 = 6;
 // rotates (its stages each need fresh cos/sin rows: a deeper ring of smaller
 // stages), 64 for a wgrad whose rope tiles come rotated.
 constexpr int kBKD = 64, kBKW = 32, kBKWPre = 64;
-// transform groups taking turns on stages, and threads per group
-__host__ __device__ constexpr int xform_groups(bool wg) { return wg ? 3 : 1; }
-__host__ __device__ constexpr int group_threads(bool wg) { return wg ? 128 : 256; }
-__host__ __device__ constexpr int bwd_threads(bool wg) {
-    return 32 * kXformWarp0 + group_threads(wg) * xform_groups(wg);
-}
+// wgrad: transform groups taking turns on stages, threads per group, block size
+constexpr int kWgGroups = 3;
+constexpr int kWgGroupThreads = 128;
+constexpr int kWgThreads = 32 * kXformWarp0 + kWgGroupThreads * kWgGroups;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;
 
@@ -291,9 +287,9 @@ __device__ __forceinline__ int pos_row(const BwdParams& p, int64_t t) {
     return (int)pp;
 }
 
-template <bool WG, int DR, int BK>
-__global__ void __launch_bounds__(bwd_threads(WG), 1)
-    bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+template <int DR, int BK>
+__global__ void __launch_bounds__(kWgThreads, 1)
+    wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmR,
                const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -302,7 +298,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     sm.S = p.stages;
     sm.base = (raw + 1023u) & ~1023u;
     sm.bars = sm.base + (uint32_t)p.stages * p.stage_bytes;
-    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * ((3 + xform_groups(WG)) * p.stages + 5);
+    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * ((3 + kWgGroups) * p.stages + 5);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
     float* db_part = reinterpret_cast<float*>(tail + 16);  // 2 x groups x 128 floats (wgrad bias sums)
@@ -313,9 +309,9 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(sm.full(s), 1);
-            mbar_init(sm.ready(s), group_threads(WG) / 32);
+            mbar_init(sm.ready(s), kWgGroupThreads / 32);
             mbar_init(sm.empty(s), 1);
-            for (int g = 0; g < xform_groups(WG); ++g) mbar_init(sm.xfull(g, s), 1);
+            for (int g = 0; g < kWgGroups; ++g) mbar_init(sm.xfull(g, s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.tfull(b), 1);
@@ -348,13 +344,13 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         // per-slot parity of each barrier's next use (full, and xfull of groups 0..2),
         // and which barrier each slot's last use went to (2 bits: 0 full, g+1 xfull g)
         uint32_t fpar = 0, xp0 = 0, xp1 = 0, xp2 = 0, last_kind = 0, issued_mask = 0;
-        StageWalk<WG> walk;
+        StageWalk<true> walk;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
             int tile, k0, k1;
             unit_range(p, u, tile, k0, k1);
             walk.begin_tile(p, tile, k0);
-            const int mt = walk.mt, nt = walk.nt;
+            const int nt = walk.nt;
             for (int kt = k0; kt < k1; ++kt, walk.next(p)) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                     ok = false;
@@ -364,7 +360,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 uint32_t kind = 0;
                 if (walk.needs(p, kt)) {
                     const int g = gnext;
-                    gnext = (gnext + 1 == xform_groups(WG)) ? 0 : gnext + 1;
+                    gnext = (gnext + 1 == kWgGroups) ? 0 : gnext + 1;
                     fb = sm.xfull(g, s);
                     if (g == 0) xp0 ^= 1u << s;
                     else if (g == 1) xp1 ^= 1u << s;
@@ -377,20 +373,15 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 last_kind = (last_kind & ~(3u << (2 * s))) | (kind << (2 * s));
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, p.tx_bytes);
-                    if (!WG) {
-                        // A: dq rows [mt*128, +128) x channels [kt*64, +64)
-                        tma_load_2d(sm.a(s, p), &tmA, kt * BK, mt * kBM, fb);
-                    } else {
-                        // A: dq^T, the tile's two 64-channel chunks, tokens [kt*BK, +BK)
-                        // (rope pair: the rope view, heads 2g and 2g+1, head stride D)
-                        if (walk.rope_pair || p.a3d)
-                            tma_load_3d(sm.a(s, p), walk.rope_pair ? &tmR : &tmA, 0, kt * BK, walk.az, fb);
-                        else {
-                            tma_load_2d(sm.a(s, p), &tmA, walk.w0, kt * BK, fb);
-                            tma_load_2d(sm.a(s, p) + CH, &tmA, walk.w1, kt * BK, fb);
-                        }
+                    // A: dq^T, the tile's two 64-channel chunks, tokens [kt*BK, +BK)
+                    // (rope pair: the rope view, heads 2g and 2g+1, head stride D)
+                    if (walk.rope_pair || p.a3d)
+                        tma_load_3d(sm.a(s, p), walk.rope_pair ? &tmR : &tmA, 0, kt * BK, walk.az, fb);
+                    else {
+                        tma_load_2d(sm.a(s, p), &tmA, walk.w0, kt * BK, fb);
+                        tma_load_2d(sm.a(s, p) + CH, &tmA, walk.w1, kt * BK, fb);
                     }
-                    // B: 64-column chunks of W (dgrad, rows = channels) or x (wgrad, rows = tokens)
+                    // B: 64-column chunks of x (rows = tokens)
                     if (p.b3d) {
                         tma_load_3d(sm.b(s, p), &tmB, 0, kt * BK, nt * nb_chunks, fb);
                     } else {
@@ -424,7 +415,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
             uint32_t ph = 0;
             int local = 0;
             uint32_t rpar = 0, fpar = 0;  // per-slot parities of the ready / full barriers
-            StageWalk<WG> walk;
+            StageWalk<true> walk;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++local) {
                 int tile, k0, k1;
@@ -453,10 +444,9 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                     const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j) {
-                        // 16 reduction rows per MMA: 32 bytes along a K-major row,
-                        // 16 rows of 128 bytes in an MN-major chunk
-                        const uint64_t ad = WG ? desc_mnmajor_sw128(a0 + 2048u * j, CH)
-                                               : desc_kmajor_sw128(a0 + 32u * j);
+                        // 16 reduction rows (tokens) per MMA: 16 rows of 128 bytes
+                        // in each MN-major chunk
+                        const uint64_t ad = desc_mnmajor_sw128(a0 + 2048u * j, CH);
                         const uint64_t bd = desc_mnmajor_sw128(b0 + 2048u * j, CH);
                         mma_bf16(d_tmem, ad, bd, p.idesc, (kt != k0 || j != 0));
                     }
@@ -480,21 +470,17 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         const int row = quad * 32 + lane;
         int local = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
-            int tile, sp;
-            unit_split(p, u, tile, sp);
+            const int tile = u;  // wgrad does not split its reduction
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
             tc_fence_after();
             const int mt = tile / p.num_n_tiles;
             const int nt = tile % p.num_n_tiles;
-            int64_t orow = (int64_t)mt * kBM + row;  // dgrad: token; wgrad: channel
-            if (WG) {
-                int c0, c1;
-                bool rp;
-                tile_chunks(p, mt, c0, c1, rp);
-                orow = (row < 64 ? c0 : c1) + (row & 63);
-            }
+            int c0, c1;
+            bool rp;
+            tile_chunks(p, mt, c0, c1, rp);
+            const int64_t orow = (row < 64 ? c0 : c1) + (row & 63);  // output channel
             const bool valid = orow < p.out_rows;
             const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
             for (int col = 0; col < p.BN; col += 32) {
@@ -502,18 +488,12 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 __syncwarp();
                 tmem_ld32(trow + col, r);
                 tmem_ld_wait();
-                const int64_t c0 = (int64_t)nt * p.BN + col;
-                if (valid && p.ws) {
-                    // partial sum of split sp, fp32
-                    float* dst = p.ws + ((int64_t)sp * p.out_rows + orow) * p.out_cols + c0;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        if (c0 + i + 4 <= p.out_cols) st_global_v4(dst + i, r[i], r[i + 1], r[i + 2], r[i + 3]);
-                } else if (valid) {
-                    uint16_t* dst = p.out + orow * p.out_cols + c0;
+                const int64_t kc = (int64_t)nt * p.BN + col;
+                if (valid) {
+                    uint16_t* dst = p.out + orow * p.out_cols + kc;
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) {
-                        if (c0 + i + 8 <= p.out_cols)
+                        if (kc + i + 8 <= p.out_cols)
                             st_global_v4(dst + i,
                                          pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
                                          pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
@@ -528,13 +508,13 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         }
     } else {
         // --------------------------------------------------------- transform
-        constexpr int G = xform_groups(WG);
-        constexpr int GT = group_threads(WG);
+        constexpr int G = kWgGroups;
+        constexpr int GT = kWgGroupThreads;
         constexpr int HH = DR / 2;
         // Work split of one stage: TPR threads per token row; each thread owns
         // the pairs [k PPI, (k + 1) PPI) of the rope regions it takes (region j
         // goes to the threads with (j * IPR + k) % TPR == sub).
-        constexpr int TPR = WG ? 4 : 2;
+        constexpr int TPR = 4;
         constexpr int PPI = (HH / TPR >= 8) ? HH / TPR : 8;  // pairs per item: 8 or 16
         constexpr int IPR = HH / PPI;                        // items per region: 1, 2 or 4
         const int xt = threadIdx.x - kXformWarp0 * 32;
@@ -547,35 +527,20 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
         int s = 0;
         uint32_t xpar = 0;  // per-slot parity of this group's next barrier use
         int gnext = 0;      // group owning the next transform stage
-        StageWalk<WG> walk;
+        StageWalk<true> walk;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             int tile, k0, k1;
             unit_range(p, u, tile, k0, k1);
             const int mt = tile / p.num_n_tiles;
             const int nt = tile % p.num_n_tiles;
-            const bool do_db = WG && p.db != nullptr && nt == 0;
+            const bool do_db = p.db != nullptr && nt == 0;
             walk.begin_tile(p, tile, k0);
             float acc0 = 0.f, acc1 = 0.f;
-            // cos/sin of this thread's pairs for its token (dgrad: fixed per tile)
+            // cos/sin of this thread's pairs for the token of the current stage
             float ci[PPI], si[PPI], cj[PPI], sj[PPI];
-            int drow = -1;
             int reg[8];
             int nreg = 0;
-            if (!WG) {
-                const int64_t t = (int64_t)mt * kBM + r;
-                if (t < p.T) drow = pos_row(p, t);
-                if (drow >= 0) {
-                    const float* cr = p.cos_tab + (int64_t)drow * p.cs_width + pb;
-                    const float* sr = p.sin_tab + (int64_t)drow * p.cs_width + pb;
-#pragma unroll
-                    for (int q = 0; q < PPI; q += 8) {
-                        load8(cr + q, vec, ci + q);
-                        load8(sr + q, vec, si + q);
-                        load8(cr + HH + q, vec, cj + q);
-                        load8(sr + HH + q, vec, sj + q);
-                    }
-                }
-            } else {
+            {
                 // rope regions of the tile, as offsets in its 128 rows
                 int c0, c1;
                 bool rp;
@@ -604,44 +569,7 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 const uint32_t xp = (xpar >> s) & 1u;
                 xpar ^= 1u << s;
                 bool wrote = false;
-                // dgrad: rotated values still to be stored to rope_out once the
-                // stage is released. A thread rotates at most two groups of 8
-                // pairs per 64-channel stage: E = 2 groups of one region when
-                // Dr = 64, else one group of each of at most two regions.
-                constexpr int E = PPI / 8;
-                uint32_t v[2][8];
-                uint16_t* ga = nullptr;
-                uint16_t* gb = nullptr;
-                if (!WG) {
-                    const bool ok = mbar_wait(xbar, xp, abort_flag);
-                    const uint32_t a0 = sm.a(s, p);
-                    int st[8];
-                    const int n = (ok && drow >= 0) ? rope_regions(p, kt * BK, BK, st) : 0;
-                    int taken = 0;
-                    for (int j = 0; j < n; ++j) {
-                        if ((j * IPR + kpart) % TPR != sub) continue;
-                        const int q0 = (st[j] - kt * BK + pb) / 8;
-                        // rope_out[t, head, pb ...]: stored once per token, by the column
-                        // tile nt = head mod (column tiles), so every unit carries an
-                        // equal share of the stores
-                        const int head = st[j] / p.D;
-                        uint16_t* g = (p.rope_out != nullptr && head % p.num_n_tiles == nt)
-                                          ? p.rope_out + ((int64_t)(mt * kBM + r) * p.H + head) * DR + pb
-                                          : nullptr;
-                        if (E == 2 || taken == 0) {
-#pragma unroll
-                            for (int e = 0; e < E; ++e)
-                                rot8(a0 + (uint32_t)r * 128, r, q0 + e, q0 + e + HH / 8, ci + 8 * e, si + 8 * e,
-                                     cj + 8 * e, sj + 8 * e, v[e]);
-                            ga = g;
-                        } else {
-                            rot8(a0 + (uint32_t)r * 128, r, q0, q0 + HH / 8, ci, si, cj, sj, v[1]);
-                            gb = g;
-                        }
-                        ++taken;
-                        wrote = true;
-                    }
-                } else {
+                {
                     const int64_t t = (int64_t)kt * BK + r;
                     bool mine = false;
                     for (int j = 0; j < nreg; ++j) mine |= ((j * IPR + kpart) % TPR == sub);
@@ -696,19 +624,6 @@ __global__ void __launch_bounds__(bwd_threads(WG), 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.ready(s));
-                if (!WG) {  // after the release: off the MMA's path
-                    if (ga != nullptr) {
-#pragma unroll
-                        for (int e = 0; e < E; ++e) {
-                            st_global_v4(ga + 8 * e, v[e][0], v[e][1], v[e][2], v[e][3]);
-                            st_global_v4(ga + 8 * e + HH, v[e][4], v[e][5], v[e][6], v[e][7]);
-                        }
-                    }
-                    if (E == 1 && gb != nullptr) {
-                        st_global_v4(gb, v[1][0], v[1][1], v[1][2], v[1][3]);
-                        st_global_v4(gb + HH, v[1][4], v[1][5], v[1][6], v[1][7]);
-                    }
-                }
                 if (++s == p.stages) s = 0;
             }
             if (do_db) {
@@ -1098,22 +1013,22 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     }
 }
 
-template <bool WG, int BK>
-int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr, const BwdParams& p,
-              int grid, size_t smem, cudaStream_t stream) {
+// wgrad rotating dq itself (32-token stages)
+int launch_wgrad_self(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr,
+                      const BwdParams& p, int grid, size_t smem, cudaStream_t stream) {
     const void* k = nullptr;
     switch (Dr) {
-        case 16: k = (const void*)bwd_kernel<WG, 16, BK>; break;
-        case 32: k = (const void*)bwd_kernel<WG, 32, BK>; break;
-        case 64: k = (const void*)bwd_kernel<WG, 64, BK>; break;
+        case 16: k = (const void*)wgrad_kernel<16, kBKW>; break;
+        case 32: k = (const void*)wgrad_kernel<32, kBKW>; break;
+        case 64: k = (const void*)wgrad_kernel<64, kBKW>; break;
         default: return MLA_ERR_UNSUPPORTED;
     }
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MLA_ERR_CUDA;
     switch (Dr) {
-        case 16: bwd_kernel<WG, 16, BK><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, tr, p); break;
-        case 32: bwd_kernel<WG, 32, BK><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, tr, p); break;
-        default: bwd_kernel<WG, 64, BK><<<grid, bwd_threads(WG), smem, stream>>>(ta, tb, tr, p); break;
+        case 16: wgrad_kernel<16, kBKW><<<grid, kWgThreads, smem, stream>>>(ta, tb, tr, p); break;
+        case 32: wgrad_kernel<32, kBKW><<<grid, kWgThreads, smem, stream>>>(ta, tb, tr, p); break;
+        default: wgrad_kernel<64, kBKW><<<grid, kWgThreads, smem, stream>>>(ta, tb, tr, p); break;
     }
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -1121,10 +1036,10 @@ int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 // wgrad with pre-rotated rope tiles: head pairs only, so Dr = 64
 int launch_wgrad_pre(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr, const BwdParams& p,
                      int grid, size_t smem, cudaStream_t stream) {
-    const void* k = (const void*)bwd_kernel<true, 64, kBKWPre>;
+    const void* k = (const void*)wgrad_kernel<64, kBKWPre>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MLA_ERR_CUDA;
-    bwd_kernel<true, 64, kBKWPre><<<grid, bwd_threads(true), smem, stream>>>(ta, tb, tr, p);
+    wgrad_kernel<64, kBKWPre><<<grid, kWgThreads, smem, stream>>>(ta, tb, tr, p);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -1287,9 +1202,8 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     }
     if (st != MLA_OK) return st;
     const int grid = p.num_units < di.num_sms ? p.num_units : di.num_sms;
-    st = !wg     ? launch_dr<false, kBKD>(a.Dr, ta, tb, tr, p, grid, smem, stream)
-         : p.pre ? launch_wgrad_pre(ta, tb, tr, p, grid, smem, stream)
-                 : launch_dr<true, kBKW>(a.Dr, ta, tb, tr, p, grid, smem, stream);
+    st = p.pre ? launch_wgrad_pre(ta, tb, tr, p, grid, smem, stream)
+               : launch_wgrad_self(a.Dr, ta, tb, tr, p, grid, smem, stream);
     if (st != MLA_OK || p.ksplit == 1) return st;
     const int64_t n = a.T * a.K;
     int64_t blocks = (n / 8 + 255) / 256;
