@@ -446,6 +446,14 @@ def run_only(args, w, inp, kernels, flush, stream, status, dev):
             mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], weight_mode="mxfp8",
                      out_mode="mxfp8", x_scales=xs, w_scales=Ws, q_out=qc, q_scales=qs, status=status)
         flop = w.fwd_flop()
+    elif args.only == "quant_cols":
+        a = torch.randn((w.T, w.N), device=dev).to(torch.bfloat16)
+        codes = torch.empty((w.N, w.T), dtype=torch.uint8, device=dev)
+        sc = torch.empty((w.N, w.T // 32), dtype=torch.uint8, device=dev)
+
+        def fn():
+            mlaq.mxfp8_quantize_cols(a, codes, sc)
+        flop = 0
     elif args.only == "quant":
         a = torch.randn((w.T, w.N), device=dev).to(torch.bfloat16)
         codes = torch.empty((w.T, w.N), dtype=torch.uint8, device=dev)
@@ -483,6 +491,19 @@ def run_parts(dev, stream, flush, pk, pk_src):
         byts = R * C * 2 + R * C + R * ((C + 31) // 32)
         gbs = byts / (ms * 1e-3) / 1e9
         parts[f"quantize_rows_bf16_{R}x{C}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                                "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                                                "algorithmic_bytes": byts}
+        del a, codes, sc
+
+    # columnwise copy (the transpose helper): dq [4096, 24576] and x [4096, 1536] reduced over tokens
+    for R, C in ((4096, 24576), (4096, 1536)):
+        a = torch.randn((R, C), device=dev, dtype=torch.float32).to(torch.bfloat16)
+        codes = torch.empty((C, R), dtype=torch.uint8, device=dev)
+        sc = torch.empty((C, (R + 31) // 32), dtype=torch.uint8, device=dev)
+        ms = time_loop(lambda: mlaq.mxfp8_quantize_cols(a, codes, sc), 20, flush, stream)
+        byts = R * C * 2 + R * C + C * ((R + 31) // 32)
+        gbs = byts / (ms * 1e-3) / 1e9
+        parts[f"quantize_cols_bf16_{R}x{C}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
                                                 "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
                                                 "algorithmic_bytes": byts}
         del a, codes, sc
@@ -638,7 +659,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "wgrad_self", "fwd_mxfp8w", "quant"),
+    ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "wgrad_self", "fwd_mxfp8w", "quant", "quant_cols"),
                     help="time one kernel alone (profiling)")
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -234,6 +234,20 @@ MLAQ_API int mla_q_uproj_bwd_dgrad_noalloc(const mla_q_shape *shape, const void 
 MLAQ_API int mxfp8_quantize_rows(int64_t R, int64_t C, int in_dtype, const void *in,
                                  int64_t ld_in, uint8_t *codes, uint8_t *scales, void *stream);
 
+/*
+ * Columnwise MXFP8 copy of in[R, C] (row pitch ld_in elements): the rowwise
+ * quantization of its transpose, for GEMM operands that are reduced over
+ * their rows. codes_t [C, R] uint8 (dense, pitch R) and scales_t
+ * [C, ceil(R/32)] uint8 (dense): blocks of 32 consecutive rows of one column
+ * (the last may be partial), same scale and element rule as
+ * mxfp8_quantize_rows. TransformerEngine PR "Add support for fused Q Up-Proj
+ * GEMM/RoPE/Quant", Greptile summary (the transpose among the MXFP8
+ * quantization helpers). Bit-exact; R = 0 or C = 0 is a no-op. Outputs may
+ * not overlap the input; pointers must be element-aligned.
+ */
+MLAQ_API int mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void *in,
+                                 int64_t ld_in, uint8_t *codes_t, uint8_t *scales_t, void *stream);
+
 /* which: 0 = forward, 1 = dgrad, 2 = wgrad. Bytes of device workspace the
  * call needs for this shape on the current device (0 = pass NULL). Only
  * dgrad ever needs any (see mla_q_uproj_bwd_dgrad). Returns 0 for an

@@ -160,6 +160,15 @@ def mxfp8_quantize(values: np.ndarray):
     return codes, scales
 
 
+def mxfp8_quantize_columns(values: np.ndarray):
+    """Columnwise MXFP8 of a 2-D float64 array [R, C]: blocks of 32 consecutive
+    rows of each column, i.e. the rowwise quantization of the transpose ->
+    (codes uint8 [C, R], scales uint8 [C, ceil(R/32)]). TransformerEngine PR
+    "Add support for fused Q Up-Proj GEMM/RoPE/Quant", Greptile summary (the
+    transpose among the MXFP8 quantization helpers)."""
+    return mxfp8_quantize(np.ascontiguousarray(np.asarray(values, np.float64).T))
+
+
 def linear(x: np.ndarray, W: np.ndarray, b=None) -> np.ndarray:
     """y = x W^T (+ b) in fp64; x [T, K], W [N, K], b [N]."""
     x = _c(x, np.float64)

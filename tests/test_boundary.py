@@ -12,6 +12,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import up_proj_gemm_gb300 as mlaq
 from up_proj_gemm_gb300 import _build
@@ -172,6 +173,26 @@ def test_quantize_rejects(L):
     assert q(4, 64, 0, ctypes.c_void_p(FAKE + 2), 64, p(1), p(2), None) == S["MLA_ERR_ALIGNMENT"]
     assert q(4, 64, 0, p(0), 64, ctypes.c_void_p(FAKE + 100), p(2), None) == S["MLA_ERR_ALIAS"]
     assert q(4, 64, 0, p(0), 64, p(1), p(1), None) == S["MLA_ERR_ALIAS"]
+
+
+def test_quantize_cols_rejects(L):
+    q = L.mxfp8_quantize_cols
+    assert q(64, 4, 0, p(0), 2, p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]   # ld < C
+    assert q(64, 4, 7, p(0), 4, p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]
+    assert q(64, 4, 0, None, 4, p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]
+    assert q(0, 4, 0, None, 4, None, None, None) == S["MLA_OK"]
+    assert q(64, 4, 0, ctypes.c_void_p(FAKE + 2), 4, p(1), p(2), None) == S["MLA_ERR_ALIGNMENT"]
+    assert q(64, 4, 0, p(0), 4, ctypes.c_void_p(FAKE + 100), p(2), None) == S["MLA_ERR_ALIAS"]
+    assert q(64, 4, 0, p(0), 4, p(1), p(1), None) == S["MLA_ERR_ALIAS"]
+
+
+def test_autograd_face_has_no_cpu_path():
+    from up_proj_gemm_gb300.autograd import q_up_proj
+    x = torch.zeros((4, 8), dtype=torch.bfloat16, requires_grad=True)
+    W = torch.zeros((12, 8), dtype=torch.bfloat16, requires_grad=True)
+    cs = torch.zeros((4, 4), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA"):
+        q_up_proj(x, W, cs, cs, 1, 8, 4)
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -159,3 +159,57 @@ def test_roundtrip_error_bound_and_saturation_free():
     # each block's largest magnitude rounds into [224, 448]
     amax_codes = (codes & 0x7F).reshape(64, 3, 32).max(axis=2)
     assert (amax_codes >= 0x76).all()  # amax * 2^-e lies in (224, 448]
+
+
+def _expected_block(vals, table):
+    """Independent reference for one block: scale byte and codes, from the
+    definition (smallest e with amax <= 448 * 2^e, clamped; nearest E4M3 of
+    v * 2^-e by exhaustive search, ties to the even code; NaN/Inf blocks ->
+    scale 0xFF and 0x7F codes with the element's sign)."""
+    pos_codes = np.arange(0x7F)
+    pos_vals = table[pos_codes]
+    if not np.all(np.isfinite(vals)):
+        return 0xFF, [0x7F | (0x80 if math.copysign(1.0, v) < 0 else 0) for v in vals]
+    amax = float(np.max(np.abs(vals))) if len(vals) else 0.0
+    if amax == 0.0:
+        e = -127
+    else:
+        e = math.ceil(math.log2(amax / 448.0))
+        while amax <= 448.0 * 2.0 ** (e - 1):
+            e -= 1
+        while amax > 448.0 * 2.0 ** e:
+            e += 1
+        e = max(-127, min(127, e))
+    codes = []
+    for v in vals:
+        a = abs(v) * 2.0 ** (-e)
+        d = np.abs(pos_vals - min(a, 448.0))
+        best = np.flatnonzero(d == d.min())
+        if best.size == 2:
+            best = best[(pos_codes[best] & 1) == 0]
+        c = int(pos_codes[best[0]])
+        codes.append(c | (0x80 if math.copysign(1.0, v) < 0 else 0))
+    return e + 127, codes
+
+
+def test_columnwise_blocks_run_down_columns():
+    """Columnwise quantization = blocks of 32 consecutive rows of a column,
+    written transposed: every code and scale of a 70 x 5 matrix (partial last
+    block, a zero block, a NaN block, signed zeros, wide magnitudes) against
+    the brute-force reference."""
+    rng = np.random.default_rng(77)
+    R, C = 70, 5
+    v = rng.standard_normal((R, C)) * np.exp2(rng.integers(-20, 20, (R, C)))
+    v[0:32, 1] = 0.0
+    v[5, 1] = -0.0
+    v[40, 2] = np.nan
+    v[64:70, 3] *= 1e-3
+    table = _all_code_values_torch()
+    codes_t, scales_t = oracle.mxfp8_quantize_columns(v)
+    assert codes_t.shape == (C, R) and scales_t.shape == (C, 3)
+    for c in range(C):
+        for blk in range(3):
+            rows = v[32 * blk:min(R, 32 * blk + 32), c]
+            sb, codes = _expected_block(rows, table)
+            assert scales_t[c, blk] == sb, (c, blk)
+            assert list(codes_t[c, 32 * blk:32 * blk + len(rows)]) == codes, (c, blk)

@@ -21,6 +21,7 @@ import torch
 
 __all__ = [
     "MlaError", "lib", "library_path", "fwd", "bwd_dgrad", "bwd_wgrad", "mxfp8_quantize_rows",
+    "mxfp8_quantize_cols",
     "workspace_size", "status_string", "check_status", "Shape", "STATUS",
 ]
 
@@ -63,6 +64,7 @@ _SIGS = {
     "mla_q_uproj_bwd_dgrad_noalloc": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                              _vp, _vp]),
     "mxfp8_quantize_rows": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
+    "mxfp8_quantize_cols": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
     "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
     "mla_status_string": (ctypes.c_char_p, [_int]),
     "mla_version": (_int, []),
@@ -272,5 +274,26 @@ def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None):
         scales = torch.empty((R, (C + 31) // 32), dtype=torch.uint8, device=dev)
     dt = 0 if inp.dtype == torch.float32 else 1
     _call(lib().mxfp8_quantize_rows, "mxfp8_quantize_rows", R, C, dt, _ptr(inp), ld_in, _ptr(codes),
+          _ptr(scales), _stream(dev, stream))
+    return codes, scales
+
+
+def mxfp8_quantize_cols(inp, codes=None, scales=None, stream=None):
+    """Columnwise MXFP8 of a 2-D fp32/bf16 CUDA tensor [R, C], i.e. the rowwise
+    quantization of its transpose -> (codes uint8 [C, R], scales uint8
+    [C, ceil(R/32)]). A row pitch larger than C is taken from ``inp.stride(0)``."""
+    if inp.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("input must be float32 or bfloat16")
+    if not inp.is_cuda or inp.dim() != 2 or inp.stride(1) != 1:
+        raise ValueError("input must be a 2-D CUDA tensor with unit inner stride")
+    R, C = inp.shape
+    ld_in = int(inp.stride(0)) if R > 1 else int(C)
+    dev = inp.device
+    if codes is None:
+        codes = torch.empty((C, R), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((C, (R + 31) // 32), dtype=torch.uint8, device=dev)
+    dt = 0 if inp.dtype == torch.float32 else 1
+    _call(lib().mxfp8_quantize_cols, "mxfp8_quantize_cols", R, C, dt, _ptr(inp), ld_in, _ptr(codes),
           _ptr(scales), _stream(dev, stream))
     return codes, scales

@@ -128,11 +128,6 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, const uint32_t (&v)[4]) {
                  "r"(v[3])
                  : "memory");
 }
-__device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
 
 __device__ __forceinline__ void load8(const float* p, bool vec, float* v) {
     if (vec) {

@@ -188,6 +188,15 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
 
 // Make this thread's generic-proxy writes to shared memory visible to later
 // async-proxy reads (TMA, tcgen05.mma / tcgen05.cp operand reads).
+__device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// cp.async (non-bulk) group bookkeeping
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

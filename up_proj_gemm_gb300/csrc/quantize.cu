@@ -176,6 +176,232 @@ int launch_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t* code
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// ------------------------------------------------------- columnwise copy
+// The MXFP8 copy along the other axis (TransformerEngine PR "Add support for
+// fused Q Up-Proj GEMM/RoPE/Quant", Greptile summary: the transpose helper
+// among the MXFP8 quantization helpers), for GEMM operands that are reduced
+// over their rows: codes_t [C, R] and scales_t [C, ceil(R/32)] are the
+// rowwise quantization of in^T, i.e. blocks of 32 consecutive rows of one
+// column.
+//
+// A CTA tile is 128 rows x 512 columns; each thread owns two adjacent
+// columns and walks the tile's four 32-row blocks: for every row it loads
+// its two elements (the warp reads 128 contiguous bytes of bf16 per row),
+// keeps the block's 32 values of each column in registers, quantizes them
+// and writes each column's 32 codes as one contiguous run of the output row.
+constexpr int kColThreads = 256;
+constexpr int kColTileR = 128;
+constexpr int kColTileC = 2 * kColThreads;
+
+__device__ __forceinline__ void load_pair(const float* p, bool both, float& a, float& b) {
+    if (both) {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(p));
+        a = v.x;
+        b = v.y;
+    } else {
+        a = __ldg(p);
+        b = 0.f;
+    }
+}
+__device__ __forceinline__ void load_pair(const __nv_bfloat16* p, bool both, float& a, float& b) {
+    if (both) {
+        const uint32_t v = __ldg(reinterpret_cast<const unsigned int*>(p));
+        a = bf16lo_to_f32(v);
+        b = bf16hi_to_f32(v);
+    } else {
+        a = load_elem(p);
+        b = 0.f;
+    }
+}
+
+// One column's block: n valid codes to dst (32-byte run when whole and aligned).
+__device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&w)[8], int n, bool vec) {
+    if (vec && n == 32) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+        for (int j = 0; j < n; ++j) dst[j] = (uint8_t)(w[j / 4] >> (8 * (j % 4)));
+    }
+}
+
+// PAIR: rows start 4-byte (bf16) / 8-byte (fp32) aligned, so a thread's two
+// columns load as one vector when both exist. VEC: R % 16 == 0 and codes_t
+// 16-byte aligned, so whole blocks store as two 16-byte vectors.
+template <typename Tin, bool PAIR, bool VEC>
+__global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_kernel(const Tin* __restrict__ in, int64_t R,
+                                                                      int64_t C, int64_t ld,
+                                                                      uint8_t* __restrict__ codes,
+                                                                      uint8_t* __restrict__ scales) {
+    const int64_t nbr = (R + 31) / 32;  // scale bytes per output row
+    const int64_t tiles_r = (R + kColTileR - 1) / kColTileR;
+    const int64_t tiles = tiles_r * ((C + kColTileC - 1) / kColTileC);
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t tr = tile % tiles_r, tc = tile / tiles_r;
+        const int64_t c = tc * kColTileC + 2 * (int64_t)threadIdx.x;  // first of this thread's columns
+        const bool has0 = c < C, has1 = c + 1 < C;
+#pragma unroll 1
+        for (int blk = 0; blk < kColTileR / 32; ++blk) {
+            const int64_t r0 = tr * kColTileR + 32 * blk;
+            if (r0 >= R) break;
+            const int n = (R - r0) < 32 ? (int)(R - r0) : 32;
+            float a[32], b[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                a[i] = 0.f;
+                b[i] = 0.f;
+                if (i < n && has0) {
+                    const Tin* src = in + (r0 + i) * ld + c;
+                    if (PAIR) {
+                        load_pair(src, has1, a[i], b[i]);
+                    } else {
+                        a[i] = load_elem(src);
+                        if (has1) b[i] = load_elem(src + 1);
+                    }
+                }
+            }
+            uint32_t wa[8], wb[8];
+            const uint32_t sa = quantize_block_regs<32>(a, n, wa);
+            const uint32_t sb = quantize_block_regs<32>(b, n, wb);
+            if (has0) {
+                store_codes(codes + c * R + r0, wa, n, VEC);
+                scales[c * nbr + r0 / 32] = (uint8_t)sa;
+            }
+            if (has1) {
+                store_codes(codes + (c + 1) * R + r0, wb, n, VEC);
+                scales[(c + 1) * nbr + r0 / 32] = (uint8_t)sb;
+            }
+        }
+    }
+}
+
+// Fast path: rows 16-byte aligned and C a multiple of the 16-byte vector.
+// A tile is 128 rows x 256 columns, loaded as four 32-row blocks with
+// 16-byte cp.async into a ring of shared-memory buffers (every warp load is
+// 512 contiguous bytes of a row); thread t then reads column t of a block
+// from shared memory (consecutive lanes, consecutive addresses), quantizes
+// it and writes its 32 codes as one run; the tile's 4 scale bytes of a
+// column leave as one 4-byte word when the scale rows allow it.
+constexpr int kColTC = 256;
+template <typename Tin>
+__host__ __device__ constexpr int cols_nbuf() { return sizeof(Tin) == 2 ? 4 : 2; }
+template <typename Tin>
+__host__ __device__ constexpr uint32_t cols_buf_bytes() { return 32u * kColTC * (uint32_t)sizeof(Tin); }
+
+template <typename Tin, bool VEC>
+__global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const Tin* __restrict__ in, int64_t R,
+                                                                     int64_t C, int64_t ld,
+                                                                     uint8_t* __restrict__ codes,
+                                                                     uint8_t* __restrict__ scales) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    constexpr int NBUF = cols_nbuf<Tin>();
+    constexpr uint32_t BUF = cols_buf_bytes<Tin>();
+    constexpr int EPV = 16 / (int)sizeof(Tin);      // elements per 16-byte vector
+    constexpr int VPR = kColTC / EPV;                // vectors per tile row
+    constexpr int VPT = 32 * VPR / kColThreads;      // vectors per thread per block
+    constexpr int NB = kColTileR / 32;               // blocks per tile
+    const uint32_t sbase = smem_u32(smem);
+    const int t = threadIdx.x;
+    const int64_t nbr = (R + 31) / 32;
+    const int64_t tiles_r = (R + kColTileR - 1) / kColTileR;
+    const int64_t tiles = tiles_r * ((C + kColTC - 1) / kColTC);
+    const bool word_scales = (nbr % 4) == 0 && (reinterpret_cast<uintptr_t>(scales) % 4) == 0;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t tr = tile % tiles_r, tc = tile / tiles_r;
+        const int64_t c0 = tc * kColTC;
+        auto issue = [&](int b) {
+            const int64_t r0 = tr * kColTileR + 32 * b;
+            const uint32_t buf = sbase + (uint32_t)(b % NBUF) * BUF;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int idx = t + k * kColThreads;
+                const int row = idx / VPR, vc = idx % VPR;
+                const int64_t r = r0 + row, c = c0 + (int64_t)vc * EPV;
+                const bool ok = r < R && c < C;
+                const Tin* src = ok ? in + r * ld + c : in;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(buf + (uint32_t)(row * kColTC * (int)sizeof(Tin) + vc * 16)),
+                             "l"(src), "r"(ok ? 16 : 0)
+                             : "memory");
+            }
+        };
+        for (int b = 0; b < NBUF - 1; ++b) {
+            if (b < NB) issue(b);
+            cp_async_commit();
+        }
+        const int64_t c = c0 + t;
+        uint32_t sword = 0;
+        for (int blk = 0; blk < NB; ++blk) {
+            if (blk + NBUF - 1 < NB) issue(blk + NBUF - 1);
+            cp_async_commit();
+            asm volatile("cp.async.wait_group %0;" ::"n"(NBUF - 1) : "memory");
+            __syncthreads();
+            const int64_t r0 = tr * kColTileR + 32 * blk;
+            if (r0 < R && c < C) {
+                const int n = (R - r0) < 32 ? (int)(R - r0) : 32;
+                const uint32_t buf = sbase + (uint32_t)(blk % NBUF) * BUF + (uint32_t)(t * (int)sizeof(Tin));
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const uint32_t a = buf + (uint32_t)(i * kColTC * (int)sizeof(Tin));
+                    if (sizeof(Tin) == 2) {
+                        uint16_t h;
+                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+                        v[i] = __uint_as_float((uint32_t)h << 16);
+                    } else {
+                        v[i] = __uint_as_float(lds_b32(a));
+                    }
+                }
+                uint32_t w[8];
+                const uint32_t sb = quantize_block_regs<32>(v, n, w);
+                store_codes(codes + c * R + r0, w, n, VEC);
+                if (word_scales) sword |= sb << (8 * blk);
+                else scales[c * nbr + r0 / 32] = (uint8_t)sb;
+            }
+            __syncthreads();  // the buffer may be refilled now
+        }
+        if (word_scales && c < C && tr * kColTileR < R)
+            *reinterpret_cast<uint32_t*>(scales + c * nbr + tr * NB) = sword;
+    }
+}
+
+template <typename Tin>
+int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t* codes, uint8_t* scales,
+                      cudaStream_t stream) {
+    DeviceInfo di;
+    int st = current_device_info(&di);
+    if (st != MLA_OK) return st;
+    const bool pair = (reinterpret_cast<uintptr_t>(in) % (2 * sizeof(Tin)) == 0) && (ld % 2 == 0);
+    const bool vec = (R % 16 == 0) && (reinterpret_cast<uintptr_t>(codes) % 16 == 0);
+    constexpr int EPV = 16 / (int)sizeof(Tin);
+    if (reinterpret_cast<uintptr_t>(in) % 16 == 0 && (ld * (int64_t)sizeof(Tin)) % 16 == 0 && C % EPV == 0) {
+        const size_t smem = (size_t)cols_nbuf<Tin>() * cols_buf_bytes<Tin>();
+        const int64_t tiles = ((R + kColTileR - 1) / kColTileR) * ((C + kColTC - 1) / kColTC);
+        int64_t blocks = tiles;
+        const int64_t cap = (int64_t)di.num_sms * 3;
+        if (blocks > cap) blocks = cap;
+        const Tin* p = static_cast<const Tin*>(in);
+        const void* k = vec ? (const void*)mxfp8_quantize_cols_tiled<Tin, true>
+                            : (const void*)mxfp8_quantize_cols_tiled<Tin, false>;
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return MLA_ERR_CUDA;
+        if (vec)
+            mxfp8_quantize_cols_tiled<Tin, true><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, scales);
+        else
+            mxfp8_quantize_cols_tiled<Tin, false><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, scales);
+        return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    }
+    const int64_t tiles = ((R + kColTileR - 1) / kColTileR) * ((C + kColTileC - 1) / kColTileC);
+    int64_t blocks = tiles;
+    const int64_t cap = (int64_t)di.num_sms * (2048 / kColThreads);
+    if (blocks > cap) blocks = cap;
+    const Tin* p = static_cast<const Tin*>(in);
+    const unsigned g = (unsigned)blocks;
+    if (pair && vec) mxfp8_quantize_cols_kernel<Tin, true, true><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, scales);
+    else if (pair) mxfp8_quantize_cols_kernel<Tin, true, false><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, scales);
+    else if (vec) mxfp8_quantize_cols_kernel<Tin, false, true><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, scales);
+    else mxfp8_quantize_cols_kernel<Tin, false, false><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, scales);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 }  // namespace
 
 int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
@@ -184,4 +410,12 @@ int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, in
     return launch_typed<__nv_bfloat16>(R, C, in, ld_in, codes, scales, stream);
 }
 
+}  // namespace mlaq
+
+namespace mlaq {
+int launch_mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                               uint8_t* codes_t, uint8_t* scales_t, cudaStream_t stream) {
+    if (in_dtype == MLA_IN_F32) return launch_cols_typed<float>(R, C, in, ld_in, codes_t, scales_t, stream);
+    return launch_cols_typed<__nv_bfloat16>(R, C, in, ld_in, codes_t, scales_t, stream);
+}
 }  // namespace mlaq
