@@ -73,7 +73,7 @@ enum {
 /* weight_mode */
 enum { MLA_WEIGHT_BF16 = 0, MLA_WEIGHT_MXFP8 = 1 };
 /* out_mode */
-enum { MLA_OUT_BF16 = 0, MLA_OUT_MXFP8 = 1 };
+enum { MLA_OUT_BF16 = 0, MLA_OUT_MXFP8 = 1, MLA_OUT_MXFP8_BHSD = 2 };
 /* in_dtype of mxfp8_quantize_rows */
 enum { MLA_IN_F32 = 0, MLA_IN_BF16 = 1 };
 
@@ -125,6 +125,11 @@ typedef struct {
  *               clamped to [-127, 127]; codes = RNE E4M3 of v * 2^-e with
  *               saturation; a block holding NaN/Inf gets scale 0xFF and NaN
  *               codes.
+ *   out_mode MLA_OUT_MXFP8_BHSD: the same codes, with the scales written
+ *               head-major, q_scales_out [H, T, ceil(D/32)] (the BHSD scale
+ *               order an attention kernel reading one head at a time wants;
+ *               TransformerEngine PR "Add support for fused Q Up-Proj
+ *               GEMM/RoPE/Quant", review thread: the BHSD scale transpose).
  * Tiling limits (else MLA_ERR_UNSUPPORTED): Dr in {16, 32, 64}, Dn % 32 == 0;
  * bf16 weights need K % 8 == 0 (16-byte rows). Pointers must be 16-byte
  * aligned (scales: 4-byte; bias: 16-byte), else MLA_ERR_ALIGNMENT.
@@ -247,6 +252,21 @@ MLAQ_API int mxfp8_quantize_rows(int64_t R, int64_t C, int in_dtype, const void 
  */
 MLAQ_API int mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void *in,
                                  int64_t ld_in, uint8_t *codes_t, uint8_t *scales_t, void *stream);
+
+/*
+ * E8M0 scales in the tiled order block-scaled GEMMs read (TransformerEngine PR
+ * "Add support for fused Q Up-Proj GEMM/RoPE/Quant": the GEMM scale swizzle
+ * among its MXFP8 helpers). in [rows, cols] row-major (pitch ld_in bytes),
+ * e.g. the scales of mxfp8_quantize_rows or of the forward's q (rows = T*H,
+ * cols = ceil(D/32)); out: mxfp8_swizzled_scale_bytes(rows, cols) bytes,
+ * 16-byte aligned: tiles of 128 rows x 4 columns (512 bytes), tile (i, j) at
+ * (i * ceil(cols/4) + j) * 512; row r, column c of a tile at byte
+ * (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4); bytes past rows or cols
+ * are 0. A pure byte permutation; rows = 0 or cols = 0 is a no-op.
+ */
+MLAQ_API size_t mxfp8_swizzled_scale_bytes(int64_t rows, int64_t cols);
+MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t *in, int64_t ld_in,
+                                  uint8_t *out, void *stream);
 
 /* which: 0 = forward, 1 = dgrad, 2 = wgrad. Bytes of device workspace the
  * call needs for this shape on the current device (0 = pass NULL). Only

@@ -169,6 +169,23 @@ def mxfp8_quantize_columns(values: np.ndarray):
     return mxfp8_quantize(np.ascontiguousarray(np.asarray(values, np.float64).T))
 
 
+def mxfp8_swizzle_scales(scales: np.ndarray) -> np.ndarray:
+    """Row-major E8M0 scales [rows, cols] -> the tiled order of block-scaled
+    GEMMs (TransformerEngine PR "Add support for fused Q Up-Proj
+    GEMM/RoPE/Quant": the GEMM scale swizzle): tiles of 128 rows x 4 columns,
+    512 bytes each, tile (i, j) at (i * ceil(cols/4) + j) * 512; inside, row r
+    and column c at (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4); padding 0.
+    Written out element by element from that definition."""
+    rows, cols = scales.shape
+    tiles_c = (cols + 3) // 4
+    out = np.zeros(((rows + 127) // 128) * 128 * tiles_c * 4, np.uint8)
+    for r in range(rows):
+        for c in range(cols):
+            tile = (r // 128) * tiles_c + c // 4
+            out[tile * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)] = scales[r, c]
+    return out
+
+
 def linear(x: np.ndarray, W: np.ndarray, b=None) -> np.ndarray:
     """y = x W^T (+ b) in fp64; x [T, K], W [N, K], b [N]."""
     x = _c(x, np.float64)

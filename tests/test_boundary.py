@@ -186,6 +186,22 @@ def test_quantize_cols_rejects(L):
     assert q(64, 4, 0, p(0), 4, p(1), p(1), None) == S["MLA_ERR_ALIAS"]
 
 
+def test_swizzle_rejects(L):
+    z = L.mxfp8_swizzle_scales
+    assert L.mxfp8_swizzled_scale_bytes(130, 5) == 2 * 128 * 8
+    assert L.mxfp8_swizzled_scale_bytes(0, 5) == 0
+    assert z(10, 4, p(0), 2, p(1), None) == S["MLA_ERR_INVALID_ARG"]          # ld < cols
+    assert z(10, 4, None, 4, p(1), None) == S["MLA_ERR_INVALID_ARG"]
+    assert z(0, 4, None, 4, None, None) == S["MLA_OK"]
+    assert z(10, 4, p(0), 4, ctypes.c_void_p(FAKE * 2 + 8), None) == S["MLA_ERR_ALIGNMENT"]
+    assert z(10, 4, p(0), 4, p(0), None) == S["MLA_ERR_ALIAS"]
+
+
+def test_fwd_accepts_bhsd_scale_mode(L):
+    assert fwd(L, shape(), om=2, qs=p(9)) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert fwd(L, shape(), om=3, qs=p(9)) == S["MLA_ERR_INVALID_ARG"]
+
+
 def test_autograd_face_has_no_cpu_path():
     from up_proj_gemm_gb300.autograd import q_up_proj
     x = torch.zeros((4, 8), dtype=torch.bfloat16, requires_grad=True)

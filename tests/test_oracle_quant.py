@@ -213,3 +213,32 @@ def test_columnwise_blocks_run_down_columns():
             sb, codes = _expected_block(rows, table)
             assert scales_t[c, blk] == sb, (c, blk)
             assert list(codes_t[c, 32 * blk:32 * blk + len(rows)]) == codes, (c, blk)
+
+
+def test_swizzle_hand_positions():
+    """Byte positions of the GEMM scale order, derived by hand from its
+    definition (tiles of 128 rows x 4 columns, 512 bytes; inside a tile row
+    r, column c at (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4) for a
+    130 x 5 scale matrix: 2 x 2 tiles, 2048 bytes."""
+    s = np.zeros((130, 5), np.uint8)
+    marks = {(0, 0): 1, (1, 0): 2, (32, 0): 3, (0, 1): 4, (127, 3): 5, (129, 4): 6, (2, 4): 7}
+    for (r, c), v in marks.items():
+        s[r, c] = v
+    out = oracle.mxfp8_swizzle_scales(s)
+    assert out.shape == (2048,)
+    expect = {0: 1, 16: 2, 4: 3, 1: 4, 31 * 16 + 3 * 4 + 3: 5,
+              3 * 512 + 1 * 16: 6,          # tile (1, 1): row 129 -> r % 32 = 1, block 0; column 4 -> 0
+              1 * 512 + 2 * 16: 7}          # tile (0, 1): row 2, column 4 -> 0
+    for pos, v in expect.items():
+        assert out[pos] == v, (pos, out[pos], v)
+    assert int(np.count_nonzero(out)) == len(marks)
+
+
+def test_swizzle_is_a_permutation_with_zero_padding():
+    rng = np.random.default_rng(5)
+    for rows, cols in ((1, 1), (37, 3), (128, 4), (300, 9)):
+        s = rng.integers(1, 256, (rows, cols)).astype(np.uint8)
+        out = oracle.mxfp8_swizzle_scales(s)
+        assert out.size == ((rows + 127) // 128) * 128 * ((cols + 3) // 4) * 4
+        assert np.array_equal(np.sort(out[out != 0]), np.sort(s.reshape(-1)))
+        assert int(np.count_nonzero(out)) == rows * cols

@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "MlaError", "lib", "library_path", "fwd", "bwd_dgrad", "bwd_wgrad", "mxfp8_quantize_rows",
-    "mxfp8_quantize_cols",
+    "mxfp8_quantize_cols", "mxfp8_swizzle_scales",
     "workspace_size", "status_string", "check_status", "Shape", "STATUS",
 ]
 
@@ -34,7 +34,7 @@ STATUS = {
     "MLA_ERR_POS_RANGE": 8, "MLA_ERR_WORKSPACE": 9,
 }
 WEIGHT_MODES = {"bf16": 0, "mxfp8": 1}
-OUT_MODES = {"bf16": 0, "mxfp8": 1}
+OUT_MODES = {"bf16": 0, "mxfp8": 1, "mxfp8_bhsd": 2}
 
 
 class Shape(ctypes.Structure):
@@ -65,6 +65,8 @@ _SIGS = {
                                              _vp, _vp]),
     "mxfp8_quantize_rows": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
     "mxfp8_quantize_cols": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
+    "mxfp8_swizzle_scales": (_int, [_i64, _i64, _vp, _i64, _vp, _vp]),
+    "mxfp8_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
     "mla_status_string": (ctypes.c_char_p, [_int]),
     "mla_version": (_int, []),
@@ -144,7 +146,8 @@ def workspace_size(T, K, H, Dn, Dr, cs_rows, cs_width, which: int) -> int:
 def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_mode="mxfp8",
         x_scales=None, w_scales=None, q_out=None, q_scales=None, status=None, stream=None):
     """Fused forward. Returns q [T, H, D] (bf16 or uint8 E4M3 codes), plus the
-    scales [T, H, ceil(D/32)] uint8 when out_mode is "mxfp8".
+    scales uint8 [T, H, ceil(D/32)] when out_mode is "mxfp8", or head-major
+    [H, T, ceil(D/32)] when it is "mxfp8_bhsd".
 
     weight_mode "bf16": x [T, K] bf16, W [N, K] bf16.
     weight_mode "mxfp8": x, W uint8 E4M3 codes with x_scales [T, K/32],
@@ -173,7 +176,8 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
     if q_out is None:
         q_out = torch.empty((T, H, D), dtype=torch.uint8 if om else torch.bfloat16, device=dev)
     if om and q_scales is None:
-        q_scales = torch.empty((T, H, (D + 31) // 32), dtype=torch.uint8, device=dev)
+        sshape = (H, T, (D + 31) // 32) if out_mode == "mxfp8_bhsd" else (T, H, (D + 31) // 32)
+        q_scales = torch.empty(sshape, dtype=torch.uint8, device=dev)
     s = _shape(T, K, H, Dn, Dr, cos)
     _call(lib().mla_q_uproj_fwd, "mla_q_uproj_fwd", ctypes.byref(s), wm, om, _ptr(x),
           _ptr(x_scales), _ptr(W), _ptr(w_scales), _ptr(bias), _ptr(cos), _ptr(sin), _ptr(pos),
@@ -297,3 +301,19 @@ def mxfp8_quantize_cols(inp, codes=None, scales=None, stream=None):
     _call(lib().mxfp8_quantize_cols, "mxfp8_quantize_cols", R, C, dt, _ptr(inp), ld_in, _ptr(codes),
           _ptr(scales), _stream(dev, stream))
     return codes, scales
+
+
+def mxfp8_swizzle_scales(scales, out=None, stream=None):
+    """Row-major E8M0 scales [rows, cols] (uint8 CUDA tensor, unit inner
+    stride) -> the 128 x 4 tiled order of block-scaled GEMMs, as a flat uint8
+    tensor of mxfp8_swizzled_scale_bytes(rows, cols) bytes."""
+    if scales.dtype != torch.uint8 or not scales.is_cuda or scales.dim() != 2 or scales.stride(1) != 1:
+        raise ValueError("scales must be a 2-D uint8 CUDA tensor with unit inner stride")
+    rows, cols = scales.shape
+    n = int(lib().mxfp8_swizzled_scale_bytes(rows, cols))
+    if out is None:
+        out = torch.empty((n,), dtype=torch.uint8, device=scales.device)
+    ld = int(scales.stride(0)) if rows > 1 else int(cols)
+    _call(lib().mxfp8_swizzle_scales, "mxfp8_swizzle_scales", rows, cols, _ptr(scales), ld, _ptr(out),
+          _stream(scales.device, stream))
+    return out

@@ -222,8 +222,9 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
     if (st != MLA_OK) return st;
     const mla_q_shape& s = *shape;
     if (weight_mode != MLA_WEIGHT_BF16 && weight_mode != MLA_WEIGHT_MXFP8) return MLA_ERR_INVALID_ARG;
-    if (out_mode != MLA_OUT_BF16 && out_mode != MLA_OUT_MXFP8) return MLA_ERR_INVALID_ARG;
-    const bool mxw = weight_mode == MLA_WEIGHT_MXFP8, mxo = out_mode == MLA_OUT_MXFP8;
+    if (out_mode != MLA_OUT_BF16 && out_mode != MLA_OUT_MXFP8 && out_mode != MLA_OUT_MXFP8_BHSD)
+        return MLA_ERR_INVALID_ARG;
+    const bool mxw = weight_mode == MLA_WEIGHT_MXFP8, mxo = out_mode != MLA_OUT_BF16;
     if (mxw != (x_scales != nullptr) || mxw != (w_scales != nullptr)) return MLA_ERR_INVALID_ARG;
     if (mxo != (q_scales_out != nullptr)) return MLA_ERR_INVALID_ARG;
     if (s.T > 0 && (!x || !W || !q_out)) return MLA_ERR_INVALID_ARG;
@@ -405,6 +406,23 @@ MLAQ_API int mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void*
     if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
     return launch_mxfp8_quantize_cols(R, C, in_dtype, in, ld_in, codes_t, scales_t,
                                       static_cast<cudaStream_t>(stream));
+}
+
+MLAQ_API size_t mxfp8_swizzled_scale_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return (size_t)((rows + 127) / 128) * 128 * (size_t)((cols + 3) / 4) * 4;
+}
+
+MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t* in, int64_t ld_in, uint8_t* out,
+                                  void* stream) {
+    if (rows < 0 || cols < 0 || ld_in < cols) return MLA_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MLA_OK;
+    if (!in || !out) return MLA_ERR_INVALID_ARG;
+    if (!aligned(out, 16)) return MLA_ERR_ALIGNMENT;
+    const Range outs[] = {rng(out, (int64_t)mxfp8_swizzled_scale_bytes(rows, cols))};
+    const Range ins[] = {rng(in, (rows - 1) * ld_in + cols)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    return launch_mxfp8_swizzle(rows, cols, in, ld_in, out, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -55,6 +55,7 @@ struct FwdParams {
     uint32_t slot_bytes;  // 32 rows x 16 channels x output element size
     int cs_vec;           // cos/sin rows 16-byte aligned: float4 loads
     int nslots;           // staging slots per epilogue warp
+    int scales_bhsd;      // MXFP8 scales head-major [H, T, NB] (else [T, H, NB])
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
                           // write each row's scale bytes as one 4-byte word (else: units
                           // alternate between them and scales go byte by byte)
@@ -153,7 +154,8 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
             if (p.split_half)
                 c.sword |= sb << (8 * (int)((n + 32 * blk) / 32 - c.sbase));
             else if (valid)
-                p.q_scales[(t * p.H + h) * NB + (cin + blk * 32) / 32] = (uint8_t)sb;
+                p.q_scales[(p.scales_bhsd ? (int64_t)h * p.T + t : t * p.H + h) * NB + (cin + blk * 32) / 32] =
+                    (uint8_t)sb;
         }
     } else {
 #pragma unroll
@@ -544,10 +546,11 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.status = a.status;
     p.cs_vec = (a.cs_width % 4 == 0) && (reinterpret_cast<uintptr_t>(a.cos_tab) % 16 == 0) &&
                (reinterpret_cast<uintptr_t>(a.sin_tab) % 16 == 0);
-    const bool mxo = a.out_mode == MLA_OUT_MXFP8;
+    const bool mxo = a.out_mode != MLA_OUT_BF16;
+    p.scales_bhsd = a.out_mode == MLA_OUT_MXFP8_BHSD;
     p.slot_bytes = 32u * kSlotCh * (mxo ? 1u : 2u);
     p.nslots = mxo ? 8 : 4;  // a unit takes at most 4 slots (64 rope channels)
-    p.split_half = mxo && D % 32 == 0 && BN % 128 == 0 && N % 128 == 0 &&
+    p.split_half = mxo && !p.scales_bhsd && D % 32 == 0 && BN % 128 == 0 && N % 128 == 0 &&
                    reinterpret_cast<uintptr_t>(a.q_scales) % 4 == 0 &&
                    fwd_tile_n(N, D, a.Dn, a.Dr, BN / 2, BN / 2) == BN / 2;
 
