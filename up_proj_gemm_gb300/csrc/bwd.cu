@@ -940,12 +940,13 @@ __global__ void __launch_bounds__(kDgThreads, 1)
             }
             for (int kt = k0; kt < k1; ++kt) {
                 const bool nx = walk.needs(p, kt);
+                // first rope region of the stage, as an offset in its 64 channels; the
+                // others follow every D channels (no array: local memory lives in L2 here)
+                const int off0 = (walk.c0 <= p.Dn) ? (p.Dn - walk.c0) : (p.D + p.Dn - walk.c0);
                 walk.next(p);
                 if (nx) {
                     const bool ok = mbar_wait(sm.afull(sa), pha, abort_flag);
                     const uint32_t a0 = sm.a(sa);
-                    int st[8];
-                    const int n = (ok && drow >= 0) ? rope_regions(p, kt * BK, BK, st) : 0;
                     // rotated values still to be stored to rope_out once the stage is
                     // released: at most two groups of 8 pairs per thread and stage
                     uint32_t v[2][8];
@@ -953,12 +954,13 @@ __global__ void __launch_bounds__(kDgThreads, 1)
                     uint16_t* gb = nullptr;
                     bool wrote = false;
                     int taken = 0;
-                    for (int j = 0; j < n; ++j) {
+                    int j = 0;
+                    for (int off = off0; ok && drow >= 0 && off < BK && kt * BK + off < p.N; off += p.D, ++j) {
                         if ((j * IPR + kpart) % TPR != sub) continue;
-                        const int q0 = (st[j] - kt * BK + pb) / 8;
+                        const int q0 = (off + pb) / 8;
                         // rope_out[t, head, pb ...]: stored once per token, by the column
                         // tile nt = head mod (column tiles)
-                        const int head = st[j] / p.D;
+                        const int head = (kt * BK + off) / p.D;
                         uint16_t* g = (p.rope_out != nullptr && head % p.num_n_tiles == nt)
                                           ? p.rope_out + (tok * p.H + head) * DR + pb
                                           : nullptr;
