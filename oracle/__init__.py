@@ -228,6 +228,23 @@ def rope_bwd(dq, H, Dn, Dr, cos, sin, pos=None) -> np.ndarray:
     return _rope(_load().oracle_rope_bwd, dq, H, Dn, Dr, cos, sin, pos)
 
 
+def kv_forward(c_kv, W, k_pe, H, Dn, Dv, Dr, cos, sin, pos=None):
+    """The KV side of the attention block (Megatron-LM PR "Fix fused MLA YaRN
+    RoPE query kernel corrupting upstream tensor in-place", Solution section:
+    the KV path writes fresh o_key and o_value buffers; the pages give no
+    formula, this is the plain MLA reading): kv = c_kv W^T as [T, H, Dn + Dv];
+    o_key [T, H, Dn + Dr] = the first Dn channels of each head followed by the
+    shared k_pe [T, Dr] rotated by rotate-half RoPE (same table and positions
+    as the query), the same for every head; o_value [T, H, Dv] = the last Dv
+    channels of each head. All float64 in, float64 out."""
+    c_kv = np.asarray(c_kv, np.float64)
+    T = c_kv.shape[0]
+    kv = linear(c_kv, W).reshape(T, H, Dn + Dv)
+    kr = rope_fwd(np.asarray(k_pe, np.float64).reshape(T, Dr), 1, 0, Dr, cos, sin, pos).reshape(T, 1, Dr)
+    o_key = np.concatenate([kv[:, :, :Dn], np.broadcast_to(kr, (T, H, Dr))], axis=2)
+    return o_key, np.ascontiguousarray(kv[:, :, Dn:])
+
+
 def dgrad(dq_pre: np.ndarray, W: np.ndarray) -> np.ndarray:
     """dx = dq_pre W; dq_pre [T, N], W [N, K] -> [T, K]."""
     g = _c(dq_pre.reshape(dq_pre.shape[0], -1), np.float64)
