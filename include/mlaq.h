@@ -195,6 +195,40 @@ MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape *shape, const void *dq, con
                                    const int32_t *pos, void *dW, void *db, void *workspace,
                                    size_t ws_bytes, int *dev_status, void *stream);
 
+/* KV side of the attention block: see mla_kv_uproj_fwd. */
+typedef struct {
+    int64_t T;        /* tokens */
+    int64_t K;        /* kv_lora_rank (columns of c_kv and of W) */
+    int32_t H;        /* heads */
+    int32_t Dn;       /* key channels from the up-projection, per head */
+    int32_t Dv;       /* value channels, per head */
+    int32_t Dr;       /* rope channels of the key (the shared k_pe) */
+    int64_t cs_rows;  /* cos/sin table rows */
+    int64_t cs_width; /* cos/sin table row pitch (elements), >= Dr */
+} mla_kv_shape;
+
+/*
+ * KV up-projection with the key's rope part, into fresh buffers: kv = c_kv W^T
+ * split per head into k_nope (Dn) and v (Dv); the shared k_pe [T, Dr] is
+ * rotated by the same rotate-half rule as the query (column j of the table
+ * for rope channel j, positions pos or t) and written after every head's
+ * k_nope. Megatron-LM PR "Fix fused MLA YaRN RoPE query kernel corrupting
+ * upstream tensor in-place", Solution section: the KV path (rotary kernel
+ * for the key) writes fresh o_key and o_value buffers; the split and the
+ * broadcast follow the MLA attention block (the pages give no formula).
+ *   c_kv [T, K] bf16, W [H*(Dn+Dv), K] bf16 (head h's rows: Dn key rows, then
+ *   Dv value rows), k_pe [T, Dr] bf16, cos/sin/pos as in the forward.
+ *   o_key [T, H, Dn + Dr] bf16, o_value [T, H, Dv] bf16 (fp32 accumulation,
+ *   the rotation in fp32, each rounded to bf16 once).
+ * Requires Dn % 32 == 0, Dv % 32 == 0, 32 <= Dn + Dv <= 256, Dr in
+ * {16, 32, 64}, K % 8 == 0 and 16-byte aligned c_kv, W, k_pe, o_key,
+ * o_value; outputs may overlap nothing. Status words as in the forward.
+ */
+MLAQ_API int mla_kv_uproj_fwd(const mla_kv_shape *shape, const void *c_kv, const void *W,
+                              const void *k_pe, const float *cos_tab, const float *sin_tab,
+                              const int32_t *pos, void *o_key, void *o_value, int *dev_status,
+                              void *stream);
+
 /* Size of the device scratch array mla_q_uproj_bwd_dgrad_noalloc uses. */
 #define MLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -202,6 +202,26 @@ def test_fwd_accepts_bhsd_scale_mode(L):
     assert fwd(L, shape(), om=3, qs=p(9)) == S["MLA_ERR_INVALID_ARG"]
 
 
+def _kv(L, T=256, K=64, H=4, Dn=32, Dv=32, Dr=16, cs_rows=256, cs_width=16, c=p(0), W=p(1), kp=p(2),
+        cos=p(3), sin=p(4), pos=None, ok=p(5), ov=p(8)):
+    s = mlaq.KvShape(T=T, K=K, H=H, Dn=Dn, Dv=Dv, Dr=Dr, cs_rows=cs_rows, cs_width=cs_width)
+    return L.mla_kv_uproj_fwd(ctypes.byref(s), c, W, kp, cos, sin, pos, ok, ov, None, None)
+
+
+def test_kv_rejects(L):
+    assert _kv(L) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert _kv(L, cs_width=8) == S["MLA_ERR_ROPE_WIDTH"]
+    assert _kv(L, T=300) == S["MLA_ERR_POS_RANGE"]
+    assert _kv(L, Dv=40) == S["MLA_ERR_UNSUPPORTED"]
+    assert _kv(L, Dn=160, Dv=128) == S["MLA_ERR_UNSUPPORTED"]      # more than 256 channels per head
+    assert _kv(L, Dr=24, cs_width=24) == S["MLA_ERR_UNSUPPORTED"]
+    assert _kv(L, K=36) == S["MLA_ERR_ALIGNMENT"]
+    assert _kv(L, ok=p(0)) == S["MLA_ERR_ALIAS"]                   # key over c_kv
+    assert _kv(L, ov=p(5)) == S["MLA_ERR_ALIAS"]                   # value over key
+    assert _kv(L, c=None) == S["MLA_ERR_INVALID_ARG"]
+    assert _kv(L, T=0, c=None) == S["MLA_OK"]
+
+
 def test_autograd_face_has_no_cpu_path():
     from up_proj_gemm_gb300.autograd import q_up_proj
     x = torch.zeros((4, 8), dtype=torch.bfloat16, requires_grad=True)

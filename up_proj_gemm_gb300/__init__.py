@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "MlaError", "lib", "library_path", "fwd", "bwd_dgrad", "bwd_wgrad", "mxfp8_quantize_rows",
-    "mxfp8_quantize_cols", "mxfp8_swizzle_scales",
+    "mxfp8_quantize_cols", "mxfp8_swizzle_scales", "kv_fwd",
     "workspace_size", "status_string", "check_status", "Shape", "STATUS",
 ]
 
@@ -53,6 +53,12 @@ _lock = threading.Lock()
 _lib = None
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
+class KvShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("K", ctypes.c_int64), ("H", ctypes.c_int32), ("Dn", ctypes.c_int32),
+                ("Dv", ctypes.c_int32), ("Dr", ctypes.c_int32), ("cs_rows", ctypes.c_int64),
+                ("cs_width", ctypes.c_int64)]
+
+
 _int = ctypes.c_int
 _SIGS = {
     "mla_q_uproj_fwd": (_int, [ctypes.POINTER(Shape), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -66,6 +72,7 @@ _SIGS = {
     "mxfp8_quantize_rows": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
     "mxfp8_quantize_cols": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
     "mxfp8_swizzle_scales": (_int, [_i64, _i64, _vp, _i64, _vp, _vp]),
+    "mla_kv_uproj_fwd": (_int, [ctypes.POINTER(KvShape)] + [_vp] * 10),
     "mxfp8_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
     "mla_status_string": (ctypes.c_char_p, [_int]),
@@ -317,3 +324,29 @@ def mxfp8_swizzle_scales(scales, out=None, stream=None):
     _call(lib().mxfp8_swizzle_scales, "mxfp8_swizzle_scales", rows, cols, _ptr(scales), ld, _ptr(out),
           _stream(scales.device, stream))
     return out
+
+
+def kv_fwd(c_kv, W, k_pe, cos, sin, H, Dn, Dv, Dr, pos=None, o_key=None, o_value=None, status=None, stream=None):
+    """KV side: kv = c_kv W^T split per head -> (o_key [T, H, Dn + Dr] bf16 with
+    the rotated shared k_pe after each head's Dn channels, o_value [T, H, Dv] bf16)."""
+    dev = c_kv.device
+    _need(c_kv, "c_kv", torch.bfloat16, ndim=2)
+    _need(W, "W", torch.bfloat16, dev, ndim=2)
+    _need(k_pe, "k_pe", torch.bfloat16, dev)
+    _need(cos, "cos", torch.float32, dev, ndim=2)
+    _need(sin, "sin", torch.float32, dev, ndim=2)
+    T, K = c_kv.shape
+    if tuple(W.shape) != (H * (Dn + Dv), K):
+        raise ValueError(f"W must be [{H * (Dn + Dv)}, {K}]")
+    if k_pe.numel() != T * Dr:
+        raise ValueError("k_pe must hold T * Dr elements")
+    if pos is not None:
+        _need(pos, "pos", torch.int32, dev, ndim=1)
+    if o_key is None:
+        o_key = torch.empty((T, H, Dn + Dr), dtype=torch.bfloat16, device=dev)
+    if o_value is None:
+        o_value = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+    s = KvShape(T=T, K=K, H=H, Dn=Dn, Dv=Dv, Dr=Dr, cs_rows=cos.shape[0], cs_width=cos.shape[1])
+    _call(lib().mla_kv_uproj_fwd, "mla_kv_uproj_fwd", ctypes.byref(s), _ptr(c_kv), _ptr(W), _ptr(k_pe),
+          _ptr(cos), _ptr(sin), _ptr(pos), _ptr(o_key), _ptr(o_value), _ptr(status), _stream(dev, stream))
+    return o_key, o_value

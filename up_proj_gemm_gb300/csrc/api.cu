@@ -376,6 +376,54 @@ MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape* shape, const void* dq, con
     return launch_wgrad(a, static_cast<cudaStream_t>(stream));
 }
 
+MLAQ_API int mla_kv_uproj_fwd(const mla_kv_shape* shape, const void* c_kv, const void* W, const void* k_pe,
+                              const float* cos_tab, const float* sin_tab, const int32_t* pos, void* o_key,
+                              void* o_value, int* dev_status, void* stream) {
+    if (!shape) return MLA_ERR_INVALID_ARG;
+    const mla_kv_shape& s = *shape;
+    if (s.T < 0 || s.K <= 0 || s.H <= 0 || s.Dn < 0 || s.Dv <= 0 || s.Dr <= 0 || (s.Dr & 1) ||
+        s.cs_rows < 0 || s.cs_width < 0)
+        return MLA_ERR_INVALID_ARG;
+    const int64_t dkv = (int64_t)s.Dn + s.Dv, dk = (int64_t)s.Dn + s.Dr;
+    if (dkv * s.H > kI32Max || dk * s.H > kI32Max || s.T > kI32Max || s.K > kI32Max) return MLA_ERR_INVALID_ARG;
+    if (s.cs_width < s.Dr) return MLA_ERR_ROPE_WIDTH;
+    if (s.T > 0 && (!cos_tab || !sin_tab || !c_kv || !W || !k_pe || !o_key || !o_value))
+        return MLA_ERR_INVALID_ARG;
+    if (!pos && s.T > s.cs_rows) return MLA_ERR_POS_RANGE;
+    if (s.cs_rows == 0 && s.T > 0) return MLA_ERR_POS_RANGE;
+    if (s.T == 0) return MLA_OK;
+    if (!rope_dim_supported(s.Dr) || s.Dn % 32 || s.Dv % 32 || dkv > 256) return MLA_ERR_UNSUPPORTED;
+    if (s.K % 8) return MLA_ERR_ALIGNMENT;
+    if (!aligned(c_kv, 16) || !aligned(W, 16) || !aligned(k_pe, 16) || !aligned(o_key, 16) ||
+        !aligned(o_value, 16) || !aligned(cos_tab, 4) || !aligned(sin_tab, 4) || !aligned(pos, 4) ||
+        !aligned(dev_status, 4))
+        return MLA_ERR_ALIGNMENT;
+    const int64_t table = s.cs_rows * s.cs_width * 4;
+    const Range outs[] = {rng(o_key, s.T * s.H * dk * 2), rng(o_value, s.T * s.H * s.Dv * 2), rng(dev_status, 4)};
+    const Range ins[] = {rng(c_kv, s.T * s.K * 2), rng(W, dkv * s.H * s.K * 2), rng(k_pe, s.T * s.Dr * 2),
+                         rng(cos_tab, table), rng(sin_tab, table), rng(pos, s.T * 4)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    KvArgs a{};
+    a.T = s.T;
+    a.K = s.K;
+    a.H = s.H;
+    a.Dn = s.Dn;
+    a.Dv = s.Dv;
+    a.Dr = s.Dr;
+    a.cs_rows = s.cs_rows;
+    a.cs_width = s.cs_width;
+    a.c_kv = c_kv;
+    a.W = W;
+    a.k_pe = k_pe;
+    a.cos_tab = cos_tab;
+    a.sin_tab = sin_tab;
+    a.pos = pos;
+    a.o_key = o_key;
+    a.o_value = o_value;
+    a.status = dev_status;
+    return launch_kv_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
 MLAQ_API int mxfp8_quantize_rows(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                                  uint8_t* codes, uint8_t* scales, void* stream) {
     if (R < 0 || C < 0 || ld_in < C) return MLA_ERR_INVALID_ARG;

@@ -27,6 +27,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "internal.h"
 #include "mx.cuh"
 #include "ptx.cuh"
@@ -69,6 +71,11 @@ struct FwdParams {
     const uint8_t* x_scales;
     const uint8_t* w_scales;
     int* status;
+    // KV side: a tile is one head's [k_nope (Dn) | v (Dv)] columns
+    int Dv;
+    uint16_t* o_key;        // [T, H, Dn + Dr] bf16
+    uint16_t* o_value;      // [T, H, Dv] bf16
+    const uint16_t* k_pe;   // [T, Dr] bf16, shared by the heads
 };
 
 struct Smem {
@@ -243,7 +250,7 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
 }
 
 // ------------------------------------------------------------------- kernel
-template <bool MXW, bool MXOUT, int DR>
+template <bool MXW, bool MXOUT, int DR, bool KV = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const FwdParams p) {
@@ -401,6 +408,84 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (KV) {
+        // ------------------------------------------------- KV-side epilogue
+        // tile = 128 tokens x one head's Dn + Dv columns. The quadrant's two
+        // warps take alternate 32-column units (k_nope -> o_key, v -> o_value,
+        // 16-byte stores) and half of the shared key's rope pairs each:
+        // o_key[t, h, Dn + .] = RoPE(k_pe[t]).
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int half = (warp - 2) >> 2;
+        constexpr int HH = DR / 2;
+        constexpr int NP = HH / 2 >= 8 ? HH / 2 : HH;  // rope pairs per warp (both warps when HH >= 16)
+        const int Dk = p.Dn + DR;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+            const int b = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int mt = tile % p.num_m_tiles;
+            const int h = tile / p.num_m_tiles;
+            const int64_t t = (int64_t)mt * kBM + row;
+            const bool valid = t < p.T;
+            const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
+            for (int col = 32 * half; col < p.BN; col += 64) {  // 32-column units, alternating
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld32(trow + col, r);
+                tmem_ld_wait();
+                if (!valid) continue;
+                uint16_t* dst = col < p.Dn ? p.o_key + (t * p.H + h) * Dk + col
+                                           : p.o_value + (t * p.H + h) * p.Dv + (col - p.Dn);
+#pragma unroll
+                for (int i = 0; i < 32; i += 8)
+                    st_global_v4(dst + i, pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                 pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                 pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
+                                 pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.tempty(b));
+            // the shared key's rope part, this warp's pairs [i0, i0 + NP)
+            const int i0 = (NP == HH) ? 0 : half * NP;
+            if (valid && (NP != HH || half == 0)) {
+                int prow = -1;
+                const int64_t pp = p.pos ? (int64_t)__ldg(p.pos + t) : t;
+                if (pp < 0 || pp >= p.cs_rows) record_status(p.status, MLA_ERR_POS_RANGE);
+                else prow = (int)pp;
+                if (prow >= 0) {
+                    const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
+                    const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
+                    const uint16_t* kp = p.k_pe + t * DR;
+                    uint16_t* dst = p.o_key + (t * p.H + h) * Dk + p.Dn;
+#pragma unroll
+                    for (int q = 0; q < NP; q += 8) {
+                        const uint4 ka = __ldg(reinterpret_cast<const uint4*>(kp + i0 + q));
+                        const uint4 kc = __ldg(reinterpret_cast<const uint4*>(kp + i0 + q + HH));
+                        float ci[8], si[8], cj[8], sj[8];
+                        load_table8(cs + i0 + q, p.cs_vec != 0, ci);
+                        load_table8(sn + i0 + q, p.cs_vec != 0, si);
+                        load_table8(cs + i0 + q + HH, p.cs_vec != 0, cj);
+                        load_table8(sn + i0 + q + HH, p.cs_vec != 0, sj);
+                        const uint32_t aw[4] = {ka.x, ka.y, ka.z, ka.w}, cw[4] = {kc.x, kc.y, kc.z, kc.w};
+                        uint32_t o1[4], o2[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const float a0 = bf16lo_to_f32(aw[w]), a1 = bf16hi_to_f32(aw[w]);
+                            const float c0 = bf16lo_to_f32(cw[w]), c1 = bf16hi_to_f32(cw[w]);
+                            const int e0 = 2 * w, e1 = 2 * w + 1;
+                            o1[w] = pack_bf16x2(a0 * ci[e0] - c0 * si[e0], a1 * ci[e1] - c1 * si[e1]);
+                            o2[w] = pack_bf16x2(c0 * cj[e0] + a0 * sj[e0], c1 * cj[e1] + a1 * sj[e1]);
+                        }
+                        st_global_v4(dst + i0 + q, o1[0], o1[1], o1[2], o1[3]);
+                        st_global_v4(dst + i0 + q + HH, o2[0], o2[1], o2[2], o2[3]);
+                    }
+                }
+            }
+        }
     } else {
         // ---------------------------------------------------------- epilogue
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
@@ -489,6 +574,70 @@ int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 }
 
 }  // namespace
+
+int launch_kv_fwd(const KvArgs& a, cudaStream_t stream) {
+    DeviceInfo di;
+    int st = current_device_info(&di);
+    if (st != MLA_OK) return st;
+    const int BN = a.Dn + a.Dv;
+    const int64_t N = (int64_t)a.H * BN;
+    FwdParams p{};
+    p.T = (int)a.T;
+    p.H = a.H;
+    p.N = (int)N;
+    p.D = BN;
+    p.Dn = a.Dn;
+    p.Dv = a.Dv;
+    p.BN = BN;
+    p.num_m_tiles = (int)((a.T + kBM - 1) / kBM);
+    p.num_tiles = p.num_m_tiles * a.H;
+    p.k_tiles = (int)((a.K + 63) / 64);
+    p.a_bytes = kBM * 128;
+    p.stage_bytes = p.a_bytes + (uint32_t)BN * 128;
+    p.tx_bytes = p.stage_bytes;
+    p.idesc = idesc_bf16(kBM, (uint32_t)BN, 0, 0);
+    p.cos_tab = a.cos_tab;
+    p.sin_tab = a.sin_tab;
+    p.pos = a.pos;
+    p.cs_rows = a.cs_rows;
+    p.cs_width = a.cs_width;
+    p.cs_vec = (a.cs_width % 4 == 0) && (reinterpret_cast<uintptr_t>(a.cos_tab) % 16 == 0) &&
+               (reinterpret_cast<uintptr_t>(a.sin_tab) % 16 == 0);
+    p.o_key = static_cast<uint16_t*>(a.o_key);
+    p.o_value = static_cast<uint16_t*>(a.o_value);
+    p.k_pe = static_cast<const uint16_t*>(a.k_pe);
+    p.status = a.status;
+    p.slot_bytes = 0;
+    p.nslots = 0;
+    const size_t fixed = 1024 + 256;
+    int stages = (int)((size_t)(di.max_smem_optin - fixed) / p.stage_bytes);
+    if (stages > 8) stages = 8;
+    if (stages < 2) return MLA_ERR_UNSUPPORTED;
+    p.stages = stages;
+    const size_t smem = fixed + (size_t)stages * p.stage_bytes;
+    alignas(64) CUtensorMap ta, tb, tc;
+    memset(&tc, 0, sizeof(tc));
+    st = make_tmap_2d(&ta, a.c_kv, 1, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, kBM, true);
+    if (st != MLA_OK) return st;
+    st = make_tmap_2d(&tb, a.W, 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * 2, 64, (uint32_t)BN, true);
+    if (st != MLA_OK) return st;
+    const int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
+    const void* k = nullptr;
+    switch (a.Dr) {
+        case 16: k = (const void*)fwd_kernel<false, false, 16, true>; break;
+        case 32: k = (const void*)fwd_kernel<false, false, 32, true>; break;
+        case 64: k = (const void*)fwd_kernel<false, false, 64, true>; break;
+        default: return MLA_ERR_UNSUPPORTED;
+    }
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    switch (a.Dr) {
+        case 16: fwd_kernel<false, false, 16, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, p); break;
+        case 32: fwd_kernel<false, false, 32, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, p); break;
+        default: fwd_kernel<false, false, 64, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, p); break;
+    }
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
 
 int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn, int step) {
     for (int bn = max_bn / step * step; bn >= step; bn -= step) {

@@ -66,6 +66,22 @@ struct FwdArgs {
 };
 int launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
+struct KvArgs {
+    int64_t T, K;
+    int H, Dn, Dv, Dr;
+    int64_t cs_rows, cs_width;
+    const void* c_kv;
+    const void* W;
+    const void* k_pe;
+    const float* cos_tab;
+    const float* sin_tab;
+    const int32_t* pos;
+    void* o_key;
+    void* o_value;
+    int* status;
+};
+int launch_kv_fwd(const KvArgs& a, cudaStream_t stream);
+
 struct BwdArgs {
     int64_t T, K;
     int H, Dn, Dr;
