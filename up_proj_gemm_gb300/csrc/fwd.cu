@@ -73,6 +73,7 @@ struct FwdParams {
     int* status;
     // KV side: a tile is one head's [k_nope (Dn) | v (Dv)] columns
     int Dv;
+    int tiles_per_cta;
     uint16_t* o_key;        // [T, H, Dn + Dr] bf16
     uint16_t* o_value;      // [T, H, Dv] bf16
     const uint16_t* k_pe;   // [T, Dr] bf16, shared by the heads
@@ -249,11 +250,28 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
     emit_unit<MXOUT, DR>(p, tmC, c, y, valid, t, n, h, p.Dn);
 }
 
+// Tile order: the query side strides tiles over the CTAs (token tile fastest,
+// so CTAs running together share weight tiles in L2); the KV side gives each
+// CTA a contiguous run, head fastest, so its tiles share their tokens.
+template <bool KV>
+__device__ __forceinline__ int tile_first(const FwdParams& p) {
+    return KV ? (int)blockIdx.x * p.tiles_per_cta : (int)blockIdx.x;
+}
+template <bool KV>
+__device__ __forceinline__ int tile_end(const FwdParams& p) {
+    return KV ? min(p.num_tiles, ((int)blockIdx.x + 1) * p.tiles_per_cta) : p.num_tiles;
+}
+template <bool KV>
+__device__ __forceinline__ int tile_next(int tile) {
+    return KV ? tile + 1 : tile + (int)gridDim.x;
+}
+
 // ------------------------------------------------------------------- kernel
 template <bool MXW, bool MXOUT, int DR, bool KV = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+               const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     Smem sm;
@@ -302,9 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         uint32_t issued_mask = 0, issued_par = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            const int mt = tile % p.num_m_tiles;
-            const int nt = tile / p.num_m_tiles;
+        for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile)) {
+            const int mt = KV ? tile / p.H : tile % p.num_m_tiles;
+            const int nt = KV ? tile % p.H : tile / p.num_m_tiles;
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                     ok = false;
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             int local = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile), ++local) {
                 const int b = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
                 if (!mbar_wait(sm.tempty(b), (use & 1u) ^ 1u, abort_flag)) {
@@ -410,82 +428,127 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (KV) {
         // ------------------------------------------------- KV-side epilogue
-        // tile = 128 tokens x one head's Dn + Dv columns. The quadrant's two
-        // warps take alternate 32-column units (k_nope -> o_key, v -> o_value,
-        // 16-byte stores) and half of the shared key's rope pairs each:
-        // o_key[t, h, Dn + .] = RoPE(k_pe[t]).
+        // CTAs take contiguous runs of tiles, head fastest, so consecutive
+        // tiles share their 128 tokens. A tile = 128 tokens x one head's
+        // Dn + Dv columns; the quadrant's two warps take alternate 32-column
+        // units (k_nope -> o_key, v -> o_value), staged in a 2-slot ring and
+        // written by TMA. The shared key's rope part is computed once per token
+        // block, each warp one half of its channels (half 0: a cos_i - c sin_i,
+        // half 1: c cos_{i+h} + a sin_{i+h}), kept in a shared-memory slab and
+        // TMA-stored into every head's key.
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
-        const int half = (warp - 2) >> 2;
+        const int ew = warp - 2;
+        const int half = ew >> 2;
         constexpr int HH = DR / 2;
-        constexpr int NP = HH / 2 >= 8 ? HH / 2 : HH;  // rope pairs per warp (both warps when HH >= 16)
         const int Dk = p.Dn + DR;
+        const uint32_t ring = sm.out + (uint32_t)(ew * 3) * 2048u;  // slots 0, 1; rope slab 2
+        const uint32_t slab = ring + 2u * 2048u;
+        int slot = 0, cur_mt = -1;
         int local = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+        for (int tile = tile_first<KV>(p); tile < tile_end<KV>(p); tile = tile_next<KV>(tile), ++local) {
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
-            if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
-            tc_fence_after();
-            const int mt = tile % p.num_m_tiles;
-            const int h = tile / p.num_m_tiles;
+            const int mt = tile / p.H;
+            const int h = tile % p.H;
             const int64_t t = (int64_t)mt * kBM + row;
             const bool valid = t < p.T;
+            const int t0 = mt * kBM + quad * 32;
+            if (mt != cur_mt && (DR == 64 || half == 0)) {
+                // this warp's rope channels for the new token block: [32 half, +32)
+                // when DR = 64, else all of them in warp 0 (DR <= 32)
+                if (lane == 0) bulk_wait_group_read<0>();  // stores still reading the slab
+                __syncwarp();
+                constexpr int NO = DR == 64 ? 32 : DR;  // output channels this warp writes
+                float out[NO];
+#pragma unroll
+                for (int i = 0; i < NO; ++i) out[i] = 0.f;
+                int prow = -1;
+                if (valid) {
+                    const int64_t pp = p.pos ? (int64_t)__ldg(p.pos + t) : t;
+                    if (pp < 0 || pp >= p.cs_rows) record_status(p.status, MLA_ERR_POS_RANGE);
+                    else prow = (int)pp;
+                }
+                if (prow >= 0) {
+                    const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
+                    const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
+                    const uint16_t* kp = p.k_pe + t * DR;
+                    const int o0 = DR == 64 ? 32 * half : 0;  // first output channel
+#pragma unroll
+                    for (int q = 0; q < NO; q += 8) {
+                        const int oc = o0 + q;                 // output channel
+                        const int i = oc < HH ? oc : oc - HH;  // its pair
+                        const uint4 ka = __ldg(reinterpret_cast<const uint4*>(kp + i));
+                        const uint4 kc = __ldg(reinterpret_cast<const uint4*>(kp + i + HH));
+                        float cw[8], sw[8];
+                        load_table8(cs + oc, p.cs_vec != 0, cw);
+                        load_table8(sn + oc, p.cs_vec != 0, sw);
+                        const uint32_t aw[4] = {ka.x, ka.y, ka.z, ka.w}, ccw[4] = {kc.x, kc.y, kc.z, kc.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float a = e ? bf16hi_to_f32(aw[w]) : bf16lo_to_f32(aw[w]);
+                                const float c = e ? bf16hi_to_f32(ccw[w]) : bf16lo_to_f32(ccw[w]);
+                                const int k = 2 * w + e;
+                                out[q + k] = oc < HH ? a * cw[k] - c * sw[k] : c * cw[k] + a * sw[k];
+                            }
+                        }
+                    }
+                }
+                const uint32_t ra = slab + (uint32_t)lane * (uint32_t)(NO * 2);
+#pragma unroll
+                for (int q = 0; q < NO; q += 8)
+                    sts_v4(ra + (uint32_t)(2 * q), pack_bf16x2(out[q], out[q + 1]), pack_bf16x2(out[q + 2], out[q + 3]),
+                           pack_bf16x2(out[q + 4], out[q + 5]), pack_bf16x2(out[q + 6], out[q + 7]));
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            cur_mt = mt;
+            if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
+            tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
             for (int col = 32 * half; col < p.BN; col += 64) {  // 32-column units, alternating
                 uint32_t r[32];
                 __syncwarp();
                 tmem_ld32(trow + col, r);
                 tmem_ld_wait();
-                if (!valid) continue;
-                uint16_t* dst = col < p.Dn ? p.o_key + (t * p.H + h) * Dk + col
-                                           : p.o_value + (t * p.H + h) * p.Dv + (col - p.Dn);
+                if (lane == 0) bulk_wait_group_read<1>();  // the slot's previous store has read it
+                __syncwarp();
+                const uint32_t sa = ring + (uint32_t)slot * 2048u + (uint32_t)lane * 64u;
 #pragma unroll
                 for (int i = 0; i < 32; i += 8)
-                    st_global_v4(dst + i, pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
-                                 pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
-                                 pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
-                                 pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+                    sts_v4(sa + (uint32_t)(2 * i), pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                           pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                           pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
+                           pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (col < p.Dn) tma_store_2d(&tmC, h * Dk + col, t0, ring + (uint32_t)slot * 2048u);
+                    else tma_store_2d(&tmD, h * p.Dv + (col - p.Dn), t0, ring + (uint32_t)slot * 2048u);
+                    bulk_commit_group();
+                }
+                slot ^= 1;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.tempty(b));
-            // the shared key's rope part, this warp's pairs [i0, i0 + NP)
-            const int i0 = (NP == HH) ? 0 : half * NP;
-            if (valid && (NP != HH || half == 0)) {
-                int prow = -1;
-                const int64_t pp = p.pos ? (int64_t)__ldg(p.pos + t) : t;
-                if (pp < 0 || pp >= p.cs_rows) record_status(p.status, MLA_ERR_POS_RANGE);
-                else prow = (int)pp;
-                if (prow >= 0) {
-                    const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
-                    const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
-                    const uint16_t* kp = p.k_pe + t * DR;
-                    uint16_t* dst = p.o_key + (t * p.H + h) * Dk + p.Dn;
-#pragma unroll
-                    for (int q = 0; q < NP; q += 8) {
-                        const uint4 ka = __ldg(reinterpret_cast<const uint4*>(kp + i0 + q));
-                        const uint4 kc = __ldg(reinterpret_cast<const uint4*>(kp + i0 + q + HH));
-                        float ci[8], si[8], cj[8], sj[8];
-                        load_table8(cs + i0 + q, p.cs_vec != 0, ci);
-                        load_table8(sn + i0 + q, p.cs_vec != 0, si);
-                        load_table8(cs + i0 + q + HH, p.cs_vec != 0, cj);
-                        load_table8(sn + i0 + q + HH, p.cs_vec != 0, sj);
-                        const uint32_t aw[4] = {ka.x, ka.y, ka.z, ka.w}, cw[4] = {kc.x, kc.y, kc.z, kc.w};
-                        uint32_t o1[4], o2[4];
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const float a0 = bf16lo_to_f32(aw[w]), a1 = bf16hi_to_f32(aw[w]);
-                            const float c0 = bf16lo_to_f32(cw[w]), c1 = bf16hi_to_f32(cw[w]);
-                            const int e0 = 2 * w, e1 = 2 * w + 1;
-                            o1[w] = pack_bf16x2(a0 * ci[e0] - c0 * si[e0], a1 * ci[e1] - c1 * si[e1]);
-                            o2[w] = pack_bf16x2(c0 * cj[e0] + a0 * sj[e0], c1 * cj[e1] + a1 * sj[e1]);
-                        }
-                        st_global_v4(dst + i0 + q, o1[0], o1[1], o1[2], o1[3]);
-                        st_global_v4(dst + i0 + q + HH, o2[0], o2[1], o2[2], o2[3]);
-                    }
-                }
+            // the key's rope part of this head (32-channel slabs by TMA; 16 by plain stores)
+            if (DR >= 32 && lane == 0 && (DR == 64 || half == 0)) {
+                tma_store_2d(&tmC, h * Dk + p.Dn + (DR == 64 ? 32 * half : 0), t0, slab);
+                bulk_commit_group();
+            }
+            if (DR == 16 && half == 0 && valid) {
+                const uint4 v0 = lds_v4(slab + (uint32_t)lane * 32u);
+                const uint4 v1 = lds_v4(slab + (uint32_t)lane * 32u + 16u);
+                uint16_t* dst = p.o_key + (t * p.H + h) * Dk + p.Dn;
+                st_global_v4(dst, v0.x, v0.y, v0.z, v0.w);
+                st_global_v4(dst + 8, v1.x, v1.y, v1.z, v1.w);
             }
         }
+        if (lane == 0) bulk_wait_group_all();  // every output store has landed
+        __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
         const int quad = warp & 3;  // TMEM lane quadrant this warp may access
@@ -558,7 +621,7 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return MLA_ERR_CUDA;
-    kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, p);
+    kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, tc, p);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -607,21 +670,27 @@ int launch_kv_fwd(const KvArgs& a, cudaStream_t stream) {
     p.o_value = static_cast<uint16_t*>(a.o_value);
     p.k_pe = static_cast<const uint16_t*>(a.k_pe);
     p.status = a.status;
-    p.slot_bytes = 0;
-    p.nslots = 0;
-    const size_t fixed = 1024 + 256;
+    p.slot_bytes = 2048;  // epilogue warp: 2 ring slots + the rope slab, 32 rows x 32 bf16 each
+    p.nslots = 3;
+    const size_t fixed = 1024 + 256 + (size_t)kEpiWarps * 3 * 2048;
     int stages = (int)((size_t)(di.max_smem_optin - fixed) / p.stage_bytes);
     if (stages > 8) stages = 8;
     if (stages < 2) return MLA_ERR_UNSUPPORTED;
     p.stages = stages;
     const size_t smem = fixed + (size_t)stages * p.stage_bytes;
-    alignas(64) CUtensorMap ta, tb, tc;
-    memset(&tc, 0, sizeof(tc));
+    alignas(64) CUtensorMap ta, tb, tc, td;
     st = make_tmap_2d(&ta, a.c_kv, 1, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, kBM, true);
     if (st != MLA_OK) return st;
     st = make_tmap_2d(&tb, a.W, 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * 2, 64, (uint32_t)BN, true);
     if (st != MLA_OK) return st;
+    // outputs as 2-D [T, H*Dk] and [T, H*Dv]: store boxes of 32 channels x 32 tokens
+    const int64_t Dk = a.Dn + a.Dr;
+    st = make_tmap_2d(&tc, a.o_key, 1, (uint64_t)(a.H * Dk), (uint64_t)a.T, (uint64_t)(a.H * Dk) * 2, 32, 32, false);
+    if (st != MLA_OK) return st;
+    st = make_tmap_2d(&td, a.o_value, 1, (uint64_t)a.H * a.Dv, (uint64_t)a.T, (uint64_t)a.H * a.Dv * 2, 32, 32, false);
+    if (st != MLA_OK) return st;
     const int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
+    p.tiles_per_cta = (p.num_tiles + grid - 1) / grid;
     const void* k = nullptr;
     switch (a.Dr) {
         case 16: k = (const void*)fwd_kernel<false, false, 16, true>; break;
@@ -632,9 +701,9 @@ int launch_kv_fwd(const KvArgs& a, cudaStream_t stream) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MLA_ERR_CUDA;
     switch (a.Dr) {
-        case 16: fwd_kernel<false, false, 16, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, p); break;
-        case 32: fwd_kernel<false, false, 32, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, p); break;
-        default: fwd_kernel<false, false, 64, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, p); break;
+        case 16: fwd_kernel<false, false, 16, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, td, p); break;
+        case 32: fwd_kernel<false, false, 32, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, td, p); break;
+        default: fwd_kernel<false, false, 64, true><<<grid, kThreads, smem, stream>>>(ta, tb, tc, td, p); break;
     }
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
