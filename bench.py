@@ -554,6 +554,26 @@ def run_parts(dev, stream, flush, pk, pk_src):
                           "frac_bf16_peak": round(w.bwd_flop() / ((ms_d + ms_w) * 1e-3) / 1e12 / bf16_peak, 4)}
     del inp, dx, dW, db, rope
 
+    # KV side: c_kv [4096, 512] x W_UKV [128 x (128 + 128), 512]^T, shared k_pe rotated into every key
+    T, K, H, Dn, Dv, Dr = 4096, 512, 128, 128, 128, 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(14)
+    c_kv = torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16)
+    W = (torch.randn((H * (Dn + Dv), K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    k_pe = torch.randn((T, Dr), generator=g, device=dev).to(torch.bfloat16)
+    cos, sin = [t.to(dev) for t in synth.rope_table_standard(T, Dr)]
+    o_key = torch.empty((T, H, Dn + Dr), dtype=torch.bfloat16, device=dev)
+    o_value = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+    ms = time_loop(lambda: mlaq.kv_fwd(c_kv, W, k_pe, cos, sin, H, Dn, Dv, Dr, o_key=o_key, o_value=o_value,
+                                       status=st), 30, flush, stream)
+    flop = 2 * T * K * H * (Dn + Dv)
+    byts = (T * K + H * (Dn + Dv) * K + T * Dr + T * H * (Dn + Dr) + T * H * Dv) * 2
+    parts["kv_uproj_rope_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(flop / (ms * 1e-3) / 1e12, 1),
+                                    "GB/s": round(byts / (ms * 1e-3) / 1e9, 1),
+                                    "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                                    "algorithmic_bytes": byts, "algorithmic_flop": flop}
+    del c_kv, W, k_pe, o_key, o_value
+
     # long context: T = 4 x 4096, YaRN table, MXFP8 out, fwd + bwd
     w = synth.workload("dsv3_long_yarn")
     inp = make_device_inputs(w, dev, seed=13)
