@@ -446,6 +446,17 @@ def run_only(args, w, inp, kernels, flush, stream, status, dev):
             mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], weight_mode="mxfp8",
                      out_mode="mxfp8", x_scales=xs, w_scales=Ws, q_out=qc, q_scales=qs, status=status)
         flop = w.fwd_flop()
+    elif args.only == "bwd_mxfp8":
+        dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=dev)
+        dW = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev)
+        db = torch.empty((w.N,), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty((mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, inp["cos"].shape[0],
+                                              inp["cos"].shape[1], 3),), dtype=torch.uint8, device=dev)
+
+        def fn():
+            mlaq.bwd_mxfp8(inp["dq"], inp["W"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
+                           pos=inp["pos"], dx=dx, dW=dW, db=db, status=status, workspace=ws)
+        flop = w.bwd_flop()
     elif args.only == "quant_cols":
         a = torch.randn((w.T, w.N), device=dev).to(torch.bfloat16)
         codes = torch.empty((w.N, w.T), dtype=torch.uint8, device=dev)
@@ -552,7 +563,19 @@ def run_parts(dev, stream, flush, pk, pk_src):
                           "dgrad_TFLOP/s": round(half / (ms_d * 1e-3) / 1e12, 1),
                           "wgrad_TFLOP/s": round(half / (ms_w * 1e-3) / 1e12, 1),
                           "frac_bf16_peak": round(w.bwd_flop() / ((ms_d + ms_w) * 1e-3) / 1e12 / bf16_peak, 4)}
-    del inp, dx, dW, db, rope
+    # the same backward with MXFP8 GEMMs: rotate + both quantized copies of dq_pre, the
+    # columnwise copies of W and x, the two block-scaled GEMMs and db, in one call
+    ws = torch.empty((mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, inp["cos"].shape[0],
+                                          inp["cos"].shape[1], 3),), dtype=torch.uint8, device=dev)
+    ms_mx = time_loop(lambda: mlaq.bwd_mxfp8(inp["dq"], inp["W"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn,
+                                             w.Dr, pos=inp["pos"], dx=dx, dW=dW, db=db, status=st,
+                                             workspace=ws), 20, flush, stream)
+    tf = w.bwd_flop() / (ms_mx * 1e-3) / 1e12
+    parts["bwd_mxfp8_T8192"] = {"ms": round(ms_mx, 4), "TFLOP/s": round(tf, 1),
+                                "frac_fp8_peak": round(tf / fp8_peak, 4),
+                                "speedup_vs_bf16_bwd": round((ms_d + ms_w) / ms_mx, 3),
+                                "note": "whole call: quantization passes included"}
+    del inp, dx, dW, db, rope, ws
 
     # KV side: c_kv [4096, 512] x W_UKV [128 x (128 + 128), 512]^T, shared k_pe rotated into every key
     T, K, H, Dn, Dv, Dr = 4096, 512, 128, 128, 128, 64
@@ -679,7 +702,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "wgrad_self", "fwd_mxfp8w", "quant", "quant_cols"),
+    ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "wgrad_self", "fwd_mxfp8w", "quant", "quant_cols",
+                                          "bwd_mxfp8"),
                     help="time one kernel alone (profiling)")
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -195,6 +195,61 @@ MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape *shape, const void *dq, con
                                    const int32_t *pos, void *dW, void *db, void *workspace,
                                    size_t ws_bytes, int *dev_status, void *stream);
 
+/*
+ * Backward with MXFP8 tensor-core GEMMs: dx, dW and db from dq in one call.
+ * TransformerEngine PR "Add support for fused Q Up-Proj GEMM/RoPE/Quant",
+ * Greptile summary: the MXFP8 quantization helpers (rowwise, the transpose
+ * copy) that feed block-scaled GEMMs; the pages give no formula for the
+ * backward, so this follows the plain reading (each GEMM operand quantized
+ * along its reduction dimension):
+ *   dq_pre = J^T dq in float32: the Dn pass-through channels of each head as
+ *            they are; rope channel pairs (i, i + Dr/2) of head h, token t,
+ *            position p = pos[t] (or t), with c_j = cos_tab[p][j] and
+ *            s_j = sin_tab[p][j]:
+ *              out_i        = fl(fl(g_i c_i) + fl(g_{i+Dr/2} s_{i+Dr/2}))
+ *              out_{i+Dr/2} = fl(fl(g_{i+Dr/2} c_{i+Dr/2}) - fl(g_i s_i))
+ *            (each product and sum rounded once to float32, in that order)
+ *   dx [T, K]  = Q_rows(dq_pre) [T, N] . Q_cols(W)^T, reduced over N
+ *   dW [N, K]  = Q_cols(dq_pre) [N, T] . Q_cols(x)^T, reduced over T
+ *   db [N]     = sum over t of dq_pre (float32 sums of 32-token blocks,
+ *                added in token-block order, rounded to bf16)
+ * Q_rows is mxfp8_quantize_rows' rule on rows, Q_cols its rule on columns
+ * (mxfp8_quantize_cols); the GEMMs accumulate exact products of the decoded
+ * operands in fp32 and round once to bf16.
+ *   dq [T, H, D] bf16, W [N, K] bf16, x [T, K] bf16; dx [T, K], dW [N, K],
+ *   db [N] bf16. dx, dW and db are each optional (NULL: not computed; at
+ *   least one is required); W may be NULL without dx, x without dW.
+ *   workspace: at least mla_q_uproj_workspace_size(shape, 3) bytes,
+ *   16-byte aligned, overlapping nothing else. After the call it holds the
+ *   quantized operands at the offsets mla_q_uproj_bwd_mxfp8_layout gives
+ *   (only those of the requested gradients), e.g. for reuse or inspection;
+ *   nothing in it needs initialization.
+ * Requires Dr in {32, 64} with (Dn + Dr) % 32 == 0 (a rowwise block never
+ * spans two heads), N % 128 == 0, K % 32 == 0 (else MLA_ERR_UNSUPPORTED);
+ * 16-byte aligned dq, W, x, dx, dW. T may be any size >= 0: the token axis
+ * of the wgrad operands is padded to a multiple of 128 with zero codes and
+ * zero scale bytes. T == 0 writes dW = 0 and db = 0.
+ */
+typedef struct {
+    int64_t t_pad;       /* T rounded up to a multiple of 128: row pitch of qb and xt */
+    size_t qa;           /* E4M3 [T, N], blocks of 32 channels (dgrad operand A) */
+    size_t qa_scales;    /* E8M0 [T, N/32] */
+    size_t qb;           /* E4M3 [N, t_pad], blocks of 32 tokens (wgrad operand A) */
+    size_t qb_scales;    /* E8M0 [N, t_pad/32] */
+    size_t wt;           /* E4M3 [K, N]: Q_cols(W) (dgrad operand B) */
+    size_t wt_scales;    /* E8M0 [K, N/32] */
+    size_t xt;           /* E4M3 [K, t_pad]: Q_cols(x) (wgrad operand B) */
+    size_t xt_scales;    /* E8M0 [K, t_pad/32] */
+    size_t db_partials;  /* float32 [ceil(T/32), N] */
+    size_t total;        /* == mla_q_uproj_workspace_size(shape, 3) */
+} mla_mxfp8_bwd_layout;
+
+MLAQ_API int mla_q_uproj_bwd_mxfp8_layout(const mla_q_shape *shape, mla_mxfp8_bwd_layout *out);
+MLAQ_API int mla_q_uproj_bwd_mxfp8(const mla_q_shape *shape, const void *dq, const void *W,
+                                   const void *x, const float *cos_tab, const float *sin_tab,
+                                   const int32_t *pos, void *dx, void *dW, void *db, void *workspace,
+                                   size_t ws_bytes, int *dev_status, void *stream);
+
 /* KV side of the attention block: see mla_kv_uproj_fwd. */
 typedef struct {
     int64_t T;        /* tokens */
@@ -302,10 +357,11 @@ MLAQ_API size_t mxfp8_swizzled_scale_bytes(int64_t rows, int64_t cols);
 MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t *in, int64_t ld_in,
                                   uint8_t *out, void *stream);
 
-/* which: 0 = forward, 1 = dgrad, 2 = wgrad. Bytes of device workspace the
- * call needs for this shape on the current device (0 = pass NULL). Only
- * dgrad ever needs any (see mla_q_uproj_bwd_dgrad). Returns 0 for an
- * invalid shape or when no CUDA device is usable. */
+/* which: 0 = forward, 1 = dgrad, 2 = wgrad, 3 = MXFP8 backward. Bytes of
+ * device workspace the call needs for this shape (0 = pass NULL). Of the
+ * bf16 calls only dgrad ever needs any (see mla_q_uproj_bwd_dgrad; that size
+ * depends on the current device). Returns 0 for an invalid shape or, for
+ * which = 1, when no CUDA device is usable. */
 MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape *shape, int which);
 
 /* Static, human-readable name of a status code. */

@@ -222,6 +222,67 @@ def test_kv_rejects(L):
     assert _kv(L, T=0, c=None) == S["MLA_OK"]
 
 
+def _mx_shape(**kw):
+    base = dict(T=64, K=64, H=4, Dn=32, Dr=32, cs_rows=64, cs_width=32)
+    base.update(kw)
+    return shape(**base)
+
+
+def _bmx(L, s, dq=p(0), W=p(1), x=p(2), cos=p(3), sin=p(4), pos=None, dx=p(5), dW=p(6), db=p(7), ws=p(40),
+         ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = L.mla_q_uproj_workspace_size(ctypes.byref(s), 3)
+    return L.mla_q_uproj_bwd_mxfp8(ctypes.byref(s), dq, W, x, cos, sin, pos, dx, dW, db, ws, ws_bytes, None,
+                                   None)
+
+
+def test_bwd_mxfp8_rejects(L):
+    ok = (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert _bmx(L, _mx_shape()) in ok
+    assert _bmx(L, _mx_shape(Dr=16, cs_width=16)) == S["MLA_ERR_UNSUPPORTED"]   # D % 32: blocks span heads
+    assert _bmx(L, _mx_shape(H=1)) == S["MLA_ERR_UNSUPPORTED"]                  # N = 64: not a 128 multiple
+    assert _bmx(L, _mx_shape(K=48)) == S["MLA_ERR_UNSUPPORTED"]                 # K % 32
+    assert _bmx(L, _mx_shape(cs_width=16)) == S["MLA_ERR_ROPE_WIDTH"]
+    assert _bmx(L, _mx_shape(T=65)) == S["MLA_ERR_POS_RANGE"]
+    assert _bmx(L, _mx_shape(), dx=None, dW=None, db=None) == S["MLA_ERR_INVALID_ARG"]
+    assert _bmx(L, _mx_shape(), W=None) == S["MLA_ERR_INVALID_ARG"]              # dx needs W
+    assert _bmx(L, _mx_shape(), x=None) == S["MLA_ERR_INVALID_ARG"]              # dW needs x
+    assert _bmx(L, _mx_shape(), dq=None) == S["MLA_ERR_INVALID_ARG"]
+    assert _bmx(L, _mx_shape(), W=None, dx=None) in ok
+    assert _bmx(L, _mx_shape(), x=None, dW=None) in ok
+    assert _bmx(L, _mx_shape(), ws_bytes=1024) == S["MLA_ERR_WORKSPACE"]
+    assert _bmx(L, _mx_shape(), ws=None) == S["MLA_ERR_WORKSPACE"]
+    assert _bmx(L, _mx_shape(), dx=p(0)) == S["MLA_ERR_ALIAS"]                   # dx over dq
+    assert _bmx(L, _mx_shape(), db=p(6)) == S["MLA_ERR_ALIAS"]                   # db over dW
+    assert _bmx(L, _mx_shape(), ws=p(1)) == S["MLA_ERR_ALIAS"]                   # workspace over W
+    assert _bmx(L, _mx_shape(), ws=p(1), x=p(30), dx=None, W=None) in ok        # W unused without dx
+    assert _bmx(L, _mx_shape(), dW=ctypes.c_void_p(FAKE * 7 + 8)) == S["MLA_ERR_ALIGNMENT"]
+    assert _bmx(L, _mx_shape(), ws=ctypes.c_void_p(FAKE * 41 + 8)) == S["MLA_ERR_ALIGNMENT"]
+    assert _bmx(L, _mx_shape(T=0), dq=None, ws=None, ws_bytes=0) in ok          # writes dW = 0, db = 0
+
+
+def test_bwd_mxfp8_layout(L):
+    """The workspace regions are disjoint, 256-byte aligned, in order, and as
+    large as their operands; the token axis is padded to 128."""
+    for T, K, H, Dn, Dr in ((64, 64, 4, 32, 32), (200, 96, 2, 64, 64), (1, 32, 2, 32, 32),
+                            (4096, 1536, 128, 128, 64)):
+        N = H * (Dn + Dr)
+        lay = mlaq.bwd_mxfp8_layout(T, K, H, Dn, Dr, max(T, 1), Dr)
+        Tp = lay["t_pad"]
+        assert Tp % 128 == 0 and Tp - 128 < T <= Tp
+        sizes = [("qa", T * N), ("qa_scales", T * N // 32), ("qb", N * Tp), ("qb_scales", N * Tp // 32),
+                 ("wt", K * N), ("wt_scales", K * N // 32), ("xt", K * Tp), ("xt_scales", K * Tp // 32),
+                 ("db_partials", 4 * N * ((T + 31) // 32))]
+        end = 0
+        for name, size in sizes:
+            assert lay[name] % 256 == 0 and lay[name] >= end, name
+            end = lay[name] + size
+        assert lay["total"] >= end
+        assert lay["total"] == mlaq.workspace_size(T, K, H, Dn, Dr, max(T, 1), Dr, 3)
+    assert mlaq.workspace_size(0, 64, 4, 32, 32, 1, 32, 3) == 0
+    assert mlaq.workspace_size(64, 64, 4, 32, 32, 64, 32, 4) == 0
+
+
 def test_autograd_face_has_no_cpu_path():
     from up_proj_gemm_gb300.autograd import q_up_proj
     x = torch.zeros((4, 8), dtype=torch.bfloat16, requires_grad=True)

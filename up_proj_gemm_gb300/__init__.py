@@ -21,7 +21,8 @@ import torch
 
 __all__ = [
     "MlaError", "lib", "library_path", "fwd", "bwd_dgrad", "bwd_wgrad", "mxfp8_quantize_rows",
-    "mxfp8_quantize_cols", "mxfp8_swizzle_scales", "kv_fwd",
+    "mxfp8_quantize_cols", "mxfp8_swizzle_scales", "kv_fwd", "bwd_mxfp8", "bwd_mxfp8_layout",
+    "bwd_mxfp8_operands",
     "workspace_size", "status_string", "check_status", "Shape", "STATUS",
 ]
 
@@ -59,6 +60,11 @@ class KvShape(ctypes.Structure):
                 ("cs_width", ctypes.c_int64)]
 
 
+class Mxfp8BwdLayout(ctypes.Structure):
+    _fields_ = [("t_pad", ctypes.c_int64)] + [(n, ctypes.c_size_t) for n in (
+        "qa", "qa_scales", "qb", "qb_scales", "wt", "wt_scales", "xt", "xt_scales", "db_partials", "total")]
+
+
 _int = ctypes.c_int
 _SIGS = {
     "mla_q_uproj_fwd": (_int, [ctypes.POINTER(Shape), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -73,6 +79,8 @@ _SIGS = {
     "mxfp8_quantize_cols": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _vp]),
     "mxfp8_swizzle_scales": (_int, [_i64, _i64, _vp, _i64, _vp, _vp]),
     "mla_kv_uproj_fwd": (_int, [ctypes.POINTER(KvShape)] + [_vp] * 10),
+    "mla_q_uproj_bwd_mxfp8": (_int, [ctypes.POINTER(Shape)] + [_vp] * 10 + [ctypes.c_size_t, _vp, _vp]),
+    "mla_q_uproj_bwd_mxfp8_layout": (_int, [ctypes.POINTER(Shape), ctypes.POINTER(Mxfp8BwdLayout)]),
     "mxfp8_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
     "mla_status_string": (ctypes.c_char_p, [_int]),
@@ -265,6 +273,87 @@ def bwd_wgrad(dq, x, cos, sin, H, Dn, Dr, pos=None, dW=None, db=True, status=Non
           _ptr(dq_pre_rope), _ptr(x), _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dW), _ptr(db), None, 0,
           _ptr(status), _stream(dev, stream))
     return dW, db
+
+
+def bwd_mxfp8_layout(T, K, H, Dn, Dr, cs_rows, cs_width) -> dict:
+    """Byte offsets of the MXFP8 backward's workspace regions (and ``t_pad``,
+    ``total``) as ``mla_q_uproj_bwd_mxfp8_layout`` reports them."""
+    s = Shape(T=T, K=K, H=H, Dn=Dn, Dr=Dr, reserved=0, cs_rows=cs_rows, cs_width=cs_width)
+    out = Mxfp8BwdLayout()
+    _call(lib().mla_q_uproj_bwd_mxfp8_layout, "mla_q_uproj_bwd_mxfp8_layout", ctypes.byref(s),
+          ctypes.byref(out))
+    return {name: int(getattr(out, name)) for name, _ in Mxfp8BwdLayout._fields_}
+
+
+def bwd_mxfp8_operands(workspace, T, K, H, Dn, Dr, cs_rows, cs_width) -> dict:
+    """uint8 views of the quantized operands a bwd_mxfp8 call left in
+    ``workspace``: qa [T, N], qa_s [T, N/32], qb [N, t_pad], qb_s
+    [N, t_pad/32], wt [K, N], wt_s [K, N/32], xt [K, t_pad], xt_s
+    [K, t_pad/32] (t_pad = T rounded up to 128)."""
+    L = bwd_mxfp8_layout(T, K, H, Dn, Dr, cs_rows, cs_width)
+    N = H * (Dn + Dr)
+    Tp = L["t_pad"]
+
+    def view(off, rows, cols):
+        return workspace[off:off + rows * cols].view(rows, cols)
+
+    return dict(qa=view(L["qa"], T, N), qa_s=view(L["qa_scales"], T, N // 32),
+                qb=view(L["qb"], N, Tp), qb_s=view(L["qb_scales"], N, Tp // 32),
+                wt=view(L["wt"], K, N), wt_s=view(L["wt_scales"], K, N // 32),
+                xt=view(L["xt"], K, Tp), xt_s=view(L["xt_scales"], K, Tp // 32), t_pad=Tp)
+
+
+def bwd_mxfp8(dq, W, x, cos, sin, H, Dn, Dr, pos=None, dx=True, dW=True, db=True, status=None, stream=None,
+              workspace=None):
+    """Backward with MXFP8 tensor-core GEMMs (``mla_q_uproj_bwd_mxfp8``):
+    dx [T, K], dW [N, K], db [N] (bf16) from dq [T, H, D] bf16.
+
+    Each of dx / dW / db: True allocates it, False/None skips it, or pass a
+    tensor. W [N, K] is needed for dx, x [T, K] for dW (else may be None).
+    The workspace (``workspace_size(..., which=3)`` bytes, uint8) is
+    allocated unless passed; afterwards it holds the quantized operands
+    (``bwd_mxfp8_operands``). Returns (dx, dW, db), None where skipped."""
+    dev = dq.device
+    _need(dq, "dq", torch.bfloat16)
+    _need(cos, "cos", torch.float32, dev, ndim=2)
+    _need(sin, "sin", torch.float32, dev, ndim=2)
+    T = dq.shape[0]
+    N = H * (Dn + Dr)
+    if dq.numel() != T * N:
+        raise ValueError("dq must hold T * H * (Dn + Dr) elements")
+    want_dx = dx is not None and dx is not False
+    want_dw = dW is not None and dW is not False
+    if want_dx:
+        _need(W, "W", torch.bfloat16, dev, ndim=2)
+    if want_dw:
+        _need(x, "x", torch.bfloat16, dev, ndim=2)
+    ref = W if want_dx else x
+    if ref is None:
+        raise ValueError("need W (for dx) or x (for dW) to know K")
+    K = ref.shape[1]
+    if pos is not None:
+        _need(pos, "pos", torch.int32, dev, ndim=1)
+    if dx is True:
+        dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    elif dx is False:
+        dx = None
+    if dW is True:
+        dW = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    elif dW is False:
+        dW = None
+    if db is True:
+        db = torch.empty((N,), dtype=torch.bfloat16, device=dev)
+    elif db is False:
+        db = None
+    s = _shape(T, K, H, Dn, Dr, cos)
+    need = int(lib().mla_q_uproj_workspace_size(ctypes.byref(s), 3))
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call(lib().mla_q_uproj_bwd_mxfp8, "mla_q_uproj_bwd_mxfp8", ctypes.byref(s), _ptr(dq),
+          _ptr(W) if want_dx else None, _ptr(x) if want_dw else None, _ptr(cos), _ptr(sin), _ptr(pos),
+          _ptr(dx), _ptr(dW), _ptr(db), _ptr(workspace), ws_bytes, _ptr(status), _stream(dev, stream))
+    return dx, dW, db
 
 
 def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None):

@@ -204,7 +204,12 @@ MLAQ_API const char* mla_status_string(int status) {
 MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape* shape, int which) {
     int D;
     int64_t N;
-    if (check_shape(shape, &D, &N) != MLA_OK || which < 0 || which > 2) return 0;
+    if (check_shape(shape, &D, &N) != MLA_OK || which < 0 || which > 3) return 0;
+    if (which == 3) {  // MXFP8 backward: the quantized operands and the db partials
+        Mxfp8BwdLayout L;
+        if (shape->T == 0 || bwd_mxfp8_layout(shape->T, shape->K, N, &L) != MLA_OK) return 0;
+        return L.total;
+    }
     if (which != 1 || shape->T == 0) return 0;  // only dgrad may split its reduction
     DeviceInfo di;
     if (current_device_info(&di) != MLA_OK) return 0;
@@ -374,6 +379,81 @@ MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape* shape, const void* dq, con
     a.status = dev_status;
     // T == 0 still defines dW = 0 and db = 0: the kernel writes zeros.
     return launch_wgrad(a, static_cast<cudaStream_t>(stream));
+}
+
+MLAQ_API int mla_q_uproj_bwd_mxfp8_layout(const mla_q_shape* shape, mla_mxfp8_bwd_layout* out) {
+    int D;
+    int64_t N;
+    int st = check_shape(shape, &D, &N);
+    if (st != MLA_OK) return st;
+    if (!out) return MLA_ERR_INVALID_ARG;
+    Mxfp8BwdLayout L;
+    st = bwd_mxfp8_layout(shape->T, shape->K, N, &L);
+    if (st != MLA_OK) return st;
+    out->t_pad = L.Tp;
+    out->qa = L.qa;
+    out->qa_scales = L.qa_s;
+    out->qb = L.qb;
+    out->qb_scales = L.qb_s;
+    out->wt = L.wt;
+    out->wt_scales = L.wt_s;
+    out->xt = L.xt;
+    out->xt_scales = L.xt_s;
+    out->db_partials = L.dbp;
+    out->total = shape->T == 0 ? 0 : L.total;
+    return MLA_OK;
+}
+
+MLAQ_API int mla_q_uproj_bwd_mxfp8(const mla_q_shape* shape, const void* dq, const void* W, const void* x,
+                                   const float* cos_tab, const float* sin_tab, const int32_t* pos, void* dx,
+                                   void* dW, void* db, void* workspace, size_t ws_bytes, int* dev_status,
+                                   void* stream) {
+    int D;
+    int64_t N;
+    int st = check_shape(shape, &D, &N);
+    if (st != MLA_OK) return st;
+    const mla_q_shape& s = *shape;
+    if (!dx && !dW && !db) return MLA_ERR_INVALID_ARG;
+    if ((dx && !W) || (dW && !x)) return MLA_ERR_INVALID_ARG;
+    if (s.T > 0 && !dq) return MLA_ERR_INVALID_ARG;
+    st = check_table_and_positions(&s, cos_tab, sin_tab, pos);
+    if (st != MLA_OK) return st;
+    const size_t need = mla_q_uproj_workspace_size(shape, 3);
+    if (s.T > 0 && (ws_bytes < need || !workspace)) return MLA_ERR_WORKSPACE;
+    if (!rope_dim_supported(s.Dr) || s.Dn % 32 || D % 32 || N % 128 || s.K % 32) return MLA_ERR_UNSUPPORTED;
+    if (fwd_tile_n(s.K, (int)s.K, (int)s.K, 0, 192, 32) == 0) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(dq, 16) || !aligned(W, 16) || !aligned(x, 16) || !aligned(dx, 16) || !aligned(dW, 16) ||
+        !aligned(db, 4) || !aligned(cos_tab, 4) || !aligned(sin_tab, 4) || !aligned(pos, 4) ||
+        !aligned(dev_status, 4) || !aligned(workspace, 16))
+        return MLA_ERR_ALIGNMENT;
+    const int64_t table = s.cs_rows * s.cs_width * 4;
+    const Range outs[] = {rng(dx, s.T * s.K * 2), rng(dW, N * s.K * 2), rng(db, N * 2), rng(dev_status, 4),
+                          rng(workspace, (int64_t)need)};
+    const Range ins[] = {rng(dq, s.T * N * 2), rng(W, dx ? N * s.K * 2 : 0), rng(x, dW ? s.T * s.K * 2 : 0),
+                         rng(cos_tab, table), rng(sin_tab, table), rng(pos, s.T * 4)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    BwdArgs a{};
+    a.T = s.T;
+    a.K = s.K;
+    a.H = s.H;
+    a.Dn = s.Dn;
+    a.Dr = s.Dr;
+    a.cs_rows = s.cs_rows;
+    a.cs_width = s.cs_width;
+    a.dq = dq;
+    a.W = dx ? W : nullptr;
+    a.x = dW ? x : nullptr;
+    a.cos_tab = cos_tab;
+    a.sin_tab = sin_tab;
+    a.pos = pos;
+    a.dx = dx;
+    a.dW = dW;
+    a.db = db;
+    a.workspace = workspace;
+    a.ws_bytes = ws_bytes;
+    a.status = dev_status;
+    // T == 0: dx is empty; dW = 0 and db = 0 are written
+    return launch_bwd_mxfp8(a, static_cast<cudaStream_t>(stream));
 }
 
 MLAQ_API int mla_kv_uproj_fwd(const mla_kv_shape* shape, const void* c_kv, const void* W, const void* k_pe,

@@ -714,8 +714,8 @@ int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn, int step) {
         bool ok = true;
         const int64_t heads = N / D;
         for (int64_t h = 0; ok && h < heads; ++h) {
-            const int64_t rs = h * D + Dn, re = h * D + D - 1;  // rope region
-            if (rs / bn != re / bn) ok = false;
+            const int64_t rs = h * D + Dn, re = h * D + D - 1;  // rope region (none when Dr == 0)
+            if (Dr > 0 && rs / bn != re / bn) ok = false;
             for (int c = 0; ok && c < Dn; c += 32)  // pass-through blocks
                 if ((h * D + c) / bn != (h * D + c + 31) / bn) ok = false;
         }
@@ -750,12 +750,12 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.stage_bytes = p.a_bytes + (uint32_t)BN * 128;
     p.tx_bytes = p.stage_bytes;
     p.idesc = mxw ? idesc_mxf8(kBM, BN, 0) : idesc_bf16(kBM, BN, 0, 0);
-    p.ksb = (int)(a.K / 32);
+    p.ksb = (int)(a.ld_scale ? a.ld_scale : a.K / 32);
     p.bias = static_cast<const uint16_t*>(a.bias);
     p.cos_tab = a.cos_tab;
     p.sin_tab = a.sin_tab;
     p.pos = a.pos;
-    p.cs_rows = a.cs_rows;
+    p.cs_rows = a.Dr == 0 ? (long long)INT64_MAX : a.cs_rows;  // plain GEMM: no table rows read
     p.cs_width = a.cs_width;
     p.q_out = static_cast<uint8_t*>(a.q_out);
     p.q_scales = a.q_scales;
@@ -783,11 +783,12 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     const size_t smem = fixed + (size_t)stages * per_stage;
 
     alignas(64) CUtensorMap ta, tb;
+    const uint64_t esz = mxw ? 1 : 2;
     st = make_tmap_2d(&ta, a.x, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)a.T,
-                      (uint64_t)a.K * (mxw ? 1 : 2), 128 / (mxw ? 1 : 2), kBM, true);
+                      (uint64_t)(a.ld_x ? a.ld_x : a.K) * esz, 128 / (uint32_t)esz, kBM, true);
     if (st != MLA_OK) return st;
-    st = make_tmap_2d(&tb, a.W, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)a.K * (mxw ? 1 : 2),
-                      128 / (mxw ? 1 : 2), (uint32_t)BN, true);
+    st = make_tmap_2d(&tb, a.W, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)(a.ld_w ? a.ld_w : a.K) * esz,
+                      128 / (uint32_t)esz, (uint32_t)BN, true);
     if (st != MLA_OK) return st;
     // output q [T, N] (bf16 or E4M3 bytes): TMA store boxes of 16 channels x 32 tokens
     alignas(64) CUtensorMap tc;
@@ -796,6 +797,9 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     if (st != MLA_OK) return st;
 
     int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
+    if (a.Dr == 0)  // plain GEMM: every unit is a pass-through unit; any DR instantiation serves
+        return mxw ? launch_variant<true, false, 16>(ta, tb, tc, p, grid, smem, stream)
+                   : launch_variant<false, false, 16>(ta, tb, tc, p, grid, smem, stream);
     if (mxw)
         return mxo ? launch_dr<true, true>(a.Dr, ta, tb, tc, p, grid, smem, stream)
                    : launch_dr<true, false>(a.Dr, ta, tb, tc, p, grid, smem, stream);

@@ -44,6 +44,13 @@ int launch_mxfp8_swizzle(int64_t rows, int64_t cols, const uint8_t* in, int64_t 
                          cudaStream_t stream);
 int launch_mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                                uint8_t* codes_t, uint8_t* scales_t, cudaStream_t stream);
+// The same with output row pitches: codes_t [C, ld_codes >= R], scales_t
+// [C, ld_scales >= ceil(R/32)] (bytes past R / ceil(R/32) are not written,
+// except scale bytes inside the 4-byte word of a row's last 128-row tile,
+// which are written as 0).
+int launch_mxfp8_quantize_cols_ld(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                                  uint8_t* codes_t, int64_t ld_codes, uint8_t* scales_t, int64_t ld_scales,
+                                  cudaStream_t stream);
 int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                           uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 
@@ -63,6 +70,12 @@ struct FwdArgs {
     void* q_out;
     uint8_t* q_scales;
     int* status;
+    // Row pitches of the MXFP8 operands (codes: bytes, scales: bytes; 0 = dense
+    // K and K / 32). With Dr == 0 (H = 1, Dn = the output width) the kernel is
+    // a plain block-scaled GEMM q = x W^T with a bf16 output and no rotation;
+    // the operand rows may then be longer than K (reads past K are zero codes
+    // from the tensor map; their scale bytes must be finite).
+    int64_t ld_x = 0, ld_w = 0, ld_scale = 0;
 };
 int launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
@@ -107,6 +120,14 @@ int launch_dgrad(const BwdArgs& a, cudaStream_t stream);
 int dgrad_ksplit(int64_t T, int64_t K, int64_t N, int num_sms);
 size_t dgrad_workspace_bytes(int64_t T, int64_t K, int64_t N, int num_sms);
 int launch_wgrad(const BwdArgs& a, cudaStream_t stream);
+
+// MXFP8 backward (see mla_q_uproj_bwd_mxfp8): workspace carve-up and launch.
+struct Mxfp8BwdLayout {
+    int64_t Tp;  // tokens rounded up to 128 (row pitch of the token-blocked operands)
+    size_t qa, qa_s, qb, qb_s, wt, wt_s, xt, xt_s, dbp, total;
+};
+int bwd_mxfp8_layout(int64_t T, int64_t K, int64_t N, Mxfp8BwdLayout* out);
+int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream);
 
 // Tile width (channels) of the forward kernel for this shape: the largest
 // multiple of `step` that is <= max_bn, divides N and keeps every rope region

@@ -220,19 +220,20 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&w)[8]
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
     } else {
-        for (int j = 0; j < n; ++j) dst[j] = (uint8_t)(w[j / 4] >> (8 * (j % 4)));
+#pragma unroll
+        for (int j = 0; j < 32; ++j)  // unrolled: w stays in registers
+            if (j < n) dst[j] = (uint8_t)(w[j / 4] >> (8 * (j % 4)));
     }
 }
 
 // PAIR: rows start 4-byte (bf16) / 8-byte (fp32) aligned, so a thread's two
-// columns load as one vector when both exist. VEC: R % 16 == 0 and codes_t
+// columns load as one vector when both exist. VEC: ldc % 16 == 0 and codes_t
 // 16-byte aligned, so whole blocks store as two 16-byte vectors.
 template <typename Tin, bool PAIR, bool VEC>
 __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_kernel(const Tin* __restrict__ in, int64_t R,
                                                                       int64_t C, int64_t ld,
-                                                                      uint8_t* __restrict__ codes,
-                                                                      uint8_t* __restrict__ scales) {
-    const int64_t nbr = (R + 31) / 32;  // scale bytes per output row
+                                                                      uint8_t* __restrict__ codes, int64_t ldc,
+                                                                      uint8_t* __restrict__ scales, int64_t nbr) {
     const int64_t tiles_r = (R + kColTileR - 1) / kColTileR;
     const int64_t tiles = tiles_r * ((C + kColTileC - 1) / kColTileC);
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -263,11 +264,11 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_kernel(const 
             const uint32_t sa = quantize_block_regs<32>(a, n, wa);
             const uint32_t sb = quantize_block_regs<32>(b, n, wb);
             if (has0) {
-                store_codes(codes + c * R + r0, wa, n, VEC);
+                store_codes(codes + c * ldc + r0, wa, n, VEC);
                 scales[c * nbr + r0 / 32] = (uint8_t)sa;
             }
             if (has1) {
-                store_codes(codes + (c + 1) * R + r0, wb, n, VEC);
+                store_codes(codes + (c + 1) * ldc + r0, wb, n, VEC);
                 scales[(c + 1) * nbr + r0 / 32] = (uint8_t)sb;
             }
         }
@@ -290,8 +291,8 @@ __host__ __device__ constexpr uint32_t cols_buf_bytes() { return 32u * kColTC * 
 template <typename Tin, bool VEC>
 __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const Tin* __restrict__ in, int64_t R,
                                                                      int64_t C, int64_t ld,
-                                                                     uint8_t* __restrict__ codes,
-                                                                     uint8_t* __restrict__ scales) {
+                                                                     uint8_t* __restrict__ codes, int64_t ldc,
+                                                                     uint8_t* __restrict__ scales, int64_t nbr) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int NBUF = cols_nbuf<Tin>();
     constexpr uint32_t BUF = cols_buf_bytes<Tin>();
@@ -301,10 +302,11 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
     constexpr int NB = kColTileR / 32;               // blocks per tile
     const uint32_t sbase = smem_u32(smem);
     const int t = threadIdx.x;
-    const int64_t nbr = (R + 31) / 32;
     const int64_t tiles_r = (R + kColTileR - 1) / kColTileR;
     const int64_t tiles = tiles_r * ((C + kColTC - 1) / kColTC);
-    const bool word_scales = (nbr % 4) == 0 && (reinterpret_cast<uintptr_t>(scales) % 4) == 0;
+    // a row's scale pitch holds whole 4-byte words for every tile (bytes of blocks past R are 0)
+    const bool word_scales = (nbr % 4) == 0 && nbr >= 4 * ((R + kColTileR - 1) / kColTileR) &&
+                             (reinterpret_cast<uintptr_t>(scales) % 4) == 0;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t tr = tile % tiles_r, tc = tile / tiles_r;
         const int64_t c0 = tc * kColTC;
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
                 }
                 uint32_t w[8];
                 const uint32_t sb = quantize_block_regs<32>(v, n, w);
-                store_codes(codes + c * R + r0, w, n, VEC);
+                store_codes(codes + c * ldc + r0, w, n, VEC);
                 if (word_scales) sword |= sb << (8 * blk);
                 else scales[c * nbr + r0 / 32] = (uint8_t)sb;
             }
@@ -396,13 +398,13 @@ __global__ void __launch_bounds__(256) mxfp8_swizzle_kernel(const uint8_t* __res
 }
 
 template <typename Tin>
-int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t* codes, uint8_t* scales,
-                      cudaStream_t stream) {
+int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t* codes, int64_t ldc,
+                      uint8_t* scales, int64_t lds, cudaStream_t stream) {
     DeviceInfo di;
     int st = current_device_info(&di);
     if (st != MLA_OK) return st;
     const bool pair = (reinterpret_cast<uintptr_t>(in) % (2 * sizeof(Tin)) == 0) && (ld % 2 == 0);
-    const bool vec = (R % 16 == 0) && (reinterpret_cast<uintptr_t>(codes) % 16 == 0);
+    const bool vec = (ldc % 16 == 0) && (reinterpret_cast<uintptr_t>(codes) % 16 == 0);
     constexpr int EPV = 16 / (int)sizeof(Tin);
     if (reinterpret_cast<uintptr_t>(in) % 16 == 0 && (ld * (int64_t)sizeof(Tin)) % 16 == 0 && C % EPV == 0) {
         const size_t smem = (size_t)cols_nbuf<Tin>() * cols_buf_bytes<Tin>();
@@ -416,9 +418,9 @@ int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t*
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return MLA_ERR_CUDA;
         if (vec)
-            mxfp8_quantize_cols_tiled<Tin, true><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, scales);
+            mxfp8_quantize_cols_tiled<Tin, true><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds);
         else
-            mxfp8_quantize_cols_tiled<Tin, false><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, scales);
+            mxfp8_quantize_cols_tiled<Tin, false><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds);
         return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
     }
     const int64_t tiles = ((R + kColTileR - 1) / kColTileR) * ((C + kColTileC - 1) / kColTileC);
@@ -427,10 +429,10 @@ int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t*
     if (blocks > cap) blocks = cap;
     const Tin* p = static_cast<const Tin*>(in);
     const unsigned g = (unsigned)blocks;
-    if (pair && vec) mxfp8_quantize_cols_kernel<Tin, true, true><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, scales);
-    else if (pair) mxfp8_quantize_cols_kernel<Tin, true, false><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, scales);
-    else if (vec) mxfp8_quantize_cols_kernel<Tin, false, true><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, scales);
-    else mxfp8_quantize_cols_kernel<Tin, false, false><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, scales);
+    if (pair && vec) mxfp8_quantize_cols_kernel<Tin, true, true><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, ldc, scales, lds);
+    else if (pair) mxfp8_quantize_cols_kernel<Tin, true, false><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, ldc, scales, lds);
+    else if (vec) mxfp8_quantize_cols_kernel<Tin, false, true><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, ldc, scales, lds);
+    else mxfp8_quantize_cols_kernel<Tin, false, false><<<g, kColThreads, 0, stream>>>(p, R, C, ld, codes, ldc, scales, lds);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -447,8 +449,15 @@ int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, in
 namespace mlaq {
 int launch_mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                                uint8_t* codes_t, uint8_t* scales_t, cudaStream_t stream) {
-    if (in_dtype == MLA_IN_F32) return launch_cols_typed<float>(R, C, in, ld_in, codes_t, scales_t, stream);
-    return launch_cols_typed<__nv_bfloat16>(R, C, in, ld_in, codes_t, scales_t, stream);
+    return launch_mxfp8_quantize_cols_ld(R, C, in_dtype, in, ld_in, codes_t, R, scales_t, (R + 31) / 32, stream);
+}
+
+int launch_mxfp8_quantize_cols_ld(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                                  uint8_t* codes_t, int64_t ld_codes, uint8_t* scales_t, int64_t ld_scales,
+                                  cudaStream_t stream) {
+    if (in_dtype == MLA_IN_F32)
+        return launch_cols_typed<float>(R, C, in, ld_in, codes_t, ld_codes, scales_t, ld_scales, stream);
+    return launch_cols_typed<__nv_bfloat16>(R, C, in, ld_in, codes_t, ld_codes, scales_t, ld_scales, stream);
 }
 }  // namespace mlaq
 
