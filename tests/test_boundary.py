@@ -259,6 +259,7 @@ def test_bwd_mxfp8_rejects(L):
     assert _bmx(L, _mx_shape(), dW=ctypes.c_void_p(FAKE * 7 + 8)) == S["MLA_ERR_ALIGNMENT"]
     assert _bmx(L, _mx_shape(), ws=ctypes.c_void_p(FAKE * 41 + 8)) == S["MLA_ERR_ALIGNMENT"]
     assert _bmx(L, _mx_shape(T=0), dq=None, ws=None, ws_bytes=0) in ok          # writes dW = 0, db = 0
+    assert _bmx(L, _mx_shape(T=0), dq=None, W=None, x=None, ws=None, ws_bytes=0) in ok  # empty inputs
 
 
 def test_bwd_mxfp8_layout(L):

@@ -414,8 +414,7 @@ MLAQ_API int mla_q_uproj_bwd_mxfp8(const mla_q_shape* shape, const void* dq, con
     if (st != MLA_OK) return st;
     const mla_q_shape& s = *shape;
     if (!dx && !dW && !db) return MLA_ERR_INVALID_ARG;
-    if ((dx && !W) || (dW && !x)) return MLA_ERR_INVALID_ARG;
-    if (s.T > 0 && !dq) return MLA_ERR_INVALID_ARG;
+    if (s.T > 0 && (!dq || (dx && !W) || (dW && !x))) return MLA_ERR_INVALID_ARG;
     st = check_table_and_positions(&s, cos_tab, sin_tab, pos);
     if (st != MLA_OK) return st;
     const size_t need = mla_q_uproj_workspace_size(shape, 3);
