@@ -230,16 +230,32 @@ MLAQ_API int mla_q_uproj_bwd_wgrad(const mla_q_shape *shape, const void *dq, con
  * of the wgrad operands is padded to a multiple of 128 with zero codes and
  * zero scale bytes. T == 0 writes dW = 0 and db = 0.
  */
+/*
+ * The scale arrays of mla_mxfp8_bwd_layout are in the tiled order the
+ * block-scaled GEMMs load (one bulk copy per 128 rows and K step): for an
+ * operand with `rows` rows and `cols` scale columns (cols = its K / 32),
+ * rows go in groups of G (G = 128 for operand A, b_group for operand B);
+ * each group is padded to whole 128-row chunks; chunk i of group g, K step
+ * kt (scale columns 4kt .. 4kt+3) is the 512-byte tile
+ * ((g * ceil(G/128) + i) * ceil(cols/4) + kt), and inside it row rr of the
+ * chunk, column c sits at byte (rr % 32) * 16 + (rr / 32) * 4 + c % 4. With
+ * G = 128 this is exactly mxfp8_swizzle_scales' layout of the [rows, cols]
+ * matrix. Padding bytes of the A arrays (rows T..t_pad-1 of qa_scales,
+ * token blocks ceil(T/32)..t_pad/32-1 of qb_scales) are written as 0; the
+ * B arrays' columns past ceil(T/32) too; rows that pad a B group to whole
+ * chunks are unspecified.
+ */
 typedef struct {
     int64_t t_pad;       /* T rounded up to a multiple of 128: row pitch of qb and xt */
+    int64_t b_group;     /* G of the B operands: the GEMMs' tile width over K */
     size_t qa;           /* E4M3 [T, N], blocks of 32 channels (dgrad operand A) */
-    size_t qa_scales;    /* E8M0 [T, N/32] */
-    size_t qb;           /* E4M3 [N, t_pad], blocks of 32 tokens (wgrad operand A) */
-    size_t qb_scales;    /* E8M0 [N, t_pad/32] */
+    size_t qa_scales;    /* E8M0, tiled: rows t_pad (tokens), cols N/32, G = 128 */
+    size_t qb;           /* E4M3 [N, t_pad], blocks of 32 tokens (wgrad operand A); 0 past T */
+    size_t qb_scales;    /* E8M0, tiled: rows N, cols t_pad/32, G = 128 */
     size_t wt;           /* E4M3 [K, N]: Q_cols(W) (dgrad operand B) */
-    size_t wt_scales;    /* E8M0 [K, N/32] */
+    size_t wt_scales;    /* E8M0, tiled: rows K, cols N/32, G = b_group */
     size_t xt;           /* E4M3 [K, t_pad]: Q_cols(x) (wgrad operand B) */
-    size_t xt_scales;    /* E8M0 [K, t_pad/32] */
+    size_t xt_scales;    /* E8M0, tiled: rows K, cols t_pad/32, G = b_group */
     size_t db_partials;  /* float32 [ceil(T/32), N] */
     size_t total;        /* == mla_q_uproj_workspace_size(shape, 3) */
 } mla_mxfp8_bwd_layout;

@@ -99,3 +99,23 @@ def oracle_forward(inp, w, tokens=None, quantize=False):
 
 def to_dev(inp, dev):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def sf_tiled_offsets(rows, cols, G):
+    """Byte offsets of scale (r, c), r < rows, c < cols, in the block-scaled
+    GEMMs' tiled scale order with row groups of G (mla_mxfp8_bwd_layout):
+    groups padded to whole 128-row chunks, chunk i of group g and K step kt
+    at tile (g * ceil(G/128) + i) * ceil(cols/4) + kt of 512 bytes, inside it
+    (rr % 32) * 16 + (rr // 32) * 4 + c % 4."""
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    c = np.arange(cols, dtype=np.int64)[None, :]
+    nsub, nkt = -(-G // 128), -(-cols // 4)
+    g, rg = r // G, r % G
+    i, rr = rg // 128, rg % 128
+    return ((g * nsub + i) * nkt + c // 4) * 512 + (rr % 32) * 16 + (rr // 32) * 4 + c % 4
+
+
+def sf_untile(buf, rows, cols, G):
+    """Row-major [rows, cols] scales read back from the tiled order."""
+    buf = np.asarray(buf)
+    return buf[sf_tiled_offsets(rows, cols, G)]

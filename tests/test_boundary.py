@@ -269,10 +269,12 @@ def test_bwd_mxfp8_layout(L):
                             (4096, 1536, 128, 128, 64)):
         N = H * (Dn + Dr)
         lay = mlaq.bwd_mxfp8_layout(T, K, H, Dn, Dr, max(T, 1), Dr)
-        Tp = lay["t_pad"]
+        Tp, G = lay["t_pad"], lay["b_group"]
         assert Tp % 128 == 0 and Tp - 128 < T <= Tp
-        sizes = [("qa", T * N), ("qa_scales", T * N // 32), ("qb", N * Tp), ("qb_scales", N * Tp // 32),
-                 ("wt", K * N), ("wt_scales", K * N // 32), ("xt", K * Tp), ("xt_scales", K * Tp // 32),
+        assert K % G == 0 and G % 32 == 0 and G <= 192
+        bsz = lambda cols: K // G * -(-G // 128) * -(-cols // 4) * 512   # B: groups padded to 128 rows
+        sizes = [("qa", T * N), ("qa_scales", Tp * N // 32), ("qb", N * Tp), ("qb_scales", N * Tp // 32),
+                 ("wt", K * N), ("wt_scales", bsz(N // 32)), ("xt", K * Tp), ("xt_scales", bsz(Tp // 32)),
                  ("db_partials", 4 * N * ((T + 31) // 32))]
         end = 0
         for name, size in sizes:

@@ -32,8 +32,8 @@ SHAPES = [
     ("tiny", dict(T=256, K=64, H=4, Dn=32, Dr=32)),
     ("tiny", dict(T=1, K=32, H=2, Dn=32, Dr=32)),          # one token, smallest N
     ("tiny", dict(T=416, K=224, H=3, Dn=64, Dr=64, seq_len=128)),  # 3 heads (N = 384), positions restart
-    ("dsv3_bwd", dict(T=300, H=2, seq_len=None)),           # DeepSeek-V3 head, K = 1536
-    ("dsv3_long_yarn", dict(T=160, H=2, seq_len=None)),     # YaRN table
+    ("dsv3_bwd", dict(T=300, H=4, seq_len=None)),           # DeepSeek-V3 heads, K = 1536 (256-channel path)
+    ("dsv3_long_yarn", dict(T=160, H=2, seq_len=None)),     # YaRN table; N = 384: per-head path
 ]
 
 
@@ -82,16 +82,25 @@ def test_bwd_mxfp8_matches_oracle(cuda_device, name, ov):
     g = oracle.backward_mxfp8(helpers.f64(inp["dq"]), helpers.f64(inp["x"]), helpers.f64(inp["W"]), w.H,
                               w.Dn, w.Dr, inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy())
     ops = mlaq.bwd_mxfp8_operands(ws, w.T, w.K, w.H, w.Dn, w.Dr, d["cos"].shape[0], d["cos"].shape[1])
-    T, nbt, Tp = w.T, (w.T + 31) // 32, ops["t_pad"]
+    T, N, K, nbt, Tp, G = w.T, w.N, w.K, (w.T + 31) // 32, ops["t_pad"], ops["b_group"]
     assert Tp % 128 == 0 and Tp - 128 < T <= Tp
-    for key in ("qa", "qa_s", "wt", "wt_s"):
+    for key in ("qa", "wt"):
         assert np.array_equal(_np(ops[key]), g[key]), key
     for key in ("qb", "xt"):
         assert np.array_equal(_np(ops[key])[:, :T], g[key]), key
-    for key in ("qb_s", "xt_s"):
-        got = _np(ops[key])
-        assert np.array_equal(got[:, :nbt], g[key]), key
-        assert not got[:, nbt:].any(), f"{key}: padding scale bytes must be 0"
+    assert not _np(ops["qb"])[:, T:].any(), "qb: padding tokens must be 0"
+    # A operands: the whole tiled array is the oracle's swizzle of the zero-padded scales
+    qa_s = np.zeros((Tp, N // 32), np.uint8)
+    qa_s[:T] = g["qa_s"]
+    assert np.array_equal(_np(ops["qa_s"]), oracle.mxfp8_swizzle_scales(qa_s)), "qa_s"
+    qb_s = np.zeros((N, Tp // 32), np.uint8)
+    qb_s[:, :nbt] = g["qb_s"]
+    assert np.array_equal(_np(ops["qb_s"]), oracle.mxfp8_swizzle_scales(qb_s)), "qb_s"
+    # B operands: groups of G rows
+    assert np.array_equal(helpers.sf_untile(_np(ops["wt_s"]), K, N // 32, G), g["wt_s"]), "wt_s"
+    xt_s = helpers.sf_untile(_np(ops["xt_s"]), K, Tp // 32, G)
+    assert np.array_equal(xt_s[:, :nbt], g["xt_s"]), "xt_s"
+    assert not xt_s[:, nbt:].any(), "xt_s: padding token blocks must be 0"
     A = np.abs(oracle.mxfp8_dequantize(g["qa"], g["qa_s"]))
     B = np.abs(oracle.mxfp8_dequantize(g["wt"], g["wt_s"]))
     _check_gemm(dx, g["dx"], A @ B.T, "dx")
@@ -169,19 +178,24 @@ def test_bwd_mxfp8_full_size_sampled(cuda_device):
     mlaq.check_status(st)
     cs, sn, pos = inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy()
     ops = mlaq.bwd_mxfp8_operands(ws, w.T, w.K, w.H, w.Dn, w.Dr, cs.shape[0], cs.shape[1])
+    Tp, G = ops["t_pad"], ops["b_group"]
     rng = np.random.default_rng(7)
     W, x = helpers.f64(inp["W"]), helpers.f64(inp["x"])
     wt, wt_s = oracle.mxfp8_quantize_columns(W)
     xt, xt_s = oracle.mxfp8_quantize_columns(x)
-    assert np.array_equal(_np(ops["wt"]), wt) and np.array_equal(_np(ops["wt_s"]), wt_s)
-    assert np.array_equal(_np(ops["xt"]), xt) and np.array_equal(_np(ops["xt_s"]), xt_s)
+    assert np.array_equal(_np(ops["wt"]), wt)
+    assert np.array_equal(helpers.sf_untile(_np(ops["wt_s"]), w.K, w.N // 32, G), wt_s)
+    assert np.array_equal(_np(ops["xt"]), xt)
+    assert np.array_equal(helpers.sf_untile(_np(ops["xt_s"]), w.K, Tp // 32, G), xt_s)
+    qa_s_rows = helpers.sf_untile(_np(ops["qa_s"]), Tp, w.N // 32, 128)
+    qb_s_rows = helpers.sf_untile(_np(ops["qb_s"]), w.N, Tp // 32, 128)
     Bw, Bx = oracle.mxfp8_dequantize(wt, wt_s), oracle.mxfp8_dequantize(xt, xt_s)
     # dx and the rowwise operand on sampled tokens (rows are independent)
     toks = np.sort(rng.choice(w.T, 24, replace=False))
     dqp = oracle.rope_bwd_f32(helpers.f64(inp["dq"][torch.from_numpy(toks)]), w.H, w.Dn, w.Dr, cs, sn,
                               pos[toks]).reshape(len(toks), -1).astype(np.float64)
     qa, qa_s = oracle.mxfp8_quantize(dqp)
-    assert np.array_equal(_np(ops["qa"])[toks], qa) and np.array_equal(_np(ops["qa_s"])[toks], qa_s)
+    assert np.array_equal(_np(ops["qa"])[toks], qa) and np.array_equal(qa_s_rows[toks], qa_s)
     A = oracle.mxfp8_dequantize(qa, qa_s)
     _check_gemm(dx[torch.from_numpy(toks).to(cuda_device)], A @ Bw.T, np.abs(A) @ np.abs(Bw).T, "dx")
     # dW and the columnwise operand on sampled heads (a head's channels need only that head's dq)
@@ -190,7 +204,7 @@ def test_bwd_mxfp8_full_size_sampled(cuda_device):
                                 w.Dn, w.Dr, cs, sn, pos).reshape(w.T, -1).astype(np.float64)
     qb, qb_s = oracle.mxfp8_quantize_columns(dqp_h)
     ch = (heads[:, None] * w.D + np.arange(w.D)[None, :]).reshape(-1)
-    assert np.array_equal(_np(ops["qb"])[ch], qb) and np.array_equal(_np(ops["qb_s"])[ch], qb_s)
+    assert np.array_equal(_np(ops["qb"])[ch], qb) and np.array_equal(qb_s_rows[ch], qb_s)
     A = oracle.mxfp8_dequantize(qb, qb_s)
     _check_gemm(dW[torch.from_numpy(ch).to(cuda_device)], A @ Bx.T, np.abs(A) @ np.abs(Bx).T, "dW")
     # db on every channel, 16 heads at a time

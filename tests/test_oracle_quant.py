@@ -242,3 +242,20 @@ def test_swizzle_is_a_permutation_with_zero_padding():
         assert out.size == ((rows + 127) // 128) * 128 * ((cols + 3) // 4) * 4
         assert np.array_equal(np.sort(out[out != 0]), np.sort(s.reshape(-1)))
         assert int(np.count_nonzero(out)) == rows * cols
+
+
+def test_tiled_scale_order_is_the_swizzle_for_128_row_groups():
+    """The tests' reader of the GEMM tiled scale order agrees with the
+    oracle's swizzle (written from the definition) when groups are 128 rows,
+    and with the swizzle of each padded group otherwise."""
+    import helpers
+    rng = np.random.default_rng(3)
+    for rows, cols in ((130, 7), (256, 24), (1, 1), (300, 9)):
+        s = rng.integers(0, 256, (rows, cols), dtype=np.uint8)
+        sw = oracle.mxfp8_swizzle_scales(s)
+        assert np.array_equal(helpers.sf_untile(sw, rows, cols, 128), s)
+    for G in (192, 96, 32):
+        rows, cols = 2 * G, 10
+        s = rng.integers(0, 256, (rows, cols), dtype=np.uint8)
+        buf = np.concatenate([oracle.mxfp8_swizzle_scales(s[g * G:(g + 1) * G]) for g in range(2)])
+        assert np.array_equal(helpers.sf_untile(buf, rows, cols, G), s)

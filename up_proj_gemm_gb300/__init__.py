@@ -61,7 +61,7 @@ class KvShape(ctypes.Structure):
 
 
 class Mxfp8BwdLayout(ctypes.Structure):
-    _fields_ = [("t_pad", ctypes.c_int64)] + [(n, ctypes.c_size_t) for n in (
+    _fields_ = [("t_pad", ctypes.c_int64), ("b_group", ctypes.c_int64)] + [(n, ctypes.c_size_t) for n in (
         "qa", "qa_scales", "qb", "qb_scales", "wt", "wt_scales", "xt", "xt_scales", "db_partials", "total")]
 
 
@@ -287,20 +287,25 @@ def bwd_mxfp8_layout(T, K, H, Dn, Dr, cs_rows, cs_width) -> dict:
 
 def bwd_mxfp8_operands(workspace, T, K, H, Dn, Dr, cs_rows, cs_width) -> dict:
     """uint8 views of the quantized operands a bwd_mxfp8 call left in
-    ``workspace``: qa [T, N], qa_s [T, N/32], qb [N, t_pad], qb_s
-    [N, t_pad/32], wt [K, N], wt_s [K, N/32], xt [K, t_pad], xt_s
-    [K, t_pad/32] (t_pad = T rounded up to 128)."""
+    ``workspace``: codes qa [T, N], qb [N, t_pad], wt [K, N], xt [K, t_pad]
+    (t_pad = T rounded up to 128) and the flat scale arrays qa_s, qb_s,
+    wt_s, xt_s in the GEMMs' tiled order (see mla_mxfp8_bwd_layout), plus
+    ``t_pad`` and ``b_group``."""
     L = bwd_mxfp8_layout(T, K, H, Dn, Dr, cs_rows, cs_width)
     N = H * (Dn + Dr)
-    Tp = L["t_pad"]
+    Tp, G = L["t_pad"], L["b_group"]
 
     def view(off, rows, cols):
         return workspace[off:off + rows * cols].view(rows, cols)
 
-    return dict(qa=view(L["qa"], T, N), qa_s=view(L["qa_scales"], T, N // 32),
-                qb=view(L["qb"], N, Tp), qb_s=view(L["qb_scales"], N, Tp // 32),
-                wt=view(L["wt"], K, N), wt_s=view(L["wt_scales"], K, N // 32),
-                xt=view(L["xt"], K, Tp), xt_s=view(L["xt_scales"], K, Tp // 32), t_pad=Tp)
+    def tiled(off, rows, cols, g):
+        n = -(-rows // g) * -(-g // 128) * -(-cols // 4) * 512
+        return workspace[off:off + n]
+
+    return dict(qa=view(L["qa"], T, N), qa_s=tiled(L["qa_scales"], Tp, N // 32, 128),
+                qb=view(L["qb"], N, Tp), qb_s=tiled(L["qb_scales"], N, Tp // 32, 128),
+                wt=view(L["wt"], K, N), wt_s=tiled(L["wt_scales"], K, N // 32, G),
+                xt=view(L["xt"], K, Tp), xt_s=tiled(L["xt_scales"], K, Tp // 32, G), t_pad=Tp, b_group=G)
 
 
 def bwd_mxfp8(dq, W, x, cos, sin, H, Dn, Dr, pos=None, dx=True, dW=True, db=True, status=None, stream=None,

@@ -391,6 +391,7 @@ MLAQ_API int mla_q_uproj_bwd_mxfp8_layout(const mla_q_shape* shape, mla_mxfp8_bw
     st = bwd_mxfp8_layout(shape->T, shape->K, N, &L);
     if (st != MLA_OK) return st;
     out->t_pad = L.Tp;
+    out->b_group = L.G;
     out->qa = L.qa;
     out->qa_scales = L.qa_s;
     out->qb = L.qb;

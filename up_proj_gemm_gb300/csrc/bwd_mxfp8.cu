@@ -27,119 +27,234 @@ namespace {
 
 constexpr int kRqThreads = 256;
 
-// One CTA: 32 tokens [t0, t0 + 32) x one head's D channels (D % 32 == 0),
-// staged in shared memory as float32 with a row pitch of D + 1 words, so
-// that row-wise and column-wise reads are both free of bank conflicts.
-//   qa [T, N] / qa_s [T, N/32]: rowwise copy (nullable: skipped)
-//   qb [N, ldq] / qb_s [N, ldq/32]: columnwise copy (nullable: skipped);
-//     the CTA of the last token block also zeroes the scale bytes of the
-//     token blocks in [ceil(T/32), ldq/32) (the padding the GEMM reads)
-//   dbp [ceil(T/32), N]: per-block channel sums (nullable: skipped)
+__device__ __forceinline__ void load8_f32(const float* src, bool vec, float (&o)[8]) {
+    if (vec) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = __ldg(src + e);
+    }
+}
+
+__device__ __forceinline__ void unpack8(uint4 raw, float (&v)[8]) {
+    v[0] = bf16lo_to_f32(raw.x);
+    v[1] = bf16hi_to_f32(raw.x);
+    v[2] = bf16lo_to_f32(raw.y);
+    v[3] = bf16hi_to_f32(raw.y);
+    v[4] = bf16lo_to_f32(raw.z);
+    v[5] = bf16hi_to_f32(raw.z);
+    v[6] = bf16lo_to_f32(raw.w);
+    v[7] = bf16hi_to_f32(raw.w);
+}
+
+// Outputs of one pass (all in the workspace):
+//   qa [T, N]: rowwise codes; qa_s: their scales in the GEMM tiled order
+//     (rows = tokens up to Tp, G = 128, nkt_n = N / 128 K steps)
+//   qb [N, Tp]: columnwise codes (tokens past T are 0); qb_s: tiled order
+//     (rows = channels, G = 128, nkt_t = Tp / 128 K steps)
+//   dbp [ceil(T/32), N]: float32 sums of each 32-token block
+// Every scale byte of both tiled arrays is written (0 where the values are 0).
+struct RqArgs {
+    const uint16_t* dq;
+    int64_t T, Tp;
+    int H, Dn;
+    const float* cos_tab;
+    const float* sin_tab;
+    int64_t cs_rows, cs_width;
+    int cs_vec;
+    const int32_t* pos;
+    uint8_t* qa;
+    uint8_t* qa_s;
+    uint8_t* qb;
+    uint8_t* qb_s;
+    float* dbp;
+    int* status;
+};
+
+// Fast path: a CTA takes 32 tokens x 256 channels of dq viewed as [T, N]
+// (N % 256 == 0, and no rope region crosses a 256-channel span: Dr == 32, or
+// Dn % 64 == 0). Warp w takes token rows w, w + 8, w + 16, w + 24; lane l
+// holds channels [8l, 8l + 8) of the span (one 16-byte load). A 32-channel
+// block is a lane quad (amax by two shuffles); a rope pair's partner channels
+// sit Dr/16 lanes away (one shuffle exchange). The float32 rows then go to a
+// shared tile whose columns thread c reads for the token-blocked copy and the
+// db partial of channel c.
 template <int DR>
-__global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_kernel(
-    const uint16_t* __restrict__ dq, int64_t T, int H, int Dn, const float* __restrict__ cos_tab,
-    const float* __restrict__ sin_tab, int64_t cs_rows, int64_t cs_width, const int32_t* __restrict__ pos,
-    uint8_t* __restrict__ qa, uint8_t* __restrict__ qa_s, uint8_t* __restrict__ qb, uint8_t* __restrict__ qb_s,
-    int64_t ldq, float* __restrict__ dbp, int* status) {
-    extern __shared__ float tile[];
+__global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a) {
+    __shared__ __align__(16) float tile[32][256];
     constexpr int HH = DR / 2;
-    const int D = Dn + DR;
+    constexpr int PX = HH / 8;  // lanes between the two channels of a rope pair
+    const int D = a.Dn + DR;
+    const int64_t N = (int64_t)a.H * D;
+    const int64_t ntb = a.Tp / 32;
+    const int64_t tb = blockIdx.x % ntb;
+    const int64_t n0 = (int64_t)(blockIdx.x / ntb) * 256;
+    const int64_t t0 = tb * 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n = n0 + 8 * lane;
+    const int c = (int)(n % D);  // channel within the head
+    const bool rope = c >= a.Dn;
+    const int q0 = c - a.Dn;     // rope index of the lane's first channel
+    const bool first = q0 < HH;  // holds i (else i + Dr/2) of its pairs
+    const int64_t nkt_n = N / 128;
+#pragma unroll 1
+    for (int it = 0; it < 4; ++it) {
+        const int r = warp + 8 * it;
+        const int64_t t = t0 + r;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (t < a.T) raw = __ldg(reinterpret_cast<const uint4*>(a.dq + t * N + n));
+        float v[8];
+        unpack8(raw, v);
+        // the partner half of every rope pair (all lanes take part in the shuffle)
+        uint4 pr;
+        pr.x = __shfl_xor_sync(0xffffffffu, raw.x, PX);
+        pr.y = __shfl_xor_sync(0xffffffffu, raw.y, PX);
+        pr.z = __shfl_xor_sync(0xffffffffu, raw.z, PX);
+        pr.w = __shfl_xor_sync(0xffffffffu, raw.w, PX);
+        if (rope && t < a.T) {
+            const int64_t pp = a.pos ? (int64_t)__ldg(a.pos + t) : t;
+            if (pp < 0 || pp >= a.cs_rows) {
+                record_status(a.status, MLA_ERR_POS_RANGE);
+            } else {
+                // out_i = fl(fl(g_i c_i) + fl(g_{i+h} s_{i+h})), out_{i+h} = fl(fl(g_{i+h} c_{i+h}) - fl(g_i s_i))
+                float o[8], cw[8], sw[8];
+                unpack8(pr, o);
+                load8_f32(a.cos_tab + pp * a.cs_width + q0, a.cs_vec != 0, cw);
+                load8_f32(a.sin_tab + pp * a.cs_width + (first ? q0 + HH : q0 - HH), a.cs_vec != 0, sw);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    v[k] = first ? __fadd_rn(__fmul_rn(v[k], cw[k]), __fmul_rn(o[k], sw[k]))
+                                 : __fsub_rn(__fmul_rn(v[k], cw[k]), __fmul_rn(o[k], sw[k]));
+            }
+        }
+        // rowwise block of 32 channels = this lane quad
+        uint32_t mb = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mb = max(mb, __float_as_uint(v[k]) & 0x7FFFFFFFu);
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        uint32_t w[2];
+        const uint32_t sb = quantize8_block_scale(v, mb, w);
+        if (a.qa) {
+            if (t < a.T) *reinterpret_cast<uint2*>(a.qa + t * N + n) = make_uint2(w[0], w[1]);
+            // the scale bytes of 4 consecutive blocks are one word of the tiled order
+            const uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 4) << 8) |
+                                  (__shfl_down_sync(0xffffffffu, sb, 8) << 16) |
+                                  (__shfl_down_sync(0xffffffffu, sb, 12) << 24);
+            if ((lane & 15) == 0)
+                *reinterpret_cast<uint32_t*>(a.qa_s + sf_tiled_offset(t, n / 32, 128, nkt_n)) = word;
+        }
+        *reinterpret_cast<float4*>(&tile[r][8 * lane]) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(&tile[r][8 * lane + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    __syncthreads();
+    // token-blocked copy and db partial of channel n0 + threadIdx.x
+    const int col = threadIdx.x;
+    const int64_t ch = n0 + col;
+    float v[32];
+    float sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        v[r] = tile[r][col];
+        sum += v[r];  // token order; rows past T are 0
+    }
+    if (a.qb) {
+        const int64_t left = a.T - t0;
+        const int nv = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
+        uint32_t w[8];
+        const uint32_t sb = quantize_block_regs<32>(v, nv, w);
+        uint8_t* dst = a.qb + ch * a.Tp + t0;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        a.qb_s[sf_tiled_offset(ch, tb, 128, a.Tp / 128)] = (uint8_t)sb;
+    }
+    if (a.dbp && t0 < a.T) a.dbp[tb * N + ch] = sum;
+}
+
+// General shapes: a CTA takes 32 tokens x one head (D % 32 == 0), staged in
+// shared memory as float32 with a row pitch of D + 1 words; same outputs.
+template <int DR>
+__global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_kernel(const RqArgs a) {
+    extern __shared__ float stile[];
+    constexpr int HH = DR / 2;
+    const int D = a.Dn + DR;
     const int P = D + 1;  // row pitch (words)
-    const int64_t N = (int64_t)H * D;
-    const int64_t nbt = (T + 31) / 32;  // token blocks
-    const int64_t tb = blockIdx.x % nbt;
-    const int h = (int)(blockIdx.x / nbt);
+    const int64_t N = (int64_t)a.H * D;
+    const int64_t ntb = a.Tp / 32;
+    const int64_t tb = blockIdx.x % ntb;
+    const int h = (int)(blockIdx.x / ntb);
     const int64_t t0 = tb * 32;
     const int tid = threadIdx.x;
-    // load: 32 rows x D bf16, 8 per 16-byte vector; rows past T are zeros
     const int vpr = D / 8;
     for (int k = tid; k < 32 * vpr; k += kRqThreads) {
         const int r = k / vpr, v = k % vpr;
         const int64_t t = t0 + r;
         uint4 raw = make_uint4(0, 0, 0, 0);
-        if (t < T) raw = __ldg(reinterpret_cast<const uint4*>(dq + t * N + (int64_t)h * D + 8 * v));
-        float* dst = tile + r * P + 8 * v;
-        dst[0] = bf16lo_to_f32(raw.x);
-        dst[1] = bf16hi_to_f32(raw.x);
-        dst[2] = bf16lo_to_f32(raw.y);
-        dst[3] = bf16hi_to_f32(raw.y);
-        dst[4] = bf16lo_to_f32(raw.z);
-        dst[5] = bf16hi_to_f32(raw.z);
-        dst[6] = bf16lo_to_f32(raw.w);
-        dst[7] = bf16hi_to_f32(raw.w);
+        if (t < a.T) raw = __ldg(reinterpret_cast<const uint4*>(a.dq + t * N + (int64_t)h * D + 8 * v));
+        float f[8];
+        unpack8(raw, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) stile[r * P + 8 * v + e] = f[e];
     }
     __syncthreads();
-    // inverse rotation of the rope channels (the transpose of the forward's
-    // rotate-half pair), float32, each product and each sum rounded once:
-    //   out[i]     = fl(fl(g[i] cos_i) + fl(g[i+h] sin_{i+h}))
-    //   out[i + h] = fl(fl(g[i+h] cos_{i+h}) - fl(g[i] sin_i))
     for (int k = tid; k < 32 * HH; k += kRqThreads) {
         const int r = k / HH, i = k % HH;
         const int64_t t = t0 + r;
-        if (t >= T) continue;
-        const int64_t pp = pos ? (int64_t)__ldg(pos + t) : t;
-        if (pp < 0 || pp >= cs_rows) {
-            record_status(status, MLA_ERR_POS_RANGE);
+        if (t >= a.T) continue;
+        const int64_t pp = a.pos ? (int64_t)__ldg(a.pos + t) : t;
+        if (pp < 0 || pp >= a.cs_rows) {
+            record_status(a.status, MLA_ERR_POS_RANGE);
             continue;
         }
-        const float* cs = cos_tab + pp * cs_width;
-        const float* sn = sin_tab + pp * cs_width;
-        float* row = tile + r * P + Dn;
-        const float a = row[i], c = row[i + HH];
-        row[i] = __fadd_rn(__fmul_rn(a, __ldg(cs + i)), __fmul_rn(c, __ldg(sn + i + HH)));
-        row[i + HH] = __fsub_rn(__fmul_rn(c, __ldg(cs + i + HH)), __fmul_rn(a, __ldg(sn + i)));
+        const float* cs = a.cos_tab + pp * a.cs_width;
+        const float* sn = a.sin_tab + pp * a.cs_width;
+        float* row = stile + r * P + a.Dn;
+        const float g0 = row[i], g1 = row[i + HH];
+        row[i] = __fadd_rn(__fmul_rn(g0, __ldg(cs + i)), __fmul_rn(g1, __ldg(sn + i + HH)));
+        row[i + HH] = __fsub_rn(__fmul_rn(g1, __ldg(cs + i + HH)), __fmul_rn(g0, __ldg(sn + i)));
     }
     __syncthreads();
-    // rowwise copy: blocks of 32 channels of one token; a thread takes one
-    // (block, token) pair, the lanes of a warp 32 consecutive tokens
-    if (qa) {
-        const int nb = D / 32;
-        for (int k = tid; k < 32 * nb; k += kRqThreads) {
-            const int b = k / 32, r = k % 32;
-            const int64_t t = t0 + r;
-            if (t >= T) continue;
-            float v[32];
+    const int nb = D / 32;
+    const int64_t nkt_n = N / 128;
+    for (int k = tid; a.qa && k < 32 * nb; k += kRqThreads) {
+        const int b = k / 32, r = k % 32;
+        const int64_t t = t0 + r;
+        float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = tile[r * P + 32 * b + i];
-            uint32_t w[8];
-            const uint32_t sb = quantize_block_regs<32>(v, 32, w);
-            uint8_t* dst = qa + t * N + (int64_t)h * D + 32 * b;
+        for (int i = 0; i < 32; ++i) v[i] = stile[r * P + 32 * b + i];
+        uint32_t w[8];
+        const uint32_t sb = quantize_block_regs<32>(v, 32, w);
+        const int64_t blk = ((int64_t)h * D) / 32 + b;
+        if (t < a.T) {
+            uint8_t* dst = a.qa + t * N + (int64_t)h * D + 32 * b;
             *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
             *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-            qa_s[t * (N / 32) + ((int64_t)h * D) / 32 + b] = (uint8_t)sb;
         }
+        a.qa_s[sf_tiled_offset(t, blk, 128, nkt_n)] = (uint8_t)sb;
     }
-    // columnwise copy (blocks of 32 tokens of one channel) and the db partial sums
-    if (qb || dbp) {
-        const int n = (T - t0) < 32 ? (int)(T - t0) : 32;
-        const int64_t lds = ldq / 32;
-        for (int c = tid; c < D; c += kRqThreads) {
-            float v[32];
-            float sum = 0.f;
+    const int64_t left = a.T - t0;
+    const int nv = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
+    for (int c = tid; c < D; c += kRqThreads) {
+        float v[32];
+        float sum = 0.f;
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                v[r] = tile[r * P + c];
-                sum += v[r];  // in token order; rows past T are 0
-            }
-            const int64_t ch = (int64_t)h * D + c;
-            if (qb) {
-                uint32_t w[8];
-                const uint32_t sb = quantize_block_regs<32>(v, n, w);
-                uint8_t* dst = qb + ch * ldq + t0;
-                if (n == 32) {
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)  // unrolled: w stays in registers
-                        if (j < n) dst[j] = (uint8_t)(w[j / 4] >> (8 * (j % 4)));
-                }
-                qb_s[ch * lds + tb] = (uint8_t)sb;
-                if (tb == nbt - 1)
-                    for (int64_t j = nbt; j < lds; ++j) qb_s[ch * lds + j] = 0;
-            }
-            if (dbp) dbp[tb * N + ch] = sum;
+        for (int r = 0; r < 32; ++r) {
+            v[r] = stile[r * P + c];
+            sum += v[r];
         }
+        const int64_t ch = (int64_t)h * D + c;
+        if (a.qb) {
+            uint32_t w[8];
+            const uint32_t sb = quantize_block_regs<32>(v, nv, w);
+            uint8_t* dst = a.qb + ch * a.Tp + t0;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+            a.qb_s[sf_tiled_offset(ch, tb, 128, a.Tp / 128)] = (uint8_t)sb;
+        }
+        if (a.dbp && t0 < a.T) a.dbp[tb * N + ch] = sum;
     }
 }
 
@@ -173,6 +288,8 @@ unsigned grid_for(int64_t items, int64_t per_block, int64_t cap) {
 
 int bwd_mxfp8_layout(int64_t T, int64_t K, int64_t N, Mxfp8BwdLayout* L) {
     if (T < 0 || K <= 0 || N <= 0 || !L) return MLA_ERR_INVALID_ARG;
+    const int64_t G = fwd_tile_n(K, (int)K, (int)K, 0, 192, 32);  // the GEMMs' tile width over K
+    if (G == 0) return MLA_ERR_UNSUPPORTED;
     const int64_t Tp = (T + 127) / 128 * 128;
     const int64_t nbt = (T + 31) / 32;
     size_t off = 0;
@@ -182,46 +299,61 @@ int bwd_mxfp8_layout(int64_t T, int64_t K, int64_t N, Mxfp8BwdLayout* L) {
         return at;
     };
     L->Tp = Tp;
+    L->G = G;
     L->qa = take((size_t)T * N);
-    L->qa_s = take((size_t)T * (N / 32));
+    L->qa_s = take((size_t)sf_tiled_bytes(Tp, N / 32, 128));
     L->qb = take((size_t)N * Tp);
-    L->qb_s = take((size_t)N * (Tp / 32));
+    L->qb_s = take((size_t)sf_tiled_bytes(N, Tp / 32, 128));
     L->wt = take((size_t)K * N);
-    L->wt_s = take((size_t)K * (N / 32));
+    L->wt_s = take((size_t)sf_tiled_bytes(K, N / 32, G));
     L->xt = take((size_t)K * Tp);
-    L->xt_s = take((size_t)K * (Tp / 32));
+    L->xt_s = take((size_t)sf_tiled_bytes(K, Tp / 32, G));
     L->dbp = take((size_t)nbt * N * sizeof(float));
     L->total = off;
     return MLA_OK;
 }
 
-int launch_rope_bwd_quant(const BwdArgs& a, uint8_t* qa, uint8_t* qa_s, uint8_t* qb, uint8_t* qb_s, int64_t ldq,
+int launch_rope_bwd_quant(const BwdArgs& a, int64_t Tp, uint8_t* qa, uint8_t* qa_s, uint8_t* qb, uint8_t* qb_s,
                           float* dbp, cudaStream_t stream) {
+    RqArgs r{};
+    r.dq = static_cast<const uint16_t*>(a.dq);
+    r.T = a.T;
+    r.Tp = Tp;
+    r.H = a.H;
+    r.Dn = a.Dn;
+    r.cos_tab = a.cos_tab;
+    r.sin_tab = a.sin_tab;
+    r.cs_rows = a.cs_rows;
+    r.cs_width = a.cs_width;
+    r.cs_vec = (a.cs_width % 4 == 0) && (reinterpret_cast<uintptr_t>(a.cos_tab) % 16 == 0) &&
+               (reinterpret_cast<uintptr_t>(a.sin_tab) % 16 == 0);
+    r.pos = a.pos;
+    r.qa = qa;
+    r.qa_s = qa_s;
+    r.qb = qb;
+    r.qb_s = qb_s;
+    r.dbp = dbp;
+    r.status = a.status;
     const int D = a.Dn + a.Dr;
-    const int64_t nbt = (a.T + 31) / 32;
-    const size_t smem = (size_t)32 * (D + 1) * sizeof(float);
-    const unsigned grid = (unsigned)(nbt * a.H);
-    const uint16_t* dq = static_cast<const uint16_t*>(a.dq);
-    const void* k = nullptr;
-    switch (a.Dr) {
-        case 16: k = (const void*)rope_bwd_quant_kernel<16>; break;
-        case 32: k = (const void*)rope_bwd_quant_kernel<32>; break;
-        case 64: k = (const void*)rope_bwd_quant_kernel<64>; break;
-        default: return MLA_ERR_UNSUPPORTED;
+    const int64_t N = (int64_t)a.H * D;
+    const int64_t ntb = Tp / 32;
+    // the fast path needs whole 256-channel spans and rope pairs inside one span
+    const bool fast = N % 256 == 0 && (a.Dr == 32 || (a.Dr == 64 && a.Dn % 64 == 0));
+    if (fast) {
+        const unsigned grid = (unsigned)(ntb * (N / 256));
+        if (a.Dr == 32) rope_bwd_quant_fast<32><<<grid, kRqThreads, 0, stream>>>(r);
+        else rope_bwd_quant_fast<64><<<grid, kRqThreads, 0, stream>>>(r);
+        return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
     }
+    const size_t smem = (size_t)32 * (D + 1) * sizeof(float);
+    const unsigned grid = (unsigned)(ntb * a.H);
+    const void* k = a.Dr == 32 ? (const void*)rope_bwd_quant_kernel<32> : (const void*)rope_bwd_quant_kernel<64>;
+    if (a.Dr != 32 && a.Dr != 64) return MLA_ERR_UNSUPPORTED;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MLA_ERR_CUDA;
-#define MLAQ_RQ_LAUNCH(DRV)                                                                                   \
-    rope_bwd_quant_kernel<DRV><<<grid, kRqThreads, smem, stream>>>(dq, a.T, a.H, a.Dn, a.cos_tab, a.sin_tab,   \
-                                                                   a.cs_rows, a.cs_width, a.pos, qa, qa_s, qb, \
-                                                                   qb_s, ldq, dbp, a.status)
-    switch (a.Dr) {
-        case 16: MLAQ_RQ_LAUNCH(16); break;
-        case 32: MLAQ_RQ_LAUNCH(32); break;
-        default: MLAQ_RQ_LAUNCH(64); break;
-    }
-#undef MLAQ_RQ_LAUNCH
+    if (a.Dr == 32) rope_bwd_quant_kernel<32><<<grid, kRqThreads, smem, stream>>>(r);
+    else rope_bwd_quant_kernel<64><<<grid, kRqThreads, smem, stream>>>(r);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -250,15 +382,13 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
     if (st != MLA_OK) return st;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     const bool want_dx = a.dx != nullptr, want_dw = a.dW != nullptr, want_db = a.db != nullptr;
-    uint8_t* qa = want_dx ? ws + L.qa : nullptr;
-    uint8_t* qb = want_dw ? ws + L.qb : nullptr;
-    float* dbp = want_db ? reinterpret_cast<float*>(ws + L.dbp) : nullptr;
-    // 1. rotate dq once; both MXFP8 copies of dq_pre and the db partials
-    st = launch_rope_bwd_quant(a, qa, ws + L.qa_s, qb, ws + L.qb_s, L.Tp, dbp, stream);
+    // 1. rotate dq once: both MXFP8 copies of dq_pre (scales in the GEMM's tiled order) and the db partials
+    st = launch_rope_bwd_quant(a, L.Tp, want_dx ? ws + L.qa : nullptr, ws + L.qa_s, want_dw ? ws + L.qb : nullptr,
+                               ws + L.qb_s, want_db ? reinterpret_cast<float*>(ws + L.dbp) : nullptr, stream);
     if (st != MLA_OK) return st;
     if (want_dx) {
-        // 2. W [N, K] -> wt [K, N], blocks along N; 3. dx = qa . wt^T (reduction over N)
-        st = launch_mxfp8_quantize_cols_ld(N, K, MLA_IN_BF16, a.W, K, ws + L.wt, N, ws + L.wt_s, N / 32, stream);
+        // 2. W [N, K] -> wt [K, N], blocks along N; 3. dx = qa . wt^T (block-scaled GEMM, reduction over N)
+        st = launch_mxfp8_quantize_cols_tiled_sf(N, K, MLA_IN_BF16, a.W, K, ws + L.wt, N, ws + L.wt_s, L.G, stream);
         if (st != MLA_OK) return st;
         FwdArgs g{};
         g.T = T;
@@ -268,25 +398,23 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
         g.Dr = 0;
         g.weight_mode = MLA_WEIGHT_MXFP8;
         g.out_mode = MLA_OUT_BF16;
-        g.x = qa;
+        g.x = ws + L.qa;
         g.x_scales = ws + L.qa_s;
         g.W = ws + L.wt;
         g.w_scales = ws + L.wt_s;
+        g.sf_tiled = 1;
+        g.sf_group = (int)L.G;
         g.q_out = a.dx;
         g.status = a.status;
         st = launch_fwd(g, stream);
         if (st != MLA_OK) return st;
     }
     if (want_dw) {
-        // 4. x [T, K] -> xt [K, Tp], blocks along T; 5. dW = qb . xt^T (reduction over T)
-        uint8_t* xt_s = ws + L.xt_s;
-        st = launch_mxfp8_quantize_cols_ld(T, K, MLA_IN_BF16, a.x, K, ws + L.xt, L.Tp, xt_s, L.Tp / 32, stream);
+        // 4. x [T, K] -> xt [K, Tp], blocks along T; 5. dW = qb . xt^T (reduction over T; the
+        //    operands' extent is T, so the tensor maps read zeros past it)
+        st = launch_mxfp8_quantize_cols_tiled_sf(T, K, MLA_IN_BF16, a.x, K, ws + L.xt, L.Tp, ws + L.xt_s, L.G,
+                                                 stream);
         if (st != MLA_OK) return st;
-        const int64_t nbt = (T + 31) / 32;
-        if (L.Tp / 32 > nbt &&
-            cudaMemset2DAsync(xt_s + nbt, (size_t)(L.Tp / 32), 0, (size_t)(L.Tp / 32 - nbt), (size_t)K, stream) !=
-                cudaSuccess)
-            return MLA_ERR_CUDA;
         FwdArgs g{};
         g.T = N;
         g.K = T;
@@ -295,21 +423,22 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
         g.Dr = 0;
         g.weight_mode = MLA_WEIGHT_MXFP8;
         g.out_mode = MLA_OUT_BF16;
-        g.x = qb;
+        g.x = ws + L.qb;
         g.x_scales = ws + L.qb_s;
         g.W = ws + L.xt;
-        g.w_scales = xt_s;
+        g.w_scales = ws + L.xt_s;
         g.ld_x = L.Tp;
         g.ld_w = L.Tp;
-        g.ld_scale = L.Tp / 32;
+        g.sf_tiled = 1;
+        g.sf_group = (int)L.G;
         g.q_out = a.dW;
         g.status = a.status;
         st = launch_fwd(g, stream);
         if (st != MLA_OK) return st;
     }
     if (want_db) {
-        db_reduce_kernel<<<grid_for(N, 256, cap), 256, 0, stream>>>(dbp, (T + 31) / 32, N,
-                                                                   static_cast<uint16_t*>(a.db));
+        db_reduce_kernel<<<grid_for(N, 256, cap), 256, 0, stream>>>(reinterpret_cast<float*>(ws + L.dbp),
+                                                                   (T + 31) / 32, N, static_cast<uint16_t*>(a.db));
         if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     }
     return MLA_OK;

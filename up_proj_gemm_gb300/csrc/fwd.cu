@@ -58,6 +58,9 @@ struct FwdParams {
     int cs_vec;           // cos/sin rows 16-byte aligned: float4 loads
     int nslots;           // staging slots per epilogue warp
     int scales_bhsd;      // MXFP8 scales head-major [H, T, NB] (else [T, H, NB])
+    int sf_tiled;         // MXFP8 scales pre-tiled (sf_tiled_offset order): one 512-byte bulk
+                          // copy per 128-row chunk and K step instead of the per-row gather
+    int sf_nsub;          // 128-row chunks of a B tile: ceil(BN / 128)
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
                           // write each row's scale bytes as one 4-byte word (else: units
                           // alternate between them and scales go byte by byte)
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
-            mbar_init(sm.full(s), MXW ? 1 + 32 : 1);
+            mbar_init(sm.full(s), (MXW && !p.sf_tiled) ? 1 + 32 : 1);
             mbar_init(sm.empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -334,8 +337,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int kc = kt * (MXW ? 128 : 64);
                     tma_load_2d(sm.a(s, p), &tmA, kc, mt * kBM, sm.full(s));
                     tma_load_2d(sm.b(s, p), &tmB, kc, nt * p.BN, sm.full(s));
+                    if (MXW && p.sf_tiled) {
+                        bulk_load(sm.sfa(s), p.x_scales + ((int64_t)mt * p.k_tiles + kt) * 512, 512u, sm.full(s));
+                        for (int c = 0; c < p.sf_nsub; ++c)
+                            bulk_load(sm.sfb(s) + 512u * c,
+                                      p.w_scales + (((int64_t)nt * p.sf_nsub + c) * p.k_tiles + kt) * 512, 512u,
+                                      sm.full(s));
+                    }
                 }
-                if (MXW) {
+                if (MXW && !p.sf_tiled) {
                     // scale bytes [4 kt, 4 kt + 4) of each row; row r of a 128-row
                     // chunk goes to byte (r % 32) * 16 + (r / 32) * 4.
 #pragma unroll
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
                     if (MXW) {
-                        fence_proxy_async_smem();  // scale bytes arrived through the generic proxy
+                        if (!p.sf_tiled) fence_proxy_async_smem();  // gathered bytes came through the generic proxy
                         const uint32_t sfa_col = tmem_base + kSfCol0 + kSfColsPerStage * s;
                         const uint32_t sfb_col = sfa_col + 4;
                         tmem_cp_32x128b_warpx4(sfa_col, smem_desc(sm.sfa(s), 0, 128, kLayoutNone));
@@ -748,7 +758,10 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.k_tiles = (int)((a.K + bk - 1) / bk);
     p.a_bytes = kBM * 128;
     p.stage_bytes = p.a_bytes + (uint32_t)BN * 128;
-    p.tx_bytes = p.stage_bytes;
+    p.sf_tiled = a.sf_tiled;
+    p.sf_nsub = (BN + 127) / 128;
+    if (a.sf_tiled && (!mxw || BN != a.sf_group)) return MLA_ERR_UNSUPPORTED;
+    p.tx_bytes = p.stage_bytes + (a.sf_tiled ? 512u * (1u + (uint32_t)p.sf_nsub) : 0u);
     p.idesc = mxw ? idesc_mxf8(kBM, BN, 0) : idesc_bf16(kBM, BN, 0, 0);
     p.ksb = (int)(a.ld_scale ? a.ld_scale : a.K / 32);
     p.bias = static_cast<const uint16_t*>(a.bias);

@@ -51,6 +51,14 @@ int launch_mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void* i
 int launch_mxfp8_quantize_cols_ld(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                                   uint8_t* codes_t, int64_t ld_codes, uint8_t* scales_t, int64_t ld_scales,
                                   cudaStream_t stream);
+// The same with the scales in the GEMM's tiled order (sf_tiled_offset with
+// rows = C, cols = ceil(R/32), groups of sf_group rows; every byte of the
+// ceil(R/128) K steps written, 0 past R). Needs the 16-byte fast path (in
+// 16-byte aligned, ld_in and C multiples of the 16-byte vector), else
+// MLA_ERR_UNSUPPORTED.
+int launch_mxfp8_quantize_cols_tiled_sf(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                                        uint8_t* codes_t, int64_t ld_codes, uint8_t* scales_t, int64_t sf_group,
+                                        cudaStream_t stream);
 int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                           uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 
@@ -76,6 +84,11 @@ struct FwdArgs {
     // the operand rows may then be longer than K (reads past K are zero codes
     // from the tensor map; their scale bytes must be finite).
     int64_t ld_x = 0, ld_w = 0, ld_scale = 0;
+    // MXFP8 scales already in the GEMM's tiled order (sf_tiled_offset): x's
+    // with G = 128 over ceil(T/128) chunks, W's with G = sf_group, which must
+    // equal the tile width the kernel picks for this shape (else
+    // MLA_ERR_UNSUPPORTED); ld_scale is then unused.
+    int sf_tiled = 0, sf_group = 0;
 };
 int launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
@@ -124,6 +137,7 @@ int launch_wgrad(const BwdArgs& a, cudaStream_t stream);
 // MXFP8 backward (see mla_q_uproj_bwd_mxfp8): workspace carve-up and launch.
 struct Mxfp8BwdLayout {
     int64_t Tp;  // tokens rounded up to 128 (row pitch of the token-blocked operands)
+    int64_t G;   // GEMM tile width over K (the rows of each B operand's scale group)
     size_t qa, qa_s, qb, qb_s, wt, wt_s, xt, xt_s, dbp, total;
 };
 int bwd_mxfp8_layout(int64_t T, int64_t K, int64_t N, Mxfp8BwdLayout* out);

@@ -98,4 +98,42 @@ __device__ __forceinline__ uint32_t quantize_block_regs(const float (&v)[NV], in
     return (uint32_t)(e + 127);
 }
 
+// Quantize 8 values of a 32-element block whose other 24 elements are held by
+// three other lanes; mbits is the block's amax magnitude bits already reduced
+// over all 32 (the same rule as quantize_block_regs). Returns the scale byte.
+__device__ __forceinline__ uint32_t quantize8_block_scale(const float (&v)[8], uint32_t mbits,
+                                                          uint32_t (&codes)[2]) {
+    if (mbits >= 0x7F800000u) {
+#pragma unroll
+        for (int w = 0; w < 2; ++w)
+            codes[w] = nan_code(v[4 * w]) | (nan_code(v[4 * w + 1]) << 8) | (nan_code(v[4 * w + 2]) << 16) |
+                       (nan_code(v[4 * w + 3]) << 24);
+        return 0xFFu;
+    }
+    const int e = e8m0_exponent_f32(__uint_as_float(mbits));
+    const float s = exp2_neg(e);
+#pragma unroll
+    for (int w = 0; w < 2; ++w)
+        codes[w] = pack_e4m3x4(v[4 * w] * s, v[4 * w + 1] * s, v[4 * w + 2] * s, v[4 * w + 3] * s);
+    return (uint32_t)(e + 127);
+}
+
+// E8M0 scales in the order the block-scaled GEMM loads them: rows of one
+// operand (its M or N axis) in groups of G rows (the GEMM's tile height along
+// that axis); a group is padded to whole 128-row chunks and each chunk stored
+// as tiles of 128 rows x 4 scale columns (one 128-element K step), 512 bytes,
+// in the layout tcgen05.cp replicates into TMEM: row rr of the chunk, column
+// c at (rr % 32) * 16 + (rr / 32) * 4 + (c % 4). Chunk i of group g, K step
+// kt is tile ((g * ceil(G/128) + i) * nkt + kt), nkt = ceil(cols / 4). With
+// G = 128 this is the GEMM scale swizzle of the whole [rows, cols] matrix.
+__host__ __device__ __forceinline__ int64_t sf_tiled_offset(int64_t r, int64_t c, int64_t G, int64_t nkt) {
+    const int64_t nsub = (G + 127) / 128;
+    const int64_t g = r / G, rg = r - g * G;
+    const int64_t i = rg / 128, rr = rg - i * 128;
+    return ((g * nsub + i) * nkt + c / 4) * 512 + (rr % 32) * 16 + (rr / 32) * 4 + (c % 4);
+}
+__host__ __device__ __forceinline__ int64_t sf_tiled_bytes(int64_t rows, int64_t cols, int64_t G) {
+    return (rows + G - 1) / G * ((G + 127) / 128) * ((cols + 3) / 4) * 512;
+}
+
 }  // namespace mlaq

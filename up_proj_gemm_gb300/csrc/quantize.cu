@@ -292,7 +292,8 @@ template <typename Tin, bool VEC>
 __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const Tin* __restrict__ in, int64_t R,
                                                                      int64_t C, int64_t ld,
                                                                      uint8_t* __restrict__ codes, int64_t ldc,
-                                                                     uint8_t* __restrict__ scales, int64_t nbr) {
+                                                                     uint8_t* __restrict__ scales, int64_t nbr,
+                                                                     int64_t sf_group) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int NBUF = cols_nbuf<Tin>();
     constexpr uint32_t BUF = cols_buf_bytes<Tin>();
@@ -304,9 +305,10 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
     const int t = threadIdx.x;
     const int64_t tiles_r = (R + kColTileR - 1) / kColTileR;
     const int64_t tiles = tiles_r * ((C + kColTC - 1) / kColTC);
-    // a row's scale pitch holds whole 4-byte words for every tile (bytes of blocks past R are 0)
-    const bool word_scales = (nbr % 4) == 0 && nbr >= 4 * ((R + kColTileR - 1) / kColTileR) &&
-                             (reinterpret_cast<uintptr_t>(scales) % 4) == 0;
+    // a row's scale pitch holds whole 4-byte words for every tile (bytes of blocks past R are 0);
+    // always so in the GEMM's tiled order (sf_group > 0), where a tile's 4 bytes are one word
+    const bool word_scales = sf_group > 0 || ((nbr % 4) == 0 && nbr >= 4 * tiles_r &&
+                                              (reinterpret_cast<uintptr_t>(scales) % 4) == 0);
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int64_t tr = tile % tiles_r, tc = tile / tiles_r;
         const int64_t c0 = tc * kColTC;
@@ -361,7 +363,8 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
             __syncthreads();  // the buffer may be refilled now
         }
         if (word_scales && c < C && tr * kColTileR < R)
-            *reinterpret_cast<uint32_t*>(scales + c * nbr + tr * NB) = sword;
+            *reinterpret_cast<uint32_t*>(scales + (sf_group > 0 ? sf_tiled_offset(c, tr * NB, sf_group, tiles_r)
+                                                                : c * nbr + tr * NB)) = sword;
     }
 }
 
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(256) mxfp8_swizzle_kernel(const uint8_t* __res
 
 template <typename Tin>
 int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t* codes, int64_t ldc,
-                      uint8_t* scales, int64_t lds, cudaStream_t stream) {
+                      uint8_t* scales, int64_t lds, cudaStream_t stream, int64_t sf_group = 0) {
     DeviceInfo di;
     int st = current_device_info(&di);
     if (st != MLA_OK) return st;
@@ -418,11 +421,12 @@ int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t*
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return MLA_ERR_CUDA;
         if (vec)
-            mxfp8_quantize_cols_tiled<Tin, true><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds);
+            mxfp8_quantize_cols_tiled<Tin, true><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
         else
-            mxfp8_quantize_cols_tiled<Tin, false><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds);
+            mxfp8_quantize_cols_tiled<Tin, false><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
         return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
     }
+    if (sf_group > 0) return MLA_ERR_UNSUPPORTED;  // the tiled scale order needs the fast path
     const int64_t tiles = ((R + kColTileR - 1) / kColTileR) * ((C + kColTileC - 1) / kColTileC);
     int64_t blocks = tiles;
     const int64_t cap = (int64_t)di.num_sms * (2048 / kColThreads);
@@ -450,6 +454,15 @@ namespace mlaq {
 int launch_mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                                uint8_t* codes_t, uint8_t* scales_t, cudaStream_t stream) {
     return launch_mxfp8_quantize_cols_ld(R, C, in_dtype, in, ld_in, codes_t, R, scales_t, (R + 31) / 32, stream);
+}
+
+int launch_mxfp8_quantize_cols_tiled_sf(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                                        uint8_t* codes_t, int64_t ld_codes, uint8_t* scales_t, int64_t sf_group,
+                                        cudaStream_t stream) {
+    if (sf_group <= 0) return MLA_ERR_INVALID_ARG;
+    if (in_dtype == MLA_IN_F32)
+        return launch_cols_typed<float>(R, C, in, ld_in, codes_t, ld_codes, scales_t, 0, stream, sf_group);
+    return launch_cols_typed<__nv_bfloat16>(R, C, in, ld_in, codes_t, ld_codes, scales_t, 0, stream, sf_group);
 }
 
 int launch_mxfp8_quantize_cols_ld(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
