@@ -100,12 +100,21 @@ __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a
     const int q0 = c - a.Dn;     // rope index of the lane's first channel
     const bool first = q0 < HH;  // holds i (else i + Dr/2) of its pairs
     const int64_t nkt_n = N / 128;
-#pragma unroll 1
+    // all four rows' loads (and rope positions) in flight before any of them is used
+    uint4 raws[4];
+    int64_t pps[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int64_t t = t0 + warp + 8 * it;
+        raws[it] = make_uint4(0, 0, 0, 0);
+        if (t < a.T) raws[it] = __ldg(reinterpret_cast<const uint4*>(a.dq + t * N + n));
+        pps[it] = (rope && t < a.T) ? (a.pos ? (int64_t)__ldg(a.pos + t) : t) : 0;
+    }
+#pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int r = warp + 8 * it;
         const int64_t t = t0 + r;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (t < a.T) raw = __ldg(reinterpret_cast<const uint4*>(a.dq + t * N + n));
+        const uint4 raw = raws[it];
         float v[8];
         unpack8(raw, v);
         // the partner half of every rope pair (all lanes take part in the shuffle)
@@ -115,7 +124,7 @@ __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a
         pr.z = __shfl_xor_sync(0xffffffffu, raw.z, PX);
         pr.w = __shfl_xor_sync(0xffffffffu, raw.w, PX);
         if (rope && t < a.T) {
-            const int64_t pp = a.pos ? (int64_t)__ldg(a.pos + t) : t;
+            const int64_t pp = pps[it];
             if (pp < 0 || pp >= a.cs_rows) {
                 record_status(a.status, MLA_ERR_POS_RANGE);
             } else {
@@ -130,14 +139,14 @@ __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a
                                  : __fsub_rn(__fmul_rn(v[k], cw[k]), __fmul_rn(o[k], sw[k]));
             }
         }
-        // rowwise block of 32 channels = this lane quad
-        uint32_t mb = 0;
+        // rowwise block of 32 channels = this lane quad (NaN-propagating amax)
+        float am = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mb = max(mb, __float_as_uint(v[k]) & 0x7FFFFFFFu);
-        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        for (int k = 0; k < 8; ++k) am = amax_nan(am, v[k]);
+        am = amax_nan(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = amax_nan(am, __shfl_xor_sync(0xffffffffu, am, 2));
         uint32_t w[2];
-        const uint32_t sb = quantize8_block_scale(v, mb, w);
+        const uint32_t sb = quantize8_block_scale(v, __float_as_uint(am), w);
         if (a.qa) {
             if (t < a.T) *reinterpret_cast<uint2*>(a.qa + t * N + n) = make_uint2(w[0], w[1]);
             // the scale bytes of 4 consecutive blocks are one word of the tiled order
@@ -162,10 +171,9 @@ __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a
         sum += v[r];  // token order; rows past T are 0
     }
     if (a.qb) {
-        const int64_t left = a.T - t0;
-        const int nv = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
+        // rows past T hold zeros: they leave the amax unchanged and encode as 0
         uint32_t w[8];
-        const uint32_t sb = quantize_block_regs<32>(v, nv, w);
+        const uint32_t sb = quantize_block32(v, w);
         uint8_t* dst = a.qb + ch * a.Tp + t0;
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -404,6 +412,7 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
         g.w_scales = ws + L.wt_s;
         g.sf_tiled = 1;
         g.sf_group = (int)L.G;
+        g.n_fastest = 1;  // the row-tile of qa (the large operand) is read once
         g.q_out = a.dx;
         g.status = a.status;
         st = launch_fwd(g, stream);
@@ -431,6 +440,7 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
         g.ld_w = L.Tp;
         g.sf_tiled = 1;
         g.sf_group = (int)L.G;
+        g.n_fastest = 1;  // qb (the large operand) read once; xt stays in L2
         g.q_out = a.dW;
         g.status = a.status;
         st = launch_fwd(g, stream);

@@ -61,6 +61,9 @@ struct FwdParams {
     int sf_tiled;         // MXFP8 scales pre-tiled (sf_tiled_offset order): one 512-byte bulk
                           // copy per 128-row chunk and K step instead of the per-row gather
     int sf_nsub;          // 128-row chunks of a B tile: ceil(BN / 128)
+    int n_fastest;        // tile order with the channel tile fastest (CTAs running together
+                          // share the x row-tile; for GEMMs whose x operand is the large one)
+    int num_n_tiles;
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
                           // write each row's scale bytes as one 4-byte word (else: units
                           // alternate between them and scales go byte by byte)
@@ -268,6 +271,11 @@ template <bool KV>
 __device__ __forceinline__ int tile_next(int tile) {
     return KV ? tile + 1 : tile + (int)gridDim.x;
 }
+// (token tile, channel tile) of query-side tile index g
+__device__ __forceinline__ void q_tile(const FwdParams& p, int g, int& mt, int& nt) {
+    mt = p.n_fastest ? g / p.num_n_tiles : g % p.num_m_tiles;
+    nt = p.n_fastest ? g % p.num_n_tiles : g / p.num_m_tiles;
+}
 
 // ------------------------------------------------------------------- kernel
 template <bool MXW, bool MXOUT, int DR, bool KV = false>
@@ -324,8 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t issued_mask = 0, issued_par = 0;
         bool ok = true;
         for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile)) {
-            const int mt = KV ? tile / p.H : tile % p.num_m_tiles;
-            const int nt = KV ? tile % p.H : tile / p.num_m_tiles;
+            int mt, nt;
+            if (KV) {
+                mt = tile / p.H;
+                nt = tile % p.H;
+            } else {
+                q_tile(p, tile, mt, nt);
+            }
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                     ok = false;
@@ -575,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t use = (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
             tc_fence_after();
-            const int mt = tile % p.num_m_tiles;
-            const int nt = tile / p.num_m_tiles;
+            int mt, nt;
+            q_tile(p, tile, mt, nt);
             const int64_t t = (int64_t)mt * kBM + row;
             const bool valid = t < p.T;
             int prow = 0;
@@ -753,7 +766,9 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.Dn = a.Dn;
     p.BN = BN;
     p.num_m_tiles = (int)((a.T + kBM - 1) / kBM);
-    p.num_tiles = p.num_m_tiles * (int)(N / BN);
+    p.num_n_tiles = (int)(N / BN);
+    p.num_tiles = p.num_m_tiles * p.num_n_tiles;
+    p.n_fastest = a.n_fastest;
     const int bk = mxw ? 128 : 64;  // K elements per 128-byte row
     p.k_tiles = (int)((a.K + bk - 1) / bk);
     p.a_bytes = kBM * 128;

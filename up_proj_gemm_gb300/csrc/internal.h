@@ -89,6 +89,10 @@ struct FwdArgs {
     // equal the tile width the kernel picks for this shape (else
     // MLA_ERR_UNSUPPORTED); ld_scale is then unused.
     int sf_tiled = 0, sf_group = 0;
+    // Tile order with the output-channel tile fastest (else the token tile):
+    // the CTAs running together then share the x row-tile, for GEMMs whose x
+    // operand is the large one.
+    int n_fastest = 0;
 };
 int launch_fwd(const FwdArgs& a, cudaStream_t stream);
 

@@ -98,6 +98,37 @@ __device__ __forceinline__ uint32_t quantize_block_regs(const float (&v)[NV], in
     return (uint32_t)(e + 127);
 }
 
+// max(m, |v|) that returns NaN when either input is NaN (so a block amax taken
+// with it is NaN or Inf exactly when the block holds a non-finite element;
+// for finite inputs it equals the largest magnitude).
+__device__ __forceinline__ float amax_nan(float m, float v) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(v)));
+    return r;
+}
+
+// A whole 32-element block held by one thread: the rule of
+// quantize_block_regs, with the amax by amax_nan.
+__device__ __forceinline__ uint32_t quantize_block32(const float (&v)[32], uint32_t (&codes)[8]) {
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = amax_nan(am, v[i]);
+    const uint32_t mbits = __float_as_uint(am);
+    if (mbits >= 0x7F800000u) {
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            codes[w] = nan_code(v[4 * w]) | (nan_code(v[4 * w + 1]) << 8) | (nan_code(v[4 * w + 2]) << 16) |
+                       (nan_code(v[4 * w + 3]) << 24);
+        return 0xFFu;
+    }
+    const int e = e8m0_exponent_f32(am);
+    const float s = exp2_neg(e);
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+        codes[w] = pack_e4m3x4(v[4 * w] * s, v[4 * w + 1] * s, v[4 * w + 2] * s, v[4 * w + 3] * s);
+    return (uint32_t)(e + 127);
+}
+
 // Quantize 8 values of a 32-element block whose other 24 elements are held by
 // three other lanes; mbits is the block's amax magnitude bits already reduced
 // over all 32 (the same rule as quantize_block_regs). Returns the scale byte.
