@@ -128,15 +128,16 @@ __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a
             if (pp < 0 || pp >= a.cs_rows) {
                 record_status(a.status, MLA_ERR_POS_RANGE);
             } else {
-                // out_i = fl(fl(g_i c_i) + fl(g_{i+h} s_{i+h})), out_{i+h} = fl(fl(g_{i+h} c_{i+h}) - fl(g_i s_i))
+                // out_i = fl(fl(g_i c_i) + fl(g_{i+h} s_{i+h})), out_{i+h} = fl(fl(g_{i+h} c_{i+h}) - fl(g_i s_i));
+                // the second half adds fl(g_i * -s_i) = -fl(g_i s_i) (negation is exact), one formula
                 float o[8], cw[8], sw[8];
                 unpack8(pr, o);
                 load8_f32(a.cos_tab + pp * a.cs_width + q0, a.cs_vec != 0, cw);
                 load8_f32(a.sin_tab + pp * a.cs_width + (first ? q0 + HH : q0 - HH), a.cs_vec != 0, sw);
+                const uint32_t neg = first ? 0u : 0x80000000u;
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    v[k] = first ? __fadd_rn(__fmul_rn(v[k], cw[k]), __fmul_rn(o[k], sw[k]))
-                                 : __fsub_rn(__fmul_rn(v[k], cw[k]), __fmul_rn(o[k], sw[k]));
+                    v[k] = __fadd_rn(__fmul_rn(v[k], cw[k]), __fmul_rn(o[k], __uint_as_float(__float_as_uint(sw[k]) ^ neg)));
             }
         }
         // rowwise block of 32 channels = this lane quad (NaN-propagating amax)
@@ -412,7 +413,6 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
         g.w_scales = ws + L.wt_s;
         g.sf_tiled = 1;
         g.sf_group = (int)L.G;
-        g.n_fastest = 1;  // the row-tile of qa (the large operand) is read once
         g.q_out = a.dx;
         g.status = a.status;
         st = launch_fwd(g, stream);
@@ -440,7 +440,6 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
         g.ld_w = L.Tp;
         g.sf_tiled = 1;
         g.sf_group = (int)L.G;
-        g.n_fastest = 1;  // qb (the large operand) read once; xt stays in L2
         g.q_out = a.dW;
         g.status = a.status;
         st = launch_fwd(g, stream);

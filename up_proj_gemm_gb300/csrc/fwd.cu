@@ -61,8 +61,6 @@ struct FwdParams {
     int sf_tiled;         // MXFP8 scales pre-tiled (sf_tiled_offset order): one 512-byte bulk
                           // copy per 128-row chunk and K step instead of the per-row gather
     int sf_nsub;          // 128-row chunks of a B tile: ceil(BN / 128)
-    int n_fastest;        // tile order with the channel tile fastest (CTAs running together
-                          // share the x row-tile; for GEMMs whose x operand is the large one)
     int num_n_tiles;
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
                           // write each row's scale bytes as one 4-byte word (else: units
@@ -271,10 +269,19 @@ template <bool KV>
 __device__ __forceinline__ int tile_next(int tile) {
     return KV ? tile + 1 : tile + (int)gridDim.x;
 }
-// (token tile, channel tile) of query-side tile index g
+// (token tile, channel tile) of query-side tile index g. The rope forward
+// runs the token tile fastest (CTAs running together share W tiles); the
+// plain GEMM (DR = 0) the channel tile, so they share the x row-tile (there x
+// is the large, streamed operand).
+template <int DR>
 __device__ __forceinline__ void q_tile(const FwdParams& p, int g, int& mt, int& nt) {
-    mt = p.n_fastest ? g / p.num_n_tiles : g % p.num_m_tiles;
-    nt = p.n_fastest ? g % p.num_n_tiles : g / p.num_m_tiles;
+    if (DR == 0) {
+        mt = g / p.num_n_tiles;
+        nt = g % p.num_n_tiles;
+    } else {
+        mt = g % p.num_m_tiles;
+        nt = g / p.num_m_tiles;
+    }
 }
 
 // ------------------------------------------------------------------- kernel
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mt = tile / p.H;
                 nt = tile % p.H;
             } else {
-                q_tile(p, tile, mt, nt);
+                q_tile<DR>(p, tile, mt, nt);
             }
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (KV) {
+    } else if constexpr (KV) {
         // ------------------------------------------------- KV-side epilogue
         // CTAs take contiguous runs of tiles, head fastest, so consecutive
         // tiles share their 128 tokens. A tile = 128 tokens x one head's
@@ -589,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
             tc_fence_after();
             int mt, nt;
-            q_tile(p, tile, mt, nt);
+            q_tile<DR>(p, tile, mt, nt);
             const int64_t t = (int64_t)mt * kBM + row;
             const bool valid = t < p.T;
             int prow = 0;
@@ -613,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool nope = c < p.Dn;
                 if (p.split_half || (unit++ & 1) == half) {
                     if (nope) nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
-                    else rope_unit<MXOUT, DR>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
+                    else if constexpr (DR > 0) rope_unit<MXOUT, DR>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
                 }
                 col += nope ? 32 : DR;
             }
@@ -768,7 +775,6 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.num_m_tiles = (int)((a.T + kBM - 1) / kBM);
     p.num_n_tiles = (int)(N / BN);
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
-    p.n_fastest = a.n_fastest;
     const int bk = mxw ? 128 : 64;  // K elements per 128-byte row
     p.k_tiles = (int)((a.K + bk - 1) / bk);
     p.a_bytes = kBM * 128;
@@ -825,9 +831,9 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     if (st != MLA_OK) return st;
 
     int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
-    if (a.Dr == 0)  // plain GEMM: every unit is a pass-through unit; any DR instantiation serves
-        return mxw ? launch_variant<true, false, 16>(ta, tb, tc, p, grid, smem, stream)
-                   : launch_variant<false, false, 16>(ta, tb, tc, p, grid, smem, stream);
+    if (a.Dr == 0)  // plain GEMM: every unit is a pass-through unit
+        return mxw ? launch_variant<true, false, 0>(ta, tb, tc, p, grid, smem, stream)
+                   : launch_variant<false, false, 0>(ta, tb, tc, p, grid, smem, stream);
     if (mxw)
         return mxo ? launch_dr<true, true>(a.Dr, ta, tb, tc, p, grid, smem, stream)
                    : launch_dr<true, false>(a.Dr, ta, tb, tc, p, grid, smem, stream);

@@ -80,7 +80,8 @@ struct FwdArgs {
     int* status;
     // Row pitches of the MXFP8 operands (codes: bytes, scales: bytes; 0 = dense
     // K and K / 32). With Dr == 0 (H = 1, Dn = the output width) the kernel is
-    // a plain block-scaled GEMM q = x W^T with a bf16 output and no rotation;
+    // a plain block-scaled GEMM q = x W^T with a bf16 output and no rotation,
+    // its tiles walked with the output-channel tile fastest;
     // the operand rows may then be longer than K (reads past K are zero codes
     // from the tensor map; their scale bytes must be finite).
     int64_t ld_x = 0, ld_w = 0, ld_scale = 0;
@@ -89,10 +90,6 @@ struct FwdArgs {
     // equal the tile width the kernel picks for this shape (else
     // MLA_ERR_UNSUPPORTED); ld_scale is then unused.
     int sf_tiled = 0, sf_group = 0;
-    // Tile order with the output-channel tile fastest (else the token tile):
-    // the CTAs running together then share the x row-tile, for GEMMs whose x
-    // operand is the large one.
-    int n_fastest = 0;
 };
 int launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
