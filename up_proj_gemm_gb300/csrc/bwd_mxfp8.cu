@@ -74,70 +74,82 @@ struct RqArgs {
     int* status;
 };
 
-// Fast path: a CTA takes 32 tokens x 256 channels of dq viewed as [T, N]
-// (N % 256 == 0, and no rope region crosses a 256-channel span: Dr == 32, or
-// Dn % 64 == 0). Warp w takes token rows w, w + 8, w + 16, w + 24; lane l
-// holds channels [8l, 8l + 8) of the span (one 16-byte load). A 32-channel
-// block is a lane quad (amax by two shuffles); a rope pair's partner channels
-// sit Dr/16 lanes away (one shuffle exchange). The float32 rows then go to a
-// shared tile whose columns thread c reads for the token-blocked copy and the
-// db partial of channel c.
+// Fast path: a CTA takes 128 tokens x 64 channels of dq viewed as [T, N]
+// (N % 64 == 0; a 64-channel span is all rope or all pass-through when
+// Dn % 64 == 0 and Dr == 64, and holds a whole rope half-pair set when
+// Dr == 32). Tiles go channel span fastest.
+//  * rows: 8 lanes per token row (16 bytes = 8 channels each), 4 rows per
+//    warp at a time, 4 passes for the CTA's 128 rows, all loads issued
+//    first. A 32-channel block is a lane quad (amax by two shuffles); a rope
+//    pair's partner channels sit Dr/16 lanes away in the same row (one
+//    shuffle exchange); the rope arithmetic runs only in rope spans.
+//  * the rotated float32 rows go to a shared tile [128][64]; then warp w
+//    takes token block w / 2 (32 tokens) and channels 32 (w % 2) + lane:
+//    it quantizes that channel's block, stores 32 codes (the CTA writes each
+//    channel's 128 tokens, one whole 128-byte line of qb) and the block's
+//    float32 sum for db.
 template <int DR>
 __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a) {
-    __shared__ __align__(16) float tile[32][256];
+    __shared__ __align__(16) float tile[128][64];
     constexpr int HH = DR / 2;
     constexpr int PX = HH / 8;  // lanes between the two channels of a rope pair
     const int D = a.Dn + DR;
-    const int64_t N = (int64_t)a.H * D;
-    const int64_t ntb = a.Tp / 32;
-    const int64_t tb = blockIdx.x % ntb;
-    const int64_t n0 = (int64_t)(blockIdx.x / ntb) * 256;
-    const int64_t t0 = tb * 32;
+    const int N = a.H * D;
+    const int nsp = N / 64;     // channel spans
+    const int ts = (int)(blockIdx.x / nsp), sp = (int)(blockIdx.x % nsp);
+    const int64_t t0 = (int64_t)ts * 128;
+    const int n0 = sp * 64;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n = n0 + 8 * lane;
-    const int c = (int)(n % D);  // channel within the head
-    const bool rope = c >= a.Dn;
-    const int q0 = c - a.Dn;     // rope index of the lane's first channel
-    const bool first = q0 < HH;  // holds i (else i + Dr/2) of its pairs
-    const int64_t nkt_n = N / 128;
-    // all four rows' loads (and rope positions) in flight before any of them is used
+    const int g = lane >> 3, j = lane & 7;  // row within the warp's 4, 16-byte chunk of the row
+    const int n = n0 + 8 * j;
+    const int c = n % D;          // channel within the head
+    const bool rope = c >= a.Dn;  // (a whole span when Dr == 64)
+    const int q0 = c - a.Dn;      // rope index of the lane's first channel
+    const bool first = q0 < HH;   // holds i (else i + Dr/2) of its pairs
+    const int nkt_n = N / 128;
     uint4 raws[4];
-    int64_t pps[4];
+    int pps[4];
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
-        const int64_t t = t0 + warp + 8 * it;
+        const int64_t t = t0 + it * 32 + warp * 4 + g;
         raws[it] = make_uint4(0, 0, 0, 0);
-        if (t < a.T) raws[it] = __ldg(reinterpret_cast<const uint4*>(a.dq + t * N + n));
-        pps[it] = (rope && t < a.T) ? (a.pos ? (int64_t)__ldg(a.pos + t) : t) : 0;
+        pps[it] = 0;
+        if (t < a.T) {
+            raws[it] = __ldg(reinterpret_cast<const uint4*>(a.dq + t * N + n));
+            if (rope) pps[it] = a.pos ? __ldg(a.pos + t) : (int)t;
+        }
     }
+    const bool rope_span = __any_sync(0xffffffffu, rope);  // warp-uniform
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
-        const int r = warp + 8 * it;
+        const int r = it * 32 + warp * 4 + g;
         const int64_t t = t0 + r;
-        const uint4 raw = raws[it];
         float v[8];
-        unpack8(raw, v);
-        // the partner half of every rope pair (all lanes take part in the shuffle)
-        uint4 pr;
-        pr.x = __shfl_xor_sync(0xffffffffu, raw.x, PX);
-        pr.y = __shfl_xor_sync(0xffffffffu, raw.y, PX);
-        pr.z = __shfl_xor_sync(0xffffffffu, raw.z, PX);
-        pr.w = __shfl_xor_sync(0xffffffffu, raw.w, PX);
-        if (rope && t < a.T) {
-            const int64_t pp = pps[it];
-            if (pp < 0 || pp >= a.cs_rows) {
-                record_status(a.status, MLA_ERR_POS_RANGE);
-            } else {
-                // out_i = fl(fl(g_i c_i) + fl(g_{i+h} s_{i+h})), out_{i+h} = fl(fl(g_{i+h} c_{i+h}) - fl(g_i s_i));
-                // the second half adds fl(g_i * -s_i) = -fl(g_i s_i) (negation is exact), one formula
-                float o[8], cw[8], sw[8];
-                unpack8(pr, o);
-                load8_f32(a.cos_tab + pp * a.cs_width + q0, a.cs_vec != 0, cw);
-                load8_f32(a.sin_tab + pp * a.cs_width + (first ? q0 + HH : q0 - HH), a.cs_vec != 0, sw);
-                const uint32_t neg = first ? 0u : 0x80000000u;
+        unpack8(raws[it], v);
+        if (rope_span) {
+            uint4 pr;
+            pr.x = __shfl_xor_sync(0xffffffffu, raws[it].x, PX);
+            pr.y = __shfl_xor_sync(0xffffffffu, raws[it].y, PX);
+            pr.z = __shfl_xor_sync(0xffffffffu, raws[it].z, PX);
+            pr.w = __shfl_xor_sync(0xffffffffu, raws[it].w, PX);
+            if (rope && t < a.T) {
+                const int pp = pps[it];
+                if (pp < 0 || pp >= a.cs_rows) {
+                    record_status(a.status, MLA_ERR_POS_RANGE);
+                } else {
+                    // out_i = fl(fl(g_i c_i) + fl(g_{i+h} s_{i+h})), out_{i+h} = fl(fl(g_{i+h} c_{i+h}) - fl(g_i s_i));
+                    // the second half adds fl(g_i * -s_i) = -fl(g_i s_i) (negation is exact), one formula
+                    float o[8], cw[8], sw[8];
+                    unpack8(pr, o);
+                    const int64_t row0 = (int64_t)pp * a.cs_width;
+                    load8_f32(a.cos_tab + row0 + q0, a.cs_vec != 0, cw);
+                    load8_f32(a.sin_tab + row0 + (first ? q0 + HH : q0 - HH), a.cs_vec != 0, sw);
+                    const uint32_t neg = first ? 0u : 0x80000000u;
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    v[k] = __fadd_rn(__fmul_rn(v[k], cw[k]), __fmul_rn(o[k], __uint_as_float(__float_as_uint(sw[k]) ^ neg)));
+                    for (int k = 0; k < 8; ++k)
+                        v[k] = __fadd_rn(__fmul_rn(v[k], cw[k]),
+                                         __fmul_rn(o[k], __uint_as_float(__float_as_uint(sw[k]) ^ neg)));
+                }
             }
         }
         // rowwise block of 32 channels = this lane quad (NaN-propagating amax)
@@ -146,41 +158,49 @@ __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a
         for (int k = 0; k < 8; ++k) am = amax_nan(am, v[k]);
         am = amax_nan(am, __shfl_xor_sync(0xffffffffu, am, 1));
         am = amax_nan(am, __shfl_xor_sync(0xffffffffu, am, 2));
-        uint32_t w[2];
-        const uint32_t sb = quantize8_block_scale(v, __float_as_uint(am), w);
         if (a.qa) {
+            uint32_t w[2];
+            const uint32_t sb = quantize8_block_scale(v, __float_as_uint(am), w);
             if (t < a.T) *reinterpret_cast<uint2*>(a.qa + t * N + n) = make_uint2(w[0], w[1]);
-            // the scale bytes of 4 consecutive blocks are one word of the tiled order
-            const uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 4) << 8) |
-                                  (__shfl_down_sync(0xffffffffu, sb, 8) << 16) |
-                                  (__shfl_down_sync(0xffffffffu, sb, 12) << 24);
-            if ((lane & 15) == 0)
-                *reinterpret_cast<uint32_t*>(a.qa_s + sf_tiled_offset(t, n / 32, 128, nkt_n)) = word;
+            // the row's two scale bytes (blocks n0/32 and n0/32 + 1) are adjacent in the tiled order
+            const uint32_t pair = sb | (__shfl_down_sync(0xffffffffu, sb, 4) << 8);
+            if (j == 0)
+                *reinterpret_cast<uint16_t*>(a.qa_s + sf_tiled_offset(t, n0 / 32, 128, nkt_n)) = (uint16_t)pair;
         }
-        *reinterpret_cast<float4*>(&tile[r][8 * lane]) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(&tile[r][8 * lane + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+        // lanes with bit 2 set store their halves in the other order: no bank conflicts
+        float* dst = &tile[r][8 * j];
+        const float4 lo = make_float4(v[0], v[1], v[2], v[3]), hi = make_float4(v[4], v[5], v[6], v[7]);
+        if (j & 4) {
+            *reinterpret_cast<float4*>(dst + 4) = hi;
+            *reinterpret_cast<float4*>(dst) = lo;
+        } else {
+            *reinterpret_cast<float4*>(dst) = lo;
+            *reinterpret_cast<float4*>(dst + 4) = hi;
+        }
     }
     __syncthreads();
-    // token-blocked copy and db partial of channel n0 + threadIdx.x
-    const int col = threadIdx.x;
+    // token block tb (32 tokens) of channel ch
+    const int blk = warp >> 1;
+    const int col = 32 * (warp & 1) + lane;
     const int64_t ch = n0 + col;
+    const int64_t tb = (int64_t)ts * 4 + blk;
     float v[32];
     float sum = 0.f;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-        v[r] = tile[r][col];
+        v[r] = tile[32 * blk + r][col];
         sum += v[r];  // token order; rows past T are 0
     }
     if (a.qb) {
         // rows past T hold zeros: they leave the amax unchanged and encode as 0
         uint32_t w[8];
         const uint32_t sb = quantize_block32(v, w);
-        uint8_t* dst = a.qb + ch * a.Tp + t0;
+        uint8_t* dst = a.qb + ch * a.Tp + tb * 32;
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
         a.qb_s[sf_tiled_offset(ch, tb, 128, a.Tp / 128)] = (uint8_t)sb;
     }
-    if (a.dbp && t0 < a.T) a.dbp[tb * N + ch] = sum;
+    if (a.dbp && tb * 32 < a.T) a.dbp[tb * N + ch] = sum;
 }
 
 // General shapes: a CTA takes 32 tokens x one head (D % 32 == 0), staged in
@@ -346,10 +366,12 @@ int launch_rope_bwd_quant(const BwdArgs& a, int64_t Tp, uint8_t* qa, uint8_t* qa
     const int D = a.Dn + a.Dr;
     const int64_t N = (int64_t)a.H * D;
     const int64_t ntb = Tp / 32;
-    // the fast path needs whole 256-channel spans and rope pairs inside one span
-    const bool fast = N % 256 == 0 && (a.Dr == 32 || (a.Dr == 64 && a.Dn % 64 == 0));
+    // the fast path needs whole 64-channel spans, each all rope or all pass-through
+    // (or a whole 32-channel rope region), and 32-bit tile indices
+    const bool fast = N % 64 == 0 && (a.Dr == 32 || (a.Dr == 64 && a.Dn % 64 == 0)) &&
+                      (Tp / 128) * (N / 64) <= 0x7fffffffLL;
     if (fast) {
-        const unsigned grid = (unsigned)(ntb * (N / 256));
+        const unsigned grid = (unsigned)((Tp / 128) * (N / 64));
         if (a.Dr == 32) rope_bwd_quant_fast<32><<<grid, kRqThreads, 0, stream>>>(r);
         else rope_bwd_quant_fast<64><<<grid, kRqThreads, 0, stream>>>(r);
         return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
