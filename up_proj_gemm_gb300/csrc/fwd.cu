@@ -43,6 +43,12 @@ constexpr uint32_t kAccStride = 256;  // TMEM column offset of accumulator buffe
 constexpr uint32_t kSfCol0 = 448;     // first TMEM column of the per-stage scale factors
 constexpr uint32_t kSfColsPerStage = 12;  // 4 (A: 128 rows) + 8 (B: up to 256 rows)
 constexpr uint32_t kSfBytesPerStage = 512 + 1024;
+// The plain GEMM (DR = 0) takes 256-row x tiles: two M = 128 MMAs per K chunk
+// into two accumulators (TMEM columns 0 and 256, not double-buffered), 30%
+// fewer operand bytes per FLOP than one 128-row tile. Its stages carry the
+// scales of two 128-row x chunks.
+constexpr uint32_t kSfColsPerStage2 = 16;
+constexpr uint32_t kSfBytesPerStage2 = 1024 + 1024;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, splitting the tile's units
 constexpr int kSlotCh = 16;       // channels per slot (one TMA store box: 16 channels x 32 rows)
 
@@ -62,6 +68,9 @@ struct FwdParams {
                           // copy per 128-row chunk and K step instead of the per-row gather
     int sf_nsub;          // 128-row chunks of a B tile: ceil(BN / 128)
     int num_n_tiles;
+    int bm;               // token rows per tile: 128, or 256 for the plain GEMM
+    uint32_t sf_stage;    // scale staging bytes per stage (MXFP8 weights)
+    uint32_t sf_cols;     // TMEM scale-factor columns per stage
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
                           // write each row's scale bytes as one 4-byte word (else: units
                           // alternate between them and scales go byte by byte)
@@ -91,8 +100,9 @@ struct Smem {
     int S;
     __device__ uint32_t a(int s, const FwdParams& p) const { return base + (uint32_t)s * p.stage_bytes; }
     __device__ uint32_t b(int s, const FwdParams& p) const { return a(s, p) + p.a_bytes; }
-    __device__ uint32_t sfa(int s) const { return sf + (uint32_t)s * kSfBytesPerStage; }
-    __device__ uint32_t sfb(int s) const { return sfa(s) + 512; }
+    uint32_t sf_stage, sfb_off;
+    __device__ uint32_t sfa(int s) const { return sf + (uint32_t)s * sf_stage; }
+    __device__ uint32_t sfb(int s) const { return sfa(s) + sfb_off; }
     __device__ uint32_t full(int s) const { return bars + 8u * s; }
     __device__ uint32_t empty(int s) const { return bars + 8u * (S + s); }
     __device__ uint32_t tfull(int b) const { return bars + 8u * (2 * S + b); }
@@ -291,12 +301,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
+    constexpr bool M2 = DR == 0 && !KV;  // 256-row tiles, two accumulators
+    constexpr int BM = M2 ? 2 * kBM : kBM;
     const uint32_t raw = smem_u32(smem_raw);
     Smem sm;
     sm.S = p.stages;
     sm.base = (raw + 1023u) & ~1023u;
     sm.sf = sm.base + (uint32_t)p.stages * p.stage_bytes;
-    sm.out = sm.sf + (MXW ? (uint32_t)p.stages * kSfBytesPerStage : 0u);
+    sm.sf_stage = p.sf_stage;
+    sm.sfb_off = M2 ? 1024u : 512u;
+    sm.out = sm.sf + (MXW ? (uint32_t)p.stages * p.sf_stage : 0u);
     sm.bars = sm.out + (uint32_t)(kEpiWarps * p.nslots) * p.slot_bytes;
     uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (2 * p.stages + 5);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
@@ -346,19 +360,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 q_tile<DR>(p, tile, mt, nt);
             }
+            const bool a_hi = (int64_t)mt * BM + kBM < p.T;
+            const uint32_t tx = p.tx_bytes - ((M2 && MXW && p.sf_tiled && !a_hi) ? 512u : 0u);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(sm.full(s), p.tx_bytes);
+                    mbar_arrive_expect_tx(sm.full(s), tx);
                     // x / W tiles: inner coordinate is the K element index
                     const int kc = kt * (MXW ? 128 : 64);
-                    tma_load_2d(sm.a(s, p), &tmA, kc, mt * kBM, sm.full(s));
+                    tma_load_2d(sm.a(s, p), &tmA, kc, mt * BM, sm.full(s));
                     tma_load_2d(sm.b(s, p), &tmB, kc, nt * p.BN, sm.full(s));
                     if (MXW && p.sf_tiled) {
-                        bulk_load(sm.sfa(s), p.x_scales + ((int64_t)mt * p.k_tiles + kt) * 512, 512u, sm.full(s));
+                        bulk_load(sm.sfa(s), p.x_scales + ((int64_t)(M2 ? 2 * mt : mt) * p.k_tiles + kt) * 512, 512u,
+                                  sm.full(s));
+                        if (M2 && a_hi)  // the second 128-row chunk, when it holds rows below T
+                            bulk_load(sm.sfa(s) + 512u, p.x_scales + ((int64_t)(2 * mt + 1) * p.k_tiles + kt) * 512,
+                                      512u, sm.full(s));
                         for (int c = 0; c < p.sf_nsub; ++c)
                             bulk_load(sm.sfb(s) + 512u * c,
                                       p.w_scales + (((int64_t)nt * p.sf_nsub + c) * p.k_tiles + kt) * 512, 512u,
@@ -371,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int r = lane + 32 * j;
-                        const int64_t row = (int64_t)mt * kBM + r;
+                        const int64_t row = (int64_t)mt * BM + r;
                         if (row < p.T)
                             cp_async_4(sm.sfa(s) + lane * 16 + j * 4,
                                        p.x_scales + row * p.ksb + kt * 4);
@@ -406,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int local = 0;
             bool ok = true;
             for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile), ++local) {
-                const int b = local & 1;
-                const uint32_t use = (uint32_t)(local >> 1);
+                const int b = M2 ? 0 : (local & 1);
+                const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
                 if (!mbar_wait(sm.tempty(b), (use & 1u) ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -423,23 +443,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
                     if (MXW) {
                         if (!p.sf_tiled) fence_proxy_async_smem();  // gathered bytes came through the generic proxy
-                        const uint32_t sfa_col = tmem_base + kSfCol0 + kSfColsPerStage * s;
-                        const uint32_t sfb_col = sfa_col + 4;
+                        const uint32_t sfa_col = tmem_base + kSfCol0 + p.sf_cols * s;
+                        const uint32_t sfb_col = sfa_col + (M2 ? 8 : 4);
                         tmem_cp_32x128b_warpx4(sfa_col, smem_desc(sm.sfa(s), 0, 128, kLayoutNone));
+                        if (M2) tmem_cp_32x128b_warpx4(sfa_col + 4, smem_desc(sm.sfa(s) + 512, 0, 128, kLayoutNone));
                         for (int c = 0; c < (p.BN + 127) / 128; ++c)
                             tmem_cp_32x128b_warpx4(sfb_col + 4 * c,
                                                    smem_desc(sm.sfb(s) + 512 * c, 0, 128, kLayoutNone));
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const uint32_t id = p.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
-                            mma_mxf8(d_tmem, desc_kmajor_sw128(a0 + 32 * j), desc_kmajor_sw128(b0 + 32 * j),
-                                     id, sfa_col, sfb_col, (kt | j) != 0);
+#pragma unroll
+                            for (int hm = 0; hm < (M2 ? 2 : 1); ++hm)
+                                mma_mxf8(d_tmem + hm * kAccStride, desc_kmajor_sw128(a0 + hm * 16384u + 32 * j),
+                                         desc_kmajor_sw128(b0 + 32 * j), id, sfa_col + 4 * hm, sfb_col, (kt | j) != 0);
                         }
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            mma_bf16(d_tmem, desc_kmajor_sw128(a0 + 32 * j), desc_kmajor_sw128(b0 + 32 * j),
-                                     p.idesc, (kt | j) != 0);
+#pragma unroll
+                            for (int hm = 0; hm < (M2 ? 2 : 1); ++hm)
+                                mma_bf16(d_tmem + hm * kAccStride, desc_kmajor_sw128(a0 + hm * 16384u + 32 * j),
+                                         desc_kmajor_sw128(b0 + 32 * j), p.idesc, (kt | j) != 0);
                     }
                     mma_commit(sm.empty(s));
                     if (++s == p.stages) {
@@ -591,13 +616,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = ew >> 2;   // which of the tile's units this warp takes (alternating)
         int local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
-            const int b = local & 1;
-            const uint32_t use = (uint32_t)(local >> 1);
+            const int b = M2 ? 0 : (local & 1);
+            const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
             tc_fence_after();
             int mt, nt;
             q_tile<DR>(p, tile, mt, nt);
-            const int64_t t = (int64_t)mt * kBM + row;
+            // 256-row tiles: the warps of half 1 take the second accumulator (rows 128..255)
+            const int rbase = M2 ? half * kBM : 0;
+            const int64_t t = (int64_t)mt * BM + rbase + row;
             const bool valid = t < p.T;
             int prow = 0;
             if (valid) {
@@ -605,9 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (pp < 0 || pp >= p.cs_rows) record_status(p.status, MLA_ERR_POS_RANGE);
                 else prow = (int)pp;
             }
-            const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
+            const uint32_t trow =
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(M2 ? half : b) * kAccStride;
             const int64_t n0 = (int64_t)nt * p.BN;
-            ec.t0 = mt * kBM + quad * 32;
+            ec.t0 = mt * BM + rbase + quad * 32;
             ec.bias = p.bias ? p.bias + n0 : nullptr;
             ec.sword = 0;
             ec.sbase = (n0 + (p.split_half ? half * (p.BN / 2) : 0)) / 32;
@@ -618,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int h = (int)(n / p.D);
                 const int c = (int)(n - (int64_t)h * p.D);
                 const bool nope = c < p.Dn;
-                if (p.split_half || (unit++ & 1) == half) {
+                if (M2 || p.split_half || (unit++ & 1) == half) {
                     if (nope) nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
                     else if constexpr (DR > 0) rope_unit<MXOUT, DR>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
                 }
@@ -772,17 +800,22 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.D = D;
     p.Dn = a.Dn;
     p.BN = BN;
-    p.num_m_tiles = (int)((a.T + kBM - 1) / kBM);
+    const int bm = a.Dr == 0 ? 2 * kBM : kBM;  // the plain GEMM's 256-row tiles
+    p.bm = bm;
+    p.num_m_tiles = (int)((a.T + bm - 1) / bm);
     p.num_n_tiles = (int)(N / BN);
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
     const int bk = mxw ? 128 : 64;  // K elements per 128-byte row
     p.k_tiles = (int)((a.K + bk - 1) / bk);
-    p.a_bytes = kBM * 128;
+    p.a_bytes = (uint32_t)bm * 128;
     p.stage_bytes = p.a_bytes + (uint32_t)BN * 128;
+    p.sf_stage = bm == kBM ? kSfBytesPerStage : kSfBytesPerStage2;
+    p.sf_cols = bm == kBM ? kSfColsPerStage : kSfColsPerStage2;
     p.sf_tiled = a.sf_tiled;
     p.sf_nsub = (BN + 127) / 128;
     if (a.sf_tiled && (!mxw || BN != a.sf_group)) return MLA_ERR_UNSUPPORTED;
-    p.tx_bytes = p.stage_bytes + (a.sf_tiled ? 512u * (1u + (uint32_t)p.sf_nsub) : 0u);
+    if (a.Dr == 0 && mxw && !a.sf_tiled) return MLA_ERR_UNSUPPORTED;  // 256-row tiles load tiled scales only
+    p.tx_bytes = p.stage_bytes + (a.sf_tiled ? 512u * ((uint32_t)(bm / kBM) + (uint32_t)p.sf_nsub) : 0u);
     p.idesc = mxw ? idesc_mxf8(kBM, BN, 0) : idesc_bf16(kBM, BN, 0, 0);
     p.ksb = (int)(a.ld_scale ? a.ld_scale : a.K / 32);
     p.bias = static_cast<const uint16_t*>(a.bias);
@@ -808,18 +841,18 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
 
     const size_t fixed = 1024 /* alignment slack */ + 256 /* barriers + slots */ +
                          (size_t)kEpiWarps * p.nslots * p.slot_bytes;
-    const size_t per_stage = p.stage_bytes + (mxw ? kSfBytesPerStage : 0);
+    const size_t per_stage = p.stage_bytes + (mxw ? p.sf_stage : 0);
     int stages = (int)((size_t)(di.max_smem_optin - fixed) / per_stage);
     if (stages > 8) stages = 8;
     if (stages < 2) return MLA_ERR_UNSUPPORTED;
-    if (mxw && kSfCol0 + kSfColsPerStage * (uint32_t)stages > kTmemCols) stages = (kTmemCols - kSfCol0) / kSfColsPerStage;
+    if (mxw && kSfCol0 + p.sf_cols * (uint32_t)stages > kTmemCols) stages = (kTmemCols - kSfCol0) / p.sf_cols;
     p.stages = stages;
     const size_t smem = fixed + (size_t)stages * per_stage;
 
     alignas(64) CUtensorMap ta, tb;
     const uint64_t esz = mxw ? 1 : 2;
     st = make_tmap_2d(&ta, a.x, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)a.T,
-                      (uint64_t)(a.ld_x ? a.ld_x : a.K) * esz, 128 / (uint32_t)esz, kBM, true);
+                      (uint64_t)(a.ld_x ? a.ld_x : a.K) * esz, 128 / (uint32_t)esz, (uint32_t)bm, true);
     if (st != MLA_OK) return st;
     st = make_tmap_2d(&tb, a.W, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)(a.ld_w ? a.ld_w : a.K) * esz,
                       128 / (uint32_t)esz, (uint32_t)BN, true);
