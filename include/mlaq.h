@@ -154,15 +154,23 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_
  *   bf16: exactly the values the tensor cores consume. Pass it on to
  *   mla_q_uproj_bwd_wgrad, which then skips its own rotation. Rows whose
  *   position is out of range are left unwritten (dev_status reports it).
- *   workspace/ws_bytes: device scratch of at least
- *   mla_q_uproj_workspace_size(shape, 1) bytes, 16-byte aligned, not
- *   overlapping any input or output (NULL/0 when the query returns 0). When
- *   the tiles of dx are too few to fill the GPU's SMs evenly, each tile's
+ *   workspace/ws_bytes: device scratch, 16-byte aligned, not overlapping any
+ *   input or output (NULL/0 when the size query returns 0). Two paths:
+ *   - with at least mla_q_uproj_workspace_size(shape, 1) bytes, and when
+ *     Dr == 64, Dn % 64 == 0, K % 64 == 0: a pass of its own rotates the
+ *     rope channels into dq_pre_rope (or, when that is NULL, into the
+ *     workspace), then a plain GEMM over [pass-through | rotated] channels
+ *     runs on 256-token tiles (fewer operand bytes per FLOP);
+ *   - otherwise (at least mla_q_uproj_workspace_size(shape, 4) bytes) the
+ *     rotation happens in shared memory between the operand load and the
+ *     tensor cores.
+ *   Both round the rotated values to bf16 by the same formula. When the
+ *   tiles of dx are too few to fill the GPU's SMs evenly, each tile's
  *   reduction over channels is split into parts that write fp32 partial
- *   sums there; a second kernel on the same stream adds them in a fixed
- *   order (results do not depend on scheduling) and rounds to bf16. The
- *   contents need no initialization and are garbage afterwards; calls that
- *   share a workspace must not overlap on the GPU.
+ *   sums in the workspace; a second kernel on the same stream adds them in
+ *   a fixed order (results do not depend on scheduling) and rounds to bf16.
+ *   The contents need no initialization and are garbage afterwards; calls
+ *   that share a workspace must not overlap on the GPU.
  * Requires K % 8 == 0, Dr in {16, 32, 64}, Dn % Dr == 0, and 16-byte aligned
  * pointers.
  */
@@ -317,9 +325,10 @@ MLAQ_API int mla_kv_uproj_fwd(const mla_kv_shape *shape, const void *c_kv, const
  *   - The first call on a device looks up that device's scratch address (a
  *     CUDA runtime query, no allocation); make that first call before any
  *     stream capture. It allocates nothing, ever.
- *   - A shape whose partials need more than MLA_NOALLOC_SCRATCH_BYTES (see
- *     mla_q_uproj_workspace_size(shape, 1)) is rejected with
- *     MLA_ERR_WORKSPACE; shapes that need no workspace always run.
+ *   - A shape whose least workspace (mla_q_uproj_workspace_size(shape, 4))
+ *     exceeds MLA_NOALLOC_SCRATCH_BYTES is rejected with MLA_ERR_WORKSPACE;
+ *     shapes that need no workspace always run. dgrad takes the fastest
+ *     path whose workspace fits in the scratch.
  *   - All calls share the one array. Nothing in it has to start at zero
  *     (every partial the reduction reads is written earlier in the same
  *     call), but calls that overlap on the GPU (other streams, other threads)
@@ -373,11 +382,13 @@ MLAQ_API size_t mxfp8_swizzled_scale_bytes(int64_t rows, int64_t cols);
 MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t *in, int64_t ld_in,
                                   uint8_t *out, void *stream);
 
-/* which: 0 = forward, 1 = dgrad, 2 = wgrad, 3 = MXFP8 backward. Bytes of
- * device workspace the call needs for this shape (0 = pass NULL). Of the
- * bf16 calls only dgrad ever needs any (see mla_q_uproj_bwd_dgrad; that size
- * depends on the current device). Returns 0 for an invalid shape or, for
- * which = 1, when no CUDA device is usable. */
+/* which: 0 = forward, 1 = dgrad, 2 = wgrad, 3 = MXFP8 backward, 4 = the
+ * least workspace dgrad accepts. Bytes of device workspace the call needs
+ * for this shape (0 = pass NULL). Of the bf16 calls only dgrad ever needs
+ * any (see mla_q_uproj_bwd_dgrad; its sizes depend on the current device):
+ * with 1's size it takes its fastest path, with at least 4's a slower one
+ * that needs less. Returns 0 for an invalid shape or, for which = 1 and 4,
+ * when no CUDA device is usable. */
 MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape *shape, int which);
 
 /* Static, human-readable name of a status code. */

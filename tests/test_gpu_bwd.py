@@ -170,7 +170,8 @@ def test_dgrad_split_reduction(cuda_device):
     """Few tiles for many SMs: dgrad splits each tile's channel reduction,
     writes fp32 partials to the workspace and adds them in a fixed order.
     Sampled tokens against the oracle; two runs are bit-identical; a
-    workspace smaller than the query is rejected."""
+    workspace smaller than the least the query reports (which = 4) is
+    rejected."""
     import ctypes
     w = synth.workload("dsv3_bwd", T=1024, seq_len=None)
     inp, d = _dev_inputs(w, 9, cuda_device)
@@ -188,7 +189,9 @@ def test_dgrad_split_reduction(cuda_device):
                           inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy()[toks])
     ref = oracle.dgrad(dqp.reshape(len(toks), -1), helpers.f64(inp["W"]))
     assert helpers.frob_rel(dx1[torch.from_numpy(toks).to(cuda_device)], ref) <= TOL
-    small = torch.empty((need - 16,), dtype=torch.uint8, device=cuda_device)
+    least = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, w.cs_rows, w.Dr, 4)
+    assert 0 < least <= need
+    small = torch.empty((least - 16,), dtype=torch.uint8, device=cuda_device)
     with pytest.raises(mlaq.MlaError) as ei:
         mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], workspace=small)
     assert ei.value.status == mlaq.STATUS["MLA_ERR_WORKSPACE"]

@@ -83,3 +83,35 @@ def test_rope_handoff_full_size(cuda_device):
                              what="dq_pre_rope")
     assert not torch.isnan(r["rope"].float()).any()
     assert helpers.frob_rel(r["db_h"], helpers.bf16_to_f64(r["db"])) <= 1e-3
+
+
+def test_dgrad_paths_agree(cuda_device):
+    """The two dgrad paths: with the least workspace (mla_q_uproj_workspace_size
+    which = 4) dgrad rotates inside its GEMM (fused transform); with the full
+    one (which = 1) it rotates the rope channels in a pass of their own and
+    runs a plain GEMM over them. Both store the same rotated bits and both
+    dx agree with the oracle (their fp32 accumulation orders differ)."""
+    w = synth.workload("dsv3_bwd", T=1024, seq_len=None)
+    inp = synth.make_inputs(w, seed=8)
+    d = helpers.to_dev(inp, cuda_device)
+    cs = d["cos"].shape
+    least = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, cs[0], cs[1], 4)
+    full = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, cs[0], cs[1], 1)
+    assert 0 < least < full
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    outs = {}
+    for name, n in (("fused", least), ("pre", full)):
+        rope = torch.full((w.T, w.H, w.Dr), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+        ws = torch.empty((n,), dtype=torch.uint8, device=cuda_device)
+        dx = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st,
+                            workspace=ws, dq_pre_rope=rope)
+        outs[name] = (dx, rope)
+    torch.cuda.synchronize()
+    mlaq.check_status(st)
+    assert torch.equal(outs["fused"][1], outs["pre"][1]), "the two paths rotated differently"
+    dqp = oracle.rope_bwd(helpers.f64(inp["dq"]), w.H, w.Dn, w.Dr, inp["cos"].numpy(), inp["sin"].numpy(),
+                          inp["pos"].numpy()).reshape(w.T, -1)
+    ref = oracle.dgrad(dqp, helpers.f64(inp["W"]))
+    for name, (dx, _) in outs.items():
+        assert helpers.frob_rel(dx, ref) <= TOL, name
+    assert helpers.frob_rel(outs["pre"][0], helpers.bf16_to_f64(outs["fused"][0])) <= 2e-3

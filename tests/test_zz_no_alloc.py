@@ -47,7 +47,7 @@ def test_noalloc_dgrad_matches_workspace_dgrad(cuda_device):
     w = synth.workload("dsv3_bwd", T=1024, seq_len=None)
     inp = synth.make_inputs(w, seed=11)
     d = helpers.to_dev(inp, cuda_device)
-    need = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, w.cs_rows, w.Dr, 1)
+    need = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, w.cs_rows, w.Dr, 4)  # the least dgrad takes
     assert 0 < need <= SCRATCH_BYTES
     st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     ref = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
@@ -65,7 +65,7 @@ def test_noalloc_dgrad_matches_workspace_dgrad(cuda_device):
 
 def test_noalloc_dgrad_rejects_shapes_beyond_scratch(cuda_device):
     w = synth.workload("dsv3_bwd", T=4096, seq_len=None)
-    need = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, w.cs_rows, w.Dr, 1)
+    need = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, w.cs_rows, w.Dr, 4)
     if need <= SCRATCH_BYTES:
         pytest.skip("this device splits the shape into partials that fit the scratch")
     d = helpers.to_dev(synth.make_inputs(synth.workload("dsv3_bwd", T=4096, seq_len=None, H=128),

@@ -212,9 +212,9 @@ def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream
               dq_pre_rope=None):
     """dx [T, K] bf16 = (inverse-RoPE dq) W.
 
-    When the library splits the channel reduction for this shape, it needs a
-    device workspace (``workspace_size(..., which=1)`` bytes); it is allocated
-    here unless passed in. ``dq_pre_rope`` (a [T, H, Dr] bf16 tensor, or
+    dgrad may need a device workspace: ``workspace_size(..., which=1)``
+    bytes select its fastest path (allocated here unless passed in), at
+    least ``which=4`` bytes a slower one that needs less. ``dq_pre_rope`` (a [T, H, Dr] bf16 tensor, or
     None) receives the rotated rope channels, for bwd_wgrad."""
     dev = dq.device
     _need(dq, "dq", torch.bfloat16)

@@ -204,16 +204,18 @@ MLAQ_API const char* mla_status_string(int status) {
 MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape* shape, int which) {
     int D;
     int64_t N;
-    if (check_shape(shape, &D, &N) != MLA_OK || which < 0 || which > 3) return 0;
+    if (check_shape(shape, &D, &N) != MLA_OK || which < 0 || which > 4) return 0;
     if (which == 3) {  // MXFP8 backward: the quantized operands and the db partials
         Mxfp8BwdLayout L;
         if (shape->T == 0 || bwd_mxfp8_layout(shape->T, shape->K, N, &L) != MLA_OK) return 0;
         return L.total;
     }
-    if (which != 1 || shape->T == 0) return 0;  // only dgrad may split its reduction
+    if ((which != 1 && which != 4) || shape->T == 0) return 0;  // only dgrad needs device scratch
     DeviceInfo di;
     if (current_device_info(&di) != MLA_OK) return 0;
-    return dgrad_workspace_bytes(shape->T, shape->K, N, di.num_sms);
+    return which == 1 ? dgrad_workspace_bytes(shape->T, shape->K, shape->H, shape->Dn, shape->Dr, di.num_sms)
+                      : dgrad_min_workspace_bytes(shape->T, shape->K, shape->H, shape->Dn, shape->Dr, di.num_sms,
+                                                  false);
 }
 
 MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_mode, const void* x,
@@ -292,9 +294,7 @@ static int check_bwd(const mla_q_shape* shape, const void* dq, const void* op, c
     if (s.T > 0 && (!dq || !op || !out)) return MLA_ERR_INVALID_ARG;
     st = check_table_and_positions(&s, cos_tab, sin_tab, pos);
     if (st != MLA_OK) return st;
-    if (ws_bytes < mla_q_uproj_workspace_size(shape, which) ||
-        (mla_q_uproj_workspace_size(shape, which) > 0 && !workspace))
-        return MLA_ERR_WORKSPACE;
+    if (which == 2 && ws_bytes < mla_q_uproj_workspace_size(shape, which)) return MLA_ERR_WORKSPACE;
     if (!rope_dim_supported(s.Dr) || s.Dn % s.Dr) return MLA_ERR_UNSUPPORTED;
     if ((s.K * 2) % 16 || ((*N) * 2) % 16) return MLA_ERR_ALIGNMENT;
     return MLA_OK;
@@ -314,7 +314,17 @@ MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape* shape, const void* dq, con
         !aligned(dq_pre_rope, 16))
         return MLA_ERR_ALIGNMENT;
     const int64_t table = s.cs_rows * s.cs_width * 4;
-    const size_t need = mla_q_uproj_workspace_size(shape, 1);
+    // the least workspace dgrad takes (the fused path's); with at least
+    // mla_q_uproj_workspace_size(shape, 1) bytes it takes the pre-rotated path
+    // (without a usable device the sizes are unknown here; the launch reports it)
+    size_t least = 0, fast = (size_t)-1;
+    DeviceInfo di;
+    if (s.T > 0 && current_device_info(&di) == MLA_OK) {
+        least = dgrad_min_workspace_bytes(s.T, s.K, s.H, s.Dn, s.Dr, di.num_sms, dq_pre_rope != nullptr);
+        fast = dgrad_pre_shape_bytes(s.T, s.K, s.H, s.Dn, s.Dr, di.num_sms, dq_pre_rope != nullptr);
+    }
+    if (ws_bytes < least || (least > 0 && !workspace)) return MLA_ERR_WORKSPACE;
+    const size_t need = (fast != (size_t)-1 && ws_bytes >= fast && (fast == 0 || workspace)) ? fast : least;
     const Range outs[] = {rng(dx, s.T * s.K * 2), rng(dev_status, 4), rng(workspace, (int64_t)need),
                           rng(dq_pre_rope, s.T * s.H * s.Dr * 2)};
     const Range ins[] = {rng(dq, s.T * N * 2), rng(W, N * s.K * 2), rng(cos_tab, table),

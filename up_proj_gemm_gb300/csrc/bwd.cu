@@ -237,6 +237,28 @@ struct StageWalk {
     }
 };
 
+// Inverse RoPE of one pair in float32, one fma each with the other product
+// rounded first, so every path that rotates dq (the fused dgrad and wgrad
+// transforms, the standalone pass) produces the same bf16 bits:
+//   out[i]     = fma(g[i],   cos[i],   fl(g[i+h] sin[i+h]))
+//   out[i + h] = fma(g[i+h], cos[i+h], -fl(g[i] sin[i]))
+// 8 pairs: g1 holds g[i .. i+8) and g2 g[i+h .. i+h+8) as bf16 pairs; ci/si at
+// i, cj/sj at i + h; o1/o2 the rotated values as bf16 pairs.
+__device__ __forceinline__ void rope_inv8(const uint32_t (&g1)[4], const uint32_t (&g2)[4], const float* ci,
+                                          const float* si, const float* cj, const float* sj, uint32_t (&o1)[4],
+                                          uint32_t (&o2)[4]) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float gi0 = bf16lo_to_f32(g1[w]), gi1 = bf16hi_to_f32(g1[w]);
+        const float gj0 = bf16lo_to_f32(g2[w]), gj1 = bf16hi_to_f32(g2[w]);
+        const int e0 = 2 * w, e1 = 2 * w + 1;
+        o1[w] = pack_bf16x2(__fmaf_rn(gi0, ci[e0], __fmul_rn(gj0, sj[e0])),
+                            __fmaf_rn(gi1, ci[e1], __fmul_rn(gj1, sj[e1])));
+        o2[w] = pack_bf16x2(__fmaf_rn(gj0, cj[e0], -__fmul_rn(gi0, si[e0])),
+                            __fmaf_rn(gj1, cj[e1], -__fmul_rn(gi1, si[e1])));
+    }
+}
+
 // Inverse RoPE on 8 pairs of one token, in place in a 128-byte swizzled
 // shared-memory row (row index r inside its 1024-byte swizzle group gives
 // the XOR). Chunk q1 holds g[i], chunk q2 = q1 + Dr/16 holds g[i + Dr/2]:
@@ -253,14 +275,7 @@ __device__ __forceinline__ void rot8(uint32_t row_addr, int r, int q1, int q2, c
     lds_v4(a1, g1);
     lds_v4(a2, g2);
     uint32_t o1[4], o2[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const float gi0 = bf16lo_to_f32(g1[w]), gi1 = bf16hi_to_f32(g1[w]);
-        const float gj0 = bf16lo_to_f32(g2[w]), gj1 = bf16hi_to_f32(g2[w]);
-        const int e0 = 2 * w, e1 = 2 * w + 1;
-        o1[w] = pack_bf16x2(gi0 * ci[e0] + gj0 * sj[e0], gi1 * ci[e1] + gj1 * sj[e1]);
-        o2[w] = pack_bf16x2(-gi0 * si[e0] + gj0 * cj[e0], -gi1 * si[e1] + gj1 * cj[e1]);
-    }
+    rope_inv8(g1, g2, ci, si, cj, sj, o1, o2);
     sts_v4(a1, o1);
     sts_v4(a2, o2);
     if (o != nullptr) {
@@ -1010,6 +1025,242 @@ __global__ void __launch_bounds__(kDgThreads, 1)
     }
 }
 
+// --------------------------------------------- dgrad with pre-rotated rope
+// Rope pass: rope_out[t, h, :] = the inverse rotation of dq's last Dr = 64
+// channels of head h (rope_inv8: the bits the fused transforms produce). A
+// thread takes 8 pairs of one (token, head): 4 threads per pair set, a warp 8
+// heads of one token (reads of 128 contiguous bytes per head, 1 KB written).
+__global__ void __launch_bounds__(256) rope_pre_kernel(const uint16_t* __restrict__ dq, int64_t T, int H, int Dn,
+                                                       const float* __restrict__ cos_tab,
+                                                       const float* __restrict__ sin_tab, long long cs_rows,
+                                                       long long cs_width, int cs_vec,
+                                                       const int32_t* __restrict__ pos,
+                                                       uint16_t* __restrict__ rope_out, int* status) {
+    constexpr int DR = 64, HH = 32;
+    const int D = Dn + DR;
+    const int64_t items = T * H * 4;
+    for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < items;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int q = (int)(it & 3);
+        const int64_t th = it >> 2;
+        const int64_t t = th / H;
+        const int h = (int)(th - t * H);
+        const int64_t pp = pos ? (int64_t)__ldg(pos + t) : t;
+        if (pp < 0 || pp >= cs_rows) {
+            record_status(status, MLA_ERR_POS_RANGE);
+            continue;
+        }
+        const uint16_t* g = dq + (t * H + h) * D + Dn + 8 * q;
+        const uint4 ra = __ldg(reinterpret_cast<const uint4*>(g));
+        const uint4 rc = __ldg(reinterpret_cast<const uint4*>(g + HH));
+        const uint32_t g1[4] = {ra.x, ra.y, ra.z, ra.w}, g2[4] = {rc.x, rc.y, rc.z, rc.w};
+        float ci[8], si[8], cj[8], sj[8];
+        const float* cr = cos_tab + pp * cs_width + 8 * q;
+        const float* sr = sin_tab + pp * cs_width + 8 * q;
+        load8(cr, cs_vec != 0, ci);
+        load8(sr, cs_vec != 0, si);
+        load8(cr + HH, cs_vec != 0, cj);
+        load8(sr + HH, cs_vec != 0, sj);
+        uint32_t o1[4], o2[4];
+        rope_inv8(g1, g2, ci, si, cj, sj, o1, o2);
+        uint16_t* o = rope_out + (t * H + h) * DR + 8 * q;
+        st_global_v4(o, o1[0], o1[1], o1[2], o1[3]);
+        st_global_v4(o + HH, o2[0], o2[1], o2[2], o2[3]);
+    }
+}
+
+// dgrad as a plain GEMM over [dq pass-through | rotated rope]: Dr = 64 and
+// Dn % 64 == 0, so each 64-channel K chunk is all pass-through (A from dq) or
+// all rope (A from rope_out, a {64, T, H} view). 256-token x BN tiles: two
+// M = 128 MMAs per K step into TMEM columns 0 and 256 (one accumulator pair,
+// not double-buffered; the units are long), one ring of A + B stages.
+// Warps: 0 producer, 1 MMA issuer, 2-5 epilogue of rows 0-127, 6-9 of rows
+// 128-255 (warp w reads TMEM lanes 32 (w % 4) ...).
+constexpr int kDpThreads = 320;
+constexpr int kDpBM = 256;
+constexpr uint32_t kDpABytes = (uint32_t)kDpBM * 128u;
+
+__global__ void __launch_bounds__(kDpThreads, 1)
+    dgrad_pre_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmR, const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    Smem sm;
+    sm.S = p.stages;
+    sm.base = (raw + 1023u) & ~1023u;
+    sm.bars = sm.base + (uint32_t)p.stages * p.stage_bytes;
+    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (3 * p.stages + 5);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr int BK = kBKD;
+    constexpr uint32_t CHB = (uint32_t)BK * 128u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(sm.full(s), 1);
+            mbar_init(sm.empty(s), 1);
+        }
+        mbar_init(sm.tfull(0), 1);
+        mbar_init(sm.tempty(0), 8);
+        mbar_init(sm.drain(), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmR);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32((const void*)tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nb_chunks = p.BN / 64;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued_mask = 0, issued_par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                int tile, k0, k1;
+                unit_range(p, u, tile, k0, k1);
+                const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
+                int c0 = (k0 * BK) % p.D, head = (k0 * BK) / p.D;  // chunk position, no division per stage
+                for (int kt = k0; kt < k1; ++kt) {
+                    if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(sm.full(s), p.tx_bytes);
+                    if (c0 < p.Dn) tma_load_2d(sm.a(s, p), &tmA, kt * BK, mt * kDpBM, sm.full(s));
+                    else tma_load_3d(sm.a(s, p), &tmR, 0, mt * kDpBM, head, sm.full(s));
+                    tma_load_3d(sm.b(s, p), &tmB, 0, kt * BK, nt * nb_chunks, sm.full(s));
+                    issued_mask |= 1u << s;
+                    issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    c0 += BK;
+                    if (c0 >= p.D) {
+                        c0 -= p.D;
+                        ++head;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int q = 0; q < p.stages; ++q)
+                    if (issued_mask & (1u << q))
+                        mbar_wait(sm.full(q), (issued_par >> q) & 1u, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int local = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++local) {
+                int tile, k0, k1;
+                unit_range(p, u, tile, k0, k1);
+                if (!mbar_wait(sm.tempty(0), ((uint32_t)local & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = k0; kt < k1; ++kt) {
+                    if (!mbar_wait(sm.full(s), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)
+#pragma unroll
+                        for (int hm = 0; hm < 2; ++hm)
+                            mma_bf16(tmem_base + hm * kAccStride, desc_kmajor_sw128(a0 + hm * 16384u + 32u * j),
+                                     desc_mnmajor_sw128(b0 + 2048u * j, CHB), p.idesc, (kt != k0 || j != 0));
+                    mma_commit(sm.empty(s));
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(sm.tfull(0));
+            }
+            if (!ok) {
+                mma_commit(sm.drain());
+                mbar_wait(sm.drain(), 0, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int hm = (warp - 2) >> 2;  // which accumulator: token rows 0-127 or 128-255
+        const int row = hm * 128 + quad * 32 + lane;
+        int local = 0;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
+            int tile, sp;
+            unit_split(p, u, tile, sp);
+            if (!mbar_wait(sm.tfull(0), (uint32_t)local & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int mt = tile / p.num_n_tiles;
+            const int nt = tile % p.num_n_tiles;
+            const int64_t orow = (int64_t)mt * kDpBM + row;  // token
+            const bool valid = orow < p.out_rows;
+            const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)hm * kAccStride;
+            for (int col = 0; col < p.BN; col += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld32(trow + col, r);
+                tmem_ld_wait();
+                const int64_t c0 = (int64_t)nt * p.BN + col;
+                if (valid && p.ws) {
+                    float* dst = p.ws + ((int64_t)sp * p.out_rows + orow) * p.out_cols + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        if (c0 + i + 4 <= p.out_cols) st_global_v4(dst + i, r[i], r[i + 1], r[i + 2], r[i + 3]);
+                } else if (valid) {
+                    uint16_t* dst = p.out + orow * p.out_cols + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        if (c0 + i + 8 <= p.out_cols)
+                            st_global_v4(dst + i,
+                                         pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                         pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                         pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
+                                         pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.tempty(0));
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) record_status(p.status, MLA_ERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
 // wgrad rotating dq itself (32-token stages)
 int launch_wgrad_self(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr,
                       const BwdParams& p, int grid, size_t smem, cudaStream_t stream) {
@@ -1057,6 +1308,85 @@ __global__ void __launch_bounds__(256) dgrad_reduce_kernel(const float* __restri
         st_global_v4(dx + i, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                      pack_bf16x2(v[6], v[7]));
     }
+}
+
+// ------------------------------------------------ dgrad: which path, and its launch
+// The pre-rotated path: Dr = 64 with Dn % 64 == 0 (64-channel K chunks are
+// all pass-through or all rope), K % 64 == 0 (W's chunk view), and a
+// workspace that holds its split partials plus, without dq_pre_rope, the
+// rotated rope channels.
+bool dgrad_pre_shape(int64_t K, int Dn, int Dr) { return Dr == 64 && Dn % 64 == 0 && K % 64 == 0; }
+
+int dgrad_pre_ksplit(int64_t T, int64_t K, int64_t N, int num_sms) {
+    const int64_t tiles = ((T + kDpBM - 1) / kDpBM) * ((K + 255) / 256);
+    return best_ksplit(tiles, (N + kBKD - 1) / kBKD, num_sms);
+}
+
+size_t dgrad_pre_bytes(int64_t T, int64_t K, int64_t N, int H, int Dr, int num_sms, bool rope_buffer, size_t* rope_off) {
+    const int sp = dgrad_pre_ksplit(T, K, N, num_sms);
+    size_t off = sp > 1 ? (size_t)sp * (size_t)T * (size_t)K * sizeof(float) : 0;
+    off = (off + 255) / 256 * 256;
+    if (rope_off) *rope_off = off;
+    return rope_buffer ? off + (size_t)T * H * Dr * 2 : (sp > 1 ? off : 0);
+}
+
+bool dgrad_pre_path(const BwdArgs& a, int num_sms) {
+    if (a.T == 0 || !dgrad_pre_shape(a.K, a.Dn, a.Dr)) return false;
+    const int64_t N = (int64_t)a.H * (a.Dn + a.Dr);
+    const size_t need = dgrad_pre_bytes(a.T, a.K, N, a.H, a.Dr, num_sms, a.rope_out == nullptr, nullptr);
+    return need == 0 || (a.workspace != nullptr && a.ws_bytes >= need);
+}
+
+int launch_dgrad_pre(const BwdArgs& a, BwdParams& p, const DeviceInfo& di, cudaStream_t stream) {
+    const int64_t N = p.N;
+    size_t rope_off = 0;
+    dgrad_pre_bytes(a.T, a.K, N, a.H, a.Dr, di.num_sms, true, &rope_off);
+    uint16_t* rope = a.rope_out ? static_cast<uint16_t*>(a.rope_out)
+                                : reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.workspace) + rope_off);
+    // 1. the rope channels, rotated once
+    {
+        const int64_t items = a.T * a.H * 4;
+        int64_t blocks = (items + 255) / 256;
+        if (blocks > (int64_t)di.num_sms * 8) blocks = (int64_t)di.num_sms * 8;
+        rope_pre_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(a.dq), a.T, a.H, a.Dn,
+                                                              a.cos_tab, a.sin_tab, a.cs_rows, a.cs_width, p.cs_vec,
+                                                              a.pos, rope, a.status);
+        if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    // 2. the GEMM over [pass-through | rotated rope], 256-token tiles
+    p.num_m_tiles = (int)((a.T + kDpBM - 1) / kDpBM);
+    p.num_tiles = p.num_m_tiles * p.num_n_tiles;
+    p.ksplit = dgrad_pre_ksplit(a.T, a.K, N, di.num_sms);
+    p.kts = (p.k_tiles + p.ksplit - 1) / p.ksplit;
+    p.num_units = p.num_tiles * p.ksplit;
+    p.ws = p.ksplit > 1 ? static_cast<float*>(a.workspace) : nullptr;
+    p.a_bytes = kDpABytes;
+    p.stage_bytes = p.a_bytes + (uint32_t)(p.BN / 64) * (uint32_t)kBKD * 128u;
+    p.tx_bytes = p.stage_bytes;
+    const size_t fixed = 1024 + 256;
+    int stages = (int)((size_t)(di.max_smem_optin - fixed) / p.stage_bytes);
+    if (stages > 6) stages = 6;
+    if (stages < 2) return MLA_ERR_UNSUPPORTED;
+    p.stages = stages;
+    const size_t smem = fixed + (size_t)stages * p.stage_bytes;
+    alignas(64) CUtensorMap ta, tb, tr;
+    int st = make_tmap_2d(&ta, a.dq, 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * 2, 64, kDpBM, true);
+    if (st != MLA_OK) return st;
+    st = make_tmap_chunks(&tb, a.W, (uint64_t)N, (uint64_t)a.K, kBKD, (uint32_t)(p.BN / 64));
+    if (st != MLA_OK) return st;
+    st = make_tmap_3d(&tr, rope, 64, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.H * 128, 128, 64, kDpBM, 1);
+    if (st != MLA_OK) return st;
+    const int grid = p.num_units < di.num_sms ? p.num_units : di.num_sms;
+    if (cudaFuncSetAttribute(dgrad_pre_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    dgrad_pre_kernel<<<grid, kDpThreads, smem, stream>>>(ta, tb, tr, p);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    if (p.ksplit == 1) return MLA_OK;
+    const int64_t n = a.T * a.K;
+    int64_t blocks = (n / 8 + 255) / 256;
+    if (blocks > (int64_t)di.num_sms * 8) blocks = (int64_t)di.num_sms * 8;
+    dgrad_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p.ws, p.ksplit, n, static_cast<uint16_t*>(a.dx));
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
@@ -1107,11 +1437,12 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     p.out_cols = (int)a.K;
     p.db = wg ? static_cast<uint16_t*>(a.db) : nullptr;
     p.status = a.status;
+    if (!wg && dgrad_pre_path(a, di.num_sms)) return launch_dgrad_pre(a, p, di, stream);
     p.ksplit = wg ? 1 : dgrad_ksplit(a.T, a.K, N, di.num_sms);
     p.kts = (p.k_tiles + p.ksplit - 1) / p.ksplit;
     p.num_units = p.num_tiles * p.ksplit;
     p.ws = p.ksplit > 1 ? static_cast<float*>(a.workspace) : nullptr;
-    if (p.ksplit > 1 && (!a.workspace || a.ws_bytes < dgrad_workspace_bytes(a.T, a.K, N, di.num_sms)))
+    if (p.ksplit > 1 && (!a.workspace || a.ws_bytes < dgrad_workspace_bytes_fused(a.T, a.K, N, di.num_sms)))
         return MLA_ERR_WORKSPACE;
 
     if (wg && a.T == 0) {  // empty reduction: the gradients are zero
@@ -1214,10 +1545,8 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
 // Splits of each dgrad tile's channel reduction: the count in 1..4 (keeping
 // >= 32 stages per split) whose units fill the SMs' waves best; ties go to
 // fewer splits. 1 means no split (and no workspace).
-int dgrad_ksplit(int64_t T, int64_t K, int64_t N, int num_sms) {
+int best_ksplit(int64_t tiles, int64_t k_tiles, int num_sms) {
     if (num_sms <= 0) return 1;
-    const int64_t tiles = ((T + kBM - 1) / kBM) * ((K + 255) / 256);
-    const int64_t k_tiles = (N + kBKD - 1) / kBKD;
     int best = 1;
     double best_eff = 0.0;
     for (int sp = 1; sp <= 4; ++sp) {
@@ -1233,9 +1562,35 @@ int dgrad_ksplit(int64_t T, int64_t K, int64_t N, int num_sms) {
     return best;
 }
 
-size_t dgrad_workspace_bytes(int64_t T, int64_t K, int64_t N, int num_sms) {
+int dgrad_ksplit(int64_t T, int64_t K, int64_t N, int num_sms) {
+    return best_ksplit(((T + kBM - 1) / kBM) * ((K + 255) / 256), (N + kBKD - 1) / kBKD, num_sms);
+}
+
+size_t dgrad_workspace_bytes_fused(int64_t T, int64_t K, int64_t N, int num_sms) {
     const int sp = dgrad_ksplit(T, K, N, num_sms);
     return sp > 1 ? (size_t)sp * (size_t)T * (size_t)K * sizeof(float) : 0;
+}
+
+size_t dgrad_workspace_bytes(int64_t T, int64_t K, int H, int Dn, int Dr, int num_sms) {
+    const int64_t N = (int64_t)H * (Dn + Dr);
+    if (T > 0 && dgrad_pre_shape(K, Dn, Dr)) return dgrad_pre_bytes(T, K, N, H, Dr, num_sms, true, nullptr);
+    return dgrad_workspace_bytes_fused(T, K, N, num_sms);
+}
+
+size_t dgrad_pre_shape_bytes(int64_t T, int64_t K, int H, int Dn, int Dr, int num_sms, bool have_rope_out) {
+    if (T == 0 || !dgrad_pre_shape(K, Dn, Dr)) return (size_t)-1;  // no such path
+    const int64_t N = (int64_t)H * (Dn + Dr);
+    return dgrad_pre_bytes(T, K, N, H, Dr, num_sms, !have_rope_out, nullptr);
+}
+
+size_t dgrad_min_workspace_bytes(int64_t T, int64_t K, int H, int Dn, int Dr, int num_sms, bool have_rope_out) {
+    const int64_t N = (int64_t)H * (Dn + Dr);
+    const size_t fused = dgrad_workspace_bytes_fused(T, K, N, num_sms);
+    if (T > 0 && dgrad_pre_shape(K, Dn, Dr)) {
+        const size_t pre = dgrad_pre_bytes(T, K, N, H, Dr, num_sms, !have_rope_out, nullptr);
+        return pre < fused ? pre : fused;
+    }
+    return fused;
 }
 
 int launch_dgrad(const BwdArgs& a, cudaStream_t stream) { return launch_common(a, false, stream); }

@@ -132,7 +132,18 @@ int launch_dgrad(const BwdArgs& a, cudaStream_t stream);
 // dgrad's split of the channel reduction for this shape on a device with
 // num_sms SMs, and the fp32 workspace it needs (0 when not split).
 int dgrad_ksplit(int64_t T, int64_t K, int64_t N, int num_sms);
-size_t dgrad_workspace_bytes(int64_t T, int64_t K, int64_t N, int num_sms);
+// Best split count (1..4, each part >= 32 K steps) for this many tiles.
+int best_ksplit(int64_t tiles, int64_t k_tiles, int num_sms);
+// Workspace of the fused dgrad (split partials only).
+size_t dgrad_workspace_bytes_fused(int64_t T, int64_t K, int64_t N, int num_sms);
+// Workspace that lets dgrad take its fastest path for this shape (for the
+// pre-rotated path: its split partials plus the rotated rope channels).
+size_t dgrad_workspace_bytes(int64_t T, int64_t K, int H, int Dn, int Dr, int num_sms);
+// The pre-rotated path's workspace for this shape ((size_t)-1: no such path).
+size_t dgrad_pre_shape_bytes(int64_t T, int64_t K, int H, int Dn, int Dr, int num_sms, bool have_rope_out);
+// The least workspace dgrad accepts for this shape (the smaller of the two
+// paths' needs; the path is then chosen by the workspace given).
+size_t dgrad_min_workspace_bytes(int64_t T, int64_t K, int H, int Dn, int Dr, int num_sms, bool have_rope_out);
 int launch_wgrad(const BwdArgs& a, cudaStream_t stream);
 
 // MXFP8 backward (see mla_q_uproj_bwd_mxfp8): workspace carve-up and launch.

@@ -56,15 +56,22 @@ extern "C" MLAQ_API int mla_q_uproj_bwd_dgrad_noalloc(const mla_q_shape* shape, 
                                                       const float* sin_tab, const int32_t* pos, void* dx,
                                                       void* dq_pre_rope, int* dev_status, void* stream) {
     // Same argument checks as the allocating entry point (a NULL workspace
-    // with size 0 passes them); then the scratch stands in for the workspace.
-    const size_t need = mla_q_uproj_workspace_size(shape, 1);
-    if (need == 0)
+    // with size 0 passes them); then the scratch stands in for the workspace,
+    // and dgrad takes the fastest path whose workspace fits in it.
+    if (!shape || shape->T <= 0)
         return mla_q_uproj_bwd_dgrad(shape, dq, W, cos_tab, sin_tab, pos, dx, dq_pre_rope, nullptr, 0,
                                      dev_status, stream);
-    if (need > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;  // shape too large for the scratch
+    mlaq::DeviceInfo di;
+    if (mlaq::current_device_info(&di) != MLA_OK) return MLA_ERR_CUDA;
+    const size_t least = mlaq::dgrad_min_workspace_bytes(shape->T, shape->K, shape->H, shape->Dn, shape->Dr,
+                                                        di.num_sms, dq_pre_rope != nullptr);
+    if (least == 0)
+        return mla_q_uproj_bwd_dgrad(shape, dq, W, cos_tab, sin_tab, pos, dx, dq_pre_rope, nullptr, 0,
+                                     dev_status, stream);
+    if (least > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;  // shape too large for the scratch
     int err = MLA_OK;
     void* scratch = mlaq::scratch_address(&err);
     if (!scratch) return err;
-    return mla_q_uproj_bwd_dgrad(shape, dq, W, cos_tab, sin_tab, pos, dx, dq_pre_rope, scratch, need,
-                                 dev_status, stream);
+    return mla_q_uproj_bwd_dgrad(shape, dq, W, cos_tab, sin_tab, pos, dx, dq_pre_rope, scratch,
+                                 MLA_NOALLOC_SCRATCH_BYTES, dev_status, stream);
 }
