@@ -191,9 +191,10 @@ MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape *shape, const void *dq, con
  *   dq_pre_rope: NULL (the rope channels of dq are rotated here, on their way
  *   into the tensor cores), or the buffer mla_q_uproj_bwd_dgrad filled from
  *   the same dq, positions and tables (an input here). When Dr == 64,
- *   Dn % 128 == 0 and H is even, the rope tiles are then read from it
- *   instead of rotated again; other shapes rotate dq as with NULL. Either
- *   way the operands, and so dW and db, are the same bits.
+ *   Dn % 128 == 0, H is even and K % 64 == 0, the rope tiles are then read
+ *   from it instead of rotated again (and dW runs on 256-channel tiles);
+ *   other shapes rotate dq as with NULL. Either way the operands, and so
+ *   dW, are the same bits; db's fp32 sums are grouped differently.
  *   workspace/ws_bytes: unused (NULL/0; mla_q_uproj_workspace_size(shape, 2)
  *   is 0).
  * Requirements as for mla_q_uproj_bwd_dgrad.

@@ -1261,6 +1261,274 @@ __global__ void __launch_bounds__(kDpThreads, 1)
     }
 }
 
+// ------------------------------------- wgrad reading the rotated rope tiles
+// The hand-off case (Dr = 64, Dn % 128 == 0, H even, dq_pre_rope given): dW
+// as a plain GEMM over 256-channel tiles made of two 128-channel sub-tiles
+// of the head-pair order (tile_chunks): each sub-tile is one 3-D TMA op,
+// two pass-through chunks of dq or one head pair's rotated rope channels.
+// Two M = 128 MMAs per K step (tokens) into TMEM columns 0 and 256; 64-token
+// stages of A (4 MN-major chunks, 32 KB) and B (x, BN/64 chunks).
+// Warps: 0 producer, 1 MMA, 2-9 epilogue (accumulator (w - 2) / 4, lanes
+// 32 (w % 4)), 10-17 bias gradient: on the first column tile every stage's
+// 256 channels are summed over its tokens (thread: 8 channels x 8 of the
+// 64 token rows; the 8 row groups are added in order at the tile's end), and
+// these warps release each stage together with the MMA.
+constexpr int kWpThreads = 576;
+constexpr int kWpDbWarp0 = 10;
+constexpr int kWpBK = 64;
+
+__global__ void __launch_bounds__(kWpThreads, 1)
+    wgrad_pre_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmR, const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    Smem sm;
+    sm.S = p.stages;
+    sm.base = (raw + 1023u) & ~1023u;
+    sm.bars = sm.base + (uint32_t)p.stages * p.stage_bytes;
+    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (3 * p.stages + 5);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
+    float* db_part = reinterpret_cast<float*>(tail + 16);  // [8 row groups][256 channels]
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr int BK = kWpBK;
+    constexpr uint32_t CH = (uint32_t)BK * 128u;  // one 64-channel MN-major chunk of BK rows
+    const int n_sub = p.num_m_tiles;              // 128-channel sub-tiles
+    const int num_m2 = (n_sub + 1) / 2;
+    const int num_units = num_m2 * p.num_n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(sm.full(s), 1);
+            mbar_init(sm.empty(s), 1 + 8);  // the MMA's commit and the 8 bias warps
+        }
+        mbar_init(sm.tfull(0), 1);
+        mbar_init(sm.tempty(0), 8);
+        mbar_init(sm.drain(), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmR);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32((const void*)tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nb_chunks = p.BN / 64;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued_mask = 0, issued_par = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+                const int m2 = u / p.num_n_tiles, nt = u % p.num_n_tiles;
+                int az[2];
+                bool rp[2], has[2];
+                for (int hm = 0; hm < 2; ++hm) {
+                    const int ms = 2 * m2 + hm;
+                    has[hm] = ms < n_sub;
+                    int c0 = 0, c1 = 0;
+                    rp[hm] = false;
+                    if (has[hm]) tile_chunks(p, ms, c0, c1, rp[hm]);
+                    az[hm] = rp[hm] ? (c0 - p.Dn) / p.D : c0 / 64;
+                }
+                const uint32_t tx = p.tx_bytes - (has[1] ? 0u : 2u * CH);
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(sm.full(s), tx);
+                    for (int hm = 0; hm < 2; ++hm)
+                        if (has[hm])
+                            tma_load_3d(sm.a(s, p) + (uint32_t)hm * 2u * CH, rp[hm] ? &tmR : &tmA, 0, kt * BK,
+                                        az[hm], sm.full(s));
+                    tma_load_3d(sm.b(s, p), &tmB, 0, kt * BK, nt * nb_chunks, sm.full(s));
+                    issued_mask |= 1u << s;
+                    issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int q = 0; q < p.stages; ++q)
+                    if (issued_mask & (1u << q))
+                        mbar_wait(sm.full(q), (issued_par >> q) & 1u, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int local = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++local) {
+                if (!mbar_wait(sm.tempty(0), ((uint32_t)local & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!mbar_wait(sm.full(s), ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j) {
+                        const uint64_t bd = desc_mnmajor_sw128(b0 + 2048u * j, CH);
+#pragma unroll
+                        for (int hm = 0; hm < 2; ++hm)
+                            mma_bf16(tmem_base + hm * kAccStride,
+                                     desc_mnmajor_sw128(a0 + (uint32_t)hm * 2u * CH + 2048u * j, CH), bd, p.idesc,
+                                     (kt != 0 || j != 0));
+                    }
+                    mma_commit(sm.empty(s));
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) mma_commit(sm.tfull(0));
+            }
+            if (!ok) {
+                mma_commit(sm.drain());
+                mbar_wait(sm.drain(), 0, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp < kWpDbWarp0) {
+        // ---------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int hm = (warp - 2) >> 2;
+        const int row = quad * 32 + lane;
+        int local = 0;
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++local) {
+            if (!mbar_wait(sm.tfull(0), (uint32_t)local & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int m2 = u / p.num_n_tiles, nt = u % p.num_n_tiles;
+            const int ms = 2 * m2 + hm;
+            bool valid = ms < n_sub;
+            int64_t orow = 0;
+            if (valid) {
+                int c0, c1;
+                bool rp;
+                tile_chunks(p, ms, c0, c1, rp);
+                orow = (row < 64 ? c0 : c1) + (row & 63);  // output channel
+                valid = orow < p.out_rows;
+            }
+            const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)hm * kAccStride;
+            for (int col = 0; col < p.BN; col += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_ld32(trow + col, r);
+                tmem_ld_wait();
+                const int64_t kc = (int64_t)nt * p.BN + col;
+                if (valid) {
+                    uint16_t* dst = p.out + orow * p.out_cols + kc;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        if (kc + i + 8 <= p.out_cols)
+                            st_global_v4(dst + i,
+                                         pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                         pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                         pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
+                                         pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.tempty(0));
+        }
+    } else {
+        // ------------------------------------------------------ bias gradient
+        const int dt = threadIdx.x - 32 * kWpDbWarp0;  // 0..255
+        const int cg = dt & 31;                        // channels [8 cg, 8 cg + 8) of the tile's 256
+        const int rg = dt >> 5;                        // token rows rg, rg + 8, ... of each stage
+        const int chunk = cg >> 3, q = cg & 7;         // MN-major chunk, 16-byte group in its rows
+        int s = 0;
+        uint32_t ph = 0;
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+            const int m2 = u / p.num_n_tiles, nt = u % p.num_n_tiles;
+            const bool sum = p.db != nullptr && nt == 0;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            bool ok = true;
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!mbar_wait(sm.full(s), ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (sum) {
+                    const uint32_t base = sm.a(s, p) + (uint32_t)chunk * CH;
+#pragma unroll
+                    for (int i = 0; i < BK / 8; ++i) {
+                        const int r = rg + 8 * i;
+                        uint32_t v[4];
+                        lds_v4(base + (uint32_t)r * 128u + (uint32_t)((q ^ (r & 7)) * 16), v);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            acc[2 * w] += bf16lo_to_f32(v[w]);
+                            acc[2 * w + 1] += bf16hi_to_f32(v[w]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.empty(s));
+                if (++s == p.stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (sum) {
+                // the 8 row groups' partial sums added in order, one channel per thread
+#pragma unroll
+                for (int e = 0; e < 8; ++e) db_part[rg * 256 + 8 * cg + e] = acc[e];
+                named_bar_sync(1, 256);
+                const int c = dt;  // channel of the tile
+                float tot = 0.f;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) tot += db_part[g * 256 + c];
+                const int ms = 2 * m2 + c / 128;
+                if (ms < n_sub) {
+                    int c0, c1;
+                    bool rp;
+                    tile_chunks(p, ms, c0, c1, rp);
+                    const int cc = c & 127;
+                    const int64_t ch = (cc < 64 ? c0 : c1) + (cc & 63);
+                    if (ch < p.out_rows) p.db[ch] = (uint16_t)(pack_bf16x2(tot, 0.f) & 0xFFFFu);
+                }
+                named_bar_sync(1, 256);  // db_part is rewritten by the next tile
+            }
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) record_status(p.status, MLA_ERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
 // wgrad rotating dq itself (32-token stages)
 int launch_wgrad_self(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr,
                       const BwdParams& p, int grid, size_t smem, cudaStream_t stream) {
@@ -1282,12 +1550,23 @@ int launch_wgrad_self(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, cons
 }
 
 // wgrad with pre-rotated rope tiles: head pairs only, so Dr = 64
-int launch_wgrad_pre(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr, const BwdParams& p,
-                     int grid, size_t smem, cudaStream_t stream) {
-    const void* k = (const void*)wgrad_kernel<64, kBKWPre>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+int launch_wgrad_pre(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tr, BwdParams p,
+                     const DeviceInfo& di, cudaStream_t stream) {
+    constexpr uint32_t CH = (uint32_t)kWpBK * 128u;
+    p.a_bytes = 4u * CH;
+    p.stage_bytes = p.a_bytes + (uint32_t)(p.BN / 64) * CH;
+    p.tx_bytes = p.stage_bytes;
+    const size_t fixed = 1024 + 256 + 8 * 256 * sizeof(float);  // alignment, barriers, bias partials
+    int stages = (int)((size_t)(di.max_smem_optin - fixed) / p.stage_bytes);
+    if (stages > 6) stages = 6;
+    if (stages < 2) return MLA_ERR_UNSUPPORTED;
+    p.stages = stages;
+    const size_t smem = fixed + (size_t)stages * p.stage_bytes;
+    const int units = ((p.num_m_tiles + 1) / 2) * p.num_n_tiles;
+    const int grid = units < di.num_sms ? units : di.num_sms;
+    if (cudaFuncSetAttribute(wgrad_pre_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MLA_ERR_CUDA;
-    wgrad_kernel<64, kBKWPre><<<grid, kWgThreads, smem, stream>>>(ta, tb, tr, p);
+    wgrad_pre_kernel<<<grid, kWpThreads, smem, stream>>>(ta, tb, tr, p);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -1410,7 +1689,7 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
         p.tiles_per_pair = a.Dn / 64 + 1;
         p.num_m_tiles = (a.H / 2) * p.tiles_per_pair;
     }
-    p.pre = p.paired && a.rope_in != nullptr;
+    p.pre = p.paired && a.rope_in != nullptr && a.K % 64 == 0;  // its B loads use x's chunk view
     p.rope_out = wg ? nullptr : static_cast<uint16_t*>(a.rope_out);
     p.H = a.H;
     p.Dr = a.Dr;
@@ -1530,7 +1809,7 @@ int launch_common(const BwdArgs& a, bool wg, cudaStream_t stream) {
     }
     if (st != MLA_OK) return st;
     const int grid = p.num_units < di.num_sms ? p.num_units : di.num_sms;
-    st = p.pre ? launch_wgrad_pre(ta, tb, tr, p, grid, smem, stream)
+    st = p.pre ? launch_wgrad_pre(ta, tb, tr, p, di, stream)
                : launch_wgrad_self(a.Dr, ta, tb, tr, p, grid, smem, stream);
     if (st != MLA_OK || p.ksplit == 1) return st;
     const int64_t n = a.T * a.K;
