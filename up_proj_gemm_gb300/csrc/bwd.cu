@@ -81,7 +81,7 @@ struct BwdParams {
     int a3d, b3d;  // operand maps are 3-D chunk views (one TMA op per operand and stage)
     // wgrad channel tiles by head pair (see tile_chunks); tiles per pair
     int paired, tiles_per_pair;
-    // wgrad: rope-pair tiles load already rotated values (no transform)
+    // wgrad: the rope tiles come rotated from dq_pre_rope (wgrad_pre_kernel)
     int pre;
     // dgrad: rotated rope channels out, [T, H, Dr] bf16 (nullable; each head's
     // channels written by the units of column tile head mod num_n_tiles)
@@ -219,7 +219,7 @@ struct StageWalk {
         c0 = WG ? 0 : (k0 * kBKD) % p.D;
         if (WG) {
             tile_chunks(p, mt, w0, w1, rope_pair);
-            const bool rot = rope_pair ? !p.pre : (has_rope(p, w0, 64) || has_rope(p, w1, 64));
+            const bool rot = rope_pair || has_rope(p, w0, 64) || has_rope(p, w1, 64);
             tile_x = rot || (p.db != nullptr && nt == 0);
             az = rope_pair ? (w0 - p.Dn) / p.D : w0 / 64;
         }
@@ -555,8 +555,8 @@ __global__ void __launch_bounds__(kWgThreads, 1)
                 int c0, c1;
                 bool rp;
                 tile_chunks(p, mt, c0, c1, rp);
-                // (rotating wgrad only: 32-token stages, 4 threads per token row)
-                if (BK == kBKW && !(rp && p.pre)) {
+                // (32-token stages, 4 threads per token row)
+                {
                     int r0[8], r1[8];
                     const int n0r = rope_regions(p, c0, 64, r0), n1r = rope_regions(p, c1, 64, r1);
                     for (int j = 0; j < n0r && nreg < 8; ++j) reg[nreg++] = r0[j] - c0;
