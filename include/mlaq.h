@@ -144,8 +144,9 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_
  * Backward, input gradient: dx = (J^T dq) W.
  * TransformerEngine PR "Add a backwards linear function to be used with the
  * fused mla q up-proj", summary and sequence diagram (RoPE backward, then the
- * linear backward with the weight). The inverse rotation is applied to dq
- * tiles on their way into the tensor cores; the full dq_pre is never stored.
+ * linear backward with the weight). Only the rope channels of dq change under
+ * the inverse rotation; the pass-through channels go to the tensor cores as
+ * they are, and at most the rotated rope channels are ever stored.
  *   dq [T, H, D] bf16, W [N, K] bf16 (the bf16 master weight), dx [T, K] bf16
  *   (fp32 accumulation). cos_tab/sin_tab/pos as in the forward.
  *   dq_pre_rope: NULL, or [T, H, Dr] bf16 (16-byte aligned, not overlapping
@@ -153,7 +154,8 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_
  *   last Dr channels of every head after the inverse rotation, rounded to
  *   bf16: exactly the values the tensor cores consume. Pass it on to
  *   mla_q_uproj_bwd_wgrad, which then skips its own rotation. Rows whose
- *   position is out of range are left unwritten (dev_status reports it).
+ *   position is out of range are left unwritten and their dx is unspecified
+ *   (dev_status reports it).
  *   workspace/ws_bytes: device scratch, 16-byte aligned, not overlapping any
  *   input or output (NULL/0 when the size query returns 0). Two paths:
  *   - with at least mla_q_uproj_workspace_size(shape, 1) bytes, and when

@@ -1289,7 +1289,9 @@ __global__ void __launch_bounds__(kWpThreads, 1)
     uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (3 * p.stages + 5);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
-    float* db_part = reinterpret_cast<float*>(tail + 16);  // [8 row groups][256 channels]
+    // bias partials: written by the 8 bias warps (dba), read by them (dbb)
+    const uint32_t dba = smem_u32(tail + 16), dbb = smem_u32(tail + 24);
+    float* db_part = reinterpret_cast<float*>(tail + 32);  // [8 row groups][256 channels]
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int BK = kWpBK;
@@ -1306,6 +1308,8 @@ __global__ void __launch_bounds__(kWpThreads, 1)
         mbar_init(sm.tfull(0), 1);
         mbar_init(sm.tempty(0), 8);
         mbar_init(sm.drain(), 1);
+        mbar_init(dba, 8);
+        mbar_init(dbb, 8);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -1464,6 +1468,7 @@ __global__ void __launch_bounds__(kWpThreads, 1)
         const int chunk = cg >> 3, q = cg & 7;         // MN-major chunk, 16-byte group in its rows
         int s = 0;
         uint32_t ph = 0;
+        uint32_t nsum = 0;  // tiles summed so far (the phase of dba / dbb)
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             const int m2 = u / p.num_n_tiles, nt = u % p.num_n_tiles;
             const bool sum = p.db != nullptr && nt == 0;
@@ -1497,10 +1502,14 @@ __global__ void __launch_bounds__(kWpThreads, 1)
             }
             if (!ok) break;
             if (sum) {
-                // the 8 row groups' partial sums added in order, one channel per thread
+                // the 8 row groups' partial sums added in order, one channel per thread; the
+                // previous tile's readers are done with db_part first (dbb). Bounded waits.
+                if (nsum > 0 && !mbar_wait(dbb, (nsum - 1) & 1u, abort_flag)) break;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) db_part[rg * 256 + 8 * cg + e] = acc[e];
-                named_bar_sync(1, 256);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dba);
+                if (!mbar_wait(dba, nsum & 1u, abort_flag)) break;
                 const int c = dt;  // channel of the tile
                 float tot = 0.f;
 #pragma unroll
@@ -1514,7 +1523,9 @@ __global__ void __launch_bounds__(kWpThreads, 1)
                     const int64_t ch = (cc < 64 ? c0 : c1) + (cc & 63);
                     if (ch < p.out_rows) p.db[ch] = (uint16_t)(pack_bf16x2(tot, 0.f) & 0xFFFFu);
                 }
-                named_bar_sync(1, 256);  // db_part is rewritten by the next tile
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dbb);
+                ++nsum;
             }
         }
     }
