@@ -115,16 +115,20 @@ def test_bwd_canaries_untouched(cuda_device):
         assert (buf[:pad] == 9.0).all() and (buf[pad + n:] == 9.0).all()
 
 
-def test_bwd_position_out_of_range_reports_status(cuda_device):
-    w = synth.workload("tiny", T=64)
+@pytest.mark.parametrize("name,ov", [("tiny", dict(T=64)),                          # fused paths
+                                     ("dsv3_bwd", dict(T=300, H=4, seq_len=None))])  # pre-rotated dgrad, hand-off wgrad
+def test_bwd_position_out_of_range_reports_status(cuda_device, name, ov):
+    w = synth.workload(name, **ov)
     inp = synth.make_inputs(w, seed=7)
     inp["pos"] = inp["pos"].clone()
     inp["pos"][5] = -1
     d = helpers.to_dev(inp, cuda_device)
+    rope = torch.empty((w.T, w.H, w.Dr), dtype=torch.bfloat16, device=cuda_device)
     for which in ("dgrad", "wgrad"):
         st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
         if which == "dgrad":
-            mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
+            mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st,
+                           dq_pre_rope=rope)
         else:
             mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
         assert int(st.item()) == mlaq.STATUS["MLA_ERR_POS_RANGE"], which

@@ -115,3 +115,26 @@ def test_dgrad_paths_agree(cuda_device):
     for name, (dx, _) in outs.items():
         assert helpers.frob_rel(dx, ref) <= TOL, name
     assert helpers.frob_rel(outs["pre"][0], helpers.bf16_to_f64(outs["fused"][0])) <= 2e-3
+
+
+def test_handoff_wgrad_without_bias(cuda_device):
+    """The hand-off wgrad's bias warps share each stage's release with the
+    MMA: asking for no db gives the same dW bits and leaves db's buffer
+    alone."""
+    w = synth.workload("dsv3_bwd", T=300, H=4, seq_len=None)
+    inp = synth.make_inputs(w, seed=9)
+    d = helpers.to_dev(inp, cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    rope = torch.empty((w.T, w.H, w.Dr), dtype=torch.bfloat16, device=cuda_device)
+    mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st, dq_pre_rope=rope)
+    dW_b, db = mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st,
+                              dq_pre_rope=rope)
+    dW_n, none = mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st,
+                                dq_pre_rope=rope, db=None)
+    torch.cuda.synchronize()
+    mlaq.check_status(st)
+    assert none is None
+    assert torch.equal(dW_b, dW_n)
+    dqp = oracle.rope_bwd(helpers.f64(inp["dq"]), w.H, w.Dn, w.Dr, inp["cos"].numpy(), inp["sin"].numpy(),
+                          inp["pos"].numpy())
+    assert helpers.frob_rel(db, oracle.bgrad(dqp.reshape(w.T, -1))) <= TOL
