@@ -68,7 +68,6 @@ struct FwdParams {
                           // copy per 128-row chunk and K step instead of the per-row gather
     int sf_nsub;          // 128-row chunks of a B tile: ceil(BN / 128)
     int num_n_tiles;
-    int bm;               // token rows per tile: 128, or 256 for the plain GEMM
     uint32_t sf_stage;    // scale staging bytes per stage (MXFP8 weights)
     uint32_t sf_cols;     // TMEM scale-factor columns per stage
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
@@ -801,7 +800,6 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.Dn = a.Dn;
     p.BN = BN;
     const int bm = a.Dr == 0 ? 2 * kBM : kBM;  // the plain GEMM's 256-row tiles
-    p.bm = bm;
     p.num_m_tiles = (int)((a.T + bm - 1) / bm);
     p.num_n_tiles = (int)(N / BN);
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
