@@ -40,10 +40,6 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
     return cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);
 }
 
-__device__ __forceinline__ bool not_finite(float v) {
-    return (__float_as_uint(v) & 0x7F800000u) == 0x7F800000u;
-}
-
 // NaN code keeping the element's sign.
 __device__ __forceinline__ uint32_t nan_code(float v) {
     return 0x7Fu | ((__float_as_uint(v) >> 24) & 0x80u);
@@ -61,19 +57,28 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) {
     return __uint_as_float(packed & 0xFFFF0000u);
 }
 
+// max(m, |v|) that returns NaN when either input is NaN (so a block amax taken
+// with it is NaN or Inf exactly when the block holds a non-finite element;
+// for finite inputs it equals the largest magnitude).
+__device__ __forceinline__ float amax_nan(float m, float v) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(v)));
+    return r;
+}
+
 // Quantize n <= 32 fp32 values held by ONE thread (a whole block) into codes
 // (packed little-endian, 4 per word) and return the scale byte. Entries past
 // n are ignored for the amax and encoded anyway (callers do not store them).
-// The amax is taken on the magnitude bits as integers: for non-negative
-// floats the integer order is the float order, and any Inf/NaN magnitude is
-// >= 0x7F800000, so one max finds both the amax and a non-finite element.
+// The amax is a NaN-propagating float max of the magnitudes: its bits are
+// >= 0x7F800000 exactly when the block holds an Inf or a NaN.
 template <int NV>
 __device__ __forceinline__ uint32_t quantize_block_regs(const float (&v)[NV], int n,
                                                         uint32_t (&codes)[(NV + 3) / 4]) {
-    uint32_t mbits = 0;
+    float am = 0.f;
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-        if (i < n) mbits = max(mbits, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        if (i < n) am = amax_nan(am, v[i]);
+    const uint32_t mbits = __float_as_uint(am);
     if (mbits >= 0x7F800000u) {
 #pragma unroll
         for (int w = 0; w < (NV + 3) / 4; ++w) {
@@ -96,15 +101,6 @@ __device__ __forceinline__ uint32_t quantize_block_regs(const float (&v)[NV], in
         codes[w] = pack_e4m3x4(a, b, c, d);
     }
     return (uint32_t)(e + 127);
-}
-
-// max(m, |v|) that returns NaN when either input is NaN (so a block amax taken
-// with it is NaN or Inf exactly when the block holds a non-finite element;
-// for finite inputs it equals the largest magnitude).
-__device__ __forceinline__ float amax_nan(float m, float v) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(v)));
-    return r;
 }
 
 // A whole 32-element block held by one thread: the rule of

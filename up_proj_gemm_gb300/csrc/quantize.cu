@@ -95,19 +95,14 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quantize_kernel(const Tin* __r
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int64_t c0 = c_base + (int64_t)u * STEP + (int64_t)lane * E;
+            // NaN-propagating amax: Inf or NaN in the block leaves it non-finite;
+            // elements past C were loaded as 0 and cannot raise it
             float amax = 0.f;
-            uint32_t bad = 0;
 #pragma unroll
-            for (int j = 0; j < E; ++j) {
-                // elements past C were loaded as 0 and cannot raise the amax
-                bad |= not_finite(v[u][j]) ? 1u : 0u;
-                amax = fmaxf(amax, fabsf(v[u][j]));
-            }
+            for (int j = 0; j < E; ++j) amax = amax_nan(amax, v[u][j]);
 #pragma unroll
-            for (int off = 1; off < TPB; off <<= 1) {
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-                bad |= __shfl_xor_sync(0xffffffffu, bad, off);
-            }
+            for (int off = 1; off < TPB; off <<= 1) amax = amax_nan(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const bool bad = __float_as_uint(amax) >= 0x7F800000u;
             uint32_t w[E / 4];
             uint32_t sbyte;
             if (bad) {
@@ -354,8 +349,9 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
                         v[i] = __uint_as_float(lds_b32(a));
                     }
                 }
+                // rows past R were zero-filled by the loads: they leave the amax unchanged
                 uint32_t w[8];
-                const uint32_t sb = quantize_block_regs<32>(v, n, w);
+                const uint32_t sb = quantize_block32(v, w);
                 store_codes(codes + c * ldc + r0, w, n, VEC);
                 if (word_scales) sword |= sb << (8 * blk);
                 else scales[c * nbr + r0 / 32] = (uint8_t)sb;
