@@ -119,6 +119,7 @@ struct EpiCtx {
     const uint16_t* bias;  // the tile's bias (bf16, 16-byte aligned rows of 8), or null
     int cursor;       // next free slot (counts pieces; taken modulo nslots)
     int prev_pieces;  // pieces of the previous unit (its store may still read)
+    int prev2_pieces; // pieces of the unit before it
     int32_t t0;       // first token row of this warp's 32-row slab
     uint32_t sword;   // packed scale bytes of this row's half tile (split_half)
     int64_t sbase;    // first 32-channel block index of that half
@@ -153,7 +154,10 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
     const int lane = threadIdx.x & 31;
     // the slots about to be written were last read by stores older than the previous unit's
     if (lane == 0) {
-        if (c.prev_pieces + PIECES <= p.nslots) bulk_wait_group_read<1>();
+        // the stores of the last two units may still read their slots when those
+        // and this unit's fit in the ring together (ring positions never overlap)
+        if (c.prev2_pieces + c.prev_pieces + PIECES <= p.nslots) bulk_wait_group_read<2>();
+        else if (c.prev_pieces + PIECES <= p.nslots) bulk_wait_group_read<1>();
         else bulk_wait_group_read<0>();
     }
     __syncwarp();
@@ -198,6 +202,7 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
         bulk_commit_group();
     }
     c.cursor = first + PIECES;
+    c.prev2_pieces = c.prev_pieces;
     c.prev_pieces = PIECES;
 }
 
@@ -612,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ec.slots = sm.out + (uint32_t)(ew * p.nslots) * p.slot_bytes;
         ec.cursor = 0;
         ec.prev_pieces = 0;
+        ec.prev2_pieces = 0;
         const int half = ew >> 2;   // which of the tile's units this warp takes (alternating)
         int local = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
