@@ -385,6 +385,23 @@ MLAQ_API size_t mxfp8_swizzled_scale_bytes(int64_t rows, int64_t cols);
 MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t *in, int64_t ld_in,
                                   uint8_t *out, void *stream);
 
+/*
+ * Device self-test of the bounded pipeline waits behind MLA_ERR_TIMEOUT.
+ * The pages define no such operation. It checks the library's own contract:
+ * no device wait spins forever, and a wait that gives up is reported in the
+ * status word with the context still usable. One CTA of two roles, with the
+ * kernels' wait routine: role 0 waits on an mbarrier that only arrive != 0
+ * completes, role 1 on one that only role 0's success completes. With
+ * arrive == 0, role 0 gives up after limit_ns of %globaltimer and sets the
+ * CTA's abort flag, role 1 leaves through that flag, and MLA_ERR_TIMEOUT is
+ * written to *dev_status (if it held 0); with arrive != 0 nothing is
+ * written. No copy or MMA is in flight at any point. limit_ns in
+ * [1e6, 1e9] (else MLA_ERR_INVALID_ARG); dev_status: device int, 4-byte
+ * aligned, required. Asynchronous on the stream; the kernel ends within
+ * 2 * limit_ns of starting.
+ */
+MLAQ_API int mla_wait_selftest(int arrive, uint64_t limit_ns, int *dev_status, void *stream);
+
 /* which: 0 = forward, 1 = dgrad, 2 = wgrad, 3 = MXFP8 backward, 4 = the
  * least workspace dgrad accepts. Bytes of device workspace the call needs
  * for this shape (0 = pass NULL). Of the bf16 calls only dgrad ever needs

@@ -300,3 +300,12 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mlaq, "library_path", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no non-CUDA fallback"):
         mlaq.lib()
+
+
+def test_wait_selftest_rejects(L):
+    """mla_wait_selftest checks its arguments before any launch."""
+    bad = S["MLA_ERR_INVALID_ARG"]
+    assert L.mla_wait_selftest(0, 50_000_000, None, None) == bad            # status required
+    assert L.mla_wait_selftest(0, 50_000_000, ctypes.c_void_p(FAKE + 2), None) == bad  # misaligned
+    assert L.mla_wait_selftest(0, 999_999, p(0), None) == bad               # limit below 1 ms
+    assert L.mla_wait_selftest(1, 1_000_000_001, p(0), None) == bad         # limit above 1 s

@@ -83,6 +83,7 @@ _SIGS = {
     "mla_q_uproj_bwd_mxfp8_layout": (_int, [ctypes.POINTER(Shape), ctypes.POINTER(Mxfp8BwdLayout)]),
     "mxfp8_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
+    "mla_wait_selftest": (_int, [_int, ctypes.c_uint64, _vp, _vp]),
     "mla_status_string": (ctypes.c_char_p, [_int]),
     "mla_version": (_int, []),
 }
@@ -104,6 +105,15 @@ def lib() -> ctypes.CDLL:
                 f.argtypes = args
             _lib = l
     return _lib
+
+
+def wait_selftest(arrive: bool, limit_ms: float, status: torch.Tensor, stream=None) -> None:
+    """Run the bounded-wait self-test (mla_wait_selftest) on the status
+    tensor's device: with arrive=False a device wait gives up after limit_ms
+    and MLA_ERR_TIMEOUT lands in ``status``; with arrive=True nothing does."""
+    _need(status, "status", torch.int32)
+    _call(lib().mla_wait_selftest, "mla_wait_selftest", int(bool(arrive)), int(round(limit_ms * 1e6)),
+          _ptr(status), _stream(status.device, stream))
 
 
 def status_string(code: int) -> str:
