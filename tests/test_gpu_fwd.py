@@ -24,6 +24,9 @@ SHAPES = [
     ("tiny", dict(T=129, K=64, H=16, Dn=64, Dr=32, w_std=0.1)),
     ("dsv3_fwd_bf16w", dict(T=300, H=8)),                 # 256-wide tiles cut heads at 64/128
     ("dsv3_fwd_bf16w", dict(T=260, K=1000, H=3, bias=True)),
+    ("dsv3_fwd_bf16w", dict(T=513, H=2, K=256, bias=True)),   # ragged last token tile, bias
+    ("dsv3_fwd_bf16w", dict(T=100, H=6, Dn=64, K=128)),       # D = 128: rope regions at channel 64 mod 128
+    ("tiny", dict(T=1, K=64, H=4, Dn=64, Dr=32)),             # single token, Dr = 32
 ]
 
 
@@ -82,16 +85,22 @@ def test_fwd_inputs_unchanged(cuda_device):
         assert torch.equal(inp[k], v), k
 
 
-def test_fwd_writes_nothing_outside_outputs(cuda_device):
+# a Dr = 16 shape and a DeepSeek-V3 head shape (Dr = 64)
+KERNELS = [("tiny", {}), ("dsv3_fwd_bf16w", dict(K=128, H=2, bias=True))]
+
+
+@pytest.mark.parametrize("name,ov", KERNELS)
+def test_fwd_writes_nothing_outside_outputs(cuda_device, name, ov):
     """Canary bytes around q and its scales stay untouched."""
-    w = synth.workload("tiny", T=130)
+    w = synth.workload(name, **dict(ov, T=130))
     inp = helpers.to_dev(synth.make_inputs(w, seed=4), cuda_device)
     pad = 4096
-    nq, ns = w.T * w.H * w.D, w.T * w.H * 2
+    nb = (w.D + 31) // 32
+    nq, ns = w.T * w.H * w.D, w.T * w.H * nb
     qbuf = torch.full((nq + 2 * pad,), 0xA5, dtype=torch.uint8, device=cuda_device)
     sbuf = torch.full((ns + 2 * pad,), 0x5A, dtype=torch.uint8, device=cuda_device)
     q = qbuf[pad:pad + nq].view(w.T, w.H, w.D)
-    s = sbuf[pad:pad + ns].view(w.T, w.H, 2)
+    s = sbuf[pad:pad + ns].view(w.T, w.H, nb)
     mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"],
              pos=inp["pos"], out_mode="mxfp8", q_out=q, q_scales=s)
     torch.cuda.synchronize()
@@ -99,8 +108,9 @@ def test_fwd_writes_nothing_outside_outputs(cuda_device):
     assert (sbuf[:pad] == 0x5A).all() and (sbuf[pad + ns:] == 0x5A).all()
 
 
-def test_fwd_position_out_of_range_reports_status(cuda_device):
-    w = synth.workload("tiny", T=64)
+@pytest.mark.parametrize("name,ov", KERNELS)
+def test_fwd_position_out_of_range_reports_status(cuda_device, name, ov):
+    w = synth.workload(name, **dict(ov, T=64))
     inp = synth.make_inputs(w, seed=5)
     inp["pos"] = inp["pos"].clone()
     inp["pos"][7] = w.cs_rows + 3  # outside the table: reported, never read
@@ -109,11 +119,12 @@ def test_fwd_position_out_of_range_reports_status(cuda_device):
     assert int(st.item()) == mlaq.STATUS["MLA_ERR_POS_RANGE"]
 
 
-def test_fwd_wide_table_and_packed_positions(cuda_device):
+@pytest.mark.parametrize("name,ov", KERNELS)
+def test_fwd_wide_table_and_packed_positions(cuda_device, name, ov):
     """cs_width > Dr (row pitch = cs_width) and positions restarting per sequence."""
-    w = synth.workload("tiny", T=256, seq_len=100)
+    w = synth.workload(name, **dict(ov, T=256, seq_len=100))
     inp = synth.make_inputs(w, seed=6)
-    cos, sin = synth.rope_table_standard(100, 24)  # 24 columns, Dr = 16 reads the first 16
+    cos, sin = synth.rope_table_standard(100, w.Dr + 8)  # the kernel reads the first Dr columns
     inp["cos"], inp["sin"] = cos, sin
     q = _run(w, inp, cuda_device, "bf16")
     ref = helpers.oracle_forward(inp, w)
@@ -142,3 +153,41 @@ def test_fwd_full_size_sampled(cuda_device, out_mode):
         q_ref = helpers.oracle_forward(inp, w, tokens=tokens)
         idx = torch.from_numpy(tokens).to(cuda_device)
         helpers.check_bf16_close(out[idx], q_ref)
+
+
+@pytest.mark.parametrize("name,ov", KERNELS)
+def test_fwd_nonfinite_blocks(cuda_device, name, ov):
+    """An Inf weight element makes its channel non-finite for every token (and,
+    through the rotation, its rope partner). Every MXFP8 block holding a
+    non-finite value gets scale 0xFF and NaN codes (0x7F with the element's
+    sign); the other blocks are unaffected. The oracle decides which blocks."""
+    w = synth.workload(name, **dict(ov, T=150))
+    inp = synth.make_inputs(w, seed=9)
+    W = inp["W"].clone()
+    W[w.Dn + 3, 5] = float("inf")            # a rope channel of head 0
+    W[w.D + min(w.Dn - 1, 40), 2] = float("-inf")  # a pass-through channel of head 1
+    inp["W"] = W
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    codes, scales = _run(w, inp, cuda_device, "mxfp8", st)
+    mlaq.check_status(st)
+    codes, scales = codes.cpu().numpy(), scales.cpu().numpy()
+    q_ref, rc, rs = helpers.oracle_forward(inp, w, quantize=True)
+    bad = rs == 0xFF
+    assert bad.any() and (~bad).any()
+    assert np.array_equal(scales == 0xFF, bad)
+    nb = rs.shape[2]
+    bad_el = np.repeat(bad, 32, axis=2)[:, :, :w.D]
+    assert ((codes[bad_el] & 0x7F) == 0x7F).all()
+    # finite elements of those blocks keep their sign
+    fin = bad_el & np.isfinite(q_ref) & (np.abs(q_ref) > 1e-6)
+    assert np.array_equal(codes[fin] >> 7, (q_ref[fin] < 0).astype(np.uint8))
+    # every other block as usual: scales as the oracle's (>= 99.9%), elements
+    # within one E4M3 step of the reference
+    ok_blk = ~bad
+    assert (scales[ok_blk] == rs[ok_blk]).mean() >= 0.999
+    e_el = np.repeat(scales.astype(np.int64) - 127, 32, axis=2)[:, :, :w.D].astype(np.float64)
+    ok_el = ~bad_el
+    deq = helpers.e4m3_lut()[codes[ok_el]] * np.exp2(e_el[ok_el])
+    tol = helpers.ulp_e4m3(np.abs(q_ref[ok_el]) * np.exp2(-e_el[ok_el])) * np.exp2(e_el[ok_el])
+    assert (np.abs(deq - q_ref[ok_el]) <= tol).all()
+    assert nb == (w.D + 31) // 32

@@ -24,6 +24,8 @@ SHAPES = [
     ("tiny", dict(T=77, K=256, H=6)),                         # BN 96 (2 heads), ragged tokens
     ("dsv3_fwd_mxfp8w", dict(T=260, H=4)),                    # one head per 192-wide tile
     ("dsv3_fwd_mxfp8w", dict(T=140, H=2, K=1024, bias=True)),
+    ("dsv3_fwd_mxfp8w", dict(T=200, H=3, K=256)),
+    ("tiny", dict(T=450, K=256, H=4, Dn=64, Dr=32)),          # Dr = 32, 4 token tiles (ragged)
 ]
 
 
