@@ -73,7 +73,7 @@ enum {
 /* weight_mode */
 enum { MLA_WEIGHT_BF16 = 0, MLA_WEIGHT_MXFP8 = 1 };
 /* out_mode */
-enum { MLA_OUT_BF16 = 0, MLA_OUT_MXFP8 = 1, MLA_OUT_MXFP8_BHSD = 2 };
+enum { MLA_OUT_BF16 = 0, MLA_OUT_MXFP8 = 1, MLA_OUT_MXFP8_BHSD = 2, MLA_OUT_MXFP8_BHSD_SWIZZLED = 3 };
 /* in_dtype of mxfp8_quantize_rows */
 enum { MLA_IN_F32 = 0, MLA_IN_BF16 = 1 };
 
@@ -130,6 +130,16 @@ typedef struct {
  *               order an attention kernel reading one head at a time wants;
  *               TransformerEngine PR "Add support for fused Q Up-Proj
  *               GEMM/RoPE/Quant", review thread: the BHSD scale transpose).
+ *   out_mode MLA_OUT_MXFP8_BHSD_SWIZZLED: the same codes; each head's
+ *               scales [T, ceil(D/32)] leave the epilogue already in the
+ *               tiled order a block-scaled GEMM reads, i.e. the layout
+ *               mxfp8_swizzle_scales gives that head's matrix. Head h takes
+ *               bytes [h * S, (h + 1) * S), S = mxfp8_swizzled_scale_bytes(T,
+ *               ceil(D/32)); the padding of the last row tile (rows T ..)
+ *               and of the last column tile is written as 0. This fuses
+ *               into the forward the step that the same PR's flowchart puts
+ *               between the quantized query and the fused attention: scales
+ *               moved to head-major order and tiled for the GEMM.
  * Tiling limits (else MLA_ERR_UNSUPPORTED): Dr in {16, 32, 64}, Dn % 32 == 0;
  * bf16 weights need K % 8 == 0 (16-byte rows). Pointers must be 16-byte
  * aligned (scales: 4-byte; bias: 16-byte), else MLA_ERR_ALIGNMENT.

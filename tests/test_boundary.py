@@ -197,9 +197,20 @@ def test_swizzle_rejects(L):
     assert z(10, 4, p(0), 4, p(0), None) == S["MLA_ERR_ALIAS"]
 
 
-def test_fwd_accepts_bhsd_scale_mode(L):
+def test_fwd_accepts_bhsd_scale_modes(L):
     assert fwd(L, shape(), om=2, qs=p(9)) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
-    assert fwd(L, shape(), om=3, qs=p(9)) == S["MLA_ERR_INVALID_ARG"]
+    assert fwd(L, shape(), om=3, qs=p(9)) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert fwd(L, shape(), om=4, qs=p(9)) == S["MLA_ERR_INVALID_ARG"]
+
+
+def test_fwd_swizzled_scales_extent_in_alias_check(L):
+    """With swizzled scales q_scales_out spans H tiles of 128 rows per head
+    (here 4 x 1024 bytes, against 2048 for the dense [T, H, 2] order): a
+    buffer ending 3072 bytes before cos overlaps it only in the swizzled mode."""
+    assert L.mxfp8_swizzled_scale_bytes(256, 2) == 1024
+    qs = ctypes.c_void_p(FAKE * 3 - 3072)  # cos is at FAKE * 3
+    assert fwd(L, shape(), om=1, qs=qs) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert fwd(L, shape(), om=3, qs=qs) == S["MLA_ERR_ALIAS"]
 
 
 def _kv(L, T=256, K=64, H=4, Dn=32, Dv=32, Dr=16, cs_rows=256, cs_width=16, c=p(0), W=p(1), kp=p(2),

@@ -32,6 +32,33 @@ def test_bhsd_scales_are_the_head_major_transpose(cuda_device, name, ov):
     assert torch.equal(sc_h, sc.transpose(0, 1).contiguous())
 
 
+@pytest.mark.parametrize("name,ov", [("tiny", dict(T=130)), ("dsv3_fwd_bf16w", dict(T=300, H=6, bias=True)),
+                                     ("dsv3_fwd_bf16w", dict(T=256, H=2, K=128))])
+def test_swizzled_bhsd_scales_from_the_epilogue(cuda_device, name, ov):
+    """out_mode mxfp8_bhsd_swizzled: the same codes as the other MXFP8 modes,
+    and each head's [T, ceil(D/32)] scales in the GEMM's tiled order, i.e.
+    the oracle's swizzle of the head-major scales, head after head, with the
+    padding rows and columns written as 0 (the buffer starts filled with
+    0xEE)."""
+    w = synth.workload(name, **ov)
+    d = helpers.to_dev(synth.make_inputs(w, seed=32), cuda_device)
+    args = (d["x"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr)
+    kw = dict(bias=d.get("b"), pos=d["pos"])
+    codes_h, sc_h = mlaq.fwd(*args, out_mode="mxfp8_bhsd", **kw)
+    nb = (w.D + 31) // 32
+    per_head = int(mlaq.lib().mxfp8_swizzled_scale_bytes(w.T, nb))
+    assert per_head == -(-w.T // 128) * 128 * -(-nb // 4) * 4
+    buf = torch.full((w.H, per_head), 0xEE, dtype=torch.uint8, device=cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    codes_s, sc_s = mlaq.fwd(*args, out_mode="mxfp8_bhsd_swizzled", q_scales=buf, status=st, **kw)
+    mlaq.check_status(st)
+    assert sc_s.data_ptr() == buf.data_ptr()
+    assert torch.equal(codes_s, codes_h)
+    sc_h, sc_s = sc_h.cpu().numpy(), sc_s.cpu().numpy()
+    for h in range(w.H):
+        assert np.array_equal(sc_s[h], oracle.mxfp8_swizzle_scales(sc_h[h])), h
+
+
 @pytest.mark.parametrize("rows,cols", [(1, 1), (37, 3), (128, 4), (300, 9), (4096 * 128, 6)])
 def test_swizzle_matches_oracle(cuda_device, rows, cols):
     g = torch.Generator().manual_seed(rows + cols)

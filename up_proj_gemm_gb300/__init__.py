@@ -35,7 +35,7 @@ STATUS = {
     "MLA_ERR_POS_RANGE": 8, "MLA_ERR_WORKSPACE": 9,
 }
 WEIGHT_MODES = {"bf16": 0, "mxfp8": 1}
-OUT_MODES = {"bf16": 0, "mxfp8": 1, "mxfp8_bhsd": 2}
+OUT_MODES = {"bf16": 0, "mxfp8": 1, "mxfp8_bhsd": 2, "mxfp8_bhsd_swizzled": 3}
 
 
 class Shape(ctypes.Structure):
@@ -172,7 +172,9 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
         x_scales=None, w_scales=None, q_out=None, q_scales=None, status=None, stream=None):
     """Fused forward. Returns q [T, H, D] (bf16 or uint8 E4M3 codes), plus the
     scales uint8 [T, H, ceil(D/32)] when out_mode is "mxfp8", or head-major
-    [H, T, ceil(D/32)] when it is "mxfp8_bhsd".
+    [H, T, ceil(D/32)] when it is "mxfp8_bhsd", or [H, S] when it is
+    "mxfp8_bhsd_swizzled": each head's scales in the block-scaled GEMM's
+    tiled order (S = mxfp8_swizzled_scale_bytes(T, ceil(D/32)))
 
     weight_mode "bf16": x [T, K] bf16, W [N, K] bf16.
     weight_mode "mxfp8": x, W uint8 E4M3 codes with x_scales [T, K/32],
@@ -201,7 +203,13 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
     if q_out is None:
         q_out = torch.empty((T, H, D), dtype=torch.uint8 if om else torch.bfloat16, device=dev)
     if om and q_scales is None:
-        sshape = (H, T, (D + 31) // 32) if out_mode == "mxfp8_bhsd" else (T, H, (D + 31) // 32)
+        nb = (D + 31) // 32
+        if out_mode == "mxfp8_bhsd_swizzled":
+            sshape = (H, int(lib().mxfp8_swizzled_scale_bytes(T, nb)))
+        elif out_mode == "mxfp8_bhsd":
+            sshape = (H, T, nb)
+        else:
+            sshape = (T, H, nb)
         q_scales = torch.empty(sshape, dtype=torch.uint8, device=dev)
     s = _shape(T, K, H, Dn, Dr, cos)
     _call(lib().mla_q_uproj_fwd, "mla_q_uproj_fwd", ctypes.byref(s), wm, om, _ptr(x),

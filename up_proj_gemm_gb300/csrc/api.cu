@@ -229,7 +229,8 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
     if (st != MLA_OK) return st;
     const mla_q_shape& s = *shape;
     if (weight_mode != MLA_WEIGHT_BF16 && weight_mode != MLA_WEIGHT_MXFP8) return MLA_ERR_INVALID_ARG;
-    if (out_mode != MLA_OUT_BF16 && out_mode != MLA_OUT_MXFP8 && out_mode != MLA_OUT_MXFP8_BHSD)
+    if (out_mode != MLA_OUT_BF16 && out_mode != MLA_OUT_MXFP8 && out_mode != MLA_OUT_MXFP8_BHSD &&
+        out_mode != MLA_OUT_MXFP8_BHSD_SWIZZLED)
         return MLA_ERR_INVALID_ARG;
     const bool mxw = weight_mode == MLA_WEIGHT_MXFP8, mxo = out_mode != MLA_OUT_BF16;
     if (mxw != (x_scales != nullptr) || mxw != (w_scales != nullptr)) return MLA_ERR_INVALID_ARG;
@@ -253,7 +254,10 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
 
     const int64_t NB = (D + 31) / 32;
     const int64_t table = s.cs_rows * s.cs_width * 4;
-    const Range outs[] = {rng(q_out, s.T * N * (mxo ? 1 : 2)), rng(q_scales_out, s.T * s.H * NB),
+    const int64_t qs_bytes = out_mode == MLA_OUT_MXFP8_BHSD_SWIZZLED
+                                 ? (int64_t)s.H * (int64_t)mxfp8_swizzled_scale_bytes(s.T, NB)
+                                 : s.T * s.H * NB;
+    const Range outs[] = {rng(q_out, s.T * N * (mxo ? 1 : 2)), rng(q_scales_out, qs_bytes),
                           rng(dev_status, 4)};
     const Range ins[] = {rng(x, s.T * s.K * esz), rng(x_scales, s.T * (s.K / 32)),
                          rng(W, N * s.K * esz),   rng(w_scales, N * (s.K / 32)),

@@ -64,6 +64,9 @@ struct FwdParams {
     int cs_vec;           // cos/sin rows 16-byte aligned: float4 loads
     int nslots;           // staging slots per epilogue warp
     int scales_bhsd;      // MXFP8 scales head-major [H, T, NB] (else [T, H, NB])
+    int qs_swz;           // MXFP8 scales per head in the GEMM's tiled order
+    int qs_row_tiles;     //   128-row tiles per head: ceil(T / 128)
+    int qs_col_tiles;     //   4-column tiles: ceil(NB / 4)
     int sf_tiled;         // MXFP8 scales pre-tiled (sf_tiled_offset order): one 512-byte bulk
                           // copy per 128-row chunk and K step instead of the per-row gather
     int sf_nsub;          // 128-row chunks of a B tile: ceil(BN / 128)
@@ -176,9 +179,20 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
             if (nvalid > 16)
                 sts_v4(slot_addr(p, c, first + 2 * blk + 1) + 16u * lane, codes[4], codes[5], codes[6],
                        codes[7]);
-            if (p.split_half)
+            if (p.split_half) {
                 c.sword |= sb << (8 * (int)((n + 32 * blk) / 32 - c.sbase));
-            else if (valid)
+            } else if (p.qs_swz) {
+                // head h's [T, NB] scales in the GEMM's tiled order: 128-row x
+                // 4-column tiles of 512 bytes. Rows t >= T of the last row tile
+                // (these threads exist: token tiles are 128 rows) and the
+                // columns past NB are padding, written as 0.
+                const int bc = (cin + blk * 32) / 32;
+                const int64_t rt = ((int64_t)h * p.qs_row_tiles + t / 128) * p.qs_col_tiles;
+                const uint32_t rr = (uint32_t)(t % 32) * 16u + (uint32_t)((t % 128) / 32) * 4u;
+                p.q_scales[(rt + bc / 4) * 512 + rr + bc % 4] = valid ? (uint8_t)sb : (uint8_t)0;
+                if (bc == NB - 1)
+                    for (int pc = NB; pc < 4 * p.qs_col_tiles; ++pc) p.q_scales[(rt + pc / 4) * 512 + rr + pc % 4] = 0;
+            } else if (valid)
                 p.q_scales[(p.scales_bhsd ? (int64_t)h * p.T + t : t * p.H + h) * NB + (cin + blk * 32) / 32] =
                     (uint8_t)sb;
         }
@@ -837,9 +851,12 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
                (reinterpret_cast<uintptr_t>(a.sin_tab) % 16 == 0);
     const bool mxo = a.out_mode != MLA_OUT_BF16;
     p.scales_bhsd = a.out_mode == MLA_OUT_MXFP8_BHSD;
+    p.qs_swz = a.out_mode == MLA_OUT_MXFP8_BHSD_SWIZZLED;
+    p.qs_row_tiles = (int)((a.T + 127) / 128);
+    p.qs_col_tiles = (D / 32 + (D % 32 ? 1 : 0) + 3) / 4;
     p.slot_bytes = 32u * kSlotCh * (mxo ? 1u : 2u);
     p.nslots = mxo ? 8 : 4;  // a unit takes at most 4 slots (64 rope channels)
-    p.split_half = mxo && !p.scales_bhsd && D % 32 == 0 && BN % 128 == 0 && N % 128 == 0 &&
+    p.split_half = mxo && !p.scales_bhsd && !p.qs_swz && D % 32 == 0 && BN % 128 == 0 && N % 128 == 0 &&
                    reinterpret_cast<uintptr_t>(a.q_scales) % 4 == 0 &&
                    fwd_tile_n(N, D, a.Dn, a.Dr, BN / 2, BN / 2) == BN / 2;
 
