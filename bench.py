@@ -545,7 +545,16 @@ def run_parts(dev, stream, flush, pk, pk_src):
     tf = w.fwd_flop() / (ms * 1e-3) / 1e12
     parts["fwd_bf16w_mxfp8out_T4096_alone"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                                "frac_bf16_peak": round(tf / bf16_peak, 4)}
-    del inp, xq, xs, Wq, Ws, qc, qs
+    # the same forward writing its scales per head in the block-scaled GEMM's tiled order
+    qsw = torch.empty((w.H, int(mlaq.lib().mxfp8_swizzled_scale_bytes(w.T, (w.D + 31) // 32))),
+                      dtype=torch.uint8, device=dev)
+    ms = time_loop(lambda: mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
+                                    pos=inp["pos"], out_mode="mxfp8_bhsd_swizzled", q_out=qc, q_scales=qsw,
+                                    status=st), 30, flush, stream)
+    tf = w.fwd_flop() / (ms * 1e-3) / 1e12
+    parts["fwd_bf16w_mxfp8out_swizzled_scales_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                                                         "frac_bf16_peak": round(tf / bf16_peak, 4)}
+    del inp, xq, xs, Wq, Ws, qc, qs, qsw
 
     # backward at T = 2 x 4096, bias on
     w = synth.workload("dsv3_bwd")

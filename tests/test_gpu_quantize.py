@@ -91,6 +91,28 @@ def test_quantize_full_size_bit_exact(cuda_device):
     assert np.array_equal(codes, rc)
 
 
+def test_quantize_weight_shape_bit_exact(cuda_device):
+    """[24576, 1536] bf16 (the projection weight quantized for the MXFP8
+    weight path, a benchmarked shape), all elements."""
+    x = synth.normal_bf16((24576, 1536), 0.02, 22)
+    codes, scales = _run(x.to(cuda_device))
+    rc, rs = _oracle(x)
+    assert np.array_equal(scales, rs)
+    assert np.array_equal(codes, rc)
+
+
+def test_quantize_long_context_shape_sampled(cuda_device):
+    """[16384, 24576] bf16 (the long-context q shape, a benchmarked shape):
+    every row-block of 128 rows checked on one sampled row, plus the last row."""
+    g = torch.Generator().manual_seed(23)
+    xd = (torch.randn((16384, 24576), generator=g) * 1.0).to(torch.bfloat16)
+    codes, scales = _run(xd.to(cuda_device))
+    rows = np.concatenate([np.arange(0, 16384, 128) + np.random.default_rng(4).integers(0, 128, 128), [16383]])
+    rc, rs = _oracle(xd[torch.from_numpy(rows)])
+    assert np.array_equal(scales[rows], rs)
+    assert np.array_equal(codes[rows], rc)
+
+
 def test_quantize_does_not_touch_input(cuda_device):
     x = synth.normal_bf16((300, 1000), 1.0, 8).to(cuda_device)
     before = x.clone()
