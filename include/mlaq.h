@@ -71,7 +71,7 @@ enum {
 };
 
 /* weight_mode */
-enum { MLA_WEIGHT_BF16 = 0, MLA_WEIGHT_MXFP8 = 1 };
+enum { MLA_WEIGHT_BF16 = 0, MLA_WEIGHT_MXFP8 = 1, MLA_WEIGHT_MXFP8_TILED = 2 };
 /* out_mode */
 enum { MLA_OUT_BF16 = 0, MLA_OUT_MXFP8 = 1, MLA_OUT_MXFP8_BHSD = 2, MLA_OUT_MXFP8_BHSD_SWIZZLED = 3 };
 /* in_dtype of mxfp8_quantize_rows */
@@ -112,6 +112,17 @@ typedef struct {
  *               [N, K/32]: value = e4m3(code) * 2^(scale - 127), blocks of 32
  *               along K (the layout mxfp8_quantize_rows writes).
  *               Requires K % 128 == 0.
+ *   weight_mode MLA_WEIGHT_MXFP8_TILED: the same codes, with both scale
+ *               tensors already in the tiled order the block-scaled GEMM reads,
+ *               so they arrive by bulk copies instead of a per-row gather (the
+ *               same outputs, bit for bit, in less time):
+ *               x_scales = mxfp8_swizzle_scales of the [T, K/32] scales
+ *               (mxfp8_swizzled_scale_bytes(T, K/32) bytes); w_scales =
+ *               mxfp8_swizzle_scales_grouped of the [N, K/32] scales with
+ *               group = mla_q_uproj_w_scale_group(shape) (the kernel's
+ *               channel tile; mxfp8_grouped_scale_bytes(N, K/32, group)
+ *               bytes). W is a weight: its tiled scales are prepared once.
+ *               Both 16-byte aligned.
  *   bias        [N] bf16 or NULL (added before the rotation).
  *   cos_tab, sin_tab [cs_rows, cs_width] fp32.
  *   pos         [T] int32 positions, or NULL for pos[t] = t (then
@@ -411,6 +422,26 @@ MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t *in,
  * 2 * limit_ns of starting.
  */
 MLAQ_API int mla_wait_selftest(int arrive, uint64_t limit_ns, int *dev_status, void *stream);
+
+/*
+ * Row-group variant of mxfp8_swizzle_scales: rows in groups of `group`, each
+ * group padded to whole 128-row tiles (so a GEMM tile of `group` rows starts
+ * at a tile boundary). Chunk i of group g and column tile j is the 512-byte
+ * tile ((g * ceil(group/128) + i) * ceil(cols/4) + j); inside it the byte
+ * order of mxfp8_swizzle_scales; padding bytes 0. group = 128 is
+ * mxfp8_swizzle_scales. out: mxfp8_grouped_scale_bytes(rows, cols, group)
+ * bytes, 16-byte aligned. A pure byte permutation (TransformerEngine PR "Add
+ * support for fused Q Up-Proj GEMM/RoPE/Quant": the GEMM scale swizzle among
+ * its MXFP8 helpers), used to tile W's scales for MLA_WEIGHT_MXFP8_TILED.
+ */
+MLAQ_API size_t mxfp8_grouped_scale_bytes(int64_t rows, int64_t cols, int64_t group);
+MLAQ_API int mxfp8_swizzle_scales_grouped(int64_t rows, int64_t cols, int64_t group, const uint8_t *in,
+                                          int64_t ld_in, uint8_t *out, void *stream);
+
+/* The row group of W's tiled scales for MLA_WEIGHT_MXFP8_TILED at this shape
+ * (the forward's channel tile with MXFP8 weights), or 0 when the shape is
+ * invalid or not tiled. */
+MLAQ_API int64_t mla_q_uproj_w_scale_group(const mla_q_shape *shape);
 
 /* which: 0 = forward, 1 = dgrad, 2 = wgrad, 3 = MXFP8 backward, 4 = the
  * least workspace dgrad accepts. Bytes of device workspace the call needs

@@ -320,3 +320,38 @@ def test_wait_selftest_rejects(L):
     assert L.mla_wait_selftest(0, 50_000_000, ctypes.c_void_p(FAKE + 2), None) == bad  # misaligned
     assert L.mla_wait_selftest(0, 999_999, p(0), None) == bad               # limit below 1 ms
     assert L.mla_wait_selftest(1, 1_000_000_001, p(0), None) == bad         # limit above 1 s
+
+
+def test_w_scale_group_and_grouped_bytes(L):
+    """The W scale group for MLA_WEIGHT_MXFP8_TILED is the forward's channel
+    tile with MXFP8 weights: 192 (one head) at the DeepSeek-V3 shape."""
+    assert L.mla_q_uproj_w_scale_group(ctypes.byref(shape(T=4096, K=1536, H=128, Dn=128, Dr=64,
+                                                          cs_rows=4096, cs_width=64))) == 192
+    assert L.mla_q_uproj_w_scale_group(ctypes.byref(shape())) == 192   # 4 heads of 48
+    assert L.mla_q_uproj_w_scale_group(ctypes.byref(shape(Dr=3))) == 0
+    gb = L.mxfp8_grouped_scale_bytes
+    assert gb(300, 48, 192) == 2 * 2 * 12 * 512          # 2 groups x 2 row tiles x 12 column tiles
+    assert gb(300, 48, 128) == L.mxfp8_swizzled_scale_bytes(300, 48)
+    assert gb(0, 48, 192) == 0 and gb(10, 48, 0) == 0
+    z = L.mxfp8_swizzle_scales_grouped
+    assert z(10, 4, 0, p(0), 4, p(1), None) == S["MLA_ERR_INVALID_ARG"]
+    assert z(10, 4, 96, p(0), 2, p(1), None) == S["MLA_ERR_INVALID_ARG"]
+    assert z(10, 4, 96, p(0), 4, ctypes.c_void_p(FAKE * 2 + 8), None) == S["MLA_ERR_ALIGNMENT"]
+    assert z(0, 4, 96, None, 4, None, None) == S["MLA_OK"]
+
+
+def test_fwd_tiled_scales_checks(L):
+    """weight_mode MLA_WEIGHT_MXFP8_TILED: scales required, 16-byte aligned,
+    and their tiled extents enter the overlap check."""
+    s = shape(K=128)
+    mx = dict(wm=2, xs=p(6), ws=p(7))
+    assert fwd(L, s, **mx) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert fwd(L, s, wm=2, xs=None, ws=p(7)) == S["MLA_ERR_INVALID_ARG"]
+    assert fwd(L, s, wm=2, xs=ctypes.c_void_p(FAKE * 7 + 4), ws=p(7)) == S["MLA_ERR_ALIGNMENT"]
+    assert fwd(L, s, wm=3, xs=p(6), ws=p(7)) == S["MLA_ERR_INVALID_ARG"]
+    # W's tiled scales: 192 rows -> 1 group x 2 row tiles x 1 column tile = 1024 bytes, against
+    # 192 x 4 = 768 dense: a buffer starting 896 bytes before q overlaps it only when tiled
+    assert L.mxfp8_grouped_scale_bytes(192, 4, 192) == 1024
+    ws = ctypes.c_void_p(FAKE * 5 - 896)  # q is at FAKE * 5
+    assert fwd(L, s, wm=1, xs=p(6), ws=ws) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert fwd(L, s, wm=2, xs=p(6), ws=ws) == S["MLA_ERR_ALIAS"]

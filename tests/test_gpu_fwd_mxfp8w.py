@@ -92,3 +92,52 @@ def test_fwd_mxfp8_weights_full_size_sampled(cuda_device):
     q_bf = helpers.oracle_forward(inp, w, tokens=toks)
     rel = np.linalg.norm(q_ref - q_bf) / np.linalg.norm(q_bf)
     assert rel < 0.1
+
+
+def _tiled_scales(xsc, Wsc, w):
+    """The two scale tensors in the GEMM's tiled order (x: 128-row groups;
+    W: groups of the kernel's channel tile, from the library's query)."""
+    G = mlaq.w_scale_group(w.T, w.K, w.H, w.Dn, w.Dr, w.cs_rows, w.Dr)
+    assert G > 0
+    return mlaq.mxfp8_swizzle_scales(xsc), mlaq.mxfp8_swizzle_scales(Wsc, group=G)
+
+
+@pytest.mark.parametrize("name,ov", SHAPES)
+def test_fwd_tiled_scales_bit_identical(cuda_device, name, ov):
+    """weight_mode mxfp8_tiled (scales pre-tiled, fetched by bulk copies) gives
+    exactly the outputs of weight_mode mxfp8 (per-row scale gather), which
+    test_fwd_mxfp8_weights checks against the oracle."""
+    w = synth.workload(name, **ov)
+    inp = synth.make_inputs(w, seed=4)
+    d = helpers.to_dev(inp, cuda_device)
+    xq, xsc = mlaq.mxfp8_quantize_rows(d["x"])
+    Wq, Wsc = mlaq.mxfp8_quantize_rows(d["W"])
+    xst, Wst = _tiled_scales(xsc, Wsc, w)
+    args = (xq, Wq, d["cos"], d["sin"], w.H, w.Dn, w.Dr)
+    kw = dict(bias=d.get("b"), pos=d["pos"], out_mode="mxfp8")
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    c1, s1 = mlaq.fwd(*args, weight_mode="mxfp8", x_scales=xsc, w_scales=Wsc, status=st, **kw)
+    c2, s2 = mlaq.fwd(*args, weight_mode="mxfp8_tiled", x_scales=xst, w_scales=Wst, status=st, **kw)
+    mlaq.check_status(st)
+    assert torch.equal(c1, c2) and torch.equal(s1, s2)
+
+
+def test_fwd_tiled_scales_full_size(cuda_device):
+    """The DeepSeek-V3 MXFP8-weight configuration (T = 4096, 1% x outliers
+    x50) as the benchmark runs it: tiled and gathered scales give the same
+    bytes, and sampled tokens match the oracle on the dequantized operands."""
+    w = synth.workload("dsv3_fwd_mxfp8w")
+    inp = synth.make_inputs(w, seed=6)
+    d = helpers.to_dev(inp, cuda_device)
+    (xq, xsc, Wq, Wsc), (x_deq, W_deq) = _quantized_operands(inp, cuda_device)
+    xst, Wst = _tiled_scales(xsc, Wsc, w)
+    args = (xq, Wq, d["cos"], d["sin"], w.H, w.Dn, w.Dr)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    c1, s1 = mlaq.fwd(*args, pos=d["pos"], weight_mode="mxfp8", x_scales=xsc, w_scales=Wsc, status=st)
+    c2, s2 = mlaq.fwd(*args, pos=d["pos"], weight_mode="mxfp8_tiled", x_scales=xst, w_scales=Wst, status=st)
+    mlaq.check_status(st)
+    assert torch.equal(c1, c2) and torch.equal(s1, s2)
+    tokens = np.sort(np.random.default_rng(5).choice(w.T, 24, replace=False))
+    q_ref, rc, rs = _oracle(inp, w, x_deq, W_deq, tokens=tokens, quantize=True)
+    idx = torch.from_numpy(tokens).to(cuda_device)
+    helpers.check_mxfp8_close(c2[idx].cpu().numpy(), s2[idx].cpu().numpy(), q_ref, rc, rs)

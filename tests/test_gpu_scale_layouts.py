@@ -74,6 +74,26 @@ def test_swizzle_matches_oracle(cuda_device, rows, cols):
         assert np.array_equal(out.cpu().numpy(), oracle.mxfp8_swizzle_scales(s.numpy()))
 
 
+@pytest.mark.parametrize("rows,cols,group", [(300, 48, 192), (24576, 48, 192), (77, 9, 96), (1000, 5, 256),
+                                            (130, 4, 32), (128, 3, 128)])
+def test_grouped_swizzle_matches_oracle(cuda_device, rows, cols, group):
+    """Rows in groups of `group`, each group padded to whole 128-row tiles:
+    the oracle's plain swizzle applied group by group, concatenated."""
+    g = torch.Generator().manual_seed(rows * 7 + cols + group)
+    s = torch.randint(0, 256, (rows, cols), generator=g, dtype=torch.int32).to(torch.uint8)
+    out = mlaq.mxfp8_swizzle_scales(s.to(cuda_device), group=group).cpu().numpy()
+    # every group takes ceil(group/128) row tiles; the oracle's swizzle of a
+    # short last group covers fewer, the rest is zero padding
+    per = -(-group // 128) * -(-cols // 4) * 512
+    blocks = []
+    for r0 in range(0, rows, group):
+        b = oracle.mxfp8_swizzle_scales(s[r0:r0 + group].numpy())
+        blocks.append(np.concatenate([b, np.zeros(per - b.size, np.uint8)]))
+    ref = np.concatenate(blocks)
+    assert out.size == ref.size == int(mlaq.lib().mxfp8_grouped_scale_bytes(rows, cols, group))
+    assert np.array_equal(out, ref)
+
+
 def test_swizzle_strided_input(cuda_device):
     base = torch.randint(0, 256, (200, 16), dtype=torch.int32).to(torch.uint8)
     view = base.to(cuda_device)[:, 3:10]  # pitch 16, 7 columns

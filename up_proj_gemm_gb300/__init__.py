@@ -34,7 +34,7 @@ STATUS = {
     "MLA_ERR_ALIAS": 4, "MLA_ERR_UNSUPPORTED": 5, "MLA_ERR_CUDA": 6, "MLA_ERR_TIMEOUT": 7,
     "MLA_ERR_POS_RANGE": 8, "MLA_ERR_WORKSPACE": 9,
 }
-WEIGHT_MODES = {"bf16": 0, "mxfp8": 1}
+WEIGHT_MODES = {"bf16": 0, "mxfp8": 1, "mxfp8_tiled": 2}
 OUT_MODES = {"bf16": 0, "mxfp8": 1, "mxfp8_bhsd": 2, "mxfp8_bhsd_swizzled": 3}
 
 
@@ -82,6 +82,9 @@ _SIGS = {
     "mla_q_uproj_bwd_mxfp8": (_int, [ctypes.POINTER(Shape)] + [_vp] * 10 + [ctypes.c_size_t, _vp, _vp]),
     "mla_q_uproj_bwd_mxfp8_layout": (_int, [ctypes.POINTER(Shape), ctypes.POINTER(Mxfp8BwdLayout)]),
     "mxfp8_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "mxfp8_grouped_scale_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
+    "mxfp8_swizzle_scales_grouped": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "mla_q_uproj_w_scale_group": (ctypes.c_int64, [ctypes.POINTER(Shape)]),
     "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
     "mla_wait_selftest": (_int, [_int, ctypes.c_uint64, _vp, _vp]),
     "mla_status_string": (ctypes.c_char_p, [_int]),
@@ -178,7 +181,10 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
 
     weight_mode "bf16": x [T, K] bf16, W [N, K] bf16.
     weight_mode "mxfp8": x, W uint8 E4M3 codes with x_scales [T, K/32],
-    w_scales [N, K/32] uint8 E8M0."""
+    w_scales [N, K/32] uint8 E8M0.
+    weight_mode "mxfp8_tiled": the same codes with the scales already tiled:
+    x_scales = mxfp8_swizzle_scales(x scales), w_scales =
+    mxfp8_swizzle_scales(W scales, group=w_scale_group(...)) (flat uint8)."""
     wm, om = WEIGHT_MODES[weight_mode], OUT_MODES[out_mode]
     in_dtype = torch.uint8 if wm else torch.bfloat16
     dev = x.device
@@ -197,9 +203,9 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
         _need(bias, "bias", torch.bfloat16, dev, ndim=1)
     if pos is not None:
         _need(pos, "pos", torch.int32, dev, ndim=1)
-    if wm:
-        _need(x_scales, "x_scales", torch.uint8, dev, ndim=2)
-        _need(w_scales, "w_scales", torch.uint8, dev, ndim=2)
+    if wm:  # "mxfp8": [rows, K/32] scales; "mxfp8_tiled": flat tiled buffers
+        _need(x_scales, "x_scales", torch.uint8, dev, ndim=1 if wm == 2 else 2)
+        _need(w_scales, "w_scales", torch.uint8, dev, ndim=1 if wm == 2 else 2)
     if q_out is None:
         q_out = torch.empty((T, H, D), dtype=torch.uint8 if om else torch.bfloat16, device=dev)
     if om and q_scales is None:
@@ -422,20 +428,32 @@ def mxfp8_quantize_cols(inp, codes=None, scales=None, stream=None):
     return codes, scales
 
 
-def mxfp8_swizzle_scales(scales, out=None, stream=None):
+def mxfp8_swizzle_scales(scales, out=None, stream=None, group=128):
     """Row-major E8M0 scales [rows, cols] (uint8 CUDA tensor, unit inner
     stride) -> the 128 x 4 tiled order of block-scaled GEMMs, as a flat uint8
-    tensor of mxfp8_swizzled_scale_bytes(rows, cols) bytes."""
+    tensor of mxfp8_grouped_scale_bytes(rows, cols, group) bytes; rows in
+    groups of `group`, each padded to whole 128-row tiles (group 128: the
+    plain swizzle, mxfp8_swizzle_scales)."""
     if scales.dtype != torch.uint8 or not scales.is_cuda or scales.dim() != 2 or scales.stride(1) != 1:
         raise ValueError("scales must be a 2-D uint8 CUDA tensor with unit inner stride")
     rows, cols = scales.shape
-    n = int(lib().mxfp8_swizzled_scale_bytes(rows, cols))
+    n = int(lib().mxfp8_grouped_scale_bytes(rows, cols, group))
     if out is None:
         out = torch.empty((n,), dtype=torch.uint8, device=scales.device)
     ld = int(scales.stride(0)) if rows > 1 else int(cols)
-    _call(lib().mxfp8_swizzle_scales, "mxfp8_swizzle_scales", rows, cols, _ptr(scales), ld, _ptr(out),
-          _stream(scales.device, stream))
+    if group == 128:
+        _call(lib().mxfp8_swizzle_scales, "mxfp8_swizzle_scales", rows, cols, _ptr(scales), ld, _ptr(out),
+              _stream(scales.device, stream))
+    else:
+        _call(lib().mxfp8_swizzle_scales_grouped, "mxfp8_swizzle_scales_grouped", rows, cols, int(group),
+              _ptr(scales), ld, _ptr(out), _stream(scales.device, stream))
     return out
+
+
+def w_scale_group(T, K, H, Dn, Dr, cs_rows, cs_width) -> int:
+    """Row group of W's tiled scales for weight_mode "mxfp8_tiled" (0: none)."""
+    s = Shape(T=T, K=K, H=H, Dn=Dn, Dr=Dr, reserved=0, cs_rows=cs_rows, cs_width=cs_width)
+    return int(lib().mla_q_uproj_w_scale_group(ctypes.byref(s)))
 
 
 def kv_fwd(c_kv, W, k_pe, cos, sin, H, Dn, Dv, Dr, pos=None, o_key=None, o_value=None, status=None, stream=None):

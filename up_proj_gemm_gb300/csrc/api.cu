@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "mx.cuh"
 
 namespace mlaq {
 
@@ -228,11 +229,13 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
     int st = check_shape(shape, &D, &N);
     if (st != MLA_OK) return st;
     const mla_q_shape& s = *shape;
-    if (weight_mode != MLA_WEIGHT_BF16 && weight_mode != MLA_WEIGHT_MXFP8) return MLA_ERR_INVALID_ARG;
+    if (weight_mode != MLA_WEIGHT_BF16 && weight_mode != MLA_WEIGHT_MXFP8 && weight_mode != MLA_WEIGHT_MXFP8_TILED)
+        return MLA_ERR_INVALID_ARG;
+    const bool tiled = weight_mode == MLA_WEIGHT_MXFP8_TILED;
     if (out_mode != MLA_OUT_BF16 && out_mode != MLA_OUT_MXFP8 && out_mode != MLA_OUT_MXFP8_BHSD &&
         out_mode != MLA_OUT_MXFP8_BHSD_SWIZZLED)
         return MLA_ERR_INVALID_ARG;
-    const bool mxw = weight_mode == MLA_WEIGHT_MXFP8, mxo = out_mode != MLA_OUT_BF16;
+    const bool mxw = weight_mode != MLA_WEIGHT_BF16, mxo = out_mode != MLA_OUT_BF16;
     if (mxw != (x_scales != nullptr) || mxw != (w_scales != nullptr)) return MLA_ERR_INVALID_ARG;
     if (mxo != (q_scales_out != nullptr)) return MLA_ERR_INVALID_ARG;
     if (s.T > 0 && (!x || !W || !q_out)) return MLA_ERR_INVALID_ARG;
@@ -243,7 +246,10 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
 
     if (!rope_dim_supported(s.Dr) || s.Dn % 32) return MLA_ERR_UNSUPPORTED;
     if (mxw && s.K % 128) return MLA_ERR_UNSUPPORTED;
-    if (fwd_tile_n(N, D, s.Dn, s.Dr, mxw ? 192 : 256, mxw ? 32 : 16) == 0) return MLA_ERR_UNSUPPORTED;
+    const int bn = fwd_tile_n(N, D, s.Dn, s.Dr, mxw ? 192 : 256, mxw ? 32 : 16);
+    if (bn == 0) return MLA_ERR_UNSUPPORTED;
+    // tiled scales arrive by 16-byte bulk copies
+    if (tiled && (!aligned(x_scales, 16) || !aligned(w_scales, 16))) return MLA_ERR_ALIGNMENT;
 
     const int64_t esz = mxw ? 1 : 2;
     if ((s.K * esz) % 16) return MLA_ERR_ALIGNMENT;
@@ -259,8 +265,10 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
                                  : s.T * s.H * NB;
     const Range outs[] = {rng(q_out, s.T * N * (mxo ? 1 : 2)), rng(q_scales_out, qs_bytes),
                           rng(dev_status, 4)};
-    const Range ins[] = {rng(x, s.T * s.K * esz), rng(x_scales, s.T * (s.K / 32)),
-                         rng(W, N * s.K * esz),   rng(w_scales, N * (s.K / 32)),
+    const int64_t xs_bytes = tiled ? (int64_t)sf_tiled_bytes(s.T, s.K / 32, 128) : s.T * (s.K / 32);
+    const int64_t ws_bytes = tiled ? (int64_t)sf_tiled_bytes(N, s.K / 32, bn) : N * (s.K / 32);
+    const Range ins[] = {rng(x, s.T * s.K * esz), rng(x_scales, xs_bytes),
+                         rng(W, N * s.K * esz),   rng(w_scales, ws_bytes),
                          rng(bias, N * 2),        rng(cos_tab, table),
                          rng(sin_tab, table),     rng(pos, s.T * 4)};
     if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
@@ -273,8 +281,12 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
     a.Dr = s.Dr;
     a.cs_rows = s.cs_rows;
     a.cs_width = s.cs_width;
-    a.weight_mode = weight_mode;
+    a.weight_mode = mxw ? MLA_WEIGHT_MXFP8 : MLA_WEIGHT_BF16;
     a.out_mode = out_mode;
+    if (tiled) {
+        a.sf_tiled = 1;
+        a.sf_group = bn;
+    }
     a.x = x;
     a.x_scales = x_scales;
     a.W = W;
@@ -555,16 +567,33 @@ MLAQ_API size_t mxfp8_swizzled_scale_bytes(int64_t rows, int64_t cols) {
     return (size_t)((rows + 127) / 128) * 128 * (size_t)((cols + 3) / 4) * 4;
 }
 
-MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t* in, int64_t ld_in, uint8_t* out,
-                                  void* stream) {
-    if (rows < 0 || cols < 0 || ld_in < cols) return MLA_ERR_INVALID_ARG;
+MLAQ_API size_t mxfp8_grouped_scale_bytes(int64_t rows, int64_t cols, int64_t group) {
+    if (rows <= 0 || cols <= 0 || group <= 0) return 0;
+    return (size_t)sf_tiled_bytes(rows, cols, group);
+}
+
+MLAQ_API int mxfp8_swizzle_scales_grouped(int64_t rows, int64_t cols, int64_t group, const uint8_t* in,
+                                          int64_t ld_in, uint8_t* out, void* stream) {
+    if (rows < 0 || cols < 0 || ld_in < cols || group <= 0) return MLA_ERR_INVALID_ARG;
     if (rows == 0 || cols == 0) return MLA_OK;
     if (!in || !out) return MLA_ERR_INVALID_ARG;
     if (!aligned(out, 16)) return MLA_ERR_ALIGNMENT;
-    const Range outs[] = {rng(out, (int64_t)mxfp8_swizzled_scale_bytes(rows, cols))};
+    const Range outs[] = {rng(out, (int64_t)mxfp8_grouped_scale_bytes(rows, cols, group))};
     const Range ins[] = {rng(in, (rows - 1) * ld_in + cols)};
     if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
-    return launch_mxfp8_swizzle(rows, cols, in, ld_in, out, static_cast<cudaStream_t>(stream));
+    return launch_mxfp8_swizzle(rows, cols, group, in, ld_in, out, static_cast<cudaStream_t>(stream));
+}
+
+MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t* in, int64_t ld_in, uint8_t* out,
+                                  void* stream) {
+    return mxfp8_swizzle_scales_grouped(rows, cols, 128, in, ld_in, out, stream);
+}
+
+MLAQ_API int64_t mla_q_uproj_w_scale_group(const mla_q_shape* shape) {
+    int D;
+    int64_t N;
+    if (check_shape(shape, &D, &N) != MLA_OK || !rope_dim_supported(shape->Dr) || shape->Dn % 32) return 0;
+    return fwd_tile_n(N, D, shape->Dn, shape->Dr, 192, 32);
 }
 
 }  // extern "C"

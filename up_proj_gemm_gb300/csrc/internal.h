@@ -40,7 +40,7 @@ int make_tmap_3d(void* tmap_out, const void* base, uint64_t d0, uint64_t d1, uin
 
 // ------------------------------------------------------------- launchers
 // All launchers assume arguments were validated by the API layer.
-int launch_mxfp8_swizzle(int64_t rows, int64_t cols, const uint8_t* in, int64_t ld, uint8_t* out,
+int launch_mxfp8_swizzle(int64_t rows, int64_t cols, int64_t group, const uint8_t* in, int64_t ld, uint8_t* out,
                          cudaStream_t stream);
 int launch_mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                                uint8_t* codes_t, uint8_t* scales_t, cudaStream_t stream);

@@ -367,28 +367,34 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
 // ------------------------------------------------------- scale swizzle
 // Row-major E8M0 scales [rows, cols] -> the tiled order block-scaled GEMMs
 // read (TransformerEngine PR "Add support for fused Q Up-Proj
-// GEMM/RoPE/Quant": the GEMM scale swizzle among its MXFP8 helpers): tiles of
-// 128 rows x 4 scale columns, 512 bytes each, tile (i, j) at
-// (i * ceil(cols/4) + j) * 512; inside a tile, row r and column c at byte
-// (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4). Bytes past rows or cols are 0.
+// GEMM/RoPE/Quant": the GEMM scale swizzle among its MXFP8 helpers): rows in
+// groups of G (the GEMM's tile height along that operand), each group padded
+// to whole 128-row chunks; chunk i of group g and column tile j (4 scale
+// columns) is the 512-byte tile ((g * ceil(G/128) + i) * ceil(cols/4) + j);
+// inside it, row r of the chunk and column c at byte
+// (r % 32) * 16 + (r / 32) * 4 + (c % 4). Bytes past the rows of a group or
+// past cols are 0. With G = 128 this is the plain swizzle of the matrix.
 // One thread writes the 16 bytes of one (tile, r % 32) pair.
 __global__ void __launch_bounds__(256) mxfp8_swizzle_kernel(const uint8_t* __restrict__ in, int64_t rows,
-                                                            int64_t cols, int64_t ld, uint8_t* __restrict__ out,
-                                                            int64_t tiles_c, int64_t nthreads) {
+                                                            int64_t cols, int64_t ld, int64_t group, int64_t nsub,
+                                                            uint8_t* __restrict__ out, int64_t tiles_c,
+                                                            int64_t nthreads) {
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < nthreads;
          g += (int64_t)gridDim.x * blockDim.x) {
         const int64_t tile = g / 32;
         const int r32 = (int)(g % 32);
         const int64_t ti = tile / tiles_c, tj = tile % tiles_c;
+        const int64_t grp = ti / nsub, chunk = ti % nsub;
         uint32_t w[4];
 #pragma unroll
         for (int rb = 0; rb < 4; ++rb) {
-            const int64_t r = ti * 128 + rb * 32 + r32;
+            const int64_t rg = chunk * 128 + rb * 32 + r32;  // row within the group
+            const int64_t r = grp * group + rg;
             uint32_t word = 0;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int64_t c = tj * 4 + cc;
-                if (r < rows && c < cols) word |= (uint32_t)__ldg(in + r * ld + c) << (8 * cc);
+                if (rg < group && r < rows && c < cols) word |= (uint32_t)__ldg(in + r * ld + c) << (8 * cc);
             }
             w[rb] = word;
         }
@@ -471,17 +477,18 @@ int launch_mxfp8_quantize_cols_ld(int64_t R, int64_t C, int in_dtype, const void
 }  // namespace mlaq
 
 namespace mlaq {
-int launch_mxfp8_swizzle(int64_t rows, int64_t cols, const uint8_t* in, int64_t ld, uint8_t* out,
+int launch_mxfp8_swizzle(int64_t rows, int64_t cols, int64_t group, const uint8_t* in, int64_t ld, uint8_t* out,
                          cudaStream_t stream) {
     DeviceInfo di;
     int st = current_device_info(&di);
     if (st != MLA_OK) return st;
     const int64_t tiles_c = (cols + 3) / 4;
-    const int64_t n = ((rows + 127) / 128) * tiles_c * 32;
+    const int64_t nsub = (group + 127) / 128;
+    const int64_t n = ((rows + group - 1) / group) * nsub * tiles_c * 32;
     int64_t blocks = (n + 255) / 256;
     const int64_t cap = (int64_t)di.num_sms * 8;
     if (blocks > cap) blocks = cap;
-    mxfp8_swizzle_kernel<<<(unsigned)blocks, 256, 0, stream>>>(in, rows, cols, ld, out, tiles_c, n);
+    mxfp8_swizzle_kernel<<<(unsigned)blocks, 256, 0, stream>>>(in, rows, cols, ld, group, nsub, out, tiles_c, n);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 }  // namespace mlaq
