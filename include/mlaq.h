@@ -117,7 +117,8 @@ typedef struct {
  *               so they arrive by bulk copies instead of a per-row gather (the
  *               same outputs, bit for bit, in less time):
  *               x_scales = mxfp8_swizzle_scales of the [T, K/32] scales
- *               (mxfp8_swizzled_scale_bytes(T, K/32) bytes); w_scales =
+ *               (mxfp8_swizzled_scale_bytes(T, K/32) bytes; or written so
+ *               directly by mxfp8_quantize_rows_tiled, group 128); w_scales =
  *               mxfp8_swizzle_scales_grouped of the [N, K/32] scales with
  *               group = mla_q_uproj_w_scale_group(shape) (the kernel's
  *               channel tile; mxfp8_grouped_scale_bytes(N, K/32, group)
@@ -376,6 +377,18 @@ MLAQ_API int mla_q_uproj_bwd_dgrad_noalloc(const mla_q_shape *shape, const void 
  */
 MLAQ_API int mxfp8_quantize_rows(int64_t R, int64_t C, int in_dtype, const void *in,
                                  int64_t ld_in, uint8_t *codes, uint8_t *scales, void *stream);
+
+/*
+ * mxfp8_quantize_rows with the scales written in the tiled order block-scaled
+ * GEMMs read: the layout mxfp8_swizzle_scales_grouped(R, ceil(C/32), group)
+ * gives the row-major scales, padding bytes 0 (scales: that many bytes,
+ * mxfp8_grouped_scale_bytes). Codes as mxfp8_quantize_rows. For
+ * MLA_WEIGHT_MXFP8_TILED: x with group 128, W with
+ * mla_q_uproj_w_scale_group(shape). Same errors as mxfp8_quantize_rows, and
+ * MLA_ERR_INVALID_ARG for group <= 0.
+ */
+MLAQ_API int mxfp8_quantize_rows_tiled(int64_t R, int64_t C, int in_dtype, const void *in, int64_t ld_in,
+                                       uint8_t *codes, uint8_t *scales, int64_t group, void *stream);
 
 /*
  * Columnwise MXFP8 copy of in[R, C] (row pitch ld_in elements): the rowwise

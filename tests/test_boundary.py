@@ -355,3 +355,15 @@ def test_fwd_tiled_scales_checks(L):
     ws = ctypes.c_void_p(FAKE * 5 - 896)  # q is at FAKE * 5
     assert fwd(L, s, wm=1, xs=p(6), ws=ws) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
     assert fwd(L, s, wm=2, xs=p(6), ws=ws) == S["MLA_ERR_ALIAS"]
+
+
+def test_quantize_rows_tiled_checks(L):
+    q = L.mxfp8_quantize_rows_tiled
+    assert q(10, 64, 1, p(0), 64, p(1), p(2), 0, None) == S["MLA_ERR_INVALID_ARG"]     # group <= 0
+    assert q(10, 64, 2, p(0), 64, p(1), p(2), 128, None) == S["MLA_ERR_INVALID_ARG"]   # dtype
+    assert q(0, 64, 1, None, 64, None, None, 128, None) == S["MLA_OK"]
+    # 10 rows x 2 blocks tile to 512 bytes (128 rows x 4 columns): a scale buffer
+    # starting 256 bytes before the input overlaps it only in the tiled order
+    sc = ctypes.c_void_p(FAKE - 256)  # the input is at FAKE
+    assert L.mxfp8_quantize_rows(10, 64, 1, p(0), 64, p(1), sc, None) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    assert q(10, 64, 1, p(0), 64, p(1), sc, 128, None) == S["MLA_ERR_ALIAS"]

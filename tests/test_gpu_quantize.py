@@ -118,3 +118,33 @@ def test_quantize_does_not_touch_input(cuda_device):
     before = x.clone()
     _run(x)
     assert torch.equal(x, before)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("R,C,group", [(4096, 1536, 128), (24576, 1536, 192), (300, 100, 96), (77, 1000, 128),
+                                       (64, 40, 256), (130, 64, 32)])
+def test_quantize_rows_tiled_scales(cuda_device, dtype, R, C, group):
+    """mxfp8_quantize_rows_tiled: the codes of mxfp8_quantize_rows and its
+    scales in the grouped tiled order (= mxfp8_swizzle_scales_grouped of the
+    row-major scales, padding 0). The buffer starts filled with 0xEE so every
+    padding byte must be written."""
+    g = torch.Generator().manual_seed(R + C + group)
+    x = (torch.randn((R, C), generator=g) * 3.0).to(dtype).to(cuda_device)
+    codes, scales = mlaq.mxfp8_quantize_rows(x)
+    n = int(mlaq.lib().mxfp8_grouped_scale_bytes(R, (C + 31) // 32, group))
+    tiled = torch.full((n,), 0xEE, dtype=torch.uint8, device=cuda_device)
+    codes_t, tiled = mlaq.mxfp8_quantize_rows(x, scales=tiled, group=group)
+    ref = mlaq.mxfp8_swizzle_scales(scales, group=group)
+    torch.cuda.synchronize()
+    assert torch.equal(codes_t, codes)
+    assert torch.equal(tiled, ref)
+
+
+def test_quantize_rows_tiled_strided_input(cuda_device):
+    base = (torch.randn((200, 80)) * 2.0).to(torch.bfloat16).to(cuda_device)
+    view = base[:, 3:67]  # pitch 80, 64 columns, not 16-byte aligned rows
+    codes, scales = mlaq.mxfp8_quantize_rows(view)
+    codes_t, tiled = mlaq.mxfp8_quantize_rows(view, group=128)
+    torch.cuda.synchronize()
+    assert torch.equal(codes_t, codes)
+    assert torch.equal(tiled, mlaq.mxfp8_swizzle_scales(scales))

@@ -82,6 +82,7 @@ _SIGS = {
     "mla_q_uproj_bwd_mxfp8": (_int, [ctypes.POINTER(Shape)] + [_vp] * 10 + [ctypes.c_size_t, _vp, _vp]),
     "mla_q_uproj_bwd_mxfp8_layout": (_int, [ctypes.POINTER(Shape), ctypes.POINTER(Mxfp8BwdLayout)]),
     "mxfp8_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "mxfp8_quantize_rows_tiled": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _i64, _vp]),
     "mxfp8_grouped_scale_bytes": (ctypes.c_size_t, [_i64, _i64, _i64]),
     "mxfp8_swizzle_scales_grouped": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _vp]),
     "mla_q_uproj_w_scale_group": (ctypes.c_int64, [ctypes.POINTER(Shape)]),
@@ -385,11 +386,13 @@ def bwd_mxfp8(dq, W, x, cos, sin, H, Dn, Dr, pos=None, dx=True, dW=True, db=True
     return dx, dW, db
 
 
-def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None):
+def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None, group=None):
     """Rowwise MXFP8 of a 2-D fp32/bf16 CUDA tensor -> (codes uint8 [R, C], scales uint8 [R, ceil(C/32)]).
 
     A row pitch larger than C is taken from ``inp.stride(0)`` (the tensor must
-    have unit inner stride)."""
+    have unit inner stride). With ``group``, the scales come back flat in the
+    block-scaled GEMM's tiled order with row groups of that size
+    (mxfp8_quantize_rows_tiled)."""
     if inp.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("input must be float32 or bfloat16")
     if not inp.is_cuda or inp.dim() != 2 or inp.stride(1) != 1:
@@ -399,9 +402,16 @@ def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None):
     dev = inp.device
     if codes is None:
         codes = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    dt = 0 if inp.dtype == torch.float32 else 1
+    if group is not None:
+        if scales is None:
+            n = int(lib().mxfp8_grouped_scale_bytes(R, (C + 31) // 32, int(group)))
+            scales = torch.empty((n,), dtype=torch.uint8, device=dev)
+        _call(lib().mxfp8_quantize_rows_tiled, "mxfp8_quantize_rows_tiled", R, C, dt, _ptr(inp), ld_in,
+              _ptr(codes), _ptr(scales), int(group), _stream(dev, stream))
+        return codes, scales
     if scales is None:
         scales = torch.empty((R, (C + 31) // 32), dtype=torch.uint8, device=dev)
-    dt = 0 if inp.dtype == torch.float32 else 1
     _call(lib().mxfp8_quantize_rows, "mxfp8_quantize_rows", R, C, dt, _ptr(inp), ld_in, _ptr(codes),
           _ptr(scales), _stream(dev, stream))
     return codes, scales

@@ -546,6 +546,22 @@ MLAQ_API int mxfp8_quantize_rows(int64_t R, int64_t C, int in_dtype, const void*
                                  static_cast<cudaStream_t>(stream));
 }
 
+MLAQ_API int mxfp8_quantize_rows_tiled(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                                       uint8_t* codes, uint8_t* scales, int64_t group, void* stream) {
+    if (R < 0 || C < 0 || ld_in < C || group <= 0) return MLA_ERR_INVALID_ARG;
+    if (in_dtype != MLA_IN_F32 && in_dtype != MLA_IN_BF16) return MLA_ERR_INVALID_ARG;
+    if (R == 0 || C == 0) return MLA_OK;
+    if (!in || !codes || !scales) return MLA_ERR_INVALID_ARG;
+    const int64_t esz = in_dtype == MLA_IN_F32 ? 4 : 2;
+    if (!aligned(in, (uintptr_t)esz)) return MLA_ERR_ALIGNMENT;
+    const int64_t nb = (C + 31) / 32;
+    const Range outs[] = {rng(codes, R * C), rng(scales, (int64_t)sf_tiled_bytes(R, nb, group))};
+    const Range ins[] = {rng(in, ((R - 1) * ld_in + C) * esz)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    return launch_mxfp8_quantize(R, C, in_dtype, in, ld_in, codes, scales, static_cast<cudaStream_t>(stream),
+                                 group);
+}
+
 MLAQ_API int mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                                  uint8_t* codes_t, uint8_t* scales_t, void* stream) {
     if (R < 0 || C < 0 || ld_in < C) return MLA_ERR_INVALID_ARG;

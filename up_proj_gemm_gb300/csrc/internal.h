@@ -59,8 +59,10 @@ int launch_mxfp8_quantize_cols_ld(int64_t R, int64_t C, int in_dtype, const void
 int launch_mxfp8_quantize_cols_tiled_sf(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
                                         uint8_t* codes_t, int64_t ld_codes, uint8_t* scales_t, int64_t sf_group,
                                         cudaStream_t stream);
+// sf_group > 0: scales in the GEMM's tiled order with row groups of sf_group
+// (padding zero-filled); 0: row-major [R, ceil(C/32)].
 int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
-                          uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+                          uint8_t* codes, uint8_t* scales, cudaStream_t stream, int64_t sf_group = 0);
 
 struct FwdArgs {
     int64_t T, K;

@@ -59,11 +59,15 @@ __device__ __forceinline__ float load_elem(const __nv_bfloat16* p) {
 
 // VEC: rows start 16-byte aligned and C % kElems == 0, so every 16-byte
 // vector is either wholly inside a row or wholly past its end.
-template <typename Tin, bool VEC>
+// TILED: the scale of (row r, block c) goes to the GEMM's tiled order
+// with row groups of sf_group (sf_tiled_offset, sf_nkt = ceil(nb / 4)); the
+// host zero-fills the buffer first when it has padding.
+template <typename Tin, bool VEC, bool TILED>
 __global__ void __launch_bounds__(kThreads) mxfp8_quantize_kernel(const Tin* __restrict__ in,
                                                                   int64_t R, int64_t C, int64_t ld,
                                                                   uint8_t* __restrict__ codes,
-                                                                  uint8_t* __restrict__ scales) {
+                                                                  uint8_t* __restrict__ scales, int64_t sf_group,
+                                                                  int64_t sf_nkt) {
     constexpr int E = VecTraits<Tin>::kElems;  // elements per 16-byte vector
     constexpr int TPB = 32 / E;                // lanes per 32-element block
     constexpr int STEP = 32 * E;               // elements per warp per unrolled step
@@ -132,7 +136,9 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quantize_kernel(const Tin* __r
                     for (int j = 0; j < E; ++j)
                         if (c0 + j < C) dst[j] = (uint8_t)(w[j / 4] >> (8 * (j % 4)));
                 }
-                if ((lane % TPB) == 0) scales[r * nb + c0 / 32] = (uint8_t)sbyte;
+                if ((lane % TPB) == 0)
+                    scales[TILED ? sf_tiled_offset(r, c0 / 32, sf_group, sf_nkt) : r * nb + c0 / 32] =
+                        (uint8_t)sbyte;
             }
         }
     }
@@ -140,13 +146,20 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quantize_kernel(const Tin* __r
 
 template <typename Tin>
 int launch_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t* codes, uint8_t* scales,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, int64_t sf_group = 0) {
     constexpr int E = VecTraits<Tin>::kElems;
     DeviceInfo di;
     int st = current_device_info(&di);
     if (st != MLA_OK) return st;
-    // Contiguous rows whose blocks never straddle a row end: one long row.
-    if (ld == C && C % 32 == 0) {
+    const int64_t nb = (C + 31) / 32, nkt = (nb + 3) / 4;
+    if (sf_group > 0 && (sf_group % 128 || R % sf_group || nb % 4)) {
+        // the tiled order has padding rows or columns: they read as 0
+        if (cudaMemsetAsync(scales, 0, (size_t)sf_tiled_bytes(R, nb, sf_group), stream) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    }
+    // Contiguous rows whose blocks never straddle a row end: one long row
+    // (scale positions unchanged only in the row-major order).
+    if (sf_group == 0 && ld == C && C % 32 == 0) {
         C = R * C;
         ld = C;
         R = 1;
@@ -162,12 +175,14 @@ int launch_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t* code
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     const Tin* p = static_cast<const Tin*>(in);
-    if (vec)
-        mxfp8_quantize_kernel<Tin, true><<<(unsigned)blocks, kThreads, 0, stream>>>(p, R, C, ld, codes,
-                                                                                   scales);
-    else
-        mxfp8_quantize_kernel<Tin, false><<<(unsigned)blocks, kThreads, 0, stream>>>(p, R, C, ld,
-                                                                                    codes, scales);
+    const unsigned g = (unsigned)blocks;
+    if (sf_group > 0) {
+        if (vec) mxfp8_quantize_kernel<Tin, true, true><<<g, kThreads, 0, stream>>>(p, R, C, ld, codes, scales, sf_group, nkt);
+        else mxfp8_quantize_kernel<Tin, false, true><<<g, kThreads, 0, stream>>>(p, R, C, ld, codes, scales, sf_group, nkt);
+    } else {
+        if (vec) mxfp8_quantize_kernel<Tin, true, false><<<g, kThreads, 0, stream>>>(p, R, C, ld, codes, scales, 0, 0);
+        else mxfp8_quantize_kernel<Tin, false, false><<<g, kThreads, 0, stream>>>(p, R, C, ld, codes, scales, 0, 0);
+    }
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -445,9 +460,9 @@ int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t*
 }  // namespace
 
 int launch_mxfp8_quantize(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
-                          uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
-    if (in_dtype == MLA_IN_F32) return launch_typed<float>(R, C, in, ld_in, codes, scales, stream);
-    return launch_typed<__nv_bfloat16>(R, C, in, ld_in, codes, scales, stream);
+                          uint8_t* codes, uint8_t* scales, cudaStream_t stream, int64_t sf_group) {
+    if (in_dtype == MLA_IN_F32) return launch_typed<float>(R, C, in, ld_in, codes, scales, stream, sf_group);
+    return launch_typed<__nv_bfloat16>(R, C, in, ld_in, codes, scales, stream, sf_group);
 }
 
 }  // namespace mlaq
