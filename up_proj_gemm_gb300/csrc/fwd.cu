@@ -661,9 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int col = p.split_half ? half * (p.BN / 2) : 0, unit = 0;
             const int col_end = p.split_half ? col + p.BN / 2 : p.BN;
             while (col < col_end) {
-                const int64_t n = n0 + col;
-                const int h = (int)(n / p.D);
-                const int c = (int)(n - (int64_t)h * p.D);
+                const int n32 = (int)n0 + col;  // channel indices fit in 32 bits (N is an int)
+                const int h = n32 / p.D;
+                const int c = n32 - h * p.D;
+                const int64_t n = n32;
                 const bool nope = c < p.Dn;
                 if (M2 || p.split_half || (unit++ & 1) == half) {
                     if (nope) nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
