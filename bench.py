@@ -438,6 +438,7 @@ def run_only(args, w, inp, kernels, flush, stream, status, dev):
     """One kernel alone, K timed calls (for profiling: a short, fixed launch
     sequence). Prints a JSON line with its mean time."""
     import torch
+    import synth
     import up_proj_gemm_gb300 as mlaq
     if args.only in kernels:
         fn = kernels[args.only]
@@ -484,6 +485,21 @@ def run_only(args, w, inp, kernels, flush, stream, status, dev):
         def fn():
             mlaq.mxfp8_quantize_rows(a, codes, sc)
         flop = 0
+    elif args.only == "kv":
+        # the KV side at the DeepSeek-V3 shape: kv_lora_rank 512, H 128, 128 + 128 + 64
+        T, K, H, Dn, Dv, Dr = w.T, 512, w.H, 128, 128, 64
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        c_kv = torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16)
+        Wkv = (torch.randn((H * (Dn + Dv), K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        k_pe = torch.randn((T, Dr), generator=g, device=dev).to(torch.bfloat16)
+        kcos, ksin = [t.to(dev) for t in synth.rope_table_standard(T, Dr)]
+        o_key = torch.empty((T, H, Dn + Dr), dtype=torch.bfloat16, device=dev)
+        o_value = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+
+        def fn():
+            mlaq.kv_fwd(c_kv, Wkv, k_pe, kcos, ksin, H, Dn, Dv, Dr, o_key=o_key, o_value=o_value, status=status)
+        flop = 2 * T * K * H * (Dn + Dv)
     else:
         raise SystemExit(f"unknown --only {args.only}")
     ms = time_loop(fn, args.steps, flush, stream, warmup=args.warmup)
@@ -732,7 +748,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "wgrad_self", "fwd_mxfp8w", "quant", "quant_cols",
-                                          "bwd_mxfp8"),
+                                          "bwd_mxfp8", "kv"),
                     help="time one kernel alone (profiling)")
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
