@@ -1030,30 +1030,41 @@ __global__ void __launch_bounds__(kDgThreads, 1)
 // channels of head h (rope_inv8: the bits the fused transforms produce). A
 // thread takes 8 pairs of one (token, head): 4 threads per pair set, a warp 8
 // heads of one token (reads of 128 contiguous bytes per head, 1 KB written).
+constexpr int kRopeHeads = 8;  // heads per thread in rope_pre_kernel (2, 4, 16 measured slower)
+
 __global__ void __launch_bounds__(256) rope_pre_kernel(const uint16_t* __restrict__ dq, int64_t T, int H, int Dn,
                                                        const float* __restrict__ cos_tab,
                                                        const float* __restrict__ sin_tab, long long cs_rows,
                                                        long long cs_width, int cs_vec,
                                                        const int32_t* __restrict__ pos,
                                                        uint16_t* __restrict__ rope_out, int* status) {
+    // A thread takes one quarter q of the 32 pairs (8 pairs) of kRopeHeads
+    // heads of one token: the token's table entries are loaded once and used
+    // for every head (the rows depend on the position only).
     constexpr int DR = 64, HH = 32;
     const int D = Dn + DR;
-    const int64_t items = T * H * 4;
+    const int nhg = (H + kRopeHeads - 1) / kRopeHeads;
+    const int64_t items = T * nhg * 4;
     for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < items;
          it += (int64_t)gridDim.x * blockDim.x) {
         const int q = (int)(it & 3);
-        const int64_t th = it >> 2;
-        const int64_t t = th / H;
-        const int h = (int)(th - t * H);
+        const int64_t tg = it >> 2;
+        const int64_t t = tg / nhg;
+        const int h0 = (int)(tg - t * nhg) * kRopeHeads;
         const int64_t pp = pos ? (int64_t)__ldg(pos + t) : t;
         if (pp < 0 || pp >= cs_rows) {
             record_status(status, MLA_ERR_POS_RANGE);
             continue;
         }
-        const uint16_t* g = dq + (t * H + h) * D + Dn + 8 * q;
-        const uint4 ra = __ldg(reinterpret_cast<const uint4*>(g));
-        const uint4 rc = __ldg(reinterpret_cast<const uint4*>(g + HH));
-        const uint32_t g1[4] = {ra.x, ra.y, ra.z, ra.w}, g2[4] = {rc.x, rc.y, rc.z, rc.w};
+        uint4 ra[kRopeHeads], rc[kRopeHeads];
+#pragma unroll
+        for (int k = 0; k < kRopeHeads; ++k) {
+            if (h0 + k < H) {
+                const uint16_t* g = dq + (t * H + h0 + k) * D + Dn + 8 * q;
+                ra[k] = __ldg(reinterpret_cast<const uint4*>(g));
+                rc[k] = __ldg(reinterpret_cast<const uint4*>(g + HH));
+            }
+        }
         float ci[8], si[8], cj[8], sj[8];
         const float* cr = cos_tab + pp * cs_width + 8 * q;
         const float* sr = sin_tab + pp * cs_width + 8 * q;
@@ -1061,11 +1072,18 @@ __global__ void __launch_bounds__(256) rope_pre_kernel(const uint16_t* __restric
         load8(sr, cs_vec != 0, si);
         load8(cr + HH, cs_vec != 0, cj);
         load8(sr + HH, cs_vec != 0, sj);
-        uint32_t o1[4], o2[4];
-        rope_inv8(g1, g2, ci, si, cj, sj, o1, o2);
-        uint16_t* o = rope_out + (t * H + h) * DR + 8 * q;
-        st_global_v4(o, o1[0], o1[1], o1[2], o1[3]);
-        st_global_v4(o + HH, o2[0], o2[1], o2[2], o2[3]);
+#pragma unroll
+        for (int k = 0; k < kRopeHeads; ++k) {
+            if (h0 + k < H) {
+                const uint32_t g1[4] = {ra[k].x, ra[k].y, ra[k].z, ra[k].w};
+                const uint32_t g2[4] = {rc[k].x, rc[k].y, rc[k].z, rc[k].w};
+                uint32_t o1[4], o2[4];
+                rope_inv8(g1, g2, ci, si, cj, sj, o1, o2);
+                uint16_t* o = rope_out + (t * H + h0 + k) * DR + 8 * q;
+                st_global_v4(o, o1[0], o1[1], o1[2], o1[3]);
+                st_global_v4(o + HH, o2[0], o2[1], o2[2], o2[3]);
+            }
+        }
     }
 }
 
@@ -1635,7 +1653,7 @@ int launch_dgrad_pre(const BwdArgs& a, BwdParams& p, const DeviceInfo& di, cudaS
                                 : reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.workspace) + rope_off);
     // 1. the rope channels, rotated once
     {
-        const int64_t items = a.T * a.H * 4;
+        const int64_t items = a.T * ((a.H + kRopeHeads - 1) / kRopeHeads) * 4;
         int64_t blocks = (items + 255) / 256;
         if (blocks > (int64_t)di.num_sms * 8) blocks = (int64_t)di.num_sms * 8;
         rope_pre_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(a.dq), a.T, a.H, a.Dn,
