@@ -27,6 +27,9 @@ SHAPES = [
     ("dsv3_fwd_bf16w", dict(T=513, H=2, K=256, bias=True)),   # ragged last token tile, bias
     ("dsv3_fwd_bf16w", dict(T=100, H=6, Dn=64, K=128)),       # D = 128: rope regions at channel 64 mod 128
     ("tiny", dict(T=1, K=64, H=4, Dn=64, Dr=32)),             # single token, Dr = 32
+    # 128-channel tiles (N = 128): MXFP8 scales written byte by byte
+    ("dsv3_fwd_bf16w", dict(T=100, H=2, Dn=0, K=128)),        # Dn = 0: heads are all rope
+    ("tiny", dict(T=200, K=64, H=2, Dn=32, Dr=32)),
 ]
 
 

@@ -857,7 +857,11 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.qs_col_tiles = (D / 32 + (D % 32 ? 1 : 0) + 3) / 4;
     p.slot_bytes = 32u * kSlotCh * (mxo ? 1u : 2u);
     p.nslots = mxo ? 8 : 4;  // a unit takes at most 4 slots (64 rope channels)
-    p.split_half = mxo && !p.scales_bhsd && !p.qs_swz && D % 32 == 0 && BN % 128 == 0 && N % 128 == 0 &&
+    // The half split packs a row's scale bytes for half a tile into one aligned
+    // 4-byte word: only when half a tile is exactly 4 blocks (BN = 256, so the
+    // word starts at a multiple of 4 blocks) and rows of scales keep 4-byte
+    // alignment (N % 128 == 0).
+    p.split_half = mxo && !p.scales_bhsd && !p.qs_swz && D % 32 == 0 && BN == 256 && N % 128 == 0 &&
                    reinterpret_cast<uintptr_t>(a.q_scales) % 4 == 0 &&
                    fwd_tile_n(N, D, a.Dn, a.Dr, BN / 2, BN / 2) == BN / 2;
 
