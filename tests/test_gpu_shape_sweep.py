@@ -36,7 +36,23 @@ def _shapes(n, seed):
     return out
 
 
-SHAPES = _shapes(16, 2024)
+def _shapes_mx(n, seed):
+    """Shapes inside the MXFP8 paths' limits more often: Dr 32 or 64, K a
+    multiple of 128, an even number of heads."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        Dr = int(rng.choice([32, 64]))
+        Dn = int(rng.integers(0, 4)) * 64
+        H = 2 * int(rng.integers(1, 5))
+        K = 128 * int(rng.integers(1, 10))
+        T = int(rng.integers(1, 700))
+        seq = None if rng.random() < 0.5 else int(rng.integers(16, 300))
+        out.append(dict(T=T, K=K, H=H, Dn=Dn, Dr=Dr, seq_len=seq, bias=bool(rng.random() < 0.5)))
+    return out
+
+
+SHAPES = _shapes(16, 2024) + _shapes_mx(12, 7)
 
 
 def _unsupported(e):
