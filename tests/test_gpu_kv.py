@@ -74,3 +74,25 @@ def test_kv_full_size_sampled(cuda_device):
                                cos.numpy(), sin.numpy(), pos.numpy()[toks.numpy()])
     helpers.check_bf16_close(o_key[toks.to(dev)], rk, what="o_key")
     helpers.check_bf16_close(o_value[toks.to(dev)], rv, what="o_value")
+
+
+def _kv_sweep(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        Dr = int(rng.choice([16, 32, 64]))
+        Dn = 32 * int(rng.integers(0, 5))
+        Dv = 32 * int(rng.integers(1, 5))
+        if Dn + Dv > 256:
+            continue
+        out.append((int(rng.integers(1, 500)), 8 * int(rng.integers(1, 80)), int(rng.integers(1, 7)), Dn, Dv, Dr,
+                    None if rng.random() < 0.5 else int(rng.integers(16, 300))))
+    return out
+
+
+@pytest.mark.parametrize("T,K,H,Dn,Dv,Dr,seq", _kv_sweep(10, 99))
+def test_kv_shape_sweep(cuda_device, T, K, H, Dn, Dv, Dr, seq):
+    """Seeded random KV shapes inside the documented limits (Dn, Dv multiples
+    of 32 with Dn + Dv <= 256, any K % 8 == 0, ragged T, positions restarting
+    or not)."""
+    _check(cuda_device, T, K, H, Dn, Dv, Dr, 40 + T, seq_len=seq)
