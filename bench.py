@@ -142,6 +142,18 @@ def gpu_id_for(local_rank: int) -> str:
     return str(local_rank)
 
 
+def device_info(dev):
+    """Name, SM count and L2 size of the GPU the step ran on."""
+    import torch
+    pr = torch.cuda.get_device_properties(dev)
+    out = {"name": pr.name, "sm_count": pr.multi_processor_count,
+           "compute_capability": f"{pr.major}.{pr.minor}"}
+    l2 = getattr(pr, "L2_cache_size", None)
+    if l2:
+        out["l2_mb"] = round(l2 / 2 ** 20, 1)
+    return out
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for name in ("fwd.cu", "bwd.cu", "quantize.cu", "ptx.cuh", "mx.cuh"):
@@ -300,8 +312,12 @@ def run_ours(args):
     mlaq.check_status(status, "timed steps")
     per = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(3)]
     mean_k = [statistics.mean(p) for p in per]
-    step_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in ev)
+    step_times = sorted(e[0].elapsed_time(e[3]) for e in ev)
+    step_ms = statistics.mean(step_times)
     step_ms_max = reduce_max([step_ms], world)[0]
+
+    def pct(q):  # nearest-rank percentile of this rank's step times
+        return step_times[min(len(step_times) - 1, max(0, int(round(q * (len(step_times) - 1)))))]
     flop_step = w.fwd_flop() + w.bwd_flop()
     value = aggregate(step_ms_max, flop_step, world)
     clocks = clk.summary(busy_from_mhz=500.0)
@@ -333,6 +349,8 @@ def run_ours(args):
         "roofline": roofline,
         "gpu_launches": kernels_per_step * K,
         "clocks": clocks,
+        "ms_per_step_p10_p50_p90": [round(pct(0.1), 4), round(pct(0.5), 4), round(pct(0.9), 4)],
+        "device": device_info(dev),
         "kernels_ms": {n: round(m, 4) for n, m in zip(names, mean_k)},
         "kernels_tflops": {n: round(f / (m * 1e-3) / 1e12, 1) for n, f, m in zip(names, flops, mean_k)},
     }
