@@ -718,9 +718,14 @@ def cpu_baseline(w, budget_s=15.0):
     import oracle
     probe = 8
     t = oracle_step_sample(w, probe, oracle_inputs(w, probe))
-    tokens = int(max(probe, min(2048, probe * budget_s / max(t, 1e-6))))
+    tokens = int(max(probe, min(w.T, probe * budget_s / max(t, 1e-6))))
     if tokens > probe:
         t = oracle_step_sample(w, tokens, oracle_inputs(w, tokens))
+        # a small probe under-uses the cores, so the first sample can land well
+        # under the budget: rescale once from that sample
+        if t < 0.5 * budget_s and tokens < w.T:
+            tokens = int(min(w.T, tokens * budget_s / max(t, 1e-6)))
+            t = oracle_step_sample(w, tokens, oracle_inputs(w, tokens))
     flop = 6.0 * tokens * w.K * w.N
     return {"value": round(flop / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": round(t, 3),
