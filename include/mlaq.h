@@ -152,9 +152,14 @@ typedef struct {
  *               into the forward the step that the same PR's flowchart puts
  *               between the quantized query and the fused attention: scales
  *               moved to head-major order and tiled for the GEMM.
- * Tiling limits (else MLA_ERR_UNSUPPORTED): Dr in {16, 32, 64}, Dn % 32 == 0;
- * bf16 weights need K % 8 == 0 (16-byte rows). Pointers must be 16-byte
- * aligned (scales: 4-byte; bias: 16-byte), else MLA_ERR_ALIGNMENT.
+ * Tiling limits (else MLA_ERR_UNSUPPORTED): Dr in {16, 32, 64}, Dn % 32 == 0,
+ * and some channel tile width must divide N while keeping every head's rope
+ * region and every 32-channel block whole: a multiple of 16 up to 256 with
+ * bf16 weights, a multiple of 32 up to 192 with MXFP8 weights (one head
+ * always qualifies when D fits; mla_q_uproj_w_scale_group reports the MXFP8
+ * one, 0 when none). bf16 weights need K % 8 == 0 (16-byte rows). Pointers
+ * must be 16-byte aligned (scales: 4-byte, tiled scales 16-byte; bias:
+ * 16-byte), else MLA_ERR_ALIGNMENT.
  */
 MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_mode,
                              const void *x, const uint8_t *x_scales, const void *W,
