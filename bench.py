@@ -205,6 +205,11 @@ def make_device_inputs(w, dev, seed=0):
     }
 
 
+# the other rows' timing: warm-up calls, then timed calls (mean of CUDA events)
+PART_WARMUP = 10
+PART_ITERS = 50
+
+
 def time_loop(fn, iters, flush, stream, warmup=3):
     """Mean ms per call: CUDA events on `stream` around each call, the L2
     flush between calls outside the events."""
@@ -543,7 +548,7 @@ def run_parts(dev, stream, flush, pk, pk_src):
         a = torch.randn((R, C), device=dev, dtype=torch.float32).to(torch.bfloat16)
         codes = torch.empty((R, C), dtype=torch.uint8, device=dev)
         sc = torch.empty((R, (C + 31) // 32), dtype=torch.uint8, device=dev)
-        ms = time_loop(lambda: mlaq.mxfp8_quantize_rows(a, codes, sc), 20, flush, stream)
+        ms = time_loop(lambda: mlaq.mxfp8_quantize_rows(a, codes, sc), PART_ITERS, flush, stream, warmup=PART_WARMUP)
         byts = R * C * 2 + R * C + R * ((C + 31) // 32)
         gbs = byts / (ms * 1e-3) / 1e9
         parts[f"quantize_rows_bf16_{R}x{C}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
@@ -556,7 +561,7 @@ def run_parts(dev, stream, flush, pk, pk_src):
         a = torch.randn((R, C), device=dev, dtype=torch.float32).to(torch.bfloat16)
         codes = torch.empty((C, R), dtype=torch.uint8, device=dev)
         sc = torch.empty((C, (R + 31) // 32), dtype=torch.uint8, device=dev)
-        ms = time_loop(lambda: mlaq.mxfp8_quantize_cols(a, codes, sc), 20, flush, stream)
+        ms = time_loop(lambda: mlaq.mxfp8_quantize_cols(a, codes, sc), PART_ITERS, flush, stream, warmup=PART_WARMUP)
         byts = R * C * 2 + R * C + C * ((R + 31) // 32)
         gbs = byts / (ms * 1e-3) / 1e9
         parts[f"quantize_cols_bf16_{R}x{C}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
@@ -573,14 +578,14 @@ def run_parts(dev, stream, flush, pk, pk_src):
     qs = torch.empty((w.T, w.H, (w.D + 31) // 32), dtype=torch.uint8, device=dev)
     ms_g = time_loop(lambda: mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
                                       weight_mode="mxfp8", out_mode="mxfp8", x_scales=xs, w_scales=Ws,
-                                      q_out=qc, q_scales=qs, status=st), 30, flush, stream)
+                                      q_out=qc, q_scales=qs, status=st), PART_ITERS, flush, stream, warmup=PART_WARMUP)
     # the same operands with the quantizer writing the scales in the GEMM's tiled order
     G = mlaq.w_scale_group(w.T, w.K, w.H, w.Dn, w.Dr, inp["cos"].shape[0], inp["cos"].shape[1])
     _, xst = mlaq.mxfp8_quantize_rows(inp["x"], group=128)
     _, Wst = mlaq.mxfp8_quantize_rows(inp["W"], group=G)
     ms = time_loop(lambda: mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
                                     weight_mode="mxfp8_tiled", out_mode="mxfp8", x_scales=xst, w_scales=Wst,
-                                    q_out=qc, q_scales=qs, status=st), 30, flush, stream)
+                                    q_out=qc, q_scales=qs, status=st), PART_ITERS, flush, stream, warmup=PART_WARMUP)
     tf = w.fwd_flop() / (ms * 1e-3) / 1e12
     parts["fwd_mxfp8w_mxfp8out_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                           "frac_fp8_peak": round(tf / fp8_peak, 4),
@@ -589,7 +594,7 @@ def run_parts(dev, stream, flush, pk, pk_src):
                                           "ms_row_major_scales": round(ms_g, 4)}
     ms = time_loop(lambda: mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
                                     pos=inp["pos"], out_mode="mxfp8", q_out=qc, q_scales=qs, status=st),
-                   30, flush, stream)
+                   PART_ITERS, flush, stream, warmup=PART_WARMUP)
     tf = w.fwd_flop() / (ms * 1e-3) / 1e12
     parts["fwd_bf16w_mxfp8out_T4096_alone"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                                "frac_bf16_peak": round(tf / bf16_peak, 4)}
@@ -598,7 +603,7 @@ def run_parts(dev, stream, flush, pk, pk_src):
                       dtype=torch.uint8, device=dev)
     ms = time_loop(lambda: mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
                                     pos=inp["pos"], out_mode="mxfp8_bhsd_swizzled", q_out=qc, q_scales=qsw,
-                                    status=st), 30, flush, stream)
+                                    status=st), PART_ITERS, flush, stream, warmup=PART_WARMUP)
     tf = w.fwd_flop() / (ms * 1e-3) / 1e12
     parts["fwd_bf16w_mxfp8out_swizzled_scales_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                                          "frac_bf16_peak": round(tf / bf16_peak, 4)}
@@ -613,12 +618,12 @@ def run_parts(dev, stream, flush, pk, pk_src):
     rope = torch.empty((w.T, w.H, w.Dr), dtype=torch.bfloat16, device=dev)
     ms_d = time_loop(lambda: mlaq.bwd_dgrad(inp["dq"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
                                             pos=inp["pos"], dx=dx, status=st, dq_pre_rope=rope),
-                     20, flush, stream)
+                     PART_ITERS, flush, stream, warmup=PART_WARMUP)
     ms_w = time_loop(lambda: mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
                                             pos=inp["pos"], dW=dW, db=db, status=st, dq_pre_rope=rope),
-                     20, flush, stream)
+                     PART_ITERS, flush, stream, warmup=PART_WARMUP)
     ms_ws = time_loop(lambda: mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
-                                             pos=inp["pos"], dW=dW, db=db, status=st), 20, flush, stream)
+                                             pos=inp["pos"], dW=dW, db=db, status=st), PART_ITERS, flush, stream, warmup=PART_WARMUP)
     half = w.bwd_flop() / 2
     parts["bwd_T8192"] = {"dgrad_ms": round(ms_d, 4), "wgrad_db_ms": round(ms_w, 4),
                           "wgrad_db_self_rotating_ms": round(ms_ws, 4),
@@ -632,7 +637,7 @@ def run_parts(dev, stream, flush, pk, pk_src):
                                           inp["cos"].shape[1], 3),), dtype=torch.uint8, device=dev)
     ms_mx = time_loop(lambda: mlaq.bwd_mxfp8(inp["dq"], inp["W"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn,
                                              w.Dr, pos=inp["pos"], dx=dx, dW=dW, db=db, status=st,
-                                             workspace=ws), 20, flush, stream)
+                                             workspace=ws), PART_ITERS, flush, stream, warmup=PART_WARMUP)
     tf = w.bwd_flop() / (ms_mx * 1e-3) / 1e12
     parts["bwd_mxfp8_T8192"] = {"ms": round(ms_mx, 4), "TFLOP/s": round(tf, 1),
                                 "frac_fp8_peak": round(tf / fp8_peak, 4),
@@ -651,7 +656,7 @@ def run_parts(dev, stream, flush, pk, pk_src):
     o_key = torch.empty((T, H, Dn + Dr), dtype=torch.bfloat16, device=dev)
     o_value = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
     ms = time_loop(lambda: mlaq.kv_fwd(c_kv, W, k_pe, cos, sin, H, Dn, Dv, Dr, o_key=o_key, o_value=o_value,
-                                       status=st), 30, flush, stream)
+                                       status=st), PART_ITERS, flush, stream, warmup=PART_WARMUP)
     flop = 2 * T * K * H * (Dn + Dv)
     byts = (T * K + H * (Dn + Dv) * K + T * Dr + T * H * (Dn + Dr) + T * H * Dv) * 2
     parts["kv_uproj_rope_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(flop / (ms * 1e-3) / 1e12, 1),
@@ -677,7 +682,7 @@ def run_parts(dev, stream, flush, pk, pk_src):
         mlaq.bwd_wgrad(inp["dq"], inp["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
                        dW=dW, db=None, status=st, dq_pre_rope=rope)
 
-    ms = time_loop(long_step, 10, flush, stream)
+    ms = time_loop(long_step, 20, flush, stream, warmup=PART_WARMUP)
     tf = (w.fwd_flop() + w.bwd_flop()) / (ms * 1e-3) / 1e12
     parts["long_yarn_T16384_fwd_bwd"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                          "frac_bf16_peak": round(tf / bf16_peak, 4)}
