@@ -155,10 +155,16 @@ def device_info(dev):
 
 
 def kernel_hash():
+    """Hash of the kernel sources' code: comments and blank space removed, so
+    an edit to a comment does not invalidate the captured DRAM counters."""
+    import re
     h = hashlib.sha256()
     for name in ("fwd.cu", "bwd.cu", "quantize.cu", "ptx.cuh", "mx.cuh"):
-        with open(os.path.join(ROOT, "up_proj_gemm_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "up_proj_gemm_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                  # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

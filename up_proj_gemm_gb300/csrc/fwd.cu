@@ -11,16 +11,20 @@
 //     running together share weight tiles in L2);
 //   * warp 0: TMA producer, filling an S-stage shared-memory ring with x and
 //     W tiles (128-byte rows, 128-byte swizzle). For MXFP8 weights it also
-//     gathers the E8M0 scale bytes of both operands with 4-byte cp.async
-//     into the 32x16-byte layout that tcgen05.cp replicates into TMEM;
+//     brings the E8M0 scale bytes of both operands into the 32x16-byte
+//     layout that tcgen05.cp replicates into TMEM: one 512-byte bulk copy
+//     per 128-row chunk when the scales come pre-tiled, else a gather with
+//     4-byte cp.async;
 //   * warp 1: one thread issues tcgen05.mma (M=128, N=BN, K=16 bf16 or K=32
 //     block-scaled E4M3) into a double-buffered fp32 TMEM accumulator and
 //     commits each stage back to the producer;
-//   * warps 2-5: epilogue. Each thread owns one token row of the tile
-//     (tcgen05.ld 32x32b), adds the bias, applies the rotate-half RoPE pair
-//     (i, i+Dr/2) thread-locally, and writes bf16 or MXFP8 (per-32-channel
-//     amax -> E8M0 scale -> E4M3 codes) with 16-byte stores into a fresh
-//     output. The next tile's mainloop runs in the other accumulator buffer
+//   * warps 2-9: epilogue, two per TMEM lane quadrant. Each thread owns one
+//     token row of the tile (tcgen05.ld 32x32b) for half of its columns,
+//     adds the bias, applies the rotate-half RoPE pair (i, i+Dr/2)
+//     thread-locally, and converts to bf16 or MXFP8 (per-32-channel amax ->
+//     E8M0 scale -> E4M3 codes). The values pass through a ring of
+//     shared-memory slots and leave as TMA tile stores into a fresh output.
+//     The next tile's main loop runs in the other accumulator buffer
 //     meanwhile.
 //
 // Tiles never split a rope region or an MXFP8 block (the host picks BN so).
