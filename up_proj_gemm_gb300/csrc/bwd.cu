@@ -8,38 +8,41 @@
 //   bgrad  db[N]    = sum_t dq_pre[t, N]          (review: "BF16 bias gradient
 //                                                   remains missing")
 // The pages run the RoPE backward as its own Triton kernel and hand dq_pre
-// to a library GEMM. Here the full dq_pre never exists in memory: dq tiles
-// land in shared memory by TMA, "transform" warps rotate the rope channels of
-// each tile in place (fp32 math, rounded to bf16, the MMA operand type),
-// fence them into the async proxy and release the stage to the MMA thread.
+// to a library GEMM. Here only the rope third of dq_pre is ever stored, and
+// on some shapes not even that. Persistent kernels (one CTA per SM), each
+// with a single-thread tcgen05.mma issuer and 128-byte-swizzled TMA stages:
 //
-// dgrad can also store the rotated rope channels it computes (dq_pre_rope
-// [T, H, Dr] bf16, exactly the MMA operand values); wgrad, given that
-// buffer, loads its rope tiles from it already rotated: the rotation then
-// runs once, in dgrad's operand path, where each thread reads its cos/sin row
-// once per tile, instead of once per 32-token stage in every wgrad tile.
+//   rope_pre_kernel (Dr = 64, Dn % 64 == 0): rotates every head's rope
+//     channels once into dq_pre_rope [T, H, 64] bf16 (the caller's buffer or
+//     dgrad's workspace); a thread takes 8 pairs of eight heads of a token,
+//     loading the token's table entries once.
+//   dgrad_pre_kernel: dx as a plain GEMM over [dq pass-through | rotated rope]:
+//     every 64-channel K chunk comes whole from one of the two. 256-token
+//     tiles are two M = 128 MMAs per stage into TMEM columns 0 and 256. The
+//     reduction is split by wave efficiency into fp32 partials that
+//     dgrad_reduce_kernel adds in a fixed order.
+//   dgrad_kernel (other shapes, or less workspace): A = dq [T x N] K-major,
+//     B = W [N x K] MN-major, reduction over channels, 64 per stage, with
+//     separate rings and producers for A and B (warps 0 and 14). Warps 2-5
+//     are the epilogue (bf16 dx, or fp32 partials when split); warps 6-13
+//     are "transform" warps. Each thread of those owns half of one token row
+//     for a whole work unit, keeps that row's cos/sin in registers, and
+//     rotates the rope channels of each dq tile in shared memory (fp32 math,
+//     rounded to bf16, the MMA operand type). They fence the tile into the
+//     async proxy and release the stage. They can also store the rotated
+//     channels to dq_pre_rope.
+//   wgrad_pre_kernel (paired heads: Dr = 64, Dn % 128 == 0, even H,
+//     K % 64 == 0, dq_pre_rope given): 256-channel tiles of two 128-channel
+//     sub-tiles in head-pair order, A = dq_pre^T MN-major from dq or the
+//     rotated buffer, B = x [T x K] MN-major, 64-token stages, two
+//     accumulators. Warps 10-17 sum db over the tokens of the first column
+//     tile, in a fixed order.
+//   wgrad_kernel (other shapes, or no hand-off): 128-channel tiles,
+//     32-token stages (each stage needs fresh table rows), three transform
+//     groups of 4 warps rotating the rope stages and summing db.
 //
-// Two persistent kernels (one CTA per SM), both with a single-thread
-// tcgen05.mma issuer, double-buffered TMEM accumulators and 128-byte-swizzled
-// TMA stages:
-//
-//   dgrad_kernel: A = dq [T x N] K-major (tokens x channels), B = W [N x K]
-//     MN-major (K contiguous); reduction over channels, 64 per stage. A and B
-//     have separate rings and producers (warps 0 and 14) so that dq tiles,
-//     the ones the transform rewrites, are fetched further ahead. Warps 2-5
-//     epilogue (bf16 dx, or fp32 partials when the reduction is split),
-//     warps 6-13 transform: each thread owns half of one token row for a
-//     whole work unit and keeps that row's cos/sin in registers.
-//   wgrad_kernel: A = dq^T MN-major (channels contiguous), B = x [T x K]
-//     MN-major; reduction over tokens. Warps 0 producer, 1 MMA, 2-5 epilogue,
-//     then three transform groups of 4 warps taking turns on stages (each
-//     stage brings new tokens, so new table rows); they also sum db over the
-//     tokens on the first column tile (fixed order, no atomics). Given the
-//     buffer dgrad stored, the rope tiles arrive rotated and the stages are
-//     64 tokens; otherwise 32.
-//
-// In both, a shared-memory "row" is 128 bytes = 64 consecutive channels of
-// one token, which is what the transform rewrites.
+// In the transform kernels a shared-memory "row" is 128 bytes = 64
+// consecutive channels of one token, which is what the transform rewrites.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
