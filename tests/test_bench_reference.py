@@ -24,3 +24,21 @@ def test_reference_arm_json_line():
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_kernel_hash_ignores_comments(tmp_path, monkeypatch):
+    """The DRAM counters in profiles/traffic.json stay valid across comment
+    edits of the kernel sources, and not across code edits."""
+    import shutil
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "up_proj_gemm_gb300" / "csrc"
+    shutil.copytree(os.path.join(ROOT, "up_proj_gemm_gb300", "csrc"), csrc)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_hash()
+    f = csrc / "fwd.cu"
+    src = f.read_text()
+    f.write_text("// a new comment line\n/* and a block\n   comment */\n" + src.replace("\n", "\n\n", 3))
+    assert bench.kernel_hash() == h0
+    f.write_text(src.replace("constexpr int kBM = 128;", "constexpr int kBM = 64;"))
+    assert bench.kernel_hash() != h0
