@@ -304,6 +304,26 @@ MLAQ_API int mla_q_uproj_bwd_mxfp8(const mla_q_shape *shape, const void *dq, con
                                    const int32_t *pos, void *dx, void *dW, void *db, void *workspace,
                                    size_t ws_bytes, int *dev_status, void *stream);
 
+/*
+ * mla_q_uproj_bwd_mxfp8 with W's columnwise MXFP8 copy prepared by the
+ * caller instead of W. W stays fixed across the micro-batches of a step, so
+ * it is quantized once instead of on every call. The results are bit for
+ * bit those of mla_q_uproj_bwd_mxfp8 given W.
+ *   wt [K, N] E4M3 codes (row pitch N): the columnwise quantization of W
+ *   [N, K], i.e. mxfp8_quantize_cols_tiled(N, K, MLA_IN_BF16, W, K, wt,
+ *   wt_scales, group, ...) with group = the b_group that
+ *   mla_q_uproj_bwd_mxfp8_layout reports for this shape. wt_scales then
+ *   holds mxfp8_grouped_scale_bytes(K, N/32, group) bytes. Both 16-byte
+ *   aligned, both required when dx is requested (else unused).
+ * Everything else as mla_q_uproj_bwd_mxfp8; the workspace's wt regions stay
+ * unused.
+ */
+MLAQ_API int mla_q_uproj_bwd_mxfp8_prepared(const mla_q_shape *shape, const void *dq, const uint8_t *wt,
+                                            const uint8_t *wt_scales, const void *x, const float *cos_tab,
+                                            const float *sin_tab, const int32_t *pos, void *dx, void *dW,
+                                            void *db, void *workspace, size_t ws_bytes, int *dev_status,
+                                            void *stream);
+
 /* KV side of the attention block: see mla_kv_uproj_fwd. */
 typedef struct {
     int64_t T;        /* tokens */
@@ -408,6 +428,18 @@ MLAQ_API int mxfp8_quantize_rows_tiled(int64_t R, int64_t C, int in_dtype, const
  */
 MLAQ_API int mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void *in,
                                  int64_t ld_in, uint8_t *codes_t, uint8_t *scales_t, void *stream);
+
+/*
+ * mxfp8_quantize_cols with the scales of the transposed copy written in the
+ * block-scaled GEMM's tiled order: scales_t = mxfp8_swizzle_scales_grouped
+ * of the [C, ceil(R/32)] scales with row groups of `group`, padding 0
+ * (mxfp8_grouped_scale_bytes(C, ceil(R/32), group) bytes). codes_t [C, R]
+ * as mxfp8_quantize_cols. Needs a 16-byte aligned input with a 16-byte row
+ * pitch and C a multiple of the vector width (else MLA_ERR_UNSUPPORTED); for
+ * the prepared weight of mla_q_uproj_bwd_mxfp8_prepared.
+ */
+MLAQ_API int mxfp8_quantize_cols_tiled(int64_t R, int64_t C, int in_dtype, const void *in, int64_t ld_in,
+                                       uint8_t *codes_t, uint8_t *scales_t, int64_t group, void *stream);
 
 /*
  * E8M0 scales in the tiled order block-scaled GEMMs read (TransformerEngine PR

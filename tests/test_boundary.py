@@ -367,3 +367,21 @@ def test_quantize_rows_tiled_checks(L):
     sc = ctypes.c_void_p(FAKE - 256)  # the input is at FAKE
     assert L.mxfp8_quantize_rows(10, 64, 1, p(0), 64, p(1), sc, None) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
     assert q(10, 64, 1, p(0), 64, p(1), sc, 128, None) == S["MLA_ERR_ALIAS"]
+
+
+def test_bwd_mxfp8_prepared_checks(L):
+    """mla_q_uproj_bwd_mxfp8_prepared: the prepared copy is wt and its scales
+    together, 16-byte aligned, and required when dx is asked for."""
+    s = shape(T=64, K=64, H=2, Dn=32, Dr=32, cs_rows=64, cs_width=32)
+    need = L.mla_q_uproj_workspace_size(ctypes.byref(s), 3)
+    f = L.mla_q_uproj_bwd_mxfp8_prepared
+    ws = p(20)
+    args = lambda wt, wts, dx=p(9): (ctypes.byref(s), p(0), wt, wts, p(2), p(3), p(4), None, dx, p(10), p(11),
+                                     ws, need, None, None)
+    assert f(*args(p(1), None)) == S["MLA_ERR_INVALID_ARG"]                 # scales missing
+    assert f(*args(None, None)) == S["MLA_ERR_INVALID_ARG"]                 # dx without W's copy
+    assert f(*args(ctypes.c_void_p(FAKE * 2 + 8), p(12))) == S["MLA_ERR_ALIGNMENT"]
+    assert f(*args(p(1), p(12))) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+    q = L.mxfp8_quantize_cols_tiled
+    assert q(64, 32, 1, p(0), 32, p(1), p(2), 0, None) == S["MLA_ERR_INVALID_ARG"]
+    assert q(0, 32, 1, None, 32, None, None, 128, None) == S["MLA_OK"]

@@ -212,3 +212,30 @@ def test_bwd_mxfp8_full_size_sampled(cuda_device):
         dqp_c = oracle.rope_bwd_f32(helpers.f64(inp["dq"][:, h0:h0 + 16].contiguous()), 16, w.Dn, w.Dr,
                                     cs, sn, pos).reshape(w.T, -1).astype(np.float64)
         _check_db(db[h0 * w.D:(h0 + 16) * w.D], dqp_c, f"db heads {h0}+")
+
+
+@pytest.mark.parametrize("name,ov", [SHAPES[0], SHAPES[3], SHAPES[4]])
+def test_prepared_weight_bit_identical(cuda_device, name, ov):
+    """mla_q_uproj_bwd_mxfp8_prepared with W's columnwise copy made once
+    (mxfp8_quantize_cols_tiled, the layout's b_group) gives the bytes of the
+    call that quantizes W itself; the prepared copy equals the one that call
+    leaves in its workspace."""
+    w = synth.workload(name, **ov)
+    inp, d = _inputs(w, 31, cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    ws = _workspace(w, d, cuda_device)
+    dx1, dW1, db1 = _run(w, d, st, ws)
+    ops = mlaq.bwd_mxfp8_operands(ws, w.T, w.K, w.H, w.Dn, w.Dr, d["cos"].shape[0], d["cos"].shape[1])
+    wt, wts = mlaq.bwd_mxfp8_prepare_weight(d["W"], w.T, w.H, w.Dn, w.Dr, d["cos"])
+    torch.cuda.synchronize()
+    assert torch.equal(wt, ops["wt"])
+    lay = mlaq.bwd_mxfp8_layout(w.T, w.K, w.H, w.Dn, w.Dr, d["cos"].shape[0], d["cos"].shape[1])
+    # the real scale entries agree (the workspace's padding bytes are unspecified)
+    G = lay["b_group"]
+    ws_s = ws[lay["wt_scales"]:lay["wt_scales"] + wts.numel()].cpu().numpy()
+    assert np.array_equal(helpers.sf_untile(wts.cpu().numpy(), w.K, w.N // 32, G),
+                          helpers.sf_untile(ws_s, w.K, w.N // 32, G))
+    dx2, dW2, db2 = mlaq.bwd_mxfp8(d["dq"], None, d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
+                                   status=st, prepared=(wt, wts))
+    mlaq.check_status(st)
+    assert torch.equal(dx1, dx2) and torch.equal(dW1, dW2) and torch.equal(db1, db2)

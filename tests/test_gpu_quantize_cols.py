@@ -75,3 +75,20 @@ def test_quantize_cols_full_size_sampled(cuda_device):
     rc, rs = oracle.mxfp8_quantize_columns(v[:, cols].double().numpy())
     assert np.array_equal(codes[cols.to(cuda_device)].cpu().numpy(), rc)
     assert np.array_equal(scales[cols.to(cuda_device)].cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("R,C,group", [(24576, 1536, 192), (4096, 1536, 192), (300, 64, 96), (1000, 40, 128)])
+def test_quantize_cols_tiled_scales(cuda_device, R, C, group):
+    """mxfp8_quantize_cols_tiled: the codes of mxfp8_quantize_cols and its
+    scales in the grouped tiled order (= mxfp8_swizzle_scales_grouped of the
+    row-major ones, padding 0; the buffer starts filled with 0xEE)."""
+    g = torch.Generator().manual_seed(R + C)
+    x = (torch.randn((R, C), generator=g) * 0.05).to(torch.bfloat16).to(cuda_device)
+    codes, scales = mlaq.mxfp8_quantize_cols(x)
+    n = int(mlaq.lib().mxfp8_grouped_scale_bytes(C, (R + 31) // 32, group))
+    buf = torch.full((n,), 0xEE, dtype=torch.uint8, device=cuda_device)
+    codes_t, tiled = mlaq.mxfp8_quantize_cols(x, scales=buf, group=group)
+    ref = mlaq.mxfp8_swizzle_scales(scales, group=group)
+    torch.cuda.synchronize()
+    assert torch.equal(codes_t, codes)
+    assert torch.equal(tiled, ref)

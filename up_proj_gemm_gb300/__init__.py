@@ -80,6 +80,8 @@ _SIGS = {
     "mxfp8_swizzle_scales": (_int, [_i64, _i64, _vp, _i64, _vp, _vp]),
     "mla_kv_uproj_fwd": (_int, [ctypes.POINTER(KvShape)] + [_vp] * 10),
     "mla_q_uproj_bwd_mxfp8": (_int, [ctypes.POINTER(Shape)] + [_vp] * 10 + [ctypes.c_size_t, _vp, _vp]),
+    "mla_q_uproj_bwd_mxfp8_prepared": (_int, [ctypes.POINTER(Shape)] + [_vp] * 11 + [ctypes.c_size_t, _vp, _vp]),
+    "mxfp8_quantize_cols_tiled": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _i64, _vp]),
     "mla_q_uproj_bwd_mxfp8_layout": (_int, [ctypes.POINTER(Shape), ctypes.POINTER(Mxfp8BwdLayout)]),
     "mxfp8_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "mxfp8_quantize_rows_tiled": (_int, [_i64, _i64, _int, _vp, _i64, _vp, _vp, _i64, _vp]),
@@ -334,12 +336,14 @@ def bwd_mxfp8_operands(workspace, T, K, H, Dn, Dr, cs_rows, cs_width) -> dict:
 
 
 def bwd_mxfp8(dq, W, x, cos, sin, H, Dn, Dr, pos=None, dx=True, dW=True, db=True, status=None, stream=None,
-              workspace=None):
+              workspace=None, prepared=None):
     """Backward with MXFP8 tensor-core GEMMs (``mla_q_uproj_bwd_mxfp8``):
     dx [T, K], dW [N, K], db [N] (bf16) from dq [T, H, D] bf16.
 
     Each of dx / dW / db: True allocates it, False/None skips it, or pass a
     tensor. W [N, K] is needed for dx, x [T, K] for dW (else may be None).
+    ``prepared``: W's columnwise MXFP8 copy from ``bwd_mxfp8_prepare_weight``
+    (then W must be None; ``mla_q_uproj_bwd_mxfp8_prepared``, same results).
     The workspace (``workspace_size(..., which=3)`` bytes, uint8) is
     allocated unless passed; afterwards it holds the quantized operands
     (``bwd_mxfp8_operands``). Returns (dx, dW, db), None where skipped."""
@@ -353,14 +357,22 @@ def bwd_mxfp8(dq, W, x, cos, sin, H, Dn, Dr, pos=None, dx=True, dW=True, db=True
         raise ValueError("dq must hold T * H * (Dn + Dr) elements")
     want_dx = dx is not None and dx is not False
     want_dw = dW is not None and dW is not False
-    if want_dx:
-        _need(W, "W", torch.bfloat16, dev, ndim=2)
+    if prepared is not None:
+        if W is not None:
+            raise ValueError("pass either W or its prepared copy, not both")
+        wt, wt_s = prepared
+        _need(wt, "wt", torch.uint8, dev, ndim=2)
+        _need(wt_s, "wt_scales", torch.uint8, dev, ndim=1)
+        K = wt.shape[0]
+    else:
+        if want_dx:
+            _need(W, "W", torch.bfloat16, dev, ndim=2)
+        ref = W if want_dx else x
+        if ref is None:
+            raise ValueError("need W (for dx) or x (for dW) to know K")
+        K = ref.shape[1]
     if want_dw:
         _need(x, "x", torch.bfloat16, dev, ndim=2)
-    ref = W if want_dx else x
-    if ref is None:
-        raise ValueError("need W (for dx) or x (for dW) to know K")
-    K = ref.shape[1]
     if pos is not None:
         _need(pos, "pos", torch.int32, dev, ndim=1)
     if dx is True:
@@ -380,10 +392,26 @@ def bwd_mxfp8(dq, W, x, cos, sin, H, Dn, Dr, pos=None, dx=True, dW=True, db=True
     if workspace is None and need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _call(lib().mla_q_uproj_bwd_mxfp8, "mla_q_uproj_bwd_mxfp8", ctypes.byref(s), _ptr(dq),
-          _ptr(W) if want_dx else None, _ptr(x) if want_dw else None, _ptr(cos), _ptr(sin), _ptr(pos),
-          _ptr(dx), _ptr(dW), _ptr(db), _ptr(workspace), ws_bytes, _ptr(status), _stream(dev, stream))
+    if prepared is not None:
+        _call(lib().mla_q_uproj_bwd_mxfp8_prepared, "mla_q_uproj_bwd_mxfp8_prepared", ctypes.byref(s), _ptr(dq),
+              _ptr(prepared[0]), _ptr(prepared[1]), _ptr(x) if want_dw else None, _ptr(cos), _ptr(sin),
+              _ptr(pos), _ptr(dx), _ptr(dW), _ptr(db), _ptr(workspace), ws_bytes, _ptr(status),
+              _stream(dev, stream))
+    else:
+        _call(lib().mla_q_uproj_bwd_mxfp8, "mla_q_uproj_bwd_mxfp8", ctypes.byref(s), _ptr(dq),
+              _ptr(W) if want_dx else None, _ptr(x) if want_dw else None, _ptr(cos), _ptr(sin), _ptr(pos),
+              _ptr(dx), _ptr(dW), _ptr(db), _ptr(workspace), ws_bytes, _ptr(status), _stream(dev, stream))
     return dx, dW, db
+
+
+def bwd_mxfp8_prepare_weight(W, T, H, Dn, Dr, cos, stream=None):
+    """W [N, K] bf16 -> (wt [K, N] E4M3 codes, wt_scales flat, in the GEMM's
+    tiled order): the copy ``bwd_mxfp8(..., prepared=...)`` takes in place of
+    W, to quantize a weight once for several backward calls."""
+    _need(W, "W", torch.bfloat16, ndim=2)
+    N, K = W.shape
+    G = bwd_mxfp8_layout(max(int(T), 1), K, H, Dn, Dr, cos.shape[0], cos.shape[1])["b_group"]
+    return mxfp8_quantize_cols(W, group=G, stream=stream)
 
 
 def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None, group=None):
@@ -417,10 +445,12 @@ def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None, group=None):
     return codes, scales
 
 
-def mxfp8_quantize_cols(inp, codes=None, scales=None, stream=None):
+def mxfp8_quantize_cols(inp, codes=None, scales=None, stream=None, group=None):
     """Columnwise MXFP8 of a 2-D fp32/bf16 CUDA tensor [R, C], i.e. the rowwise
     quantization of its transpose -> (codes uint8 [C, R], scales uint8
-    [C, ceil(R/32)]). A row pitch larger than C is taken from ``inp.stride(0)``."""
+    [C, ceil(R/32)]). A row pitch larger than C is taken from ``inp.stride(0)``.
+    With ``group``, the scales come back flat in the block-scaled GEMM's tiled
+    order with row groups of that size (mxfp8_quantize_cols_tiled)."""
     if inp.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("input must be float32 or bfloat16")
     if not inp.is_cuda or inp.dim() != 2 or inp.stride(1) != 1:
@@ -430,9 +460,16 @@ def mxfp8_quantize_cols(inp, codes=None, scales=None, stream=None):
     dev = inp.device
     if codes is None:
         codes = torch.empty((C, R), dtype=torch.uint8, device=dev)
+    dt = 0 if inp.dtype == torch.float32 else 1
+    if group is not None:
+        if scales is None:
+            n = int(lib().mxfp8_grouped_scale_bytes(C, (R + 31) // 32, int(group)))
+            scales = torch.empty((n,), dtype=torch.uint8, device=dev)
+        _call(lib().mxfp8_quantize_cols_tiled, "mxfp8_quantize_cols_tiled", R, C, dt, _ptr(inp), ld_in,
+              _ptr(codes), _ptr(scales), int(group), _stream(dev, stream))
+        return codes, scales
     if scales is None:
         scales = torch.empty((C, (R + 31) // 32), dtype=torch.uint8, device=dev)
-    dt = 0 if inp.dtype == torch.float32 else 1
     _call(lib().mxfp8_quantize_cols, "mxfp8_quantize_cols", R, C, dt, _ptr(inp), ld_in, _ptr(codes),
           _ptr(scales), _stream(dev, stream))
     return codes, scales

@@ -431,17 +431,22 @@ MLAQ_API int mla_q_uproj_bwd_mxfp8_layout(const mla_q_shape* shape, mla_mxfp8_bw
     return MLA_OK;
 }
 
-MLAQ_API int mla_q_uproj_bwd_mxfp8(const mla_q_shape* shape, const void* dq, const void* W, const void* x,
-                                   const float* cos_tab, const float* sin_tab, const int32_t* pos, void* dx,
-                                   void* dW, void* db, void* workspace, size_t ws_bytes, int* dev_status,
-                                   void* stream) {
+}  // extern "C"
+
+// The MXFP8 backward, with W or (wt, wt_s), its columnwise MXFP8 copy.
+static int bwd_mxfp8_call(const mla_q_shape* shape, const void* dq, const void* W, const uint8_t* wt,
+                          const uint8_t* wt_s, const void* x, const float* cos_tab, const float* sin_tab,
+                          const int32_t* pos, void* dx, void* dW, void* db, void* workspace, size_t ws_bytes,
+                          int* dev_status, void* stream) {
     int D;
     int64_t N;
     int st = check_shape(shape, &D, &N);
     if (st != MLA_OK) return st;
     const mla_q_shape& s = *shape;
     if (!dx && !dW && !db) return MLA_ERR_INVALID_ARG;
-    if (s.T > 0 && (!dq || (dx && !W) || (dW && !x))) return MLA_ERR_INVALID_ARG;
+    const bool prepared = wt != nullptr || wt_s != nullptr;
+    if (prepared && (!wt || !wt_s || W)) return MLA_ERR_INVALID_ARG;
+    if (s.T > 0 && (!dq || (dx && !W && !prepared) || (dW && !x))) return MLA_ERR_INVALID_ARG;
     st = check_table_and_positions(&s, cos_tab, sin_tab, pos);
     if (st != MLA_OK) return st;
     const size_t need = mla_q_uproj_workspace_size(shape, 3);
@@ -450,13 +455,16 @@ MLAQ_API int mla_q_uproj_bwd_mxfp8(const mla_q_shape* shape, const void* dq, con
     if (fwd_tile_n(s.K, (int)s.K, (int)s.K, 0, 192, 32) == 0) return MLA_ERR_UNSUPPORTED;
     if (!aligned(dq, 16) || !aligned(W, 16) || !aligned(x, 16) || !aligned(dx, 16) || !aligned(dW, 16) ||
         !aligned(db, 4) || !aligned(cos_tab, 4) || !aligned(sin_tab, 4) || !aligned(pos, 4) ||
-        !aligned(dev_status, 4) || !aligned(workspace, 16))
+        !aligned(dev_status, 4) || !aligned(workspace, 16) || !aligned(wt, 16) || !aligned(wt_s, 16))
         return MLA_ERR_ALIGNMENT;
     const int64_t table = s.cs_rows * s.cs_width * 4;
+    const int64_t G = fwd_tile_n(s.K, (int)s.K, (int)s.K, 0, 192, 32);
+    const int64_t wts = prepared && dx ? (int64_t)sf_tiled_bytes(s.K, N / 32, G) : 0;
     const Range outs[] = {rng(dx, s.T * s.K * 2), rng(dW, N * s.K * 2), rng(db, N * 2), rng(dev_status, 4),
                           rng(workspace, (int64_t)need)};
     const Range ins[] = {rng(dq, s.T * N * 2), rng(W, dx ? N * s.K * 2 : 0), rng(x, dW ? s.T * s.K * 2 : 0),
-                         rng(cos_tab, table), rng(sin_tab, table), rng(pos, s.T * 4)};
+                         rng(cos_tab, table), rng(sin_tab, table), rng(pos, s.T * 4),
+                         rng(wt, prepared && dx ? s.K * N : 0), rng(wt_s, wts)};
     if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
     BwdArgs a{};
     a.T = s.T;
@@ -478,8 +486,29 @@ MLAQ_API int mla_q_uproj_bwd_mxfp8(const mla_q_shape* shape, const void* dq, con
     a.workspace = workspace;
     a.ws_bytes = ws_bytes;
     a.status = dev_status;
+    a.wt = dx ? wt : nullptr;
+    a.wt_s = dx ? wt_s : nullptr;
     // T == 0: dx is empty; dW = 0 and db = 0 are written
     return launch_bwd_mxfp8(a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" {
+
+MLAQ_API int mla_q_uproj_bwd_mxfp8(const mla_q_shape* shape, const void* dq, const void* W, const void* x,
+                                   const float* cos_tab, const float* sin_tab, const int32_t* pos, void* dx,
+                                   void* dW, void* db, void* workspace, size_t ws_bytes, int* dev_status,
+                                   void* stream) {
+    return bwd_mxfp8_call(shape, dq, W, nullptr, nullptr, x, cos_tab, sin_tab, pos, dx, dW, db, workspace,
+                          ws_bytes, dev_status, stream);
+}
+
+MLAQ_API int mla_q_uproj_bwd_mxfp8_prepared(const mla_q_shape* shape, const void* dq, const uint8_t* wt,
+                                            const uint8_t* wt_scales, const void* x, const float* cos_tab,
+                                            const float* sin_tab, const int32_t* pos, void* dx, void* dW,
+                                            void* db, void* workspace, size_t ws_bytes, int* dev_status,
+                                            void* stream) {
+    return bwd_mxfp8_call(shape, dq, nullptr, wt, wt_scales, x, cos_tab, sin_tab, pos, dx, dW, db, workspace,
+                          ws_bytes, dev_status, stream);
 }
 
 MLAQ_API int mla_kv_uproj_fwd(const mla_kv_shape* shape, const void* c_kv, const void* W, const void* k_pe,
@@ -576,6 +605,30 @@ MLAQ_API int mxfp8_quantize_cols(int64_t R, int64_t C, int in_dtype, const void*
     if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
     return launch_mxfp8_quantize_cols(R, C, in_dtype, in, ld_in, codes_t, scales_t,
                                       static_cast<cudaStream_t>(stream));
+}
+
+MLAQ_API int mxfp8_quantize_cols_tiled(int64_t R, int64_t C, int in_dtype, const void* in, int64_t ld_in,
+                                       uint8_t* codes_t, uint8_t* scales_t, int64_t group, void* stream) {
+    if (R < 0 || C < 0 || ld_in < C || group <= 0) return MLA_ERR_INVALID_ARG;
+    if (in_dtype != MLA_IN_F32 && in_dtype != MLA_IN_BF16) return MLA_ERR_INVALID_ARG;
+    if (R == 0 || C == 0) return MLA_OK;
+    if (!in || !codes_t || !scales_t) return MLA_ERR_INVALID_ARG;
+    const int64_t esz = in_dtype == MLA_IN_F32 ? 4 : 2;
+    if (!aligned(in, (uintptr_t)esz)) return MLA_ERR_ALIGNMENT;
+    // the tiled scale order is written by the tiled kernel only (16-byte rows)
+    if (!aligned(in, 16) || (ld_in * esz) % 16 || C % (16 / esz)) return MLA_ERR_UNSUPPORTED;
+    const int64_t nbr = (R + 31) / 32;
+    const int64_t sbytes = (int64_t)sf_tiled_bytes(C, nbr, group);
+    const Range outs[] = {rng(codes_t, C * R), rng(scales_t, sbytes)};
+    const Range ins[] = {rng(in, ((R - 1) * ld_in + C) * esz)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the kernel writes the real (row, block) entries; padding rows of a
+    // group's last 128-row tile and padding columns read as 0
+    if (group % 128 || C % group || nbr % 4) {
+        if (cudaMemsetAsync(scales_t, 0, (size_t)sbytes, s) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    return launch_mxfp8_quantize_cols_tiled_sf(R, C, in_dtype, in, ld_in, codes_t, R, scales_t, group, s);
 }
 
 MLAQ_API size_t mxfp8_swizzled_scale_bytes(int64_t rows, int64_t cols) {

@@ -418,9 +418,15 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
                                ws + L.qb_s, want_db ? reinterpret_cast<float*>(ws + L.dbp) : nullptr, stream);
     if (st != MLA_OK) return st;
     if (want_dx) {
-        // 2. W [N, K] -> wt [K, N], blocks along N; 3. dx = qa . wt^T (block-scaled GEMM, reduction over N)
-        st = launch_mxfp8_quantize_cols_tiled_sf(N, K, MLA_IN_BF16, a.W, K, ws + L.wt, N, ws + L.wt_s, L.G, stream);
-        if (st != MLA_OK) return st;
+        // 2. W [N, K] -> wt [K, N], blocks along N (unless the caller prepared it);
+        // 3. dx = qa . wt^T (block-scaled GEMM, reduction over N)
+        const uint8_t* wt = a.wt ? a.wt : ws + L.wt;
+        const uint8_t* wt_s = a.wt ? a.wt_s : ws + L.wt_s;
+        if (!a.wt) {
+            st = launch_mxfp8_quantize_cols_tiled_sf(N, K, MLA_IN_BF16, a.W, K, ws + L.wt, N, ws + L.wt_s, L.G,
+                                                     stream);
+            if (st != MLA_OK) return st;
+        }
         FwdArgs g{};
         g.T = T;
         g.K = N;
@@ -431,8 +437,8 @@ int launch_bwd_mxfp8(const BwdArgs& a, cudaStream_t stream) {
         g.out_mode = MLA_OUT_BF16;
         g.x = ws + L.qa;
         g.x_scales = ws + L.qa_s;
-        g.W = ws + L.wt;
-        g.w_scales = ws + L.wt_s;
+        g.W = wt;
+        g.w_scales = wt_s;
         g.sf_tiled = 1;
         g.sf_group = (int)L.G;
         g.q_out = a.dx;

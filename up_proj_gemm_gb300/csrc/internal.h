@@ -129,6 +129,10 @@ struct BwdArgs {
     void* workspace; // dgrad split partials (see dgrad_workspace_bytes)
     size_t ws_bytes;
     int* status;
+    // MXFP8 backward only: W's columnwise MXFP8 copy prepared by the caller
+    // (wt [K, N] codes, scales in the GEMM's tiled order); W is then unused
+    const uint8_t* wt = nullptr;
+    const uint8_t* wt_s = nullptr;
 };
 int launch_dgrad(const BwdArgs& a, cudaStream_t stream);
 // dgrad's split of the channel reduction for this shape on a device with
