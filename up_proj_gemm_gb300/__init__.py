@@ -14,6 +14,7 @@ wgrad, plus the bias gradient.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import threading
 
@@ -117,7 +118,7 @@ def wait_selftest(arrive: bool, limit_ms: float, status: torch.Tensor, stream=No
     """Run the bounded-wait self-test (mla_wait_selftest) on the status
     tensor's device: with arrive=False a device wait gives up after limit_ms
     and MLA_ERR_TIMEOUT lands in ``status``; with arrive=True nothing does."""
-    _need(status, "status", torch.int32)
+    _need(status, "status", torch.int32, min_numel=1)
     _call(lib().mla_wait_selftest, "mla_wait_selftest", int(bool(arrive)), int(round(limit_ms * 1e6)),
           _ptr(status), _stream(status.device, stream))
 
@@ -136,19 +137,48 @@ def _stream(device, stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _need(t, name, dtype, device=None, ndim=None):
+def _need(t, name, dtype, device=None, ndim=None, shape=None, numel=None, min_numel=None):
+    """Check a tensor argument. The C ABI receives bare pointers, so every
+    extent a kernel reads or writes is checked here: type, dtype, rank and
+    size first, then device and layout."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {list(shape)}, got {list(t.shape)}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got {t.numel()}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name} must hold at least {min_numel} elements, got {t.numel()}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if device is not None and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if ndim is not None and t.dim() != ndim:
-        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def _cols(t):
+    """Last extent of a tensor argument (None when it has none), read before
+    `_need` has checked it."""
+    return t.shape[-1] if isinstance(t, torch.Tensor) and t.dim() > 0 else None
+
+
+def _tables(cos, sin, dev, T, pos):
+    """The rotary tables (fp32 [rows, width], same shape) and positions (int32 [T])."""
+    _need(cos, "cos", torch.float32, dev, ndim=2)
+    _need(sin, "sin", torch.float32, dev, shape=cos.shape)
+    if pos is not None:
+        _need(pos, "pos", torch.int32, dev, shape=(T,))
+
+
+def _status(status, dev):
+    """The optional device status word (int32, at least one element)."""
+    if status is not None:
+        _need(status, "status", torch.int32, dev, min_numel=1)
 
 
 def _shape(T, K, H, Dn, Dr, cos):
@@ -192,34 +222,40 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
     in_dtype = torch.uint8 if wm else torch.bfloat16
     dev = x.device
     _need(x, "x", in_dtype, ndim=2)
-    _need(W, "W", in_dtype, dev, ndim=2)
-    _need(cos, "cos", torch.float32, dev, ndim=2)
-    _need(sin, "sin", torch.float32, dev, ndim=2)
-    if cos.shape != sin.shape:
-        raise ValueError("cos and sin must have the same shape")
     T, K = x.shape
     D = Dn + Dr
     N = H * D
-    if tuple(W.shape) != (N, K):
-        raise ValueError(f"W must be [{N}, {K}]")
+    _need(W, "W", in_dtype, dev, shape=(N, K))
+    _tables(cos, sin, dev, T, pos)
+    _status(status, dev)
     if bias is not None:
-        _need(bias, "bias", torch.bfloat16, dev, ndim=1)
-    if pos is not None:
-        _need(pos, "pos", torch.int32, dev, ndim=1)
-    if wm:  # "mxfp8": [rows, K/32] scales; "mxfp8_tiled": flat tiled buffers
-        _need(x_scales, "x_scales", torch.uint8, dev, ndim=1 if wm == 2 else 2)
-        _need(w_scales, "w_scales", torch.uint8, dev, ndim=1 if wm == 2 else 2)
+        _need(bias, "bias", torch.bfloat16, dev, shape=(N,))
+    if wm == 1:  # [rows, K/32] scales (K not a multiple of 32 is refused by the library)
+        kb = (K + 31) // 32
+        _need(x_scales, "x_scales", torch.uint8, dev, shape=(T, kb))
+        _need(w_scales, "w_scales", torch.uint8, dev, shape=(N, kb))
+    elif wm == 2:  # flat buffers in the tiled order: x in 128-row groups, W in the kernel's column tiles
+        kb = K // 32
+        G = w_scale_group(T, K, H, Dn, Dr, cos.shape[0], cos.shape[1])
+        _need(x_scales, "x_scales", torch.uint8, dev, ndim=1,
+              min_numel=int(lib().mxfp8_grouped_scale_bytes(T, kb, 128)))
+        _need(w_scales, "w_scales", torch.uint8, dev, ndim=1,
+              min_numel=int(lib().mxfp8_grouped_scale_bytes(N, kb, G)) if G else None)
+    nb = (D + 31) // 32
+    if out_mode == "mxfp8_bhsd_swizzled":
+        sshape = (H, int(lib().mxfp8_swizzled_scale_bytes(T, nb)))
+    elif out_mode == "mxfp8_bhsd":
+        sshape = (H, T, nb)
+    else:
+        sshape = (T, H, nb)
+    q_dtype = torch.uint8 if om else torch.bfloat16
     if q_out is None:
-        q_out = torch.empty((T, H, D), dtype=torch.uint8 if om else torch.bfloat16, device=dev)
+        q_out = torch.empty((T, H, D), dtype=q_dtype, device=dev)
+    _need(q_out, "q_out", q_dtype, dev, numel=T * N)
     if om and q_scales is None:
-        nb = (D + 31) // 32
-        if out_mode == "mxfp8_bhsd_swizzled":
-            sshape = (H, int(lib().mxfp8_swizzled_scale_bytes(T, nb)))
-        elif out_mode == "mxfp8_bhsd":
-            sshape = (H, T, nb)
-        else:
-            sshape = (T, H, nb)
         q_scales = torch.empty(sshape, dtype=torch.uint8, device=dev)
+    if om:
+        _need(q_scales, "q_scales", torch.uint8, dev, numel=math.prod(sshape))
     s = _shape(T, K, H, Dn, Dr, cos)
     _call(lib().mla_q_uproj_fwd, "mla_q_uproj_fwd", ctypes.byref(s), wm, om, _ptr(x),
           _ptr(x_scales), _ptr(W), _ptr(w_scales), _ptr(bias), _ptr(cos), _ptr(sin), _ptr(pos),
@@ -228,10 +264,9 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
 
 
 def _rope_buf(t, T, H, Dr, dev):
+    """The optional rope hand-off buffer: contiguous bf16 holding T * H * Dr."""
     if t is not None:
-        _need(t, "dq_pre_rope", torch.bfloat16, dev)
-        if t.numel() != T * H * Dr or not t.is_contiguous():
-            raise ValueError("dq_pre_rope must be a contiguous [T, H, Dr] bf16 tensor")
+        _need(t, "dq_pre_rope", torch.bfloat16, dev, numel=T * H * Dr)
     return t
 
 
@@ -244,24 +279,24 @@ def bwd_dgrad(dq, W, cos, sin, H, Dn, Dr, pos=None, dx=None, status=None, stream
     least ``which=4`` bytes a slower one that needs less. ``dq_pre_rope`` (a [T, H, Dr] bf16 tensor, or
     None) receives the rotated rope channels, for bwd_wgrad."""
     dev = dq.device
-    _need(dq, "dq", torch.bfloat16)
-    _need(W, "W", torch.bfloat16, dev, ndim=2)
-    _need(cos, "cos", torch.float32, dev, ndim=2)
-    _need(sin, "sin", torch.float32, dev, ndim=2)
-    T = dq.shape[0]
-    N, K = W.shape
-    if dq.numel() != T * N:
-        raise ValueError("dq must hold T * H * (Dn + Dr) elements")
-    if pos is not None:
-        _need(pos, "pos", torch.int32, dev, ndim=1)
+    T = dq.shape[0] if isinstance(dq, torch.Tensor) and dq.dim() > 0 else 0
+    N = H * (Dn + Dr)
+    K = _cols(W)
+    _need(dq, "dq", torch.bfloat16, numel=T * N)
+    _need(W, "W", torch.bfloat16, dev, ndim=2, shape=(N, K))
+    _tables(cos, sin, dev, T, pos)
+    _status(status, dev)
     if dx is None:
         dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    _need(dx, "dx", torch.bfloat16, dev, numel=T * K)
     _rope_buf(dq_pre_rope, T, H, Dr, dev)
     s = _shape(T, K, H, Dn, Dr, cos)
     with torch.cuda.device(dev):
         need = int(lib().mla_q_uproj_workspace_size(ctypes.byref(s), 1))
     if workspace is None and need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, dev, ndim=1)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _call(lib().mla_q_uproj_bwd_dgrad, "mla_q_uproj_bwd_dgrad", ctypes.byref(s), _ptr(dq), _ptr(W),
           _ptr(cos), _ptr(sin), _ptr(pos), _ptr(dx), _ptr(dq_pre_rope), _ptr(workspace), ws_bytes,
@@ -278,22 +313,21 @@ def bwd_wgrad(dq, x, cos, sin, H, Dn, Dr, pos=None, dW=None, db=True, status=Non
     same dq (its rope tiles are then read instead of rotated again).
     Returns (dW, db-or-None)."""
     dev = dq.device
-    _need(dq, "dq", torch.bfloat16)
     _need(x, "x", torch.bfloat16, dev, ndim=2)
-    _need(cos, "cos", torch.float32, dev, ndim=2)
-    _need(sin, "sin", torch.float32, dev, ndim=2)
     T, K = x.shape
     N = H * (Dn + Dr)
-    if dq.numel() != T * N:
-        raise ValueError("dq must hold T * H * (Dn + Dr) elements")
-    if pos is not None:
-        _need(pos, "pos", torch.int32, dev, ndim=1)
+    _need(dq, "dq", torch.bfloat16, numel=T * N)
+    _tables(cos, sin, dev, T, pos)
+    _status(status, dev)
     if dW is None:
         dW = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    _need(dW, "dW", torch.bfloat16, dev, numel=N * K)
     if db is True:
         db = torch.empty((N,), dtype=torch.bfloat16, device=dev)
     elif db is False:
         db = None
+    if db is not None:
+        _need(db, "db", torch.bfloat16, dev, numel=N)
     _rope_buf(dq_pre_rope, T, H, Dr, dev)
     s = _shape(T, K, H, Dn, Dr, cos)
     _call(lib().mla_q_uproj_bwd_wgrad, "mla_q_uproj_bwd_wgrad", ctypes.byref(s), _ptr(dq),
@@ -348,49 +382,47 @@ def bwd_mxfp8(dq, W, x, cos, sin, H, Dn, Dr, pos=None, dx=True, dW=True, db=True
     allocated unless passed; afterwards it holds the quantized operands
     (``bwd_mxfp8_operands``). Returns (dx, dW, db), None where skipped."""
     dev = dq.device
-    _need(dq, "dq", torch.bfloat16)
-    _need(cos, "cos", torch.float32, dev, ndim=2)
-    _need(sin, "sin", torch.float32, dev, ndim=2)
-    T = dq.shape[0]
+    T = dq.shape[0] if isinstance(dq, torch.Tensor) and dq.dim() > 0 else 0
     N = H * (Dn + Dr)
-    if dq.numel() != T * N:
-        raise ValueError("dq must hold T * H * (Dn + Dr) elements")
+    _need(dq, "dq", torch.bfloat16, numel=T * N)
+    _tables(cos, sin, dev, T, pos)
+    _status(status, dev)
     want_dx = dx is not None and dx is not False
     want_dw = dW is not None and dW is not False
     if prepared is not None:
         if W is not None:
             raise ValueError("pass either W or its prepared copy, not both")
         wt, wt_s = prepared
-        _need(wt, "wt", torch.uint8, dev, ndim=2)
-        _need(wt_s, "wt_scales", torch.uint8, dev, ndim=1)
-        K = wt.shape[0]
+        K = wt.shape[0] if isinstance(wt, torch.Tensor) and wt.dim() == 2 else None
+        _need(wt, "wt", torch.uint8, dev, ndim=2, shape=(K, N))
+        G = bwd_mxfp8_layout(max(int(T), 1), K, H, Dn, Dr, cos.shape[0], cos.shape[1])["b_group"]
+        _need(wt_s, "wt_scales", torch.uint8, dev, ndim=1,
+              min_numel=int(lib().mxfp8_grouped_scale_bytes(K, N // 32, G)))
+    elif want_dx:
+        K = _cols(W)
+        _need(W, "W", torch.bfloat16, dev, ndim=2, shape=(N, K))
+    elif x is not None:
+        K = _cols(x)
     else:
-        if want_dx:
-            _need(W, "W", torch.bfloat16, dev, ndim=2)
-        ref = W if want_dx else x
-        if ref is None:
-            raise ValueError("need W (for dx) or x (for dW) to know K")
-        K = ref.shape[1]
-    if want_dw:
-        _need(x, "x", torch.bfloat16, dev, ndim=2)
-    if pos is not None:
-        _need(pos, "pos", torch.int32, dev, ndim=1)
-    if dx is True:
-        dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
-    elif dx is False:
-        dx = None
-    if dW is True:
-        dW = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
-    elif dW is False:
-        dW = None
-    if db is True:
-        db = torch.empty((N,), dtype=torch.bfloat16, device=dev)
-    elif db is False:
-        db = None
+        raise ValueError("need W (for dx) or x (for dW) to know K")
+    if want_dw or x is not None:
+        _need(x, "x", torch.bfloat16, dev, ndim=2, shape=(T, K))
+    outs = {}
+    for name, t, shape in (("dx", dx, (T, K)), ("dW", dW, (N, K)), ("db", db, (N,))):
+        if t is True:
+            t = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        elif t is False:
+            t = None
+        if t is not None:
+            _need(t, name, torch.bfloat16, dev, numel=math.prod(shape))
+        outs[name] = t
+    dx, dW, db = outs["dx"], outs["dW"], outs["db"]
     s = _shape(T, K, H, Dn, Dr, cos)
     need = int(lib().mla_q_uproj_workspace_size(ctypes.byref(s), 3))
     if workspace is None and need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, dev, ndim=1)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if prepared is not None:
         _call(lib().mla_q_uproj_bwd_mxfp8_prepared, "mla_q_uproj_bwd_mxfp8_prepared", ctypes.byref(s), _ptr(dq),
@@ -430,16 +462,19 @@ def mxfp8_quantize_rows(inp, codes=None, scales=None, stream=None, group=None):
     dev = inp.device
     if codes is None:
         codes = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    _need(codes, "codes", torch.uint8, dev, numel=R * C)
     dt = 0 if inp.dtype == torch.float32 else 1
     if group is not None:
+        n = int(lib().mxfp8_grouped_scale_bytes(R, (C + 31) // 32, int(group)))
         if scales is None:
-            n = int(lib().mxfp8_grouped_scale_bytes(R, (C + 31) // 32, int(group)))
             scales = torch.empty((n,), dtype=torch.uint8, device=dev)
+        _need(scales, "scales", torch.uint8, dev, numel=n)
         _call(lib().mxfp8_quantize_rows_tiled, "mxfp8_quantize_rows_tiled", R, C, dt, _ptr(inp), ld_in,
               _ptr(codes), _ptr(scales), int(group), _stream(dev, stream))
         return codes, scales
     if scales is None:
         scales = torch.empty((R, (C + 31) // 32), dtype=torch.uint8, device=dev)
+    _need(scales, "scales", torch.uint8, dev, numel=R * ((C + 31) // 32))
     _call(lib().mxfp8_quantize_rows, "mxfp8_quantize_rows", R, C, dt, _ptr(inp), ld_in, _ptr(codes),
           _ptr(scales), _stream(dev, stream))
     return codes, scales
@@ -460,16 +495,19 @@ def mxfp8_quantize_cols(inp, codes=None, scales=None, stream=None, group=None):
     dev = inp.device
     if codes is None:
         codes = torch.empty((C, R), dtype=torch.uint8, device=dev)
+    _need(codes, "codes", torch.uint8, dev, numel=R * C)
     dt = 0 if inp.dtype == torch.float32 else 1
     if group is not None:
+        n = int(lib().mxfp8_grouped_scale_bytes(C, (R + 31) // 32, int(group)))
         if scales is None:
-            n = int(lib().mxfp8_grouped_scale_bytes(C, (R + 31) // 32, int(group)))
             scales = torch.empty((n,), dtype=torch.uint8, device=dev)
+        _need(scales, "scales", torch.uint8, dev, numel=n)
         _call(lib().mxfp8_quantize_cols_tiled, "mxfp8_quantize_cols_tiled", R, C, dt, _ptr(inp), ld_in,
               _ptr(codes), _ptr(scales), int(group), _stream(dev, stream))
         return codes, scales
     if scales is None:
         scales = torch.empty((C, (R + 31) // 32), dtype=torch.uint8, device=dev)
+    _need(scales, "scales", torch.uint8, dev, numel=C * ((R + 31) // 32))
     _call(lib().mxfp8_quantize_cols, "mxfp8_quantize_cols", R, C, dt, _ptr(inp), ld_in, _ptr(codes),
           _ptr(scales), _stream(dev, stream))
     return codes, scales
@@ -487,6 +525,7 @@ def mxfp8_swizzle_scales(scales, out=None, stream=None, group=128):
     n = int(lib().mxfp8_grouped_scale_bytes(rows, cols, group))
     if out is None:
         out = torch.empty((n,), dtype=torch.uint8, device=scales.device)
+    _need(out, "out", torch.uint8, scales.device, numel=n)
     ld = int(scales.stride(0)) if rows > 1 else int(cols)
     if group == 128:
         _call(lib().mxfp8_swizzle_scales, "mxfp8_swizzle_scales", rows, cols, _ptr(scales), ld, _ptr(out),
@@ -508,21 +547,17 @@ def kv_fwd(c_kv, W, k_pe, cos, sin, H, Dn, Dv, Dr, pos=None, o_key=None, o_value
     the rotated shared k_pe after each head's Dn channels, o_value [T, H, Dv] bf16)."""
     dev = c_kv.device
     _need(c_kv, "c_kv", torch.bfloat16, ndim=2)
-    _need(W, "W", torch.bfloat16, dev, ndim=2)
-    _need(k_pe, "k_pe", torch.bfloat16, dev)
-    _need(cos, "cos", torch.float32, dev, ndim=2)
-    _need(sin, "sin", torch.float32, dev, ndim=2)
     T, K = c_kv.shape
-    if tuple(W.shape) != (H * (Dn + Dv), K):
-        raise ValueError(f"W must be [{H * (Dn + Dv)}, {K}]")
-    if k_pe.numel() != T * Dr:
-        raise ValueError("k_pe must hold T * Dr elements")
-    if pos is not None:
-        _need(pos, "pos", torch.int32, dev, ndim=1)
+    _need(W, "W", torch.bfloat16, dev, shape=(H * (Dn + Dv), K))
+    _need(k_pe, "k_pe", torch.bfloat16, dev, numel=T * Dr)
+    _tables(cos, sin, dev, T, pos)
+    _status(status, dev)
     if o_key is None:
         o_key = torch.empty((T, H, Dn + Dr), dtype=torch.bfloat16, device=dev)
     if o_value is None:
         o_value = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+    _need(o_key, "o_key", torch.bfloat16, dev, numel=T * H * (Dn + Dr))
+    _need(o_value, "o_value", torch.bfloat16, dev, numel=T * H * Dv)
     s = KvShape(T=T, K=K, H=H, Dn=Dn, Dv=Dv, Dr=Dr, cs_rows=cos.shape[0], cs_width=cos.shape[1])
     _call(lib().mla_kv_uproj_fwd, "mla_kv_uproj_fwd", ctypes.byref(s), _ptr(c_kv), _ptr(W), _ptr(k_pe),
           _ptr(cos), _ptr(sin), _ptr(pos), _ptr(o_key), _ptr(o_value), _ptr(status), _stream(dev, stream))
