@@ -85,6 +85,8 @@ enum { MLA_IN_F32 = 0, MLA_IN_BF16 = 1 };
  *   Dr       rotated channels per head, even, > 0
  *   cs_rows  rows of the cos and sin tables (positions)
  *   cs_width columns of the tables = their row pitch in floats; must be >= Dr
+ *   T, K, H * (Dn + Dr), cs_rows and cs_width are at most INT32_MAX, else
+ *   MLA_ERR_INVALID_ARG
  *            (the width guard of the Megatron-LM PR above: a narrow table
  *            gives MLA_ERR_ROPE_WIDTH, never an out-of-bounds read). Rope
  *            channel j of a head reads column j. */

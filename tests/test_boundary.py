@@ -88,6 +88,10 @@ def test_fwd_valid_args_reach_cuda(L):
     (dict(wm=2), "MLA_ERR_INVALID_ARG"),
     (dict(wm=1), "MLA_ERR_INVALID_ARG"),                    # MXFP8 weights need both scale arrays
     (dict(cos=None), "MLA_ERR_INVALID_ARG"),
+    (dict(s=shape(cs_rows=1 << 31)), "MLA_ERR_INVALID_ARG"),  # no int32 position reaches such a row
+    (dict(s=shape(cs_width=1 << 40)), "MLA_ERR_INVALID_ARG"),  # table bytes would overflow int64
+    (dict(s=shape(H=1 << 26)), "MLA_ERR_INVALID_ARG"),        # N = H * (Dn + Dr) past INT32_MAX
+    (dict(s=shape(T=1 << 31, cs_rows=(1 << 31) - 1)), "MLA_ERR_INVALID_ARG"),
     (dict(s=shape(cs_width=15)), "MLA_ERR_ROPE_WIDTH"),     # table narrower than Dr
     (dict(s=shape(cs_width=0)), "MLA_ERR_ROPE_WIDTH"),
     (dict(s=shape(T=300, cs_rows=256)), "MLA_ERR_POS_RANGE"),  # implicit pos = t beyond the table
@@ -230,6 +234,8 @@ def test_kv_rejects(L):
     assert _kv(L, ok=p(0)) == S["MLA_ERR_ALIAS"]                   # key over c_kv
     assert _kv(L, ov=p(5)) == S["MLA_ERR_ALIAS"]                   # value over key
     assert _kv(L, c=None) == S["MLA_ERR_INVALID_ARG"]
+    assert _kv(L, cs_rows=1 << 31) == S["MLA_ERR_INVALID_ARG"]
+    assert _kv(L, cs_width=1 << 40) == S["MLA_ERR_INVALID_ARG"]
     assert _kv(L, T=0, c=None) == S["MLA_OK"]
 
 

@@ -160,6 +160,9 @@ int check_shape(const mla_q_shape* s, int* D, int64_t* N) {
     const int64_t d = (int64_t)s->Dn + s->Dr;
     const int64_t n = d * s->H;
     if (d > kI32Max || n > kI32Max || s->T > kI32Max || s->K > kI32Max) return MLA_ERR_INVALID_ARG;
+    // positions are int32, so no row past INT32_MAX is reachable; both bounds
+    // keep the table's byte extent (rows * width * 4) inside int64
+    if (s->cs_rows > kI32Max || s->cs_width > kI32Max) return MLA_ERR_INVALID_ARG;
     *D = (int)d;
     *N = n;
     return MLA_OK;
@@ -521,6 +524,7 @@ MLAQ_API int mla_kv_uproj_fwd(const mla_kv_shape* shape, const void* c_kv, const
         return MLA_ERR_INVALID_ARG;
     const int64_t dkv = (int64_t)s.Dn + s.Dv, dk = (int64_t)s.Dn + s.Dr;
     if (dkv * s.H > kI32Max || dk * s.H > kI32Max || s.T > kI32Max || s.K > kI32Max) return MLA_ERR_INVALID_ARG;
+    if (s.cs_rows > kI32Max || s.cs_width > kI32Max) return MLA_ERR_INVALID_ARG;
     if (s.cs_width < s.Dr) return MLA_ERR_ROPE_WIDTH;
     if (s.T > 0 && (!cos_tab || !sin_tab || !c_kv || !W || !k_pe || !o_key || !o_value))
         return MLA_ERR_INVALID_ARG;
