@@ -391,3 +391,12 @@ def test_bwd_mxfp8_prepared_checks(L):
     q = L.mxfp8_quantize_cols_tiled
     assert q(64, 32, 1, p(0), 32, p(1), p(2), 0, None) == S["MLA_ERR_INVALID_ARG"]
     assert q(0, 32, 1, None, 32, None, None, 128, None) == S["MLA_OK"]
+
+
+def test_public_names_are_exported():
+    """Every public function and structure of the binding is in __all__."""
+    import inspect
+    public = {n for n, o in vars(mlaq).items() if not n.startswith("_")
+              and (inspect.isfunction(o) or inspect.isclass(o)) and o.__module__ == mlaq.__name__}
+    assert public <= set(mlaq.__all__), sorted(public - set(mlaq.__all__))
+    assert all(hasattr(mlaq, n) for n in mlaq.__all__)

@@ -23,8 +23,9 @@ import torch
 __all__ = [
     "MlaError", "lib", "library_path", "fwd", "bwd_dgrad", "bwd_wgrad", "mxfp8_quantize_rows",
     "mxfp8_quantize_cols", "mxfp8_swizzle_scales", "kv_fwd", "bwd_mxfp8", "bwd_mxfp8_layout",
-    "bwd_mxfp8_operands",
-    "workspace_size", "status_string", "check_status", "Shape", "STATUS",
+    "bwd_mxfp8_operands", "bwd_mxfp8_prepare_weight", "w_scale_group", "wait_selftest",
+    "workspace_size", "status_string", "check_status", "Shape", "KvShape", "Mxfp8BwdLayout", "STATUS",
+    "WEIGHT_MODES", "OUT_MODES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
