@@ -258,3 +258,37 @@ def test_kv_and_quantizer_refusals(calls, what, call):
     with pytest.raises(ValueError):
         call()
     assert calls == []
+
+
+@pytest.mark.parametrize("grads,expect", [
+    ("xwb", ["mla_q_uproj_fwd", "mla_q_uproj_bwd_dgrad", "mla_q_uproj_bwd_wgrad"]),
+    ("x", ["mla_q_uproj_fwd", "mla_q_uproj_bwd_dgrad"]),
+    ("w", ["mla_q_uproj_fwd", "mla_q_uproj_bwd_wgrad"]),
+])
+def test_autograd_calls_only_the_needed_passes(calls, monkeypatch, grads, expect):
+    """The autograd face computes only what autograd asks for: dgrad for x,
+    one wgrad call for W and b, and dgrad hands the rotated rope channels to
+    wgrad when both run."""
+    from up_proj_gemm_gb300 import autograd
+    seen = {}
+    real_wgrad = autograd.bwd_wgrad
+
+    def wgrad(*a, **k):
+        seen["rope"] = k.get("dq_pre_rope")
+        return real_wgrad(*a, **k)
+
+    monkeypatch.setattr(autograd, "bwd_wgrad", wgrad)
+    s = _q()
+    x = s["x"].clone().requires_grad_("x" in grads)
+    W = s["W"].clone().requires_grad_("w" in grads)
+    b = s["b"].clone().requires_grad_("b" in grads)
+    q = autograd.q_up_proj(x, W, s["cos"], s["sin"], s["H"], s["Dn"], s["Dr"], bias=b, pos=s["pos"])
+    assert q.shape == (s["T"], s["H"], s["Dn"] + s["Dr"])
+    q.backward(torch.zeros_like(q))
+    assert calls == expect
+    assert (x.grad is not None) == ("x" in grads) and (W.grad is not None) == ("w" in grads)
+    assert (b.grad is not None) == ("b" in grads)
+    if grads == "xwb":
+        assert seen["rope"] is not None and seen["rope"].shape == (s["T"], s["H"], s["Dr"])
+    elif "rope" in seen:
+        assert seen["rope"] is None
