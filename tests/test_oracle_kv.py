@@ -57,3 +57,34 @@ def test_kv_identity_rotation_and_unchanged_inputs():
                 assert math.isclose(o_value[t, h, c], sum(c_kv[t, k] * rows[Dn + c, k] for k in range(K)),
                                     rel_tol=1e-12, abs_tol=1e-12)
     assert all(np.array_equal(a, b) for a, b in zip(before, (c_kv, W, k_pe)))
+
+
+def test_kv_rope_pairs_turn_by_their_table_angle():
+    """Geometry of rotate-half RoPE on the shared k_pe, with a distinct angle
+    per channel pair: each pair (j, j + Dr/2) keeps its length and turns by
+    exactly the angle its table row gives, at every position, for every head.
+    A wrong pairing (adjacent channels) or a wrong direction fails this."""
+    rng = np.random.default_rng(11)
+    T, K, H, Dn, Dv, Dr = 6, 8, 3, 4, 4, 8
+    half = Dr // 2
+    rows = 9
+    theta = rng.uniform(-math.pi, math.pi, size=(rows, half))
+    cos = np.cos(np.concatenate([theta, theta], axis=1)).astype(np.float32)
+    sin = np.sin(np.concatenate([theta, theta], axis=1)).astype(np.float32)
+    pos = rng.integers(0, rows, size=T).astype(np.int32)
+    k_pe = rng.standard_normal((T, Dr))
+    o_key, _ = oracle.kv_forward(rng.standard_normal((T, K)), rng.standard_normal((H * (Dn + Dv), K)), k_pe,
+                                 H, Dn, Dv, Dr, cos, sin, pos)
+    for t in range(T):
+        for h in range(H):
+            assert np.array_equal(o_key[t, h, Dn:], o_key[t, 0, Dn:])  # one rope part for all heads
+        out = o_key[t, 0, Dn:]
+        for j in range(half):
+            a_in, b_in = k_pe[t, j], k_pe[t, j + half]
+            a_out, b_out = out[j], out[j + half]
+            assert math.isclose(math.hypot(a_out, b_out), math.hypot(a_in, b_in), rel_tol=1e-6)
+            # the table holds the angle in float32: compare with the angle it encodes
+            want = math.atan2(float(sin[pos[t], j]), float(cos[pos[t], j]))
+            turn = math.atan2(b_out, a_out) - math.atan2(b_in, a_in)
+            d = (turn - want + math.pi) % (2 * math.pi) - math.pi
+            assert abs(d) < 1e-6, (t, j, turn, want)
