@@ -501,7 +501,7 @@ def run_only(args, w, inp, kernels, flush, stream, status, dev):
     elif args.only == "quant_cols":
         a = torch.randn((w.T, w.N), device=dev).to(torch.bfloat16)
         codes = torch.empty((w.N, w.T), dtype=torch.uint8, device=dev)
-        sc = torch.empty((w.N, w.T // 32), dtype=torch.uint8, device=dev)
+        sc = torch.empty((w.N, (w.T + 31) // 32), dtype=torch.uint8, device=dev)
 
         def fn():
             mlaq.mxfp8_quantize_cols(a, codes, sc)
@@ -509,7 +509,7 @@ def run_only(args, w, inp, kernels, flush, stream, status, dev):
     elif args.only == "quant":
         a = torch.randn((w.T, w.N), device=dev).to(torch.bfloat16)
         codes = torch.empty((w.T, w.N), dtype=torch.uint8, device=dev)
-        sc = torch.empty((w.T, w.N // 32), dtype=torch.uint8, device=dev)
+        sc = torch.empty((w.T, (w.N + 31) // 32), dtype=torch.uint8, device=dev)
 
         def fn():
             mlaq.mxfp8_quantize_rows(a, codes, sc)
