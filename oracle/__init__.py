@@ -228,43 +228,20 @@ def rope_bwd(dq, H, Dn, Dr, cos, sin, pos=None) -> np.ndarray:
     return _rope(_load().oracle_rope_bwd, dq, H, Dn, Dr, cos, sin, pos)
 
 
-def rope_bwd_f32(dq, H, Dn, Dr, cos, sin, pos=None) -> np.ndarray:
-    """The inverse rotation of the RoPE backward evaluated in float32 with
-    every product and sum rounded once, in this order:
-      out[Dn+i]      = fl(fl(g[i] cos[p,i]) + fl(g[i+h] sin[p,i+h]))
-      out[Dn+i+h]    = fl(fl(g[i+h] cos[p,i+h]) - fl(g[i] sin[p,i]))
-    (h = Dr/2; pass-through channels copied). It is the arithmetic the MXFP8
-    backward quantizes, so that the quantized codes, decided on these float32
-    values, can be compared bit for bit. dq [T, H, Dn+Dr] (float32-exact
-    values, e.g. decoded bf16) -> float32 [T, H, Dn+Dr]."""
-    g = np.asarray(dq, np.float64).reshape(dq.shape[0], H, Dn + Dr).astype(np.float32)
-    T = g.shape[0]
-    p = np.arange(T) if pos is None else np.asarray(pos, np.int64)
-    cs = np.asarray(cos, np.float32)[p]
-    sn = np.asarray(sin, np.float32)[p]
-    h = Dr // 2
-    out = g.copy()
-    a, c = g[:, :, Dn:Dn + h], g[:, :, Dn + h:]
-    ci, si = cs[:, None, :h], sn[:, None, :h]
-    cj, sj = cs[:, None, h:Dr], sn[:, None, h:Dr]
-    out[:, :, Dn:Dn + h] = (a * ci).astype(np.float32) + (c * sj).astype(np.float32)
-    out[:, :, Dn + h:] = (c * cj).astype(np.float32) - (a * si).astype(np.float32)
-    return out
-
-
 def backward_mxfp8(dq, x, W, H, Dn, Dr, cos, sin, pos=None):
     """MXFP8 backward (the low-precision backward beyond the fused bf16 one;
     TransformerEngine PR "Add support for fused Q Up-Proj GEMM/RoPE/Quant"
-    names the MXFP8 quantization helpers it would use; the pages give no
-    formula, so this is the plain reading): dq_pre = the float32 inverse
-    rotation (rope_bwd_f32); dgrad operands quantized along their reduction
-    dimension, the channels: rowwise MXFP8 of dq_pre [T, N] and columnwise
-    MXFP8 of W [N, K]; wgrad operands along the tokens: columnwise MXFP8 of
-    dq_pre and of x [T, K]; dx, dW = exact products of the dequantized
-    operands; db = the token sum of the float32 dq_pre.
-    Returns dict(dx, dW, db, qa, qa_s, qb, qb_s, wt, wt_s, xt, xt_s)."""
+    names the MXFP8 quantization helpers it would use, the rowwise copy and
+    its transpose; the pages give no formula, so this is the plain reading):
+    dq_pre = the exact (fp64) RoPE backward of dq (rope_bwd); every GEMM
+    operand quantized along its reduction dimension with the MXFP8 rule:
+    dgrad's along the channels (rowwise MXFP8 of dq_pre [T, N], columnwise
+    of W [N, K]), wgrad's along the tokens (columnwise MXFP8 of dq_pre and of
+    x [T, K]); dx, dW = exact products of the dequantized operands; db = the
+    token sum of dq_pre.
+    Returns dict(dx, dW, db, dq_pre, qa, qa_s, qb, qb_s, wt, wt_s, xt, xt_s)."""
     T = dq.shape[0]
-    dqp = rope_bwd_f32(dq, H, Dn, Dr, cos, sin, pos).reshape(T, -1).astype(np.float64)
+    dqp = rope_bwd(dq, H, Dn, Dr, cos, sin, pos).reshape(T, -1)
     qa, qa_s = mxfp8_quantize(dqp)                 # [T, N], blocks along N
     qb, qb_s = mxfp8_quantize_columns(dqp)         # [N, T], blocks along T
     wt, wt_s = mxfp8_quantize_columns(W)           # [K, N], blocks along N
@@ -273,8 +250,8 @@ def backward_mxfp8(dq, x, W, H, Dn, Dr, cos, sin, pos=None):
     B = mxfp8_dequantize(wt, wt_s)
     dx = A @ B.T
     dW = mxfp8_dequantize(qb, qb_s) @ mxfp8_dequantize(xt, xt_s).T
-    return dict(dx=dx, dW=dW, db=dqp.sum(axis=0), qa=qa, qa_s=qa_s, qb=qb, qb_s=qb_s, wt=wt, wt_s=wt_s,
-                xt=xt, xt_s=xt_s)
+    return dict(dx=dx, dW=dW, db=dqp.sum(axis=0), dq_pre=dqp, qa=qa, qa_s=qa_s, qb=qb, qb_s=qb_s, wt=wt,
+                wt_s=wt_s, xt=xt, xt_s=xt_s)
 
 
 def kv_forward(c_kv, W, k_pe, H, Dn, Dv, Dr, cos, sin, pos=None):

@@ -119,3 +119,153 @@ def sf_untile(buf, rows, cols, G):
     """Row-major [rows, cols] scales read back from the tiled order."""
     buf = np.asarray(buf)
     return buf[sf_tiled_offsets(rows, cols, G)]
+
+
+def e8m0_exponent_vec(amax):
+    """The MXFP8 scale exponent of each block amax (float64 array, >= 0): the
+    smallest integer e with amax <= 448 * 2^e, clamped to [-127, 127]. With
+    amax = m * 2^k (m in [0.5, 1), numpy.frexp) and 448 = 0.875 * 2^9 this is
+    k - 9, or k - 8 when m > 0.875; exact, no logarithm."""
+    m, k = np.frexp(np.asarray(amax, np.float64))
+    e = k.astype(np.int64) - 9 + (m > 0.875)
+    e = np.where(m == 0, -127, e)
+    return np.clip(e, -127, 127)
+
+
+def mxfp8_decided(v, eb):
+    """Which rowwise MXFP8 scales and codes of float64 values v [R, C] (blocks
+    of 32 along C) are fixed by the quantization rule for every value within
+    +-eb [R, C] of v, i.e. whatever rounding a float32 evaluation of v made:
+    a block's scale is fixed when the exponents of its smallest and largest
+    possible amax agree; an element's code when, on that scale, no rounding
+    midpoint of the E4M3 grid lies in its interval and its sign is fixed.
+    Returns (scale_fixed [R, nb], code_fixed [R, C], e_lo [R, nb], e_hi [R, nb])."""
+    v = np.asarray(v, np.float64)
+    eb = np.asarray(eb, np.float64)
+    R, C = v.shape
+    nb = (C + 31) // 32
+    pad = nb * 32 - C
+    a = np.pad(np.abs(v), ((0, 0), (0, pad))).reshape(R, nb, 32)
+    b = np.pad(eb, ((0, 0), (0, pad))).reshape(R, nb, 32)
+    e_lo = e8m0_exponent_vec(np.maximum(a - b, 0.0).max(-1))
+    e_hi = e8m0_exponent_vec((a + b).max(-1))
+    scale_fixed = e_lo == e_hi
+    s = np.repeat(np.exp2(-e_lo.astype(np.float64)), 32, axis=1)[:, :C]
+    lut = e4m3_lut()[:127]                     # codes 0x00..0x7E: 0 .. 448, increasing
+    mids = (lut[:-1] + lut[1:]) / 2
+    lo = (np.abs(v) - eb) * s
+    hi = (np.abs(v) + eb) * s
+    no_mid = np.searchsorted(mids, lo, side="left") == np.searchsorted(mids, hi, side="right")
+    sign_fixed = (np.abs(v) > eb) | ((v == 0) & (eb == 0))
+    code_fixed = no_mid & sign_fixed & np.repeat(scale_fixed, 32, axis=1)[:, :C]
+    return scale_fixed, code_fixed, e_lo, e_hi
+
+
+def check_mxfp8_decided(codes, scales, v, eb, ref_codes, ref_scales, what, min_fixed=0.99):
+    """GPU MXFP8 rows (codes [R, C], scales [R, nb], numpy) of values the GPU
+    evaluated within +-eb of the float64 v: bit-exact against the oracle's
+    quantization of v (ref_codes, ref_scales) wherever the rule fixes the
+    result (mxfp8_decided); elsewhere every element within one E4M3 step of
+    v on the GPU's own grid. At least `min_fixed` of the elements must be
+    fixed (so the bound is not vacuous). Returns the undecided mask."""
+    codes, scales = np.asarray(codes), np.asarray(scales)
+    R, C = v.shape
+    sf, cf, _, _ = mxfp8_decided(v, eb)
+    assert cf.mean() >= min_fixed, f"{what}: only {cf.mean():.5f} of the codes are decided"
+    assert np.array_equal(scales[sf], ref_scales[sf]), f"{what}: decided scales differ"
+    assert np.array_equal(codes[cf], ref_codes[cf]), (
+        f"{what}: {(codes[cf] != ref_codes[cf]).sum()} decided codes differ")
+    und = ~cf
+    if und.any():
+        e = np.repeat(scales.astype(np.int64) - 127, 32, axis=1)[:, :C].astype(np.float64)[und]
+        deq = e4m3_lut()[codes[und]] * np.exp2(e)
+        tol = ulp_e4m3(np.abs(v[und]) * np.exp2(-e)) * np.exp2(e)
+        assert (np.abs(deq - v[und]) <= tol).all(), f"{what}: an undecided element is beyond one E4M3 step"
+    return und
+
+
+# ------------------------------------------------------- full-tensor checks
+class FrobAcc:
+    """The relative Frobenius error of a tensor compared chunk by chunk."""
+
+    def __init__(self):
+        self.num = 0.0
+        self.den = 0.0
+
+    def add(self, gpu, ref):
+        g = bf16_to_f64(gpu).reshape(ref.shape)
+        assert not np.isnan(g).any(), "NaN in GPU output"
+        self.num += float(np.sum((g - ref) ** 2))
+        self.den += float(np.sum(ref * ref))
+
+    def rel(self):
+        return float(np.sqrt(self.num) / max(np.sqrt(self.den), 1e-300))
+
+
+def check_fwd_all_tokens(inp, w, q=None, codes=None, scales=None, x64=None, W64=None, chunk=2048):
+    """Every element of a forward output against the oracle, in token chunks
+    (tokens are independent in the forward): bf16 q (``q``) with the bf16 bar
+    (the rms of the bar taken over each chunk of ``chunk`` tokens, which on
+    these homogeneous synthetic inputs equals the whole tensor's to well
+    under 1%), and/or MXFP8 q (``codes``, ``scales``: [T, H, D] and
+    [T, H, ceil(D/32)]) with the MXFP8 bar. ``x64``, ``W64``: the float64
+    operands (default: the decoded bf16 inputs; the MXFP8-weight path passes
+    its dequantized operands)."""
+    x = f64(inp["x"]) if x64 is None else x64
+    W = f64(inp["W"]) if W64 is None else W64
+    b = f64(inp["b"]) if inp.get("b") is not None else None
+    pos, cos, sin = inp["pos"].numpy(), inp["cos"].numpy(), inp["sin"].numpy()
+    q_h = None if q is None else q.cpu()
+    c_h = None if codes is None else codes.cpu().numpy()
+    s_h = None if scales is None else scales.cpu().numpy()
+    for t0 in range(0, w.T, chunk):
+        t1 = min(w.T, t0 + chunk)
+        if c_h is not None:
+            q_ref, rc, rs = oracle.forward(x[t0:t1], W, w.H, w.Dn, w.Dr, cos, sin, pos[t0:t1], b, quantize=True)
+            check_mxfp8_close(c_h[t0:t1], s_h[t0:t1], q_ref, rc, rs, what=f"q tokens {t0}:{t1}")
+        else:
+            q_ref = oracle.forward(x[t0:t1], W, w.H, w.Dn, w.Dr, cos, sin, pos[t0:t1], b)
+        if q_h is not None:
+            check_bf16_close(q_h[t0:t1], q_ref, what=f"q tokens {t0}:{t1}")
+
+
+def check_bwd_all(inp, w, dx=None, dW=None, db=None, rope=None, tol=5e-3, tok_chunk=2048, head_chunk=16):
+    """Every element of the backward's outputs against the oracle: dx
+    (relative Frobenius error over the whole tensor <= tol) and the stored
+    rope channels dq_pre_rope [T, H, Dr] (bf16 bar) token chunk by token
+    chunk; dW and db (relative Frobenius <= tol) head group by head group
+    (a head's rows need only that head's dq, over every token)."""
+    pos, cos, sin = inp["pos"].numpy(), inp["cos"].numpy(), inp["sin"].numpy()
+    T, H, D, Dn, Dr = w.T, w.H, w.D, w.Dn, w.Dr
+    if dx is not None or rope is not None:
+        W64 = f64(inp["W"])
+        dx_h = None if dx is None else dx.cpu()
+        rope_h = None if rope is None else rope.cpu()
+        acc = FrobAcc()
+        for t0 in range(0, T, tok_chunk):
+            t1 = min(T, t0 + tok_chunk)
+            dqp = oracle.rope_bwd(f64(inp["dq"][t0:t1]), H, Dn, Dr, cos, sin, pos[t0:t1])
+            if rope_h is not None:
+                check_bf16_close(rope_h[t0:t1], dqp[:, :, Dn:], what=f"dq_pre_rope tokens {t0}:{t1}")
+            if dx_h is not None:
+                acc.add(dx_h[t0:t1], oracle.dgrad(dqp.reshape(t1 - t0, -1), W64))
+        if dx_h is not None:
+            assert acc.rel() <= tol, f"dx: relative Frobenius error {acc.rel():.3e}"
+    if dW is not None or db is not None:
+        x64 = f64(inp["x"])
+        dW_h = None if dW is None else dW.cpu()
+        db_h = None if db is None else db.cpu()
+        accw, accb = FrobAcc(), FrobAcc()
+        for h0 in range(0, H, head_chunk):
+            h1 = min(H, h0 + head_chunk)
+            dqp = oracle.rope_bwd(f64(inp["dq"][:, h0:h1].contiguous()), h1 - h0, Dn, Dr, cos, sin,
+                                  pos).reshape(T, -1)
+            rows = slice(h0 * D, h1 * D)
+            if dW_h is not None:
+                accw.add(dW_h[rows], oracle.wgrad(dqp, x64))
+            if db_h is not None:
+                accb.add(db_h[rows], oracle.bgrad(dqp))
+        if dW_h is not None:
+            assert accw.rel() <= tol, f"dW: relative Frobenius error {accw.rel():.3e}"
+        if db_h is not None:
+            assert accb.rel() <= tol, f"db: relative Frobenius error {accb.rel():.3e}"

@@ -134,40 +134,21 @@ def test_bwd_position_out_of_range_reports_status(cuda_device, name, ov):
         assert int(st.item()) == mlaq.STATUS["MLA_ERR_POS_RANGE"], which
 
 
-def test_bwd_full_size_sampled(cuda_device):
+def test_bwd_full_size(cuda_device):
     """DeepSeek-V3 backward shape (T = 2 x 4096, pos = t mod 4096, K=1536,
-    H=128): dx on 32 sampled tokens, dW on 4 sampled heads, db on every channel."""
+    H=128, bias on) in the benchmark's calls (dgrad storing the rotated rope
+    channels, wgrad reading them): every element of dx, dW, db and of the
+    stored rope channels against the oracle."""
     w = synth.workload("dsv3_bwd")
     inp, d = _dev_inputs(w, 0, cuda_device)
     st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    dx = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st)
+    rope = torch.full((w.T, w.H, w.Dr), float("nan"), dtype=torch.bfloat16, device=cuda_device)
+    dx = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st,
+                        dq_pre_rope=rope)
     dW, db = mlaq.bwd_wgrad(d["dq"], d["x"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
-                            status=st)
+                            status=st, dq_pre_rope=rope)
     mlaq.check_status(st)
-    cos, sin, pos = inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy()
-    rng = np.random.default_rng(1)
-    W = helpers.f64(inp["W"])
-    # dx: sampled tokens (rows are independent)
-    toks = np.sort(rng.choice(w.T, 32, replace=False))
-    dq_t = helpers.f64(inp["dq"][torch.from_numpy(toks)])
-    dqp_t = oracle.rope_bwd(dq_t, w.H, w.Dn, w.Dr, cos, sin, pos[toks]).reshape(len(toks), -1)
-    ref_dx = oracle.dgrad(dqp_t, W)
-    assert helpers.frob_rel(dx[torch.from_numpy(toks).to(cuda_device)], ref_dx) <= TOL
-    # dW: sampled heads over all tokens (a head's channels only need that head's dq)
-    x = helpers.f64(inp["x"])
-    heads = np.array([0, 37, 64, 127])
-    dq_h = helpers.f64(inp["dq"][:, torch.from_numpy(heads)].contiguous())
-    dqp_h = oracle.rope_bwd(dq_h, len(heads), w.Dn, w.Dr, cos, sin, pos).reshape(w.T, -1)
-    ref_dW = oracle.wgrad(dqp_h, x)
-    ch = (heads[:, None] * w.D + np.arange(w.D)[None, :]).reshape(-1)
-    assert helpers.frob_rel(dW[torch.from_numpy(ch).to(cuda_device)], ref_dW) <= TOL
-    # db: every channel, 16 heads at a time
-    ref_db = np.empty(w.N)
-    for h0 in range(0, w.H, 16):
-        dq_c = helpers.f64(inp["dq"][:, h0:h0 + 16].contiguous())
-        dqp = oracle.rope_bwd(dq_c, 16, w.Dn, w.Dr, cos, sin, pos).reshape(w.T, -1)
-        ref_db[h0 * w.D:(h0 + 16) * w.D] = oracle.bgrad(dqp)
-    assert helpers.frob_rel(db, ref_db) <= TOL
+    helpers.check_bwd_all(inp, w, dx=dx, dW=dW, db=db, rope=rope, tol=TOL)
 
 
 def test_dgrad_split_reduction(cuda_device):

@@ -3,18 +3,26 @@
 TransformerEngine PR "Add support for fused Q Up-Proj GEMM/RoPE/Quant",
 Greptile summary: the MXFP8 helpers (rowwise, the transpose copy) that feed
 block-scaled GEMMs. The pages give no backward formula; the oracle's reading
-(oracle.backward_mxfp8): dq_pre is the float32 inverse rotation with single
-roundings, each GEMM operand is quantized along its reduction dimension, and
-dx, dW are exact products of the decoded operands.
+(oracle.backward_mxfp8): dq_pre is the exact (fp64) RoPE backward, each GEMM
+operand is quantized along its reduction dimension, and dx, dW are exact
+products of the decoded operands.
 
-Bars:
-  * the four quantized operands (codes and scales) are bit-exact, including
-    the zero padding of the token axis to a multiple of 128;
-  * dx, dW: |gpu - ref| <= 2^-8 |ref| + 2^-14 S elementwise, S = the sum of
-    |products| (bf16 output rounding plus fp32 accumulation of exact
-    products), and the relative Frobenius error <= 2^-8;
-  * db: |gpu - ref| <= 2^-8 |ref| + T 2^-23 sum|dq_pre| (bf16 rounding plus
-    fp32 sequential sums).
+The GPU evaluates dq_pre in float32, so its value of each rope channel lies
+within eb = 2^-22 (|g_i| + |g_{i+h}|) max|table| of the exact one (at most
+three float32 roundings of a two-term sum of products); pass-through
+channels are exact. Bars:
+  * W's and x's columnwise copies (quantized straight from bf16): bit-exact;
+  * dq_pre's two copies: bit-exact wherever the MXFP8 rule decides the scale
+    and code for every value within +-eb (helpers.mxfp8_decided: at least
+    99% of the elements), elsewhere within one E4M3 step on the GPU's grid;
+    the token padding to a multiple of 128 is zero;
+  * dx, dW: |gpu - ref| <= 2^-8 |ref| + 2^-14 S + F elementwise, S = the sum
+    of |products| (bf16 output rounding plus fp32 accumulation of exact
+    products), F = the products of two E4M3 steps of the undecided operand
+    elements with the other operand (0 when every code is decided), and the
+    relative Frobenius error <= 2^-8;
+  * db: |gpu - ref| <= 2^-8 |ref| + T 2^-23 sum|dq_pre| + sum eb (bf16
+    rounding, float32 sums of float32 values).
 """
 import numpy as np
 import pytest
@@ -46,18 +54,50 @@ def _np(t):
     return t.cpu().numpy()
 
 
-def _check_gemm(got, ref, S, what):
+def rot_error_bound(dq, H, Dn, Dr, cos):
+    """eb [T, N]: how far a float32 evaluation of the inverse rotation may be
+    from the exact one (see the module docstring); 0 on pass-through channels."""
+    T = dq.shape[0]
+    g = np.abs(np.asarray(dq, np.float64).reshape(T, H, Dn + Dr))
+    h = Dr // 2
+    amp = float(np.max(np.abs(cos))) if Dr else 0.0
+    eb = np.zeros_like(g)
+    pair = g[:, :, Dn:Dn + h] + g[:, :, Dn + h:]
+    eb[:, :, Dn:Dn + h] = pair
+    eb[:, :, Dn + h:] = pair
+    return (eb * 2.0 ** -22 * max(amp, 1.0)).reshape(T, -1)
+
+
+def _step_max(v, e_hi):
+    """One E4M3 step of |v| at the larger of a block's possible exponents."""
+    a = np.abs(v)
+    normal = np.exp2(np.floor(np.log2(np.maximum(a, 1e-300))) - 3)
+    return np.maximum(normal, np.exp2(-9.0 + e_hi))
+
+
+def _flip_terms(v, eb, other_abs):
+    """F: two E4M3 steps of every undecided element of v [R, C] (blocks along
+    C) times |other| [C, M], summed: [R, M] (0 when all codes are decided)."""
+    _, cf, _, e_hi = helpers.mxfp8_decided(v, eb)
+    und = np.argwhere(~cf)
+    F = np.zeros((v.shape[0], other_abs.shape[1]))
+    for r, c in und:
+        F[r] += 2 * _step_max(v[r, c], float(e_hi[r, c // 32])) * other_abs[c]
+    return F
+
+
+def _check_gemm(got, ref, S, what, F=0.0):
     got = helpers.bf16_to_f64(got)
-    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * S
+    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * S + F
     bad = np.abs(got - ref) > bound
     assert not bad.any(), f"{what}: {bad.sum()} elements outside the bound"
     assert np.linalg.norm(got - ref) <= 2.0 ** -8 * np.linalg.norm(ref), what
 
 
-def _check_db(got, dqp, what="db"):
+def _check_db(got, dqp, eb, what="db"):
     ref = dqp.sum(0)
     got = helpers.bf16_to_f64(got)
-    bound = 2.0 ** -8 * np.abs(ref) + dqp.shape[0] * 2.0 ** -23 * np.abs(dqp).sum(0)
+    bound = 2.0 ** -8 * np.abs(ref) + dqp.shape[0] * 2.0 ** -23 * np.abs(dqp).sum(0) + eb.sum(0)
     assert np.all(np.abs(got - ref) <= bound), what
 
 
@@ -79,37 +119,37 @@ def test_bwd_mxfp8_matches_oracle(cuda_device, name, ov):
     ws = _workspace(w, d, cuda_device)
     dx, dW, db = _run(w, d, st, ws)
     mlaq.check_status(st)
-    g = oracle.backward_mxfp8(helpers.f64(inp["dq"]), helpers.f64(inp["x"]), helpers.f64(inp["W"]), w.H,
+    dq64 = helpers.f64(inp["dq"])
+    g = oracle.backward_mxfp8(dq64, helpers.f64(inp["x"]), helpers.f64(inp["W"]), w.H,
                               w.Dn, w.Dr, inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy())
     ops = mlaq.bwd_mxfp8_operands(ws, w.T, w.K, w.H, w.Dn, w.Dr, d["cos"].shape[0], d["cos"].shape[1])
     T, N, K, nbt, Tp, G = w.T, w.N, w.K, (w.T + 31) // 32, ops["t_pad"], ops["b_group"]
     assert Tp % 128 == 0 and Tp - 128 < T <= Tp
-    for key in ("qa", "wt"):
-        assert np.array_equal(_np(ops[key]), g[key]), key
-    for key in ("qb", "xt"):
-        assert np.array_equal(_np(ops[key])[:, :T], g[key]), key
-    assert not _np(ops["qb"])[:, T:].any(), "qb: padding tokens must be 0"
-    # A operands: the whole tiled array is the oracle's swizzle of the zero-padded scales
-    qa_s = np.zeros((Tp, N // 32), np.uint8)
-    qa_s[:T] = g["qa_s"]
-    assert np.array_equal(_np(ops["qa_s"]), oracle.mxfp8_swizzle_scales(qa_s)), "qa_s"
-    qb_s = np.zeros((N, Tp // 32), np.uint8)
-    qb_s[:, :nbt] = g["qb_s"]
-    assert np.array_equal(_np(ops["qb_s"]), oracle.mxfp8_swizzle_scales(qb_s)), "qb_s"
-    # B operands: groups of G rows
+    # W's and x's columnwise copies come straight from bf16: bit-exact
+    assert np.array_equal(_np(ops["wt"]), g["wt"]), "wt"
+    assert np.array_equal(_np(ops["xt"])[:, :T], g["xt"]), "xt"
     assert np.array_equal(helpers.sf_untile(_np(ops["wt_s"]), K, N // 32, G), g["wt_s"]), "wt_s"
     xt_s = helpers.sf_untile(_np(ops["xt_s"]), K, Tp // 32, G)
     assert np.array_equal(xt_s[:, :nbt], g["xt_s"]), "xt_s"
     assert not xt_s[:, nbt:].any(), "xt_s: padding token blocks must be 0"
+    # dq_pre's copies: decided codes bit-exact, the rest within one step
+    dqp, eb = g["dq_pre"], rot_error_bound(dq64, w.H, w.Dn, w.Dr, inp["cos"].numpy())
+    qa_s = helpers.sf_untile(_np(ops["qa_s"]), Tp, N // 32, 128)
+    assert not qa_s[T:].any(), "qa_s: padding rows must be 0"
+    helpers.check_mxfp8_decided(_np(ops["qa"]), qa_s[:T], dqp, eb, g["qa"], g["qa_s"], "qa")
+    qb = _np(ops["qb"])
+    assert not qb[:, T:].any(), "qb: padding tokens must be 0"
+    qb_s = helpers.sf_untile(_np(ops["qb_s"]), N, Tp // 32, 128)
+    assert not qb_s[:, nbt:].any(), "qb_s: padding token blocks must be 0"
+    helpers.check_mxfp8_decided(qb[:, :T], qb_s[:, :nbt], dqp.T.copy(), eb.T.copy(), g["qb"], g["qb_s"], "qb")
+    # products against the oracle's operands
     A = np.abs(oracle.mxfp8_dequantize(g["qa"], g["qa_s"]))
     B = np.abs(oracle.mxfp8_dequantize(g["wt"], g["wt_s"]))
-    _check_gemm(dx, g["dx"], A @ B.T, "dx")
+    _check_gemm(dx, g["dx"], A @ B.T, "dx", _flip_terms(dqp, eb, B.T))
     A = np.abs(oracle.mxfp8_dequantize(g["qb"], g["qb_s"]))
     B = np.abs(oracle.mxfp8_dequantize(g["xt"], g["xt_s"]))
-    _check_gemm(dW, g["dW"], A @ B.T, "dW")
-    dqp = oracle.rope_bwd_f32(helpers.f64(inp["dq"]), w.H, w.Dn, w.Dr, inp["cos"].numpy(),
-                              inp["sin"].numpy(), inp["pos"].numpy()).reshape(T, -1).astype(np.float64)
-    _check_db(db, dqp)
+    _check_gemm(dW, g["dW"], A @ B.T, "dW", _flip_terms(dqp.T.copy(), eb.T.copy(), B.T))
+    _check_db(db, dqp, eb)
 
 
 def test_bwd_mxfp8_subsets_are_the_same_bits(cuda_device):
@@ -167,9 +207,9 @@ def test_bwd_mxfp8_position_out_of_range_reports_status(cuda_device):
 
 def test_bwd_mxfp8_full_size_sampled(cuda_device):
     """DeepSeek-V3 backward shape (T = 2 x 4096, pos = t mod 4096, K = 1536,
-    H = 128), as the benchmark runs it: the quantized operands on sampled
-    tokens / channels bit-exact, dx on sampled tokens, dW on sampled
-    channels, db on every channel."""
+    H = 128), as the benchmark runs it: W's and x's copies bit-exact in
+    full; dq_pre's copies and dx on 64 sampled tokens, dq_pre's columnwise
+    copy and dW on 8 sampled heads over all tokens; db on every channel."""
     w = synth.workload("dsv3_bwd")
     inp, d = _inputs(w, 0, cuda_device)
     st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
@@ -191,27 +231,32 @@ def test_bwd_mxfp8_full_size_sampled(cuda_device):
     qb_s_rows = helpers.sf_untile(_np(ops["qb_s"]), w.N, Tp // 32, 128)
     Bw, Bx = oracle.mxfp8_dequantize(wt, wt_s), oracle.mxfp8_dequantize(xt, xt_s)
     # dx and the rowwise operand on sampled tokens (rows are independent)
-    toks = np.sort(rng.choice(w.T, 24, replace=False))
-    dqp = oracle.rope_bwd_f32(helpers.f64(inp["dq"][torch.from_numpy(toks)]), w.H, w.Dn, w.Dr, cs, sn,
-                              pos[toks]).reshape(len(toks), -1).astype(np.float64)
+    toks = np.unique(np.concatenate([[0, 4095, 4096, w.T - 1], rng.choice(w.T, 60, replace=False)]))
+    dq_t = helpers.f64(inp["dq"][torch.from_numpy(toks)])
+    dqp = oracle.rope_bwd(dq_t, w.H, w.Dn, w.Dr, cs, sn, pos[toks]).reshape(len(toks), -1)
+    eb = rot_error_bound(dq_t, w.H, w.Dn, w.Dr, cs)
     qa, qa_s = oracle.mxfp8_quantize(dqp)
-    assert np.array_equal(_np(ops["qa"])[toks], qa) and np.array_equal(qa_s_rows[toks], qa_s)
+    helpers.check_mxfp8_decided(_np(ops["qa"])[toks], qa_s_rows[toks], dqp, eb, qa, qa_s, "qa")
     A = oracle.mxfp8_dequantize(qa, qa_s)
-    _check_gemm(dx[torch.from_numpy(toks).to(cuda_device)], A @ Bw.T, np.abs(A) @ np.abs(Bw).T, "dx")
+    _check_gemm(dx[torch.from_numpy(toks).to(cuda_device)], A @ Bw.T, np.abs(A) @ np.abs(Bw).T, "dx",
+                _flip_terms(dqp, eb, np.abs(Bw).T))
     # dW and the columnwise operand on sampled heads (a head's channels need only that head's dq)
-    heads = np.array([0, 45, 127])
-    dqp_h = oracle.rope_bwd_f32(helpers.f64(inp["dq"][:, torch.from_numpy(heads)].contiguous()), len(heads),
-                                w.Dn, w.Dr, cs, sn, pos).reshape(w.T, -1).astype(np.float64)
+    heads = np.array([0, 17, 45, 64, 90, 101, 126, 127])
+    dq_h = helpers.f64(inp["dq"][:, torch.from_numpy(heads)].contiguous())
+    dqp_h = oracle.rope_bwd(dq_h, len(heads), w.Dn, w.Dr, cs, sn, pos).reshape(w.T, -1)
+    eb_h = rot_error_bound(dq_h, len(heads), w.Dn, w.Dr, cs)
     qb, qb_s = oracle.mxfp8_quantize_columns(dqp_h)
     ch = (heads[:, None] * w.D + np.arange(w.D)[None, :]).reshape(-1)
-    assert np.array_equal(_np(ops["qb"])[ch], qb) and np.array_equal(qb_s_rows[ch], qb_s)
+    helpers.check_mxfp8_decided(_np(ops["qb"])[ch][:, :w.T], qb_s_rows[ch], dqp_h.T.copy(), eb_h.T.copy(),
+                                qb, qb_s, "qb")
     A = oracle.mxfp8_dequantize(qb, qb_s)
-    _check_gemm(dW[torch.from_numpy(ch).to(cuda_device)], A @ Bx.T, np.abs(A) @ np.abs(Bx).T, "dW")
+    _check_gemm(dW[torch.from_numpy(ch).to(cuda_device)], A @ Bx.T, np.abs(A) @ np.abs(Bx).T, "dW",
+                _flip_terms(dqp_h.T.copy(), eb_h.T.copy(), np.abs(Bx).T))
     # db on every channel, 16 heads at a time
     for h0 in range(0, w.H, 16):
-        dqp_c = oracle.rope_bwd_f32(helpers.f64(inp["dq"][:, h0:h0 + 16].contiguous()), 16, w.Dn, w.Dr,
-                                    cs, sn, pos).reshape(w.T, -1).astype(np.float64)
-        _check_db(db[h0 * w.D:(h0 + 16) * w.D], dqp_c, f"db heads {h0}+")
+        dq_c = helpers.f64(inp["dq"][:, h0:h0 + 16].contiguous())
+        dqp_c = oracle.rope_bwd(dq_c, 16, w.Dn, w.Dr, cs, sn, pos).reshape(w.T, -1)
+        _check_db(db[h0 * w.D:(h0 + 16) * w.D], dqp_c, rot_error_bound(dq_c, 16, w.Dn, w.Dr, cs), f"db heads {h0}+")
 
 
 @pytest.mark.parametrize("name,ov", [SHAPES[0], SHAPES[3], SHAPES[4]])

@@ -72,23 +72,28 @@ def test_fwd_mxfp8_weights(cuda_device, name, ov, out_mode):
         helpers.check_mxfp8_close(out[0].cpu().numpy(), out[1].cpu().numpy(), q_ref, rc, rs)
 
 
-def test_fwd_mxfp8_weights_full_size_sampled(cuda_device):
+def test_fwd_mxfp8_weights_full_size(cuda_device):
     """DeepSeek-V3 shape with 1% x50 activation outliers, MXFP8 x and W, MXFP8
-    out, in the benchmark's launch configuration; 32 sampled tokens."""
+    out, in the benchmark's launch configuration (scales in the GEMM's tiled
+    order): every code and scale against the oracle on the dequantized
+    operands; the row-major-scale call gives the same bytes."""
     w = synth.workload("dsv3_fwd_mxfp8w")
     inp = synth.make_inputs(w, seed=0)
     (xq, xsc, Wq, Wsc), (x_deq, W_deq) = _quantized_operands(inp, cuda_device)
+    xst, Wst = _tiled_scales(xsc, Wsc, w)
     d = helpers.to_dev(inp, cuda_device)
     st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    codes, scales = mlaq.fwd(xq, Wq, d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"],
-                             weight_mode="mxfp8", out_mode="mxfp8", x_scales=xsc, w_scales=Wsc,
-                             status=st)
+    args = (xq, Wq, d["cos"], d["sin"], w.H, w.Dn, w.Dr)
+    c1, s1 = mlaq.fwd(*args, pos=d["pos"], weight_mode="mxfp8_tiled", out_mode="mxfp8", x_scales=xst,
+                      w_scales=Wst, status=st)
+    c2, s2 = mlaq.fwd(*args, pos=d["pos"], weight_mode="mxfp8", out_mode="mxfp8", x_scales=xsc, w_scales=Wsc,
+                      status=st)
     mlaq.check_status(st)
-    toks = np.sort(np.random.default_rng(3).choice(w.T, 32, replace=False))
-    q_ref, rc, rs = _oracle(inp, w, x_deq, W_deq, tokens=toks, quantize=True)
-    idx = torch.from_numpy(toks).to(cuda_device)
-    helpers.check_mxfp8_close(codes[idx].cpu().numpy(), scales[idx].cpu().numpy(), q_ref, rc, rs)
+    assert torch.equal(c1, c2) and torch.equal(s1, s2)
+    helpers.check_fwd_all_tokens(inp, w, codes=c1, scales=s1, x64=x_deq, W64=W_deq)
     # context only: error of the quantized path against the unquantized bf16 operands
+    toks = np.arange(0, w.T, 97)
+    q_ref = _oracle(inp, w, x_deq, W_deq, tokens=toks)
     q_bf = helpers.oracle_forward(inp, w, tokens=toks)
     rel = np.linalg.norm(q_ref - q_bf) / np.linalg.norm(q_bf)
     assert rel < 0.1
@@ -120,24 +125,3 @@ def test_fwd_tiled_scales_bit_identical(cuda_device, name, ov):
     c2, s2 = mlaq.fwd(*args, weight_mode="mxfp8_tiled", x_scales=xst, w_scales=Wst, status=st, **kw)
     mlaq.check_status(st)
     assert torch.equal(c1, c2) and torch.equal(s1, s2)
-
-
-def test_fwd_tiled_scales_full_size(cuda_device):
-    """The DeepSeek-V3 MXFP8-weight configuration (T = 4096, 1% x outliers
-    x50) as the benchmark runs it: tiled and gathered scales give the same
-    bytes, and sampled tokens match the oracle on the dequantized operands."""
-    w = synth.workload("dsv3_fwd_mxfp8w")
-    inp = synth.make_inputs(w, seed=6)
-    d = helpers.to_dev(inp, cuda_device)
-    (xq, xsc, Wq, Wsc), (x_deq, W_deq) = _quantized_operands(inp, cuda_device)
-    xst, Wst = _tiled_scales(xsc, Wsc, w)
-    args = (xq, Wq, d["cos"], d["sin"], w.H, w.Dn, w.Dr)
-    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    c1, s1 = mlaq.fwd(*args, pos=d["pos"], weight_mode="mxfp8", x_scales=xsc, w_scales=Wsc, status=st)
-    c2, s2 = mlaq.fwd(*args, pos=d["pos"], weight_mode="mxfp8_tiled", x_scales=xst, w_scales=Wst, status=st)
-    mlaq.check_status(st)
-    assert torch.equal(c1, c2) and torch.equal(s1, s2)
-    tokens = np.sort(np.random.default_rng(5).choice(w.T, 24, replace=False))
-    q_ref, rc, rs = _oracle(inp, w, x_deq, W_deq, tokens=tokens, quantize=True)
-    idx = torch.from_numpy(tokens).to(cuda_device)
-    helpers.check_mxfp8_close(c2[idx].cpu().numpy(), s2[idx].cpu().numpy(), q_ref, rc, rs)

@@ -1,48 +1,19 @@
-"""Pins of the oracle's MXFP8 backward and of its float32 inverse rotation.
+"""Pins of the oracle's MXFP8 backward.
 
 The pages name the MXFP8 quantization helpers (TransformerEngine PR "Add
 support for fused Q Up-Proj GEMM/RoPE/Quant") but give no formula for a
-low-precision backward; the oracle takes the plain reading (operands
-quantized along their reduction dimension, exact products). Pins: a hand
-example of the float32 rotation, its single-rounding order computed through
-float64, the fp64 rotation within float32 rounding, lossless quantization on
-E4M3-exact inputs, and the whole chain rebuilt from the brute-force block
-quantizer of test_oracle_quant and a float64 matmul.
+low-precision backward; the oracle takes the plain reading: the exact RoPE
+backward, operands quantized along their reduction dimension, exact
+products. Pins: lossless quantization on E4M3-exact inputs, the whole chain
+rebuilt from the brute-force block quantizer of test_oracle_quant and a
+float64 matmul (which catches a block along the wrong axis or a transposed
+operand), and the quantization error bound against the unquantized
+gradients.
 """
 import numpy as np
 
 import oracle
 from test_oracle_quant import _all_code_values_torch, _expected_block
-
-
-def test_rope_bwd_f32_hand_example():
-    dq = np.array([[[7.0, 1.0, 2.0]]])                  # T=1, H=1, Dn=1, Dr=2
-    cos = np.array([[0.5, 0.5]], np.float32)
-    sin = np.array([[0.25, 0.25]], np.float32)
-    out = oracle.rope_bwd_f32(dq, 1, 1, 2, cos, sin)
-    assert out.dtype == np.float32
-    assert out.tolist() == [[[7.0, 1.0 * 0.5 + 2.0 * 0.25, 2.0 * 0.5 - 1.0 * 0.25]]]
-
-
-def test_rope_bwd_f32_rounding_order():
-    rng = np.random.default_rng(0)
-    T, H, Dn, Dr = 64, 2, 4, 8
-    dq = rng.standard_normal((T, H, Dn + Dr)).astype(np.float32).astype(np.float64)
-    ang = rng.uniform(0, 6.3, (T, Dr))
-    cos, sin = np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
-    out = oracle.rope_bwd_f32(dq, H, Dn, Dr, cos, sin)
-    h = Dr // 2
-    f32 = lambda v: np.float32(v)  # from float64: products of two float32 are exact there
-    for t in range(T):
-        for hd in range(H):
-            for i in range(h):
-                a, c = dq[t, hd, Dn + i], dq[t, hd, Dn + h + i]
-                p1, p2 = f32(a * float(cos[t, i])), f32(c * float(sin[t, h + i]))
-                q1, q2 = f32(c * float(cos[t, h + i])), f32(a * float(sin[t, i]))
-                assert out[t, hd, Dn + i] == f32(float(p1) + float(p2))
-                assert out[t, hd, Dn + h + i] == f32(float(q1) - float(q2))
-    ref = oracle.rope_bwd(dq, H, Dn, Dr, cos, sin)
-    assert np.max(np.abs(out - ref)) <= 4 * 2.0 ** -24 * np.max(np.abs(ref)) * 2
 
 
 def test_backward_mxfp8_lossless_on_e4m3_values():
@@ -81,10 +52,47 @@ def test_backward_mxfp8_rebuilt_from_brute_force_blocks():
                 out[r, b0:b0 + len(codes)] = table[np.array(codes)] * 2.0 ** (sb - 127)
         return out
 
-    dqp = oracle.rope_bwd_f32(dq, H, Dn, Dr, cos, sin).reshape(T, -1).astype(np.float64)
+    # the rotation: the pinned fp64 RoPE backward (test_oracle_bwd), not this chain's own
+    dqp = oracle.rope_bwd(dq, H, Dn, Dr, cos, sin).reshape(T, -1)
+    assert np.array_equal(g["dq_pre"], dqp)
     A = deq_blocks(dqp)            # blocks along the channels
     B = deq_blocks(W.T)            # W^T rows = columns of W, blocks along the channels
     assert np.allclose(g["dx"], A @ B.T, rtol=0, atol=1e-12)
     Ac = deq_blocks(dqp.T)         # blocks along the tokens
     Xc = deq_blocks(x.T)
     assert np.allclose(g["dW"], Ac @ Xc.T, rtol=0, atol=1e-12)
+
+
+def test_backward_mxfp8_within_the_quantization_bound():
+    """Against the unquantized fp64 gradients: each operand element moves by
+    at most half an E4M3 step, |q - v| <= 2^-4 |v| + 2^-10 2^e (normal
+    relative half-step, plus the subnormal step of the block), so each
+    product term by at most ((1 + 2^-4)^2 - 1) |a b| plus the subnormal
+    terms; summed, that bounds |dx_mx - dx| and |dW_mx - dW|."""
+    rng = np.random.default_rng(3)
+    T, H, Dn, Dr, K = 96, 2, 32, 32, 64
+    dq = rng.standard_normal((T, H, Dn + Dr))
+    x = rng.standard_normal((T, K))
+    W = rng.standard_normal((H * (Dn + Dr), K)) * 0.02
+    ang = rng.uniform(0, 6.3, (T, Dr))
+    cos, sin = np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+    g = oracle.backward_mxfp8(dq, x, W, H, Dn, Dr, cos, sin)
+    ex = oracle.backward(dq, x, W, H, Dn, Dr, cos, sin)
+
+    def half_step(v, axis):  # bound on |quantized - v| with blocks of 32 along `axis`
+        a = np.moveaxis(np.abs(v), axis, -1)
+        n = a.shape[-1]
+        pad = (-n) % 32
+        blk = np.pad(a, [(0, 0)] * (a.ndim - 1) + [(0, pad)]).reshape(a.shape[:-1] + (-1, 32))
+        e = np.ceil(np.log2(np.maximum(blk.max(-1), 1e-300) / 448.0))
+        sub = np.repeat(2.0 ** (e - 10), 32, axis=-1)[..., :n]
+        return np.moveaxis(2.0 ** -4 * a + sub, -1, axis)
+
+    A, B = ex["dq_pre"], W
+    dA, dB = half_step(A, 1), half_step(B, 0)
+    bound_dx = np.abs(A) @ dB + dA @ np.abs(B) + dA @ dB
+    assert (np.abs(g["dx"] - ex["dx"]) <= bound_dx * (1 + 1e-9)).all()
+    dAt, dX = half_step(A, 0), half_step(x, 0)
+    bound_dw = np.abs(A).T @ dX + dAt.T @ np.abs(x) + dAt.T @ dX
+    assert (np.abs(g["dW"] - ex["dW"]) <= bound_dw * (1 + 1e-9)).all()
+    assert np.allclose(g["db"], ex["db"], rtol=0, atol=0)

@@ -48,6 +48,26 @@ def test_decode_closed_form(code, value):
     assert oracle.e4m3_decode(code) == value
 
 
+def test_decode_bf16_every_pattern_matches_torch():
+    """All 65 536 bf16 bit patterns decode to torch's own bf16 -> float64
+    conversion (a library routine): same value, same sign of zero, NaN
+    exactly where torch gives NaN. Every oracle test feeds its inputs through
+    this decode, so it is pinned on its own."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode_bf16(bits)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    nan_ref, nan_got = np.isnan(ref), np.isnan(got)
+    assert np.array_equal(nan_ref, nan_got)
+    assert nan_got.sum() == 2 * 127  # exponent field 255, mantissa != 0, both signs
+    assert np.array_equal(got[~nan_got], ref[~nan_ref])
+    assert np.array_equal(np.signbit(got[~nan_got]), np.signbit(ref[~nan_ref]))
+    # closed forms: 1.0, -2.0, the smallest subnormal, the largest finite, infinity
+    for b, v in ((0x3F80, 1.0), (0xC000, -2.0), (0x0001, 2.0 ** -133),
+                 (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127), (0x7F80, np.inf), (0x8000, -0.0)):
+        assert oracle.decode_bf16(np.array([b], np.uint16))[0] == v
+        assert math.copysign(1.0, oracle.decode_bf16(np.array([b], np.uint16))[0]) == math.copysign(1.0, v)
+
+
 def test_encode_every_bf16_matches_torch_rne():
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     vals = oracle.decode_bf16(bits)

@@ -53,7 +53,6 @@ for T, K, H, Dn, Dr in [(37, 24, 3, 32, 16), (5, 8, 2, 0, 64), (19, 40, 1, 64, 3
     oracle.forward(x, W, H, Dn, Dr, cos, sin, pos, b, quantize=True)
     oracle.forward(x, W, H, Dn, Dr, cos, sin, pos, None, quantize=False)
     oracle.backward(dq, x, W, H, Dn, Dr, cos, sin, pos)
-    oracle.rope_bwd_f32(dq, H, Dn, Dr, cos, sin, pos)
     if Dr in (32, 64) and D % 32 == 0:
         oracle.backward_mxfp8(dq, x, W, H, Dn, Dr, cos, sin, pos)
     # rejections: a position past the table, a table narrower than Dr
