@@ -170,6 +170,40 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape *shape, int weight_mode, int out_
                              uint8_t *q_scales_out, int *dev_status, void *stream);
 
 /*
+ * The per-position rotary table in the layout the forward's epilogue reads
+ * fastest (an addition of this library; the pages only name the cos/sin
+ * cache, Megatron-LM PR "Fix fused MLA YaRN RoPE query kernel corrupting
+ * upstream tensor in-place", Problem section). For i < Dr/2 and p < cs_rows,
+ * packed[i][p] is the float4 (cos[p][i], sin[p][i], cos[p][i + Dr/2],
+ * sin[p][i + Dr/2]): the four values that rotate pair i of a token at
+ * position p, with the entries of consecutive positions adjacent. It holds
+ * the table's first Dr columns, copied bit for bit (no arithmetic).
+ *   cos_tab/sin_tab [cs_rows, cs_width] fp32 (row pitch cs_width >= Dr, else
+ *   MLA_ERR_ROPE_WIDTH), packed: mla_rope_table_packed_bytes(cs_rows, Dr)
+ *   bytes, 16-byte aligned, overlapping neither table (MLA_ERR_ALIAS).
+ *   Enqueued on `stream`; cs_rows = 0 is a no-op. Dr must be even and > 0.
+ * A table is a model constant: pack it once and pass it to every
+ * mla_q_uproj_fwd_packed call.
+ */
+MLAQ_API size_t mla_rope_table_packed_bytes(int64_t cs_rows, int Dr);
+MLAQ_API int mla_rope_table_pack(int64_t cs_rows, int64_t cs_width, int Dr, const float *cos_tab,
+                                 const float *sin_tab, float *packed, void *stream);
+
+/*
+ * mla_q_uproj_fwd with the rotary table packed by mla_rope_table_pack
+ * (rope_packed, 16-byte aligned, shape->cs_rows positions; shape->cs_width
+ * is the width of the table it was packed from and must be >= Dr). Same
+ * arguments otherwise, same checks, same results bit for bit: only the
+ * table's memory layout differs, so a warp's table reads for 32 tokens at
+ * consecutive positions are 512 contiguous bytes instead of 32 rows.
+ */
+MLAQ_API int mla_q_uproj_fwd_packed(const mla_q_shape *shape, int weight_mode, int out_mode,
+                                    const void *x, const uint8_t *x_scales, const void *W,
+                                    const uint8_t *w_scales, const void *bias, const float *rope_packed,
+                                    const int32_t *pos, void *q_out, uint8_t *q_scales_out,
+                                    int *dev_status, void *stream);
+
+/*
  * Backward, input gradient: dx = (J^T dq) W.
  * TransformerEngine PR "Add a backwards linear function to be used with the
  * fused mla q up-proj", summary and sequence diagram (RoPE backward, then the
@@ -361,7 +395,7 @@ MLAQ_API int mla_kv_uproj_fwd(const mla_kv_shape *shape, const void *c_kv, const
                               void *stream);
 
 /* Size of the device scratch array mla_q_uproj_bwd_dgrad_noalloc uses. */
-#define MLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+#define MLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
 /*
  * dgrad without any workspace argument, for callers that cannot allocate
@@ -371,20 +405,25 @@ MLAQ_API int mla_kv_uproj_fwd(const mla_kv_shape *shape, const void *c_kv, const
  * other device memory, or a latency-critical path that cannot pay for
  * cudaMalloc's implicit synchronization. This entry point computes exactly
  * what mla_q_uproj_bwd_dgrad computes, with the same arguments minus the
- * workspace, and takes its split-reduction partials from a scratch array of
+ * workspace, and takes its workspace (the partial sums of split tiles and,
+ * without dq_pre_rope, the rotated rope channels) from a scratch array of
  * MLA_NOALLOC_SCRATCH_BYTES that the library keeps in device global memory
  * (every GPU that loads the library holds it until the process exits).
- *   - The first call on a device looks up that device's scratch address (a
+ *   - Arguments are checked first, exactly as mla_q_uproj_bwd_dgrad checks
+ *     them, and return the same codes.
+ *   - The first call in a CUDA context (per device; a context created after
+ *     a device reset counts as new) looks up the scratch address there (a
  *     CUDA runtime query, no allocation); make that first call before any
  *     stream capture. It allocates nothing, ever.
- *   - A shape whose least workspace (mla_q_uproj_workspace_size(shape, 4))
- *     exceeds MLA_NOALLOC_SCRATCH_BYTES is rejected with MLA_ERR_WORKSPACE;
- *     shapes that need no workspace always run. dgrad takes the fastest
- *     path whose workspace fits in the scratch.
+ *   - A shape whose least workspace (mla_q_uproj_workspace_size(shape, 4),
+ *     or less with dq_pre_rope) exceeds MLA_NOALLOC_SCRATCH_BYTES is rejected
+ *     with MLA_ERR_WORKSPACE. Otherwise the whole scratch is handed to dgrad,
+ *     which takes the fastest path whose workspace fits in it (with the same
+ *     path, the result is bit-identical to mla_q_uproj_bwd_dgrad's).
  *   - All calls share the one array. Nothing in it has to start at zero
- *     (every partial the reduction reads is written earlier in the same
- *     call), but calls that overlap on the GPU (other streams, other threads)
- *     race on it: serialize them.
+ *     (every partial dgrad reads is written earlier in the same call, and
+ *     its flags carry a value new to each launch), but calls that overlap on
+ *     the GPU (other streams, other threads) race on it: serialize them.
  */
 MLAQ_API int mla_q_uproj_bwd_dgrad_noalloc(const mla_q_shape *shape, const void *dq, const void *W,
                                            const float *cos_tab, const float *sin_tab,

@@ -143,6 +143,51 @@ def test_bwd_rejects(L, which):
     assert _bwd(L, which, shape()) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
 
 
+def test_noalloc_dgrad_returns_the_same_codes(L):
+    """mla_q_uproj_bwd_dgrad_noalloc runs the allocating entry point's
+    argument checks before anything else: the same status for every bad
+    argument (narrow table, null pointer, overlap, unsupported split, odd K,
+    implicit positions past the table, misaligned rope buffer) and for a good
+    one on a machine without a GPU."""
+    def noalloc(s, dq=p(0), W=p(1), cos=p(2), sin=p(3), pos=None, dx=p(4), rope=None):
+        return L.mla_q_uproj_bwd_dgrad_noalloc(ctypes.byref(s), dq, W, cos, sin, pos, dx, rope, None, None)
+    cases = [dict(s=shape(cs_width=8)), dict(s=shape(), dq=None), dict(s=shape(), dx=p(0)),
+             dict(s=shape(), dx=p(1)), dict(s=shape(Dn=24)), dict(s=shape(K=36)), dict(s=shape(T=257)),
+             dict(s=shape(Dr=3)), dict(s=shape(), rope=p(0)), dict(s=shape(), rope=ctypes.c_void_p(FAKE * 9 + 8)),
+             dict(s=shape())]
+    for c in cases:
+        kw = {k: v for k, v in c.items() if k != "s"}
+        ref = _bwd(L, "dgrad", c["s"], dq=kw.get("dq", p(0)), op=kw.get("W", p(1)), out=kw.get("dx", p(4)),
+                   rope=kw.get("rope"))
+        assert noalloc(c["s"], **kw) == ref, c
+
+
+def test_rope_table_pack_rejects(L):
+    pk = L.mla_rope_table_pack
+    assert L.mla_rope_table_packed_bytes(100, 64) == 100 * 32 * 16
+    assert L.mla_rope_table_packed_bytes(100, 63) == 0
+    assert pk(10, 8, 16, p(0), p(1), p(2), None) == S["MLA_ERR_ROPE_WIDTH"]   # narrower than Dr
+    assert pk(10, 16, 15, p(0), p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]  # odd Dr
+    assert pk(-1, 16, 16, p(0), p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]
+    assert pk(10, 16, 16, None, p(1), p(2), None) == S["MLA_ERR_INVALID_ARG"]
+    assert pk(10, 16, 16, p(0), p(1), ctypes.c_void_p(FAKE * 2 + 4), None) == S["MLA_ERR_ALIGNMENT"]
+    assert pk(10, 16, 16, p(0), p(1), p(0), None) == S["MLA_ERR_ALIAS"]        # over cos
+    assert pk(0, 16, 16, None, None, None, None) == S["MLA_OK"]                 # nothing to pack
+    assert pk(10, 16, 16, p(0), p(1), p(2), None) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+
+
+def test_fwd_packed_checks(L):
+    def fp(s, packed=p(2), q=p(5), qs=p(6), pos=None):
+        return L.mla_q_uproj_fwd_packed(ctypes.byref(s), 0, 1, p(0), None, p(1), None, None, packed, pos,
+                                        q, qs, None, None)
+    assert fp(shape(cs_width=8)) == S["MLA_ERR_ROPE_WIDTH"]
+    assert fp(shape(), packed=None) == S["MLA_ERR_INVALID_ARG"]
+    assert fp(shape(), packed=ctypes.c_void_p(FAKE * 2 + 4)) == S["MLA_ERR_ALIGNMENT"]  # needs 16 bytes
+    assert fp(shape(), q=p(2)) == S["MLA_ERR_ALIAS"]            # q over the packed table
+    assert fp(shape(T=257)) == S["MLA_ERR_POS_RANGE"]
+    assert fp(shape()) in (S["MLA_ERR_CUDA"], S["MLA_OK"])
+
+
 def test_rope_buffer_checks(L):
     # dgrad writes dq_pre_rope (an output): it may overlap nothing
     ok = (S["MLA_ERR_CUDA"], S["MLA_OK"])

@@ -14,7 +14,8 @@ channels are exact. Bars:
   * W's and x's columnwise copies (quantized straight from bf16): bit-exact;
   * dq_pre's two copies: bit-exact wherever the MXFP8 rule decides the scale
     and code for every value within +-eb (helpers.mxfp8_decided: at least
-    99% of the elements), elsewhere within one E4M3 step on the GPU's grid;
+    90% of the elements; a single token at position 0 has rotation ties),
+    elsewhere within one E4M3 step on the GPU's grid;
     the token padding to a multiple of 128 is zero;
   * dx, dW: |gpu - ref| <= 2^-8 |ref| + 2^-14 S + F elementwise, S = the sum
     of |products| (bf16 output rounding plus fp32 accumulation of exact

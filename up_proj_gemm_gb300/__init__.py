@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "MlaError", "lib", "library_path", "fwd", "bwd_dgrad", "bwd_wgrad", "mxfp8_quantize_rows",
-    "mxfp8_quantize_cols", "mxfp8_swizzle_scales", "kv_fwd", "bwd_mxfp8", "bwd_mxfp8_layout",
+    "mxfp8_quantize_cols", "mxfp8_swizzle_scales", "kv_fwd", "rope_table_pack", "bwd_mxfp8", "bwd_mxfp8_layout",
     "bwd_mxfp8_operands", "bwd_mxfp8_prepare_weight", "w_scale_group", "wait_selftest",
     "workspace_size", "status_string", "check_status", "Shape", "KvShape", "Mxfp8BwdLayout", "STATUS",
     "WEIGHT_MODES", "OUT_MODES",
@@ -71,6 +71,10 @@ _int = ctypes.c_int
 _SIGS = {
     "mla_q_uproj_fwd": (_int, [ctypes.POINTER(Shape), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                _vp, _vp, _vp, _vp, _vp]),
+    "mla_q_uproj_fwd_packed": (_int, [ctypes.POINTER(Shape), _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _vp, _vp, _vp]),
+    "mla_rope_table_pack": (_int, [_i64, _i64, _int, _vp, _vp, _vp, _vp]),
+    "mla_rope_table_packed_bytes": (ctypes.c_size_t, [_i64, _int]),
     "mla_q_uproj_bwd_dgrad": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _vp, _vp]),
     "mla_q_uproj_bwd_wgrad": (_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -205,8 +209,24 @@ def workspace_size(T, K, H, Dn, Dr, cs_rows, cs_width, which: int) -> int:
     return int(lib().mla_q_uproj_workspace_size(ctypes.byref(s), int(which)))
 
 
+def rope_table_pack(cos, sin, Dr, out=None, stream=None):
+    """The rotary table in the forward's packed layout (mla_rope_table_pack):
+    float32 [Dr/2, rows, 4], entry [i, p] = (cos[p, i], sin[p, i],
+    cos[p, i + Dr/2], sin[p, i + Dr/2]). Pack once, pass as ``rope_packed``."""
+    dev = cos.device
+    _need(cos, "cos", torch.float32, dev, ndim=2)
+    _need(sin, "sin", torch.float32, dev, shape=cos.shape)
+    rows, width = cos.shape
+    if out is None:
+        out = torch.empty((Dr // 2, rows, 4), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev, numel=rows * (Dr // 2) * 4)
+    _call(lib().mla_rope_table_pack, "mla_rope_table_pack", int(rows), int(width), int(Dr), _ptr(cos), _ptr(sin),
+          _ptr(out), _stream(dev, stream))
+    return out
+
+
 def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_mode="mxfp8",
-        x_scales=None, w_scales=None, q_out=None, q_scales=None, status=None, stream=None):
+        x_scales=None, w_scales=None, q_out=None, q_scales=None, status=None, stream=None, rope_packed=None):
     """Fused forward. Returns q [T, H, D] (bf16 or uint8 E4M3 codes), plus the
     scales uint8 [T, H, ceil(D/32)] when out_mode is "mxfp8", or head-major
     [H, T, ceil(D/32)] when it is "mxfp8_bhsd", or [H, S] when it is
@@ -218,7 +238,10 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
     w_scales [N, K/32] uint8 E8M0.
     weight_mode "mxfp8_tiled": the same codes with the scales already tiled:
     x_scales = mxfp8_swizzle_scales(x scales), w_scales =
-    mxfp8_swizzle_scales(W scales, group=w_scale_group(...)) (flat uint8)."""
+    mxfp8_swizzle_scales(W scales, group=w_scale_group(...)) (flat uint8).
+
+    rope_packed: the table packed by rope_table_pack(cos, sin, Dr); cos and
+    sin are then only read for their shape (same results, bit for bit)."""
     wm, om = WEIGHT_MODES[weight_mode], OUT_MODES[out_mode]
     in_dtype = torch.uint8 if wm else torch.bfloat16
     dev = x.device
@@ -228,6 +251,8 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
     N = H * D
     _need(W, "W", in_dtype, dev, shape=(N, K))
     _tables(cos, sin, dev, T, pos)
+    if rope_packed is not None:
+        _need(rope_packed, "rope_packed", torch.float32, dev, numel=cos.shape[0] * (Dr // 2) * 4)
     _status(status, dev)
     if bias is not None:
         _need(bias, "bias", torch.bfloat16, dev, shape=(N,))
@@ -258,9 +283,14 @@ def fwd(x, W, cos, sin, H, Dn, Dr, bias=None, pos=None, weight_mode="bf16", out_
     if om:
         _need(q_scales, "q_scales", torch.uint8, dev, numel=math.prod(sshape))
     s = _shape(T, K, H, Dn, Dr, cos)
-    _call(lib().mla_q_uproj_fwd, "mla_q_uproj_fwd", ctypes.byref(s), wm, om, _ptr(x),
-          _ptr(x_scales), _ptr(W), _ptr(w_scales), _ptr(bias), _ptr(cos), _ptr(sin), _ptr(pos),
-          _ptr(q_out), _ptr(q_scales if om else None), _ptr(status), _stream(dev, stream))
+    if rope_packed is not None:
+        _call(lib().mla_q_uproj_fwd_packed, "mla_q_uproj_fwd_packed", ctypes.byref(s), wm, om, _ptr(x),
+              _ptr(x_scales), _ptr(W), _ptr(w_scales), _ptr(bias), _ptr(rope_packed), _ptr(pos),
+              _ptr(q_out), _ptr(q_scales if om else None), _ptr(status), _stream(dev, stream))
+    else:
+        _call(lib().mla_q_uproj_fwd, "mla_q_uproj_fwd", ctypes.byref(s), wm, om, _ptr(x),
+              _ptr(x_scales), _ptr(W), _ptr(w_scales), _ptr(bias), _ptr(cos), _ptr(sin), _ptr(pos),
+              _ptr(q_out), _ptr(q_scales if om else None), _ptr(status), _stream(dev, stream))
     return (q_out, q_scales) if om else q_out
 
 

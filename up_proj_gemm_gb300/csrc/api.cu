@@ -222,11 +222,12 @@ MLAQ_API size_t mla_q_uproj_workspace_size(const mla_q_shape* shape, int which) 
                                                   false);
 }
 
-MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_mode, const void* x,
-                             const uint8_t* x_scales, const void* W, const uint8_t* w_scales,
-                             const void* bias, const float* cos_tab, const float* sin_tab,
-                             const int32_t* pos, void* q_out, uint8_t* q_scales_out, int* dev_status,
-                             void* stream) {
+// The forward behind mla_q_uproj_fwd (cos_tab, sin_tab) and
+// mla_q_uproj_fwd_packed (packed, the mla_rope_table_pack layout).
+static int fwd_entry(const mla_q_shape* shape, int weight_mode, int out_mode, const void* x,
+                     const uint8_t* x_scales, const void* W, const uint8_t* w_scales, const void* bias,
+                     const float* cos_tab, const float* sin_tab, const float* packed, const int32_t* pos,
+                     void* q_out, uint8_t* q_scales_out, int* dev_status, void* stream) {
     int D;
     int64_t N;
     int st = check_shape(shape, &D, &N);
@@ -243,7 +244,8 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
     if (mxo != (q_scales_out != nullptr)) return MLA_ERR_INVALID_ARG;
     if (s.T > 0 && (!x || !W || !q_out)) return MLA_ERR_INVALID_ARG;
     if (mxw && (s.K % 32)) return MLA_ERR_INVALID_ARG;  // scales are per 32 along K
-    st = check_table_and_positions(&s, cos_tab, sin_tab, pos);
+    st = packed ? check_table_and_positions(&s, packed, packed, pos)
+                : check_table_and_positions(&s, cos_tab, sin_tab, pos);
     if (st != MLA_OK) return st;
     if (s.T == 0) return MLA_OK;
 
@@ -258,11 +260,13 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
     if ((s.K * esz) % 16) return MLA_ERR_ALIGNMENT;
     if (!aligned(x, 16) || !aligned(W, 16) || !aligned(q_out, 16) || !aligned(x_scales, 4) ||
         !aligned(w_scales, 4) || !aligned(bias, 16) || !aligned(cos_tab, 4) || !aligned(sin_tab, 4) ||
-        !aligned(pos, 4) || !aligned(dev_status, 4))
+        !aligned(packed, 16) || !aligned(pos, 4) || !aligned(dev_status, 4))
         return MLA_ERR_ALIGNMENT;
 
     const int64_t NB = (D + 31) / 32;
-    const int64_t table = s.cs_rows * s.cs_width * 4;
+    // the table's byte extent: rows x width fp32 each, or the packed rows x Dr fp32
+    const int64_t table = packed ? s.cs_rows * s.Dr * 4 : s.cs_rows * s.cs_width * 4;
+    if (packed) cos_tab = sin_tab = packed;  // (extents for the overlap check only)
     const int64_t qs_bytes = out_mode == MLA_OUT_MXFP8_BHSD_SWIZZLED
                                  ? (int64_t)s.H * (int64_t)mxfp8_swizzled_scale_bytes(s.T, NB)
                                  : s.T * s.H * NB;
@@ -295,13 +299,51 @@ MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_
     a.W = W;
     a.w_scales = w_scales;
     a.bias = bias;
-    a.cos_tab = cos_tab;
-    a.sin_tab = sin_tab;
+    a.cos_tab = packed ? nullptr : cos_tab;
+    a.sin_tab = packed ? nullptr : sin_tab;
+    a.rope_packed = packed;
     a.pos = pos;
     a.q_out = q_out;
     a.q_scales = q_scales_out;
     a.status = dev_status;
     return launch_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+MLAQ_API int mla_q_uproj_fwd(const mla_q_shape* shape, int weight_mode, int out_mode, const void* x,
+                             const uint8_t* x_scales, const void* W, const uint8_t* w_scales,
+                             const void* bias, const float* cos_tab, const float* sin_tab,
+                             const int32_t* pos, void* q_out, uint8_t* q_scales_out, int* dev_status,
+                             void* stream) {
+    return fwd_entry(shape, weight_mode, out_mode, x, x_scales, W, w_scales, bias, cos_tab, sin_tab, nullptr, pos,
+                     q_out, q_scales_out, dev_status, stream);
+}
+
+MLAQ_API int mla_q_uproj_fwd_packed(const mla_q_shape* shape, int weight_mode, int out_mode, const void* x,
+                                    const uint8_t* x_scales, const void* W, const uint8_t* w_scales,
+                                    const void* bias, const float* rope_packed, const int32_t* pos, void* q_out,
+                                    uint8_t* q_scales_out, int* dev_status, void* stream) {
+    return fwd_entry(shape, weight_mode, out_mode, x, x_scales, W, w_scales, bias, nullptr, nullptr, rope_packed,
+                     pos, q_out, q_scales_out, dev_status, stream);
+}
+
+MLAQ_API size_t mla_rope_table_packed_bytes(int64_t cs_rows, int Dr) {
+    if (cs_rows < 0 || cs_rows > kI32Max || Dr <= 0 || (Dr & 1)) return 0;
+    return (size_t)cs_rows * (size_t)(Dr / 2) * 16;
+}
+
+MLAQ_API int mla_rope_table_pack(int64_t cs_rows, int64_t cs_width, int Dr, const float* cos_tab,
+                                 const float* sin_tab, float* packed, void* stream) {
+    if (cs_rows < 0 || cs_width < 0 || cs_rows > kI32Max || cs_width > kI32Max || Dr <= 0 || (Dr & 1))
+        return MLA_ERR_INVALID_ARG;
+    if (cs_width < Dr) return MLA_ERR_ROPE_WIDTH;
+    if (cs_rows == 0) return MLA_OK;
+    if (!cos_tab || !sin_tab || !packed) return MLA_ERR_INVALID_ARG;
+    if (!aligned(cos_tab, 4) || !aligned(sin_tab, 4) || !aligned(packed, 16)) return MLA_ERR_ALIGNMENT;
+    const int64_t table = cs_rows * cs_width * 4;
+    const Range outs[] = {rng(packed, (int64_t)mla_rope_table_packed_bytes(cs_rows, Dr))};
+    const Range ins[] = {rng(cos_tab, table), rng(sin_tab, table)};
+    if (any_alias(outs, ins)) return MLA_ERR_ALIAS;
+    return launch_rope_table_pack(cs_rows, cs_width, Dr, cos_tab, sin_tab, packed, static_cast<cudaStream_t>(stream));
 }
 
 static int check_bwd(const mla_q_shape* shape, const void* dq, const void* op, const float* cos_tab,
@@ -319,19 +361,34 @@ static int check_bwd(const mla_q_shape* shape, const void* dq, const void* op, c
     return MLA_OK;
 }
 
+extern "C++" {
+namespace mlaq {
+// dgrad's checks that do not involve the workspace (shape, table, positions,
+// support, alignment), in the order both dgrad entry points run them.
+int dgrad_check_args(const mla_q_shape* shape, const void* dq, const void* W, const float* cos_tab,
+                     const float* sin_tab, const int32_t* pos, const void* dx, const void* dq_pre_rope,
+                     const int* dev_status) {
+    int D;
+    int64_t N;
+    int st = check_bwd(shape, dq, W, cos_tab, sin_tab, pos, dx, nullptr, 0, 1, &D, &N);
+    if (st != MLA_OK) return st;
+    if (!aligned(dq, 16) || !aligned(W, 16) || !aligned(dx, 16) || !aligned(cos_tab, 4) ||
+        !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4) || !aligned(dq_pre_rope, 16))
+        return MLA_ERR_ALIGNMENT;
+    return MLA_OK;
+}
+}  // namespace mlaq
+}  // extern "C++"
+
 MLAQ_API int mla_q_uproj_bwd_dgrad(const mla_q_shape* shape, const void* dq, const void* W,
                                    const float* cos_tab, const float* sin_tab, const int32_t* pos,
                                    void* dx, void* dq_pre_rope, void* workspace, size_t ws_bytes,
                                    int* dev_status, void* stream) {
-    int D;
-    int64_t N;
-    int st = check_bwd(shape, dq, W, cos_tab, sin_tab, pos, dx, workspace, ws_bytes, 1, &D, &N);
+    int st = dgrad_check_args(shape, dq, W, cos_tab, sin_tab, pos, dx, dq_pre_rope, dev_status);
     if (st != MLA_OK) return st;
+    if (!aligned(workspace, 16)) return MLA_ERR_ALIGNMENT;
     const mla_q_shape& s = *shape;
-    if (!aligned(dq, 16) || !aligned(W, 16) || !aligned(dx, 16) || !aligned(cos_tab, 4) ||
-        !aligned(sin_tab, 4) || !aligned(pos, 4) || !aligned(dev_status, 4) || !aligned(workspace, 16) ||
-        !aligned(dq_pre_rope, 16))
-        return MLA_ERR_ALIGNMENT;
+    const int64_t N = (int64_t)s.H * (s.Dn + s.Dr);
     const int64_t table = s.cs_rows * s.cs_width * 4;
     // the least workspace dgrad takes (the fused path's); with at least
     // mla_q_uproj_workspace_size(shape, 1) bytes it takes the pre-rotated path

@@ -46,6 +46,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstring>
 
 #include "internal.h"
@@ -99,6 +100,13 @@ struct BwdParams {
     // (dgrad only; the parts write fp32 partials to ws, summed afterwards)
     int ksplit, kts, num_units;
     float* ws;
+    // dgrad_pre_kernel's stream-K schedule: (token tile, K step) iterations,
+    // one fp32 partial slot [BN/4][256] float4 and one flag per CTA (null
+    // when no tile is split), and this launch's flag value
+    long long sk_total;
+    float* sk_slots;
+    unsigned* sk_flags;
+    unsigned sk_epoch;
     uint16_t* db;
     int* status;
 };
@@ -1094,12 +1102,45 @@ __global__ void __launch_bounds__(256) rope_pre_kernel(const uint16_t* __restric
 // Dn % 64 == 0, so each 64-channel K chunk is all pass-through (A from dq) or
 // all rope (A from rope_out, a {64, T, H} view). 256-token x BN tiles: two
 // M = 128 MMAs per K step into TMEM columns 0 and 256 (one accumulator pair,
-// not double-buffered; the units are long), one ring of A + B stages.
+// not double-buffered; the segments are long), one ring of A + B stages.
 // Warps: 0 producer, 1 MMA issuer, 2-5 epilogue of rows 0-127, 6-9 of rows
 // 128-255 (warp w reads TMEM lanes 32 (w % 4) ...).
+//
+// Schedule (stream-K over groups): the CTAs form groups of num_n_tiles, CTA
+// j of a group computing column tile j, so the CTAs of a group read the same
+// dq rows at the same time and share them in L2. The groups split the
+// (token tile, K step) iterations evenly: group g takes the contiguous range
+// [sk_begin(g), sk_begin(g + 1)), in token-tile-major order. A range starts
+// and ends anywhere inside a token tile, so a tile may be split between
+// consecutive groups: the CTA holding the tile's first K step (its owner)
+// finishes it. A CTA whose range starts inside a tile (its first segment;
+// only that one can) writes that segment's fp32 partial sums to its own
+// workspace slot and raises its flag; the owner, which reaches the tile at
+// the end of its range, waits for the flags of the later CTAs of the same
+// column (bounded), adds their partials in group order (deterministic) and
+// writes dx. Partials are stored column-group-major: float4 (row, 4c..4c+3)
+// at [c][row], so a warp's 32 rows of one float4 column are 512 contiguous
+// bytes.
 constexpr int kDpThreads = 320;
 constexpr int kDpBM = 256;
 constexpr uint32_t kDpABytes = (uint32_t)kDpBM * 128u;
+
+// First (token tile, K step) iteration of group g (of `groups`), iterations
+// token-tile major: sk_total = token tiles x K steps.
+__device__ __forceinline__ long long sk_begin(const BwdParams& p, int g, int groups) {
+    return p.sk_total * (long long)g / groups;
+}
+
+// The next segment [k0, k1) of token tile mt in a range that continues at
+// iteration it (< end); advances it.
+__device__ __forceinline__ void sk_segment(const BwdParams& p, long long& it, long long end, int& mt, int& k0,
+                                           int& k1) {
+    mt = (int)(it / p.k_tiles);
+    k0 = (int)(it - (long long)mt * p.k_tiles);
+    const long long left = end - it;
+    k1 = left < (long long)(p.k_tiles - k0) ? k0 + (int)left : p.k_tiles;
+    it += k1 - k0;
+}
 
 __global__ void __launch_bounds__(kDpThreads, 1)
     dgrad_pre_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -1117,6 +1158,11 @@ __global__ void __launch_bounds__(kDpThreads, 1)
     const int lane = threadIdx.x & 31;
     constexpr int BK = kBKD;
     constexpr uint32_t CHB = (uint32_t)BK * 128u;
+    const int NT = p.num_n_tiles;
+    const int groups = (int)gridDim.x / NT;
+    const int grp = (int)blockIdx.x / NT;
+    const int nt = (int)blockIdx.x - grp * NT;  // this CTA's column tile
+    const long long beg = sk_begin(p, grp, groups), end = sk_begin(p, grp + 1, groups);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -1150,10 +1196,9 @@ __global__ void __launch_bounds__(kDpThreads, 1)
             int s = 0;
             uint32_t ph = 0, issued_mask = 0, issued_par = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                int tile, k0, k1;
-                unit_range(p, u, tile, k0, k1);
-                const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
+            for (long long it = beg; ok && it < end;) {
+                int mt, k0, k1;
+                sk_segment(p, it, end, mt, k0, k1);
                 int c0 = (k0 * BK) % p.D, head = (k0 * BK) / p.D;  // chunk position, no division per stage
                 for (int kt = k0; kt < k1; ++kt) {
                     if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
@@ -1191,9 +1236,9 @@ __global__ void __launch_bounds__(kDpThreads, 1)
             uint32_t ph = 0;
             int local = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++local) {
-                int tile, k0, k1;
-                unit_range(p, u, tile, k0, k1);
+            for (long long it = beg; ok && it < end; ++local) {
+                int mt, k0, k1;
+                sk_segment(p, it, end, mt, k0, k1);
                 if (!mbar_wait(sm.tempty(0), ((uint32_t)local & 1u) ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -1228,17 +1273,34 @@ __global__ void __launch_bounds__(kDpThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
+        // The 8 warps agree through named barrier 1 (256 threads) on every
+        // step that one of them may fail, so none waits at a barrier for a
+        // warp that has left.
         const int quad = warp & 3;
         const int hm = (warp - 2) >> 2;  // which accumulator: token rows 0-127 or 128-255
         const int row = hm * 128 + quad * 32 + lane;
+        const bool leader = threadIdx.x == 64;  // warp 2, lane 0: flag waits and writes
+        const long long slot_floats = (long long)kDpBM * p.BN;
+        float* my_slot = p.sk_slots ? p.sk_slots + (long long)blockIdx.x * slot_floats : nullptr;
         int local = 0;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
-            int tile, sp;
-            unit_split(p, u, tile, sp);
-            if (!mbar_wait(sm.tfull(0), (uint32_t)local & 1u, abort_flag)) break;
+        for (long long it = beg; it < end; ++local) {
+            int mt, k0, k1;
+            sk_segment(p, it, end, mt, k0, k1);
+            bool ok = mbar_wait(sm.tfull(0), (uint32_t)local & 1u, abort_flag);
+            if (!named_bar_and(1, 256, ok)) break;
             tc_fence_after();
-            const int mt = tile / p.num_n_tiles;
-            const int nt = tile % p.num_n_tiles;
+            const bool contrib = k0 > 0;               // a later part of a split tile
+            const bool owner = !contrib && k1 < p.k_tiles;  // a split tile's first part
+            int g_last = grp;                          // the last group holding part of this tile
+            if (owner) {
+                const long long s_last = (long long)(mt + 1) * p.k_tiles - 1;
+                g_last = (int)(((s_last + 1) * groups - 1) / p.sk_total);
+                bool got = true;
+                if (leader)
+                    for (int g2 = grp + 1; got && g2 <= g_last; ++g2)
+                        got = wait_flag_gpu(p.sk_flags + g2 * NT + nt, p.sk_epoch, abort_flag);
+                if (!named_bar_and(1, 256, got)) g_last = grp;  // timed out: the status says so
+            }
             const int64_t orow = (int64_t)mt * kDpBM + row;  // token
             const bool valid = orow < p.out_rows;
             const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)hm * kAccStride;
@@ -1247,26 +1309,51 @@ __global__ void __launch_bounds__(kDpThreads, 1)
                 __syncwarp();
                 tmem_ld32(trow + col, r);
                 tmem_ld_wait();
-                const int64_t c0 = (int64_t)nt * p.BN + col;
-                if (valid && p.ws) {
-                    float* dst = p.ws + ((int64_t)sp * p.out_rows + orow) * p.out_cols + c0;
+                if (contrib) {
+                    float4* dst = reinterpret_cast<float4*>(my_slot) + (int64_t)(col / 4) * kDpBM + row;
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        if (c0 + i + 4 <= p.out_cols) st_global_v4(dst + i, r[i], r[i + 1], r[i + 2], r[i + 3]);
-                } else if (valid) {
+                    for (int i = 0; i < 8; ++i)
+                        dst[(int64_t)i * kDpBM] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                              __uint_as_float(r[4 * i + 2]),
+                                                              __uint_as_float(r[4 * i + 3]));
+                    continue;
+                }
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                for (int g2 = grp + 1; g2 <= g_last; ++g2) {
+                    const float4* src = reinterpret_cast<const float4*>(p.sk_slots + (long long)(g2 * NT + nt) * slot_floats) +
+                                        (int64_t)(col / 4) * kDpBM + row;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 a = __ldcg(src + (int64_t)i * kDpBM);
+                        v[4 * i] += a.x;
+                        v[4 * i + 1] += a.y;
+                        v[4 * i + 2] += a.z;
+                        v[4 * i + 3] += a.w;
+                    }
+                }
+                const int64_t c0 = (int64_t)nt * p.BN + col;
+                if (valid) {
                     uint16_t* dst = p.out + orow * p.out_cols + c0;
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) {
                         if (c0 + i + 8 <= p.out_cols)
-                            st_global_v4(dst + i,
-                                         pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
-                                         pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
-                                         pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
-                                         pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+                            st_global_v4(dst + i, pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
+                                         pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]));
                     }
                 }
             }
             tc_fence_before();
+            if (contrib) {
+                __threadfence();  // this thread's partials, before the flag
+                named_bar_sync(1, 256);
+                if (leader) st_release_gpu(p.sk_flags + blockIdx.x, p.sk_epoch);
+            } else if (g_last > grp) {
+                named_bar_sync(1, 256);  // every thread has read the partials
+                if (leader)
+                    for (int g2 = grp + 1; g2 <= g_last; ++g2) p.sk_flags[g2 * NT + nt] = 0u;
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.tempty(0));
         }
@@ -1628,17 +1715,44 @@ __global__ void __launch_bounds__(256) dgrad_reduce_kernel(const float* __restri
 // rotated rope channels.
 bool dgrad_pre_shape(int64_t K, int Dn, int Dr) { return Dr == 64 && Dn % 64 == 0 && K % 64 == 0; }
 
-int dgrad_pre_ksplit(int64_t T, int64_t K, int64_t N, int num_sms) {
-    const int64_t tiles = ((T + kDpBM - 1) / kDpBM) * ((K + 255) / 256);
-    return best_ksplit(tiles, (N + kBKD - 1) / kBKD, num_sms);
+// The pre-rotated path's stream-K schedule for this shape: groups of
+// num_n_tiles CTAs (at most the SM count, each group with at least
+// kSkMinIters iterations), and whether a group boundary falls inside a token
+// tile (then the workspace holds one flag and one fp32 partial tile per CTA).
+constexpr long long kSkMinIters = 32;
+struct SkLayout {
+    int groups = 1, grid = 1;
+    long long total = 0;
+    bool split = false;
+    size_t slots_off = 0, bytes = 0;  // flags at 0, slots at slots_off
+};
+
+SkLayout sk_layout(int64_t T, int64_t K, int64_t N, int num_sms) {
+    SkLayout L;
+    const int64_t bn = (K + 63) / 64 * 64;
+    const int64_t BN = bn > 256 ? 256 : bn;
+    const int NT = (int)((K + BN - 1) / BN);
+    const int64_t KT = (N + kBKD - 1) / kBKD;
+    L.total = ((T + kDpBM - 1) / kDpBM) * KT;
+    long long groups = num_sms / NT;
+    const long long by_work = L.total / kSkMinIters;
+    if (groups > by_work) groups = by_work;
+    if (groups < 1) groups = 1;
+    L.groups = (int)groups;
+    L.grid = (int)groups * NT;
+    for (long long g = 1; g < groups && !L.split; ++g) L.split = (L.total * g / groups) % KT != 0;
+    if (L.split) {
+        L.slots_off = ((size_t)L.grid * 4 + 255) / 256 * 256;
+        L.bytes = L.slots_off + (size_t)L.grid * kDpBM * (size_t)BN * sizeof(float);
+    }
+    return L;
 }
 
 size_t dgrad_pre_bytes(int64_t T, int64_t K, int64_t N, int H, int Dr, int num_sms, bool rope_buffer, size_t* rope_off) {
-    const int sp = dgrad_pre_ksplit(T, K, N, num_sms);
-    size_t off = sp > 1 ? (size_t)sp * (size_t)T * (size_t)K * sizeof(float) : 0;
-    off = (off + 255) / 256 * 256;
+    const SkLayout L = sk_layout(T, K, N, num_sms);
+    const size_t off = (L.bytes + 255) / 256 * 256;
     if (rope_off) *rope_off = off;
-    return rope_buffer ? off + (size_t)T * H * Dr * 2 : (sp > 1 ? off : 0);
+    return rope_buffer ? off + (size_t)T * H * Dr * 2 : L.bytes;
 }
 
 bool dgrad_pre_path(const BwdArgs& a, int num_sms) {
@@ -1646,6 +1760,18 @@ bool dgrad_pre_path(const BwdArgs& a, int num_sms) {
     const int64_t N = (int64_t)a.H * (a.Dn + a.Dr);
     const size_t need = dgrad_pre_bytes(a.T, a.K, N, a.H, a.Dr, num_sms, a.rope_out == nullptr, nullptr);
     return need == 0 || (a.workspace != nullptr && a.ws_bytes >= need);
+}
+
+// Flag value of a stream-K launch: new for every launch (never 0, the value
+// the owners leave behind), so a flag left by an earlier launch is never
+// taken for this one's.
+unsigned next_sk_epoch() {
+    static std::atomic<unsigned> counter{0x9E3779B9u};
+    unsigned e;
+    do {
+        e = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    } while (e == 0u);
+    return e;
 }
 
 int launch_dgrad_pre(const BwdArgs& a, BwdParams& p, const DeviceInfo& di, cudaStream_t stream) {
@@ -1664,13 +1790,14 @@ int launch_dgrad_pre(const BwdArgs& a, BwdParams& p, const DeviceInfo& di, cudaS
                                                               a.pos, rope, a.status);
         if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     }
-    // 2. the GEMM over [pass-through | rotated rope], 256-token tiles
+    // 2. the GEMM over [pass-through | rotated rope], 256-token tiles, stream-K over groups
     p.num_m_tiles = (int)((a.T + kDpBM - 1) / kDpBM);
     p.num_tiles = p.num_m_tiles * p.num_n_tiles;
-    p.ksplit = dgrad_pre_ksplit(a.T, a.K, N, di.num_sms);
-    p.kts = (p.k_tiles + p.ksplit - 1) / p.ksplit;
-    p.num_units = p.num_tiles * p.ksplit;
-    p.ws = p.ksplit > 1 ? static_cast<float*>(a.workspace) : nullptr;
+    const SkLayout L = sk_layout(a.T, a.K, N, di.num_sms);
+    p.sk_total = L.total;
+    p.sk_flags = L.split ? static_cast<unsigned*>(a.workspace) : nullptr;
+    p.sk_slots = L.split ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + L.slots_off) : nullptr;
+    p.sk_epoch = next_sk_epoch();
     p.a_bytes = kDpABytes;
     p.stage_bytes = p.a_bytes + (uint32_t)(p.BN / 64) * (uint32_t)kBKD * 128u;
     p.tx_bytes = p.stage_bytes;
@@ -1687,16 +1814,21 @@ int launch_dgrad_pre(const BwdArgs& a, BwdParams& p, const DeviceInfo& di, cudaS
     if (st != MLA_OK) return st;
     st = make_tmap_3d(&tr, rope, 64, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.H * 128, 128, 64, kDpBM, 1);
     if (st != MLA_OK) return st;
-    const int grid = p.num_units < di.num_sms ? p.num_units : di.num_sms;
     if (cudaFuncSetAttribute(dgrad_pre_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MLA_ERR_CUDA;
-    dgrad_pre_kernel<<<grid, kDpThreads, smem, stream>>>(ta, tb, tr, p);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
-    if (p.ksplit == 1) return MLA_OK;
-    const int64_t n = a.T * a.K;
-    int64_t blocks = (n / 8 + 255) / 256;
-    if (blocks > (int64_t)di.num_sms * 8) blocks = (int64_t)di.num_sms * 8;
-    dgrad_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p.ws, p.ksplit, n, static_cast<uint16_t*>(a.dx));
+    // The owners of split tiles wait for other CTAs of the grid: launched
+    // cooperatively, so all CTAs are resident together.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)L.grid);
+    cfg.blockDim = dim3(kDpThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.split ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, dgrad_pre_kernel, ta, tb, tr, p) != cudaSuccess) return MLA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -83,6 +83,10 @@ struct FwdParams {
     const uint16_t* bias;
     const float* cos_tab;
     const float* sin_tab;
+    // the packed table (mla_rope_table_pack): float4 (cos_i, sin_i,
+    // cos_{i+Dr/2}, sin_{i+Dr/2}) of position p at tab4[i * cs_rows + p];
+    // used instead of cos_tab/sin_tab when not null
+    const float4* tab4;
     const int32_t* pos;
     long long cs_rows, cs_width;
     uint8_t* q_out;
@@ -251,7 +255,16 @@ __device__ __forceinline__ void load_table8(const float* src, bool vec, float (&
     }
 }
 
-template <bool MXOUT, int DR>
+// The rotate-half pair (a, b) = (y[i], y[i + Dr/2]) of position p, with one
+// rounding order for both table layouts: the second product is rounded,
+// then the first is added by one fused multiply-add.
+__device__ __forceinline__ void rot_pair_fwd(float& a, float& b, float ci, float si, float cj, float sj) {
+    const float a0 = a, b0 = b;
+    a = __fmaf_rn(a0, ci, -__fmul_rn(b0, si));  // a cos_i - b sin_i
+    b = __fmaf_rn(b0, cj, __fmul_rn(a0, sj));   // b cos_{i+h} + a sin_{i+h}
+}
+
+template <bool MXOUT, int DR, bool PACKED>
 __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
                                           uint32_t taddr, int col, bool valid, int64_t t, int64_t n, int h,
                                           int prow) {
@@ -265,22 +278,36 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
 #pragma unroll
     for (int i = 0; i < DR; ++i) y[i] = __uint_as_float(r[i / 16][i % 16]);
     if (c.bias) add_bias(y, DR, c.bias + col);
-    const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
-    const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
-    const bool vec = p.cs_vec != 0;
-    // rotate in place, 8 pairs at a time: (a, c) = (y[i], y[i + HH])
+    if constexpr (PACKED) {
+        // packed table: one 16-byte load per pair; the lanes of a warp (tokens
+        // with consecutive positions) read consecutive 16-byte entries
+        const float4* tp = p.tab4 + prow;
+        const int64_t stride = p.cs_rows;
 #pragma unroll
-    for (int q = 0; q < HH; q += 8) {
-        float ci[8], si[8], cj[8], sj[8];
-        load_table8(cs + q, vec, ci);
-        load_table8(sn + q, vec, si);
-        load_table8(cs + q + HH, vec, cj);
-        load_table8(sn + q + HH, vec, sj);
+        for (int q = 0; q < HH; q += 4) {
+            float4 tv[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float a = y[q + e], b = y[q + e + HH];
-            y[q + e] = a * ci[e] - b * si[e];
-            y[q + e + HH] = b * cj[e] + a * sj[e];
+            for (int e = 0; e < 4; ++e) {
+                tv[e] = __ldg(tp);
+                tp += stride;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) rot_pair_fwd(y[q + e], y[q + e + HH], tv[e].x, tv[e].y, tv[e].z, tv[e].w);
+        }
+    } else {
+        const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
+        const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
+        const bool vec = p.cs_vec != 0;
+        // rotate in place, 8 pairs at a time: (a, c) = (y[i], y[i + HH])
+#pragma unroll
+        for (int q = 0; q < HH; q += 8) {
+            float ci[8], si[8], cj[8], sj[8];
+            load_table8(cs + q, vec, ci);
+            load_table8(sn + q, vec, si);
+            load_table8(cs + q + HH, vec, cj);
+            load_table8(sn + q + HH, vec, sj);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rot_pair_fwd(y[q + e], y[q + e + HH], ci[e], si[e], cj[e], sj[e]);
         }
     }
     emit_unit<MXOUT, DR>(p, tmC, c, y, valid, t, n, h, p.Dn);
@@ -317,7 +344,7 @@ __device__ __forceinline__ void q_tile(const FwdParams& p, int g, int& mt, int& 
 }
 
 // ------------------------------------------------------------------- kernel
-template <bool MXW, bool MXOUT, int DR, bool KV = false>
+template <bool MXW, bool MXOUT, int DR, bool KV = false, bool PACKED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -672,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool nope = c < p.Dn;
                 if (M2 || p.split_half || (unit++ & 1) == half) {
                     if (nope) nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
-                    else if constexpr (DR > 0) rope_unit<MXOUT, DR>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
+                    else if constexpr (DR > 0) rope_unit<MXOUT, DR, PACKED>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
                 }
                 col += nope ? 32 : DR;
             }
@@ -696,10 +723,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool MXW, bool MXOUT, int DR>
+template <bool MXW, bool MXOUT, int DR, bool PACKED = false>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                    const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
-    auto kern = fwd_kernel<MXW, MXOUT, DR>;
+    auto kern = fwd_kernel<MXW, MXOUT, DR, false, PACKED>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return MLA_ERR_CUDA;
@@ -707,15 +734,23 @@ int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+template <bool MXW, bool MXOUT, bool PACKED>
+int launch_dr_t(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
+    switch (Dr) {
+        case 16: return launch_variant<MXW, MXOUT, 16, PACKED>(ta, tb, tc, p, grid, smem, stream);
+        case 32: return launch_variant<MXW, MXOUT, 32, PACKED>(ta, tb, tc, p, grid, smem, stream);
+        case 64: return launch_variant<MXW, MXOUT, 64, PACKED>(ta, tb, tc, p, grid, smem, stream);
+        default: return MLA_ERR_UNSUPPORTED;
+    }
+}
+
+// the table layout is a compile-time choice: one table path per kernel
 template <bool MXW, bool MXOUT>
 int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
               const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
-    switch (Dr) {
-        case 16: return launch_variant<MXW, MXOUT, 16>(ta, tb, tc, p, grid, smem, stream);
-        case 32: return launch_variant<MXW, MXOUT, 32>(ta, tb, tc, p, grid, smem, stream);
-        case 64: return launch_variant<MXW, MXOUT, 64>(ta, tb, tc, p, grid, smem, stream);
-        default: return MLA_ERR_UNSUPPORTED;
-    }
+    return p.tab4 ? launch_dr_t<MXW, MXOUT, true>(Dr, ta, tb, tc, p, grid, smem, stream)
+                  : launch_dr_t<MXW, MXOUT, false>(Dr, ta, tb, tc, p, grid, smem, stream);
 }
 
 }  // namespace
@@ -790,6 +825,32 @@ int launch_kv_fwd(const KvArgs& a, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+namespace {
+// out[i * rows + p] = (cos[p, i], sin[p, i], cos[p, i + h], sin[p, i + h]):
+// a re-layout of the table's first 2h columns, no arithmetic.
+__global__ void __launch_bounds__(256) rope_table_pack_kernel(const float* __restrict__ cos_tab,
+                                                              const float* __restrict__ sin_tab, long long rows,
+                                                              long long width, int h, float4* __restrict__ out) {
+    const long long n = rows * h;
+    for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += (long long)gridDim.x * blockDim.x) {
+        const long long i = k / rows, pr = k - i * rows;
+        const long long o = pr * width + i;
+        out[k] = make_float4(__ldg(cos_tab + o), __ldg(sin_tab + o), __ldg(cos_tab + o + h), __ldg(sin_tab + o + h));
+    }
+}
+}  // namespace
+
+int launch_rope_table_pack(int64_t rows, int64_t width, int Dr, const float* cos_tab, const float* sin_tab,
+                           void* packed, cudaStream_t stream) {
+    const long long n = rows * (Dr / 2);
+    if (n == 0) return MLA_OK;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    rope_table_pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(cos_tab, sin_tab, rows, width, Dr / 2,
+                                                                 static_cast<float4*>(packed));
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 int fwd_tile_n(int64_t N, int D, int Dn, int Dr, int max_bn, int step) {
     for (int bn = max_bn / step * step; bn >= step; bn -= step) {
         if (N % bn) continue;
@@ -844,6 +905,7 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.bias = static_cast<const uint16_t*>(a.bias);
     p.cos_tab = a.cos_tab;
     p.sin_tab = a.sin_tab;
+    p.tab4 = static_cast<const float4*>(a.rope_packed);
     p.pos = a.pos;
     p.cs_rows = a.Dr == 0 ? (long long)INT64_MAX : a.cs_rows;  // plain GEMM: no table rows read
     p.cs_width = a.cs_width;

@@ -76,6 +76,7 @@ struct FwdArgs {
     const void* bias;
     const float* cos_tab;
     const float* sin_tab;
+    const void* rope_packed = nullptr;  // mla_rope_table_pack's layout, used instead of cos/sin when set
     const int32_t* pos;
     void* q_out;
     uint8_t* q_scales;
@@ -94,6 +95,9 @@ struct FwdArgs {
     int sf_tiled = 0, sf_group = 0;
 };
 int launch_fwd(const FwdArgs& a, cudaStream_t stream);
+// The packed rotary table (see mla_rope_table_pack).
+int launch_rope_table_pack(int64_t rows, int64_t width, int Dr, const float* cos_tab, const float* sin_tab,
+                           void* packed, cudaStream_t stream);
 
 struct KvArgs {
     int64_t T, K;
@@ -151,6 +155,10 @@ size_t dgrad_pre_shape_bytes(int64_t T, int64_t K, int H, int Dn, int Dr, int nu
 // paths' needs; the path is then chosen by the workspace given).
 size_t dgrad_min_workspace_bytes(int64_t T, int64_t K, int H, int Dn, int Dr, int num_sms, bool have_rope_out);
 int launch_wgrad(const BwdArgs& a, cudaStream_t stream);
+// The checks of mla_q_uproj_bwd_dgrad that do not involve the workspace.
+int dgrad_check_args(const mla_q_shape* shape, const void* dq, const void* W, const float* cos_tab,
+                     const float* sin_tab, const int32_t* pos, const void* dx, const void* dq_pre_rope,
+                     const int* dev_status);
 
 // MXFP8 backward (see mla_q_uproj_bwd_mxfp8): workspace carve-up and launch.
 struct Mxfp8BwdLayout {

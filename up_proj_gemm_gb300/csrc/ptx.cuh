@@ -323,6 +323,49 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// bar.sync on a named barrier that also ANDs a predicate over the
+// participating threads: every thread learns whether all of them passed true.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// GPU-scope release store / acquire load of a 32-bit flag in global memory.
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (bounded, like mbar_wait) until *flag == value, written by another CTA
+// of the same grid. Returns false on the time limit or when *abort is set;
+// on the time limit it also sets *abort.
+__device__ __forceinline__ bool wait_flag_gpu(const unsigned* flag, unsigned value, volatile int* abort,
+                                              uint64_t limit_ns = MLAQ_WAIT_NS) {
+    if (ld_acquire_gpu(flag) == value) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(100);
+        if (ld_acquire_gpu(flag) == value) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ void record_status(int* status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
