@@ -240,8 +240,16 @@ def make_step(w, inp, status, dev):
     cs_rows, cs_width = inp["cos"].shape
     need = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, cs_rows, cs_width, 1)
     ws = torch.empty((need,), dtype=torch.uint8, device=dev) if need else None
+    # the rotary table is a model constant: packed once into the layout the
+    # forward reads fastest (a copy; the forward's bytes are the same)
+    packed = mlaq.rope_table_pack(inp["cos"], inp["sin"], w.Dr)
 
     def k_fwd():
+        mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"],
+                 pos=inp["pos"], out_mode="mxfp8", q_out=o["q"], q_scales=o["qs"], status=status,
+                 rope_packed=packed)
+
+    def k_fwd_plain():  # the same forward reading the plain cos/sin tables
         mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"],
                  pos=inp["pos"], out_mode="mxfp8", q_out=o["q"], q_scales=o["qs"], status=status)
 
@@ -263,7 +271,8 @@ def make_step(w, inp, status, dev):
     # reduction when its channel reduction is split); wgrad
     pre = w.Dr == 64 and w.Dn % 64 == 0 and w.K % 64 == 0
     kernels = 1 + (2 if pre else 1 + (1 if need > 0 else 0)) + 1
-    calls = {"fwd": k_fwd, "dgrad": k_dgrad, "wgrad": k_wgrad, "wgrad_self": k_wgrad_self}
+    calls = {"fwd": k_fwd, "fwd_plain": k_fwd_plain, "dgrad": k_dgrad, "wgrad": k_wgrad,
+             "wgrad_self": k_wgrad_self}
     return calls, o, kernels
 
 
@@ -316,8 +325,9 @@ def workload_config(w, world):
     return {"workload": f"{w.name}: T={w.T} fwd(bf16 W{', +bias' if w.bias else ''}, RoPE, MXFP8 q) + "
                         f"dgrad + wgrad{' + db' if w.bias else ''}",
             "T": w.T, "K": w.K, "H": w.H, "Dn": w.Dn, "Dr": w.Dr, "N": w.N,
-            "pos": f"t mod {w.seq_len}" if w.seq_len else "t", "rope_table": table, "bias": w.bias,
+            "pos": f"t mod {w.seq_len}" if w.seq_len else "t", "bias": w.bias,
             "rope_handoff": "dgrad stores the rotated rope channels [T, H, Dr] bf16; wgrad reads them",
+            "rope_table": table + "; packed once (mla_rope_table_pack) outside the timed steps",
             "l2": "flushed (256 MiB write) between steps, outside the timed events; step inputs > L2",
             "parallelism": f"replicas x{world} (no data exchange)"}
 
@@ -452,6 +462,7 @@ def run_e2e(w, inp, status, flop_step, world, steps, warmup, dev):
         })
     need = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, inp["cos"].shape[0], inp["cos"].shape[1], 1)
     ws = torch.empty((need,), dtype=torch.uint8, device=dev) if need else None
+    packed = mlaq.rope_table_pack(inp["cos"], inp["sin"], w.Dr)  # a model constant, packed once
     s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=False)
     in_done, cmp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -468,7 +479,7 @@ def run_e2e(w, inp, status, flop_step, world, steps, warmup, dev):
             s_cmp.wait_event(in_done[j])
             s_cmp.wait_event(out_done[j])  # step i-2's outputs in set j have been read back
             mlaq.fwd(b["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, bias=inp["b"], pos=inp["pos"],
-                     out_mode="mxfp8", q_out=b["q"], q_scales=b["qs"], status=status)
+                     out_mode="mxfp8", q_out=b["q"], q_scales=b["qs"], status=status, rope_packed=packed)
             mlaq.bwd_dgrad(b["dq"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
                            dx=b["dx"], status=status, workspace=ws, dq_pre_rope=b["rope"])
             mlaq.bwd_wgrad(b["dq"], b["x"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
@@ -519,7 +530,7 @@ def run_only(args, flush, stream, status, dev):
     kernels["dgrad"]()  # fills the rope buffer wgrad reads
     if args.only in kernels:
         fn = kernels[args.only]
-        flop = w.fwd_flop() if args.only == "fwd" else w.bwd_flop() / 2
+        flop = w.fwd_flop() if args.only in ("fwd", "fwd_plain") else w.bwd_flop() / 2
     elif args.only == "fwd_mxfp8w":
         xq, xs = mlaq.mxfp8_quantize_rows(inp["x"])
         Wq, Ws = mlaq.mxfp8_quantize_rows(inp["W"])
@@ -639,21 +650,33 @@ def run_parts(dev, stream, flush, pk, pk_src):
     G = mlaq.w_scale_group(w.T, w.K, w.H, w.Dn, w.Dr, inp["cos"].shape[0], inp["cos"].shape[1])
     _, xst = mlaq.mxfp8_quantize_rows(inp["x"], group=128)
     _, Wst = mlaq.mxfp8_quantize_rows(inp["W"], group=G)
+    packed = mlaq.rope_table_pack(inp["cos"], inp["sin"], w.Dr)  # a model constant, packed once
+    ms_t = time_loop(lambda: mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
+                                      weight_mode="mxfp8_tiled", out_mode="mxfp8", x_scales=xst, w_scales=Wst,
+                                      q_out=qc, q_scales=qs, status=st), PART_ITERS, flush, stream,
+                     warmup=PART_WARMUP)
     ms = time_loop(lambda: mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"],
                                     weight_mode="mxfp8_tiled", out_mode="mxfp8", x_scales=xst, w_scales=Wst,
-                                    q_out=qc, q_scales=qs, status=st), PART_ITERS, flush, stream, warmup=PART_WARMUP)
+                                    q_out=qc, q_scales=qs, status=st, rope_packed=packed), PART_ITERS, flush,
+                   stream, warmup=PART_WARMUP)
     tf = w.fwd_flop() / (ms * 1e-3) / 1e12
     parts["fwd_mxfp8w_mxfp8out_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                           "frac_fp8_peak": round(tf / fp8_peak, 4),
                                           "peak": f"{pk_src} bf16 burst x{FP8_OVER_BF16:g} (nominal fp8/bf16)",
                                           "scales": "in the GEMM's tiled order (mxfp8_quantize_rows_tiled)",
-                                          "ms_row_major_scales": round(ms_g, 4)}
+                                          "rope_table": "packed (mla_rope_table_pack)",
+                                          "ms_plain_table": round(ms_t, 4),
+                                          "ms_row_major_scales_plain_table": round(ms_g, 4)}
+    ms_p = time_loop(lambda: mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
+                                      pos=inp["pos"], out_mode="mxfp8", q_out=qc, q_scales=qs, status=st),
+                     PART_ITERS, flush, stream, warmup=PART_WARMUP)
     ms = time_loop(lambda: mlaq.fwd(inp["x"], inp["W"], inp["cos"], inp["sin"], w.H, w.Dn, w.Dr,
-                                    pos=inp["pos"], out_mode="mxfp8", q_out=qc, q_scales=qs, status=st),
-                   PART_ITERS, flush, stream, warmup=PART_WARMUP)
+                                    pos=inp["pos"], out_mode="mxfp8", q_out=qc, q_scales=qs, status=st,
+                                    rope_packed=packed), PART_ITERS, flush, stream, warmup=PART_WARMUP)
     tf = w.fwd_flop() / (ms * 1e-3) / 1e12
     parts["fwd_bf16w_mxfp8out_T4096_alone"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
-                                               "frac_bf16_peak": round(tf / bf16_peak, 4)}
+                                               "frac_bf16_peak": round(tf / bf16_peak, 4),
+                                               "rope_table": "packed", "ms_plain_table": round(ms_p, 4)}
     # the same forward writing its scales per head in the block-scaled GEMM's tiled order
     qsw = torch.empty((w.H, int(mlaq.lib().mxfp8_swizzled_scale_bytes(w.T, (w.D + 31) // 32))),
                       dtype=torch.uint8, device=dev)
@@ -663,7 +686,7 @@ def run_parts(dev, stream, flush, pk, pk_src):
     tf = w.fwd_flop() / (ms * 1e-3) / 1e12
     parts["fwd_bf16w_mxfp8out_swizzled_scales_T4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                                          "frac_bf16_peak": round(tf / bf16_peak, 4)}
-    del inp, xq, xs, Wq, Ws, qc, qs, qsw, Wst, xst
+    del inp, xq, xs, Wq, Ws, qc, qs, qsw, Wst, xst, packed
 
     # backward at T = 2 x 4096, bias on
     w = synth.workload("dsv3_bwd")
@@ -827,7 +850,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--only", choices=("fwd", "dgrad", "wgrad", "wgrad_self", "fwd_mxfp8w", "quant", "quant_cols",
+    ap.add_argument("--only", choices=("fwd", "fwd_plain", "dgrad", "wgrad", "wgrad_self", "fwd_mxfp8w", "quant",
+                                      "quant_cols",
                                           "bwd_mxfp8", "kv"),
                     help="time one kernel alone (profiling)")
     ap.add_argument("--workload", choices=("tiny", "dsv3_fwd_bf16w", "dsv3_fwd_mxfp8w", "dsv3_bwd", HEADLINE),

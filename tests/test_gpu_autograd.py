@@ -65,3 +65,32 @@ def test_autograd_partial_gradients(cuda_device):
     q = q_up_proj(d["x"], W, d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"])
     q.backward(d["dq"])
     assert helpers.frob_rel(W.grad, g["dW"]) <= TOL
+
+
+@pytest.mark.parametrize("out_mode", ["mxfp8", "mxfp8_bhsd", "mxfp8_bhsd_swizzled"])
+def test_mxfp8_query_face(cuda_device, out_mode):
+    """q_up_proj_mxfp8: the MXFP8 query is the forward's own output for that
+    mode (bytes equal to the plain call), and query.backward(dq) with a bf16
+    dq gives the gradients of the bf16 face (which the test above checks
+    against the oracle), bit for bit."""
+    from up_proj_gemm_gb300 import fwd
+    from up_proj_gemm_gb300.autograd import q_up_proj_mxfp8
+    w, inp, d = _case("dsv3_bwd", dict(T=260, H=4, seq_len=None), cuda_device, 23)
+    xa = d["x"].clone().requires_grad_(True)
+    Wa = d["W"].clone().requires_grad_(True)
+    ba = d["b"].clone().requires_grad_(True)
+    qm = q_up_proj_mxfp8(xa, Wa, d["cos"], d["sin"], w.H, w.Dn, w.Dr, bias=ba, pos=d["pos"], out_mode=out_mode)
+    codes, scales = fwd(d["x"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, bias=d["b"], pos=d["pos"],
+                        out_mode=out_mode)
+    assert torch.equal(qm.codes, codes) and torch.equal(qm.scales, scales)
+    assert not qm.codes.requires_grad and qm.anchor.requires_grad
+    qm.backward(d["dq"])
+    xb = d["x"].clone().requires_grad_(True)
+    Wb = d["W"].clone().requires_grad_(True)
+    bb = d["b"].clone().requires_grad_(True)
+    q = q_up_proj(xb, Wb, d["cos"], d["sin"], w.H, w.Dn, w.Dr, bias=bb, pos=d["pos"])
+    q.backward(d["dq"])
+    torch.cuda.synchronize()
+    assert torch.equal(xa.grad, xb.grad) and torch.equal(Wa.grad, Wb.grad) and torch.equal(ba.grad, bb.grad)
+    with pytest.raises(ValueError):
+        qm.backward(d["dq"].float())
