@@ -542,9 +542,12 @@ def run_only(args, flush, stream, status, dev):
         _, xst = mlaq.mxfp8_quantize_rows(inp["x"], group=128)
         _, Wst = mlaq.mxfp8_quantize_rows(inp["W"], group=G)
 
+        packed = mlaq.rope_table_pack(inp["cos"], inp["sin"], w.Dr)
+
         def fn():
             mlaq.fwd(xq, Wq, inp["cos"], inp["sin"], w.H, w.Dn, w.Dr, pos=inp["pos"], weight_mode="mxfp8_tiled",
-                     out_mode="mxfp8", x_scales=xst, w_scales=Wst, q_out=qc, q_scales=qs, status=status)
+                     out_mode="mxfp8", x_scales=xst, w_scales=Wst, q_out=qc, q_scales=qs, status=status,
+                     rope_packed=packed)
         flop = w.fwd_flop()
     elif args.only == "bwd_mxfp8":
         dx = torch.empty((w.T, w.K), dtype=torch.bfloat16, device=dev)

@@ -1196,6 +1196,9 @@ __global__ void __launch_bounds__(kDpThreads, 1)
             int s = 0;
             uint32_t ph = 0, issued_mask = 0, issued_par = 0;
             bool ok = true;
+            // dq (and its rotated rope channels) stream through L2 once per
+            // group; W is re-read by every group: keep W, let dq go first
+            const uint64_t stream_pol = l2_evict_first_policy(), keep_pol = l2_evict_last_policy();
             for (long long it = beg; ok && it < end;) {
                 int mt, k0, k1;
                 sk_segment(p, it, end, mt, k0, k1);
@@ -1206,9 +1209,9 @@ __global__ void __launch_bounds__(kDpThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(sm.full(s), p.tx_bytes);
-                    if (c0 < p.Dn) tma_load_2d(sm.a(s, p), &tmA, kt * BK, mt * kDpBM, sm.full(s));
-                    else tma_load_3d(sm.a(s, p), &tmR, 0, mt * kDpBM, head, sm.full(s));
-                    tma_load_3d(sm.b(s, p), &tmB, 0, kt * BK, nt * nb_chunks, sm.full(s));
+                    if (c0 < p.Dn) tma_load_2d_hint(sm.a(s, p), &tmA, kt * BK, mt * kDpBM, sm.full(s), stream_pol);
+                    else tma_load_3d_hint(sm.a(s, p), &tmR, 0, mt * kDpBM, head, sm.full(s), stream_pol);
+                    tma_load_3d_hint(sm.b(s, p), &tmB, 0, kt * BK, nt * nb_chunks, sm.full(s), keep_pol);
                     issued_mask |= 1u << s;
                     issued_par = (issued_par & ~(1u << s)) | (ph << s);
                     if (++s == p.stages) {

@@ -218,9 +218,10 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
+        const uint64_t pol = l2_evict_first_policy();  // q is written once: do not let it push x, W out of L2
 #pragma unroll
         for (int pc = 0; pc < PIECES; ++pc)
-            tma_store_2d(tmC, (int32_t)(n + 16 * pc), c.t0, slot_addr(p, c, first + pc));
+            tma_store_2d_hint(tmC, (int32_t)(n + 16 * pc), c.t0, slot_addr(p, c, first + pc), pol);
         bulk_commit_group();
     }
     c.cursor = first + PIECES;
@@ -313,20 +314,26 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
     emit_unit<MXOUT, DR>(p, tmC, c, y, valid, t, n, h, p.Dn);
 }
 
-// Tile order: the query side strides tiles over the CTAs (token tile fastest,
-// so CTAs running together share weight tiles in L2); the KV side gives each
-// CTA a contiguous run, head fastest, so its tiles share their tokens.
+// Tile order: tiles are strided over the CTAs, so the CTAs running together
+// take consecutive tiles. The query side numbers them token tile fastest,
+// the KV side (kv_tile) the same: the tiles of a wave share a few heads'
+// rows of W, which stay in L2 while the outputs stream past.
 template <bool KV>
-__device__ __forceinline__ int tile_first(const FwdParams& p) {
-    return KV ? (int)blockIdx.x * p.tiles_per_cta : (int)blockIdx.x;
+__device__ __forceinline__ int tile_first(const FwdParams&) {
+    return (int)blockIdx.x;
 }
 template <bool KV>
 __device__ __forceinline__ int tile_end(const FwdParams& p) {
-    return KV ? min(p.num_tiles, ((int)blockIdx.x + 1) * p.tiles_per_cta) : p.num_tiles;
+    return p.num_tiles;
 }
 template <bool KV>
 __device__ __forceinline__ int tile_next(int tile) {
-    return KV ? tile + 1 : tile + (int)gridDim.x;
+    return tile + (int)gridDim.x;
+}
+// KV tile -> (token tile, head)
+__device__ __forceinline__ void kv_tile(const FwdParams& p, int tile, int& mt, int& h) {
+    h = tile / p.num_m_tiles;
+    mt = tile - h * p.num_m_tiles;
 }
 // (token tile, channel tile) of query-side tile index g. The rope forward
 // runs the token tile fastest (CTAs running together share W tiles); the
@@ -401,11 +408,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         uint32_t issued_mask = 0, issued_par = 0;
         bool ok = true;
+        // x's row tiles are re-read for every channel tile (keep them in L2),
+        // except in the plain GEMM, whose large A operand streams through once
+        const uint64_t a_pol = (DR == 0 && !KV) ? l2_evict_first_policy() : l2_evict_last_policy();
         for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile)) {
             int mt, nt;
             if (KV) {
-                mt = tile / p.H;
-                nt = tile % p.H;
+                kv_tile(p, tile, mt, nt);
             } else {
                 q_tile<DR>(p, tile, mt, nt);
             }
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(sm.full(s), tx);
                     // x / W tiles: inner coordinate is the K element index
                     const int kc = kt * (MXW ? 128 : 64);
-                    tma_load_2d(sm.a(s, p), &tmA, kc, mt * BM, sm.full(s));
+                    tma_load_2d_hint(sm.a(s, p), &tmA, kc, mt * BM, sm.full(s), a_pol);
                     tma_load_2d(sm.b(s, p), &tmB, kc, nt * p.BN, sm.full(s));
                     if (MXW && p.sf_tiled) {
                         bulk_load(sm.sfa(s), p.x_scales + ((int64_t)(M2 ? 2 * mt : mt) * p.k_tiles + kt) * 512, 512u,
@@ -532,19 +541,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if constexpr (KV) {
         // ------------------------------------------------- KV-side epilogue
-        // CTAs take contiguous runs of tiles, head fastest, so consecutive
-        // tiles share their 128 tokens. A tile = 128 tokens x one head's
-        // Dn + Dv columns; the quadrant's two warps take alternate 32-column
-        // units (k_nope -> o_key, v -> o_value), staged in a 2-slot ring and
-        // written by TMA. The shared key's rope part is computed once per token
-        // block, each warp one half of its channels (half 0: a cos_i - c sin_i,
-        // half 1: c cos_{i+h} + a sin_{i+h}), kept in a shared-memory slab and
-        // TMA-stored into every head's key.
+        // A tile = 128 tokens x one head's Dn + Dv columns; the quadrant's two
+        // warps take alternate 32-column units (k_nope -> o_key, v -> o_value),
+        // staged in a 2-slot ring and written by TMA. The shared key's rope
+        // part was rotated once per token by kv_rope_pre_kernel into head 0's
+        // rope slot; each tile of another head copies it from there (through
+        // a shared-memory slab, each warp one half of the channels when
+        // DR = 64) into its own.
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int ew = warp - 2;
         const int half = ew >> 2;
-        constexpr int HH = DR / 2;
         const int Dk = p.Dn + DR;
         const uint32_t ring = sm.out + (uint32_t)(ew * 3) * 2048u;  // slots 0, 1; rope slab 2
         const uint32_t slab = ring + 2u * 2048u;
@@ -553,62 +560,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = tile_first<KV>(p); tile < tile_end<KV>(p); tile = tile_next<KV>(tile), ++local) {
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
-            const int mt = tile / p.H;
-            const int h = tile % p.H;
+            int mt, h;
+            kv_tile(p, tile, mt, h);
             const int64_t t = (int64_t)mt * kBM + row;
             const bool valid = t < p.T;
             const int t0 = mt * kBM + quad * 32;
-            if (mt != cur_mt && (DR == 64 || half == 0)) {
-                // this warp's rope channels for the new token block: [32 half, +32)
+            if (h != 0 && mt != cur_mt && (DR == 64 || half == 0)) {
+                // this warp's rope channels of the token block: [32 half, +32)
                 // when DR = 64, else all of them in warp 0 (DR <= 32)
                 if (lane == 0) bulk_wait_group_read<0>();  // stores still reading the slab
                 __syncwarp();
-                constexpr int NO = DR == 64 ? 32 : DR;  // output channels this warp writes
-                float out[NO];
-#pragma unroll
-                for (int i = 0; i < NO; ++i) out[i] = 0.f;
-                int prow = -1;
-                if (valid) {
-                    const int64_t pp = p.pos ? (int64_t)__ldg(p.pos + t) : t;
-                    if (pp < 0 || pp >= p.cs_rows) record_status(p.status, MLA_ERR_POS_RANGE);
-                    else prow = (int)pp;
-                }
-                if (prow >= 0) {
-                    const float* cs = p.cos_tab + (int64_t)prow * p.cs_width;
-                    const float* sn = p.sin_tab + (int64_t)prow * p.cs_width;
-                    const uint16_t* kp = p.k_pe + t * DR;
-                    const int o0 = DR == 64 ? 32 * half : 0;  // first output channel
-#pragma unroll
-                    for (int q = 0; q < NO; q += 8) {
-                        const int oc = o0 + q;                 // output channel
-                        const int i = oc < HH ? oc : oc - HH;  // its pair
-                        const uint4 ka = __ldg(reinterpret_cast<const uint4*>(kp + i));
-                        const uint4 kc = __ldg(reinterpret_cast<const uint4*>(kp + i + HH));
-                        float cw[8], sw[8];
-                        load_table8(cs + oc, p.cs_vec != 0, cw);
-                        load_table8(sn + oc, p.cs_vec != 0, sw);
-                        const uint32_t aw[4] = {ka.x, ka.y, ka.z, ka.w}, ccw[4] = {kc.x, kc.y, kc.z, kc.w};
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const float a = e ? bf16hi_to_f32(aw[w]) : bf16lo_to_f32(aw[w]);
-                                const float c = e ? bf16hi_to_f32(ccw[w]) : bf16lo_to_f32(ccw[w]);
-                                const int k = 2 * w + e;
-                                out[q + k] = oc < HH ? a * cw[k] - c * sw[k] : c * cw[k] + a * sw[k];
-                            }
-                        }
-                    }
-                }
+                constexpr int NO = DR == 64 ? 32 : DR;  // channels this warp copies
+                const int o0 = DR == 64 ? 32 * half : 0;
                 const uint32_t ra = slab + (uint32_t)lane * (uint32_t)(NO * 2);
+                const uint16_t* src = p.o_key + t * ((int64_t)p.H * Dk) + p.Dn + o0;  // head 0
 #pragma unroll
-                for (int q = 0; q < NO; q += 8)
-                    sts_v4(ra + (uint32_t)(2 * q), pack_bf16x2(out[q], out[q + 1]), pack_bf16x2(out[q + 2], out[q + 3]),
-                           pack_bf16x2(out[q + 4], out[q + 5]), pack_bf16x2(out[q + 6], out[q + 7]));
+                for (int q = 0; q < NO; q += 8) {
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (valid) v = __ldcg(reinterpret_cast<const uint4*>(src + q));
+                    sts_v4(ra + (uint32_t)(2 * q), v.x, v.y, v.z, v.w);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
+                cur_mt = mt;
             }
-            cur_mt = mt;
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
             tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)b * kAccStride;
@@ -638,12 +613,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.tempty(b));
-            // the key's rope part of this head (32-channel slabs by TMA; 16 by plain stores)
-            if (DR >= 32 && lane == 0 && (DR == 64 || half == 0)) {
+            // the key's rope part of this head (32-channel slabs by TMA; 16 by plain
+            // stores); head 0's holds it already
+            if (h != 0 && DR >= 32 && lane == 0 && (DR == 64 || half == 0)) {
                 tma_store_2d(&tmC, h * Dk + p.Dn + (DR == 64 ? 32 * half : 0), t0, slab);
                 bulk_commit_group();
             }
-            if (DR == 16 && half == 0 && valid) {
+            if (h != 0 && DR == 16 && half == 0 && valid) {
                 const uint4 v0 = lds_v4(slab + (uint32_t)lane * 32u);
                 const uint4 v1 = lds_v4(slab + (uint32_t)lane * 32u + 16u);
                 uint16_t* dst = p.o_key + (t * p.H + h) * Dk + p.Dn;
@@ -755,6 +731,61 @@ int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 
 }  // namespace
 
+namespace {
+// The shared k_pe rotated once per token (rotate-half pairs (i, i + Dr/2),
+// the query's rule, fp32, rounded to bf16 once) into head 0's rope slot of
+// o_key; the KV kernel copies it into the other heads. A thread takes 8
+// pairs of one token. Positions outside the table: zeros, and the status.
+__global__ void __launch_bounds__(256) kv_rope_pre_kernel(const uint16_t* __restrict__ k_pe, int64_t T, int Dr,
+                                                          const float* __restrict__ cos_tab,
+                                                          const float* __restrict__ sin_tab, long long cs_rows,
+                                                          long long cs_width, const int32_t* __restrict__ pos,
+                                                          uint16_t* __restrict__ o_key, int64_t key_pitch, int Dn,
+                                                          int* status) {
+    const int HH = Dr / 2;
+    const int groups = (HH + 7) / 8;
+    const int64_t items = T * groups;
+    for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < items;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = it / groups;
+        const int i0 = (int)(it - t * groups) * 8;
+        const int n = HH - i0 < 8 ? HH - i0 : 8;  // Dr = 16: one group of 8
+        const int64_t pp = pos ? (int64_t)__ldg(pos + t) : t;
+        const bool ok = pp >= 0 && pp < cs_rows;
+        if (!ok) record_status(status, MLA_ERR_POS_RANGE);
+        uint32_t oa[4] = {0u, 0u, 0u, 0u}, oc[4] = {0u, 0u, 0u, 0u};
+        if (ok) {
+            const uint16_t* kp = k_pe + t * Dr;
+            const float* cr = cos_tab + pp * cs_width;
+            const float* sr = sin_tab + pp * cs_width;
+            float ra[8], rc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (e < n) {
+                    const float a = __uint_as_float((uint32_t)__ldg(kp + i0 + e) << 16);
+                    const float c = __uint_as_float((uint32_t)__ldg(kp + i0 + e + HH) << 16);
+                    ra[e] = a;
+                    rc[e] = c;
+                    rot_pair_fwd(ra[e], rc[e], __ldg(cr + i0 + e), __ldg(sr + i0 + e), __ldg(cr + i0 + e + HH),
+                                 __ldg(sr + i0 + e + HH));
+                } else {
+                    ra[e] = rc[e] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                oa[w] = pack_bf16x2(ra[2 * w], ra[2 * w + 1]);
+                oc[w] = pack_bf16x2(rc[2 * w], rc[2 * w + 1]);
+            }
+        }
+        uint16_t* dst = o_key + t * key_pitch + Dn;
+        // 8 channels at i0 and at i0 + HH (16-byte aligned: Dn, HH and i0 are multiples of 8)
+        st_global_v4(dst + i0, oa[0], oa[1], oa[2], oa[3]);
+        st_global_v4(dst + i0 + HH, oc[0], oc[1], oc[2], oc[3]);
+    }
+}
+}  // namespace
+
 int launch_kv_fwd(const KvArgs& a, cudaStream_t stream) {
     DeviceInfo di;
     int st = current_device_info(&di);
@@ -807,7 +838,18 @@ int launch_kv_fwd(const KvArgs& a, cudaStream_t stream) {
     st = make_tmap_2d(&td, a.o_value, 1, (uint64_t)a.H * a.Dv, (uint64_t)a.T, (uint64_t)a.H * a.Dv * 2, 32, 32, false);
     if (st != MLA_OK) return st;
     const int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
-    p.tiles_per_cta = (p.num_tiles + grid - 1) / grid;
+    // 1. the shared k_pe, rotated once into head 0's rope slot
+    {
+        const int64_t items = a.T * ((a.Dr / 2 + 7) / 8);
+        int64_t blocks = (items + 255) / 256;
+        if (blocks > (int64_t)di.num_sms * 8) blocks = (int64_t)di.num_sms * 8;
+        if (blocks > 0)
+            kv_rope_pre_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+                static_cast<const uint16_t*>(a.k_pe), a.T, a.Dr, a.cos_tab, a.sin_tab, a.cs_rows, a.cs_width, a.pos,
+                static_cast<uint16_t*>(a.o_key), (int64_t)a.H * Dk, a.Dn, a.status);
+        if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    // 2. the GEMM, its epilogue copying the rope part into the other heads
     const void* k = nullptr;
     switch (a.Dr) {
         case 16: k = (const void*)fwd_kernel<false, false, 16, true>; break;
