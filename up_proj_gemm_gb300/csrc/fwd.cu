@@ -41,7 +41,11 @@ namespace mlaq {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+// warp 0 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 the tiled-scale copies
+// (MXFP8 weights). 11 warps keep three per SM sub-partition at most, so the
+// per-thread register cap stays at 168.
+constexpr int kThreads = 352;
+constexpr int kSfWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;  // TMEM column offset of accumulator buffer 1
 constexpr uint32_t kSfCol0 = 448;     // first TMEM column of the per-stage scale factors
@@ -265,10 +269,12 @@ __device__ __forceinline__ void rot_pair_fwd(float& a, float& b, float ci, float
     b = __fmaf_rn(b0, cj, __fmul_rn(a0, sj));   // b cos_{i+h} + a sin_{i+h}
 }
 
+// part < 0: this warp emits the whole rope unit; part 0 / 1 (DR = 64): the
+// quadrant's two warps both rotate it and each emits one 32-channel half.
 template <bool MXOUT, int DR, bool PACKED>
 __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
                                           uint32_t taddr, int col, bool valid, int64_t t, int64_t n, int h,
-                                          int prow) {
+                                          int prow, int part) {
     constexpr int HH = DR / 2;
     uint32_t r[DR / 16][16];
     __syncwarp();
@@ -311,7 +317,14 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
             for (int e = 0; e < 8; ++e) rot_pair_fwd(y[q + e], y[q + e + HH], ci[e], si[e], cj[e], sj[e]);
         }
     }
-    emit_unit<MXOUT, DR>(p, tmC, c, y, valid, t, n, h, p.Dn);
+    if (DR == 64 && part >= 0) {
+        float yb[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) yb[i] = part ? y[(32 + i) % DR] : y[i];
+        emit_unit<MXOUT, 32>(p, tmC, c, yb, valid, t, n + 32 * part, h, p.Dn + 32 * part);
+    } else {
+        emit_unit<MXOUT, DR>(p, tmC, c, y, valid, t, n, h, p.Dn);
+    }
 }
 
 // Tile order: tiles are strided over the CTAs, so the CTAs running together
@@ -431,17 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int kc = kt * (MXW ? 128 : 64);
                     tma_load_2d_hint(sm.a(s, p), &tmA, kc, mt * BM, sm.full(s), a_pol);
                     tma_load_2d(sm.b(s, p), &tmB, kc, nt * p.BN, sm.full(s));
-                    if (MXW && p.sf_tiled) {
-                        bulk_load(sm.sfa(s), p.x_scales + ((int64_t)(M2 ? 2 * mt : mt) * p.k_tiles + kt) * 512, 512u,
-                                  sm.full(s));
-                        if (M2 && a_hi)  // the second 128-row chunk, when it holds rows below T
-                            bulk_load(sm.sfa(s) + 512u, p.x_scales + ((int64_t)(2 * mt + 1) * p.k_tiles + kt) * 512,
-                                      512u, sm.full(s));
-                        for (int c = 0; c < p.sf_nsub; ++c)
-                            bulk_load(sm.sfb(s) + 512u * c,
-                                      p.w_scales + (((int64_t)nt * p.sf_nsub + c) * p.k_tiles + kt) * 512, 512u,
-                                      sm.full(s));
-                    }
+                    // (the tiled scales: warp kSfWarp, on the same stage barrier)
                 }
                 if (MXW && !p.sf_tiled) {
                     // scale bytes [4 kt, 4 kt + 4) of each row; row r of a 128-row
@@ -476,6 +479,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (issued_mask & (1u << q))
                     mbar_wait(sm.full(q), (issued_par >> q) & 1u, nullptr, 200000000ull);
         }
+    } else if (warp == kSfWarp) {
+        // -------------------------------------------- tiled-scale producer
+        // The stage's E8M0 scale tiles (one 512-byte bulk copy per 128-row
+        // chunk of each operand), issued by a second thread so that warp 0
+        // issues only the two operand tiles per stage. The copies complete
+        // on the stage's full barrier, whose expected bytes warp 0 posts.
+        if (MXW && p.sf_tiled && lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued_mask = 0, issued_par = 0;
+            bool ok = true;
+            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile)) {
+                int mt, nt;
+                q_tile<DR>(p, tile, mt, nt);
+                const bool a_hi = (int64_t)mt * BM + kBM < p.T;
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    bulk_load(sm.sfa(s), p.x_scales + ((int64_t)(M2 ? 2 * mt : mt) * p.k_tiles + kt) * 512, 512u,
+                              sm.full(s));
+                    if (M2 && a_hi)  // the second 128-row chunk, when it holds rows below T
+                        bulk_load(sm.sfa(s) + 512u, p.x_scales + ((int64_t)(2 * mt + 1) * p.k_tiles + kt) * 512, 512u,
+                                  sm.full(s));
+                    for (int c = 0; c < p.sf_nsub; ++c)
+                        bulk_load(sm.sfb(s) + 512u * c,
+                                  p.w_scales + (((int64_t)nt * p.sf_nsub + c) * p.k_tiles + kt) * 512, 512u,
+                                  sm.full(s));
+                    issued_mask |= 1u << s;
+                    issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // unwinding: let every copy this thread started land before the CTA exits
+                for (int q = 0; q < p.stages; ++q)
+                    if (issued_mask & (1u << q))
+                        mbar_wait(sm.full(q), (issued_par >> q) & 1u, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -673,9 +720,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c = n32 - h * p.D;
                 const int64_t n = n32;
                 const bool nope = c < p.Dn;
-                if (M2 || p.split_half || (unit++ & 1) == half) {
+                if (DR == 64 && !nope && !M2 && !p.split_half) {
+                    // units alternate between the quadrant's two warps: both rotate the
+                    // rope unit and each writes one half, which balances their work
+                    if constexpr (DR == 64) rope_unit<MXOUT, DR, PACKED>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow, half);
+                    ++unit;
+                } else if (M2 || p.split_half || (unit++ & 1) == half) {
                     if (nope) nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
-                    else if constexpr (DR > 0) rope_unit<MXOUT, DR, PACKED>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow);
+                    else if constexpr (DR > 0) rope_unit<MXOUT, DR, PACKED>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow, -1);
                 }
                 col += nope ? 32 : DR;
             }
