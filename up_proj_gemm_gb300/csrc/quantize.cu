@@ -288,29 +288,35 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_kernel(const 
 // Fast path: rows 16-byte aligned and C a multiple of the 16-byte vector.
 // A tile is 128 rows x 256 columns, loaded as four 32-row blocks with
 // 16-byte cp.async into a ring of shared-memory buffers (every warp load is
-// 512 contiguous bytes of a row); thread t then reads column t of a block
-// from shared memory (consecutive lanes, consecutive addresses), quantizes
-// it and writes its 32 codes as one run; the tile's 4 scale bytes of a
-// column leave as one 4-byte word when the scale rows allow it.
+// 512 contiguous bytes of a row). Each thread then takes CPT adjacent
+// columns of a block (bf16: two, read together by one 4-byte shared load per
+// row; fp32: one), quantizes each column's 32 values and writes its 32
+// codes as one run; a column's 4 scale bytes of the tile leave as one 4-byte
+// word when the scale rows allow it.
 constexpr int kColTC = 256;
 template <typename Tin>
 __host__ __device__ constexpr int cols_nbuf() { return sizeof(Tin) == 2 ? 4 : 2; }
 template <typename Tin>
 __host__ __device__ constexpr uint32_t cols_buf_bytes() { return 32u * kColTC * (uint32_t)sizeof(Tin); }
+template <typename Tin>
+__host__ __device__ constexpr int cols_cpt() { return sizeof(Tin) == 2 ? 2 : 1; }  // columns per thread
+template <typename Tin>
+__host__ __device__ constexpr int cols_threads() { return kColTC / cols_cpt<Tin>(); }
 
 template <typename Tin, bool VEC>
-__global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const Tin* __restrict__ in, int64_t R,
-                                                                     int64_t C, int64_t ld,
-                                                                     uint8_t* __restrict__ codes, int64_t ldc,
-                                                                     uint8_t* __restrict__ scales, int64_t nbr,
-                                                                     int64_t sf_group) {
+__global__ void __launch_bounds__(cols_threads<Tin>()) mxfp8_quantize_cols_tiled(
+    const Tin* __restrict__ in, int64_t R, int64_t C, int64_t ld, uint8_t* __restrict__ codes, int64_t ldc,
+    uint8_t* __restrict__ scales, int64_t nbr, int64_t sf_group) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int NBUF = cols_nbuf<Tin>();
     constexpr uint32_t BUF = cols_buf_bytes<Tin>();
+    constexpr int CPT = cols_cpt<Tin>();
+    constexpr int NT = cols_threads<Tin>();
     constexpr int EPV = 16 / (int)sizeof(Tin);      // elements per 16-byte vector
     constexpr int VPR = kColTC / EPV;                // vectors per tile row
-    constexpr int VPT = 32 * VPR / kColThreads;      // vectors per thread per block
+    constexpr int VPT = 32 * VPR / NT;               // vectors per thread per block
     constexpr int NB = kColTileR / 32;               // blocks per tile
+    constexpr uint32_t ROWB = (uint32_t)kColTC * (uint32_t)sizeof(Tin);  // bytes per staged row
     const uint32_t sbase = smem_u32(smem);
     const int t = threadIdx.x;
     const int64_t tiles_r = (R + kColTileR - 1) / kColTileR;
@@ -327,12 +333,12 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
             const uint32_t buf = sbase + (uint32_t)(b % NBUF) * BUF;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int idx = t + k * kColThreads;
+                const int idx = t + k * NT;
                 const int row = idx / VPR, vc = idx % VPR;
                 const int64_t r = r0 + row, c = c0 + (int64_t)vc * EPV;
                 const bool ok = r < R && c < C;
                 const Tin* src = ok ? in + r * ld + c : in;
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(buf + (uint32_t)(row * kColTC * (int)sizeof(Tin) + vc * 16)),
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(buf + (uint32_t)row * ROWB + (uint32_t)(vc * 16)),
                              "l"(src), "r"(ok ? 16 : 0)
                              : "memory");
             }
@@ -341,8 +347,10 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
             if (b < NB) issue(b);
             cp_async_commit();
         }
-        const int64_t c = c0 + t;
-        uint32_t sword = 0;
+        const int64_t c = c0 + (int64_t)CPT * t;  // this thread's first column (C % EPV == 0: all CPT exist or none)
+        uint32_t sword[CPT];
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) sword[j] = 0;
         for (int blk = 0; blk < NB; ++blk) {
             if (blk + NBUF - 1 < NB) issue(blk + NBUF - 1);
             cp_async_commit();
@@ -351,31 +359,36 @@ __global__ void __launch_bounds__(kColThreads) mxfp8_quantize_cols_tiled(const T
             const int64_t r0 = tr * kColTileR + 32 * blk;
             if (r0 < R && c < C) {
                 const int n = (R - r0) < 32 ? (int)(R - r0) : 32;
-                const uint32_t buf = sbase + (uint32_t)(blk % NBUF) * BUF + (uint32_t)(t * (int)sizeof(Tin));
-                float v[32];
+                const uint32_t buf = sbase + (uint32_t)(blk % NBUF) * BUF + (uint32_t)(t * CPT * (int)sizeof(Tin));
+                float v[CPT][32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const uint32_t a = buf + (uint32_t)(i * kColTC * (int)sizeof(Tin));
+                    const uint32_t w = lds_b32(buf + (uint32_t)i * ROWB);
                     if (sizeof(Tin) == 2) {
-                        uint16_t h;
-                        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
-                        v[i] = __uint_as_float((uint32_t)h << 16);
+                        v[0][i] = bf16lo_to_f32(w);
+                        v[CPT - 1][i] = bf16hi_to_f32(w);
                     } else {
-                        v[i] = __uint_as_float(lds_b32(a));
+                        v[0][i] = __uint_as_float(w);
                     }
                 }
                 // rows past R were zero-filled by the loads: they leave the amax unchanged
-                uint32_t w[8];
-                const uint32_t sb = quantize_block32(v, w);
-                store_codes(codes + c * ldc + r0, w, n, VEC);
-                if (word_scales) sword |= sb << (8 * blk);
-                else scales[c * nbr + r0 / 32] = (uint8_t)sb;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) {
+                    uint32_t w[8];
+                    const uint32_t sb = quantize_block32(v[j], w);
+                    store_codes(codes + (c + j) * ldc + r0, w, n, VEC);
+                    if (word_scales) sword[j] |= sb << (8 * blk);
+                    else scales[(c + j) * nbr + r0 / 32] = (uint8_t)sb;
+                }
             }
             __syncthreads();  // the buffer may be refilled now
         }
-        if (word_scales && c < C && tr * kColTileR < R)
-            *reinterpret_cast<uint32_t*>(scales + (sf_group > 0 ? sf_tiled_offset(c, tr * NB, sf_group, tiles_r)
-                                                                : c * nbr + tr * NB)) = sword;
+        if (word_scales && c < C && tr * kColTileR < R) {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j)
+                *reinterpret_cast<uint32_t*>(scales + (sf_group > 0 ? sf_tiled_offset(c + j, tr * NB, sf_group, tiles_r)
+                                                                    : (c + j) * nbr + tr * NB)) = sword[j];
+        }
     }
 }
 
@@ -437,10 +450,11 @@ int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t*
                             : (const void*)mxfp8_quantize_cols_tiled<Tin, false>;
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return MLA_ERR_CUDA;
+        constexpr int NT = cols_threads<Tin>();
         if (vec)
-            mxfp8_quantize_cols_tiled<Tin, true><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
+            mxfp8_quantize_cols_tiled<Tin, true><<<(unsigned)blocks, NT, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
         else
-            mxfp8_quantize_cols_tiled<Tin, false><<<(unsigned)blocks, kColThreads, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
+            mxfp8_quantize_cols_tiled<Tin, false><<<(unsigned)blocks, NT, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
         return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
     }
     if (sf_group > 0) return MLA_ERR_UNSUPPORTED;  // the tiled scale order needs the fast path
