@@ -158,29 +158,37 @@ def device_info(dev):
     return out
 
 
-def kernel_hash():
-    """Hash of the kernel sources' code: comments and blank space removed, so
-    an edit to a comment does not invalidate the captured DRAM counters."""
+def source_hash(name):
+    """Hash of one kernel source's code (csrc/<name>): comments and blank
+    space removed, so an edit to a comment does not invalidate the DRAM
+    counters captured for it."""
     import re
-    h = hashlib.sha256()
-    for name in ("fwd.cu", "bwd.cu", "quantize.cu", "ptx.cuh", "mx.cuh"):
-        with open(os.path.join(ROOT, "up_proj_gemm_gb300", "csrc", name)) as f:
-            src = f.read()
-        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
-        src = re.sub(r"//[^\n]*", " ", src)                  # line comments
-        h.update(" ".join(src.split()).encode())
-    return h.hexdigest()[:16]
+    with open(os.path.join(ROOT, "up_proj_gemm_gb300", "csrc", name)) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
+    src = re.sub(r"//[^\n]*", " ", src)                  # line comments
+    return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()[:16]
 
 
-def traffic_for(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the kernels as they are now (same source hash); else None."""
+# the sources each captured call's kernels are built from
+TRAFFIC_SOURCES = {"fwd": ("fwd.cu", "ptx.cuh", "mx.cuh"), "dgrad": ("bwd.cu", "ptx.cuh", "mx.cuh"),
+                   "wgrad": ("bwd.cu", "ptx.cuh", "mx.cuh")}
+
+
+def kernel_hashes(call):
+    return {n: source_hash(n) for n in TRAFFIC_SOURCES[call]}
+
+
+def traffic_for(key: str):
+    """DRAM bytes per launch of a call from the committed ncu summary, if it
+    was taken on the kernel sources as they are now (same hashes); else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
-        if d.get("kernel_hash") != kernel_hash():
+        e = d["entries"][key]
+        if e["sources"] != kernel_hashes(e["call"]):
             return None
-        return d["per_launch_bytes"].get(kernel)
+        return e["bytes"]
     except Exception:
         return None
 
@@ -391,7 +399,7 @@ def run_ours(args):
     labels = {"dgrad": "dgrad (rope pass + stream-K GEMM, one call)"}
     roofline = {"bound": "tensor", "kernel": labels.get(names[dom], names[dom]), "achieved": round(achieved, 1),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic_for(f"{names[dom]}_T{w.T}"),
+                "traffic": traffic_for(f"{('fwd', 'dgrad', 'wgrad')[dom]}_T{w.T}"),
                 "peak_source": f"{pk_src} bf16_tflops (cuBLAS bf16 burst; the timed region is "
                                f"{K} steps of ~{step_ms:.1f} ms, not a seconds-long loop)",
                 "algorithmic_flop_per_launch": flops[dom]}

@@ -35,10 +35,11 @@ def test_kernel_hash_ignores_comments(tmp_path, monkeypatch):
     csrc = tmp_path / "up_proj_gemm_gb300" / "csrc"
     shutil.copytree(os.path.join(ROOT, "up_proj_gemm_gb300", "csrc"), csrc)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    h0 = bench.kernel_hash()
+    h0, hb = bench.kernel_hashes("fwd"), bench.kernel_hashes("dgrad")
     f = csrc / "fwd.cu"
     src = f.read_text()
     f.write_text("// a new comment line\n/* and a block\n   comment */\n" + src.replace("\n", "\n\n", 3))
-    assert bench.kernel_hash() == h0
+    assert bench.kernel_hashes("fwd") == h0
     f.write_text(src.replace("constexpr int kBM = 128;", "constexpr int kBM = 64;"))
-    assert bench.kernel_hash() != h0
+    assert bench.kernel_hashes("fwd") != h0
+    assert bench.kernel_hashes("dgrad") == hb  # the backward's counters do not depend on fwd.cu

@@ -180,3 +180,29 @@ def test_dgrad_split_reduction(cuda_device):
     with pytest.raises(mlaq.MlaError) as ei:
         mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], workspace=small)
     assert ei.value.status == mlaq.STATUS["MLA_ERR_WORKSPACE"]
+
+
+@pytest.mark.parametrize("ov", [
+    dict(T=3000, seq_len=None),                 # ragged last token tile, split tiles with one later part
+    dict(T=300, seq_len=None),                  # 24 groups of 32 K steps: an owner adds 11 partial tiles
+    dict(T=2048, K=256, H=16, seq_len=512),     # one column tile: 12 groups, positions restart
+])
+def test_dgrad_stream_k_schedules(cuda_device, ov):
+    """dgrad's stream-K schedule on shapes whose tiles split between groups in
+    different ways: every dx element against the oracle, two runs
+    bit-identical (the owner adds the parts in a fixed order), and the same
+    bits with the rotated rope channels kept in the workspace or handed out
+    through dq_pre_rope."""
+    w = synth.workload("dsv3_bwd", **ov)
+    inp, d = _dev_inputs(w, 17, cuda_device)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    need = mlaq.workspace_size(w.T, w.K, w.H, w.Dn, w.Dr, w.cs_rows, w.Dr, 1)
+    ws = torch.empty((need,), dtype=torch.uint8, device=cuda_device)
+    args = (d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr)
+    dx1 = mlaq.bwd_dgrad(*args, pos=d["pos"], status=st, workspace=ws)
+    dx2 = mlaq.bwd_dgrad(*args, pos=d["pos"], status=st, workspace=ws)
+    rope = torch.empty((w.T, w.H, w.Dr), dtype=torch.bfloat16, device=cuda_device)
+    dx3 = mlaq.bwd_dgrad(*args, pos=d["pos"], status=st, dq_pre_rope=rope)
+    mlaq.check_status(st)
+    assert torch.equal(dx1, dx2) and torch.equal(dx1, dx3)
+    helpers.check_bwd_all(inp, w, dx=dx1, rope=rope, tol=TOL)
