@@ -515,6 +515,19 @@ MLAQ_API int mxfp8_swizzle_scales(int64_t rows, int64_t cols, const uint8_t *in,
 MLAQ_API int mla_wait_selftest(int arrive, uint64_t limit_ns, int *dev_status, void *stream);
 
 /*
+ * The same check for the other kind of device wait, the one on a flag in
+ * global memory that another CTA raises (dgrad's stream-K owners wait so
+ * for the partial sums of the later CTAs of their column; the pages define
+ * no such operation). One CTA: role 0 waits on a flag that role 1 raises
+ * only when set != 0, then releases role 1. With set == 0 role 0 gives up
+ * after limit_ns of %globaltimer, role 1 leaves through the CTA's abort flag,
+ * and MLA_ERR_TIMEOUT is written to *dev_status (if it held 0). The flag is
+ * a word of the library's own device memory: calls must not overlap.
+ * limit_ns in [1e6, 1e9], dev_status as for mla_wait_selftest.
+ */
+MLAQ_API int mla_wait_selftest_flag(int set, uint64_t limit_ns, int *dev_status, void *stream);
+
+/*
  * Row-group variant of mxfp8_swizzle_scales: rows in groups of `group`, each
  * group padded to whole 128-row tiles (so a GEMM tile of `group` rows starts
  * at a tile boundary). Chunk i of group g and column tile j is the 512-byte

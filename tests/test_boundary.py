@@ -364,6 +364,14 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         mlaq.lib()
 
 
+def test_wait_selftest_flag_rejects(L):
+    f = L.mla_wait_selftest_flag
+    assert f(0, 50_000_000, None, None) == S["MLA_ERR_INVALID_ARG"]                      # no status word
+    assert f(0, 50_000_000, ctypes.c_void_p(FAKE + 2), None) == S["MLA_ERR_INVALID_ARG"]  # misaligned
+    assert f(0, 999_999, p(0), None) == S["MLA_ERR_INVALID_ARG"]                          # limit below 1 ms
+    assert f(0, 1_000_000_001, p(0), None) == S["MLA_ERR_INVALID_ARG"]                    # above 1 s
+
+
 def test_wait_selftest_rejects(L):
     """mla_wait_selftest checks its arguments before any launch."""
     bad = S["MLA_ERR_INVALID_ARG"]

@@ -62,3 +62,32 @@ def test_context_usable_after_timeout(cuda_device):
                  out_mode="bf16", status=st2)
     mlaq.check_status(st2)
     helpers.check_bf16_close(q, helpers.oracle_forward(inp, w))
+
+
+def test_flag_wait_completes_when_raised(cuda_device):
+    """The cross-CTA flag wait of dgrad's stream-K owners: a raised flag ends
+    the wait at once, nothing is reported."""
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    ms = _timed(lambda: mlaq.wait_selftest_flag(True, 50.0, st))
+    assert int(st.item()) == S["MLA_OK"]
+    assert ms < 25.0, f"a raised flag still waited {ms:.1f} ms"
+
+
+def test_flag_wait_gives_up_and_reports(cuda_device):
+    """A flag nothing raises: the wait gives up at its limit, the other role
+    leaves through the abort flag, MLA_ERR_TIMEOUT reaches the host, and the
+    context stays usable (a dgrad afterwards matches the oracle)."""
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    ms = _timed(lambda: mlaq.wait_selftest_flag(False, 50.0, st))
+    assert int(st.item()) == S["MLA_ERR_TIMEOUT"]
+    assert 50.0 <= ms < 90.0, f"{ms:.1f} ms"
+    w = synth.workload("dsv3_bwd", T=300, H=8, seq_len=None)
+    inp = synth.make_inputs(w, seed=19)
+    d = helpers.to_dev(inp, cuda_device)
+    st2 = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    dx = mlaq.bwd_dgrad(d["dq"], d["W"], d["cos"], d["sin"], w.H, w.Dn, w.Dr, pos=d["pos"], status=st2)
+    mlaq.check_status(st2)
+    import oracle
+    g = oracle.backward(helpers.f64(inp["dq"]), helpers.f64(inp["x"]), helpers.f64(inp["W"]), w.H, w.Dn, w.Dr,
+                        inp["cos"].numpy(), inp["sin"].numpy(), inp["pos"].numpy())
+    assert helpers.frob_rel(dx, g["dx"]) <= 5e-3

@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "MlaError", "lib", "library_path", "fwd", "bwd_dgrad", "bwd_wgrad", "mxfp8_quantize_rows",
     "mxfp8_quantize_cols", "mxfp8_swizzle_scales", "kv_fwd", "rope_table_pack", "bwd_mxfp8", "bwd_mxfp8_layout",
-    "bwd_mxfp8_operands", "bwd_mxfp8_prepare_weight", "w_scale_group", "wait_selftest",
+    "bwd_mxfp8_operands", "bwd_mxfp8_prepare_weight", "w_scale_group", "wait_selftest", "wait_selftest_flag",
     "workspace_size", "status_string", "check_status", "Shape", "KvShape", "Mxfp8BwdLayout", "STATUS",
     "WEIGHT_MODES", "OUT_MODES",
 ]
@@ -96,6 +96,7 @@ _SIGS = {
     "mla_q_uproj_w_scale_group": (ctypes.c_int64, [ctypes.POINTER(Shape)]),
     "mla_q_uproj_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), _int]),
     "mla_wait_selftest": (_int, [_int, ctypes.c_uint64, _vp, _vp]),
+    "mla_wait_selftest_flag": (_int, [_int, ctypes.c_uint64, _vp, _vp]),
     "mla_status_string": (ctypes.c_char_p, [_int]),
     "mla_version": (_int, []),
 }
@@ -125,6 +126,15 @@ def wait_selftest(arrive: bool, limit_ms: float, status: torch.Tensor, stream=No
     and MLA_ERR_TIMEOUT lands in ``status``; with arrive=True nothing does."""
     _need(status, "status", torch.int32, min_numel=1)
     _call(lib().mla_wait_selftest, "mla_wait_selftest", int(bool(arrive)), int(round(limit_ms * 1e6)),
+          _ptr(status), _stream(status.device, stream))
+
+
+def wait_selftest_flag(set_flag: bool, limit_ms: float, status: torch.Tensor, stream=None) -> None:
+    """Run the flag-wait self-test (mla_wait_selftest_flag): with
+    set_flag=False a device wait on a flag nothing raises gives up after
+    limit_ms and MLA_ERR_TIMEOUT lands in ``status``."""
+    _need(status, "status", torch.int32, min_numel=1)
+    _call(lib().mla_wait_selftest_flag, "mla_wait_selftest_flag", int(bool(set_flag)), int(round(limit_ms * 1e6)),
           _ptr(status), _stream(status.device, stream))
 
 

@@ -43,8 +43,47 @@ __global__ void __launch_bounds__(64) wait_selftest_kernel(int arrive, uint64_t 
     if (threadIdx.x == 0 && *ab) record_status(status, MLA_ERR_TIMEOUT);
 }
 
+// The cross-CTA flag wait of dgrad's stream-K owners (wait_flag_gpu), run
+// on its own: warp 0 waits for a flag in global memory that warp 1 sets only
+// when `set` is non-zero; warp 1 then waits on a barrier that only warp 0's
+// success releases. One CTA; the flag is the file's own word, reset first.
+__device__ unsigned g_selftest_flag;
+
+__global__ void __launch_bounds__(64) flag_selftest_kernel(int set, uint64_t limit_ns, int* status) {
+    __shared__ alignas(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t done = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(done, 1);
+        abort_flag = 0;
+        fence_mbarrier_init();
+        st_release_gpu(&g_selftest_flag, 0u);
+    }
+    __syncthreads();
+    volatile int* ab = &abort_flag;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (warp == 0) {
+        bool ok = true;
+        if (lane == 0) ok = wait_flag_gpu(&g_selftest_flag, 1u, ab, limit_ns);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (ok && lane == 0) mbar_arrive(done);
+    } else {
+        if (set && lane == 0) st_release_gpu(&g_selftest_flag, 1u);
+        mbar_wait(done, 0, ab, 2 * limit_ns);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *ab) record_status(status, MLA_ERR_TIMEOUT);
+}
+
 }  // namespace
 }  // namespace mlaq
+
+extern "C" MLAQ_API int mla_wait_selftest_flag(int set, uint64_t limit_ns, int* dev_status, void* stream) {
+    if (dev_status == nullptr || (reinterpret_cast<uintptr_t>(dev_status) & 3)) return MLA_ERR_INVALID_ARG;
+    if (limit_ns < 1000000ull || limit_ns > 1000000000ull) return MLA_ERR_INVALID_ARG;
+    mlaq::flag_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(set != 0, limit_ns, dev_status);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
 
 extern "C" MLAQ_API int mla_wait_selftest(int arrive, uint64_t limit_ns, int* dev_status, void* stream) {
     if (dev_status == nullptr || (reinterpret_cast<uintptr_t>(dev_status) & 3)) return MLA_ERR_INVALID_ARG;
