@@ -58,7 +58,16 @@ constexpr uint32_t kSfBytesPerStage = 512 + 1024;
 constexpr uint32_t kSfColsPerStage2 = 16;
 constexpr uint32_t kSfBytesPerStage2 = 1024 + 1024;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, splitting the tile's units
-constexpr int kSlotCh = 16;       // channels per slot (one TMA store box: 16 channels x 32 rows)
+// Output staging slot: one TMA store box of 32 token rows. bf16 output: 16
+// channels (32 bytes a row); MXFP8 output: one 32-channel block (32 bytes a
+// row), or 16 channels (16 bytes a row) when Dr = 16, whose rope part is a
+// 16-channel block. The TMA unit of an SM
+// handles a fixed number of tile operations per second whatever their size,
+// so the MXFP8 forward's q stores (one per block instead of two) matter.
+template <bool MXOUT, int DR>
+__host__ __device__ constexpr int slot_ch() {
+    return (MXOUT && DR % 32 == 0) ? 32 : 16;
+}
 
 struct FwdParams {
     int T, H, N, D, Dn;
@@ -68,7 +77,7 @@ struct FwdParams {
     uint32_t a_bytes, stage_bytes, tx_bytes;
     uint32_t idesc;
     int ksb;  // scale bytes per operand row (K / 32)
-    uint32_t slot_bytes;  // 32 rows x 16 channels x output element size
+    uint32_t slot_bytes;  // room for one store box (32 rows x at most 32 bytes)
     int cs_vec;           // cos/sin rows 16-byte aligned: float4 loads
     int nslots;           // staging slots per epilogue warp
     int scales_bhsd;      // MXFP8 scales head-major [H, T, NB] (else [T, H, NB])
@@ -126,7 +135,7 @@ struct Smem {
 
 // ------------------------------------------------------------ epilogue parts
 // Each epilogue warp owns 32 token rows of the tile. Its results go through a
-// ring of p.nslots shared-memory slots (32 rows x 16 channels each) and leave
+// ring of p.nslots shared-memory slots (one store box each) and leave
 // as TMA tile stores (one per slot), so global writes are whole, coalesced
 // boxes and the LSU queue carries no per-row stores.
 struct EpiCtx {
@@ -160,13 +169,18 @@ __device__ __forceinline__ void add_bias(float* v, int nv, const uint16_t* bias)
 
 // Quantize/convert this thread's NV values (output channels [n, n + NV) of
 // token t, i.e. channels [cin, cin + NV) of head h) into the staging ring and
-// store them with TMA. NV is a multiple of 16.
-template <bool MXOUT, int NV>
+// store them with TMA, one store per CH channels. NV is a multiple of CH.
+// A lane's 32-byte row of a slot is written as two 16-byte halves, lanes
+// with bit 2 set upper half first, so each store instruction of the warp
+// takes the minimum four shared-memory wavefronts.
+template <bool MXOUT, int NV, int CH>
 __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
                                           const float (&v)[NV], bool valid, int64_t t, int64_t n, int h,
                                           int cin) {
-    constexpr int PIECES = NV / 16;
+    static_assert(NV % CH == 0 && (CH == 16 || (MXOUT && CH == 32)), "slot width");
+    constexpr int PIECES = NV / CH;
     const int lane = threadIdx.x & 31;
+    const uint32_t h0 = (lane & 4) ? 16u : 0u, h1 = 16u - h0;  // byte offsets of the two halves, in store order
     // the slots about to be written were last read by stores older than the previous unit's
     if (lane == 0) {
         // the stores of the last two units may still read their slots when those
@@ -187,10 +201,20 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
             const int nvalid = (NV - blk * 32) < 32 ? (NV - blk * 32) : 32;
             uint32_t codes[8];
             const uint32_t sb = quantize_block_regs<32>(b, nvalid, codes);
-            sts_v4(slot_addr(p, c, first + 2 * blk) + 16u * lane, codes[0], codes[1], codes[2], codes[3]);
-            if (nvalid > 16)
-                sts_v4(slot_addr(p, c, first + 2 * blk + 1) + 16u * lane, codes[4], codes[5], codes[6],
-                       codes[7]);
+            if (CH == 32) {
+                // the block's 32 codes: one 32-byte slot row
+                const uint32_t a = slot_addr(p, c, first + blk) + 32u * lane;
+                const uint32_t* q0 = (lane & 4) ? codes + 4 : codes;
+                const uint32_t* q1 = (lane & 4) ? codes : codes + 4;
+                sts_v4(a + h0, q0[0], q0[1], q0[2], q0[3]);
+                sts_v4(a + h1, q1[0], q1[1], q1[2], q1[3]);
+            } else {
+                // 16-channel slots (a 16 x 32 box: rows 16 bytes apart), two per block
+                sts_v4(slot_addr(p, c, first + 2 * blk) + 16u * lane, codes[0], codes[1], codes[2], codes[3]);
+                if (nvalid > 16)
+                    sts_v4(slot_addr(p, c, first + 2 * blk + 1) + 16u * lane, codes[4], codes[5], codes[6],
+                           codes[7]);
+            }
             if (p.split_half) {
                 c.sword |= sb << (8 * (int)((n + 32 * blk) / 32 - c.sbase));
             } else if (p.qs_swz) {
@@ -213,10 +237,12 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
         for (int pc = 0; pc < PIECES; ++pc) {
             const uint32_t a = slot_addr(p, c, first + pc) + 32u * lane;
             const float* w = v + 16 * pc;
-            sts_v4(a, pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
-                   pack_bf16x2(w[6], w[7]));
-            sts_v4(a + 16, pack_bf16x2(w[8], w[9]), pack_bf16x2(w[10], w[11]), pack_bf16x2(w[12], w[13]),
-                   pack_bf16x2(w[14], w[15]));
+            const float* w0 = (lane & 4) ? w + 8 : w;
+            const float* w1 = (lane & 4) ? w : w + 8;
+            sts_v4(a + h0, pack_bf16x2(w0[0], w0[1]), pack_bf16x2(w0[2], w0[3]), pack_bf16x2(w0[4], w0[5]),
+                   pack_bf16x2(w0[6], w0[7]));
+            sts_v4(a + h1, pack_bf16x2(w1[0], w1[1]), pack_bf16x2(w1[2], w1[3]), pack_bf16x2(w1[4], w1[5]),
+                   pack_bf16x2(w1[6], w1[7]));
         }
     }
     fence_proxy_async_smem();
@@ -225,7 +251,7 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
         const uint64_t pol = l2_evict_first_policy();  // q is written once: do not let it push x, W out of L2
 #pragma unroll
         for (int pc = 0; pc < PIECES; ++pc)
-            tma_store_2d_hint(tmC, (int32_t)(n + 16 * pc), c.t0, slot_addr(p, c, first + pc), pol);
+            tma_store_2d_hint(tmC, (int32_t)(n + CH * pc), c.t0, slot_addr(p, c, first + pc), pol);
         bulk_commit_group();
     }
     c.cursor = first + PIECES;
@@ -233,7 +259,7 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
     c.prev_pieces = PIECES;
 }
 
-template <bool MXOUT>
+template <bool MXOUT, int CH>
 __device__ __forceinline__ void nope_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
                                           uint32_t taddr, int col, bool valid, int64_t t, int64_t n, int h,
                                           int cin) {
@@ -245,7 +271,7 @@ __device__ __forceinline__ void nope_unit(const FwdParams& p, const CUtensorMap*
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
     if (c.bias) add_bias(v, 32, c.bias + col);
-    emit_unit<MXOUT, 32>(p, tmC, c, v, valid, t, n, h, cin);
+    emit_unit<MXOUT, 32, CH>(p, tmC, c, v, valid, t, n, h, cin);
 }
 
 __device__ __forceinline__ void load_table8(const float* src, bool vec, float (&o)[8]) {
@@ -321,9 +347,9 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
         float yb[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) yb[i] = part ? y[(32 + i) % DR] : y[i];
-        emit_unit<MXOUT, 32>(p, tmC, c, yb, valid, t, n + 32 * part, h, p.Dn + 32 * part);
+        emit_unit<MXOUT, 32, slot_ch<MXOUT, DR>()>(p, tmC, c, yb, valid, t, n + 32 * part, h, p.Dn + 32 * part);
     } else {
-        emit_unit<MXOUT, DR>(p, tmC, c, y, valid, t, n, h, p.Dn);
+        emit_unit<MXOUT, DR, slot_ch<MXOUT, DR>()>(p, tmC, c, y, valid, t, n, h, p.Dn);
     }
 }
 
@@ -726,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (DR == 64) rope_unit<MXOUT, DR, PACKED>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow, half);
                     ++unit;
                 } else if (M2 || p.split_half || (unit++ & 1) == half) {
-                    if (nope) nope_unit<MXOUT>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
+                    if (nope) nope_unit<MXOUT, slot_ch<MXOUT, DR>()>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
                     else if constexpr (DR > 0) rope_unit<MXOUT, DR, PACKED>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow, -1);
                 }
                 col += nope ? 32 : DR;
@@ -1015,8 +1041,11 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.qs_swz = a.out_mode == MLA_OUT_MXFP8_BHSD_SWIZZLED;
     p.qs_row_tiles = (int)((a.T + 127) / 128);
     p.qs_col_tiles = (D / 32 + (D % 32 ? 1 : 0) + 3) / 4;
-    p.slot_bytes = 32u * kSlotCh * (mxo ? 1u : 2u);
-    p.nslots = mxo ? 8 : 4;  // a unit takes at most 4 slots (64 rope channels)
+    // 32 rows x 32 bytes per slot; a unit takes at most 4 slots (64 bf16 rope
+    // channels, or 16-channel MXFP8 slots), 2 with 32-channel MXFP8 slots
+    const int slot_c = mxo && a.Dr % 32 == 0 ? 32 : 16;
+    p.slot_bytes = 1024;
+    p.nslots = 4;
     // The half split packs a row's scale bytes for half a tile into one aligned
     // 4-byte word: only when half a tile is exactly 4 blocks (BN = 256, so the
     // word starts at a multiple of 4 blocks) and rows of scales keep 4-byte
@@ -1043,10 +1072,10 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     st = make_tmap_2d(&tb, a.W, mxw ? 0 : 1, (uint64_t)a.K, (uint64_t)N, (uint64_t)(a.ld_w ? a.ld_w : a.K) * esz,
                       128 / (uint32_t)esz, (uint32_t)BN, true);
     if (st != MLA_OK) return st;
-    // output q [T, N] (bf16 or E4M3 bytes): TMA store boxes of 16 channels x 32 tokens
+    // output q [T, N] (bf16 or E4M3 bytes): TMA store boxes of slot_c channels x 32 tokens
     alignas(64) CUtensorMap tc;
     st = make_tmap_2d(&tc, a.q_out, mxo ? 0 : 1, (uint64_t)N, (uint64_t)a.T, (uint64_t)N * (mxo ? 1 : 2),
-                      kSlotCh, 32, false);
+                      (uint32_t)slot_c, 32, false);
     if (st != MLA_OK) return st;
 
     int grid = p.num_tiles < di.num_sms ? p.num_tiles : di.num_sms;
