@@ -125,3 +125,40 @@ def test_fwd_tiled_scales_bit_identical(cuda_device, name, ov):
     c2, s2 = mlaq.fwd(*args, weight_mode="mxfp8_tiled", x_scales=xst, w_scales=Wst, status=st, **kw)
     mlaq.check_status(st)
     assert torch.equal(c1, c2) and torch.equal(s1, s2)
+
+
+TILED_CASES = [
+    # (workload, overrides, out_mode, packed table)
+    ("dsv3_fwd_mxfp8w", dict(T=300, H=4), "mxfp8", True),                 # ragged last token tile
+    ("dsv3_fwd_mxfp8w", dict(T=129, H=2, bias=True), "mxfp8_bhsd", False),  # one token in the last tile
+    ("dsv3_fwd_mxfp8w", dict(T=64, H=3), "mxfp8_bhsd_swizzled", True),      # one partial tile
+    ("dsv3_fwd_mxfp8w", dict(T=520, H=5, K=512), "bf16", True),
+    ("tiny", dict(T=390, K=256, H=8, Dn=64, Dr=32), "mxfp8", False),        # Dr = 32
+    ("tiny", dict(T=1, K=128, H=4), "mxfp8", True),                         # one token, Dr = 16
+]
+
+
+@pytest.mark.parametrize("name,ov,out_mode,packed", TILED_CASES)
+def test_fwd_tiled_scales_every_mode(cuda_device, name, ov, out_mode, packed):
+    """The tiled-scale forward (three bulk copies of scale tiles per stage)
+    equals the per-row-gather forward, which test_fwd_mxfp8_weights checks
+    against the oracle, for every output mode, both table layouts and
+    ragged token counts."""
+    w = synth.workload(name, **ov)
+    inp = synth.make_inputs(w, seed=23)
+    d = helpers.to_dev(inp, cuda_device)
+    xq, xsc = mlaq.mxfp8_quantize_rows(d["x"])
+    Wq, Wsc = mlaq.mxfp8_quantize_rows(d["W"])
+    xst, Wst = _tiled_scales(xsc, Wsc, w)
+    args = (xq, Wq, d["cos"], d["sin"], w.H, w.Dn, w.Dr)
+    kw = dict(bias=d.get("b"), pos=d["pos"], out_mode=out_mode)
+    if packed:
+        kw["rope_packed"] = mlaq.rope_table_pack(d["cos"], d["sin"], w.Dr)
+    st = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    a = mlaq.fwd(*args, weight_mode="mxfp8", x_scales=xsc, w_scales=Wsc, status=st, **kw)
+    b = mlaq.fwd(*args, weight_mode="mxfp8_tiled", x_scales=xst, w_scales=Wst, status=st, **kw)
+    mlaq.check_status(st)
+    a = a if isinstance(a, tuple) else (a,)
+    b = b if isinstance(b, tuple) else (b,)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
