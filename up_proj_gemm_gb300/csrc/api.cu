@@ -44,7 +44,8 @@ int current_device_info(DeviceInfo* out) {
 
 // ------------------------------------------------------------- tensor maps
 int make_tmap_2d(void* tmap_out, const void* base, int dtype, uint64_t inner, uint64_t outer,
-                 uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+                 uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128,
+                 bool swizzle64) {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     std::call_once(once, [] {
@@ -64,7 +65,8 @@ int make_tmap_2d(void* tmap_out, const void* base, int dtype, uint64_t inner, ui
                         dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                         const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : (swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE),
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -90,6 +90,7 @@ struct FwdParams {
     int num_n_tiles;
     uint32_t sf_stage;    // scale staging bytes per stage (MXFP8 weights)
     uint32_t sf_cols;     // TMEM scale-factor columns per stage
+    int half_store;       // (with split_half, MXFP8 q) 64-channel store boxes, two per half tile
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
                           // write each row's scale bytes as one 4-byte word (else: units
                           // alternate between them and scales go byte by byte)
@@ -147,6 +148,8 @@ struct EpiCtx {
     int32_t t0;       // first token row of this warp's 32-row slab
     uint32_t sword;   // packed scale bytes of this row's half tile (split_half)
     int64_t sbase;    // first 32-channel block index of that half
+    int32_t hcol0;    // (half_store) first channel of this warp's half tile
+    const CUtensorMap* tmh;  // (half_store) q as 64-channel x 32-token boxes, 64-byte swizzle
 };
 
 __device__ __forceinline__ uint32_t slot_addr(const FwdParams& p, const EpiCtx& c, int k) {
@@ -181,6 +184,44 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
     constexpr int PIECES = NV / CH;
     const int lane = threadIdx.x & 31;
     const uint32_t h0 = (lane & 4) ? 16u : 0u, h1 = 16u - h0;  // byte offsets of the two halves, in store order
+    if constexpr (MXOUT && CH == 32) {
+        if (p.half_store) {
+            // A warp's half tile (128 channels, in column order) leaves in two
+            // 64-channel store boxes: two 2 KB slots, rows 64 bytes apart in
+            // the 64-byte swizzled order of the store's tensor map (16-byte
+            // chunk k of row r at position k ^ ((r / 2) % 4)), so each store
+            // instruction takes the minimum four wavefronts. A slot is reused
+            // once the store before the previous one has read it.
+#pragma unroll
+            for (int blk = 0; blk < NV / 32; ++blk) {
+                float b[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) b[i] = v[blk * 32 + i];
+                uint32_t codes[8];
+                const uint32_t sb = quantize_block_regs<32>(b, 32, codes);
+                const int co = (int)n + 32 * blk - c.hcol0;  // 0, 32, 64 or 96
+                const uint32_t slot = c.slots + (uint32_t)(co / 64) * 2048u;
+                if ((co & 63) == 0) {
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                }
+                const uint32_t k0 = (uint32_t)(co & 63) / 16u, sw = ((uint32_t)lane >> 1) & 3u;
+                const uint32_t row = slot + 64u * lane;
+                sts_v4(row + ((k0 ^ sw) << 4), codes[0], codes[1], codes[2], codes[3]);
+                sts_v4(row + (((k0 + 1u) ^ sw) << 4), codes[4], codes[5], codes[6], codes[7]);
+                c.sword |= sb << (8 * (int)((n + 32 * blk) / 32 - c.sbase));
+                if ((co & 63) == 32) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d_hint(c.tmh, c.hcol0 + (co & ~63), c.t0, slot, l2_evict_first_policy());
+                        bulk_commit_group();
+                    }
+                }
+            }
+            return;
+        }
+    }
     // the slots about to be written were last read by stores older than the previous unit's
     if (lane == 0) {
         // the stores of the last two units may still read their slots when those
@@ -709,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - 2;    // epilogue warp 0..3
         EpiCtx ec;
         ec.slots = sm.out + (uint32_t)(ew * p.nslots) * p.slot_bytes;
+        ec.tmh = &tmD;
         ec.cursor = 0;
         ec.prev_pieces = 0;
         ec.prev2_pieces = 0;
@@ -738,6 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ec.bias = p.bias ? p.bias + n0 : nullptr;
             ec.sword = 0;
             ec.sbase = (n0 + (p.split_half ? half * (p.BN / 2) : 0)) / 32;
+            ec.hcol0 = (int32_t)n0 + half * (p.BN / 2);
             int col = p.split_half ? half * (p.BN / 2) : 0, unit = 0;
             const int col_end = p.split_half ? col + p.BN / 2 : p.BN;
             while (col < col_end) {
@@ -779,32 +822,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool MXW, bool MXOUT, int DR, bool PACKED = false>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                   const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
+                   const FwdParams& p, int grid, size_t smem, cudaStream_t stream, const CUtensorMap* td = nullptr) {
     auto kern = fwd_kernel<MXW, MXOUT, DR, false, PACKED>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return MLA_ERR_CUDA;
-    kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, tc, p);
+    kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, td ? *td : tc, p);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 template <bool MXW, bool MXOUT, bool PACKED>
-int launch_dr_t(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+int launch_dr_t(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& td,
                 const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
     switch (Dr) {
-        case 16: return launch_variant<MXW, MXOUT, 16, PACKED>(ta, tb, tc, p, grid, smem, stream);
-        case 32: return launch_variant<MXW, MXOUT, 32, PACKED>(ta, tb, tc, p, grid, smem, stream);
-        case 64: return launch_variant<MXW, MXOUT, 64, PACKED>(ta, tb, tc, p, grid, smem, stream);
+        case 16: return launch_variant<MXW, MXOUT, 16, PACKED>(ta, tb, tc, p, grid, smem, stream, &td);
+        case 32: return launch_variant<MXW, MXOUT, 32, PACKED>(ta, tb, tc, p, grid, smem, stream, &td);
+        case 64: return launch_variant<MXW, MXOUT, 64, PACKED>(ta, tb, tc, p, grid, smem, stream, &td);
         default: return MLA_ERR_UNSUPPORTED;
     }
 }
 
 // the table layout is a compile-time choice: one table path per kernel
 template <bool MXW, bool MXOUT>
-int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+int launch_dr(int Dr, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& td,
               const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
-    return p.tab4 ? launch_dr_t<MXW, MXOUT, true>(Dr, ta, tb, tc, p, grid, smem, stream)
-                  : launch_dr_t<MXW, MXOUT, false>(Dr, ta, tb, tc, p, grid, smem, stream);
+    return p.tab4 ? launch_dr_t<MXW, MXOUT, true>(Dr, ta, tb, tc, td, p, grid, smem, stream)
+                  : launch_dr_t<MXW, MXOUT, false>(Dr, ta, tb, tc, td, p, grid, smem, stream);
 }
 
 }  // namespace
@@ -1053,6 +1096,11 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     p.split_half = mxo && !p.scales_bhsd && !p.qs_swz && D % 32 == 0 && BN == 256 && N % 128 == 0 &&
                    reinterpret_cast<uintptr_t>(a.q_scales) % 4 == 0 &&
                    fwd_tile_n(N, D, a.Dn, a.Dr, BN / 2, BN / 2) == BN / 2;
+    // Two 64-channel store boxes per half tile: the warp's 4 KB of staging
+    // slots hold them, 512-byte aligned (the stages before them are multiples
+    // of 1 KB with bf16 weights); rope regions start on 64-channel boundaries.
+    p.half_store = p.split_half && !mxw && a.Dr % 32 == 0 && BN / 2 == 128 && a.Dn % 64 == 0 && D % 64 == 0 &&
+                   p.nslots * p.slot_bytes == 4096;
 
     const size_t fixed = 1024 /* alignment slack */ + 256 /* barriers + slots */ +
                          (size_t)kEpiWarps * p.nslots * p.slot_bytes;
@@ -1082,11 +1130,17 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     if (a.Dr == 0)  // plain GEMM: every unit is a pass-through unit
         return mxw ? launch_variant<true, false, 0>(ta, tb, tc, p, grid, smem, stream)
                    : launch_variant<false, false, 0>(ta, tb, tc, p, grid, smem, stream);
+    // the half-tile stores: 64 channels x 32 tokens, 64-byte swizzle
+    alignas(64) CUtensorMap td = tc;
+    if (p.half_store) {
+        st = make_tmap_2d(&td, a.q_out, 0, (uint64_t)N, (uint64_t)a.T, (uint64_t)N, 64, 32, false, true);
+        if (st != MLA_OK) return st;
+    }
     if (mxw)
-        return mxo ? launch_dr<true, true>(a.Dr, ta, tb, tc, p, grid, smem, stream)
-                   : launch_dr<true, false>(a.Dr, ta, tb, tc, p, grid, smem, stream);
-    return mxo ? launch_dr<false, true>(a.Dr, ta, tb, tc, p, grid, smem, stream)
-               : launch_dr<false, false>(a.Dr, ta, tb, tc, p, grid, smem, stream);
+        return mxo ? launch_dr<true, true>(a.Dr, ta, tb, tc, td, p, grid, smem, stream)
+                   : launch_dr<true, false>(a.Dr, ta, tb, tc, td, p, grid, smem, stream);
+    return mxo ? launch_dr<false, true>(a.Dr, ta, tb, tc, td, p, grid, smem, stream)
+               : launch_dr<false, false>(a.Dr, ta, tb, tc, td, p, grid, smem, stream);
 }
 
 }  // namespace mlaq

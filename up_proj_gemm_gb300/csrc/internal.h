@@ -19,11 +19,11 @@ int current_device_info(DeviceInfo* out);  // returns an mla status
 
 // cuTensorMapEncodeTiled, resolved through the runtime's driver entry point.
 // 2-D, row-major tensor: dims {inner, outer}, row pitch in bytes, box
-// {box_inner, box_outer}, 128-byte swizzle when swizzle128 else none.
-// dtype: 0 = uint8, 1 = bf16.
+// {box_inner, box_outer}, 128-byte swizzle when swizzle128 (64-byte
+// swizzle when swizzle64), else none. dtype: 0 = uint8, 1 = bf16.
 int make_tmap_2d(void* tmap_out /* CUtensorMap, 64 B aligned */, const void* base, int dtype,
                  uint64_t inner, uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner,
-                 uint32_t box_outer, bool swizzle128);
+                 uint32_t box_outer, bool swizzle128, bool swizzle64 = false);
 
 // 3-D view of a row-major bf16 matrix [rows, cols] as 64-column chunks:
 // dims {64, rows, cols / 64} with strides {row pitch, 128 bytes}; a box
