@@ -22,12 +22,16 @@
 //     token row of the tile (tcgen05.ld 32x32b) for half of its columns,
 //     adds the bias, applies the rotate-half RoPE pair (i, i+Dr/2)
 //     thread-locally, and converts to bf16 or MXFP8 (per-32-channel amax ->
-//     E8M0 scale -> E4M3 codes). The values pass through a ring of
-//     shared-memory slots and leave as TMA tile stores into a fresh output.
-//     The next tile's main loop runs in the other accumulator buffer
-//     meanwhile.
+//     E8M0 scale -> E4M3 codes). The values pass through shared-memory
+//     staging slots and leave as TMA tile stores into a fresh output (one
+//     store box per 32-channel block, or per 64 channels when the two warps
+//     of a quadrant take the tile's two halves). The next tile's main loop
+//     runs in the other accumulator buffer meanwhile;
+//   * warp 10 (MXFP8 weights, pre-tiled scales): the scale bulk copies.
 //
 // Tiles never split a rope region or an MXFP8 block (the host picks BN so).
+// With Dr = 0 the kernel is a plain GEMM on 256-token tiles (two M = 128
+// MMAs per K step into one accumulator pair), used by the MXFP8 backward.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -61,9 +65,9 @@ constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, splitting the tile'
 // Output staging slot: one TMA store box of 32 token rows. bf16 output: 16
 // channels (32 bytes a row); MXFP8 output: one 32-channel block (32 bytes a
 // row), or 16 channels (16 bytes a row) when Dr = 16, whose rope part is a
-// 16-channel block. The TMA unit of an SM
-// handles a fixed number of tile operations per second whatever their size,
-// so the MXFP8 forward's q stores (one per block instead of two) matter.
+// 16-channel block. The TMA unit of an SM handles a fixed number of tile
+// operations per second whatever their size, so the number of q stores
+// matters (hence also the 64-channel boxes of the half-tile split).
 template <bool MXOUT, int DR>
 __host__ __device__ constexpr int slot_ch() {
     return (MXOUT && DR % 32 == 0) ? 32 : 16;
