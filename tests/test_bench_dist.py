@@ -51,3 +51,14 @@ def test_two_rank_max_and_aggregate():
 def test_single_process_helpers():
     assert bench.reduce_max([1.5, 2.5], 1) == [1.5, 2.5]
     assert bench.aggregate(1.0, 1e12, 1) == pytest.approx(1000.0)
+
+
+def test_tensor_peak_follows_how_the_step_ran():
+    """Short region at full clocks: burst; long region or power cap: sustained."""
+    pk = {"bf16_tflops": 1910.7, "bf16_tflops_sustained": 1710.9}
+    full = {"reasons": []}
+    capped = {"reasons": ["sw_power_cap"]}
+    assert bench.tensor_peak_for(pk, 0.05, full) == (1910.7, False)
+    assert bench.tensor_peak_for(pk, 0.05, capped) == (1710.9, True)
+    assert bench.tensor_peak_for(pk, 1.2, full) == (1710.9, True)
+    assert bench.tensor_peak_for(pk, 0.499, None) == (1910.7, False)
