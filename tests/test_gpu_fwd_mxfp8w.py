@@ -135,12 +135,18 @@ TILED_CASES = [
     ("dsv3_fwd_mxfp8w", dict(T=520, H=5, K=512), "bf16", True),
     ("tiny", dict(T=390, K=256, H=8, Dn=64, Dr=32), "mxfp8", False),        # Dr = 32
     ("tiny", dict(T=1, K=128, H=4), "mxfp8", True),                         # one token, Dr = 16
+    # weight scales resident in TMEM per channel tile, CTAs on contiguous tile ranges:
+    ("dsv3_fwd_mxfp8w", dict(T=2000, H=24), "mxfp8", True),      # 384 tiles: ranges cross channel tiles
+    ("dsv3_fwd_mxfp8w", dict(T=130, H=200, K=512), "mxfp8", True),  # K steps = stages, 2 token tiles
+    ("dsv3_fwd_mxfp8w", dict(T=700, H=40, K=1792), "mxfp8_bhsd", False),  # 14 K steps: the most held
+    ("dsv3_fwd_mxfp8w", dict(T=300, H=40, K=1920), "bf16", True),   # 15 K steps: scales per stage again
 ]
 
 
 @pytest.mark.parametrize("name,ov,out_mode,packed", TILED_CASES)
 def test_fwd_tiled_scales_every_mode(cuda_device, name, ov, out_mode, packed):
-    """The tiled-scale forward (three bulk copies of scale tiles per stage)
+    """The tiled-scale forward (bulk copies of scale tiles; the weight scales
+    kept in TMEM across a CTA's tiles of one channel tile when they fit)
     equals the per-row-gather forward, which test_fwd_mxfp8_weights checks
     against the oracle, for every output mode, both table layouts and
     ragged token counts."""

@@ -94,6 +94,12 @@ struct FwdParams {
     int num_n_tiles;
     uint32_t sf_stage;    // scale staging bytes per stage (MXFP8 weights)
     uint32_t sf_cols;     // TMEM scale-factor columns per stage
+    int contig;           // each CTA takes one contiguous range of tiles (else strided)
+    int sfb_res;          // (tiled MXFP8 scales, 128-row tiles) the weight scales of the
+                          // current channel tile stay in TMEM: copied in on the CTA's first
+                          // tile of that channel tile only, K step kt at column sfb_col(kt)
+    int sfb_n1;           //   K steps held in the columns [BN, 256) between the accumulators
+    int sfb_col2;         //   first column for the K steps after those (after the x scales)
     int half_store;       // (with split_half, MXFP8 q) 64-channel store boxes, two per half tile
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
                           // write each row's scale bytes as one 4-byte word (else: units
@@ -401,18 +407,21 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
 // Tile order: tiles are strided over the CTAs, so the CTAs running together
 // take consecutive tiles. The query side numbers them token tile fastest,
 // the KV side (kv_tile) the same: the tiles of a wave share a few heads'
-// rows of W, which stay in L2 while the outputs stream past.
+// rows of W, which stay in L2 while the outputs stream past. With resident
+// weight scales (sfb_res) each CTA instead takes one contiguous range of
+// tiles, so that it keeps a channel tile for up to num_m_tiles tiles in a
+// row (W and x then sit in L2 whole: the range order costs no DRAM reads).
 template <bool KV>
-__device__ __forceinline__ int tile_first(const FwdParams&) {
-    return (int)blockIdx.x;
+__device__ __forceinline__ int tile_first(const FwdParams& p) {
+    return p.contig ? (int)((int64_t)blockIdx.x * p.num_tiles / gridDim.x) : (int)blockIdx.x;
 }
 template <bool KV>
 __device__ __forceinline__ int tile_end(const FwdParams& p) {
-    return p.num_tiles;
+    return p.contig ? (int)((int64_t)(blockIdx.x + 1) * p.num_tiles / gridDim.x) : p.num_tiles;
 }
 template <bool KV>
-__device__ __forceinline__ int tile_next(int tile) {
-    return tile + (int)gridDim.x;
+__device__ __forceinline__ int tile_next(const FwdParams& p, int tile) {
+    return tile + (p.contig ? 1 : (int)gridDim.x);
 }
 // KV tile -> (token tile, head)
 __device__ __forceinline__ void kv_tile(const FwdParams& p, int tile, int& mt, int& h) {
@@ -495,7 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // x's row tiles are re-read for every channel tile (keep them in L2),
         // except in the plain GEMM, whose large A operand streams through once
         const uint64_t a_pol = (DR == 0 && !KV) ? l2_evict_first_policy() : l2_evict_last_policy();
-        for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile)) {
+        int prev_nt = -1;
+        for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile)) {
             int mt, nt;
             if (KV) {
                 kv_tile(p, tile, mt, nt);
@@ -503,7 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 q_tile<DR>(p, tile, mt, nt);
             }
             const bool a_hi = (int64_t)mt * BM + kBM < p.T;
-            const uint32_t tx = p.tx_bytes - ((M2 && MXW && p.sf_tiled && !a_hi) ? 512u : 0u);
+            // resident weight scales: none to load while the channel tile stays
+            const bool sfb_keep = MXW && p.sfb_res && nt == prev_nt;
+            prev_nt = nt;
+            const uint32_t tx = p.tx_bytes - ((M2 && MXW && p.sf_tiled && !a_hi) ? 512u : 0u) -
+                                (sfb_keep ? 512u * (uint32_t)p.sf_nsub : 0u);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                     ok = false;
@@ -560,10 +574,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0;
             uint32_t ph = 0, issued_mask = 0, issued_par = 0;
             bool ok = true;
-            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile)) {
+            int prev_nt = -1;
+            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile)) {
                 int mt, nt;
                 q_tile<DR>(p, tile, mt, nt);
                 const bool a_hi = (int64_t)mt * BM + kBM < p.T;
+                const bool sfb_keep = p.sfb_res && nt == prev_nt;  // (same rule as warp 0)
+                prev_nt = nt;
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
                     if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                         ok = false;
@@ -574,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (M2 && a_hi)  // the second 128-row chunk, when it holds rows below T
                         bulk_load(sm.sfa(s) + 512u, p.x_scales + ((int64_t)(2 * mt + 1) * p.k_tiles + kt) * 512, 512u,
                                   sm.full(s));
-                    for (int c = 0; c < p.sf_nsub; ++c)
+                    for (int c = 0; c < (sfb_keep ? 0 : p.sf_nsub); ++c)
                         bulk_load(sm.sfb(s) + 512u * c,
                                   p.w_scales + (((int64_t)nt * p.sf_nsub + c) * p.k_tiles + kt) * 512, 512u,
                                   sm.full(s));
@@ -601,9 +618,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             int local = 0;
             bool ok = true;
-            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(tile), ++local) {
+            int prev_nt = -1;
+            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile), ++local) {
                 const int b = M2 ? 0 : (local & 1);
                 const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
+                // Resident weight scales: copied into TMEM on the first tile of a
+                // channel tile only. A K step's columns are next rewritten k_tiles
+                // >= stages steps later, after the full barrier of that step, which
+                // follows the empty-barrier commit of every MMA that read them.
+                bool sfb_keep = false;
+                if (MXW && !KV && p.sfb_res) {
+                    int mt_r, nt_r;
+                    q_tile<DR>(p, tile, mt_r, nt_r);
+                    sfb_keep = nt_r == prev_nt;
+                    prev_nt = nt_r;
+                }
                 if (!mbar_wait(sm.tempty(b), (use & 1u) ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -620,10 +649,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (MXW) {
                         if (!p.sf_tiled) fence_proxy_async_smem();  // gathered bytes came through the generic proxy
                         const uint32_t sfa_col = tmem_base + kSfCol0 + p.sf_cols * s;
-                        const uint32_t sfb_col = sfa_col + (M2 ? 8 : 4);
+                        const uint32_t sfb_col =
+                            !p.sfb_res ? sfa_col + (M2 ? 8 : 4)
+                            : tmem_base + (kt < p.sfb_n1 ? (uint32_t)(p.BN + 8 * kt)
+                                                         : (uint32_t)(p.sfb_col2 + 8 * (kt - p.sfb_n1)));
                         tmem_cp_32x128b_warpx4(sfa_col, smem_desc(sm.sfa(s), 0, 128, kLayoutNone));
                         if (M2) tmem_cp_32x128b_warpx4(sfa_col + 4, smem_desc(sm.sfa(s) + 512, 0, 128, kLayoutNone));
-                        for (int c = 0; c < (p.BN + 127) / 128; ++c)
+                        for (int c = 0; c < (sfb_keep ? 0 : (p.BN + 127) / 128); ++c)
                             tmem_cp_32x128b_warpx4(sfb_col + 4 * c,
                                                    smem_desc(sm.sfb(s) + 512 * c, 0, 128, kLayoutNone));
 #pragma unroll
@@ -675,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slab = ring + 2u * 2048u;
         int slot = 0, cur_mt = -1;
         int local = 0;
-        for (int tile = tile_first<KV>(p); tile < tile_end<KV>(p); tile = tile_next<KV>(tile), ++local) {
+        for (int tile = tile_first<KV>(p); tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile), ++local) {
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             int mt, h;
@@ -760,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ec.prev2_pieces = 0;
         const int half = ew >> 2;   // which of the tile's units this warp takes (alternating)
         int local = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+        for (int tile = tile_first<false>(p); tile < tile_end<false>(p); tile = tile_next<false>(p, tile), ++local) {
             const int b = M2 ? 0 : (local & 1);
             const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
@@ -1114,6 +1146,23 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     if (stages < 2) return MLA_ERR_UNSUPPORTED;
     if (mxw && kSfCol0 + p.sf_cols * (uint32_t)stages > kTmemCols) stages = (kTmemCols - kSfCol0) / p.sf_cols;
     p.stages = stages;
+    // Resident weight scales (MXFP8 weights, tiled scales, 128-row tiles): 8
+    // TMEM columns per K step, first in the columns between the accumulators
+    // ([BN, 256); accumulator 1 ends at 256 + BN <= kSfCol0), then after the
+    // x scales, which keep 4 columns per stage. Each CTA then takes one range
+    // of tiles, token tile fastest, so it keeps a channel tile for up to
+    // num_m_tiles tiles.
+    if (mxw && a.sf_tiled && bm == kBM && BN <= 192 && p.k_tiles >= stages) {
+        const int n1 = (256 - BN) / 8;
+        const int col2 = (int)kSfCol0 + 4 * stages;
+        if (p.k_tiles <= n1 + ((int)kTmemCols - col2) / 8) {
+            p.sfb_res = 1;
+            p.contig = 1;
+            p.sf_cols = 4;
+            p.sfb_n1 = n1;
+            p.sfb_col2 = col2;
+        }
+    }
     const size_t smem = fixed + (size_t)stages * per_stage;
 
     alignas(64) CUtensorMap ta, tb;
