@@ -140,14 +140,17 @@ TILED_CASES = [
     ("dsv3_fwd_mxfp8w", dict(T=130, H=200, K=512), "mxfp8", True),  # K steps = stages, 2 token tiles
     ("dsv3_fwd_mxfp8w", dict(T=700, H=40, K=1792), "mxfp8_bhsd", False),  # 14 K steps: the most held
     ("dsv3_fwd_mxfp8w", dict(T=300, H=40, K=1920), "bf16", True),   # 15 K steps: scales per stage again
+    ("dsv3_fwd_mxfp8w", dict(T=900, H=30, K=1408), "mxfp8", True),  # 11 K steps, 8 token tiles (ragged)
+    ("dsv3_fwd_mxfp8w", dict(T=640, H=34, K=1664), "mxfp8_bhsd_swizzled", True),  # 13 K steps
 ]
 
 
 @pytest.mark.parametrize("name,ov,out_mode,packed", TILED_CASES)
 def test_fwd_tiled_scales_every_mode(cuda_device, name, ov, out_mode, packed):
-    """The tiled-scale forward (bulk copies of scale tiles; the weight scales
-    kept in TMEM across a CTA's tiles of one channel tile when they fit)
-    equals the per-row-gather forward, which test_fwd_mxfp8_weights checks
+    """The tiled-scale forward (bulk copies of scale tiles; when they fit, the
+    weight scales kept in TMEM across a CTA's tiles of one channel tile and
+    each tile's x scales fetched in one copy) equals the per-row-gather
+    forward, which test_fwd_mxfp8_weights checks
     against the oracle, for every output mode, both table layouts and
     ragged token counts."""
     w = synth.workload(name, **ov)

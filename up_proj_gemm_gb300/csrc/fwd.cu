@@ -100,6 +100,9 @@ struct FwdParams {
                           // tile of that channel tile only, K step kt at column sfb_col(kt)
     int sfb_n1;           //   K steps held in the columns [BN, 256) between the accumulators
     int sfb_col2;         //   first column for the K steps after those (after the x scales)
+                          //   With sfb_res the x scales of a tile come in one bulk copy (all
+                          //   its K steps, contiguous in the tiled order) into one of two
+                          //   shared-memory buffers, so that a stage is two TMA operations.
     int half_store;       // (with split_half, MXFP8 q) 64-channel store boxes, two per half tile
     int split_half;       // the two warps of a lane quadrant take the tile's two halves and
                           // write each row's scale bytes as one 4-byte word (else: units
@@ -129,6 +132,7 @@ struct FwdParams {
 struct Smem {
     uint32_t base;      // shared address of stage 0 (1024-aligned)
     uint32_t sf;        // scale staging (MXFP8 weights)
+    uint32_t sfx;       // (sfb_res) the two x-scale tile buffers, k_tiles * 512 bytes each
     uint32_t out;       // output staging: kEpiWarps x nslots slots
     uint32_t bars;      // mbarriers
     int S;
@@ -142,6 +146,8 @@ struct Smem {
     __device__ uint32_t tfull(int b) const { return bars + 8u * (2 * S + b); }
     __device__ uint32_t tempty(int b) const { return bars + 8u * (2 * S + 2 + b); }
     __device__ uint32_t drain() const { return bars + 8u * (2 * S + 4); }
+    __device__ uint32_t xfull(int b) const { return bars + 8u * (2 * S + 5 + b); }
+    __device__ uint32_t xempty(int b) const { return bars + 8u * (2 * S + 7 + b); }
 };
 
 // ------------------------------------------------------------ epilogue parts
@@ -458,10 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.base = (raw + 1023u) & ~1023u;
     sm.sf = sm.base + (uint32_t)p.stages * p.stage_bytes;
     sm.sf_stage = p.sf_stage;
-    sm.sfb_off = M2 ? 1024u : 512u;
-    sm.out = sm.sf + (MXW ? (uint32_t)p.stages * p.sf_stage : 0u);
+    sm.sfb_off = M2 ? 1024u : (p.sfb_res ? 0u : 512u);  // resident mode: stages stage only W's scales
+    sm.sfx = sm.sf + (MXW ? (uint32_t)p.stages * p.sf_stage : 0u);
+    sm.out = sm.sfx + (MXW && p.sfb_res ? 2u * 512u * (uint32_t)p.k_tiles : 0u);
     sm.bars = sm.out + (uint32_t)(kEpiWarps * p.nslots) * p.slot_bytes;
-    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (2 * p.stages + 5);
+    uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (2 * p.stages + 9);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 4);
 
@@ -478,6 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sm.tempty(b), kEpiWarps);
         }
         mbar_init(sm.drain(), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sm.xfull(b), 1);
+            mbar_init(sm.xempty(b), 1);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -516,15 +527,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // resident weight scales: none to load while the channel tile stays
             const bool sfb_keep = MXW && p.sfb_res && nt == prev_nt;
             prev_nt = nt;
-            const uint32_t tx = p.tx_bytes - ((M2 && MXW && p.sf_tiled && !a_hi) ? 512u : 0u) -
-                                (sfb_keep ? 512u * (uint32_t)p.sf_nsub : 0u);
+            const uint32_t tx = p.tx_bytes - ((M2 && MXW && p.sf_tiled && !a_hi) ? 512u : 0u);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
                 if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(sm.full(s), tx);
+                    // resident weight scales: the weight-scale bytes on a channel tile's first
+                    // tile only; the x scales come on their own barrier
+                    mbar_arrive_expect_tx(
+                        sm.full(s), (MXW && p.sfb_res) ? p.stage_bytes + (sfb_keep ? 0u : 512u * (uint32_t)p.sf_nsub)
+                                                       : tx);
                     // x / W tiles: inner coordinate is the K element index
                     const int kc = kt * (MXW ? 128 : 64);
                     tma_load_2d_hint(sm.a(s, p), &tmA, kc, mt * BM, sm.full(s), a_pol);
@@ -570,24 +584,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         // chunk of each operand), issued by a second thread so that warp 0
         // issues only the two operand tiles per stage. The copies complete
         // on the stage's full barrier, whose expected bytes warp 0 posts.
+        // With resident weight scales, W's scale tiles come on a channel
+        // tile's first tile only, and the x scales of a whole tile in one
+        // bulk copy into x-scale buffer (local tile & 1), on its own barrier.
         if (MXW && p.sf_tiled && lane == 0) {
             int s = 0;
             uint32_t ph = 0, issued_mask = 0, issued_par = 0;
+            uint32_t x_issued = 0, x_par = 0;
             bool ok = true;
-            int prev_nt = -1;
-            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile)) {
+            int prev_nt = -1, local = 0;
+            const uint32_t xbytes = 512u * (uint32_t)p.k_tiles;
+            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile), ++local) {
                 int mt, nt;
                 q_tile<DR>(p, tile, mt, nt);
                 const bool a_hi = (int64_t)mt * BM + kBM < p.T;
                 const bool sfb_keep = p.sfb_res && nt == prev_nt;  // (same rule as warp 0)
                 prev_nt = nt;
+                if (p.sfb_res) {
+                    const int xb = local & 1;
+                    const uint32_t xu = (uint32_t)(local >> 1);
+                    if (!mbar_wait(sm.xempty(xb), (xu & 1u) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(sm.xfull(xb), xbytes);
+                    bulk_load(sm.sfx + (uint32_t)xb * xbytes, p.x_scales + (int64_t)mt * p.k_tiles * 512, xbytes,
+                              sm.xfull(xb));
+                    x_issued |= 1u << xb;
+                    x_par = (x_par & ~(1u << xb)) | ((xu & 1u) << xb);
+                }
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
                     if (!mbar_wait(sm.empty(s), ph ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    bulk_load(sm.sfa(s), p.x_scales + ((int64_t)(M2 ? 2 * mt : mt) * p.k_tiles + kt) * 512, 512u,
-                              sm.full(s));
+                    if (!p.sfb_res)
+                        bulk_load(sm.sfa(s), p.x_scales + ((int64_t)(M2 ? 2 * mt : mt) * p.k_tiles + kt) * 512,
+                                  512u, sm.full(s));
                     if (M2 && a_hi)  // the second 128-row chunk, when it holds rows below T
                         bulk_load(sm.sfa(s) + 512u, p.x_scales + ((int64_t)(2 * mt + 1) * p.k_tiles + kt) * 512, 512u,
                                   sm.full(s));
@@ -608,17 +641,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q = 0; q < p.stages; ++q)
                     if (issued_mask & (1u << q))
                         mbar_wait(sm.full(q), (issued_par >> q) & 1u, nullptr, 200000000ull);
+                for (int q = 0; q < 2; ++q)
+                    if (x_issued & (1u << q)) mbar_wait(sm.xfull(q), (x_par >> q) & 1u, nullptr, 200000000ull);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
+        // One thread issues every tcgen05 op of the CTA, and its own instruction
+        // count per K step shows in the tensor pipe's idle time (the pipe runs
+        // only a few ops ahead of it): the shared-memory descriptors are built
+        // once and advanced by adding to their start-address field (address / 16,
+        // 14 bits: shared addresses stay below 2^18, so the field never carries).
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             int local = 0;
             bool ok = true;
             int prev_nt = -1;
+            const uint64_t da0 = desc_kmajor_sw128(sm.a(0, p)), db0 = desc_kmajor_sw128(sm.b(0, p));
+            const uint64_t ds0 = smem_desc(sm.sfa(0), 0, 128, kLayoutNone);
+            const uint64_t dop = p.stage_bytes >> 4, dsf = p.sf_stage >> 4, dsfb = sm.sfb_off >> 4;
+            uint64_t da = da0, db = db0, ds = ds0;  // stage s's A, B and scale descriptors
+            const uint32_t idesc = p.idesc;
+            const int nsub = (p.BN + 127) / 128;
+            const uint32_t xbytes = 512u * (uint32_t)p.k_tiles;
             for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile), ++local) {
                 const int b = M2 ? 0 : (local & 1);
                 const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
@@ -637,50 +684,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                // resident weight scales: the tile's x scales, one buffer of K steps
+                const int xb = local & 1;
+                uint64_t dsx = 0;
+                if (MXW && !KV && p.sfb_res) {
+                    if (!mbar_wait(sm.xfull(xb), (uint32_t)(local >> 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    dsx = smem_desc(sm.sfx + (uint32_t)xb * xbytes, 0, 128, kLayoutNone);
+                }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)b * kAccStride;
+                uint32_t sfb_res_col = tmem_base + (uint32_t)p.BN;  // K step kt's weight-scale columns
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
                     if (!mbar_wait(sm.full(s), ph, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
                     if (MXW) {
                         if (!p.sf_tiled) fence_proxy_async_smem();  // gathered bytes came through the generic proxy
                         const uint32_t sfa_col = tmem_base + kSfCol0 + p.sf_cols * s;
-                        const uint32_t sfb_col =
-                            !p.sfb_res ? sfa_col + (M2 ? 8 : 4)
-                            : tmem_base + (kt < p.sfb_n1 ? (uint32_t)(p.BN + 8 * kt)
-                                                         : (uint32_t)(p.sfb_col2 + 8 * (kt - p.sfb_n1)));
-                        tmem_cp_32x128b_warpx4(sfa_col, smem_desc(sm.sfa(s), 0, 128, kLayoutNone));
-                        if (M2) tmem_cp_32x128b_warpx4(sfa_col + 4, smem_desc(sm.sfa(s) + 512, 0, 128, kLayoutNone));
-                        for (int c = 0; c < (sfb_keep ? 0 : (p.BN + 127) / 128); ++c)
-                            tmem_cp_32x128b_warpx4(sfb_col + 4 * c,
-                                                   smem_desc(sm.sfb(s) + 512 * c, 0, 128, kLayoutNone));
+                        const uint32_t sfb_col = p.sfb_res ? sfb_res_col : sfa_col + (M2 ? 8u : 4u);
+                        tmem_cp_32x128b_warpx4(sfa_col, p.sfb_res ? dsx : ds);
+                        if (M2) tmem_cp_32x128b_warpx4(sfa_col + 4u, ds + 32u);
+                        for (int c = 0; c < (sfb_keep ? 0 : nsub); ++c)
+                            tmem_cp_32x128b_warpx4(sfb_col + 4u * c, ds + dsfb + 32u * (uint32_t)c);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint32_t id = p.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
+                            const uint32_t id = idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
 #pragma unroll
                             for (int hm = 0; hm < (M2 ? 2 : 1); ++hm)
-                                mma_mxf8(d_tmem + hm * kAccStride, desc_kmajor_sw128(a0 + hm * 16384u + 32 * j),
-                                         desc_kmajor_sw128(b0 + 32 * j), id, sfa_col + 4 * hm, sfb_col, (kt | j) != 0);
+                                mma_mxf8(d_tmem + hm * kAccStride, da + 1024u * hm + 2u * j, db + 2u * j, id,
+                                         sfa_col + 4 * hm, sfb_col, (kt | j) != 0);
                         }
+                        dsx += 32u;  // the next K step's 512 bytes
+                        sfb_res_col = kt + 1 == p.sfb_n1 ? tmem_base + (uint32_t)p.sfb_col2 : sfb_res_col + 8u;
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
 #pragma unroll
                             for (int hm = 0; hm < (M2 ? 2 : 1); ++hm)
-                                mma_bf16(d_tmem + hm * kAccStride, desc_kmajor_sw128(a0 + hm * 16384u + 32 * j),
-                                         desc_kmajor_sw128(b0 + 32 * j), p.idesc, (kt | j) != 0);
+                                mma_bf16(d_tmem + hm * kAccStride, da + 1024u * hm + 2u * j, db + 2u * j, idesc,
+                                         (kt | j) != 0);
                     }
                     mma_commit(sm.empty(s));
-                    if (++s == p.stages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                    const bool wrap = s + 1 == p.stages;
+                    s = wrap ? 0 : s + 1;
+                    ph ^= wrap ? 1u : 0u;
+                    da = wrap ? da0 : da + dop;
+                    db = wrap ? db0 : db + dop;
+                    ds = wrap ? ds0 : ds + dsf;
                 }
-                if (ok) mma_commit(sm.tfull(b));
+                if (ok) {
+                    mma_commit(sm.tfull(b));
+                    if (MXW && !KV && p.sfb_res) mma_commit(sm.xempty(xb));  // the x-scale buffer is read
+                }
             }
             if (!ok) {
                 // unwinding: wait (bounded) for the MMAs already issued
@@ -1149,21 +1209,31 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     // Resident weight scales (MXFP8 weights, tiled scales, 128-row tiles): 8
     // TMEM columns per K step, first in the columns between the accumulators
     // ([BN, 256); accumulator 1 ends at 256 + BN <= kSfCol0), then after the
-    // x scales, which keep 4 columns per stage. Each CTA then takes one range
-    // of tiles, token tile fastest, so it keeps a channel tile for up to
-    // num_m_tiles tiles.
+    // x scales (4 columns per stage from kSfCol0). Each CTA then takes one
+    // range of tiles, token tile fastest, so it keeps a channel tile for up
+    // to num_m_tiles tiles. A tile's x scales come in one bulk copy into one
+    // of two buffers (k_tiles x 512 bytes each), so a stage carries only the
+    // two operand tiles: the SM's TMA unit completes operations at a fixed
+    // rate whatever their size, and that rate paces this main loop.
+    size_t stage_sf = mxw ? p.sf_stage : 0, xbuf = 0;
     if (mxw && a.sf_tiled && bm == kBM && BN <= 192 && p.k_tiles >= stages) {
         const int n1 = (256 - BN) / 8;
         const int col2 = (int)kSfCol0 + 4 * stages;
-        if (p.k_tiles <= n1 + ((int)kTmemCols - col2) / 8) {
+        const uint32_t sfs = 512u * (uint32_t)p.sf_nsub;
+        const size_t xb = 2u * 512u * (size_t)p.k_tiles;
+        if (p.k_tiles <= n1 + ((int)kTmemCols - col2) / 8 &&
+            fixed + (size_t)stages * (p.stage_bytes + sfs) + xb <= (size_t)di.max_smem_optin) {
             p.sfb_res = 1;
             p.contig = 1;
             p.sf_cols = 4;
             p.sfb_n1 = n1;
             p.sfb_col2 = col2;
+            p.sf_stage = sfs;
+            stage_sf = sfs;
+            xbuf = xb;
         }
     }
-    const size_t smem = fixed + (size_t)stages * per_stage;
+    const size_t smem = fixed + (size_t)stages * (p.stage_bytes + stage_sf) + xbuf;
 
     alignas(64) CUtensorMap ta, tb;
     const uint64_t esz = mxw ? 1 : 2;
