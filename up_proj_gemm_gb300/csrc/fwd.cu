@@ -417,17 +417,18 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
 // weight scales (sfb_res) each CTA instead takes one contiguous range of
 // tiles, so that it keeps a channel tile for up to num_m_tiles tiles in a
 // row (W and x then sit in L2 whole: the range order costs no DRAM reads).
-template <bool KV>
+// (STRIDED: an instantiation that never takes ranges, decided at compile time)
+template <bool KV, bool STRIDED = false>
 __device__ __forceinline__ int tile_first(const FwdParams& p) {
-    return p.contig ? (int)((int64_t)blockIdx.x * p.num_tiles / gridDim.x) : (int)blockIdx.x;
+    return (!STRIDED && p.contig) ? (int)((int64_t)blockIdx.x * p.num_tiles / gridDim.x) : (int)blockIdx.x;
 }
-template <bool KV>
+template <bool KV, bool STRIDED = false>
 __device__ __forceinline__ int tile_end(const FwdParams& p) {
-    return p.contig ? (int)((int64_t)(blockIdx.x + 1) * p.num_tiles / gridDim.x) : p.num_tiles;
+    return (!STRIDED && p.contig) ? (int)((int64_t)(blockIdx.x + 1) * p.num_tiles / gridDim.x) : p.num_tiles;
 }
-template <bool KV>
+template <bool KV, bool STRIDED = false>
 __device__ __forceinline__ int tile_next(const FwdParams& p, int tile) {
-    return tile + (p.contig ? 1 : (int)gridDim.x);
+    return tile + ((!STRIDED && p.contig) ? 1 : (int)gridDim.x);
 }
 // KV tile -> (token tile, head)
 __device__ __forceinline__ void kv_tile(const FwdParams& p, int tile, int& mt, int& h) {
@@ -516,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // except in the plain GEMM, whose large A operand streams through once
         const uint64_t a_pol = (DR == 0 && !KV) ? l2_evict_first_policy() : l2_evict_last_policy();
         int prev_nt = -1;
-        for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile)) {
+        for (int tile = tile_first<KV, M2>(p); ok && tile < tile_end<KV, M2>(p); tile = tile_next<KV, M2>(p, tile)) {
             int mt, nt;
             if (KV) {
                 kv_tile(p, tile, mt, nt);
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool a_hi = (int64_t)mt * BM + kBM < p.T;
             // resident weight scales: none to load while the channel tile stays
-            const bool sfb_keep = MXW && p.sfb_res && nt == prev_nt;
+            const bool sfb_keep = MXW && !M2 && p.sfb_res && nt == prev_nt;
             prev_nt = nt;
             const uint32_t tx = p.tx_bytes - ((M2 && MXW && p.sf_tiled && !a_hi) ? 512u : 0u);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
@@ -537,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // resident weight scales: the weight-scale bytes on a channel tile's first
                     // tile only; the x scales come on their own barrier
                     mbar_arrive_expect_tx(
-                        sm.full(s), (MXW && p.sfb_res) ? p.stage_bytes + (sfb_keep ? 0u : 512u * (uint32_t)p.sf_nsub)
+                        sm.full(s), (MXW && !M2 && p.sfb_res) ? p.stage_bytes + (sfb_keep ? 0u : 512u * (uint32_t)p.sf_nsub)
                                                        : tx);
                     // x / W tiles: inner coordinate is the K element index
                     const int kc = kt * (MXW ? 128 : 64);
@@ -594,13 +595,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int prev_nt = -1, local = 0;
             const uint32_t xbytes = 512u * (uint32_t)p.k_tiles;
-            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile), ++local) {
+            for (int tile = tile_first<KV, M2>(p); ok && tile < tile_end<KV, M2>(p); tile = tile_next<KV, M2>(p, tile), ++local) {
                 int mt, nt;
                 q_tile<DR>(p, tile, mt, nt);
                 const bool a_hi = (int64_t)mt * BM + kBM < p.T;
-                const bool sfb_keep = p.sfb_res && nt == prev_nt;  // (same rule as warp 0)
+                const bool sfb_keep = !M2 && p.sfb_res && nt == prev_nt;  // (same rule as warp 0)
                 prev_nt = nt;
-                if (p.sfb_res) {
+                if (!M2 && p.sfb_res) {
                     const int xb = local & 1;
                     const uint32_t xu = (uint32_t)(local >> 1);
                     if (!mbar_wait(sm.xempty(xb), (xu & 1u) ^ 1u, abort_flag)) {
@@ -618,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (!p.sfb_res)
+                    if (M2 || !p.sfb_res)
                         bulk_load(sm.sfa(s), p.x_scales + ((int64_t)(M2 ? 2 * mt : mt) * p.k_tiles + kt) * 512,
                                   512u, sm.full(s));
                     if (M2 && a_hi)  // the second 128-row chunk, when it holds rows below T
@@ -666,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = p.idesc;
             const int nsub = (p.BN + 127) / 128;
             const uint32_t xbytes = 512u * (uint32_t)p.k_tiles;
-            for (int tile = tile_first<KV>(p); ok && tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile), ++local) {
+            for (int tile = tile_first<KV, M2>(p); ok && tile < tile_end<KV, M2>(p); tile = tile_next<KV, M2>(p, tile), ++local) {
                 const int b = M2 ? 0 : (local & 1);
                 const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
                 // Resident weight scales: copied into TMEM on the first tile of a
@@ -674,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // >= stages steps later, after the full barrier of that step, which
                 // follows the empty-barrier commit of every MMA that read them.
                 bool sfb_keep = false;
-                if (MXW && !KV && p.sfb_res) {
+                if (MXW && !KV && !M2 && p.sfb_res) {
                     int mt_r, nt_r;
                     q_tile<DR>(p, tile, mt_r, nt_r);
                     sfb_keep = nt_r == prev_nt;
@@ -687,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // resident weight scales: the tile's x scales, one buffer of K steps
                 const int xb = local & 1;
                 uint64_t dsx = 0;
-                if (MXW && !KV && p.sfb_res) {
+                if (MXW && !KV && !M2 && p.sfb_res) {
                     if (!mbar_wait(sm.xfull(xb), (uint32_t)(local >> 1) & 1u, abort_flag)) {
                         ok = false;
                         break;
@@ -703,31 +704,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    if constexpr (M2) {
+                        // 256-row tiles (the plain GEMM): this per-step sequence measured
+                        // faster here than the prebuilt-descriptor one below (0.892 against
+                        // 0.916 ms for the MXFP8 backward at T = 8192)
+                        const uint32_t a0 = sm.a(s, p), b0 = sm.b(s, p);
+                        if (MXW) {
+                            if (!p.sf_tiled) fence_proxy_async_smem();
+                            const uint32_t sfa_col = tmem_base + kSfCol0 + p.sf_cols * s;
+                            const uint32_t sfb_col = sfa_col + 8u;
+                            tmem_cp_32x128b_warpx4(sfa_col, smem_desc(sm.sfa(s), 0, 128, kLayoutNone));
+                            tmem_cp_32x128b_warpx4(sfa_col + 4, smem_desc(sm.sfa(s) + 512, 0, 128, kLayoutNone));
+                            for (int c = 0; c < (p.BN + 127) / 128; ++c)
+                                tmem_cp_32x128b_warpx4(sfb_col + 4 * c,
+                                                       smem_desc(sm.sfb(s) + 512 * c, 0, 128, kLayoutNone));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t id = p.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
+#pragma unroll
+                                for (int hm = 0; hm < 2; ++hm)
+                                    mma_mxf8(d_tmem + hm * kAccStride, desc_kmajor_sw128(a0 + hm * 16384u + 32 * j),
+                                             desc_kmajor_sw128(b0 + 32 * j), id, sfa_col + 4 * hm, sfb_col,
+                                             (kt | j) != 0);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                                for (int hm = 0; hm < 2; ++hm)
+                                    mma_bf16(d_tmem + hm * kAccStride, desc_kmajor_sw128(a0 + hm * 16384u + 32 * j),
+                                             desc_kmajor_sw128(b0 + 32 * j), p.idesc, (kt | j) != 0);
+                        }
+                        mma_commit(sm.empty(s));
+                        if (++s == p.stages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
+                    }
                     if (MXW) {
                         if (!p.sf_tiled) fence_proxy_async_smem();  // gathered bytes came through the generic proxy
                         const uint32_t sfa_col = tmem_base + kSfCol0 + p.sf_cols * s;
-                        const uint32_t sfb_col = p.sfb_res ? sfb_res_col : sfa_col + (M2 ? 8u : 4u);
+                        const uint32_t sfb_col = p.sfb_res ? sfb_res_col : sfa_col + 4u;
                         tmem_cp_32x128b_warpx4(sfa_col, p.sfb_res ? dsx : ds);
-                        if (M2) tmem_cp_32x128b_warpx4(sfa_col + 4u, ds + 32u);
                         for (int c = 0; c < (sfb_keep ? 0 : nsub); ++c)
                             tmem_cp_32x128b_warpx4(sfb_col + 4u * c, ds + dsfb + 32u * (uint32_t)c);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const uint32_t id = idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
-#pragma unroll
-                            for (int hm = 0; hm < (M2 ? 2 : 1); ++hm)
-                                mma_mxf8(d_tmem + hm * kAccStride, da + 1024u * hm + 2u * j, db + 2u * j, id,
-                                         sfa_col + 4 * hm, sfb_col, (kt | j) != 0);
+                            mma_mxf8(d_tmem, da + 2u * j, db + 2u * j, id, sfa_col, sfb_col, (kt | j) != 0);
                         }
                         dsx += 32u;  // the next K step's 512 bytes
                         sfb_res_col = kt + 1 == p.sfb_n1 ? tmem_base + (uint32_t)p.sfb_col2 : sfb_res_col + 8u;
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-#pragma unroll
-                            for (int hm = 0; hm < (M2 ? 2 : 1); ++hm)
-                                mma_bf16(d_tmem + hm * kAccStride, da + 1024u * hm + 2u * j, db + 2u * j, idesc,
-                                         (kt | j) != 0);
+                            mma_bf16(d_tmem, da + 2u * j, db + 2u * j, idesc, (kt | j) != 0);
                     }
                     mma_commit(sm.empty(s));
                     const bool wrap = s + 1 == p.stages;
@@ -739,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ok) {
                     mma_commit(sm.tfull(b));
-                    if (MXW && !KV && p.sfb_res) mma_commit(sm.xempty(xb));  // the x-scale buffer is read
+                    if (MXW && !KV && !M2 && p.sfb_res) mma_commit(sm.xempty(xb));  // the x-scale buffer is read
                 }
             }
             if (!ok) {
@@ -767,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slab = ring + 2u * 2048u;
         int slot = 0, cur_mt = -1;
         int local = 0;
-        for (int tile = tile_first<KV>(p); tile < tile_end<KV>(p); tile = tile_next<KV>(p, tile), ++local) {
+        for (int tile = tile_first<KV, M2>(p); tile < tile_end<KV, M2>(p); tile = tile_next<KV, M2>(p, tile), ++local) {
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             int mt, h;
@@ -852,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ec.prev2_pieces = 0;
         const int half = ew >> 2;   // which of the tile's units this warp takes (alternating)
         int local = 0;
-        for (int tile = tile_first<false>(p); tile < tile_end<false>(p); tile = tile_next<false>(p, tile), ++local) {
+        for (int tile = tile_first<false, M2>(p); tile < tile_end<false, M2>(p); tile = tile_next<false, M2>(p, tile), ++local) {
             const int b = M2 ? 0 : (local & 1);
             const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
