@@ -417,7 +417,9 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
 // weight scales (sfb_res) each CTA instead takes one contiguous range of
 // tiles, so that it keeps a channel tile for up to num_m_tiles tiles in a
 // row (W and x then sit in L2 whole: the range order costs no DRAM reads).
-// (STRIDED: an instantiation that never takes ranges, decided at compile time)
+// (STRIDED: an instantiation that never takes ranges, decided at compile time:
+// ranges come only with resident weight scales, so with MXFP8 weights and
+// 128-row tiles)
 template <bool KV, bool STRIDED = false>
 __device__ __forceinline__ int tile_first(const FwdParams& p) {
     return (!STRIDED && p.contig) ? (int)((int64_t)blockIdx.x * p.num_tiles / gridDim.x) : (int)blockIdx.x;
@@ -517,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // except in the plain GEMM, whose large A operand streams through once
         const uint64_t a_pol = (DR == 0 && !KV) ? l2_evict_first_policy() : l2_evict_last_policy();
         int prev_nt = -1;
-        for (int tile = tile_first<KV, M2>(p); ok && tile < tile_end<KV, M2>(p); tile = tile_next<KV, M2>(p, tile)) {
+        for (int tile = tile_first<KV, M2 || !MXW>(p); ok && tile < tile_end<KV, M2 || !MXW>(p); tile = tile_next<KV, M2 || !MXW>(p, tile)) {
             int mt, nt;
             if (KV) {
                 kv_tile(p, tile, mt, nt);
@@ -595,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int prev_nt = -1, local = 0;
             const uint32_t xbytes = 512u * (uint32_t)p.k_tiles;
-            for (int tile = tile_first<KV, M2>(p); ok && tile < tile_end<KV, M2>(p); tile = tile_next<KV, M2>(p, tile), ++local) {
+            for (int tile = tile_first<KV, M2 || !MXW>(p); ok && tile < tile_end<KV, M2 || !MXW>(p); tile = tile_next<KV, M2 || !MXW>(p, tile), ++local) {
                 int mt, nt;
                 q_tile<DR>(p, tile, mt, nt);
                 const bool a_hi = (int64_t)mt * BM + kBM < p.T;
@@ -667,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = p.idesc;
             const int nsub = (p.BN + 127) / 128;
             const uint32_t xbytes = 512u * (uint32_t)p.k_tiles;
-            for (int tile = tile_first<KV, M2>(p); ok && tile < tile_end<KV, M2>(p); tile = tile_next<KV, M2>(p, tile), ++local) {
+            for (int tile = tile_first<KV, M2 || !MXW>(p); ok && tile < tile_end<KV, M2 || !MXW>(p); tile = tile_next<KV, M2 || !MXW>(p, tile), ++local) {
                 const int b = M2 ? 0 : (local & 1);
                 const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
                 // Resident weight scales: copied into TMEM on the first tile of a
@@ -799,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slab = ring + 2u * 2048u;
         int slot = 0, cur_mt = -1;
         int local = 0;
-        for (int tile = tile_first<KV, M2>(p); tile < tile_end<KV, M2>(p); tile = tile_next<KV, M2>(p, tile), ++local) {
+        for (int tile = tile_first<KV, M2 || !MXW>(p); tile < tile_end<KV, M2 || !MXW>(p); tile = tile_next<KV, M2 || !MXW>(p, tile), ++local) {
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             int mt, h;
@@ -884,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ec.prev2_pieces = 0;
         const int half = ew >> 2;   // which of the tile's units this warp takes (alternating)
         int local = 0;
-        for (int tile = tile_first<false, M2>(p); tile < tile_end<false, M2>(p); tile = tile_next<false, M2>(p, tile), ++local) {
+        for (int tile = tile_first<false, M2 || !MXW>(p); tile < tile_end<false, M2 || !MXW>(p); tile = tile_next<false, M2 || !MXW>(p, tile), ++local) {
             const int b = M2 ? 0 : (local & 1);
             const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
