@@ -94,8 +94,8 @@ struct FwdParams {
     int num_n_tiles;
     uint32_t sf_stage;    // scale staging bytes per stage (MXFP8 weights)
     uint32_t sf_cols;     // TMEM scale-factor columns per stage
-    int contig;           // each CTA takes one contiguous range of tiles (else strided)
-    int sfb_res;          // (tiled MXFP8 scales, 128-row tiles) the weight scales of the
+    int sfb_res;          // (tiled MXFP8 scales, 128-row tiles; launches the RES variant, whose
+                          // CTAs take contiguous tile ranges) the weight scales of the
                           // current channel tile stay in TMEM: copied in on the CTA's first
                           // tile of that channel tile only, K step kt at column sfb_col(kt)
     int sfb_n1;           //   K steps held in the columns [BN, 256) between the accumulators
@@ -417,20 +417,18 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
 // weight scales (sfb_res) each CTA instead takes one contiguous range of
 // tiles, so that it keeps a channel tile for up to num_m_tiles tiles in a
 // row (W and x then sit in L2 whole: the range order costs no DRAM reads).
-// (STRIDED: an instantiation that never takes ranges, decided at compile time:
-// ranges come only with resident weight scales, so with MXFP8 weights and
-// 128-row tiles)
-template <bool KV, bool STRIDED = false>
+// (CONTIG, a compile-time choice: the ranges come with resident weight scales)
+template <bool KV, bool CONTIG>
 __device__ __forceinline__ int tile_first(const FwdParams& p) {
-    return (!STRIDED && p.contig) ? (int)((int64_t)blockIdx.x * p.num_tiles / gridDim.x) : (int)blockIdx.x;
+    return CONTIG ? (int)((int64_t)blockIdx.x * p.num_tiles / gridDim.x) : (int)blockIdx.x;
 }
-template <bool KV, bool STRIDED = false>
+template <bool KV, bool CONTIG>
 __device__ __forceinline__ int tile_end(const FwdParams& p) {
-    return (!STRIDED && p.contig) ? (int)((int64_t)(blockIdx.x + 1) * p.num_tiles / gridDim.x) : p.num_tiles;
+    return CONTIG ? (int)((int64_t)(blockIdx.x + 1) * p.num_tiles / gridDim.x) : p.num_tiles;
 }
-template <bool KV, bool STRIDED = false>
-__device__ __forceinline__ int tile_next(const FwdParams& p, int tile) {
-    return tile + ((!STRIDED && p.contig) ? 1 : (int)gridDim.x);
+template <bool KV, bool CONTIG>
+__device__ __forceinline__ int tile_next(const FwdParams&, int tile) {
+    return tile + (CONTIG ? 1 : (int)gridDim.x);
 }
 // KV tile -> (token tile, head)
 __device__ __forceinline__ void kv_tile(const FwdParams& p, int tile, int& mt, int& h) {
@@ -453,13 +451,16 @@ __device__ __forceinline__ void q_tile(const FwdParams& p, int g, int& mt, int& 
 }
 
 // ------------------------------------------------------------------- kernel
-template <bool MXW, bool MXOUT, int DR, bool KV = false, bool PACKED = false>
+template <bool MXW, bool MXOUT, int DR, bool KV = false, bool PACKED = false, bool RES = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr bool M2 = DR == 0 && !KV;  // 256-row tiles, two accumulators
+    // resident weight scales (the host's sfb_res), with contiguous tile ranges
+    // and per-tile x scales: a compile-time variant
+    constexpr bool RESC = RES && MXW && !KV && !M2;
     constexpr int BM = M2 ? 2 * kBM : kBM;
     const uint32_t raw = smem_u32(smem_raw);
     Smem sm;
@@ -467,9 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.base = (raw + 1023u) & ~1023u;
     sm.sf = sm.base + (uint32_t)p.stages * p.stage_bytes;
     sm.sf_stage = p.sf_stage;
-    sm.sfb_off = M2 ? 1024u : (p.sfb_res ? 0u : 512u);  // resident mode: stages stage only W's scales
+    sm.sfb_off = M2 ? 1024u : (RESC ? 0u : 512u);  // resident mode: stages stage only W's scales
     sm.sfx = sm.sf + (MXW ? (uint32_t)p.stages * p.sf_stage : 0u);
-    sm.out = sm.sfx + (MXW && p.sfb_res ? 2u * 512u * (uint32_t)p.k_tiles : 0u);
+    sm.out = sm.sfx + (RESC ? 2u * 512u * (uint32_t)p.k_tiles : 0u);
     sm.bars = sm.out + (uint32_t)(kEpiWarps * p.nslots) * p.slot_bytes;
     uint8_t* tail = smem_raw + (sm.bars - raw) + 8u * (2 * p.stages + 9);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tail);
@@ -519,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // except in the plain GEMM, whose large A operand streams through once
         const uint64_t a_pol = (DR == 0 && !KV) ? l2_evict_first_policy() : l2_evict_last_policy();
         int prev_nt = -1;
-        for (int tile = tile_first<KV, M2 || !MXW>(p); ok && tile < tile_end<KV, M2 || !MXW>(p); tile = tile_next<KV, M2 || !MXW>(p, tile)) {
+        for (int tile = tile_first<KV, RESC>(p); ok && tile < tile_end<KV, RESC>(p); tile = tile_next<KV, RESC>(p, tile)) {
             int mt, nt;
             if (KV) {
                 kv_tile(p, tile, mt, nt);
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool a_hi = (int64_t)mt * BM + kBM < p.T;
             // resident weight scales: none to load while the channel tile stays
-            const bool sfb_keep = MXW && !M2 && p.sfb_res && nt == prev_nt;
+            const bool sfb_keep = RESC && nt == prev_nt;
             prev_nt = nt;
             const uint32_t tx = p.tx_bytes - ((M2 && MXW && p.sf_tiled && !a_hi) ? 512u : 0u);
             for (int kt = 0; kt < p.k_tiles; ++kt) {
@@ -540,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // resident weight scales: the weight-scale bytes on a channel tile's first
                     // tile only; the x scales come on their own barrier
                     mbar_arrive_expect_tx(
-                        sm.full(s), (MXW && !M2 && p.sfb_res) ? p.stage_bytes + (sfb_keep ? 0u : 512u * (uint32_t)p.sf_nsub)
+                        sm.full(s), RESC ? p.stage_bytes + (sfb_keep ? 0u : 512u * (uint32_t)p.sf_nsub)
                                                        : tx);
                     // x / W tiles: inner coordinate is the K element index
                     const int kc = kt * (MXW ? 128 : 64);
@@ -597,13 +598,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int prev_nt = -1, local = 0;
             const uint32_t xbytes = 512u * (uint32_t)p.k_tiles;
-            for (int tile = tile_first<KV, M2 || !MXW>(p); ok && tile < tile_end<KV, M2 || !MXW>(p); tile = tile_next<KV, M2 || !MXW>(p, tile), ++local) {
+            for (int tile = tile_first<KV, RESC>(p); ok && tile < tile_end<KV, RESC>(p); tile = tile_next<KV, RESC>(p, tile), ++local) {
                 int mt, nt;
                 q_tile<DR>(p, tile, mt, nt);
                 const bool a_hi = (int64_t)mt * BM + kBM < p.T;
-                const bool sfb_keep = !M2 && p.sfb_res && nt == prev_nt;  // (same rule as warp 0)
+                const bool sfb_keep = RESC && nt == prev_nt;  // (same rule as warp 0)
                 prev_nt = nt;
-                if (!M2 && p.sfb_res) {
+                if (RESC) {
                     const int xb = local & 1;
                     const uint32_t xu = (uint32_t)(local >> 1);
                     if (!mbar_wait(sm.xempty(xb), (xu & 1u) ^ 1u, abort_flag)) {
@@ -621,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (M2 || !p.sfb_res)
+                    if (!RESC)
                         bulk_load(sm.sfa(s), p.x_scales + ((int64_t)(M2 ? 2 * mt : mt) * p.k_tiles + kt) * 512,
                                   512u, sm.full(s));
                     if (M2 && a_hi)  // the second 128-row chunk, when it holds rows below T
@@ -669,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = p.idesc;
             const int nsub = (p.BN + 127) / 128;
             const uint32_t xbytes = 512u * (uint32_t)p.k_tiles;
-            for (int tile = tile_first<KV, M2 || !MXW>(p); ok && tile < tile_end<KV, M2 || !MXW>(p); tile = tile_next<KV, M2 || !MXW>(p, tile), ++local) {
+            for (int tile = tile_first<KV, RESC>(p); ok && tile < tile_end<KV, RESC>(p); tile = tile_next<KV, RESC>(p, tile), ++local) {
                 const int b = M2 ? 0 : (local & 1);
                 const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
                 // Resident weight scales: copied into TMEM on the first tile of a
@@ -677,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // >= stages steps later, after the full barrier of that step, which
                 // follows the empty-barrier commit of every MMA that read them.
                 bool sfb_keep = false;
-                if (MXW && !KV && !M2 && p.sfb_res) {
+                if (RESC) {
                     int mt_r, nt_r;
                     q_tile<DR>(p, tile, mt_r, nt_r);
                     sfb_keep = nt_r == prev_nt;
@@ -690,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // resident weight scales: the tile's x scales, one buffer of K steps
                 const int xb = local & 1;
                 uint64_t dsx = 0;
-                if (MXW && !KV && !M2 && p.sfb_res) {
+                if (RESC) {
                     if (!mbar_wait(sm.xfull(xb), (uint32_t)(local >> 1) & 1u, abort_flag)) {
                         ok = false;
                         break;
@@ -747,8 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (MXW) {
                         if (!p.sf_tiled) fence_proxy_async_smem();  // gathered bytes came through the generic proxy
                         const uint32_t sfa_col = tmem_base + kSfCol0 + p.sf_cols * s;
-                        const uint32_t sfb_col = p.sfb_res ? sfb_res_col : sfa_col + 4u;
-                        tmem_cp_32x128b_warpx4(sfa_col, p.sfb_res ? dsx : ds);
+                        const uint32_t sfb_col = RESC ? sfb_res_col : sfa_col + 4u;
+                        tmem_cp_32x128b_warpx4(sfa_col, RESC ? dsx : ds);
                         for (int c = 0; c < (sfb_keep ? 0 : nsub); ++c)
                             tmem_cp_32x128b_warpx4(sfb_col + 4u * c, ds + dsfb + 32u * (uint32_t)c);
 #pragma unroll
@@ -773,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ok) {
                     mma_commit(sm.tfull(b));
-                    if (MXW && !KV && !M2 && p.sfb_res) mma_commit(sm.xempty(xb));  // the x-scale buffer is read
+                    if (RESC) mma_commit(sm.xempty(xb));  // the x-scale buffer is read
                 }
             }
             if (!ok) {
@@ -801,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slab = ring + 2u * 2048u;
         int slot = 0, cur_mt = -1;
         int local = 0;
-        for (int tile = tile_first<KV, M2 || !MXW>(p); tile < tile_end<KV, M2 || !MXW>(p); tile = tile_next<KV, M2 || !MXW>(p, tile), ++local) {
+        for (int tile = tile_first<KV, RESC>(p); tile < tile_end<KV, RESC>(p); tile = tile_next<KV, RESC>(p, tile), ++local) {
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             int mt, h;
@@ -886,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ec.prev2_pieces = 0;
         const int half = ew >> 2;   // which of the tile's units this warp takes (alternating)
         int local = 0;
-        for (int tile = tile_first<false, M2 || !MXW>(p); tile < tile_end<false, M2 || !MXW>(p); tile = tile_next<false, M2 || !MXW>(p, tile), ++local) {
+        for (int tile = tile_first<false, RESC>(p); tile < tile_end<false, RESC>(p); tile = tile_next<false, RESC>(p, tile), ++local) {
             const int b = M2 ? 0 : (local & 1);
             const uint32_t use = M2 ? (uint32_t)local : (uint32_t)(local >> 1);
             if (!mbar_wait(sm.tfull(b), use & 1u, abort_flag)) break;
@@ -950,10 +951,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool MXW, bool MXOUT, int DR, bool PACKED = false>
+template <bool MXW, bool MXOUT, int DR, bool PACKED = false, bool RES = false>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                    const FwdParams& p, int grid, size_t smem, cudaStream_t stream, const CUtensorMap* td = nullptr) {
-    auto kern = fwd_kernel<MXW, MXOUT, DR, false, PACKED>;
+    if constexpr (MXW && !RES && DR != 0) {  // resident weight scales: their own instantiation
+        if (p.sfb_res) return launch_variant<MXW, MXOUT, DR, PACKED, true>(ta, tb, tc, p, grid, smem, stream, td);
+    }
+    auto kern = fwd_kernel<MXW, MXOUT, DR, false, PACKED, RES>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return MLA_ERR_CUDA;
@@ -1258,7 +1262,6 @@ int launch_fwd(const FwdArgs& a, cudaStream_t stream) {
         if (p.k_tiles <= n1 + ((int)kTmemCols - col2) / 8 &&
             fixed + (size_t)stages * (p.stage_bytes + sfs) + xb <= (size_t)di.max_smem_optin) {
             p.sfb_res = 1;
-            p.contig = 1;
             p.sf_cols = 4;
             p.sfb_n1 = n1;
             p.sfb_col2 = col2;
