@@ -192,7 +192,9 @@ __device__ __forceinline__ void add_bias(float* v, int nv, const uint16_t* bias)
 // A lane's 32-byte row of a slot is written as two 16-byte halves, lanes
 // with bit 2 set upper half first, so each store instruction of the warp
 // takes the minimum four shared-memory wavefronts.
-template <bool MXOUT, int NV, int CH>
+// HS: the 64-channel half-tile store boxes (p.half_store), fixed at compile
+// time: the kernel variant launched exactly when p.half_store is set.
+template <bool MXOUT, int NV, int CH, bool HS = false>
 __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
                                           const float (&v)[NV], bool valid, int64_t t, int64_t n, int h,
                                           int cin) {
@@ -200,8 +202,8 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
     constexpr int PIECES = NV / CH;
     const int lane = threadIdx.x & 31;
     const uint32_t h0 = (lane & 4) ? 16u : 0u, h1 = 16u - h0;  // byte offsets of the two halves, in store order
-    if constexpr (MXOUT && CH == 32) {
-        if (p.half_store) {
+    if constexpr (MXOUT && CH == 32 && HS) {
+        {
             // A warp's half tile (128 channels, in column order) leaves in two
             // 64-channel store boxes: two 2 KB slots, rows 64 bytes apart in
             // the 64-byte swizzled order of the store's tensor map (16-byte
@@ -316,7 +318,7 @@ __device__ __forceinline__ void emit_unit(const FwdParams& p, const CUtensorMap*
     c.prev_pieces = PIECES;
 }
 
-template <bool MXOUT, int CH>
+template <bool MXOUT, int CH, bool HS = false>
 __device__ __forceinline__ void nope_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
                                           uint32_t taddr, int col, bool valid, int64_t t, int64_t n, int h,
                                           int cin) {
@@ -328,7 +330,7 @@ __device__ __forceinline__ void nope_unit(const FwdParams& p, const CUtensorMap*
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
     if (c.bias) add_bias(v, 32, c.bias + col);
-    emit_unit<MXOUT, 32, CH>(p, tmC, c, v, valid, t, n, h, cin);
+    emit_unit<MXOUT, 32, CH, HS>(p, tmC, c, v, valid, t, n, h, cin);
 }
 
 __device__ __forceinline__ void load_table8(const float* src, bool vec, float (&o)[8]) {
@@ -354,7 +356,7 @@ __device__ __forceinline__ void rot_pair_fwd(float& a, float& b, float ci, float
 
 // part < 0: this warp emits the whole rope unit; part 0 / 1 (DR = 64): the
 // quadrant's two warps both rotate it and each emits one 32-channel half.
-template <bool MXOUT, int DR, bool PACKED>
+template <bool MXOUT, int DR, bool PACKED, bool HS = false>
 __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap* tmC, EpiCtx& c,
                                           uint32_t taddr, int col, bool valid, int64_t t, int64_t n, int h,
                                           int prow, int part) {
@@ -404,9 +406,9 @@ __device__ __forceinline__ void rope_unit(const FwdParams& p, const CUtensorMap*
         float yb[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) yb[i] = part ? y[(32 + i) % DR] : y[i];
-        emit_unit<MXOUT, 32, slot_ch<MXOUT, DR>()>(p, tmC, c, yb, valid, t, n + 32 * part, h, p.Dn + 32 * part);
+        emit_unit<MXOUT, 32, slot_ch<MXOUT, DR>(), HS>(p, tmC, c, yb, valid, t, n + 32 * part, h, p.Dn + 32 * part);
     } else {
-        emit_unit<MXOUT, DR, slot_ch<MXOUT, DR>()>(p, tmC, c, y, valid, t, n, h, p.Dn);
+        emit_unit<MXOUT, DR, slot_ch<MXOUT, DR>(), HS>(p, tmC, c, y, valid, t, n, h, p.Dn);
     }
 }
 
@@ -451,7 +453,8 @@ __device__ __forceinline__ void q_tile(const FwdParams& p, int g, int& mt, int& 
 }
 
 // ------------------------------------------------------------------- kernel
-template <bool MXW, bool MXOUT, int DR, bool KV = false, bool PACKED = false, bool RES = false>
+template <bool MXW, bool MXOUT, int DR, bool KV = false, bool PACKED = false, bool RES = false,
+          bool HALF = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -461,6 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // resident weight scales (the host's sfb_res), with contiguous tile ranges
     // and per-tile x scales: a compile-time variant
     constexpr bool RESC = RES && MXW && !KV && !M2;
+    // the half-tile split with 64-channel store boxes (p.split_half and
+    // p.half_store set): a compile-time variant as well
+    constexpr bool HS = HALF && !MXW && MXOUT && !KV && DR == 64;
     constexpr int BM = M2 ? 2 * kBM : kBM;
     const uint32_t raw = smem_u32(smem_raw);
     Smem sm;
@@ -910,28 +916,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             ec.t0 = mt * BM + rbase + quad * 32;
             ec.bias = p.bias ? p.bias + n0 : nullptr;
             ec.sword = 0;
-            ec.sbase = (n0 + (p.split_half ? half * (p.BN / 2) : 0)) / 32;
+            const bool split = HS || p.split_half;
+            ec.sbase = (n0 + (split ? half * (p.BN / 2) : 0)) / 32;
             ec.hcol0 = (int32_t)n0 + half * (p.BN / 2);
-            int col = p.split_half ? half * (p.BN / 2) : 0, unit = 0;
-            const int col_end = p.split_half ? col + p.BN / 2 : p.BN;
+            int col = split ? half * (p.BN / 2) : 0, unit = 0;
+            const int col_end = split ? col + p.BN / 2 : p.BN;
             while (col < col_end) {
                 const int n32 = (int)n0 + col;  // channel indices fit in 32 bits (N is an int)
                 const int h = n32 / p.D;
                 const int c = n32 - h * p.D;
                 const int64_t n = n32;
                 const bool nope = c < p.Dn;
-                if (DR == 64 && !nope && !M2 && !p.split_half) {
+                if (DR == 64 && !nope && !M2 && !split) {
                     // units alternate between the quadrant's two warps: both rotate the
                     // rope unit and each writes one half, which balances their work
-                    if constexpr (DR == 64) rope_unit<MXOUT, DR, PACKED>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow, half);
+                    if constexpr (DR == 64) rope_unit<MXOUT, DR, PACKED, HS>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow, half);
                     ++unit;
-                } else if (M2 || p.split_half || (unit++ & 1) == half) {
-                    if (nope) nope_unit<MXOUT, slot_ch<MXOUT, DR>()>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
-                    else if constexpr (DR > 0) rope_unit<MXOUT, DR, PACKED>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow, -1);
+                } else if (M2 || split || (unit++ & 1) == half) {
+                    if (nope) nope_unit<MXOUT, slot_ch<MXOUT, DR>(), HS>(p, &tmC, ec, trow + col, col, valid, t, n, h, c);
+                    else if constexpr (DR > 0) rope_unit<MXOUT, DR, PACKED, HS>(p, &tmC, ec, trow + col, col, valid, t, n, h, prow, -1);
                 }
                 col += nope ? 32 : DR;
             }
-            if (MXOUT && p.split_half && valid)
+            if (MXOUT && split && valid)
                 *reinterpret_cast<uint32_t*>(p.q_scales + t * (p.N / 32) + ec.sbase) = ec.sword;
             tc_fence_before();
             __syncwarp();
@@ -951,13 +958,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool MXW, bool MXOUT, int DR, bool PACKED = false, bool RES = false>
+template <bool MXW, bool MXOUT, int DR, bool PACKED = false, bool RES = false, bool HALF = false>
 int launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                    const FwdParams& p, int grid, size_t smem, cudaStream_t stream, const CUtensorMap* td = nullptr) {
-    if constexpr (MXW && !RES && DR != 0) {  // resident weight scales: their own instantiation
+    // resident weight scales, and the half-tile stores: their own instantiations
+    if constexpr (MXW && !RES && DR != 0) {
         if (p.sfb_res) return launch_variant<MXW, MXOUT, DR, PACKED, true>(ta, tb, tc, p, grid, smem, stream, td);
     }
-    auto kern = fwd_kernel<MXW, MXOUT, DR, false, PACKED, RES>;
+    if constexpr (!MXW && MXOUT && DR == 64 && !HALF) {
+        if (p.half_store) return launch_variant<MXW, MXOUT, DR, PACKED, RES, true>(ta, tb, tc, p, grid, smem, stream, td);
+    }
+    auto kern = fwd_kernel<MXW, MXOUT, DR, false, PACKED, RES, HALF>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return MLA_ERR_CUDA;
