@@ -28,7 +28,9 @@ def _run(inp):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("R,C", [(32, 1), (100, 7), (1536, 64), (4000, 33), (5, 3), (4096, 1536),
-                                 (96, 513), (130, 1025)])
+                                 (96, 513), (130, 1025),
+                                 # code rows 16- but not 32-byte aligned: 16-byte stores instead of 32
+                                 (4016, 64), (48, 300)])
 def test_quantize_cols_matches_oracle(cuda_device, dtype, R, C):
     g = torch.Generator().manual_seed(R * 1000 + C + 1)
     v = torch.randn((R, C), generator=g) * torch.exp2(torch.randint(-20, 20, (1, C), generator=g).float())

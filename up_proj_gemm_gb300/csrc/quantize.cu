@@ -225,8 +225,15 @@ __device__ __forceinline__ void load_pair(const __nv_bfloat16* p, bool both, flo
 }
 
 // One column's block: n valid codes to dst (32-byte run when whole and aligned).
+// V32: dst 32-byte aligned; a whole block leaves in one 32-byte store
+// (`st.global.v8.b32`, sm_100 and later), one full sector per instruction.
+template <bool V32 = false>
 __device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&w)[8], int n, bool vec) {
-    if (vec && n == 32) {
+    if (V32 && n == 32) {
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    } else if (vec && n == 32) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
     } else {
@@ -303,7 +310,8 @@ __host__ __device__ constexpr int cols_cpt() { return sizeof(Tin) == 2 ? 2 : 1; 
 template <typename Tin>
 __host__ __device__ constexpr int cols_threads() { return kColTC / cols_cpt<Tin>(); }
 
-template <typename Tin, bool VEC>
+// V32: ldc % 32 == 0 and codes 32-byte aligned (every block's run is 32-byte aligned)
+template <typename Tin, bool VEC, bool V32 = false>
 __global__ void __launch_bounds__(cols_threads<Tin>()) mxfp8_quantize_cols_tiled(
     const Tin* __restrict__ in, int64_t R, int64_t C, int64_t ld, uint8_t* __restrict__ codes, int64_t ldc,
     uint8_t* __restrict__ scales, int64_t nbr, int64_t sf_group) {
@@ -376,7 +384,7 @@ __global__ void __launch_bounds__(cols_threads<Tin>()) mxfp8_quantize_cols_tiled
                 for (int j = 0; j < CPT; ++j) {
                     uint32_t w[8];
                     const uint32_t sb = quantize_block32(v[j], w);
-                    store_codes(codes + (c + j) * ldc + r0, w, n, VEC);
+                    store_codes<V32>(codes + (c + j) * ldc + r0, w, n, VEC);
                     if (word_scales) sword[j] |= sb << (8 * blk);
                     else scales[(c + j) * nbr + r0 / 32] = (uint8_t)sb;
                 }
@@ -446,12 +454,16 @@ int launch_cols_typed(int64_t R, int64_t C, const void* in, int64_t ld, uint8_t*
         const int64_t cap = (int64_t)di.num_sms * 3;
         if (blocks > cap) blocks = cap;
         const Tin* p = static_cast<const Tin*>(in);
-        const void* k = vec ? (const void*)mxfp8_quantize_cols_tiled<Tin, true>
-                            : (const void*)mxfp8_quantize_cols_tiled<Tin, false>;
+        const bool v32 = vec && (ldc % 32 == 0) && (reinterpret_cast<uintptr_t>(codes) % 32 == 0);
+        const void* k = v32   ? (const void*)mxfp8_quantize_cols_tiled<Tin, true, true>
+                        : vec ? (const void*)mxfp8_quantize_cols_tiled<Tin, true>
+                              : (const void*)mxfp8_quantize_cols_tiled<Tin, false>;
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return MLA_ERR_CUDA;
         constexpr int NT = cols_threads<Tin>();
-        if (vec)
+        if (v32)
+            mxfp8_quantize_cols_tiled<Tin, true, true><<<(unsigned)blocks, NT, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
+        else if (vec)
             mxfp8_quantize_cols_tiled<Tin, true><<<(unsigned)blocks, NT, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
         else
             mxfp8_quantize_cols_tiled<Tin, false><<<(unsigned)blocks, NT, smem, stream>>>(p, R, C, ld, codes, ldc, scales, lds, sf_group);
