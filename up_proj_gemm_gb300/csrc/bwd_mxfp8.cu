@@ -88,7 +88,9 @@ struct RqArgs {
 //    it quantizes that channel's block, stores 32 codes (the CTA writes each
 //    channel's 128 tokens, one whole 128-byte line of qb) and the block's
 //    float32 sum for db.
-template <int DR>
+// V32: qb 32-byte aligned (its rows are Tp bytes, Tp % 128 == 0): a block's
+// 32 codes leave in one 32-byte store (`st.global.v8.b32`, sm_100 and later)
+template <int DR, bool V32>
 __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a) {
     __shared__ __align__(16) float tile[128][64];
     constexpr int HH = DR / 2;
@@ -196,8 +198,14 @@ __global__ void __launch_bounds__(kRqThreads) rope_bwd_quant_fast(const RqArgs a
         uint32_t w[8];
         const uint32_t sb = quantize_block32(v, w);
         uint8_t* dst = a.qb + ch * a.Tp + tb * 32;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        if (V32) {
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                         "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                         : "memory");
+        } else {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
         a.qb_s[sf_tiled_offset(ch, tb, 128, a.Tp / 128)] = (uint8_t)sb;
     }
     if (a.dbp && tb * 32 < a.T) a.dbp[tb * N + ch] = sum;
@@ -372,8 +380,11 @@ int launch_rope_bwd_quant(const BwdArgs& a, int64_t Tp, uint8_t* qa, uint8_t* qa
                       (Tp / 128) * (N / 64) <= 0x7fffffffLL;
     if (fast) {
         const unsigned grid = (unsigned)((Tp / 128) * (N / 64));
-        if (a.Dr == 32) rope_bwd_quant_fast<32><<<grid, kRqThreads, 0, stream>>>(r);
-        else rope_bwd_quant_fast<64><<<grid, kRqThreads, 0, stream>>>(r);
+        const bool v32 = reinterpret_cast<uintptr_t>(qb) % 32 == 0;
+        if (a.Dr == 32 && v32) rope_bwd_quant_fast<32, true><<<grid, kRqThreads, 0, stream>>>(r);
+        else if (a.Dr == 32) rope_bwd_quant_fast<32, false><<<grid, kRqThreads, 0, stream>>>(r);
+        else if (v32) rope_bwd_quant_fast<64, true><<<grid, kRqThreads, 0, stream>>>(r);
+        else rope_bwd_quant_fast<64, false><<<grid, kRqThreads, 0, stream>>>(r);
         return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
     }
     const size_t smem = (size_t)32 * (D + 1) * sizeof(float);
