@@ -8,7 +8,8 @@
 //
 //   * persistent CTAs (one per SM), each walking a static list of
 //     128-token x BN-channel output tiles (token index fastest, so the CTAs
-//     running together share weight tiles in L2);
+//     running together share weight tiles in L2; with resident weight scales
+//     each CTA takes one contiguous range of them instead);
 //   * warp 0: TMA producer, filling an S-stage shared-memory ring with x and
 //     W tiles (128-byte rows, 128-byte swizzle). For MXFP8 weights it also
 //     brings the E8M0 scale bytes of both operands into the 32x16-byte
@@ -27,7 +28,14 @@
 //     store box per 32-channel block, or per 64 channels when the two warps
 //     of a quadrant take the tile's two halves). The next tile's main loop
 //     runs in the other accumulator buffer meanwhile;
-//   * warp 10 (MXFP8 weights, pre-tiled scales): the scale bulk copies.
+//   * warp 10 (MXFP8 weights, pre-tiled scales): the scale bulk copies. With
+//     resident weight scales (the RES variant) W's scale tiles come only on a
+//     channel tile's first tile (kept in TMEM while the CTA stays on it) and
+//     a tile's x scales in one copy into one of two buffers.
+//
+// The tile order, the resident scales and the half-tile store layout are
+// compile-time variants: run-time checks of them in every role's loops
+// measured slower.
 //
 // Tiles never split a rope region or an MXFP8 block (the host picks BN so).
 // With Dr = 0 the kernel is a plain GEMM on 256-token tiles (two M = 128
