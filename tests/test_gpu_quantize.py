@@ -29,7 +29,9 @@ def _run(inp):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("R,C", [(1, 32), (7, 100), (64, 1536), (33, 4000), (3, 5), (128, 24576),
-                                 (513, 96)])
+                                 (513, 96),
+                                 # rows of C % 32 == 16: each row's last block half full
+                                 (5, 48), (9, 1552)])
 def test_quantize_matches_oracle(cuda_device, dtype, R, C):
     g = torch.Generator().manual_seed(R * 1000 + C)
     v = torch.randn((R, C), generator=g) * torch.exp2(torch.randint(-20, 20, (R, 1), generator=g).float())
@@ -46,6 +48,19 @@ def test_quantize_strided_rows(cuda_device, dtype):
     base = (torch.randn((40, 200), generator=g) * 3).to(dtype).to(cuda_device)
     for C in (160, 150, 37):
         view = base[:, :C]  # row pitch 200 > C
+        codes, scales = _run(view)
+        rc, rs = _oracle(view)
+        assert np.array_equal(scales, rs) and np.array_equal(codes, rc)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quantize_strided_rows_32_byte_pitch(cuda_device, dtype):
+    """Rows 32-byte aligned but not contiguous (pitch 192 elements), with
+    C % 32 == 0 and C % 32 == 16."""
+    g = torch.Generator().manual_seed(6)
+    base = (torch.randn((40, 192), generator=g) * 3).to(dtype).to(cuda_device)
+    for C in (160, 144):
+        view = base[:, :C]
         codes, scales = _run(view)
         rc, rs = _oracle(view)
         assert np.array_equal(scales, rs) and np.array_equal(codes, rc)
